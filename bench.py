@@ -1,0 +1,329 @@
+"""Decode-throughput benchmark of the persistent MoE decode megakernel.
+
+Default workload: the full-scale shape (48 layers, hidden 2048, 32q/4kv x 128,
+128 experts top-8, expert FFN 768, vocab 151936), batch 1, 8192 cached tokens,
+bf16 random-init weights, paged bf16 KV cache.  One step = one decode step of
+the whole model = one megakernel launch.  Inputs stay resident in HBM; every
+step streams ~6.9 GB, far larger than the 129 MB L2, so no flush is needed.
+
+Prints one JSON line (see the keys below).  `--impl reference` times the CPU
+oracle instead (the reference arm): a bounded sample of the same step on the
+host cores.  Under torchrun each rank runs an independent replica on its own
+GPU (the path does not shard), timed between barriers, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s (bs1, 8K ctx) and achieved HBM GB/s as % of speed-of-light"
+KERNEL_SOURCES = ["persistent_moe_decode_02_gb300/csrc/megakernel.cu",
+                  "persistent_moe_decode_02_gb300/csrc/mk_internal.h",
+                  "persistent_moe_decode_02_gb300/csrc/plan.cu"]
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------- reference arm / CPU baseline
+
+class OracleSample:
+    """A bounded sample of one decode step for the CPU oracle: `layers`
+    transformer layers of request 0 plus the LM head, scaled to the full
+    step.  Generating the sampled weights and KV is input preparation and
+    happens in prepare(), before any clock starts."""
+
+    def __init__(self, wl, layers: int = 2):
+        import synth
+        self.wl, self.layers, self.D = wl, layers, wl.dims
+        self.W = synth.SynthWeights(self.D, wl.seed, cache_limit_bytes=24 << 30)
+        self.store = {}
+        self.tok = synth.first_token(self.D, wl.seed, 0)
+
+    def _prior(self, rid, l, n):
+        import synth
+        if (rid, l, n) not in self.store:
+            self.store[(rid, l, n)] = synth.prior_kv(self.D, self.wl.seed, rid, l, n)
+        return self.store[(rid, l, n)]
+
+    def _run(self):
+        from oracle import decode as O
+        D = self.D
+        req = O.OracleRequest(0, self.wl.ctx[0], self._prior, D.n_layers)
+        x = O.widen(self.W.embed_rows([self.tok])[0])
+        t0 = time.perf_counter()
+        for l in range(self.layers):
+            x, _ = O.decode_layer(self.W, D, l, x, req, self.wl.ctx[0])
+        t1 = time.perf_counter()
+        O.lm_head(self.W, D, x)
+        t2 = time.perf_counter()
+        return (t1 - t0) * D.n_layers / self.layers + (t2 - t1)
+
+    def prepare(self):
+        self._run()          # fills the weight and KV caches (not timed)
+        return self
+
+    def step_seconds(self) -> float:
+        return self._run()
+
+    def describe(self) -> str:
+        return (f"{self.layers} of {self.D.n_layers} layers of one decode step of request 0 plus the LM head, "
+                f"scaled to the full step; inputs generated before timing")
+
+
+def reference_arm(args, wl):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    smp = OracleSample(wl, layers=2).prepare()
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = smp.step_seconds()
+        if i >= args.warmup:
+            times.append(s)
+    step_s = statistics.mean(times)
+    cores = torch.get_num_threads()
+    v = wl.batch / step_s
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": config_of(wl),
+           "cpu_baseline": {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                            "sample": smp.describe()},
+           "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def config_of(wl) -> dict:
+    D = wl.dims
+    return {"workload": wl.name, "layers": D.n_layers, "hidden": D.hidden,
+            "heads": f"{D.n_q_heads}q/{D.n_kv_heads}kv x {D.head_dim}",
+            "experts": f"{D.n_experts} top-{D.top_k}, ffn {D.expert_ffn}", "vocab": D.vocab,
+            "batch": wl.batch, "ctx": wl.ctx if wl.batch <= 8 else f"{min(wl.ctx)}..{max(wl.ctx)}",
+            "weights": "bf16 random-init", "kv": "paged bf16, page 16, shuffled",
+            "l2": "inputs larger than L2 (the step streams GBs; no flush needed)", "logits": False}
+
+
+# ---------------------------------------------------------------- our arm
+
+def our_arm(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from persistent_moe_decode_02_gb300 import mk
+    from persistent_moe_decode_02_gb300.roofline import step_bytes
+    from synth.device import DeviceModel, PagedKV, initial_tokens, kv_pages_needed
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    D = wl.dims
+    model = DeviceModel(D, wl.seed)
+    e2e_steps = max(3, args.steps // 4)
+    total_steps = args.warmup + args.steps + e2e_steps + 2
+    ps = D.page_size
+    max_pages = max((c + total_steps + ps) // ps for c in wl.ctx) + 1
+    kv = PagedKV(D, kv_pages_needed(D, wl.ctx, total_steps) + 4, max_pages, wl.seed)
+    reqs = [kv.admit(rid, c, total_steps) for rid, c in enumerate(wl.ctx)]
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages)
+    B = wl.batch
+    tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    # warm-up (next token feeds back in place: d_tokens aliases d_next_token)
+    for _ in range(args.warmup):
+        rc = plan.step(tok, tok)
+        assert rc == 0, mk.status_string(rc)
+    st = plan.sync()
+    assert st == 0, mk.status_string(st)
+    ctx_at_start = [r.length + args.warmup for r in reqs]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        for i in range(args.steps):
+            plan.step(tok, tok)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    st = plan.sync()
+    assert st == 0, mk.status_string(st)
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    elapsed_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t)
+    union = torch.zeros(D.n_layers, dtype=torch.int32)
+    plan.read_debug(mk.MK_DBG_UNION, union)
+    plan.sync()
+    nbytes = 0
+    for s in range(args.steps):
+        nbytes += step_bytes(D, [c + s for c in ctx_at_start], union_per_layer=union.tolist())["total"]
+    bytes_per_launch = nbytes / args.steps
+    mean_launch_ms = statistics.mean(per_launch)
+    achieved = bytes_per_launch / (mean_launch_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    value = world * B * args.steps / (elapsed_ms * 1e-3)
+
+    # end to end through the host-buffer entry point: H2D tokens, step, D2H next tokens, sync
+    h_tok = torch.tensor(tok.cpu().tolist(), dtype=torch.int32).pin_memory()
+    h_next = torch.empty(B, dtype=torch.int32).pin_memory()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        rc = plan.step_host(h_tok, h_next)
+        assert rc == 0, mk.status_string(rc)
+        h_tok.copy_(h_next)
+    t1 = time.perf_counter()
+    e2e_s = t1 - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t)
+    e2e = {"value": world * B * e2e_steps / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+           "d2h_bytes_per_step": 4 * B + 16, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(wl, layers=2).prepare()
+        s = smp.step_seconds()
+        cpu = {"value": B / s, "unit": "tok/s", "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": smp.describe()}
+    if rank == 0:
+        info = plan.info()
+        out = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "config": dict(config_of(wl), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                              weights_gb=round(model.nbytes() / 1e9, 2)),
+               "sol_pct_of_8tbs": 100.0 * achieved / 8000.0,
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                            "traffic": ncu_traffic(wl.name), "algorithmic_bytes_per_launch": bytes_per_launch,
+                            "kernel": "mk_megakernel", "mean_launch_ms": mean_launch_ms},
+               "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+               "clocks": clk.summary(), "plan": info, "kernel_hash": kernel_hash()}
+        print(json.dumps(out), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_bs1_8k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    import synth
+    wl = synth.workload(args.workload)
+    if args.impl == "reference":
+        reference_arm(args, wl)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        our_arm(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/* mk.h — C ABI of the persistent MoE decode megakernel (libmk.so, sm_103a).
+ *
+ * One decode step of a pre-norm MoE transformer (RMSNorm, QKV projection with
+ * RoPE, KV append into a paged cache, split-KV paged GQA attention, O
+ * projection, softmax/top-k router, SwiGLU experts, LM head, greedy argmax)
+ * runs as ONE persistent kernel: one CTA per SM walks a host-prepared list of
+ * tile tasks, and counters in global memory say when a tile's inputs are
+ * ready, so a tile starts as soon as its own inputs land while immutable
+ * weights (and already-cached KV pages) stream in ahead of it.
+ *   Source of the design: "Cohere Publishes One-Kernel Server for North Mini
+ *   Code" — "One resident program, many small tasks" and "What the
+ *   scheduling change is meant to avoid"; "Inside the Megakernel Serving
+ *   Engine for North Mini Code" — architecture paragraph (task list per SM,
+ *   counters in global memory, tile-level scheduling, weight prefetch).
+ *
+ * Conventions for every function:
+ *   - returns MK_OK (0) or a negative MK_ERR_* code; never aborts the process;
+ *   - "device" pointers are CUDA device (or managed) memory on the current
+ *     device; "host" pointers are ordinary host memory;
+ *   - the caller owns all weights, KV pools and input/output buffers; the
+ *     plan owns its task lists, counters, per-layer activations and status;
+ *   - all matrices are bf16, row-major [out, in]; activations are fp32.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mk_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  MK_OK = 0,
+  MK_ERR_INVALID = -1,      /* bad argument: dims, pointer, size or page table */
+  MK_ERR_CUDA = -2,         /* a CUDA runtime call failed */
+  MK_ERR_DEP_TIMEOUT = -3,  /* a bounded device wait on a dependency ran out */
+  MK_ERR_CAPACITY = -4,     /* batch, pages or positions beyond what the plan holds */
+  MK_ERR_UNSUPPORTED = -5   /* shape this build does not implement */
+};
+
+/* Model shape.  Requirements: n_q_heads % n_kv_heads == 0 with at most 8 query
+ * heads per KV head; head_dim 64 or 128; hidden, expert_ffn and
+ * n_q_heads*head_dim multiples of 8; top_k <= 8; top_k <= n_experts <= 256;
+ * page_size == 16; batch <= 8. */
+typedef struct mk_model_dims {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
+  int n_experts, top_k, expert_ffn, vocab, page_size;
+  float rms_eps, rope_theta;
+} mk_model_dims;
+
+/* Weight pointers (all device, bf16).  Per-layer entries are HOST arrays of
+ * n_layers device pointers; the plan copies them at creation.
+ *   embed       [vocab, hidden]          lm_head   [vocab, hidden]
+ *   final_norm  [hidden]
+ *   attn_norm[l], ffn_norm[l]            [hidden]
+ *   wqkv[l]     [n_kv_heads * (G + 2) * head_dim, hidden], G = n_q/n_kv,
+ *               rows grouped per KV head g: the G query heads of group g
+ *               (G*head_dim rows), then key head g, then value head g
+ *   wo[l]       [hidden, n_q_heads * head_dim]
+ *   router[l]   [n_experts, hidden]
+ *   w_gate_up[l][n_experts, 2*expert_ffn, hidden]: gate rows, then up rows
+ *   w_down[l]   [n_experts, hidden, expert_ffn]
+ * Every pointer must be 16-byte aligned. */
+typedef struct mk_weights {
+  const void* embed;
+  const void* final_norm;
+  const void* lm_head;
+  const void* const* attn_norm;
+  const void* const* wqkv;
+  const void* const* wo;
+  const void* const* ffn_norm;
+  const void* const* router;
+  const void* const* w_gate_up;
+  const void* const* w_down;
+} mk_weights;
+
+/* Paged KV cache: per layer one K pool and one V pool (HOST arrays of
+ * n_layers device pointers), each bf16 [num_pages, n_kv_heads, page_size,
+ * head_dim].  Token t of request b lives in page page_table[b][t / page_size],
+ * slot t % page_size.  16-byte aligned. */
+typedef struct mk_kv {
+  void* const* k_pool;
+  void* const* v_pool;
+  int num_pages;
+} mk_kv;
+
+/* Plan options; zero-initialise for defaults. */
+typedef struct mk_plan_opts {
+  int timeout_us;    /* limit of every device spin-wait; 0 -> 2,000,000 us */
+  int num_ctas;      /* persistent CTAs; 0 -> one per SM */
+  int max_batch;     /* batch capacity for mk_plan_update; 0 -> batch */
+  int split_pages;   /* KV pages per attention task; 0 -> balance over the CTAs */
+  int debug_drop_task; /* test hook: >0 removes task (value-1) from the list so its
+                          counter never fires and the step returns MK_ERR_DEP_TIMEOUT;
+                          0 in production */
+} mk_plan_opts;
+
+typedef struct mk_plan mk_plan;
+
+/* Build the task list and dependency counters for `batch` requests whose
+ * caches hold seq_lens[b] tokens (host array), with the host page table
+ * page_table[b * max_pages_per_seq + i] (page ids of request b in order).
+ * Every page that covers positions [0, seq_lens[b]] must be present and in
+ * [0, kv->num_pages).  Allocates the plan's device buffers on the current
+ * device.  *out is set only on success. */
+int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
+                   const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   const mk_plan_opts* opts, mk_plan** out);
+
+/* One decode step, enqueued on `stream`: request b decodes d_tokens[b] (device
+ * int32[batch]) at position seq_len[b], writes its K/V there, and the greedy
+ * next token to d_next_token[b] (device int32[batch]); d_logits (device
+ * fp32[batch, vocab]) is written when non-NULL.  d_tokens may alias
+ * d_next_token.  After the step the plan's lengths are seq_len + 1.  Returns
+ * MK_ERR_CAPACITY (nothing enqueued) if a request's next position has no page.
+ * Device failures (MK_ERR_DEP_TIMEOUT) are reported by mk_plan_sync; once one
+ * is recorded, later steps do no work until mk_plan_update. */
+int mk_decode_step(mk_plan* plan, const int* d_tokens, float* d_logits, int* d_next_token,
+                   mk_stream stream);
+
+/* The same step with HOST buffers: copies h_tokens in, runs the step, copies
+ * the next tokens (and logits when h_logits != NULL) out, and waits for the
+ * stream.  Host buffers may be pageable or pinned. */
+int mk_decode_step_host(mk_plan* plan, const int* h_tokens, float* h_logits, int* h_next_token,
+                        mk_stream stream);
+
+/* Continuous batching: replace the batch (requests joining or leaving) with
+ * `batch` requests (<= the plan's capacity), their cached lengths and page
+ * table (host arrays, same layout as mk_plan_create).  Rebuilds the task list,
+ * uploads it with the lengths and page table on `stream`, resets counters and
+ * clears a recorded device error.  No kernel is launched. */
+int mk_plan_update(mk_plan* plan, int batch, const int* seq_lens, const int* page_table,
+                   int max_pages_per_seq, mk_stream stream);
+
+/* Wait for `stream`, then return the device status (MK_OK or the first error
+ * a step recorded). */
+int mk_plan_sync(mk_plan* plan, mk_stream stream);
+
+/* Copy a per-step intermediate of the most recent step into dst (device or
+ * host memory, `bytes` long), on `stream`:
+ *   MK_DBG_HIDDEN        fp32 [batch, n_layers, hidden]  x after each layer
+ *   MK_DBG_EXPERT_IDS    int32 [batch, n_layers, top_k]  rank order
+ *   MK_DBG_GATES         fp32 [batch, n_layers, top_k]
+ *   MK_DBG_ROUTER_LOGITS fp32 [batch, n_layers, n_experts]
+ *   MK_DBG_SEQ_LENS      int32 [batch]                   device lengths
+ *   MK_DBG_UNION         int32 [n_layers]                distinct experts per layer */
+enum { MK_DBG_HIDDEN = 1, MK_DBG_EXPERT_IDS = 2, MK_DBG_GATES = 3, MK_DBG_ROUTER_LOGITS = 4,
+       MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6 };
+int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stream stream);
+
+/* Describe the current plan (host-side numbers): writes up to `n` ints:
+ * [num_ctas, num_tasks, nstages, stage_bytes, smem_bytes, batch, n_attn_tasks,
+ *  n_gu_tasks, n_lm_tiles, replans]. */
+int mk_plan_info(const mk_plan* plan, int* out, int n);
+
+void mk_plan_destroy(mk_plan* plan);
+
+const char* mk_status_string(int status);
+
+/* Text of the most recent library failure on the calling thread (for example
+ * the CUDA call and error behind an MK_ERR_CUDA); "" when none. */
+const char* mk_last_error(void);
+
+/* Host-only planner, for inspection and tests (no CUDA call): builds the task
+ * list the plan would run for these lengths on `num_ctas` CTAs.  Writes up to
+ * max_tasks tasks as 12 int32 each into `tasks` (type, layer, a0..a7,
+ * wait_counter, wait_count) and num_ctas + 1 offsets into `cta_start`;
+ * returns the task count (or a negative error). */
+int mk_plan_inspect(const mk_model_dims* dims, int batch, const int* seq_lens, int num_ctas,
+                    int split_pages, int* tasks, int max_tasks, int* cta_start);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -28,5 +28,6 @@ pages: beyond those pins, end-to-end values are "parity unpinned".
 """
 from .decode import (  # noqa: F401
     bf16_rne, rmsnorm, rope, gqa_attention, route, silu, expert_ffn,
-    OracleRequest, LayerTrace, StepResult, decode_layer, decode_step,
+    OracleRequest, LayerTrace, StepResult, attention_block, moe_block, decode_layer, lm_head,
+    decode_step,
 )

@@ -158,11 +158,9 @@ class StepResult:
         return torch.stack([t.x_out for t in self.layers])
 
 
-def decode_layer(W, dims, l: int, x: torch.Tensor, req: OracleRequest, pos: int,
-                 force: Optional[Sequence[int]] = None):
-    """One transformer layer for one request; appends this token's K/V."""
+def attention_block(W, dims, l: int, x: torch.Tensor, req: OracleRequest, pos: int) -> torch.Tensor:
+    """x + Wo * Attn(rmsnorm(x)) for one request; appends this token's K/V."""
     nq, nkv, d = dims.n_q_heads, dims.n_kv_heads, dims.head_dim
-    # attention block
     xn = rmsnorm(x, W.attn_norm(l), dims.rms_eps)
     q = (widen(W.wq(l)) @ xn).view(nq, d)
     k = (widen(W.wk(l)) @ xn).view(nkv, d)
@@ -177,8 +175,11 @@ def decode_layer(W, dims, l: int, x: torch.Tensor, req: OracleRequest, pos: int,
     K = torch.cat([K, k_b[None]])
     V = torch.cat([V, v_b[None]])
     o = gqa_attention(q, K, V).reshape(nq * d)
-    x_mid = x + widen(W.wo(l)) @ o
-    # MoE block
+    return x + widen(W.wo(l)) @ o
+
+
+def moe_block(W, dims, l: int, x_mid: torch.Tensor, force: Optional[Sequence[int]] = None):
+    """x_mid + sum_j gate_j * expert_j(rmsnorm(x_mid)); no side effects."""
     xn2 = rmsnorm(x_mid, W.ffn_norm(l), dims.rms_eps)
     r = widen(W.router(l)) @ xn2
     ids, gates, _ = route(r, dims.top_k, force)
@@ -187,6 +188,22 @@ def decode_layer(W, dims, l: int, x: torch.Tensor, req: OracleRequest, pos: int,
         wg, wu, wd = W.expert(l, e)
         x_out = x_out + gates[j] * expert_ffn(xn2, wg, wu, wd)
     return x_out, LayerTrace(r, ids, gates, x_mid, x_out)
+
+
+def decode_layer(W, dims, l: int, x: torch.Tensor, req: OracleRequest, pos: int,
+                 force: Optional[Sequence[int]] = None):
+    """One transformer layer for one request; appends this token's K/V."""
+    x_mid = attention_block(W, dims, l, x, req, pos)
+    return moe_block(W, dims, l, x_mid, force)
+
+
+def lm_head(W, dims, x: torch.Tensor):
+    """Final RMSNorm, LM head and greedy argmax (float32 decision, lowest index on ties)."""
+    xf = rmsnorm(x, W.final_norm(), dims.rms_eps)
+    Wl = W.lm_head()
+    logits = torch.cat([widen(Wl[i:i + 16384]) @ xf for i in range(0, Wl.shape[0], 16384)])
+    nxt = int(torch.argmax(logits.to(torch.float32)))   # first index among equal maxima
+    return logits, nxt
 
 
 def decode_step(W, dims, req: OracleRequest, token: int,
@@ -198,8 +215,5 @@ def decode_step(W, dims, req: OracleRequest, token: int,
     for l in range(dims.n_layers):
         x, tr = decode_layer(W, dims, l, x, req, pos, None if force is None else force.get(l))
         traces.append(tr)
-    xf = rmsnorm(x, W.final_norm(), dims.rms_eps)
-    Wl = W.lm_head()
-    logits = torch.cat([widen(Wl[i:i + 16384]) @ xf for i in range(0, Wl.shape[0], 16384)])
-    nxt = int(torch.argmax(logits.to(torch.float32)))   # first index among equal maxima
+    logits, nxt = lm_head(W, dims, x)
     return StepResult(logits, nxt, traces)

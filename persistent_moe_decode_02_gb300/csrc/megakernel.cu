@@ -1,0 +1,1230 @@
+// Persistent MoE decode megakernel for GB300 (sm_103a).
+//
+// One CTA per SM stays resident for the whole decode step and walks its slice
+// of a host-prepared task list ("Cohere Publishes One-Kernel Server for North
+// Mini Code" — "One resident program, many small tasks"; "Inside the
+// Megakernel Serving Engine for North Mini Code" — architecture paragraph).
+//
+// Inside a CTA:
+//   * warp 8 (one lane) is the producer: it walks the CTA's tasks in order and
+//     streams each task's weight rows (or cached KV pages) into a ring of
+//     shared-memory stages with bulk async copies (cp.async.bulk, completion
+//     on an mbarrier).  It never waits for a task's activations, so immutable
+//     bytes land while the dependency is still pending ("What the scheduling
+//     change is meant to avoid", third bullet).  Only expert tiles wait, for
+//     the router's choice, since their addresses depend on it.
+//   * warps 0-7 are consumers: per task they wait on a global-memory
+//     dependency counter, load the small fp32 activation into shared memory,
+//     consume the ring stages (bf16 x fp32 dot products on CUDA cores, or
+//     online-softmax attention), write the outputs and bump the task's
+//     counter.  A tile starts when its own inputs are ready, not when a whole
+//     op is done ("False dependencies" bullet).
+// Every spin-wait has a time limit; on expiry the kernel records
+// MK_ERR_DEP_TIMEOUT in the status word, all CTAs drain and return.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int NCT = NCW * 32;  // consumer threads
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Global -> shared bulk copy; completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_release(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Barrier over the 256 consumer threads (named barrier 1).
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Same barrier, returning the OR of every consumer thread's predicate.
+__device__ __forceinline__ bool cbar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+// Sum of v[h] over the 32 lanes for the head h = (lane >> 2) & 7, by halving
+// exchanges (9 shuffles for 8 values instead of 40).
+__device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
+  float a[4];
+  const bool u16 = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float send = u16 ? v[i] : v[i + 4];
+    float keep = u16 ? v[i + 4] : v[i];
+    a[i] = keep + __shfl_xor_sync(FULL, send, 16);
+  }
+  float b[2];
+  const bool u8 = lane & 8;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float send = u8 ? a[i] : a[i + 2];
+    float keep = u8 ? a[i + 2] : a[i];
+    b[i] = keep + __shfl_xor_sync(FULL, send, 8);
+  }
+  const bool u4 = lane & 4;
+  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(FULL, u4 ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(FULL, c, 2);
+  c += __shfl_xor_sync(FULL, c, 1);
+  return c;
+}
+
+// ------------------------------------------------------------------ shared state
+
+struct Misc {
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  int armed[MAX_STAGES];   // round in which the producer last armed a stage, -1 never
+  int dead;                // the status word was already set at kernel entry
+  int abort_flag;          // a warp of this CTA gave up
+  int ticket_last;
+  int pad;
+  float red[NCW * MAX_BATCH];
+  float best_v[NCW * MAX_BATCH];
+  int best_i[NCW * MAX_BATCH];
+  int seg_tok[MAX_BATCH];
+  int seg_rank[MAX_BATCH];
+  int sel[MAX_BATCH * MAX_TOPK];
+  int slot_of[MAX_EXPERTS];
+  int cnt_of[MAX_EXPERTS];
+};
+
+struct Ring {
+  uint8_t* base;
+  Misc* m;
+  int nst, sb;
+  int stage, round;
+  __device__ void advance() {
+    if (++stage == nst) { stage = 0; ++round; }
+  }
+};
+
+// ------------------------------------------------------------------ failure handling
+
+__device__ __forceinline__ bool failed(const Params& p) {
+  return *(volatile int*)p.status != 0;
+}
+
+__device__ void set_error(const Params& p, int code, int task, int info) {
+  if (atomicCAS(p.status, 0, code) == 0) {
+    p.status[1] = task;
+    p.status[2] = blockIdx.x;
+    p.status[3] = info;
+    __threadfence();
+  }
+}
+
+// Wait until counter `ctr` holds epoch * cnt signals (bounded).
+__device__ bool wait_ctr(const Params& p, int ctr, uint32_t cnt, int task) {
+  if (ctr < 0) return true;
+  const uint32_t* c = p.ctr + (size_t)ctr * CTR_STRIDE;
+  const uint32_t target = p.epoch * cnt;
+  if ((int32_t)(ld_acquire(c) - target) >= 0) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    if ((int32_t)(ld_acquire(c) - target) >= 0) return true;
+    if ((it & 31) == 0) {
+      if (failed(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        set_error(p, MK_ERR_DEP_TIMEOUT, task, ctr);
+        return false;
+      }
+    }
+    if (it > 256) __nanosleep(100);
+  }
+}
+
+// Bounded mbarrier parity wait; gives up when this CTA or any CTA failed.
+__device__ bool mbar_wait(const Params& p, Misc* m, uint64_t* bar, uint32_t parity, int info) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 0) {
+      if (*(volatile int*)&m->abort_flag || failed(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        set_error(p, MK_ERR_DEP_TIMEOUT, -1, info);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ stage geometry
+// Producer and consumers derive the same stage sequence from the task and the
+// same device state, so they agree on what every stage holds.
+
+__device__ __forceinline__ int rows_per_stage(const Params& p, int K) {
+  return max(1, p.stage_bytes / (K * 2));
+}
+
+__device__ __forceinline__ int pages_per_stage(const Params& p) {
+  return max(1, p.stage_bytes / (2 * p.ps * p.d * 2));
+}
+
+__device__ __forceinline__ int pairs_per_stage(const Params& p) {
+  return max(1, p.stage_bytes / (4 * p.H));
+}
+
+// Token range [tok0, tok1) of an attention task at the current lengths.
+__device__ __forceinline__ void attn_range(const Params& p, const Task& t, int pos, int& tok0,
+                                           int& tok1) {
+  tok0 = t.a[2] * p.ps;
+  tok1 = (t.a[3] < 0) ? pos + 1 : min(t.a[3] * p.ps, pos + 1);
+}
+
+// Flattened (distinct expert, ffn row) range of gate/up tile a0 of a1.
+__device__ __forceinline__ void gu_range(const Params& p, const Task& t, int U, long long& q0,
+                                         long long& q1) {
+  const long long tot = (long long)U * p.F;
+  q0 = tot * t.a[0] / t.a[1];
+  q1 = tot * (t.a[0] + 1) / t.a[1];
+}
+
+__device__ __forceinline__ const int* route_of(const Params& p, int l) {
+  return p.route + (size_t)l * p.rm.ints;
+}
+
+// ------------------------------------------------------------------ producer
+
+struct Producer {
+  const Params& p;
+  Ring r;
+  uint64_t pol;
+
+  // Claim the next stage (waiting for its release) and arm it for `bytes`.
+  __device__ bool open(uint32_t bytes, uint8_t*& dst, uint64_t*& bar) {
+    Misc* m = r.m;
+    if (!mbar_wait(p, m, &m->empty[r.stage], (r.round & 1) ^ 1, -3)) return false;
+    bar = &m->full[r.stage];
+    dst = r.base + (size_t)r.stage * r.sb;
+    m->armed[r.stage] = r.round;
+    mbar_expect_tx(bar, bytes);
+    return true;
+  }
+
+  __device__ bool rows(const uint16_t* W, int K, int r0, int r1) {
+    const int rps = rows_per_stage(p, K);
+    for (int s0 = r0; s0 < r1; s0 += rps) {
+      const int n = min(rps, r1 - s0);
+      const uint32_t bytes = (uint32_t)n * K * 2;
+      uint8_t* dst;
+      uint64_t* bar;
+      if (!open(bytes, dst, bar)) return false;
+      bulk_g2s(dst, W + (size_t)s0 * K, bytes, bar, pol);
+      r.advance();
+    }
+    return true;
+  }
+
+  __device__ bool attn(const Task& t) {
+    const int l = t.layer, b = t.a[0], g = t.a[1];
+    const int pos = __ldcg(p.seq_len + b);
+    int tok0, tok1;
+    attn_range(p, t, pos, tok0, tok1);
+    const int ppg = pages_per_stage(p);
+    const uint32_t PB = (uint32_t)p.ps * p.d * 2;
+    const int pg1 = (tok1 + p.ps - 1) / p.ps;
+    const int* pt = p.page_table + (size_t)b * p.max_pages;
+    const uint16_t* kp = p.k_pool[l];
+    const uint16_t* vp = p.v_pool[l];
+    for (int pg = tok0 / p.ps; pg < pg1; pg += ppg) {
+      const int n = min(ppg, pg1 - pg);
+      uint8_t* dst;
+      uint64_t* bar;
+      if (!open(2u * n * PB, dst, bar)) return false;
+      for (int i = 0; i < n; ++i) {
+        const size_t off = ((size_t)pt[pg + i] * p.nkv + g) * p.ps * p.d;
+        bulk_g2s(dst + (size_t)i * PB, kp + off, PB, bar, pol);
+        bulk_g2s(dst + (size_t)(ppg + i) * PB, vp + off, PB, bar, pol);
+      }
+      r.advance();
+    }
+    return true;
+  }
+
+  __device__ bool gu(const Task& t, int ti) {
+    const int l = t.layer;
+    if (!wait_ctr(p, p.cm.rdone + l, 1, ti)) return false;
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    long long q0, q1;
+    gu_range(p, t, U, q0, q1);
+    const int F = p.F, H = p.H, pps = pairs_per_stage(p);
+    const uint16_t* W = p.w_gate_up[l];
+    for (long long q = q0; q < q1;) {
+      const int u = (int)(q / F);
+      const int fa = (int)(q - (long long)u * F);
+      const int fb = (int)min((long long)F, q1 - (long long)u * F);
+      const int e = __ldcg(rt + 1 + u);
+      const uint16_t* We = W + (size_t)e * 2 * F * H;
+      for (int f = fa; f < fb; f += pps) {
+        const int n = min(pps, fb - f);
+        const uint32_t half = (uint32_t)n * H * 2;
+        uint8_t* dst;
+        uint64_t* bar;
+        if (!open(2 * half, dst, bar)) return false;
+        bulk_g2s(dst, We + (size_t)f * H, half, bar, pol);
+        bulk_g2s(dst + half, We + (size_t)(F + f) * H, half, bar, pol);
+        r.advance();
+      }
+      q = (long long)(u + 1) * F;
+    }
+    return true;
+  }
+
+  __device__ bool down(const Task& t, int ti) {
+    const int l = t.layer;
+    if (!wait_ctr(p, p.cm.rdone + l, 1, ti)) return false;
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    const int r0 = t.a[0], r1 = t.a[1], F = p.F, H = p.H;
+    const int rps = rows_per_stage(p, F);
+    const uint16_t* W = p.w_down[l];
+    for (int u = 0; u < U; ++u) {
+      const int e = __ldcg(rt + 1 + u);
+      const uint16_t* We = W + (size_t)e * H * F;
+      for (int s0 = r0; s0 < r1; s0 += rps) {
+        const int n = min(rps, r1 - s0);
+        uint8_t* dst;
+        uint64_t* bar;
+        if (!open((uint32_t)n * F * 2, dst, bar)) return false;
+        bulk_g2s(dst, We + (size_t)s0 * F, (uint32_t)n * F * 2, bar, pol);
+        r.advance();
+      }
+    }
+    return true;
+  }
+
+  __device__ void run(int t0, int t1) {
+    for (int ti = t0; ti < t1; ++ti) {
+      if (failed(p)) return;
+      const Task t = p.tasks[ti];
+      const int l = t.layer;
+      bool ok = true;
+      switch (t.type) {
+        case T_QKV: ok = rows(p.wqkv[l], p.H, t.a[0], t.a[1]); break;
+        case T_ATTN: ok = attn(t); break;
+        case T_OPROJ: ok = rows(p.wo[l], p.nq * p.d, t.a[0], t.a[1]); break;
+        case T_ROUTER: ok = rows(p.router[l], p.H, t.a[0], t.a[1]); break;
+        case T_GU: ok = gu(t, ti); break;
+        case T_DOWN: ok = down(t, ti); break;
+        case T_LM: ok = rows(p.lm_head, p.H, t.a[0], t.a[1]); break;
+        default: set_error(p, MK_ERR_INVALID, ti, t.type); ok = false;
+      }
+      if (!ok) {
+        r.m->abort_flag = 1;
+        return;
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ consumer pieces
+
+template <int NB>
+struct Consumer {
+  const Params& p;
+  Ring r;
+  float* act;
+  Misc* m;
+  float* ydown;
+  int ct, cw, lane;
+
+  // ---- ring access (per warp)
+  __device__ const uint8_t* wait_stage(bool& ab) {
+    if (ab) return nullptr;
+    if (!mbar_wait(p, m, &m->full[r.stage], r.round & 1, -4)) {
+      ab = true;
+      m->abort_flag = 1;
+      return nullptr;
+    }
+    return r.base + (size_t)r.stage * r.sb;
+  }
+  __device__ void release_stage(bool ab) {
+    __syncwarp();
+    if (!ab && lane == 0) mbar_arrive(&m->empty[r.stage]);
+    r.advance();
+  }
+
+  // ---- activations
+  // act[b * H + i] = x_b[i] / sqrt(mean(x_b^2) + eps) * gamma[i], b < B.
+  template <class Src>
+  __device__ void fill_rmsnorm(const uint16_t* gamma, Src src) {
+    const int H = p.H, B = p.B;
+    for (int b = 0; b < B; ++b) {
+      float ss = 0.f;
+      for (int i = ct; i < H; i += NCT) {
+        const float v = src(b, i);
+        act[b * H + i] = v;
+        ss = fmaf(v, v, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) m->red[b * NCW + cw] = ss;
+    }
+    cbar();
+    for (int b = 0; b < B; ++b) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) tot += m->red[b * NCW + w];
+      const float inv = 1.0f / sqrtf(tot / (float)H + p.eps);
+      for (int i = ct; i < H; i += NCT) act[b * H + i] = act[b * H + i] * inv * bf2f(gamma[i]);
+    }
+  }
+
+  __device__ float x_in(int l, int b, int i) const {
+    if (l == 0) {
+      const int tok = __ldcg(p.tokens + b);
+      return bf2f(p.embed[(size_t)tok * p.H + i]);
+    }
+    return __ldcg(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H + i);
+  }
+
+  // ---- dot products of one bf16 row (K elements, smem) with nb activation rows
+  // act + map(j) * stride, j < nb; full sums returned in every lane.
+  __device__ __forceinline__ void row_dot(const uint8_t* wrow, int K, const float* a, int stride,
+                                          const int* map, int nb, float (&out)[NB]) const {
+    float acc0[NB], acc1[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) acc0[j] = acc1[j] = 0.f;
+    const uint4* w4 = reinterpret_cast<const uint4*>(wrow);
+    const int ng = K >> 3;
+#pragma unroll 2
+    for (int gi = lane; gi < ng; gi += 32) {
+      const uint4 wv = w4[gi];
+      const float w0 = bf_lo(wv.x), w1 = bf_hi(wv.x), w2 = bf_lo(wv.y), w3 = bf_hi(wv.y);
+      const float w5 = bf_hi(wv.z), w4f = bf_lo(wv.z), w6 = bf_lo(wv.w), w7 = bf_hi(wv.w);
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        if (j < nb) {
+          const int row = map ? map[j] : j;
+          const float4* av = reinterpret_cast<const float4*>(a + (size_t)row * stride + gi * 8);
+          const float4 x0 = av[0], x1 = av[1];
+          acc0[j] = fmaf(w0, x0.x, acc0[j]);
+          acc1[j] = fmaf(w1, x0.y, acc1[j]);
+          acc0[j] = fmaf(w2, x0.z, acc0[j]);
+          acc1[j] = fmaf(w3, x0.w, acc1[j]);
+          acc0[j] = fmaf(w4f, x1.x, acc0[j]);
+          acc1[j] = fmaf(w5, x1.y, acc1[j]);
+          acc0[j] = fmaf(w6, x1.z, acc0[j]);
+          acc1[j] = fmaf(w7, x1.w, acc1[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) out[j] = warp_sum(acc0[j] + acc1[j]);
+  }
+
+  // Consume the stages of rows [r0, r1) of a K-wide matrix; epi(row, sums).
+  template <class Epi>
+  __device__ bool rows(int K, int r0, int r1, const float* a, int stride, const int* map, int nb,
+                       bool ab, Epi epi) {
+    const int rps = rows_per_stage(p, K);
+    for (int s0 = r0; s0 < r1; s0 += rps) {
+      const int n = min(rps, r1 - s0);
+      const uint8_t* st = wait_stage(ab);
+      if (st) {
+        for (int rr = cw; rr < n; rr += NCW) {
+          float out[NB];
+          row_dot(st + (size_t)rr * K * 2, K, a, stride, map, nb, out);
+          epi(s0 + rr, out);
+        }
+      }
+      release_stage(ab);
+    }
+    return ab;
+  }
+
+  // End of a task: make this thread's writes visible, agree on failure.
+  __device__ bool finish(bool ab) {
+    __threadfence();
+    return cbar_or(ab);
+  }
+
+  __device__ void signal(int ctr) {
+    if (ct == 0) atom_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
+  }
+
+  // Uniform "am I the last of n producers this step" for counter ctr.
+  __device__ bool ticket(int ctr, uint32_t n) {
+    if (ct == 0) {
+      const uint32_t old = atom_add_acq_rel(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
+      m->ticket_last = (old == p.epoch * n - 1u) ? 1 : 0;
+    }
+    cbar();
+    const bool last = m->ticket_last != 0;
+    if (last) __threadfence();
+    return last;
+  }
+
+  // ------------------------------------------------------------ tasks
+
+  __device__ bool qkv(const Task& t, bool ab) {
+    const int l = t.layer;
+    if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i) { return x_in(l, b, i); });
+    cbar();
+    float* out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
+    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        if (j < p.B && lane == j) out[(size_t)j * p.qkv_rows + row] = s[j];
+    });
+    ab = finish(ab);
+    if (!ab) signal(p.cm.qkv + l * p.nkv + t.a[2]);
+    return ab;
+  }
+
+  __device__ bool oproj(const Task& t, bool ab) {
+    const int l = t.layer, K = p.nq * p.d;
+    if (!ab) {
+      const float* o = p.o + (size_t)l * p.bcap * K;
+      for (int i = ct; i < p.B * K; i += NCT) act[i] = __ldcg(o + i);
+    }
+    cbar();
+    float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
+    ab = rows(K, t.a[0], t.a[1], act, K, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        if (j < p.B && lane == j) xm[(size_t)j * p.H + row] = x_in(l, j, row) + s[j];
+    });
+    ab = finish(ab);
+    if (!ab) signal(p.cm.o + l);
+    return ab;
+  }
+
+  __device__ void fill_ffn_norm(int l) {
+    const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
+    fill_rmsnorm(p.ffn_norm[l], [&](int b, int i) { return __ldcg(xm + (size_t)b * p.H + i); });
+  }
+
+  // Top-k of every request's router logits, gates, and the distinct-expert list.
+  __device__ void route_finish(int l) {
+    const int E = p.E, k = p.k, B = p.B;
+    int* rt = const_cast<int*>(route_of(p, l));
+    if (cw < B) {
+      const int b = cw;
+      const float* rl = p.rlog + ((size_t)l * p.bcap + b) * E;
+      float v[MAX_EXPERTS / 32];
+#pragma unroll
+      for (int i = 0; i < MAX_EXPERTS / 32; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
+      }
+      float selv = 0.f, first = 0.f;
+      int mysel = 0;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < MAX_EXPERTS / 32; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ov = __shfl_xor_sync(FULL, bv, o);
+          const int oi = __shfl_xor_sync(FULL, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
+        if (j == 0) first = bv;
+        if (lane == j) { selv = bv; mysel = bi; }
+      }
+      const float ex = lane < k ? expf(selv - first) : 0.f;
+      const float tot = warp_sum(ex);
+      if (lane < k) {
+        p.ids[((size_t)l * p.bcap + b) * k + lane] = mysel;
+        p.gates[((size_t)l * p.bcap + b) * k + lane] = ex / tot;
+        m->sel[b * k + lane] = mysel;
+      }
+    }
+    if (ct < MAX_EXPERTS) m->cnt_of[ct] = 0;
+    cbar();
+    if (ct < B * k) atomicAdd(&m->cnt_of[m->sel[ct]], 1);
+    cbar();
+    const int umax = p.rm.umax, bc = p.rm.bcap;
+    if (cw == 0) {
+      int base = 0;
+      for (int c = 0; c < (E + 31) / 32; ++c) {
+        const int e = c * 32 + lane;
+        const bool pres = e < E && m->cnt_of[e] > 0;
+        const unsigned mask = __ballot_sync(FULL, pres);
+        if (pres) {
+          const int u = base + __popc(mask & ((1u << lane) - 1u));
+          m->slot_of[e] = u;
+          rt[1 + u] = e;
+          rt[1 + umax + u] = m->cnt_of[e];
+        }
+        base += __popc(mask);
+      }
+      if (lane == 0) rt[0] = base;
+    }
+    cbar();
+    if (ct < B * k) {
+      const int e = m->sel[ct];
+      int rank = 0;
+      for (int q = 0; q < ct; ++q) rank += (m->sel[q] == e);
+      const int u = m->slot_of[e];
+      rt[1 + 2 * umax + u * bc + rank] = ct / k;
+      rt[1 + 2 * umax + umax * bc + u * bc + rank] = ct % k;
+    }
+  }
+
+  __device__ bool router(const Task& t, bool ab) {
+    const int l = t.layer;
+    if (!ab) fill_ffn_norm(l);
+    cbar();
+    float* rl = p.rlog + (size_t)l * p.bcap * p.E;
+    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        if (j < p.B && lane == j) rl[(size_t)j * p.E + row] = s[j];
+    });
+    ab = finish(ab);
+    if (ab) return ab;
+    if (ticket(p.cm.rticket + l, (uint32_t)t.a[2])) {
+      route_finish(l);
+      ab = finish(false);
+      if (!ab) signal(p.cm.rdone + l);
+    }
+    return ab;
+  }
+
+  // Load the token list of distinct-expert slot u into smem (all consumer threads).
+  __device__ int load_segment(const int* rt, int u) {
+    const int umax = p.rm.umax, bc = p.rm.bcap;
+    const int nt = __ldcg(rt + 1 + umax + u);
+    cbar();  // previous segment's readers are done
+    if (ct < nt) {
+      m->seg_tok[ct] = __ldcg(rt + 1 + 2 * umax + u * bc + ct);
+      m->seg_rank[ct] = __ldcg(rt + 1 + 2 * umax + umax * bc + u * bc + ct);
+    }
+    cbar();
+    return nt;
+  }
+
+  __device__ bool gate_up(const Task& t, bool ab) {
+    const int l = t.layer, H = p.H, F = p.F, k = p.k;
+    if (!ab) fill_ffn_norm(l);
+    cbar();
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    long long q0, q1;
+    gu_range(p, t, U, q0, q1);
+    const int pps = pairs_per_stage(p);
+    float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
+    for (long long q = q0; q < q1;) {
+      const int u = (int)(q / F);
+      const int fa = (int)(q - (long long)u * F);
+      const int fb = (int)min((long long)F, q1 - (long long)u * F);
+      const int nt = load_segment(rt, u);
+      for (int f0 = fa; f0 < fb; f0 += pps) {
+        const int n = min(pps, fb - f0);
+        const uint8_t* st = wait_stage(ab);
+        if (st) {
+          for (int rr = cw; rr < n; rr += NCW) {
+            float sg[NB], su[NB];
+            row_dot(st + (size_t)rr * H * 2, H, act, H, m->seg_tok, nt, sg);
+            row_dot(st + (size_t)(n + rr) * H * 2, H, act, H, m->seg_tok, nt, su);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              if (j < nt && lane == j) {
+                const float gv = sg[j];
+                const float h = gv / (1.0f + expf(-gv)) * su[j];
+                hb[((size_t)m->seg_tok[j] * k + m->seg_rank[j]) * F + f0 + rr] = h;
+              }
+            }
+          }
+        }
+        release_stage(ab);
+      }
+      q = (long long)(u + 1) * F;
+    }
+    ab = finish(ab);
+    if (!ab) signal(p.cm.gu + l);
+    return ab;
+  }
+
+  __device__ bool down(const Task& t, bool ab) {
+    const int l = t.layer, F = p.F, k = p.k, B = p.B;
+    const int r0 = t.a[0], r1 = t.a[1], nr = r1 - r0, drm = p.down_rows_max;
+    const float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
+    if (!ab && p.allh) {
+      for (int i = ct; i < B * k * F; i += NCT) act[i] = __ldcg(hb + i);
+    }
+    cbar();
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    const int rps = rows_per_stage(p, F);
+    for (int u = 0; u < U; ++u) {
+      const int nt = load_segment(rt, u);
+      int* map = m->seg_rank;  // reused below as the act row map
+      if (p.allh) {
+        if (ct < nt) map[ct] = m->seg_tok[ct] * k + m->seg_rank[ct];
+      } else if (!ab) {
+        for (int i = ct; i < nt * F; i += NCT) {
+          const int j = i / F;
+          act[i] = __ldcg(hb + ((size_t)m->seg_tok[j] * k + m->seg_rank[j]) * F + (i - j * F));
+        }
+      }
+      // seg_rank is overwritten only in allh mode; keep the true rank for ydown
+      int rank_of[NB];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) rank_of[j] = 0;
+      cbar();
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        if (j < nt) rank_of[j] = p.allh ? map[j] - m->seg_tok[j] * k : m->seg_rank[j];
+      for (int s0 = r0; s0 < r1; s0 += rps) {
+        const int n = min(rps, r1 - s0);
+        const uint8_t* st = wait_stage(ab);
+        if (st) {
+          for (int rr = cw; rr < n; rr += NCW) {
+            float s[NB];
+            row_dot(st + (size_t)rr * F * 2, F, act, F, p.allh ? map : nullptr, nt, s);
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              if (j < nt && lane == j)
+                ydown[((size_t)m->seg_tok[j] * k + rank_of[j]) * drm + (s0 + rr - r0)] = s[j];
+          }
+        }
+        release_stage(ab);
+      }
+    }
+    cbar();
+    if (!ab) {
+      const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
+      float* xo = p.x_out + (size_t)l * p.bcap * p.H;
+      const float* gt = p.gates + (size_t)l * p.bcap * k;
+      for (int i = ct; i < B * nr; i += NCT) {
+        const int b = i / nr, rr = i - b * nr;
+        float x = __ldcg(xm + (size_t)b * p.H + r0 + rr);
+        for (int j = 0; j < k; ++j)
+          x = fmaf(__ldcg(gt + b * k + j), ydown[((size_t)b * k + j) * drm + rr], x);
+        xo[(size_t)b * p.H + r0 + rr] = x;
+      }
+    }
+    ab = finish(ab);
+    if (!ab) signal(p.cm.down + l);
+    return ab;
+  }
+
+  __device__ bool attn(const Task& t, bool ab) {
+    const int l = t.layer, b = t.a[0], g = t.a[1];
+    const int G = p.G, d = p.d, ps = p.ps, half = d >> 1, dpl = d >> 5;
+    const int pos = __ldcg(p.seq_len + b);
+    int tok0, tok1;
+    attn_range(p, t, pos, tok0, tok1);
+    float* q_s = act;                 // [MAX_G][d]
+    float* kn_s = q_s + MAX_G * d;    // new token's key (bf16 values)
+    float* vn_s = kn_s + d;
+    float* mrg = vn_s + d;            // [NCW][G][d + 2]
+    const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
+    const float2* rope = p.rope + (size_t)pos * half;
+    const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
+    if (!ab) {
+      for (int idx = ct; idx < G * half; idx += NCT) {
+        const int h = idx / half, i = idx - h * half;
+        const float2 cs = rope[i];
+        const float a = __ldcg(qkv + h * d + i), c = __ldcg(qkv + h * d + i + half);
+        q_s[h * d + i] = (a * cs.x - c * cs.y) * qscale;
+        q_s[h * d + i + half] = (c * cs.x + a * cs.y) * qscale;
+      }
+      if (pos >= tok0 && pos < tok1) {
+        const float* kr = qkv + (size_t)G * d;
+        const float* vr = kr + d;
+        const size_t off =
+            (((size_t)p.page_table[(size_t)b * p.max_pages + pos / ps] * p.nkv + g) * ps + pos % ps) * d;
+        uint16_t* kd = p.k_pool[l] + off;
+        uint16_t* vd = p.v_pool[l] + off;
+        for (int i = ct; i < half; i += NCT) {
+          const float2 cs = rope[i];
+          const float a = __ldcg(kr + i), c = __ldcg(kr + i + half);
+          const uint16_t k0 = f2bf(a * cs.x - c * cs.y), k1 = f2bf(c * cs.x + a * cs.y);
+          kd[i] = k0;
+          kd[i + half] = k1;
+          kn_s[i] = bf2f(k0);
+          kn_s[i + half] = bf2f(k1);
+        }
+        for (int i = ct; i < d; i += NCT) {
+          const uint16_t v0 = f2bf(__ldcg(vr + i));
+          vd[i] = v0;
+          vn_s[i] = bf2f(v0);
+        }
+      }
+    }
+    cbar();
+    float qr[MAX_G][4], acc[MAX_G][4];
+#pragma unroll
+    for (int h = 0; h < MAX_G; ++h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qr[h][i] = (h < G && i < dpl) ? q_s[h * d + lane * dpl + i] : 0.f;
+        acc[h][i] = 0.f;
+      }
+    const int hl = (lane >> 2) & 7;  // head whose softmax state this lane keeps
+    float mrun = -INFINITY, lrun = 0.f;
+    const int ppg = pages_per_stage(p);
+    const int PB = ps * d * 2;
+    const int tps = ppg * ps;
+    for (int ts = tok0; ts < tok1; ts += tps) {
+      const int nt = min(tps, tok1 - ts);
+      const uint8_t* st = wait_stage(ab);
+      if (st) {
+        for (int jb = cw; jb < nt; jb += NCW * 8) {
+          float s[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int tl = jb + NCW * j;
+            float kf[4] = {0.f, 0.f, 0.f, 0.f};
+            if (tl < nt) {
+              if (ts + tl == pos) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (i < dpl) kf[i] = kn_s[lane * dpl + i];
+              } else {
+                const uint8_t* kr = st + (size_t)(tl / ps) * PB + (size_t)(tl % ps) * d * 2 + lane * dpl * 2;
+                if (dpl == 4) {
+                  const uint2 u = *reinterpret_cast<const uint2*>(kr);
+                  kf[0] = bf_lo(u.x); kf[1] = bf_hi(u.x); kf[2] = bf_lo(u.y); kf[3] = bf_hi(u.y);
+                } else {
+                  const uint32_t u = *reinterpret_cast<const uint32_t*>(kr);
+                  kf[0] = bf_lo(u); kf[1] = bf_hi(u);
+                }
+              }
+            }
+            float part[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+              part[h] = qr[h][0] * kf[0] + qr[h][1] * kf[1] + qr[h][2] * kf[2] + qr[h][3] * kf[3];
+            const float sv = reduce8(part, lane);
+            s[j] = (tl < nt && hl < G) ? sv : -INFINITY;
+          }
+          float bm = s[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j) bm = fmaxf(bm, s[j]);
+          const float mnew = fmaxf(mrun, bm);
+          float sc = 1.f, pj[8];
+          if (mnew == -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pj[j] = 0.f;
+          } else {
+            sc = exp2f(mrun - mnew);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pj[j] = exp2f(s[j] - mnew);
+          }
+          float psum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) psum += pj[j];
+          lrun = lrun * sc + psum;
+          mrun = mnew;
+#pragma unroll
+          for (int h = 0; h < MAX_G; ++h) {
+            const float sch = __shfl_sync(FULL, sc, h * 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[h][i] *= sch;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int tl = jb + NCW * j;
+            if (tl < nt) {
+              float vf[4] = {0.f, 0.f, 0.f, 0.f};
+              if (ts + tl == pos) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (i < dpl) vf[i] = vn_s[lane * dpl + i];
+              } else {
+                const uint8_t* vr =
+                    st + (size_t)(ppg + tl / ps) * PB + (size_t)(tl % ps) * d * 2 + lane * dpl * 2;
+                if (dpl == 4) {
+                  const uint2 u = *reinterpret_cast<const uint2*>(vr);
+                  vf[0] = bf_lo(u.x); vf[1] = bf_hi(u.x); vf[2] = bf_lo(u.y); vf[3] = bf_hi(u.y);
+                } else {
+                  const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
+                  vf[0] = bf_lo(u); vf[1] = bf_hi(u);
+                }
+              }
+#pragma unroll
+              for (int h = 0; h < MAX_G; ++h) {
+                const float ph = __shfl_sync(FULL, pj[j], h * 4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(ph, vf[i], acc[h][i]);
+              }
+            }
+          }
+        }
+      }
+      release_stage(ab);
+    }
+    // merge the 8 warps' partial softmax states of this chunk
+    const int RS = d + 2;
+    if (!ab) {
+      if ((lane & 3) == 0 && hl < G) {
+        mrg[(cw * G + hl) * RS + d] = mrun;
+        mrg[(cw * G + hl) * RS + d + 1] = lrun;
+      }
+#pragma unroll
+      for (int h = 0; h < MAX_G; ++h)
+        if (h < G)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < dpl) mrg[(cw * G + h) * RS + lane * dpl + i] = acc[h][i];
+    }
+    ab = cbar_or(ab);
+    if (ab) return ab;
+    const int nslots = p.part_slots;
+    float* part = p.part + ((size_t)l * nslots + t.a[4]) * G * RS;
+    for (int idx = ct; idx < G * d; idx += NCT) {
+      const int h = idx / d, i = idx - h * d;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
+      float Ls = 0.f, A = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) {
+        const float mw = mrg[(w * G + h) * RS + d];
+        if (mw != -INFINITY) {
+          const float f = exp2f(mw - M);
+          Ls = fmaf(mrg[(w * G + h) * RS + d + 1], f, Ls);
+          A = fmaf(mrg[(w * G + h) * RS + i], f, A);
+        }
+      }
+      part[h * RS + i] = A;
+      if (i == 0) {
+        part[h * RS + d] = M;
+        part[h * RS + d + 1] = Ls;
+      }
+    }
+    ab = finish(ab);
+    if (ab) return ab;
+    if (ticket(p.cm.attn_idx(l, b, g), (uint32_t)t.a[6])) {
+      const float* p0 = p.part + ((size_t)l * nslots + t.a[5]) * G * RS;
+      const int nc = t.a[6];
+      float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
+      for (int idx = ct; idx < G * d; idx += NCT) {
+        const int h = idx / d, i = idx - h * d;
+        float M = -INFINITY;
+        for (int c = 0; c < nc; ++c) M = fmaxf(M, __ldcg(p0 + ((size_t)c * G + h) * RS + d));
+        float Ls = 0.f, A = 0.f;
+        for (int c = 0; c < nc; ++c) {
+          const float* pc = p0 + ((size_t)c * G + h) * RS;
+          const float f = exp2f(__ldcg(pc + d) - M);
+          Ls = fmaf(__ldcg(pc + d + 1), f, Ls);
+          A = fmaf(__ldcg(pc + i), f, A);
+        }
+        o[h * d + i] = A / Ls;
+      }
+      ab = finish(false);
+      if (!ab) signal(p.cm.combine + l);
+    }
+    return ab;
+  }
+
+  __device__ bool lm(const Task& t, bool ab) {
+    const int L = p.L, B = p.B;
+    if (!ab) {
+      const float* xo = p.x_out + (size_t)(L - 1) * p.bcap * p.H;
+      fill_rmsnorm(p.final_norm, [&](int b, int i) { return __ldcg(xo + (size_t)b * p.H + i); });
+    }
+    cbar();
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    float* lg = p.logits;
+    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, const float(&s)[NB]) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        if (j < B && lane == j) {
+          if (lg) lg[(size_t)j * p.V + row] = s[j];
+          if (s[j] > bv || (s[j] == bv && row < bi)) { bv = s[j]; bi = row; }
+        }
+      }
+    });
+    if (!ab && lane < B) {
+      m->best_v[cw * MAX_BATCH + lane] = bv;
+      m->best_i[cw * MAX_BATCH + lane] = bi;
+    }
+    ab = cbar_or(ab);
+    if (ab) return ab;
+    const int tiles = p.lm_tiles, tile = t.a[2];
+    if (ct < B) {
+      float v = -INFINITY;
+      int ix = 0x7fffffff;
+      for (int w = 0; w < NCW; ++w) {
+        const float wv = m->best_v[w * MAX_BATCH + ct];
+        const int wi = m->best_i[w * MAX_BATCH + ct];
+        if (wv > v || (wv == v && wi < ix)) { v = wv; ix = wi; }
+      }
+      p.lm_val[(size_t)ct * tiles + tile] = v;
+      p.lm_idx[(size_t)ct * tiles + tile] = ix;
+    }
+    ab = finish(ab);
+    if (ab) return ab;
+    if (ticket(p.cm.lm, (uint32_t)t.a[3])) {
+      if (cw < B) {
+        const int b = cw;
+        float v = -INFINITY;
+        int ix = 0x7fffffff;
+        for (int i = lane; i < tiles; i += 32) {
+          const float tv = __ldcg(p.lm_val + (size_t)b * tiles + i);
+          const int tix = __ldcg(p.lm_idx + (size_t)b * tiles + i);
+          if (tv > v || (tv == v && tix < ix)) { v = tv; ix = tix; }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ov = __shfl_xor_sync(FULL, v, o);
+          const int oi = __shfl_xor_sync(FULL, ix, o);
+          if (ov > v || (ov == v && oi < ix)) { v = ov; ix = oi; }
+        }
+        if (lane == 0) {
+          p.next_token[b] = ix;
+          p.seq_len[b] = __ldcg(p.seq_len + b) + 1;
+        }
+      }
+      ab = finish(false);
+    }
+    return ab;
+  }
+
+  __device__ void run(int t0, int t1) {
+    for (int ti = t0; ti < t1; ++ti) {
+      const Task t = p.tasks[ti];
+      bool ab = false;
+      if (ct == 0) ab = !wait_ctr(p, t.wait_ctr, t.wait_cnt, ti);
+      ab = cbar_or(ab);
+      if (ab) break;
+      if (ct == 0) __threadfence();
+      switch (t.type) {
+        case T_QKV: ab = qkv(t, ab); break;
+        case T_ATTN: ab = attn(t, ab); break;
+        case T_OPROJ: ab = oproj(t, ab); break;
+        case T_ROUTER: ab = router(t, ab); break;
+        case T_GU: ab = gate_up(t, ab); break;
+        case T_DOWN: ab = down(t, ab); break;
+        case T_LM: ab = lm(t, ab); break;
+        default: ab = true;
+      }
+      if (ab) break;
+    }
+    if (ct == 0) m->abort_flag = m->abort_flag;  // keep the flag for the drain
+  }
+};
+
+// Wait (bounded) for every bulk copy still in flight before the CTA exits.
+__device__ void drain(const Params& p, Misc* m, int nst) {
+  for (int s = 0; s < nst; ++s) {
+    const int rd = m->armed[s];
+    if (rd < 0) continue;
+    const uint64_t t0 = gtimer();
+    while (!mbar_try_wait(&m->full[s], rd & 1)) {
+      if (gtimer() - t0 > p.timeout_ns) {
+        set_error(p, MK_ERR_DEP_TIMEOUT, -1, -5);
+        break;
+      }
+    }
+  }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Misc* m = reinterpret_cast<Misc*>(smem + p.misc_off);
+  float* act = reinterpret_cast<float*>(smem + p.act_off);
+  float* ydown = reinterpret_cast<float*>(smem + p.misc_off + sizeof(Misc));
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < p.nstages; ++s) {
+      mbar_init(&m->full[s], 1);
+      mbar_init(&m->empty[s], NCW);
+      m->armed[s] = -1;
+    }
+    m->abort_flag = 0;
+    m->dead = failed(p) ? 1 : 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (!m->dead) {
+    const int t0 = p.cta_start[blockIdx.x], t1 = p.cta_start[blockIdx.x + 1];
+    Ring ring{smem, m, p.nstages, p.stage_bytes, 0, 0};
+    if (tid >= NCT) {
+      if (tid == NCT) {
+        Producer pr{p, ring, evict_first_policy()};
+        pr.run(t0, t1);
+      }
+    } else {
+      Consumer<NB> c{p, ring, act, m, ydown, tid, tid >> 5, tid & 31};
+      c.run(t0, t1);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) drain(p, m, p.nstages);
+}
+
+__global__ void k_rope_table(float2* tab, int npos, int half, int d, double theta) {
+  const long long n = (long long)npos * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int pos = (int)(idx / half), i = (int)(idx % half);
+    const double inv = pow(theta, -2.0 * i / d);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+template <int NB>
+cudaError_t set_smem_attr() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(mk_megakernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+template <int NB>
+cudaError_t launch_nb(const Params& p, int grid, int smem, cudaStream_t st) {
+  cudaError_t e = set_smem_attr<NB>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mk_megakernel<NB>, p);
+}
+
+template <int NB>
+int occupancy(int smem) {
+  if (set_smem_attr<NB>() != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mk_megakernel<NB>, NTHREADS, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_megakernel(const Params& p, int nb, int grid, int smem, cudaStream_t st) {
+  switch (nb) {
+    case 1: return launch_nb<1>(p, grid, smem, st);
+    case 2: return launch_nb<2>(p, grid, smem, st);
+    case 4: return launch_nb<4>(p, grid, smem, st);
+    case 8: return launch_nb<8>(p, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_rope_table(float2* tab, int npos, int d, double theta, cudaStream_t st) {
+  const int half = d / 2;
+  long long n = (long long)npos * half;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  k_rope_table<<<blocks, 256, 0, st>>>(tab, npos, half, d, theta);
+  return cudaGetLastError();
+}
+
+int max_active_ctas(int nb, int smem) {
+  switch (nb) {
+    case 1: return occupancy<1>(smem);
+    case 2: return occupancy<2>(smem);
+    case 4: return occupancy<4>(smem);
+    case 8: return occupancy<8>(smem);
+    default: return 0;
+  }
+}
+
+size_t misc_bytes() { return sizeof(Misc); }
+
+}  // namespace mk

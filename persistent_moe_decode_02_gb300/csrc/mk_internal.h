@@ -1,0 +1,130 @@
+// Internal layout shared by the host planner (plan.cu) and the megakernel
+// (megakernel.cu): the task record, the counter map and the kernel parameters.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mk {
+
+constexpr int NCW = 8;                     // consumer warps per CTA
+constexpr int NTHREADS = (NCW + 1) * 32;   // + one producer warp
+constexpr int MAX_STAGES = 16;             // smem ring stages (upper bound)
+constexpr int MAX_TOPK = 8;
+constexpr int MAX_G = 8;                   // query heads per KV head
+constexpr int MAX_BATCH = 8;
+constexpr int MAX_EXPERTS = 256;
+constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
+constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
+
+// Task kinds in per-layer order.  Each kind signals one counter family.
+enum TaskType : int32_t {
+  T_QKV = 0,     // rows [a0,a1) of the grouped QKV matrix, all requests; a2 = KV group
+  T_ATTN = 1,    // request a0, KV group a1, KV pages [a2, a3) (a3 < 0: to the current end);
+                 // a4 = partial slot, a5 = first slot of (a0, a1), a6 = chunks of (a0, a1)
+  T_OPROJ = 2,   // rows [a0,a1) of Wo, residual add
+  T_ROUTER = 3,  // rows [a0,a1) of the router; a2 = router tiles (ticket target)
+  T_GU = 4,      // gate/up tile a0 of a1 over the flattened (distinct expert, ffn row) space
+  T_DOWN = 5,    // rows [a0,a1) of the hidden dim over every selected expert, residual add
+  T_LM = 6,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
+};
+
+struct alignas(16) Task {
+  int32_t type;
+  int32_t layer;
+  int32_t a[8];
+  int32_t wait_ctr;    // counter index or -1
+  uint32_t wait_cnt;   // signals per step that satisfy the wait
+};
+static_assert(sizeof(Task) == 48, "task record is 48 bytes");
+
+// Counter map.  All counters only grow; a wait for `cnt` signals per step is
+// satisfied when counter >= epoch * cnt (epoch = 1, 2, ... since the last reset).
+struct CtrMap {
+  int L, nkv, bcap;
+  int qkv, attn, combine, o, rticket, rdone, gu, down, lm, total;
+
+  void init(int L_, int nkv_, int bcap_) {
+    L = L_; nkv = nkv_; bcap = bcap_;
+    int c = 0;
+    qkv = c; c += L * nkv;
+    attn = c; c += L * bcap * nkv;
+    combine = c; c += L;
+    o = c; c += L;
+    rticket = c; c += L;
+    rdone = c; c += L;
+    gu = c; c += L;
+    down = c; c += L;
+    lm = c; c += 1;
+    total = c;
+  }
+#if defined(__CUDACC__)
+  __host__ __device__
+#endif
+  int attn_idx(int l, int b, int g) const { return attn + (l * bcap + b) * nkv + g; }
+};
+
+// Per-layer routing record in global memory (ints):
+//   [0] distinct experts U, then expert[umax], count[umax], tok[umax][bcap], rank[umax][bcap]
+struct RouteMap {
+  int umax, bcap, ints;
+  void init(int umax_, int bcap_) { umax = umax_; bcap = bcap_; ints = 1 + 2 * umax + 2 * umax * bcap; }
+};
+
+struct Params {
+  // shape
+  int L, H, nq, nkv, d, E, k, F, V, ps, G;
+  int qkv_rows;        // nkv * (G + 2) * d
+  float eps;
+  int B, bcap, max_pages;
+  // weights (device arrays of L device pointers where per layer)
+  const uint16_t* embed;
+  const uint16_t* final_norm;
+  const uint16_t* lm_head;
+  const uint16_t* const* attn_norm;
+  const uint16_t* const* wqkv;
+  const uint16_t* const* wo;
+  const uint16_t* const* ffn_norm;
+  const uint16_t* const* router;
+  const uint16_t* const* w_gate_up;
+  const uint16_t* const* w_down;
+  uint16_t* const* k_pool;
+  uint16_t* const* v_pool;
+  // plan
+  const Task* tasks;
+  const int* cta_start;
+  uint32_t* ctr;
+  int* status;          // [0] code, [1] task, [2] cta, [3] info
+  uint32_t epoch;
+  unsigned long long timeout_ns;
+  CtrMap cm;
+  RouteMap rm;
+  int nstages, stage_bytes;
+  int act_off, act_floats, misc_off;
+  int allh;             // 1: the down task keeps every (request, rank) h row in smem
+  int down_rows_max;
+  int* seq_len;         // device [bcap]
+  const int* page_table;  // device [bcap * max_pages]
+  const float2* rope;   // [max_pos][d/2] (cos, sin)
+  int rope_npos;
+  // per-layer scratch (fp32 unless noted), all strided by bcap
+  float* qkv;           // [L][bcap][qkv_rows]
+  float* part;          // [L][part_slots][G][d + 2]
+  int part_slots;
+  float* o;             // [L][bcap][nq*d]
+  float* x_mid;         // [L][bcap][H]
+  float* x_out;         // [L][bcap][H]
+  float* rlog;          // [L][bcap][E]
+  int* ids;             // [L][bcap][k]
+  float* gates;         // [L][bcap][k]
+  int* route;           // [L][rm.ints]
+  float* hbuf;          // [L][bcap][k][F]
+  float* lm_val;        // [bcap][lm_tiles]
+  int* lm_idx;          // [bcap][lm_tiles]
+  int lm_tiles;
+  // io
+  const int* tokens;
+  float* logits;        // nullable [B][V]
+  int* next_token;
+};
+
+}  // namespace mk

@@ -1,0 +1,791 @@
+// Host side of libmk: the task-list and dependency-counter builder ("Each SM
+// gets a task list, and dependencies are tracked with counters in global
+// memory" — "Inside the Megakernel Serving Engine for North Mini Code",
+// architecture paragraph) and the C ABI of include/mk.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <new>
+#include <vector>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+cudaError_t launch_megakernel(const Params& p, int nb, int grid, int smem, cudaStream_t st);
+cudaError_t launch_rope_table(float2* tab, int npos, int d, double theta, cudaStream_t st);
+int max_active_ctas(int nb, int smem);
+size_t misc_bytes();
+}  // namespace mk
+
+using mk::Task;
+
+namespace {
+
+// Text of the most recent failure inside the library (per thread).
+thread_local char g_last_error[256] = "";
+
+int note_cuda(cudaError_t e, const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  return MK_ERR_CUDA;
+}
+
+struct Shape {
+  int L, H, nq, nkv, d, E, k, F, V, ps, G, qkv_rows;
+  float eps, theta;
+};
+
+int check_dims(const mk_model_dims* m, Shape& s) {
+  if (!m) return MK_ERR_INVALID;
+  s.L = m->n_layers; s.H = m->hidden; s.nq = m->n_q_heads; s.nkv = m->n_kv_heads; s.d = m->head_dim;
+  s.E = m->n_experts; s.k = m->top_k; s.F = m->expert_ffn; s.V = m->vocab; s.ps = m->page_size;
+  s.eps = m->rms_eps; s.theta = m->rope_theta;
+  if (s.L < 1 || s.H < 8 || s.nq < 1 || s.nkv < 1 || s.E < 1 || s.k < 1 || s.F < 8 || s.V < 1)
+    return MK_ERR_INVALID;
+  if (s.nq % s.nkv) return MK_ERR_INVALID;
+  s.G = s.nq / s.nkv;
+  if (s.k > s.E || !(s.eps >= 0.f) || !(s.theta > 0.f)) return MK_ERR_INVALID;
+  if (s.H % 8 || s.F % 8 || (s.nq * s.d) % 8) return MK_ERR_INVALID;
+  if (s.ps != 16) return MK_ERR_UNSUPPORTED;
+  if (s.d != 64 && s.d != 128) return MK_ERR_UNSUPPORTED;
+  if (s.G > mk::MAX_G || s.k > mk::MAX_TOPK || s.E > mk::MAX_EXPERTS) return MK_ERR_UNSUPPORTED;
+  s.qkv_rows = s.nkv * (s.G + 2) * s.d;
+  return MK_OK;
+}
+
+struct Counts {
+  int qkv_per_g = 0, attn = 0, o = 0, router = 0, gu = 0, down = 0, lm = 0;
+  int part_slots = 0, pages_per_chunk = 1, down_rows_max = 1;
+};
+
+// Phase-balanced assignment: tasks of one phase go, largest first, to the CTA
+// with the least work in this phase (ties: least work so far, then lowest id).
+struct Assigner {
+  int C;
+  std::vector<std::vector<Task>> per_cta;
+  std::vector<double> total;
+  explicit Assigner(int c) : C(c), per_cta(c), total(c, 0.0) {}
+  void phase(std::vector<std::pair<double, Task>>& ts) {
+    std::stable_sort(ts.begin(), ts.end(),
+                     [](const std::pair<double, Task>& a, const std::pair<double, Task>& b) {
+                       return a.first > b.first;
+                     });
+    std::vector<double> ph(C, 0.0);
+    for (auto& t : ts) {
+      int best = 0;
+      for (int c = 1; c < C; ++c) {
+        if (ph[c] < ph[best] || (ph[c] == ph[best] && total[c] < total[best])) best = c;
+      }
+      ph[best] += t.first;
+      total[best] += t.first;
+      per_cta[best].push_back(t.second);
+    }
+  }
+};
+
+Task mk_task(int type, int layer, int wait_ctr, uint32_t wait_cnt) {
+  Task t;
+  memset(&t, 0, sizeof(t));
+  t.type = type;
+  t.layer = layer;
+  t.wait_ctr = wait_ctr;
+  t.wait_cnt = wait_cnt;
+  return t;
+}
+
+// Pages covering positions [0, len] (the cached tokens plus the new one).
+inline int pages_for(int len, int ps) { return len / ps + 1; }
+
+// Split n items into `parts` nearly equal contiguous ranges.
+inline void split_range(int n, int parts, int i, int& a, int& b) {
+  a = (int)((long long)n * i / parts);
+  b = (int)((long long)n * (i + 1) / parts);
+}
+
+// Builds the task list in global topological order, phase by phase, then
+// hands each phase's tasks to CTAs; every CTA's list is a subsequence of one
+// topological order, so with all CTAs resident the step cannot deadlock.
+int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int split_pages,
+                std::vector<Task>& out, std::vector<int>& cta_start, Counts& cnt,
+                std::vector<int>& open_start) {
+  if (B < 1 || B > bcap || C < 1) return MK_ERR_INVALID;
+  mk::CtrMap cm;
+  cm.init(s.L, s.nkv, bcap);
+  Assigner asg(C);
+  const int Rg = (s.G + 2) * s.d;
+  const int nqd = s.nq * s.d;
+  // tile counts
+  cnt.qkv_per_g = std::max(1, std::min(Rg, (C + s.nkv - 1) / s.nkv));
+  cnt.o = std::max(1, std::min(s.H, C));
+  cnt.router = std::max(1, std::min(s.E, 32));
+  const int umax = std::min(s.E, B * s.k);
+  cnt.gu = std::max(1, std::min(C, umax * s.F));
+  cnt.down = std::max(1, std::min(s.H, C));
+  cnt.lm = std::max(1, std::min(s.V, 4 * C));
+  cnt.down_rows_max = (s.H + cnt.down - 1) / cnt.down;
+  // attention chunking
+  long long total_pages = 0;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0) return MK_ERR_INVALID;
+    total_pages += pages_for(seq_lens[b], s.ps);
+  }
+  int P = split_pages;
+  if (P <= 0) P = (int)std::max<long long>(1, (total_pages * s.nkv + C - 1) / C);
+  cnt.pages_per_chunk = P;
+  std::vector<int> nch(B);
+  open_start.assign(B, 0);
+  int slots = 0;
+  for (int b = 0; b < B; ++b) {
+    nch[b] = (pages_for(seq_lens[b], s.ps) + P - 1) / P;
+    open_start[b] = (nch[b] - 1) * P;
+    slots += nch[b] * s.nkv;
+  }
+  cnt.part_slots = slots;
+  cnt.attn = slots;
+  const double PB = 2.0 * s.ps * s.d * 2;
+
+  for (int l = 0; l < s.L; ++l) {
+    std::vector<std::pair<double, Task>> ph;
+    // QKV projection tiles, per KV group
+    for (int g = 0; g < s.nkv; ++g) {
+      for (int i = 0; i < cnt.qkv_per_g; ++i) {
+        int a, b;
+        split_range(Rg, cnt.qkv_per_g, i, a, b);
+        Task t = mk_task(mk::T_QKV, l, l == 0 ? -1 : cm.down + l - 1, (uint32_t)cnt.down);
+        t.a[0] = g * Rg + a;
+        t.a[1] = g * Rg + b;
+        t.a[2] = g;
+        ph.push_back({(double)(b - a) * s.H * 2, t});
+      }
+    }
+    asg.phase(ph);
+    ph.clear();
+    // split-KV attention chunks
+    int slot = 0;
+    for (int b = 0; b < B; ++b) {
+      const int np = pages_for(seq_lens[b], s.ps);
+      for (int g = 0; g < s.nkv; ++g) {
+        const int first = slot;
+        for (int c = 0; c < nch[b]; ++c) {
+          Task t = mk_task(mk::T_ATTN, l, cm.qkv + l * s.nkv + g, (uint32_t)cnt.qkv_per_g);
+          t.a[0] = b;
+          t.a[1] = g;
+          t.a[2] = c * P;
+          t.a[3] = (c == nch[b] - 1) ? -1 : (c + 1) * P;
+          t.a[4] = slot++;
+          t.a[5] = first;
+          t.a[6] = nch[b];
+          const int pages = (c == nch[b] - 1) ? np - c * P : P;
+          ph.push_back({pages * PB, t});
+        }
+      }
+    }
+    asg.phase(ph);
+    ph.clear();
+    // O projection + residual
+    for (int i = 0; i < cnt.o; ++i) {
+      int a, b;
+      split_range(s.H, cnt.o, i, a, b);
+      Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)(B * s.nkv));
+      t.a[0] = a;
+      t.a[1] = b;
+      ph.push_back({(double)(b - a) * nqd * 2, t});
+    }
+    asg.phase(ph);
+    ph.clear();
+    // router logits (last tile also takes the top-k)
+    for (int i = 0; i < cnt.router; ++i) {
+      int a, b;
+      split_range(s.E, cnt.router, i, a, b);
+      Task t = mk_task(mk::T_ROUTER, l, cm.o + l, (uint32_t)cnt.o);
+      t.a[0] = a;
+      t.a[1] = b;
+      t.a[2] = cnt.router;
+      ph.push_back({(double)(b - a) * s.H * 2, t});
+    }
+    asg.phase(ph);
+    ph.clear();
+    // expert gate/up tiles over the distinct selected experts
+    for (int i = 0; i < cnt.gu; ++i) {
+      Task t = mk_task(mk::T_GU, l, cm.rdone + l, 1u);
+      t.a[0] = i;
+      t.a[1] = cnt.gu;
+      ph.push_back({(double)umax * s.F * 4.0 * s.H / cnt.gu, t});
+    }
+    asg.phase(ph);
+    ph.clear();
+    // expert down tiles + weighted combine + residual
+    for (int i = 0; i < cnt.down; ++i) {
+      int a, b;
+      split_range(s.H, cnt.down, i, a, b);
+      Task t = mk_task(mk::T_DOWN, l, cm.gu + l, (uint32_t)cnt.gu);
+      t.a[0] = a;
+      t.a[1] = b;
+      ph.push_back({(double)(b - a) * umax * s.F * 2, t});
+    }
+    asg.phase(ph);
+  }
+  std::vector<std::pair<double, Task>> ph;
+  for (int i = 0; i < cnt.lm; ++i) {
+    int a, b;
+    split_range(s.V, cnt.lm, i, a, b);
+    Task t = mk_task(mk::T_LM, s.L - 1, cm.down + s.L - 1, (uint32_t)cnt.down);
+    t.a[0] = a;
+    t.a[1] = b;
+    t.a[2] = i;
+    t.a[3] = cnt.lm;
+    ph.push_back({(double)(b - a) * s.H * 2, t});
+  }
+  asg.phase(ph);
+
+  out.clear();
+  cta_start.assign(C + 1, 0);
+  for (int c = 0; c < C; ++c) {
+    cta_start[c] = (int)out.size();
+    out.insert(out.end(), asg.per_cta[c].begin(), asg.per_cta[c].end());
+  }
+  cta_start[C] = (int)out.size();
+  return MK_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ the plan
+
+struct mk_plan {
+  Shape s;
+  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0;
+  int max_pages = 0, num_pages = 0, rope_npos = 0;
+  int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0, allh = 0;
+  int replans = 0;
+  uint32_t epoch = 0;
+  unsigned long long timeout_ns = 0;
+  std::vector<int> seq, pt, open_start;
+  std::vector<Task> tasks;
+  std::vector<int> cta_start;
+  Counts cnt;
+  mk::CtrMap cm;
+  mk::RouteMap rm;
+  mk::Params P;
+  // device buffers owned by the plan
+  std::vector<void*> allocs;
+  Task* d_tasks = nullptr;
+  size_t tasks_cap = 0;
+  int* d_cta = nullptr;
+  uint32_t* d_ctr = nullptr;
+  int* d_status = nullptr;
+  int* d_seq = nullptr;
+  int* d_pt = nullptr;
+  size_t pt_cap = 0;
+  float2* d_rope = nullptr;
+  float* d_part = nullptr;
+  size_t part_cap_slots = 0;
+  int* d_io_tok = nullptr;
+  int* d_io_next = nullptr;
+  float* d_io_logits = nullptr;
+  // pinned staging for uploads, protected by an event
+  void* h_stage = nullptr;
+  size_t h_stage_cap = 0;
+  cudaEvent_t ev_stage = nullptr;
+  int* h_status = nullptr;
+};
+
+namespace {
+
+template <class T>
+cudaError_t dalloc(mk_plan* p, T** ptr, size_t bytes) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, bytes ? bytes : 16);
+  if (e != cudaSuccess) return e;
+  p->allocs.push_back(v);
+  *ptr = (T*)v;
+  return cudaSuccess;
+}
+
+void dfree(mk_plan* p, void* ptr) {
+  if (!ptr) return;
+  auto it = std::find(p->allocs.begin(), p->allocs.end(), ptr);
+  if (it != p->allocs.end()) p->allocs.erase(it);
+  cudaFree(ptr);
+}
+
+bool aligned16(const void* q) { return q && ((uintptr_t)q % 16) == 0; }
+
+int validate_batch(const Shape& s, int B, const int* seq_lens, const int* page_table, int max_pages,
+                   int num_pages) {
+  if (!seq_lens || !page_table || max_pages < 1) return MK_ERR_INVALID;
+  std::vector<char> used((size_t)num_pages, 0);
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0) return MK_ERR_INVALID;
+    const int np = pages_for(seq_lens[b], s.ps);
+    if (np > max_pages) return MK_ERR_CAPACITY;
+    for (int i = 0; i < np; ++i) {
+      const int pg = page_table[(size_t)b * max_pages + i];
+      if (pg < 0 || pg >= num_pages) return MK_ERR_INVALID;
+      if (used[pg]) return MK_ERR_INVALID;  // two positions may not share a page
+      used[pg] = 1;
+    }
+  }
+  return MK_OK;
+}
+
+// Stage the bytes in pinned memory and enqueue the copy to `dst` on `st`.
+cudaError_t upload(mk_plan* p, void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  cudaError_t e;
+  if (p->ev_stage) {
+    e = cudaEventSynchronize(p->ev_stage);  // previous upload no longer reads the staging buffer
+    if (e != cudaSuccess) return e;
+  }
+  if (bytes > p->h_stage_cap) {
+    if (p->h_stage) cudaFreeHost(p->h_stage);
+    p->h_stage = nullptr;
+    e = cudaMallocHost(&p->h_stage, bytes);
+    if (e != cudaSuccess) return e;
+    p->h_stage_cap = bytes;
+  }
+  memcpy(p->h_stage, src, bytes);
+  e = cudaMemcpyAsync(dst, p->h_stage, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecord(p->ev_stage, st);
+}
+
+// Rebuild tasks for the plan's current lengths, upload them, reset counters.
+int replan(mk_plan* p, cudaStream_t st) {
+  std::vector<Task> tasks;
+  std::vector<int> cs;
+  Counts cnt;
+  std::vector<int> open;
+  int rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, tasks, cs, cnt, open);
+  if (rc != MK_OK) return rc;
+  if (p->drop_task > 0 && p->drop_task - 1 < (int)tasks.size()) {
+    const int victim = p->drop_task - 1;
+    tasks.erase(tasks.begin() + victim);
+    for (int c = 0; c <= p->C; ++c)
+      if (cs[c] > victim) cs[c]--;
+  }
+  cudaError_t e;
+  // one device blob: tasks, then the C + 1 CTA offsets (48-byte tasks keep it 16-byte aligned)
+  const size_t blob_bytes = tasks.size() * sizeof(Task) + cs.size() * sizeof(int);
+  if (blob_bytes > p->tasks_cap) {
+    if (p->d_tasks) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+      dfree(p, p->d_tasks);
+      p->d_tasks = nullptr;
+    }
+    const size_t cap = blob_bytes + blob_bytes / 2 + 4096;
+    if ((e = dalloc(p, (uint8_t**)&p->d_tasks, cap)) != cudaSuccess) return MK_ERR_CUDA;
+    p->tasks_cap = cap;
+  }
+  if ((size_t)cnt.part_slots > p->part_cap_slots) {
+    // grow the attention partial buffer (rare: only when a replan adds chunks)
+    if (p->d_part) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+      dfree(p, p->d_part);
+      p->d_part = nullptr;
+    }
+    size_t cap = (size_t)cnt.part_slots * 2 + 16;
+    if (dalloc(p, &p->d_part, (size_t)p->s.L * cap * p->s.G * (p->s.d + 2) * sizeof(float)) != cudaSuccess)
+      return MK_ERR_CUDA;
+    p->part_cap_slots = cap;
+  }
+  std::vector<uint8_t> blob(blob_bytes);
+  memcpy(blob.data(), tasks.data(), tasks.size() * sizeof(Task));
+  memcpy(blob.data() + tasks.size() * sizeof(Task), cs.data(), cs.size() * sizeof(int));
+  if (upload(p, p->d_tasks, blob.data(), blob_bytes, st) != cudaSuccess) return MK_ERR_CUDA;
+  p->d_cta = (int*)((uint8_t*)p->d_tasks + tasks.size() * sizeof(Task));
+  if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  p->epoch = 0;
+  p->tasks.swap(tasks);
+  p->cta_start.swap(cs);
+  p->cnt = cnt;
+  p->open_start.swap(open);
+  p->replans++;
+  return MK_OK;
+}
+
+bool needs_replan(const mk_plan* p) {
+  const int P = p->cnt.pages_per_chunk;
+  const int slack = std::max(2, P / 2);
+  for (int b = 0; b < p->B; ++b) {
+    const int open_pages = pages_for(p->seq[b], p->s.ps) - p->open_start[b];
+    if (open_pages > P + slack) return true;
+  }
+  return false;
+}
+
+void fill_params(mk_plan* p) {
+  mk::Params& P = p->P;
+  const Shape& s = p->s;
+  P.L = s.L; P.H = s.H; P.nq = s.nq; P.nkv = s.nkv; P.d = s.d; P.E = s.E; P.k = s.k; P.F = s.F;
+  P.V = s.V; P.ps = s.ps; P.G = s.G; P.qkv_rows = s.qkv_rows; P.eps = s.eps;
+  P.B = p->B; P.bcap = p->bcap; P.max_pages = p->max_pages;
+  P.tasks = p->d_tasks; P.cta_start = p->d_cta; P.ctr = p->d_ctr; P.status = p->d_status;
+  P.timeout_ns = p->timeout_ns; P.cm = p->cm; P.rm = p->rm;
+  P.nstages = p->nstages; P.stage_bytes = p->stage_bytes;
+  P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
+  P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
+  P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_last_error(void) { return g_last_error; }
+
+const char* mk_status_string(int st) {
+  switch (st) {
+    case MK_OK: return "ok";
+    case MK_ERR_INVALID: return "invalid argument";
+    case MK_ERR_CUDA: return "CUDA runtime error";
+    case MK_ERR_DEP_TIMEOUT: return "device dependency wait timed out";
+    case MK_ERR_CAPACITY: return "capacity exceeded (batch, pages or positions)";
+    case MK_ERR_UNSUPPORTED: return "unsupported shape";
+    default: return "unknown status";
+  }
+}
+
+int mk_plan_inspect(const mk_model_dims* dims, int batch, const int* seq_lens, int num_ctas,
+                    int split_pages, int* tasks_out, int max_tasks, int* cta_start_out) {
+  Shape s;
+  int rc = check_dims(dims, s);
+  if (rc != MK_OK) return rc;
+  if (!seq_lens || batch < 1 || batch > mk::MAX_BATCH || num_ctas < 1) return MK_ERR_INVALID;
+  std::vector<Task> tasks;
+  std::vector<int> cs, open;
+  Counts cnt;
+  rc = build_tasks(s, batch, batch, seq_lens, num_ctas, split_pages, tasks, cs, cnt, open);
+  if (rc != MK_OK) return rc;
+  if (tasks_out) {
+    const int n = std::min<int>(max_tasks, (int)tasks.size());
+    for (int i = 0; i < n; ++i) {
+      const Task& t = tasks[i];
+      int* o = tasks_out + 12 * i;
+      o[0] = t.type; o[1] = t.layer;
+      for (int j = 0; j < 8; ++j) o[2 + j] = t.a[j];
+      o[10] = t.wait_ctr; o[11] = (int)t.wait_cnt;
+    }
+  }
+  if (cta_start_out) memcpy(cta_start_out, cs.data(), cs.size() * sizeof(int));
+  return (int)tasks.size();
+}
+
+int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
+                   const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   const mk_plan_opts* opts, mk_plan** out) {
+  if (!out) return MK_ERR_INVALID;
+  *out = nullptr;
+  Shape s;
+  int rc = check_dims(dims, s);
+  if (rc != MK_OK) return rc;
+  if (!w || !kv || batch < 1) return MK_ERR_INVALID;
+  mk_plan_opts o = {};
+  if (opts) o = *opts;
+  const int bcap = o.max_batch > 0 ? o.max_batch : batch;
+  if (batch > bcap) return MK_ERR_INVALID;
+  if (bcap > mk::MAX_BATCH) return MK_ERR_UNSUPPORTED;
+  if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head)) return MK_ERR_INVALID;
+  if (!w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->router || !w->w_gate_up || !w->w_down)
+    return MK_ERR_INVALID;
+  if (!kv->k_pool || !kv->v_pool || kv->num_pages < 1) return MK_ERR_INVALID;
+  for (int l = 0; l < s.L; ++l) {
+    if (!aligned16(w->attn_norm[l]) || !aligned16(w->wqkv[l]) || !aligned16(w->wo[l]) ||
+        !aligned16(w->ffn_norm[l]) || !aligned16(w->router[l]) || !aligned16(w->w_gate_up[l]) ||
+        !aligned16(w->w_down[l]) || !aligned16(kv->k_pool[l]) || !aligned16(kv->v_pool[l]))
+      return MK_ERR_INVALID;
+  }
+  rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages);
+  if (rc != MK_OK) return rc;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MK_ERR_CUDA;
+
+  mk_plan* p = new (std::nothrow) mk_plan();
+  if (!p) return MK_ERR_CUDA;
+  p->s = s;
+  p->B = batch;
+  p->bcap = bcap;
+  p->nb = bcap <= 1 ? 1 : bcap <= 2 ? 2 : bcap <= 4 ? 4 : 8;
+  p->C = o.num_ctas > 0 ? std::min(o.num_ctas, sms) : sms;
+  p->split_opt = o.split_pages;
+  p->drop_task = o.debug_drop_task;
+  p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
+  p->max_pages = max_pages_per_seq;
+  p->num_pages = kv->num_pages;
+  p->seq.assign(seq_lens, seq_lens + batch);
+  p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
+  p->cm.init(s.L, s.nkv, bcap);
+  p->rm.init(std::min(s.E, bcap * s.k), bcap);
+
+  auto fail = [&](int code) {
+    if (code == MK_ERR_CUDA && !g_last_error[0]) note_cuda(cudaGetLastError(), "mk_plan_create");
+    mk_plan_destroy(p);
+    return code;
+  };
+  g_last_error[0] = 0;
+
+  // shared-memory budget: activations + misc, the rest is the weight ring
+  const int nqd = s.nq * s.d;
+  const long long A1 = (long long)bcap * std::max(std::max(s.H, nqd), s.F);
+  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 2);
+  const long long Ah = (long long)bcap * s.k * s.F;
+  p->allh = (Ah * 4 <= 64 * 1024) ? 1 : 0;
+  p->act_floats = (int)std::max(std::max(A1, A3), p->allh ? Ah : 0LL);
+  const int C = p->C;
+  const int down_rows_max = (s.H + std::min(s.H, C) - 1) / std::min(s.H, C);
+  const size_t act_bytes = ((size_t)p->act_floats * 4 + 127) / 128 * 128;
+  const size_t misc = ((mk::misc_bytes() + (size_t)bcap * s.k * down_rows_max * 4) + 127) / 128 * 128;
+  const long long avail = (long long)mk::SMEM_LIMIT - (long long)act_bytes - (long long)misc;
+  const int need = std::max(std::max(2 * std::max(std::max(s.H, nqd), s.F), 4 * s.H), 2 * s.ps * s.d * 2);
+  int sb = 32768;
+  if (avail < 4LL * sb) sb = 16384;
+  while (sb < need) sb *= 2;
+  int nst = (int)std::min<long long>(mk::MAX_STAGES, avail / sb);
+  if (nst < 2) return fail(MK_ERR_UNSUPPORTED);
+  p->stage_bytes = sb;
+  p->nstages = nst;
+  p->smem = (int)((size_t)nst * sb + act_bytes + misc);
+  p->P.act_off = nst * sb;
+  p->P.act_floats = p->act_floats;
+  p->P.misc_off = (int)(nst * sb + act_bytes);
+  p->P.allh = p->allh;
+  if (mk::max_active_ctas(p->nb, p->smem) < 1) {
+    snprintf(g_last_error, sizeof(g_last_error), "megakernel does not fit on an SM with %d bytes of shared memory",
+             p->smem);
+    return fail(MK_ERR_CUDA);
+  }
+
+  cudaStream_t st = 0;
+  mk::Params& P = p->P;
+  const size_t L = s.L;
+  // weight pointer tables
+  {
+    std::vector<const void*> tab(9 * L);
+    for (size_t l = 0; l < L; ++l) {
+      tab[0 * L + l] = w->attn_norm[l];
+      tab[1 * L + l] = w->wqkv[l];
+      tab[2 * L + l] = w->wo[l];
+      tab[3 * L + l] = w->ffn_norm[l];
+      tab[4 * L + l] = w->router[l];
+      tab[5 * L + l] = w->w_gate_up[l];
+      tab[6 * L + l] = w->w_down[l];
+      tab[7 * L + l] = kv->k_pool[l];
+      tab[8 * L + l] = kv->v_pool[l];
+    }
+    const void** d_tab = nullptr;
+    if (dalloc(p, &d_tab, tab.size() * sizeof(void*)) != cudaSuccess) return fail(MK_ERR_CUDA);
+    if (cudaMemcpy(d_tab, tab.data(), tab.size() * sizeof(void*), cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(MK_ERR_CUDA);
+    P.attn_norm = (const uint16_t* const*)(d_tab + 0 * L);
+    P.wqkv = (const uint16_t* const*)(d_tab + 1 * L);
+    P.wo = (const uint16_t* const*)(d_tab + 2 * L);
+    P.ffn_norm = (const uint16_t* const*)(d_tab + 3 * L);
+    P.router = (const uint16_t* const*)(d_tab + 4 * L);
+    P.w_gate_up = (const uint16_t* const*)(d_tab + 5 * L);
+    P.w_down = (const uint16_t* const*)(d_tab + 6 * L);
+    P.k_pool = (uint16_t* const*)(d_tab + 7 * L);
+    P.v_pool = (uint16_t* const*)(d_tab + 8 * L);
+    P.embed = (const uint16_t*)w->embed;
+    P.final_norm = (const uint16_t*)w->final_norm;
+    P.lm_head = (const uint16_t*)w->lm_head;
+  }
+  bool ok = true;
+  ok &= dalloc(p, &p->d_ctr, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t)) == cudaSuccess;
+  ok &= dalloc(p, &p->d_status, 4 * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &p->d_seq, (size_t)bcap * sizeof(int)) == cudaSuccess;
+  p->pt_cap = (size_t)bcap * max_pages_per_seq;
+  ok &= dalloc(p, &p->d_pt, p->pt_cap * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &P.qkv, L * bcap * s.qkv_rows * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.o, L * bcap * nqd * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.x_mid, L * bcap * s.H * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.x_out, L * bcap * s.H * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.rlog, L * bcap * s.E * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.ids, L * bcap * s.k * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &P.gates, L * bcap * s.k * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.route, L * p->rm.ints * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &P.hbuf, L * bcap * s.k * s.F * sizeof(float)) == cudaSuccess;
+  const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
+  ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &p->d_io_tok, (size_t)bcap * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &p->d_io_next, (size_t)bcap * sizeof(int)) == cudaSuccess;
+  p->rope_npos = max_pages_per_seq * s.ps;
+  ok &= dalloc(p, &p->d_rope, (size_t)p->rope_npos * (s.d / 2) * sizeof(float2)) == cudaSuccess;
+  if (!ok) return fail(MK_ERR_CUDA);
+  if (cudaEventCreateWithFlags(&p->ev_stage, cudaEventDisableTiming) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaMallocHost(&p->h_status, 4 * sizeof(int)) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaMemsetAsync(P.route, 0, L * p->rm.ints * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (mk::launch_rope_table(p->d_rope, p->rope_npos, s.d, (double)s.theta, st) != cudaSuccess)
+    return fail(MK_ERR_CUDA);
+  if (upload(p, p->d_seq, p->seq.data(), (size_t)batch * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (upload(p, p->d_pt, p->pt.data(), p->pt.size() * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
+  rc = replan(p, st);
+  if (rc != MK_OK) return fail(rc);
+  p->replans = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(MK_ERR_CUDA);
+  fill_params(p);
+  *out = p;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
+  if (!p || !d_tokens || !d_next_token) return MK_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Shape& s = p->s;
+  for (int b = 0; b < p->B; ++b) {
+    const int pos = p->seq[b];
+    if (pos / s.ps >= p->max_pages || pos >= p->rope_npos) return MK_ERR_CAPACITY;
+    const int pg = p->pt[(size_t)b * p->max_pages + pos / s.ps];
+    if (pg < 0 || pg >= p->num_pages) return MK_ERR_CAPACITY;
+  }
+  if (needs_replan(p)) {
+    int rc = replan(p, st);
+    if (rc != MK_OK) return rc;
+  }
+  // keep epoch * count far from 32-bit wrap-around
+  if ((unsigned long long)(p->epoch + 1) * 1024ull * 1024ull > 0x7fffffffull) {
+    if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) !=
+        cudaSuccess)
+      return MK_ERR_CUDA;
+    p->epoch = 0;
+  }
+  p->epoch++;
+  fill_params(p);
+  mk::Params P = p->P;
+  P.epoch = p->epoch;
+  P.tokens = d_tokens;
+  P.logits = d_logits;
+  P.next_token = d_next_token;
+  cudaError_t e = mk::launch_megakernel(P, p->nb, p->C, p->smem, st);
+  if (e != cudaSuccess) return note_cuda(e, "megakernel launch");
+  for (int b = 0; b < p->B; ++b) p->seq[b]++;
+  return MK_OK;
+}
+
+int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
+  if (!p || !h_tokens || !h_next_token) return MK_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t tb = (size_t)p->B * sizeof(int);
+  if (h_logits && !p->d_io_logits) {
+    if (dalloc(p, &p->d_io_logits, (size_t)p->bcap * p->s.V * sizeof(float)) != cudaSuccess) return MK_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(p->d_io_tok, h_tokens, tb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MK_ERR_CUDA;
+  int rc = mk_decode_step(p, p->d_io_tok, h_logits ? p->d_io_logits : nullptr, p->d_io_next, stream);
+  if (rc != MK_OK) return rc;
+  if (cudaMemcpyAsync(h_next_token, p->d_io_next, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (h_logits &&
+      cudaMemcpyAsync(h_logits, p->d_io_logits, (size_t)p->B * p->s.V * sizeof(float), cudaMemcpyDeviceToHost,
+                      st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (cudaMemcpyAsync(p->h_status, p->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+  return p->h_status[0];
+}
+
+int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   mk_stream stream) {
+  if (!p || batch < 1) return MK_ERR_INVALID;
+  if (batch > p->bcap) return MK_ERR_CAPACITY;
+  cudaStream_t st = (cudaStream_t)stream;
+  int rc = validate_batch(p->s, batch, seq_lens, page_table, max_pages_per_seq, p->num_pages);
+  if (rc != MK_OK) return rc;
+  if ((size_t)p->bcap * max_pages_per_seq > p->pt_cap || max_pages_per_seq * p->s.ps > p->rope_npos) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+    dfree(p, p->d_pt);
+    p->d_pt = nullptr;
+    p->pt_cap = (size_t)p->bcap * max_pages_per_seq;
+    if (dalloc(p, &p->d_pt, p->pt_cap * sizeof(int)) != cudaSuccess) return MK_ERR_CUDA;
+    if (max_pages_per_seq * p->s.ps > p->rope_npos) {
+      dfree(p, p->d_rope);
+      p->d_rope = nullptr;
+      p->rope_npos = max_pages_per_seq * p->s.ps;
+      if (dalloc(p, &p->d_rope, (size_t)p->rope_npos * (p->s.d / 2) * sizeof(float2)) != cudaSuccess)
+        return MK_ERR_CUDA;
+      if (mk::launch_rope_table(p->d_rope, p->rope_npos, p->s.d, (double)p->s.theta, st) != cudaSuccess)
+        return MK_ERR_CUDA;
+    }
+  }
+  p->B = batch;
+  p->max_pages = max_pages_per_seq;
+  p->seq.assign(seq_lens, seq_lens + batch);
+  p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
+  if (upload(p, p->d_seq, p->seq.data(), (size_t)batch * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
+  if (upload(p, p->d_pt, p->pt.data(), p->pt.size() * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
+  if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
+  rc = replan(p, st);
+  if (rc != MK_OK) return rc;
+  fill_params(p);
+  return MK_OK;
+}
+
+int mk_plan_sync(mk_plan* p, mk_stream stream) {
+  if (!p) return MK_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(p->h_status, p->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+  return p->h_status[0];
+}
+
+int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream stream) {
+  if (!p || !dst) return MK_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Shape& s = p->s;
+  const size_t B = p->B, bc = p->bcap, L = s.L;
+  size_t row = 0;
+  const uint8_t* src = nullptr;
+  switch (what) {
+    case MK_DBG_HIDDEN: row = s.H * 4; src = (const uint8_t*)p->P.x_out; break;
+    case MK_DBG_EXPERT_IDS: row = s.k * 4; src = (const uint8_t*)p->P.ids; break;
+    case MK_DBG_GATES: row = s.k * 4; src = (const uint8_t*)p->P.gates; break;
+    case MK_DBG_ROUTER_LOGITS: row = s.E * 4; src = (const uint8_t*)p->P.rlog; break;
+    case MK_DBG_SEQ_LENS:
+      if (bytes < B * 4) return MK_ERR_INVALID;
+      return cudaMemcpyAsync(dst, p->d_seq, B * 4, cudaMemcpyDefault, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    case MK_DBG_UNION:
+      if (bytes < L * 4) return MK_ERR_INVALID;
+      return cudaMemcpy2DAsync(dst, 4, p->P.route, (size_t)p->rm.ints * 4, 4, L, cudaMemcpyDefault, st) ==
+                     cudaSuccess
+                 ? MK_OK
+                 : MK_ERR_CUDA;
+    default: return MK_ERR_INVALID;
+  }
+  if (bytes < B * L * row) return MK_ERR_INVALID;
+  // device layout [L][bcap][row] -> caller layout [B][L][row]
+  for (size_t b = 0; b < B; ++b) {
+    if (cudaMemcpy2DAsync((uint8_t*)dst + b * L * row, row, src + b * row, bc * row, row, L, cudaMemcpyDefault,
+                          st) != cudaSuccess)
+      return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
+
+int mk_plan_info(const mk_plan* p, int* out, int n) {
+  if (!p || !out) return MK_ERR_INVALID;
+  const int v[10] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
+                     p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans};
+  for (int i = 0; i < n && i < 10; ++i) out[i] = v[i];
+  return MK_OK;
+}
+
+void mk_plan_destroy(mk_plan* p) {
+  if (!p) return;
+  for (void* v : p->allocs) cudaFree(v);
+  p->allocs.clear();
+  if (p->h_stage) cudaFreeHost(p->h_stage);
+  if (p->h_status) cudaFreeHost(p->h_status);
+  if (p->ev_stage) cudaEventDestroy(p->ev_stage);
+  delete p;
+}
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+"""Thin ctypes binding of libmk.so (include/mk.h): argument marshalling only.
+
+Every step of the decode path runs inside the library's CUDA kernel; this
+module never computes any of it.  It fails loudly when libmk.so is missing
+(build it with ``persistent_moe_decode_02_gb300.build.build()``)."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmk.so")
+
+MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_DEP_TIMEOUT, MK_ERR_CAPACITY, MK_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
+MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ_LENS, MK_DBG_UNION = 1, 2, 3, 4, 5, 6
+
+EXPORTS = [
+    "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
+    "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
+    "mk_last_error",
+]
+
+
+class MkModelDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim",
+                                            "n_experts", "top_k", "expert_ffn", "vocab", "page_size")] + \
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class MkWeights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+                ("attn_norm", _PP), ("wqkv", _PP), ("wo", _PP), ("ffn_norm", _PP), ("router", _PP),
+                ("w_gate_up", _PP), ("w_down", _PP)]
+
+
+class MkKv(ctypes.Structure):
+    _fields_ = [("k_pool", _PP), ("v_pool", _PP), ("num_pages", ctypes.c_int)]
+
+
+class MkPlanOpts(ctypes.Structure):
+    _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int)]
+
+
+class MkError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        detail = lib().mk_last_error().decode()
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})" + (f": {detail}" if detail else ""))
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, p_int = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int)
+        L.mk_plan_create.argtypes = [ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights), ctypes.POINTER(MkKv),
+                                     i32, p_int, p_int, i32, ctypes.POINTER(MkPlanOpts), ctypes.POINTER(vp)]
+        L.mk_decode_step.argtypes = [vp, vp, vp, vp, vp]
+        L.mk_decode_step_host.argtypes = [vp, p_int, ctypes.POINTER(ctypes.c_float), p_int, vp]
+        L.mk_plan_update.argtypes = [vp, i32, p_int, p_int, i32, vp]
+        L.mk_plan_sync.argtypes = [vp, vp]
+        L.mk_plan_read_debug.argtypes = [vp, i32, vp, ctypes.c_size_t, vp]
+        L.mk_plan_info.argtypes = [vp, p_int, i32]
+        L.mk_plan_destroy.argtypes = [vp]
+        L.mk_plan_destroy.restype = None
+        L.mk_status_string.argtypes = [i32]
+        L.mk_status_string.restype = ctypes.c_char_p
+        L.mk_last_error.argtypes = []
+        L.mk_last_error.restype = ctypes.c_char_p
+        L.mk_plan_inspect.argtypes = [ctypes.POINTER(MkModelDims), i32, p_int, i32, i32, p_int, i32, p_int]
+        for f in ("mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
+                  "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().mk_status_string(code).decode()
+
+
+def dims_struct(D) -> MkModelDims:
+    return MkModelDims(D.n_layers, D.hidden, D.n_q_heads, D.n_kv_heads, D.head_dim, D.n_experts, D.top_k,
+                       D.expert_ffn, D.vocab, D.page_size, D.rms_eps, D.rope_theta)
+
+
+def _int_array(vals: Sequence[int]):
+    return (ctypes.c_int * len(vals))(*[int(v) for v in vals])
+
+
+def _ptr_array(tensors):
+    return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def inspect_tasks(D, seq_lens: Sequence[int], num_ctas: int, split_pages: int = 0):
+    """Host-only task list: returns (tasks [n, 12] int tensor, cta_start list)."""
+    dims = dims_struct(D)
+    sl = _int_array(seq_lens)
+    n = lib().mk_plan_inspect(ctypes.byref(dims), len(seq_lens), sl, num_ctas, split_pages, None, 0, None)
+    if n < 0:
+        raise MkError("mk_plan_inspect", n)
+    buf = (ctypes.c_int * (12 * n))()
+    cs = (ctypes.c_int * (num_ctas + 1))()
+    n2 = lib().mk_plan_inspect(ctypes.byref(dims), len(seq_lens), sl, num_ctas, split_pages, buf, n, cs)
+    assert n2 == n
+    return torch.tensor(list(buf), dtype=torch.int64).view(n, 12), list(cs)
+
+
+class Plan:
+    """Owns an mk_plan.  Weight/KV tensors are referenced, not copied.
+
+    weights: dict with 'embed', 'final_norm', 'lm_head' tensors and per-layer
+    lists 'attn_norm', 'wqkv', 'wo', 'ffn_norm', 'router', 'w_gate_up',
+    'w_down' (bf16 CUDA tensors in the layout of include/mk.h).
+    k_pools / v_pools: per-layer bf16 [num_pages, nkv, page_size, d]."""
+
+    def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
+                 max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
+                 split_pages: int = 0, debug_drop_task: int = 0):
+        self.D = D
+        self._keep = (weights, k_pools, v_pools)
+        self._arrays = {k: _ptr_array(weights[k]) for k in
+                        ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down")}
+        self._kp = _ptr_array(k_pools)
+        self._vp = _ptr_array(v_pools)
+        cast = lambda a: ctypes.cast(a, _PP)
+        self._w = MkWeights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
+                            weights["lm_head"].data_ptr(), *[cast(self._arrays[k]) for k in
+                                                             ("attn_norm", "wqkv", "wo", "ffn_norm", "router",
+                                                              "w_gate_up", "w_down")])
+        self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
+        self._dims = dims_struct(D)
+        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task)
+        self.batch = len(seq_lens)
+        pt = [int(x) for x in page_table]
+        h = ctypes.c_void_p()
+        rc = lib().mk_plan_create(ctypes.byref(self._dims), ctypes.byref(self._w), ctypes.byref(self._kv),
+                                  self.batch, _int_array(seq_lens), _int_array(pt), max_pages,
+                                  ctypes.byref(opts), ctypes.byref(h))
+        if rc != MK_OK:
+            raise MkError("mk_plan_create", rc)
+        self.h = h
+
+    def step(self, tokens: torch.Tensor, next_token: torch.Tensor, logits: Optional[torch.Tensor] = None,
+             stream=None) -> int:
+        """Enqueue one decode step (device buffers).  Returns the status code."""
+        return lib().mk_decode_step(self.h, ctypes.c_void_p(tokens.data_ptr()),
+                                    ctypes.c_void_p(logits.data_ptr() if logits is not None else 0),
+                                    ctypes.c_void_p(next_token.data_ptr()), _stream(stream))
+
+    def step_host(self, tokens, next_token, logits=None, stream=None) -> int:
+        """One step with host buffers (int32 / float32 CPU tensors, contiguous)."""
+        tp = ctypes.cast(tokens.data_ptr(), ctypes.POINTER(ctypes.c_int))
+        np_ = ctypes.cast(next_token.data_ptr(), ctypes.POINTER(ctypes.c_int))
+        lp = ctypes.cast(logits.data_ptr(), ctypes.POINTER(ctypes.c_float)) if logits is not None else None
+        return lib().mk_decode_step_host(self.h, tp, lp, np_, _stream(stream))
+
+    def update(self, seq_lens: Sequence[int], page_table, max_pages: int, stream=None) -> None:
+        pt = [int(x) for x in page_table]
+        rc = lib().mk_plan_update(self.h, len(seq_lens), _int_array(seq_lens), _int_array(pt), max_pages,
+                                  _stream(stream))
+        if rc != MK_OK:
+            raise MkError("mk_plan_update", rc)
+        self.batch = len(seq_lens)
+
+    def sync(self, stream=None) -> int:
+        return lib().mk_plan_sync(self.h, _stream(stream))
+
+    def read_debug(self, what: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+        rc = lib().mk_plan_read_debug(self.h, what, ctypes.c_void_p(out.data_ptr()),
+                                      out.numel() * out.element_size(), _stream(stream))
+        if rc != MK_OK:
+            raise MkError("mk_plan_read_debug", rc)
+        return out
+
+    def info(self) -> dict:
+        buf = (ctypes.c_int * 10)()
+        lib().mk_plan_info(self.h, buf, 10)
+        keys = ["num_ctas", "num_tasks", "nstages", "stage_bytes", "smem_bytes", "batch", "attn_tasks",
+                "gu_tasks", "lm_tiles", "replans"]
+        return dict(zip(keys, list(buf)))
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().mk_plan_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

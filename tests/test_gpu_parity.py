@@ -1,0 +1,134 @@
+"""GPU megakernel vs the float64 oracle on the same seeded inputs, through
+the C ABI.  Tolerances and the near-tie protocol are in gpu_util."""
+import dataclasses
+
+import pytest
+import torch
+
+import synth
+from tests.gpu_util import GpuRun, Report, run_and_check, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(built):
+    return built
+
+
+def test_tiny_32_steps_full_protocol():
+    wl = synth.workload("tiny")
+    rep = run_and_check(wl, steps=wl.steps)
+    print(rep)
+    rep.assert_ok()
+    assert rep.steps == 32
+
+
+def test_tiny_ragged_batch_and_small_splits():
+    # three requests with ragged lengths (one ending mid-page, one at a page
+    # boundary), several attention chunks per request (ragged tail chunks)
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 37, 95], steps=6)
+    rep = run_and_check(wl, steps=6, split_pages=2)
+    rep.assert_ok()
+
+
+def test_tiny_single_cta_and_few_ctas():
+    # all tasks on one CTA (pure in-order execution) and on 3 CTAs
+    wl = dataclasses.replace(synth.workload("tiny"), steps=3)
+    for n in (1, 3):
+        rep = run_and_check(wl, steps=3, num_ctas=n)
+        rep.assert_ok()
+
+
+def test_tiny_empty_prior_context():
+    # a request with no cached tokens: attention over the new token alone
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[0, 15, 16], steps=4)
+    rep = run_and_check(wl, steps=4)
+    rep.assert_ok()
+
+
+def test_mid_16_steps():
+    wl = synth.workload("mid")
+    rep = run_and_check(wl, steps=wl.steps)
+    print(rep)
+    rep.assert_ok()
+
+
+def test_paged_permutation_is_bit_identical():
+    # two different physical placements of the same logical cache give the
+    # same bits (the page table is the only thing that differs)
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 70], steps=4)
+    a = GpuRun(wl)
+    ra = [a.step() for _ in range(4)]
+    b = GpuRun(wl, model=a.model, perm_salt=1)
+    assert [r.pages for r in a.reqs] != [r.pages for r in b.reqs]
+    rb = [b.step() for _ in range(4)]
+    for x, y in zip(ra, rb):
+        assert torch.equal(x.next_tok, y.next_tok)
+        assert torch.equal(x.logits, y.logits)
+        assert torch.equal(x.hidden, y.hidden)
+
+
+def test_batch_equals_each_request_alone():
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 50, 77], steps=3)
+    full = GpuRun(wl)
+    rf = [full.step() for _ in range(3)]
+    for b in range(3):
+        run = GpuRun(dataclasses.replace(wl, ctx=[wl.ctx[b]]), model=full.model, rids=[b])
+        r1 = [run.step() for _ in range(3)]
+        for s in range(3):
+            assert int(r1[s].tok_in[0]) == int(rf[s].tok_in[b])
+            assert int(r1[s].next_tok[0]) == int(rf[s].next_tok[b])
+            assert rel_l2(r1[s].logits[0], rf[s].logits[b].double()) < 1e-5
+            assert torch.equal(r1[s].ids[0], rf[s].ids[b])
+
+
+def test_dependency_timeout_is_reported_not_hung():
+    # drop one task so its counter never fires: the bounded waits expire,
+    # the step reports MK_ERR_DEP_TIMEOUT and the context stays usable
+    from persistent_moe_decode_02_gb300 import mk
+    wl = dataclasses.replace(synth.workload("tiny"), steps=2)
+    run = GpuRun(wl, timeout_us=200000, debug_drop_task=1)
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    assert run.plan.step(run.tokens, nxt) == 0
+    assert run.plan.sync() == mk.MK_ERR_DEP_TIMEOUT
+    # later steps do no work and keep reporting the error
+    assert run.plan.step(run.tokens, nxt) == 0
+    assert run.plan.sync() == mk.MK_ERR_DEP_TIMEOUT
+    torch.cuda.synchronize()
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+def test_capacity_error_when_no_page_for_next_position():
+    from persistent_moe_decode_02_gb300 import mk
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[31], steps=1)
+    run = GpuRun(wl, steps=0)   # reserve pages for exactly one more token
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    assert run.plan.step(run.tokens, nxt) == 0        # position 31: page 1 exists
+    assert run.plan.sync() == 0
+    assert run.plan.step(nxt, nxt) == mk.MK_ERR_CAPACITY  # position 32: no page 2
+
+
+@pytest.mark.slow
+def test_full_bs1_8k_two_steps_and_determinism():
+    wl = synth.workload("full_bs1_8k")
+    rep = run_and_check(wl, steps=2, cache_prior=False)
+    print(rep)
+    rep.assert_ok()
+
+
+@pytest.mark.slow
+def test_full_b1_256k_first_layers():
+    wl = synth.workload("full_b1_256k")
+    rep = run_and_check(wl, steps=1, n_layers=2, cache_prior=False)
+    print(rep)
+    rep.assert_ok()
+
+
+@pytest.mark.slow
+def test_full_b8_long_sampled_requests():
+    wl = synth.workload("full_b8_long")
+    rep = run_and_check(wl, steps=1, requests=[0, 2], n_layers=2, cache_prior=False)
+    print(rep)
+    rep.assert_ok()
