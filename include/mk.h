@@ -173,6 +173,34 @@ const char* mk_last_error(void);
 int mk_plan_inspect(const mk_model_dims* dims, int batch, const int* seq_lens, int num_ctas,
                     int split_pages, int* tasks, int max_tasks, int* cta_start);
 
+/* One decode step that allocates no memory, for callers that cannot call
+ * cudaMalloc where they decode: hosts that reserve all device memory in their
+ * own pool and forbid raw allocations inside their enqueue callbacks, custom
+ * allocator hooks that would recurse, and latency-critical loops that cannot
+ * take the device-wide synchronisation cudaMalloc/cudaFree may cause.  The
+ * pages have no counterpart to this call; it is a deployment convenience.
+ *
+ * Same step as mk_plan_create + mk_decode_step, with no plan: request b
+ * decodes d_tokens[b] at position seq_lens[b] (host array; the cache holds
+ * seq_lens[b] tokens), writes its K/V there, the greedy next token to
+ * d_next_token[b] and, when non-NULL, logits to d_logits [batch, vocab] and
+ * the device status (code, task, cta, info) to d_status (device int32[4]).
+ * The caller advances seq_lens itself.  Arguments as in mk_plan_create.
+ *
+ * Scratch lives in one file-scope device array of MK_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that every GPU loading libmk.so holds until the process exits;
+ * the task list is staged in a 4 MiB file-scope host array.  A step needing
+ * more returns MK_ERR_CAPACITY (mk_last_error() says how much it needed).
+ * All calls share both arrays, so calls whose GPU work overlaps, or that run
+ * concurrently on several host threads, race: serialise them.  The first call
+ * on a device resolves the array's device address (cudaGetSymbolAddress with
+ * that device current); make it before any stream capture. */
+#define MK_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
+                           const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                           const int* d_tokens, float* d_logits, int* d_next_token, int* d_status,
+                           mk_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -254,6 +254,10 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
 
 }  // namespace
 
+namespace mk {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace mk
+
 // ------------------------------------------------------------------ the plan
 
 struct mk_plan {

@@ -20,7 +20,7 @@ MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
     "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
-    "mk_last_error",
+    "mk_last_error", "mk_decode_step_noalloc",
 ]
 
 
@@ -81,8 +81,10 @@ def lib():
         L.mk_last_error.argtypes = []
         L.mk_last_error.restype = ctypes.c_char_p
         L.mk_plan_inspect.argtypes = [ctypes.POINTER(MkModelDims), i32, p_int, i32, i32, p_int, i32, p_int]
+        L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights),
+                                             ctypes.POINTER(MkKv), i32, p_int, p_int, i32, vp, vp, vp, vp, vp]
         for f in ("mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
-                  "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect"):
+                  "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -122,6 +124,36 @@ def inspect_tasks(D, seq_lens: Sequence[int], num_ctas: int, split_pages: int = 
     n2 = lib().mk_plan_inspect(ctypes.byref(dims), len(seq_lens), sl, num_ctas, split_pages, buf, n, cs)
     assert n2 == n
     return torch.tensor(list(buf), dtype=torch.int64).view(n, 12), list(cs)
+
+
+def _weight_structs(D, weights: dict, k_pools, v_pools):
+    """ctypes views of the weight and KV pointers (the arrays must outlive the call)."""
+    arrays = {k: _ptr_array(weights[k]) for k in
+              ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down")}
+    kp, vp = _ptr_array(k_pools), _ptr_array(v_pools)
+    cast = lambda a: ctypes.cast(a, _PP)
+    w = MkWeights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr(),
+                  *[cast(arrays[k]) for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up",
+                                              "w_down")])
+    kv = MkKv(cast(kp), cast(vp), int(k_pools[0].shape[0]))
+    return w, kv, (arrays, kp, vp)
+
+
+def decode_step_noalloc(D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table, max_pages: int,
+                        tokens: torch.Tensor, next_token: torch.Tensor, logits: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> int:
+    """One step through mk_decode_step_noalloc (no plan, no allocation inside
+    the library).  Returns the enqueue status; the device status goes to
+    `status` (int32[4] on the device) when given."""
+    w, kv, keep = _weight_structs(D, weights, k_pools, v_pools)
+    dims = dims_struct(D)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+    pt = [int(x) for x in page_table]
+    rc = lib().mk_decode_step_noalloc(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(kv), len(seq_lens),
+                                      _int_array(seq_lens), _int_array(pt), max_pages, ptr(tokens), ptr(logits),
+                                      ptr(next_token), ptr(status), _stream(stream))
+    del keep
+    return rc
 
 
 class Plan:
