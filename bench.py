@@ -305,6 +305,83 @@ def our_arm(args, wl):
         dist.destroy_process_group()
 
 
+PHASES = ["QKV", "ATTN", "OPROJ", "ROUTER", "GATE_UP", "DOWN", "LM"]
+
+
+def summarize_timeline(tasks, stamps, step_ms) -> str:
+    """Text summary of one traced step: per task kind the mean time spent
+    waiting for the dependency, loading activations, consuming stages and
+    finishing; the producer's lead; and the per-layer phase windows."""
+    import statistics as st
+
+    import torch
+    S = stamps.double()
+    t0 = S[S > 0].min()
+    S = torch.where(S > 0, (S - t0) / 1000.0, torch.zeros_like(S))   # microseconds
+    typ, lay = tasks[:, 0], tasks[:, 1]
+    out = [f"traced step ms: {', '.join(f'{x:.3f}' for x in step_ms)}; span of last step {float(S.max()):.1f} us"]
+    seg = [("wait", 0, 1), ("act", 1, 2), ("stages", 2, 3), ("tail", 3, 4), ("prod_lead", 5, 1),
+           ("prod_issue", 5, 6)]
+    out.append("kind      n      " + "  ".join(f"{n:>10s}" for n, _, _ in seg) + "   (us, mean per task)")
+    for k, name in enumerate(PHASES):
+        m = typ == k
+        if int(m.sum()) == 0:
+            continue
+        vals = [float((S[m, b] - S[m, a]).mean()) for _, a, b in seg]
+        out.append(f"{name:8s} {int(m.sum()):6d} " + "  ".join(f"{v:10.2f}" for v in vals))
+    L = int(lay.max()) + 1
+    ends = [float(S[(typ == 5) & (lay == l), 4].max()) for l in range(L)]
+    dl = [b - a for a, b in zip(ends, ends[1:])] or [ends[0]]
+    out.append(f"per-layer time us: median {st.median(dl):.2f} min {min(dl):.2f} max {max(dl):.2f}")
+    l = L // 2
+    out.append(f"layer {l} phase windows (us): dependency met first..last | done last | producer first copy")
+    for k in range(6):
+        m = (typ == k) & (lay == l)
+        if int(m.sum()) == 0:
+            continue
+        out.append(f"  {PHASES[k]:8s} dep {float(S[m, 1].min()):9.1f}..{float(S[m, 1].max()):9.1f} | done "
+                   f"{float(S[m, 4].max()):9.1f} | prod {float(S[m, 5].min()):9.1f}..{float(S[m, 5].max()):9.1f}")
+    m = typ == 6
+    out.append(f"LM head: start {float(S[m, 1].min()):.1f} end {float(S[m, 4].max()):.1f}")
+    return "\n".join(out)
+
+
+def timeline_arm(args, wl):
+    """Trace a few steps (globaltimer stamps per task) and print the summary."""
+    import torch
+
+    from persistent_moe_decode_02_gb300 import mk
+    from synth.device import DeviceModel, PagedKV, initial_tokens, kv_pages_needed
+    D = wl.dims
+    model = DeviceModel(D, wl.seed)
+    steps = args.steps
+    ps = D.page_size
+    max_pages = max((c + steps + 2 + ps) // ps for c in wl.ctx) + 1
+    kv = PagedKV(D, kv_pages_needed(D, wl.ctx, steps + 2) + 4, max_pages, wl.seed)
+    reqs = [kv.admit(i, c, steps + 2) for i, c in enumerate(wl.ctx)]
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
+                   trace=True)
+    tok = torch.tensor(initial_tokens(wl, list(range(wl.batch))), dtype=torch.int32, device="cuda")
+    times = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        rc = plan.step(tok, tok)
+        e1.record()
+        torch.cuda.synchronize()
+        assert rc == 0 and plan.sync() == 0
+        times.append(e0.elapsed_time(e1))
+    tasks, stamps = plan.timeline()
+    text = summarize_timeline(tasks, stamps, times)
+    head = f"workload {wl.name}: {wl.dims}; batch {wl.batch}; plan {plan.info()}; kernel {kernel_hash()}"
+    print(head + "\n" + text, flush=True)
+    if args.timeline != "-":
+        with open(args.timeline, "w") as f:
+            f.write(head + "\n" + text + "\n")
+        torch.save({"tasks": tasks, "stamps": stamps, "times": times}, args.timeline + ".pt")
+    plan.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -313,11 +390,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", default=None,
+                    help="trace --steps steps per task and write a summary to this path ('-': print only)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     import synth
     wl = synth.workload(args.workload)
-    if args.impl == "reference":
+    if args.timeline:
+        import __graft_entry__
+        __graft_entry__.build()
+        timeline_arm(args, wl)
+    elif args.impl == "reference":
         reference_arm(args, wl)
     else:
         import __graft_entry__

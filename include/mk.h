@@ -97,6 +97,7 @@ typedef struct mk_plan_opts {
   int debug_drop_task; /* test hook: >0 removes task (value-1) from the list so its
                           counter never fires and the step returns MK_ERR_DEP_TIMEOUT;
                           0 in production */
+  int trace;         /* 1: record a per-task timeline every step (MK_DBG_TRACE) */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;
@@ -147,9 +148,15 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  *   MK_DBG_GATES         fp32 [batch, n_layers, top_k]
  *   MK_DBG_ROUTER_LOGITS fp32 [batch, n_layers, n_experts]
  *   MK_DBG_SEQ_LENS      int32 [batch]                   device lengths
- *   MK_DBG_UNION         int32 [n_layers]                distinct experts per layer */
+ *   MK_DBG_UNION         int32 [n_layers]                distinct experts per layer
+ *   MK_DBG_TASKS         int32 [num_tasks, 12]           the task list in CTA order
+ *                        (type, layer, a0..a7, wait counter, wait count)
+ *   MK_DBG_TRACE         uint64 [num_tasks, 8]           globaltimer stamps (ns) per task:
+ *                        consumer fetched, dependency met, activations ready, stages
+ *                        consumed, done; producer first copy, last copy, start
+ *                        (needs opts.trace) */
 enum { MK_DBG_HIDDEN = 1, MK_DBG_EXPERT_IDS = 2, MK_DBG_GATES = 3, MK_DBG_ROUTER_LOGITS = 4,
-       MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6 };
+       MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6, MK_DBG_TASKS = 7, MK_DBG_TRACE = 8 };
 int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stream stream);
 
 /* Describe the current plan (host-side numbers): writes up to `n` ints:

@@ -279,6 +279,12 @@ struct Producer {
   const Params& p;
   Ring r;
   uint64_t pol;
+  int ti = 0;
+  bool first = true;
+
+  __device__ void mark(int k) {
+    if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
+  }
 
   // Claim the next stage (waiting for its release) and arm it for `bytes`.
   __device__ bool open(uint32_t bytes, uint8_t*& dst, uint64_t*& bar) {
@@ -288,6 +294,10 @@ struct Producer {
     dst = r.base + (size_t)r.stage * r.sb;
     m->armed[r.stage] = r.round;
     mbar_expect_tx(bar, bytes);
+    if (first) {
+      mark(TR_P_FIRST);
+      first = false;
+    }
     return true;
   }
 
@@ -385,11 +395,13 @@ struct Producer {
   }
 
   __device__ void run(int t0, int t1) {
-    for (int ti = t0; ti < t1; ++ti) {
+    for (ti = t0; ti < t1; ++ti) {
       if (failed(p)) return;
       const Task t = p.tasks[ti];
       const int l = t.layer;
       bool ok = true;
+      first = true;
+      mark(TR_P_START);
       switch (t.type) {
         case T_QKV: ok = rows(p.wqkv[l], p.H, t.a[0], t.a[1]); break;
         case T_ATTN: ok = attn(t); break;
@@ -404,6 +416,7 @@ struct Producer {
         r.m->abort_flag = 1;
         return;
       }
+      mark(TR_P_LAST);
     }
   }
 };
@@ -418,6 +431,11 @@ struct Consumer {
   Misc* m;
   float* ydown;
   int ct, cw, lane;
+  int ti = 0;
+
+  __device__ void mark(int k) {
+    if (p.trace && ct == 0) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
+  }
 
   // ---- ring access (per warp)
   __device__ const uint8_t* wait_stage(bool& ab) {
@@ -508,6 +526,7 @@ struct Consumer {
   __device__ bool rows(int K, int r0, int r1, const float* a, int stride, const int* map, int nb,
                        bool ab, Epi epi) {
     const int rps = rows_per_stage(p, K);
+    mark(TR_ACT);
     for (int s0 = r0; s0 < r1; s0 += rps) {
       const int n = min(rps, r1 - s0);
       const uint8_t* st = wait_stage(ab);
@@ -520,6 +539,7 @@ struct Consumer {
       }
       release_stage(ab);
     }
+    mark(TR_STAGES);
     return ab;
   }
 
@@ -701,6 +721,7 @@ struct Consumer {
     gu_range(p, t, U, q0, q1);
     const int pps = pairs_per_stage(p);
     float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
+    mark(TR_ACT);
     for (long long q = q0; q < q1;) {
       const int u = (int)(q / F);
       const int fa = (int)(q - (long long)u * F);
@@ -728,6 +749,7 @@ struct Consumer {
       }
       q = (long long)(u + 1) * F;
     }
+    mark(TR_STAGES);
     ab = finish(ab);
     if (!ab) signal(p.cm.gu + l);
     return ab;
@@ -744,6 +766,7 @@ struct Consumer {
     const int* rt = route_of(p, l);
     const int U = __ldcg(rt);
     const int rps = rows_per_stage(p, F);
+    mark(TR_ACT);
     for (int u = 0; u < U; ++u) {
       const int nt = load_segment(rt, u);
       int* map = m->seg_rank;  // reused below as the act row map
@@ -779,6 +802,7 @@ struct Consumer {
         release_stage(ab);
       }
     }
+    mark(TR_STAGES);
     cbar();
     if (!ab) {
       const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
@@ -855,6 +879,7 @@ struct Consumer {
     const int ppg = pages_per_stage(p);
     const int PB = ps * d * 2;
     const int tps = ppg * ps;
+    mark(TR_ACT);
     for (int ts = tok0; ts < tok1; ts += tps) {
       const int nt = min(tps, tok1 - ts);
       const uint8_t* st = wait_stage(ab);
@@ -944,6 +969,7 @@ struct Consumer {
       }
       release_stage(ab);
     }
+    mark(TR_STAGES);
     // merge the 8 warps' partial softmax states of this chunk
     const int RS = d + 2;
     if (!ab) {
@@ -1074,13 +1100,14 @@ struct Consumer {
   }
 
   __device__ void run(int t0, int t1) {
-    for (int ti = t0; ti < t1; ++ti) {
+    for (ti = t0; ti < t1; ++ti) {
       const Task t = p.tasks[ti];
       bool ab = false;
+      mark(TR_FETCH);
       if (ct == 0) ab = !wait_ctr(p, t.wait_ctr, t.wait_cnt, ti);
       ab = cbar_or(ab);
       if (ab) break;
-      if (ct == 0) __threadfence();
+      mark(TR_DEP);
       switch (t.type) {
         case T_QKV: ab = qkv(t, ab); break;
         case T_ATTN: ab = attn(t, ab); break;
@@ -1092,8 +1119,8 @@ struct Consumer {
         default: ab = true;
       }
       if (ab) break;
+      mark(TR_DONE);
     }
-    if (ct == 0) m->abort_flag = m->abort_flag;  // keep the flag for the drain
   }
 };
 

@@ -262,7 +262,7 @@ void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_erro
 
 struct mk_plan {
   Shape s;
-  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0;
+  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0;
   int max_pages = 0, num_pages = 0, rope_npos = 0;
   int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0, allh = 0;
   int replans = 0;
@@ -288,6 +288,8 @@ struct mk_plan {
   float2* d_rope = nullptr;
   float* d_part = nullptr;
   size_t part_cap_slots = 0;
+  unsigned long long* d_trace = nullptr;
+  size_t trace_cap = 0;
   int* d_io_tok = nullptr;
   int* d_io_next = nullptr;
   float* d_io_logits = nullptr;
@@ -385,6 +387,17 @@ int replan(mk_plan* p, cudaStream_t st) {
     if ((e = dalloc(p, (uint8_t**)&p->d_tasks, cap)) != cudaSuccess) return MK_ERR_CUDA;
     p->tasks_cap = cap;
   }
+  if (p->trace && tasks.size() > p->trace_cap) {
+    if (p->d_trace) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+      dfree(p, p->d_trace);
+      p->d_trace = nullptr;
+    }
+    const size_t cap = tasks.size() + tasks.size() / 2 + 64;
+    if (dalloc(p, &p->d_trace, cap * mk::TRACE_SLOTS * sizeof(unsigned long long)) != cudaSuccess)
+      return MK_ERR_CUDA;
+    p->trace_cap = cap;
+  }
   if ((size_t)cnt.part_slots > p->part_cap_slots) {
     // grow the attention partial buffer (rare: only when a replan adds chunks)
     if (p->d_part) {
@@ -435,6 +448,7 @@ void fill_params(mk_plan* p) {
   P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
+  P.trace = p->trace ? p->d_trace : nullptr;
 }
 
 }  // namespace
@@ -520,6 +534,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   p->C = o.num_ctas > 0 ? std::min(o.num_ctas, sms) : sms;
   p->split_opt = o.split_pages;
   p->drop_task = o.debug_drop_task;
+  p->trace = o.trace ? 1 : 0;
   p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
   p->max_pages = max_pages_per_seq;
   p->num_pages = kv->num_pages;
@@ -756,6 +771,26 @@ int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream 
     case MK_DBG_SEQ_LENS:
       if (bytes < B * 4) return MK_ERR_INVALID;
       return cudaMemcpyAsync(dst, p->d_seq, B * 4, cudaMemcpyDefault, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    case MK_DBG_TASKS: {
+      const size_t n = p->tasks.size();
+      if (bytes < n * 12 * 4) return MK_ERR_INVALID;
+      if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+      std::vector<int> v(n * 12);
+      for (size_t i = 0; i < n; ++i) {
+        const Task& t = p->tasks[i];
+        v[i * 12 + 0] = t.type;
+        v[i * 12 + 1] = t.layer;
+        for (int j = 0; j < 8; ++j) v[i * 12 + 2 + j] = t.a[j];
+        v[i * 12 + 10] = t.wait_ctr;
+        v[i * 12 + 11] = (int)t.wait_cnt;
+      }
+      return cudaMemcpy(dst, v.data(), n * 12 * 4, cudaMemcpyDefault) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
+    case MK_DBG_TRACE: {
+      const size_t n = p->tasks.size() * mk::TRACE_SLOTS * sizeof(unsigned long long);
+      if (!p->trace || !p->d_trace || bytes < n) return MK_ERR_INVALID;
+      return cudaMemcpyAsync(dst, p->d_trace, n, cudaMemcpyDefault, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
     case MK_DBG_UNION:
       if (bytes < L * 4) return MK_ERR_INVALID;
       return cudaMemcpy2DAsync(dst, 4, p->P.route, (size_t)p->rm.ints * 4, 4, L, cudaMemcpyDefault, st) ==

@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libmk.so")
 
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_DEP_TIMEOUT, MK_ERR_CAPACITY, MK_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ_LENS, MK_DBG_UNION = 1, 2, 3, 4, 5, 6
+MK_DBG_TASKS, MK_DBG_TRACE = 7, 8
+TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start"]
 
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
@@ -45,7 +47,7 @@ class MkKv(ctypes.Structure):
 
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
-                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int)]
+                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int)]
 
 
 class MkError(RuntimeError):
@@ -166,7 +168,7 @@ class Plan:
 
     def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
                  max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
-                 split_pages: int = 0, debug_drop_task: int = 0):
+                 split_pages: int = 0, debug_drop_task: int = 0, trace: bool = False):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._arrays = {k: _ptr_array(weights[k]) for k in
@@ -180,7 +182,7 @@ class Plan:
                                                               "w_gate_up", "w_down")])
         self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
         self._dims = dims_struct(D)
-        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task)
+        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace))
         self.batch = len(seq_lens)
         pt = [int(x) for x in page_table]
         h = ctypes.c_void_p()
@@ -222,6 +224,16 @@ class Plan:
         if rc != MK_OK:
             raise MkError("mk_plan_read_debug", rc)
         return out
+
+    def timeline(self, stream=None):
+        """(tasks int32 [n, 12], stamps int64 [n, 8]) of the last step (needs trace=True)."""
+        n = self.info()["num_tasks"]
+        tasks = torch.empty(n, 12, dtype=torch.int32)
+        self.read_debug(MK_DBG_TASKS, tasks, stream)
+        stamps = torch.empty(n, 8, dtype=torch.int64)
+        self.read_debug(MK_DBG_TRACE, stamps, stream)
+        self.sync(stream)
+        return tasks, stamps
 
     def info(self) -> dict:
         buf = (ctypes.c_int * 10)()
