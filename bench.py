@@ -321,7 +321,7 @@ def summarize_timeline(tasks, stamps, step_ms) -> str:
     typ, lay = tasks[:, 0], tasks[:, 1]
     out = [f"traced step ms: {', '.join(f'{x:.3f}' for x in step_ms)}; span of last step {float(S.max()):.1f} us"]
     seg = [("wait", 0, 1), ("act", 1, 2), ("stages", 2, 3), ("tail", 3, 4), ("prod_lead", 5, 1),
-           ("prod_issue", 5, 6)]
+           ("prod_issue", 5, 6), ("act>stage0", 2, 8), ("stage0>last", 8, 9), ("last>done", 9, 3)]
     out.append("kind      n      " + "  ".join(f"{n:>10s}" for n, _, _ in seg) + "   (us, mean per task)")
     for k, name in enumerate(PHASES):
         m = typ == k

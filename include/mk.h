@@ -62,7 +62,8 @@ typedef struct mk_model_dims {
  *               (G*head_dim rows), then key head g, then value head g
  *   wo[l]       [hidden, n_q_heads * head_dim]
  *   router[l]   [n_experts, hidden]
- *   w_gate_up[l][n_experts, 2*expert_ffn, hidden]: gate rows, then up rows
+ *   w_gate_up[l][n_experts, 2*expert_ffn, hidden]: rows interleaved per ffn
+ *               unit f: row 2f = gate row f, row 2f+1 = up row f
  *   w_down[l]   [n_experts, hidden, expert_ffn]
  * Every pointer must be 16-byte aligned. */
 typedef struct mk_weights {
@@ -151,10 +152,10 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  *   MK_DBG_UNION         int32 [n_layers]                distinct experts per layer
  *   MK_DBG_TASKS         int32 [num_tasks, 12]           the task list in CTA order
  *                        (type, layer, a0..a7, wait counter, wait count)
- *   MK_DBG_TRACE         uint64 [num_tasks, 8]           globaltimer stamps (ns) per task:
+ *   MK_DBG_TRACE         uint64 [num_tasks, 10]          globaltimer stamps (ns) per task:
  *                        consumer fetched, dependency met, activations ready, stages
- *                        consumed, done; producer first copy, last copy, start
- *                        (needs opts.trace) */
+ *                        consumed, done; producer first copy, last copy, start;
+ *                        first and last stage landed (needs opts.trace) */
 enum { MK_DBG_HIDDEN = 1, MK_DBG_EXPERT_IDS = 2, MK_DBG_GATES = 3, MK_DBG_ROUTER_LOGITS = 4,
        MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6, MK_DBG_TASKS = 7, MK_DBG_TRACE = 8 };
 int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stream stream);

@@ -99,6 +99,45 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   return old;
 }
 
+// Explicit shared-memory loads (32-bit shared addresses), so the hot loops
+// never go through generic addressing.  Volatile keeps them behind the
+// mbarrier waits that publish the data.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Task records are read-only during a step: read them through the L1.
+__device__ __forceinline__ Task ldg_task(const Task* t) {
+  const int4* q = reinterpret_cast<const int4*>(t);
+  const int4 a = __ldg(q), b = __ldg(q + 1), c = __ldg(q + 2);
+  Task r;
+  r.type = a.x; r.layer = a.y; r.a[0] = a.z; r.a[1] = a.w;
+  r.a[2] = b.x; r.a[3] = b.y; r.a[4] = b.z; r.a[5] = b.w;
+  r.a[6] = c.x; r.a[7] = c.y; r.wait_ctr = c.z; r.wait_cnt = (uint32_t)c.w;
+  return r;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -159,6 +198,9 @@ __device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
 
 // ------------------------------------------------------------------ shared state
 
+constexpr int WIN_ROWS = 32;                     // rows per cross-warp partial-sum window
+constexpr int MAX_UNION = MAX_BATCH * MAX_TOPK;   // distinct experts a step can select
+
 struct Misc {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
@@ -170,11 +212,17 @@ struct Misc {
   float red[NCW * MAX_BATCH];
   float best_v[NCW * MAX_BATCH];
   int best_i[NCW * MAX_BATCH];
-  int seg_tok[MAX_BATCH];
-  int seg_rank[MAX_BATCH];
   int sel[MAX_BATCH * MAX_TOPK];
   int slot_of[MAX_EXPERTS];
   int cnt_of[MAX_EXPERTS];
+  // routing of the current layer, cached per task
+  int r_exp[MAX_UNION];
+  int r_cnt[MAX_UNION];
+  int r_tok[MAX_UNION * MAX_BATCH];
+  int r_rank[MAX_UNION * MAX_BATCH];
+  int r_row[MAX_UNION * MAX_BATCH];   // act row of (slot, i) in the down task
+  // per-warp partial sums of wide-row GEMVs, two windows of WIN_ROWS rows
+  float psum[2][NCW * WIN_ROWS * MAX_BATCH];
 };
 
 struct Ring {
@@ -355,15 +403,14 @@ struct Producer {
       const int fa = (int)(q - (long long)u * F);
       const int fb = (int)min((long long)F, q1 - (long long)u * F);
       const int e = __ldcg(rt + 1 + u);
-      const uint16_t* We = W + (size_t)e * 2 * F * H;
+      const uint16_t* We = W + (size_t)e * 2 * F * H;   // rows 2f (gate f), 2f + 1 (up f)
       for (int f = fa; f < fb; f += pps) {
         const int n = min(pps, fb - f);
-        const uint32_t half = (uint32_t)n * H * 2;
+        const uint32_t bytes = (uint32_t)n * 2 * H * 2;
         uint8_t* dst;
         uint64_t* bar;
-        if (!open(2 * half, dst, bar)) return false;
-        bulk_g2s(dst, We + (size_t)f * H, half, bar, pol);
-        bulk_g2s(dst + half, We + (size_t)(F + f) * H, half, bar, pol);
+        if (!open(bytes, dst, bar)) return false;
+        bulk_g2s(dst, We + (size_t)2 * f * H, bytes, bar, pol);
         r.advance();
       }
       q = (long long)(u + 1) * F;
@@ -438,12 +485,18 @@ struct Consumer {
   }
 
   // ---- ring access (per warp)
+  int nstage_seen = 0;   // stages of the current task seen by this warp (timeline only)
+
   __device__ const uint8_t* wait_stage(bool& ab) {
     if (ab) return nullptr;
     if (!mbar_wait(p, m, &m->full[r.stage], r.round & 1, -4)) {
       ab = true;
       m->abort_flag = 1;
       return nullptr;
+    }
+    if (p.trace) {
+      mark(nstage_seen == 0 ? TR_S_FIRST : TR_S_LAST);
+      ++nstage_seen;
     }
     return r.base + (size_t)r.stage * r.sb;
   }
@@ -454,16 +507,19 @@ struct Consumer {
   }
 
   // ---- activations
-  // act[b * H + i] = x_b[i] / sqrt(mean(x_b^2) + eps) * gamma[i], b < B.
-  template <class Src>
-  __device__ void fill_rmsnorm(const uint16_t* gamma, Src src) {
-    const int H = p.H, B = p.B;
+  // act[b * H + i] = x_b[i] / sqrt(mean(x_b^2) + eps) * gamma[i] for b < B, with
+  // x_b read four floats at a time by src(b, i4).
+  template <class Src4>
+  __device__ void fill_rmsnorm(const uint16_t* gamma, Src4 src) {
+    const int H = p.H, H4 = H >> 2, B = p.B;
     for (int b = 0; b < B; ++b) {
       float ss = 0.f;
-      for (int i = ct; i < H; i += NCT) {
-        const float v = src(b, i);
-        act[b * H + i] = v;
-        ss = fmaf(v, v, ss);
+      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
+#pragma unroll 4
+      for (int i = ct; i < H4; i += NCT) {
+        const float4 v = src(b, i);
+        dst[i] = v;
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
       }
       ss = warp_sum(ss);
       if (lane == 0) m->red[b * NCW + cw] = ss;
@@ -474,72 +530,192 @@ struct Consumer {
 #pragma unroll
       for (int w = 0; w < NCW; ++w) tot += m->red[b * NCW + w];
       const float inv = 1.0f / sqrtf(tot / (float)H + p.eps);
-      for (int i = ct; i < H; i += NCT) act[b * H + i] = act[b * H + i] * inv * bf2f(gamma[i]);
+      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
+#pragma unroll 4
+      for (int i = ct; i < H4; i += NCT) {
+        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
+        float4 v = dst[i];
+        v.x = v.x * inv * bf_lo(gb.x);
+        v.y = v.y * inv * bf_hi(gb.x);
+        v.z = v.z * inv * bf_lo(gb.y);
+        v.w = v.w * inv * bf_hi(gb.y);
+        dst[i] = v;
+      }
     }
+  }
+
+  __device__ float4 x_in4(int l, int b, int i4) const {
+    if (l == 0) {
+      const int tok = __ldcg(p.tokens + b);
+      const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.embed + (size_t)tok * p.H) + i4);
+      return make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+    }
+    return __ldcg(reinterpret_cast<const float4*>(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H) + i4);
   }
 
   __device__ float x_in(int l, int b, int i) const {
-    if (l == 0) {
-      const int tok = __ldcg(p.tokens + b);
-      return bf2f(p.embed[(size_t)tok * p.H + i]);
-    }
+    if (l == 0) return bf2f(p.embed[(size_t)__ldcg(p.tokens + b) * p.H + i]);
     return __ldcg(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H + i);
   }
 
-  // ---- dot products of one bf16 row (K elements, smem) with nb activation rows
-  // act + map(j) * stride, j < nb; full sums returned in every lane.
-  __device__ __forceinline__ void row_dot(const uint8_t* wrow, int K, const float* a, int stride,
-                                          const int* map, int nb, float (&out)[NB]) const {
-    float acc0[NB], acc1[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j) acc0[j] = acc1[j] = 0.f;
-    const uint4* w4 = reinterpret_cast<const uint4*>(wrow);
-    const int ng = K >> 3;
-#pragma unroll 2
-    for (int gi = lane; gi < ng; gi += 32) {
-      const uint4 wv = w4[gi];
-      const float w0 = bf_lo(wv.x), w1 = bf_hi(wv.x), w2 = bf_lo(wv.y), w3 = bf_hi(wv.y);
-      const float w5 = bf_hi(wv.z), w4f = bf_lo(wv.z), w6 = bf_lo(wv.w), w7 = bf_hi(wv.w);
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        if (j < nb) {
-          const int row = map ? map[j] : j;
-          const float4* av = reinterpret_cast<const float4*>(a + (size_t)row * stride + gi * 8);
-          const float4 x0 = av[0], x1 = av[1];
-          acc0[j] = fmaf(w0, x0.x, acc0[j]);
-          acc1[j] = fmaf(w1, x0.y, acc1[j]);
-          acc0[j] = fmaf(w2, x0.z, acc0[j]);
-          acc1[j] = fmaf(w3, x0.w, acc1[j]);
-          acc0[j] = fmaf(w4f, x1.x, acc0[j]);
-          acc1[j] = fmaf(w5, x1.y, acc1[j]);
-          acc0[j] = fmaf(w6, x1.z, acc0[j]);
-          acc1[j] = fmaf(w7, x1.w, acc1[j]);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) out[j] = warp_sum(acc0[j] + acc1[j]);
+  // dot of one 16-byte bf16 granule with 8 activations
+  __device__ __forceinline__ static float dot8(const uint4 wv, uint32_t a) {
+    const float4 x0 = lds128f(a);
+    const float4 x1 = lds128f(a + 16);
+    float s0 = bf_lo(wv.x) * x0.x;
+    float s1 = bf_hi(wv.x) * x0.y;
+    s0 = fmaf(bf_lo(wv.y), x0.z, s0);
+    s1 = fmaf(bf_hi(wv.y), x0.w, s1);
+    s0 = fmaf(bf_lo(wv.z), x1.x, s0);
+    s1 = fmaf(bf_hi(wv.z), x1.y, s1);
+    s0 = fmaf(bf_lo(wv.w), x1.z, s0);
+    s1 = fmaf(bf_hi(wv.w), x1.w, s1);
+    return s0 + s1;
   }
 
-  // Consume the stages of rows [r0, r1) of a K-wide matrix; epi(row, sums).
-  template <class Epi>
-  __device__ bool rows(int K, int r0, int r1, const float* a, int stride, const int* map, int nb,
-                       bool ab, Epi epi) {
-    const int rps = rows_per_stage(p, K);
-    mark(TR_ACT);
-    for (int s0 = r0; s0 < r1; s0 += rps) {
-      const int n = min(rps, r1 - s0);
-      const uint8_t* st = wait_stage(ab);
-      if (st) {
-        for (int rr = cw; rr < n; rr += NCW) {
-          float out[NB];
-          row_dot(st + (size_t)rr * K * 2, K, a, stride, map, nb, out);
-          epi(s0 + rr, out);
+  // ---- GEMV over rows [r0, r1) of a K-wide bf16 matrix streamed through the
+  // ring, against nb activation rows (act row map[j], or j when map is null).
+  //
+  // Wide rows (K a multiple of 2048, the model's hidden and attention widths):
+  // warp w owns the 256-column slices w, w+8, ...; per stage it accumulates up
+  // to 8 rows at once (independent chains), reduces them across its lanes and
+  // parks one partial per (warp, row) in a 32-row smem window.  When a window
+  // fills (or the range ends) the consumer threads sum the 8 warp partials in
+  // warp order -- the same order every run -- and call the epilogue.
+  // Narrow rows (other K): warp w owns rows w, w+8, ..., up to 8 at a time,
+  // its lanes span the whole row, and it calls the epilogue itself.
+  //
+  // PAIRS: rows come as (gate, up) pairs 2f, 2f+1 and the epilogue is
+  // epi(f, j, gate_sum, up_sum); otherwise epi(row, j, sum).
+  template <bool PAIRS, class Epi>
+  __device__ bool gemv(int K, int r0, int r1, const float* a, int stride, const int* map, int nb, bool ab,
+                       Epi epi) {
+    const int rps = PAIRS ? 2 * pairs_per_stage(p) : rows_per_stage(p, K);
+    const int ng = K >> 3;
+    const uint32_t rowb = (uint32_t)K * 2;
+    uint32_t aoff[NB];  // shared address of each activation row
+#pragma unroll
+    for (int j = 0; j < NB; ++j) aoff[j] = smem_u32(a) + (uint32_t)((j < nb ? (map ? map[j] : j) : 0) * stride * 4);
+    if ((K & 2047) == 0) {
+      const int spw = K >> 11;  // granules per lane per row
+      int wbase = r0, wrow = 0, buf = 0;
+      for (int s0 = r0; s0 < r1; s0 += rps) {
+        const int n = min(rps, r1 - s0);
+        const uint8_t* st = wait_stage(ab);
+        if (st) {
+          const uint32_t sts = smem_u32(st);
+          for (int rb = 0; rb < n; rb += 8) {
+            float part[8][NB];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+#pragma unroll
+              for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
+            for (int sw = 0; sw < spw; ++sw) {
+              const int gi = (cw + NCW * sw) * 32 + lane;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                if (rb + q < n) {
+                  const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
+#pragma unroll
+                  for (int j = 0; j < NB; ++j)
+                    if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                }
+              }
+            }
+            float* ps = m->psum[buf] + (size_t)cw * WIN_ROWS * MAX_BATCH;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              if (j < nb) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = part[q][j];
+                const float sum = reduce8(v, lane);
+                const int q = (lane >> 2) & 7;
+                if ((lane & 3) == 0 && rb + q < n) ps[(wrow + rb + q) * MAX_BATCH + j] = sum;
+              }
+            }
+          }
+        }
+        release_stage(ab);
+        wrow += n;
+        if (wrow + rps > WIN_ROWS || s0 + rps >= r1) {
+          cbar();
+          if (!ab) {
+            const float* pb = m->psum[buf];
+            const int units = PAIRS ? wrow >> 1 : wrow;
+            for (int x = ct; x < units * nb; x += NCT) {
+              const int u = x / nb, j = x - u * nb;
+              if (PAIRS) {
+                float g = 0.f, up = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) {
+                  g += pb[((size_t)w * WIN_ROWS + 2 * u) * MAX_BATCH + j];
+                  up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * MAX_BATCH + j];
+                }
+                epi((wbase >> 1) + u, j, g, up);
+              } else {
+                float s = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * MAX_BATCH + j];
+                epi(wbase + u, j, s, 0.f);
+              }
+            }
+          }
+          buf ^= 1;
+          wbase = s0 + n;
+          wrow = 0;
         }
       }
-      release_stage(ab);
+    } else {
+      for (int s0 = r0; s0 < r1; s0 += rps) {
+        const int n = min(rps, r1 - s0);
+        const uint8_t* st = wait_stage(ab);
+        if (st) {
+          const uint32_t sts = smem_u32(st);
+          // PAIRS: warp w takes pairs w, w+8, ... (rows 2f, 2f+1); else rows w, w+8, ...
+          const int unit = PAIRS ? 2 : 1;
+          const int per = 8 / unit;  // units per batch of 8 rows
+          for (int u0 = cw; u0 * unit < n; u0 += NCW * per) {
+            float part[8][NB];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+#pragma unroll
+              for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
+              if (row < n) {
+                for (int gi = lane; gi < ng; gi += 32) {
+                  const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
+#pragma unroll
+                  for (int j = 0; j < NB; ++j)
+                    if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              if (j < nb) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = part[q][j];
+                const float sum = reduce8(v, lane);
+                const int q = (lane >> 2) & 7;
+                if (PAIRS) {
+                  const float other = __shfl_down_sync(FULL, sum, 4);  // group q+1 = the up row
+                  const int row = (u0 + NCW * (q / 2)) * 2;
+                  if ((lane & 7) == 0 && row < n) epi((s0 + row) >> 1, j, sum, other);
+                } else {
+                  const int row = u0 + NCW * q;
+                  if ((lane & 3) == 0 && row < n) epi(s0 + row, j, sum, 0.f);
+                }
+              }
+            }
+          }
+        }
+        release_stage(ab);
+      }
     }
-    mark(TR_STAGES);
     return ab;
   }
 
@@ -565,36 +741,56 @@ struct Consumer {
     return last;
   }
 
+  // Routing of layer l (written by that layer's router finisher) into smem;
+  // the caller's next barrier publishes it.  Returns the distinct-expert count.
+  __device__ int load_route(int l) {
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    const int umax = p.rm.umax, bc = p.rm.bcap;
+    for (int i = ct; i < U; i += NCT) {
+      m->r_exp[i] = __ldcg(rt + 1 + i);
+      m->r_cnt[i] = __ldcg(rt + 1 + umax + i);
+    }
+    for (int i = ct; i < U * bc; i += NCT) {
+      m->r_tok[i] = __ldcg(rt + 1 + 2 * umax + i);
+      m->r_rank[i] = __ldcg(rt + 1 + 2 * umax + umax * bc + i);
+    }
+    return U;
+  }
+
   // ------------------------------------------------------------ tasks
 
   __device__ bool qkv(const Task& t, bool ab) {
     const int l = t.layer;
-    if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i) { return x_in(l, b, i); });
+    if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i4) { return x_in4(l, b, i4); });
     cbar();
+    mark(TR_ACT);
     float* out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
-    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-        if (j < p.B && lane == j) out[(size_t)j * p.qkv_rows + row] = s[j];
-    });
+    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab,
+                     [&](int row, int j, float s, float) { out[(size_t)j * p.qkv_rows + row] = s; });
+    mark(TR_STAGES);
     ab = finish(ab);
     if (!ab) signal(p.cm.qkv + l * p.nkv + t.a[2]);
     return ab;
   }
 
   __device__ bool oproj(const Task& t, bool ab) {
-    const int l = t.layer, K = p.nq * p.d;
+    const int l = t.layer, K = p.nq * p.d, r0 = t.a[0], nr = t.a[1] - r0;
+    float* xres = ydown;  // residual rows of this tile, [B][nr]
     if (!ab) {
-      const float* o = p.o + (size_t)l * p.bcap * K;
-      for (int i = ct; i < p.B * K; i += NCT) act[i] = __ldcg(o + i);
+      const float4* o = reinterpret_cast<const float4*>(p.o + (size_t)l * p.bcap * K);
+      float4* dst = reinterpret_cast<float4*>(act);
+#pragma unroll 4
+      for (int i = ct; i < (p.B * K) >> 2; i += NCT) dst[i] = __ldcg(o + i);
+      for (int i = ct; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
     }
     cbar();
+    mark(TR_ACT);
     float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
-    ab = rows(K, t.a[0], t.a[1], act, K, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-        if (j < p.B && lane == j) xm[(size_t)j * p.H + row] = x_in(l, j, row) + s[j];
+    ab = gemv<false>(K, r0, t.a[1], act, K, nullptr, p.B, ab, [&](int row, int j, float s, float) {
+      xm[(size_t)j * p.H + row] = xres[j * nr + row - r0] + s;
     });
+    mark(TR_STAGES);
     ab = finish(ab);
     if (!ab) signal(p.cm.o + l);
     return ab;
@@ -602,19 +798,22 @@ struct Consumer {
 
   __device__ void fill_ffn_norm(int l) {
     const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
-    fill_rmsnorm(p.ffn_norm[l], [&](int b, int i) { return __ldcg(xm + (size_t)b * p.H + i); });
+    fill_rmsnorm(p.ffn_norm[l], [&](int b, int i4) {
+      return __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * p.H) + i4);
+    });
   }
 
   // Top-k of every request's router logits, gates, and the distinct-expert list.
   __device__ void route_finish(int l) {
     const int E = p.E, k = p.k, B = p.B;
     int* rt = const_cast<int*>(route_of(p, l));
+    constexpr int NV = MAX_EXPERTS / 32;
     if (cw < B) {
       const int b = cw;
       const float* rl = p.rlog + ((size_t)l * p.bcap + b) * E;
-      float v[MAX_EXPERTS / 32];
+      float v[NV];
 #pragma unroll
-      for (int i = 0; i < MAX_EXPERTS / 32; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
       }
@@ -624,7 +823,7 @@ struct Consumer {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < MAX_EXPERTS / 32; ++i) {
+        for (int i = 0; i < NV; ++i) {
           const int e = lane + 32 * i;
           if (e < E && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
         }
@@ -634,7 +833,9 @@ struct Consumer {
           const int oi = __shfl_xor_sync(FULL, bi, o);
           if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
-        if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (lane + 32 * i == bi) v[i] = -INFINITY;
         if (j == 0) first = bv;
         if (lane == j) { selv = bv; mysel = bi; }
       }
@@ -682,12 +883,11 @@ struct Consumer {
     const int l = t.layer;
     if (!ab) fill_ffn_norm(l);
     cbar();
+    mark(TR_ACT);
     float* rl = p.rlog + (size_t)l * p.bcap * p.E;
-    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab, [&](int row, const float(&s)[NB]) {
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-        if (j < p.B && lane == j) rl[(size_t)j * p.E + row] = s[j];
-    });
+    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab,
+                     [&](int row, int j, float s, float) { rl[(size_t)j * p.E + row] = s; });
+    mark(TR_STAGES);
     ab = finish(ab);
     if (ab) return ab;
     if (ticket(p.cm.rticket + l, (uint32_t)t.a[2])) {
@@ -698,55 +898,29 @@ struct Consumer {
     return ab;
   }
 
-  // Load the token list of distinct-expert slot u into smem (all consumer threads).
-  __device__ int load_segment(const int* rt, int u) {
-    const int umax = p.rm.umax, bc = p.rm.bcap;
-    const int nt = __ldcg(rt + 1 + umax + u);
-    cbar();  // previous segment's readers are done
-    if (ct < nt) {
-      m->seg_tok[ct] = __ldcg(rt + 1 + 2 * umax + u * bc + ct);
-      m->seg_rank[ct] = __ldcg(rt + 1 + 2 * umax + umax * bc + u * bc + ct);
-    }
-    cbar();
-    return nt;
-  }
-
   __device__ bool gate_up(const Task& t, bool ab) {
-    const int l = t.layer, H = p.H, F = p.F, k = p.k;
-    if (!ab) fill_ffn_norm(l);
+    const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
+    int U = 0;
+    if (!ab) {
+      fill_ffn_norm(l);
+      U = load_route(l);
+    }
+    U = __shfl_sync(FULL, U, 0);
     cbar();
-    const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
+    mark(TR_ACT);
     long long q0, q1;
     gu_range(p, t, U, q0, q1);
-    const int pps = pairs_per_stage(p);
     float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
-    mark(TR_ACT);
     for (long long q = q0; q < q1;) {
       const int u = (int)(q / F);
       const int fa = (int)(q - (long long)u * F);
       const int fb = (int)min((long long)F, q1 - (long long)u * F);
-      const int nt = load_segment(rt, u);
-      for (int f0 = fa; f0 < fb; f0 += pps) {
-        const int n = min(pps, fb - f0);
-        const uint8_t* st = wait_stage(ab);
-        if (st) {
-          for (int rr = cw; rr < n; rr += NCW) {
-            float sg[NB], su[NB];
-            row_dot(st + (size_t)rr * H * 2, H, act, H, m->seg_tok, nt, sg);
-            row_dot(st + (size_t)(n + rr) * H * 2, H, act, H, m->seg_tok, nt, su);
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              if (j < nt && lane == j) {
-                const float gv = sg[j];
-                const float h = gv / (1.0f + expf(-gv)) * su[j];
-                hb[((size_t)m->seg_tok[j] * k + m->seg_rank[j]) * F + f0 + rr] = h;
-              }
-            }
-          }
-        }
-        release_stage(ab);
-      }
+      const int nt = m->r_cnt[u];
+      const int* toks = m->r_tok + u * bc;
+      const int* ranks = m->r_rank + u * bc;
+      ab = gemv<true>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, [&](int f, int j, float g, float up) {
+        hb[((size_t)toks[j] * k + ranks[j]) * F + f] = g / (1.0f + expf(-g)) * up;
+      });
       q = (long long)(u + 1) * F;
     }
     mark(TR_STAGES);
@@ -756,51 +930,44 @@ struct Consumer {
   }
 
   __device__ bool down(const Task& t, bool ab) {
-    const int l = t.layer, F = p.F, k = p.k, B = p.B;
+    const int l = t.layer, F = p.F, k = p.k, B = p.B, bc = p.rm.bcap;
     const int r0 = t.a[0], r1 = t.a[1], nr = r1 - r0, drm = p.down_rows_max;
     const float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
-    if (!ab && p.allh) {
-      for (int i = ct; i < B * k * F; i += NCT) act[i] = __ldcg(hb + i);
+    int U = 0;
+    if (!ab) {
+      U = load_route(l);
+      if (p.allh) {
+        const float4* src = reinterpret_cast<const float4*>(hb);
+        float4* dst = reinterpret_cast<float4*>(act);
+#pragma unroll 4
+        for (int i = ct; i < (B * k * F) >> 2; i += NCT) dst[i] = __ldcg(src + i);
+      }
     }
+    U = __shfl_sync(FULL, U, 0);
     cbar();
-    const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
-    const int rps = rows_per_stage(p, F);
+    if (!ab && p.allh) {
+      for (int i = ct; i < U * bc; i += NCT) m->r_row[i] = m->r_tok[i] * k + m->r_rank[i];
+      cbar();
+    }
     mark(TR_ACT);
     for (int u = 0; u < U; ++u) {
-      const int nt = load_segment(rt, u);
-      int* map = m->seg_rank;  // reused below as the act row map
-      if (p.allh) {
-        if (ct < nt) map[ct] = m->seg_tok[ct] * k + m->seg_rank[ct];
-      } else if (!ab) {
-        for (int i = ct; i < nt * F; i += NCT) {
-          const int j = i / F;
-          act[i] = __ldcg(hb + ((size_t)m->seg_tok[j] * k + m->seg_rank[j]) * F + (i - j * F));
-        }
-      }
-      // seg_rank is overwritten only in allh mode; keep the true rank for ydown
-      int rank_of[NB];
-#pragma unroll
-      for (int j = 0; j < NB; ++j) rank_of[j] = 0;
-      cbar();
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-        if (j < nt) rank_of[j] = p.allh ? map[j] - m->seg_tok[j] * k : m->seg_rank[j];
-      for (int s0 = r0; s0 < r1; s0 += rps) {
-        const int n = min(rps, r1 - s0);
-        const uint8_t* st = wait_stage(ab);
-        if (st) {
-          for (int rr = cw; rr < n; rr += NCW) {
-            float s[NB];
-            row_dot(st + (size_t)rr * F * 2, F, act, F, p.allh ? map : nullptr, nt, s);
-#pragma unroll
-            for (int j = 0; j < NB; ++j)
-              if (j < nt && lane == j)
-                ydown[((size_t)m->seg_tok[j] * k + rank_of[j]) * drm + (s0 + rr - r0)] = s[j];
+      const int nt = m->r_cnt[u];
+      const int* toks = m->r_tok + u * bc;
+      const int* ranks = m->r_rank + u * bc;
+      if (!p.allh) {
+        cbar();  // the previous expert's rows are done with act
+        if (!ab) {
+          for (int i = ct; i < nt * F; i += NCT) {
+            const int j = i / F;
+            act[i] = __ldcg(hb + ((size_t)toks[j] * k + ranks[j]) * F + (i - j * F));
           }
         }
-        release_stage(ab);
+        cbar();
       }
+      ab = gemv<false>(F, r0, r1, act, F, p.allh ? m->r_row + u * bc : nullptr, nt, ab,
+                       [&](int row, int j, float s, float) {
+                         ydown[((size_t)toks[j] * k + ranks[j]) * drm + (row - r0)] = s;
+                       });
     }
     mark(TR_STAGES);
     cbar();
@@ -823,14 +990,16 @@ struct Consumer {
 
   __device__ bool attn(const Task& t, bool ab) {
     const int l = t.layer, b = t.a[0], g = t.a[1];
-    const int G = p.G, d = p.d, ps = p.ps, half = d >> 1, dpl = d >> 5;
+    const int G = p.G, d = p.d, half = d >> 1, dpl = d >> 5;
+    constexpr int PS = 16;                         // page size (tokens)
     const int pos = __ldcg(p.seq_len + b);
     int tok0, tok1;
     attn_range(p, t, pos, tok0, tok1);
+    const int RS = d + 4;                          // partial row: acc[d], m, l, pad (16-byte rows)
     float* q_s = act;                 // [MAX_G][d]
     float* kn_s = q_s + MAX_G * d;    // new token's key (bf16 values)
     float* vn_s = kn_s + d;
-    float* mrg = vn_s + d;            // [NCW][G][d + 2]
+    float* mrg = vn_s + d;            // [NCW][G][RS]
     const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
     const float2* rope = p.rope + (size_t)pos * half;
     const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
@@ -846,7 +1015,7 @@ struct Consumer {
         const float* kr = qkv + (size_t)G * d;
         const float* vr = kr + d;
         const size_t off =
-            (((size_t)p.page_table[(size_t)b * p.max_pages + pos / ps] * p.nkv + g) * ps + pos % ps) * d;
+            (((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * PS + pos % PS) * d;
         uint16_t* kd = p.k_pool[l] + off;
         uint16_t* vd = p.v_pool[l] + off;
         for (int i = ct; i < half; i += NCT) {
@@ -866,6 +1035,7 @@ struct Consumer {
       }
     }
     cbar();
+    mark(TR_ACT);
     float qr[MAX_G][4], acc[MAX_G][4];
 #pragma unroll
     for (int h = 0; h < MAX_G; ++h)
@@ -877,13 +1047,15 @@ struct Consumer {
     const int hl = (lane >> 2) & 7;  // head whose softmax state this lane keeps
     float mrun = -INFINITY, lrun = 0.f;
     const int ppg = pages_per_stage(p);
-    const int PB = ps * d * 2;
-    const int tps = ppg * ps;
-    mark(TR_ACT);
+    const int rowb = d * 2;                        // bytes per K/V row
+    const int tps = ppg * PS;
     for (int ts = tok0; ts < tok1; ts += tps) {
       const int nt = min(tps, tok1 - ts);
+      const int newtl = pos - ts;                  // stage-local index of the new token, if inside
       const uint8_t* st = wait_stage(ab);
       if (st) {
+        const uint32_t kbase = smem_u32(st) + lane * dpl * 2;       // pages are contiguous in a stage
+        const uint32_t vbase = kbase + ppg * PS * rowb;
         for (int jb = cw; jb < nt; jb += NCW * 8) {
           float s[8];
 #pragma unroll
@@ -891,25 +1063,22 @@ struct Consumer {
             const int tl = jb + NCW * j;
             float kf[4] = {0.f, 0.f, 0.f, 0.f};
             if (tl < nt) {
-              if (ts + tl == pos) {
+              if (tl == newtl) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                   if (i < dpl) kf[i] = kn_s[lane * dpl + i];
+              } else if (dpl == 4) {
+                const uint2 u = lds64(kbase + tl * rowb);
+                kf[0] = bf_lo(u.x); kf[1] = bf_hi(u.x); kf[2] = bf_lo(u.y); kf[3] = bf_hi(u.y);
               } else {
-                const uint8_t* kr = st + (size_t)(tl / ps) * PB + (size_t)(tl % ps) * d * 2 + lane * dpl * 2;
-                if (dpl == 4) {
-                  const uint2 u = *reinterpret_cast<const uint2*>(kr);
-                  kf[0] = bf_lo(u.x); kf[1] = bf_hi(u.x); kf[2] = bf_lo(u.y); kf[3] = bf_hi(u.y);
-                } else {
-                  const uint32_t u = *reinterpret_cast<const uint32_t*>(kr);
-                  kf[0] = bf_lo(u); kf[1] = bf_hi(u);
-                }
+                const uint32_t u = lds32(kbase + tl * rowb);
+                kf[0] = bf_lo(u); kf[1] = bf_hi(u);
               }
             }
             float part[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h)
-              part[h] = qr[h][0] * kf[0] + qr[h][1] * kf[1] + qr[h][2] * kf[2] + qr[h][3] * kf[3];
+              part[h] = fmaf(qr[h][3], kf[3], fmaf(qr[h][2], kf[2], fmaf(qr[h][1], kf[1], qr[h][0] * kf[0])));
             const float sv = reduce8(part, lane);
             s[j] = (tl < nt && hl < G) ? sv : -INFINITY;
           }
@@ -942,20 +1111,16 @@ struct Consumer {
             const int tl = jb + NCW * j;
             if (tl < nt) {
               float vf[4] = {0.f, 0.f, 0.f, 0.f};
-              if (ts + tl == pos) {
+              if (tl == newtl) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                   if (i < dpl) vf[i] = vn_s[lane * dpl + i];
+              } else if (dpl == 4) {
+                const uint2 u = lds64(vbase + tl * rowb);
+                vf[0] = bf_lo(u.x); vf[1] = bf_hi(u.x); vf[2] = bf_lo(u.y); vf[3] = bf_hi(u.y);
               } else {
-                const uint8_t* vr =
-                    st + (size_t)(ppg + tl / ps) * PB + (size_t)(tl % ps) * d * 2 + lane * dpl * 2;
-                if (dpl == 4) {
-                  const uint2 u = *reinterpret_cast<const uint2*>(vr);
-                  vf[0] = bf_lo(u.x); vf[1] = bf_hi(u.x); vf[2] = bf_lo(u.y); vf[3] = bf_hi(u.y);
-                } else {
-                  const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
-                  vf[0] = bf_lo(u); vf[1] = bf_hi(u);
-                }
+                const uint32_t u = lds32(vbase + tl * rowb);
+                vf[0] = bf_lo(u); vf[1] = bf_hi(u);
               }
 #pragma unroll
               for (int h = 0; h < MAX_G; ++h) {
@@ -971,7 +1136,6 @@ struct Consumer {
     }
     mark(TR_STAGES);
     // merge the 8 warps' partial softmax states of this chunk
-    const int RS = d + 2;
     if (!ab) {
       if ((lane & 3) == 0 && hl < G) {
         mrg[(cw * G + hl) * RS + d] = mrun;
@@ -1012,21 +1176,56 @@ struct Consumer {
     ab = finish(ab);
     if (ab) return ab;
     if (ticket(p.cm.attn_idx(l, b, g), (uint32_t)t.a[6])) {
+      // Combine the nc chunks of (b, g) in chunk order: gather every chunk's
+      // (max, normaliser) in parallel, turn them into weights, then one float4
+      // of every chunk's accumulator per thread with all loads in flight.
       const float* p0 = p.part + ((size_t)l * nslots + t.a[5]) * G * RS;
       const int nc = t.a[6];
-      float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
-      for (int idx = ct; idx < G * d; idx += NCT) {
-        const int h = idx / d, i = idx - h * d;
+      float* wts = mrg;                 // [nc][G]
+      float* lsm = mrg + nc * G;        // [nc][G]
+      float* inv = q_s;                 // [G]
+      for (int idx = ct; idx < nc * G; idx += NCT) {
+        const float* pc = p0 + (size_t)idx * RS;   // idx = c * G + h
+        wts[idx] = __ldcg(pc + d);
+        lsm[idx] = __ldcg(pc + d + 1);
+      }
+      cbar();
+      if (ct < G) {
+        const int h = ct;
         float M = -INFINITY;
-        for (int c = 0; c < nc; ++c) M = fmaxf(M, __ldcg(p0 + ((size_t)c * G + h) * RS + d));
-        float Ls = 0.f, A = 0.f;
+        for (int c = 0; c < nc; ++c) M = fmaxf(M, wts[c * G + h]);
+        float Ls = 0.f;
         for (int c = 0; c < nc; ++c) {
-          const float* pc = p0 + ((size_t)c * G + h) * RS;
-          const float f = exp2f(__ldcg(pc + d) - M);
-          Ls = fmaf(__ldcg(pc + d + 1), f, Ls);
-          A = fmaf(__ldcg(pc + i), f, A);
+          const float f = exp2f(wts[c * G + h] - M);
+          wts[c * G + h] = f;
+          Ls = fmaf(lsm[c * G + h], f, Ls);
         }
-        o[h * d + i] = A / Ls;
+        inv[h] = 1.0f / Ls;
+      }
+      cbar();
+      float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
+      const int d4 = d >> 2;
+      for (int idx = ct; idx < G * d4; idx += NCT) {
+        const int h = idx / d4, i4 = idx - h * d4;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < nc; c0 += 8) {
+          float4 v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c0 + c < nc)
+              v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(c0 + c) * G + h) * RS) + i4);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c0 + c < nc) {
+              const float f = wts[(c0 + c) * G + h];
+              A.x = fmaf(v[c].x, f, A.x);
+              A.y = fmaf(v[c].y, f, A.y);
+              A.z = fmaf(v[c].z, f, A.z);
+              A.w = fmaf(v[c].w, f, A.w);
+            }
+        }
+        const float s = inv[h];
+        reinterpret_cast<float4*>(o + h * d)[i4] = make_float4(A.x * s, A.y * s, A.z * s, A.w * s);
       }
       ab = finish(false);
       if (!ab) signal(p.cm.combine + l);
@@ -1038,24 +1237,46 @@ struct Consumer {
     const int L = p.L, B = p.B;
     if (!ab) {
       const float* xo = p.x_out + (size_t)(L - 1) * p.bcap * p.H;
-      fill_rmsnorm(p.final_norm, [&](int b, int i) { return __ldcg(xo + (size_t)b * p.H + i); });
+      fill_rmsnorm(p.final_norm, [&](int b, int i4) {
+        return __ldcg(reinterpret_cast<const float4*>(xo + (size_t)b * p.H) + i4);
+      });
     }
     cbar();
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    float* lg = p.logits;
-    ab = rows(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, const float(&s)[NB]) {
+    mark(TR_ACT);
+    // each thread keeps, per activation row, the best (value, lowest index) it saw
+    float bv[NB];
+    int bi[NB];
 #pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        if (j < B && lane == j) {
-          if (lg) lg[(size_t)j * p.V + row] = s[j];
-          if (s[j] > bv || (s[j] == bv && row < bi)) { bv = s[j]; bi = row; }
+    for (int j = 0; j < NB; ++j) {
+      bv[j] = -INFINITY;
+      bi[j] = 0x7fffffff;
+    }
+    float* lg = p.logits;
+    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s, float) {
+      if (lg) lg[(size_t)j * p.V + row] = s;
+#pragma unroll
+      for (int jj = 0; jj < NB; ++jj)
+        if (jj == j && (s > bv[jj] || (s == bv[jj] && row < bi[jj]))) {
+          bv[jj] = s;
+          bi[jj] = row;
+        }
+    });
+    mark(TR_STAGES);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(FULL, bv[j], o);
+        const int oi = __shfl_xor_sync(FULL, bi[j], o);
+        if (ov > bv[j] || (ov == bv[j] && oi < bi[j])) {
+          bv[j] = ov;
+          bi[j] = oi;
         }
       }
-    });
-    if (!ab && lane < B) {
-      m->best_v[cw * MAX_BATCH + lane] = bv;
-      m->best_i[cw * MAX_BATCH + lane] = bi;
+      if (!ab && lane == 0 && j < B) {
+        m->best_v[cw * MAX_BATCH + j] = bv[j];
+        m->best_i[cw * MAX_BATCH + j] = bi[j];
+      }
     }
     ab = cbar_or(ab);
     if (ab) return ab;
@@ -1101,8 +1322,10 @@ struct Consumer {
 
   __device__ void run(int t0, int t1) {
     for (ti = t0; ti < t1; ++ti) {
-      const Task t = p.tasks[ti];
+      const Task t = ldg_task(p.tasks + ti);
+      if (ti + 1 < t1) prefetch_l1(p.tasks + ti + 1);   // the next record arrives while this task runs
       bool ab = false;
+      nstage_seen = 0;
       mark(TR_FETCH);
       if (ct == 0) ab = !wait_ctr(p, t.wait_ctr, t.wait_cnt, ti);
       ab = cbar_or(ab);

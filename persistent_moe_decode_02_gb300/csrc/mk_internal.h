@@ -15,10 +15,12 @@ constexpr int MAX_BATCH = 8;
 constexpr int MAX_EXPERTS = 256;
 constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
 constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
-constexpr int TRACE_SLOTS = 8;             // stamps per task in the optional timeline
+constexpr int TRACE_SLOTS = 10;            // stamps per task in the optional timeline
 // timeline slots: consumer fetched / dependency met / activations ready /
-// stages consumed / done; producer first copy / last copy / task start
-enum TraceSlot { TR_FETCH = 0, TR_DEP, TR_ACT, TR_STAGES, TR_DONE, TR_P_FIRST, TR_P_LAST, TR_P_START };
+// stages consumed / done; producer first copy / last copy / task start;
+// consumer warp 0 saw its first / last stage of the task land
+enum TraceSlot { TR_FETCH = 0, TR_DEP, TR_ACT, TR_STAGES, TR_DONE, TR_P_FIRST, TR_P_LAST, TR_P_START,
+                 TR_S_FIRST, TR_S_LAST };
 
 // Task kinds in per-layer order.  Each kind signals one counter family.
 enum TaskType : int32_t {

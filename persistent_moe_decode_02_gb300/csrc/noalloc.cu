@@ -292,7 +292,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_stat = dc.take(4 * sizeof(int));
   const size_t d_rope = dc.take((size_t)npos * (s.d / 2) * sizeof(float2));
   const size_t d_qkv = dc.take(L * B * s.qkv_rows * sizeof(float));
-  const size_t d_part = dc.take(L * (size_t)cnt.slots * s.G * (s.d + 2) * sizeof(float));
+  const size_t d_part = dc.take(L * (size_t)cnt.slots * s.G * (s.d + 4) * sizeof(float));
   const size_t d_o = dc.take(L * B * s.nq * s.d * sizeof(float));
   const size_t d_xm = dc.take(L * B * s.H * sizeof(float));
   const size_t d_xo = dc.take(L * B * s.H * sizeof(float));
@@ -313,7 +313,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   // shared-memory plan (same rule as mk_plan_create)
   const int nqd = s.nq * s.d;
   long long A1 = (long long)B * (s.H > nqd ? (s.H > s.F ? s.H : s.F) : (nqd > s.F ? nqd : s.F));
-  long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 2);
+  long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4);
   long long Ah = (long long)B * s.k * s.F;
   const int allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
   long long act = A1 > A3 ? A1 : A3;

@@ -406,7 +406,7 @@ int replan(mk_plan* p, cudaStream_t st) {
       p->d_part = nullptr;
     }
     size_t cap = (size_t)cnt.part_slots * 2 + 16;
-    if (dalloc(p, &p->d_part, (size_t)p->s.L * cap * p->s.G * (p->s.d + 2) * sizeof(float)) != cudaSuccess)
+    if (dalloc(p, &p->d_part, (size_t)p->s.L * cap * p->s.G * (p->s.d + 4) * sizeof(float)) != cudaSuccess)
       return MK_ERR_CUDA;
     p->part_cap_slots = cap;
   }
@@ -553,7 +553,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   // shared-memory budget: activations + misc, the rest is the weight ring
   const int nqd = s.nq * s.d;
   const long long A1 = (long long)bcap * std::max(std::max(s.H, nqd), s.F);
-  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 2);
+  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4);
   const long long Ah = (long long)bcap * s.k * s.F;
   p->allh = (Ah * 4 <= 64 * 1024) ? 1 : 0;
   p->act_floats = (int)std::max(std::max(A1, A3), p->allh ? Ah : 0LL);

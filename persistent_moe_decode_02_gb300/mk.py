@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmk.so")
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_DEP_TIMEOUT, MK_ERR_CAPACITY, MK_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ_LENS, MK_DBG_UNION = 1, 2, 3, 4, 5, 6
 MK_DBG_TASKS, MK_DBG_TRACE = 7, 8
-TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start"]
+TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start", "s_first", "s_last"]
 
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
@@ -226,11 +226,11 @@ class Plan:
         return out
 
     def timeline(self, stream=None):
-        """(tasks int32 [n, 12], stamps int64 [n, 8]) of the last step (needs trace=True)."""
+        """(tasks int32 [n, 12], stamps int64 [n, 10]) of the last step (needs trace=True)."""
         n = self.info()["num_tasks"]
         tasks = torch.empty(n, 12, dtype=torch.int32)
         self.read_debug(MK_DBG_TASKS, tasks, stream)
-        stamps = torch.empty(n, 8, dtype=torch.int64)
+        stamps = torch.empty(n, len(TRACE_SLOTS), dtype=torch.int64)
         self.read_debug(MK_DBG_TRACE, stamps, stream)
         self.sync(stream)
         return tasks, stamps

@@ -23,7 +23,8 @@ class DeviceModel:
 
     wqkv[l] rows are grouped per KV head g: the G query heads of group g,
     then key head g, then value head g (rows taken from the logical wq, wk,
-    wv streams).  w_gate_up[l][e] is the gate rows then the up rows."""
+    wv streams).  w_gate_up[l][e] interleaves the gate and up rows: row 2f is
+    gate row f, row 2f + 1 is up row f."""
 
     def __init__(self, D: Dims, seed: int = 0, device: str = "cuda"):
         self.D, self.seed = D, seed
@@ -47,11 +48,12 @@ class DeviceModel:
             self.wo.append(normal((H, D.n_q_heads * d), seed, wname("wo", l), device=dev))
             self.ffn_norm.append(normal((H,), seed, wname("ffn_norm", l), mean=1.0, device=dev))
             self.router.append(normal((E, H), seed, wname("router", l), device=dev))
-            gu = torch.empty(E, 2 * F, H, dtype=torch.bfloat16, device=dev)
+            gu = torch.empty(E, F, 2, H, dtype=torch.bfloat16, device=dev)
+            tmp = torch.empty(F, H, dtype=torch.bfloat16, device=dev)
             for e in range(E):
-                fill_normal_(gu[e, :F], seed, wname("gate", l), start=e * F * H)
-                fill_normal_(gu[e, F:], seed, wname("up", l), start=e * F * H)
-            self.w_gate_up.append(gu)
+                gu[e, :, 0].copy_(fill_normal_(tmp, seed, wname("gate", l), start=e * F * H))
+                gu[e, :, 1].copy_(fill_normal_(tmp, seed, wname("up", l), start=e * F * H))
+            self.w_gate_up.append(gu.view(E, 2 * F, H))
             self.w_down.append(normal((E, H, F), seed, wname("down", l), device=dev))
 
     def weights(self) -> dict:
