@@ -80,9 +80,12 @@ typedef struct mk_weights {
 } mk_weights;
 
 /* Paged KV cache: per layer one K pool and one V pool (HOST arrays of
- * n_layers device pointers), each bf16 [num_pages, n_kv_heads, page_size,
- * head_dim].  Token t of request b lives in page page_table[b][t / page_size],
- * slot t % page_size.  16-byte aligned. */
+ * n_layers device pointers), each bf16 [num_pages, n_kv_heads, head_dim,
+ * page_size]: a page holds, per KV head, its tokens' vectors transposed (one
+ * row of page_size slots per dimension), which keeps the tensor-core operand
+ * loads of the attention tiles nearly free of shared-memory bank conflicts.
+ * Token t of request b lives in page page_table[b][t / page_size], slot
+ * t % page_size.  16-byte aligned. */
 typedef struct mk_kv {
   void* const* k_pool;
   void* const* v_pool;

@@ -112,15 +112,24 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
+// Tensor-core helpers: 8x8 b16 matrix loads from shared memory and the
+// m16n8k16 bf16 MMA with fp32 accumulation (d += a . b).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Task records are read-only during a step: read them through the L1.
@@ -544,9 +553,20 @@ struct Consumer {
     }
   }
 
+  // Token id of request b, checked: an id outside [0, vocab) records
+  // MK_ERR_INVALID and reads row 0 instead of faulting.
+  __device__ int token(int b) const {
+    const int tok = __ldcg(p.tokens + b);
+    if (tok < 0 || tok >= p.V) {
+      set_error(p, MK_ERR_INVALID, -1, tok);
+      return 0;
+    }
+    return tok;
+  }
+
   __device__ float4 x_in4(int l, int b, int i4) const {
     if (l == 0) {
-      const int tok = __ldcg(p.tokens + b);
+      const int tok = token(b);
       const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.embed + (size_t)tok * p.H) + i4);
       return make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
     }
@@ -554,14 +574,15 @@ struct Consumer {
   }
 
   __device__ float x_in(int l, int b, int i) const {
-    if (l == 0) return bf2f(p.embed[(size_t)__ldcg(p.tokens + b) * p.H + i]);
+    if (l == 0) return bf2f(p.embed[(size_t)token(b) * p.H + i]);
     return __ldcg(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H + i);
   }
 
   // dot of one 16-byte bf16 granule with 8 activations
   __device__ __forceinline__ static float dot8(const uint4 wv, uint32_t a) {
-    const float4 x0 = lds128f(a);
-    const float4 x1 = lds128f(a + 16);
+    return dot8r(wv, lds128f(a), lds128f(a + 16));
+  }
+  __device__ __forceinline__ static float dot8r(const uint4 wv, const float4 x0, const float4 x1) {
     float s0 = bf_lo(wv.x) * x0.x;
     float s1 = bf_hi(wv.x) * x0.y;
     s0 = fmaf(bf_lo(wv.y), x0.z, s0);
@@ -612,13 +633,42 @@ struct Consumer {
               for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
             for (int sw = 0; sw < spw; ++sw) {
               const int gi = (cw + NCW * sw) * 32 + lane;
+              if constexpr (NB <= 4) {
+                // this warp's 8 activation columns are the same for every row of the batch
+                float4 x0[NB], x1[NB];
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                if (rb + q < n) {
-                  const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
+                for (int j = 0; j < NB; ++j) {
+                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if constexpr (NB <= 2) {
+                  uint4 wv[8];
 #pragma unroll
-                  for (int j = 0; j < NB; ++j)
-                    if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                  for (int q = 0; q < 8; ++q)
+                    wv[q] = rb + q < n ? lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
+                } else {
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) {
+                    if (rb + q < n) {
+                      const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
+#pragma unroll
+                      for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv, x0[j], x1[j]);
+                    }
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  if (rb + q < n) {
+                    const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
+#pragma unroll
+                    for (int j = 0; j < NB; ++j)
+                      if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                  }
                 }
               }
             }
@@ -988,178 +1038,246 @@ struct Consumer {
     return ab;
   }
 
+  // ---- split-KV attention chunk on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc)
+  // Pages hold K and V transposed ([d][16 slots]).  Per page (16 tokens):
+  //   S  [16 tok x 8 heads] = K [tok x d] . Q^T            (A = K via ldmatrix.trans, B = q regs)
+  //   O^T[16 dim x 8 heads] += V^T [dim x tok] . P^T       (A = V^T via ldmatrix, B = P via smem)
+  // q and P enter as bf16 hi + lo pairs (two MMAs each), so the products keep
+  // close to fp32 accuracy; K and V are exact bf16.  The warps of a stage take
+  // its pages (NCW / pages-per-stage warps per page, splitting the d/16 output
+  // row tiles); each page group keeps its own online-softmax state, merged at
+  // the end of the chunk, then the chunks of (request, KV head) are combined by
+  // the last one to finish.
   __device__ bool attn(const Task& t, bool ab) {
     const int l = t.layer, b = t.a[0], g = t.a[1];
-    const int G = p.G, d = p.d, half = d >> 1, dpl = d >> 5;
+    const int G = p.G, d = p.d, half = d >> 1;
     constexpr int PS = 16;                         // page size (tokens)
     const int pos = __ldcg(p.seq_len + b);
     int tok0, tok1;
     attn_range(p, t, pos, tok0, tok1);
     const int RS = d + 4;                          // partial row: acc[d], m, l, pad (16-byte rows)
-    float* q_s = act;                 // [MAX_G][d]
-    float* kn_s = q_s + MAX_G * d;    // new token's key (bf16 values)
+    float* q_s = act;                              // [MAX_G][d] rotated, scaled q
+    float* kn_s = q_s + MAX_G * d;                 // new token's key (bf16 values)
     float* vn_s = kn_s + d;
-    float* mrg = vn_s + d;            // [NCW][G][RS]
+    float* mrg = vn_s + d;                         // [groups][G][RS]
+    uint32_t* pscr = reinterpret_cast<uint32_t*>(mrg + NCW * G * RS);   // [NCW][2][8][8] packed P
     const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
     const float2* rope = p.rope + (size_t)pos * half;
     const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
+    const bool has_new = pos >= tok0 && pos < tok1;
     if (!ab) {
-      for (int idx = ct; idx < G * half; idx += NCT) {
+      for (int idx = ct; idx < MAX_G * half; idx += NCT) {
         const int h = idx / half, i = idx - h * half;
-        const float2 cs = rope[i];
-        const float a = __ldcg(qkv + h * d + i), c = __ldcg(qkv + h * d + i + half);
-        q_s[h * d + i] = (a * cs.x - c * cs.y) * qscale;
-        q_s[h * d + i + half] = (c * cs.x + a * cs.y) * qscale;
+        float qa = 0.f, qb = 0.f;
+        if (h < G) {
+          const float2 cs = rope[i];
+          const float a = __ldcg(qkv + h * d + i), c = __ldcg(qkv + h * d + i + half);
+          qa = (a * cs.x - c * cs.y) * qscale;
+          qb = (c * cs.x + a * cs.y) * qscale;
+        }
+        q_s[h * d + i] = qa;
+        q_s[h * d + i + half] = qb;
       }
-      if (pos >= tok0 && pos < tok1) {
+      if (has_new) {
         const float* kr = qkv + (size_t)G * d;
         const float* vr = kr + d;
-        const size_t off =
-            (((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * PS + pos % PS) * d;
-        uint16_t* kd = p.k_pool[l] + off;
-        uint16_t* vd = p.v_pool[l] + off;
+        const size_t base =
+            ((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * d * PS + pos % PS;
+        uint16_t* kd = p.k_pool[l] + base;
+        uint16_t* vd = p.v_pool[l] + base;
         for (int i = ct; i < half; i += NCT) {
           const float2 cs = rope[i];
           const float a = __ldcg(kr + i), c = __ldcg(kr + i + half);
           const uint16_t k0 = f2bf(a * cs.x - c * cs.y), k1 = f2bf(c * cs.x + a * cs.y);
-          kd[i] = k0;
-          kd[i + half] = k1;
+          kd[(size_t)i * PS] = k0;
+          kd[(size_t)(i + half) * PS] = k1;
           kn_s[i] = bf2f(k0);
           kn_s[i + half] = bf2f(k1);
         }
         for (int i = ct; i < d; i += NCT) {
           const uint16_t v0 = f2bf(__ldcg(vr + i));
-          vd[i] = v0;
+          vd[(size_t)i * PS] = v0;
           vn_s[i] = bf2f(v0);
         }
       }
     }
     cbar();
     mark(TR_ACT);
-    float qr[MAX_G][4], acc[MAX_G][4];
+    const int gq = lane >> 2, tq = lane & 3;       // mma fragment coordinates
+    const int nks = d >> 4;                        // 16-dim k steps (QK) = 16-dim row tiles (PV)
+    // B fragments of Q^T per k step: rows (dims) 2tq, 2tq+1 and +8, column (head) gq
+    uint32_t qh[8][2], ql[8][2];
 #pragma unroll
-    for (int h = 0; h < MAX_G; ++h)
+    for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qr[h][i] = (h < G && i < dpl) ? q_s[h * d + lane * dpl + i] : 0.f;
-        acc[h][i] = 0.f;
+      for (int hfi = 0; hfi < 2; ++hfi) {
+        float x0 = 0.f, x1 = 0.f;
+        if (ks < nks) {
+          x0 = q_s[gq * d + ks * 16 + hfi * 8 + 2 * tq];
+          x1 = q_s[gq * d + ks * 16 + hfi * 8 + 2 * tq + 1];
+        }
+        const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
+        qh[ks][hfi] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        ql[ks][hfi] = (uint32_t)f2bf(x0 - bf2f(h0)) | ((uint32_t)f2bf(x1 - bf2f(h1)) << 16);
       }
-    const int hl = (lane >> 2) & 7;  // head whose softmax state this lane keeps
-    float mrun = -INFINITY, lrun = 0.f;
+    }
     const int ppg = pages_per_stage(p);
-    const int rowb = d * 2;                        // bytes per K/V row
-    const int tps = ppg * PS;
-    for (int ts = tok0; ts < tok1; ts += tps) {
-      const int nt = min(tps, tok1 - ts);
-      const int newtl = pos - ts;                  // stage-local index of the new token, if inside
+    const int wpp = NCW / ppg;                     // warps per page
+    const int grp = cw / wpp, sub = cw - grp * wpp;
+    const int mtw = nks / wpp;                     // output row tiles per warp
+    const uint32_t PB = (uint32_t)d * PS * 2;      // bytes of one page block
+    // online-softmax state of heads 2tq, 2tq+1 (identical across gq) and O^T tiles
+    float mr0 = -INFINITY, mr1 = -INFINITY, lr0 = 0.f, lr1 = 0.f;
+    float o[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
+    uint32_t* myp = pscr + cw * 2 * 64;            // this warp's packed P^T: [hi/lo][head 8][tok/2 8]
+    const int pg0 = tok0 / PS, pg1 = (tok1 + PS - 1) / PS;
+    for (int pg = pg0; pg < pg1; pg += ppg) {
+      const int npg = min(ppg, pg1 - pg);
       const uint8_t* st = wait_stage(ab);
-      if (st) {
-        const uint32_t kbase = smem_u32(st) + lane * dpl * 2;       // pages are contiguous in a stage
-        const uint32_t vbase = kbase + ppg * PS * rowb;
-        for (int jb = cw; jb < nt; jb += NCW * 8) {
-          float s[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int tl = jb + NCW * j;
-            float kf[4] = {0.f, 0.f, 0.f, 0.f};
-            if (tl < nt) {
-              if (tl == newtl) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (i < dpl) kf[i] = kn_s[lane * dpl + i];
-              } else if (dpl == 4) {
-                const uint2 u = lds64(kbase + tl * rowb);
-                kf[0] = bf_lo(u.x); kf[1] = bf_hi(u.x); kf[2] = bf_lo(u.y); kf[3] = bf_hi(u.y);
-              } else {
-                const uint32_t u = lds32(kbase + tl * rowb);
-                kf[0] = bf_lo(u); kf[1] = bf_hi(u);
-              }
-            }
-            float part[8];
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-              part[h] = fmaf(qr[h][3], kf[3], fmaf(qr[h][2], kf[2], fmaf(qr[h][1], kf[1], qr[h][0] * kf[0])));
-            const float sv = reduce8(part, lane);
-            s[j] = (tl < nt && hl < G) ? sv : -INFINITY;
+      if (st && has_new && pos / PS >= pg && pos / PS < pg + npg) {
+        // put the new token's K and V into its stage slot before anyone reads the
+        // page, and zero the page's later slots: they hold no token yet, and
+        // although their scores are masked, their V still enters the P.V product
+        // (0 * NaN would poison the output)
+        cbar();
+        const int pi = pos / PS - pg, slot = pos % PS;
+        uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
+        uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
+        for (int i = ct; i < d * PS; i += NCT) {
+          const int dim = i / PS, sl = i - dim * PS;
+          if (sl == slot) {
+            kp[i] = f2bf(kn_s[dim]);
+            vp[i] = f2bf(vn_s[dim]);
+          } else if (sl > slot) {
+            kp[i] = 0;
+            vp[i] = 0;
           }
-          float bm = s[0];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        cbar();
+      } else if (has_new && pos / PS >= pg && pos / PS < pg + npg) {
+        cbar();
+        cbar();
+      }
+      if (st && grp < npg) {
+        const int P = pg + grp;                    // global page index of this warp's page
+        const int nvalid = min(PS, tok1 - P * PS); // tokens of the page inside the chunk
+        const uint32_t kpage = smem_u32(st) + grp * PB;
+        const uint32_t vpage = kpage + ppg * PB;
+        // S = K . Q^T : A tiles of K^T-stored rows via ldmatrix.trans
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        const int li = lane >> 3, lr = lane & 7;
 #pragma unroll
-          for (int j = 1; j < 8; ++j) bm = fmaxf(bm, s[j]);
-          const float mnew = fmaxf(mrun, bm);
-          float sc = 1.f, pj[8];
-          if (mnew == -INFINITY) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pj[j] = 0.f;
-          } else {
-            sc = exp2f(mrun - mnew);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pj[j] = exp2f(s[j] - mnew);
+        for (int ks = 0; ks < 8; ++ks) {
+          if (ks < nks) {
+            const uint32_t addr = kpage + (uint32_t)((ks * 16 + (li >> 1) * 8 + lr) * PS * 2 + (li & 1) * 16);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(addr, a0, a1, a2, a3);
+            mma_bf16(s, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+            mma_bf16(s, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
           }
-          float psum = 0.f;
+        }
+        // s[0]: (tok gq, head 2tq) s[1]: (tok gq, head 2tq+1) s[2]/s[3]: tok gq+8
+        if (gq >= nvalid) { s[0] = -INFINITY; s[1] = -INFINITY; }
+        if (gq + 8 >= nvalid) { s[2] = -INFINITY; s[3] = -INFINITY; }
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) psum += pj[j];
-          lrun = lrun * sc + psum;
-          mrun = mnew;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, off));
+        }
+        const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+        const float sc0 = exp2f(mr0 - mn0), sc1 = exp2f(mr1 - mn1);   // 0 on the first page
+        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+        float ps0 = p0 + p2, ps1 = p1 + p3;
 #pragma unroll
-          for (int h = 0; h < MAX_G; ++h) {
-            const float sch = __shfl_sync(FULL, sc, h * 4);
+        for (int off = 4; off < 32; off <<= 1) {
+          ps0 += __shfl_xor_sync(FULL, ps0, off);
+          ps1 += __shfl_xor_sync(FULL, ps1, off);
+        }
+        lr0 = lr0 * sc0 + ps0;
+        lr1 = lr1 * sc1 + ps1;
+        mr0 = mn0;
+        mr1 = mn1;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[h][i] *= sch;
+        for (int mt = 0; mt < 4; ++mt) {
+          o[mt][0] *= sc0; o[mt][1] *= sc1; o[mt][2] *= sc0; o[mt][3] *= sc1;
+        }
+        // P^T as mma B operand: element (tok k, head n) packed per token pair;
+        // store [hi/lo][head][tok/2] as bf16x2 words
+        __syncwarp();
+        {
+          uint16_t* ph = reinterpret_cast<uint16_t*>(myp);
+          uint16_t* pl = reinterpret_cast<uint16_t*>(myp + 64);
+          const float pv[4] = {p0, p1, p2, p3};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int head = 2 * tq + (e & 1), tok = gq + 8 * (e >> 1);
+            const uint16_t hb = f2bf(pv[e]);
+            ph[head * 16 + tok] = hb;
+            pl[head * 16 + tok] = f2bf(pv[e] - bf2f(hb));
           }
+        }
+        __syncwarp();
+        const uint32_t bh0 = myp[gq * 8 + tq], bh1 = myp[gq * 8 + tq + 4];
+        const uint32_t bl0 = myp[64 + gq * 8 + tq], bl1 = myp[64 + gq * 8 + tq + 4];
+        // O^T += V^T . P^T over this warp's row tiles (dims)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int tl = jb + NCW * j;
-            if (tl < nt) {
-              float vf[4] = {0.f, 0.f, 0.f, 0.f};
-              if (tl == newtl) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (i < dpl) vf[i] = vn_s[lane * dpl + i];
-              } else if (dpl == 4) {
-                const uint2 u = lds64(vbase + tl * rowb);
-                vf[0] = bf_lo(u.x); vf[1] = bf_hi(u.x); vf[2] = bf_lo(u.y); vf[3] = bf_hi(u.y);
-              } else {
-                const uint32_t u = lds32(vbase + tl * rowb);
-                vf[0] = bf_lo(u); vf[1] = bf_hi(u);
-              }
-#pragma unroll
-              for (int h = 0; h < MAX_G; ++h) {
-                const float ph = __shfl_sync(FULL, pj[j], h * 4);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[h][i] = fmaf(ph, vf[i], acc[h][i]);
-              }
-            }
+        for (int mt = 0; mt < 4; ++mt) {
+          if (mt < mtw) {
+            const int m0 = (sub * mtw + mt) * 16;
+            const uint32_t addr = vpage + (uint32_t)((m0 + (li & 1) * 8 + lr) * PS * 2 + (li >> 1) * 16);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
           }
         }
       }
       release_stage(ab);
     }
     mark(TR_STAGES);
-    // merge the 8 warps' partial softmax states of this chunk
+    // merge the page groups' partial softmax states of this chunk
+    const int ngrp = ppg;
     if (!ab) {
-      if ((lane & 3) == 0 && hl < G) {
-        mrg[(cw * G + hl) * RS + d] = mrun;
-        mrg[(cw * G + hl) * RS + d + 1] = lrun;
+      if (sub == 0 && gq == 0) {
+        if (2 * tq < G) {
+          mrg[(grp * G + 2 * tq) * RS + d] = mr0;
+          mrg[(grp * G + 2 * tq) * RS + d + 1] = lr0;
+        }
+        if (2 * tq + 1 < G) {
+          mrg[(grp * G + 2 * tq + 1) * RS + d] = mr1;
+          mrg[(grp * G + 2 * tq + 1) * RS + d + 1] = lr1;
+        }
       }
 #pragma unroll
-      for (int h = 0; h < MAX_G; ++h)
-        if (h < G)
+      for (int mt = 0; mt < 4; ++mt) {
+        if (mt < mtw) {
+          const int m0 = (sub * mtw + mt) * 16;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < dpl) mrg[(cw * G + h) * RS + lane * dpl + i] = acc[h][i];
+          for (int e = 0; e < 4; ++e) {
+            const int head = 2 * tq + (e & 1), dim = m0 + gq + 8 * (e >> 1);
+            if (head < G) mrg[(grp * G + head) * RS + dim] = o[mt][e];
+          }
+        }
+      }
     }
     ab = cbar_or(ab);
     if (ab) return ab;
     const int nslots = p.part_slots;
     float* part = p.part + ((size_t)l * nslots + t.a[4]) * G * RS;
+    const int ngrp_used = min(ngrp, pg1 - pg0);    // groups that saw at least one page
     for (int idx = ct; idx < G * d; idx += NCT) {
       const int h = idx / d, i = idx - h * d;
       float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
+      for (int w = 0; w < ngrp_used; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
       float Ls = 0.f, A = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) {
+      for (int w = 0; w < ngrp_used; ++w) {
         const float mw = mrg[(w * G + h) * RS + d];
         if (mw != -INFINITY) {
           const float f = exp2f(mw - M);

@@ -313,7 +313,8 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   // shared-memory plan (same rule as mk_plan_create)
   const int nqd = s.nq * s.d;
   long long A1 = (long long)B * (s.H > nqd ? (s.H > s.F ? s.H : s.F) : (nqd > s.F ? nqd : s.F));
-  long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4);
+  long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4) +
+                       mk::NCW * 128;  // q, new K/V, page-group states, P scratch
   long long Ah = (long long)B * s.k * s.F;
   const int allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
   long long act = A1 > A3 ? A1 : A3;
@@ -329,6 +330,11 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   long long nst = avail / sb;
   if (nst > mk::MAX_STAGES) nst = mk::MAX_STAGES;
   if (nst < 2) return fail(MK_ERR_UNSUPPORTED, "shape leaves no room for the shared-memory ring");
+  {
+    const int ppg = sb / (2 * s.ps * s.d * 2) < 1 ? 1 : sb / (2 * s.ps * s.d * 2);
+    if (mk::NCW % ppg != 0 || (s.d / 16) / (mk::NCW / ppg) > 4)
+      return fail(MK_ERR_UNSUPPORTED, "attention page split does not fit this stage size");
+  }
   const int smem = (int)((size_t)nst * sb + act_bytes + misc);
   if (mk::max_active_ctas(nb, smem) < 1) return fail(MK_ERR_CUDA, "megakernel does not fit on an SM");
 

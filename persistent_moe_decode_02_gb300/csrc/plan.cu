@@ -553,7 +553,8 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   // shared-memory budget: activations + misc, the rest is the weight ring
   const int nqd = s.nq * s.d;
   const long long A1 = (long long)bcap * std::max(std::max(s.H, nqd), s.F);
-  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4);
+  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4) +
+                       mk::NCW * 128;  // q, new K/V, page-group states, P scratch
   const long long Ah = (long long)bcap * s.k * s.F;
   p->allh = (Ah * 4 <= 64 * 1024) ? 1 : 0;
   p->act_floats = (int)std::max(std::max(A1, A3), p->allh ? Ah : 0LL);
@@ -568,6 +569,11 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   while (sb < need) sb *= 2;
   int nst = (int)std::min<long long>(mk::MAX_STAGES, avail / sb);
   if (nst < 2) return fail(MK_ERR_UNSUPPORTED);
+  {
+    // attention: the warps split a stage's pages evenly, at most 4 output row tiles each
+    const int ppg = std::max(1, sb / (2 * s.ps * s.d * 2));
+    if (mk::NCW % ppg != 0 || (s.d / 16) / (mk::NCW / ppg) > 4) return fail(MK_ERR_UNSUPPORTED);
+  }
   p->stage_bytes = sb;
   p->nstages = nst;
   p->smem = (int)((size_t)nst * sb + act_bytes + misc);
@@ -750,9 +756,10 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
 int mk_plan_sync(mk_plan* p, mk_stream stream) {
   if (!p) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(p->h_status, p->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MK_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(p->h_status, p->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return note_cuda(e, "mk_plan_sync status copy");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return note_cuda(e, "mk_plan_sync");
   return p->h_status[0];
 }
 

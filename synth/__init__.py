@@ -117,10 +117,11 @@ def uniform_ints(n: int, hi: int, seed: int, name: str, start: int = 0) -> torch
 def fill_kv_paged_(pool: torch.Tensor, page_table: torch.Tensor, n_tok: int, seed: int,
                    name: str) -> None:
     """Write the first n_tok logical K (or V) rows of one request/layer into a
-    paged pool [num_pages, nkv, page_size, d] through its page table."""
+    paged pool [num_pages, nkv, d, page_size] (each page stores its block
+    transposed, one row per dimension) through its page table."""
     assert pool.dtype == torch.bfloat16 and pool.is_contiguous() and pool.dim() == 4
     assert page_table.dtype == torch.int32 and page_table.device == pool.device
-    _, nkv, ps, d = pool.shape
+    _, nkv, d, ps = pool.shape
     need = (n_tok + ps - 1) // ps
     assert page_table.numel() >= need
     rc = _L().synth_fill_kv_paged(ctypes.c_void_p(pool.data_ptr()),

@@ -81,11 +81,14 @@ class PagedKV:
     batch: which physical pages each request holds (seeded shuffled free list)."""
 
     def __init__(self, D: Dims, num_pages: int, max_pages: int, seed: int = 0, device: str = "cuda",
-                 perm_salt: int = 0):
+                 perm_salt: int = 0, poison: bool = False):
         self.D, self.seed, self.max_pages, self.num_pages = D, seed, max_pages, num_pages
-        shape = (num_pages, D.n_kv_heads, D.page_size, D.head_dim)
+        shape = (num_pages, D.n_kv_heads, D.head_dim, D.page_size)   # pages hold [d, slot] blocks
         self.k = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(D.n_layers)]
         self.v = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(D.n_layers)]
+        if poison:   # NaN everywhere no token was written: unused slots must never matter
+            for t in self.k + self.v:
+                t.fill_(float("nan"))
         self.free = [int(x) for x in page_permutation(num_pages, seed, perm_salt)]
         self._rng = np.random.Generator(np.random.PCG64([seed, 7]))
         self.device = device

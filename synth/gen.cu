@@ -21,7 +21,8 @@ __global__ void k_fill_uniform(int32_t* out, int64_t n, syn_keys k, int64_t star
 }
 
 // Element (pos, g, e) of a request's logical [n_tok, nkv, d] cache goes to
-// pool[page_table[pos / ps]][g][pos % ps][e].
+// pool[page_table[pos / ps]][g][e][pos % ps] (each page holds its head's
+// [d, page_size] block transposed: one row per dimension).
 __global__ void k_fill_kv_paged(uint16_t* pool, const int32_t* page_table, int64_t n_tok, int nkv,
                                 int ps, int d, syn_keys k, double scale) {
   int64_t n = n_tok * nkv * d;
@@ -32,7 +33,7 @@ __global__ void k_fill_kv_paged(uint16_t* pool, const int32_t* page_table, int64
     int64_t g = (i / d) % nkv;
     int64_t pos = i / ((int64_t)d * nkv);
     int64_t page = page_table[pos / ps];
-    int64_t dst = ((page * nkv + g) * ps + pos % ps) * d + e;
+    int64_t dst = ((page * nkv + g) * d + e) * ps + pos % ps;
     pool[dst] = syn_normal_bf16(k, (uint64_t)i, 0.0, scale);
   }
 }
@@ -77,7 +78,7 @@ int synth_fill_uniform_int(int32_t* out, int64_t n, uint64_t seed, uint32_t stre
 }
 
 // page_table: n_pages_used entries covering positions [0, n_tok); device pointer
-// when on_device, host pointer otherwise.
+// when on_device, host pointer otherwise.  Pool layout [pages][nkv][d][page_size].
 int synth_fill_kv_paged(void* pool, const int32_t* page_table, int64_t n_tok, int nkv, int page_size,
                         int d, uint64_t seed, uint32_t stream, double scale, int on_device,
                         void* cuda_stream) {
@@ -96,7 +97,7 @@ int synth_fill_kv_paged(void* pool, const int32_t* page_table, int64_t n_tok, in
     int64_t g = (i / d) % nkv;
     int64_t pos = i / ((int64_t)d * nkv);
     int64_t page = page_table[pos / page_size];
-    p[((page * nkv + g) * page_size + pos % page_size) * d + e] =
+    p[((page * nkv + g) * d + e) * page_size + pos % page_size] =
         syn_normal_bf16(k, (uint64_t)i, 0.0, scale);
   }
   return 0;

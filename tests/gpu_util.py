@@ -47,7 +47,7 @@ class GpuRun:
     """A workload's model, paged cache and plan on cuda:0."""
 
     def __init__(self, wl: synth.Workload, steps: Optional[int] = None, model: Optional[DeviceModel] = None,
-                 rids: Optional[List[int]] = None, perm_salt: int = 0, **plan_kw):
+                 rids: Optional[List[int]] = None, perm_salt: int = 0, poison: bool = False, **plan_kw):
         from persistent_moe_decode_02_gb300 import mk
         D = wl.dims
         self.wl, self.D = wl, D
@@ -56,7 +56,7 @@ class GpuRun:
         ps = D.page_size
         max_pages = max((c + self.steps + 1 + ps - 1) // ps for c in wl.ctx) + 1
         num_pages = kv_pages_needed(D, wl.ctx, self.steps) + 4
-        self.kv = PagedKV(D, num_pages, max_pages, wl.seed, perm_salt=perm_salt)
+        self.kv = PagedKV(D, num_pages, max_pages, wl.seed, perm_salt=perm_salt, poison=poison)
         rids = list(range(wl.batch)) if rids is None else rids
         self.reqs = [self.kv.admit(rid, c, self.steps + 1) for rid, c in zip(rids, wl.ctx)]
         self.max_pages = max_pages
@@ -82,7 +82,7 @@ class GpuRun:
             self.plan.read_debug(mk.MK_DBG_EXPERT_IDS, ids)
             self.plan.read_debug(mk.MK_DBG_ROUTER_LOGITS, rl)
         st = self.plan.sync()
-        assert st == 0, f"device status {st}: {mk.status_string(st)}"
+        assert st == 0, f"device status {st}: {mk.status_string(st)} {mk.lib().mk_last_error().decode()}"
         if capture:
             rec = StepRecord(tok_in.cpu(), nxt.cpu(), lg.cpu() if lg is not None else None, hid.cpu(),
                              ids.cpu().long(), rl.cpu(), [r.rid for r in self.reqs])
@@ -182,10 +182,10 @@ class OracleReplay:
 
 def run_and_check(wl: synth.Workload, steps: int, oracle_steps: Optional[int] = None,
                   requests: Optional[List[int]] = None, n_layers: Optional[int] = None,
-                  cache_prior: bool = True, **plan_kw) -> Report:
+                  cache_prior: bool = True, poison: bool = False, **plan_kw) -> Report:
     """Run `steps` GPU steps, replay the first `oracle_steps` of the chosen
     requests in the oracle; returns the report (not yet asserted)."""
-    run = GpuRun(wl, steps=steps, **plan_kw)
+    run = GpuRun(wl, steps=steps, poison=poison, **plan_kw)
     oracle_steps = steps if oracle_steps is None else oracle_steps
     recs = [run.step(capture=(s < oracle_steps)) for s in range(steps)]
     requests = list(range(wl.batch)) if requests is None else requests

@@ -47,6 +47,14 @@ def test_tiny_empty_prior_context():
     rep.assert_ok()
 
 
+def test_unwritten_cache_slots_never_matter():
+    # pools full of NaN wherever no token was written (dirty memory): partial
+    # last pages and free pages must not leak into any result
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 37, 0], steps=5)
+    rep = run_and_check(wl, steps=5, poison=True)
+    rep.assert_ok()
+
+
 def test_mid_16_steps():
     wl = synth.workload("mid")
     rep = run_and_check(wl, steps=wl.steps)

@@ -37,11 +37,11 @@ def test_kv_paged_placement_matches_logical_cpu():
     D = TINY
     n = 100
     pt = torch.from_numpy(synth.page_permutation(12, 0))
-    pool = torch.zeros(12, D.n_kv_heads, D.page_size, D.head_dim, dtype=torch.bfloat16)
+    pool = torch.zeros(12, D.n_kv_heads, D.head_dim, D.page_size, dtype=torch.bfloat16)
     synth.fill_kv_paged_(pool, pt, n, 0, synth.kv_name(3, 1, "K"))
     k, _ = synth.prior_kv(D, 0, 3, 1, n)
     for pos in range(n):
-        got = pool[pt[pos // D.page_size], :, pos % D.page_size, :]
+        got = pool[pt[pos // D.page_size], :, :, pos % D.page_size]
         assert torch.equal(got.view(torch.int16), k[pos].view(torch.int16))
 
 
@@ -60,7 +60,7 @@ def test_host_and_device_bits_identical():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     D = TINY
     pt = torch.from_numpy(synth.page_permutation(12, 0))
-    pc = torch.zeros(12, D.n_kv_heads, D.page_size, D.head_dim, dtype=torch.bfloat16)
+    pc = torch.zeros(12, D.n_kv_heads, D.head_dim, D.page_size, dtype=torch.bfloat16)
     pg = pc.cuda()
     synth.fill_kv_paged_(pc, pt, 150, 0, "kvcmp")
     synth.fill_kv_paged_(pg, pt.cuda(), 150, 0, "kvcmp")

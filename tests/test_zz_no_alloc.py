@@ -71,7 +71,7 @@ def test_noalloc_rejects_oversized_step(built):
                   "lm_head": torch.zeros(8, device="cuda")}
     for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down"):
         model_like[k] = [torch.zeros(8, device="cuda")] * D.n_layers
-    pools = [torch.zeros(1 << 16, D.n_kv_heads, D.page_size, D.head_dim, dtype=torch.bfloat16, device="cuda")]
+    pools = [torch.zeros(1 << 16, D.n_kv_heads, D.head_dim, D.page_size, dtype=torch.bfloat16, device="cuda")]
     ctx = 600000
     pages = (ctx + D.page_size) // D.page_size
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
