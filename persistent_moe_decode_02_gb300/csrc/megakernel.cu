@@ -731,15 +731,35 @@ struct Consumer {
             for (int q = 0; q < 8; ++q)
 #pragma unroll
               for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
+            if constexpr (NB <= 2) {
+              for (int gi = lane; gi < ng; gi += 32) {
+                float4 x0[NB], x1[NB];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
-              if (row < n) {
-                for (int gi = lane; gi < ng; gi += 32) {
-                  const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
+                for (int j = 0; j < NB; ++j) {
+                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-                  for (int j = 0; j < NB; ++j)
-                    if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                for (int q = 0; q < 8; ++q) {
+                  const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
+                  if (row < n) {
+                    const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv, x0[j], x1[j]);
+                  }
+                }
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
+                if (row < n) {
+                  for (int gi = lane; gi < ng; gi += 32) {
+                    const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
+#pragma unroll
+                    for (int j = 0; j < NB; ++j)
+                      if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                  }
                 }
               }
             }
@@ -769,11 +789,10 @@ struct Consumer {
     return ab;
   }
 
-  // End of a task: make this thread's writes visible, agree on failure.
-  __device__ bool finish(bool ab) {
-    __threadfence();
-    return cbar_or(ab);
-  }
+  // End of a task: agree on failure.  The barrier orders every consumer
+  // thread's writes before thread 0's release (atom.release.gpu is cumulative),
+  // so the signal publishes them without a fence in every thread.
+  __device__ bool finish(bool ab) { return cbar_or(ab); }
 
   __device__ void signal(int ctr) {
     if (ct == 0) atom_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
@@ -786,26 +805,24 @@ struct Consumer {
       m->ticket_last = (old == p.epoch * n - 1u) ? 1 : 0;
     }
     cbar();
-    const bool last = m->ticket_last != 0;
-    if (last) __threadfence();
-    return last;
+    return m->ticket_last != 0;
   }
 
   // Routing of layer l (written by that layer's router finisher) into smem;
   // the caller's next barrier publishes it.  Returns the distinct-expert count.
   __device__ int load_route(int l) {
     const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
     const int umax = p.rm.umax, bc = p.rm.bcap;
-    for (int i = ct; i < U; i += NCT) {
+    // fixed bounds, so every load is in flight at once (entries past U are unused)
+    for (int i = ct; i < umax; i += NCT) {
       m->r_exp[i] = __ldcg(rt + 1 + i);
       m->r_cnt[i] = __ldcg(rt + 1 + umax + i);
     }
-    for (int i = ct; i < U * bc; i += NCT) {
+    for (int i = ct; i < umax * bc; i += NCT) {
       m->r_tok[i] = __ldcg(rt + 1 + 2 * umax + i);
       m->r_rank[i] = __ldcg(rt + 1 + 2 * umax + umax * bc + i);
     }
-    return U;
+    return __ldcg(rt);
   }
 
   // ------------------------------------------------------------ tasks
@@ -931,6 +948,7 @@ struct Consumer {
 
   __device__ bool router(const Task& t, bool ab) {
     const int l = t.layer;
+    // (the finisher below publishes act = rmsnorm(x_mid) * gamma for the gate/up tasks)
     if (!ab) fill_ffn_norm(l);
     cbar();
     mark(TR_ACT);
@@ -941,6 +959,11 @@ struct Consumer {
     ab = finish(ab);
     if (ab) return ab;
     if (ticket(p.cm.rticket + l, (uint32_t)t.a[2])) {
+      {
+        float4* dst = reinterpret_cast<float4*>(p.xnf + (size_t)l * p.bcap * p.H);
+        const float4* src = reinterpret_cast<const float4*>(act);
+        for (int i = ct; i < (p.B * p.H) >> 2; i += NCT) dst[i] = src[i];
+      }
       route_finish(l);
       ab = finish(false);
       if (!ab) signal(p.cm.rdone + l);
@@ -952,10 +975,12 @@ struct Consumer {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
     if (!ab) {
-      fill_ffn_norm(l);
       U = load_route(l);
+      const float4* src = reinterpret_cast<const float4*>(p.xnf + (size_t)l * p.bcap * H);
+      float4* dst = reinterpret_cast<float4*>(act);
+#pragma unroll 4
+      for (int i = ct; i < (p.B * H) >> 2; i += NCT) dst[i] = __ldcg(src + i);
     }
-    U = __shfl_sync(FULL, U, 0);
     cbar();
     mark(TR_ACT);
     long long q0, q1;
@@ -1169,7 +1194,7 @@ struct Consumer {
         const uint32_t kpage = smem_u32(st) + grp * PB;
         const uint32_t vpage = kpage + ppg * PB;
         // S = K . Q^T : A tiles of K^T-stored rows via ldmatrix.trans
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
         const int li = lane >> 3, lr = lane & 7;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -1178,9 +1203,11 @@ struct Consumer {
             uint32_t a0, a1, a2, a3;
             ldsm_x4_trans(addr, a0, a1, a2, a3);
             mma_bf16(s, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
-            mma_bf16(s, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+            mma_bf16(sl, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
           }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] += sl[e];
         // s[0]: (tok gq, head 2tq) s[1]: (tok gq, head 2tq+1) s[2]/s[3]: tok gq+8
         if (gq >= nvalid) { s[0] = -INFINITY; s[1] = -INFINITY; }
         if (gq + 8 >= nvalid) { s[2] = -INFINITY; s[3] = -INFINITY; }

@@ -119,6 +119,7 @@ struct Params {
   float* o;             // [L][bcap][nq*d]
   float* x_mid;         // [L][bcap][H]
   float* x_out;         // [L][bcap][H]
+  float* xnf;           // [L][bcap][H] rmsnorm(x_mid) * ffn gain, published by the router finisher
   float* rlog;          // [L][bcap][E]
   int* ids;             // [L][bcap][k]
   float* gates;         // [L][bcap][k]

@@ -296,6 +296,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_o = dc.take(L * B * s.nq * s.d * sizeof(float));
   const size_t d_xm = dc.take(L * B * s.H * sizeof(float));
   const size_t d_xo = dc.take(L * B * s.H * sizeof(float));
+  const size_t d_xn = dc.take(L * B * s.H * sizeof(float));
   const size_t d_rl = dc.take(L * B * s.E * sizeof(float));
   const size_t d_ids = dc.take(L * B * s.k * sizeof(int));
   const size_t d_gt = dc.take(L * B * s.k * sizeof(float));
@@ -419,6 +420,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.o = (float*)(base + d_o);
   P.x_mid = (float*)(base + d_xm);
   P.x_out = (float*)(base + d_xo);
+  P.xnf = (float*)(base + d_xn);
   P.rlog = (float*)(base + d_rl);
   P.ids = (int*)(base + d_ids);
   P.gates = (float*)(base + d_gt);

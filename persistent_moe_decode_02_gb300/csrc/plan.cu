@@ -631,6 +631,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   ok &= dalloc(p, &P.o, L * bcap * nqd * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_mid, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_out, L * bcap * s.H * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.xnf, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.rlog, L * bcap * s.E * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.ids, L * bcap * s.k * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &P.gates, L * bcap * s.k * sizeof(float)) == cudaSuccess;
