@@ -101,7 +101,13 @@ typedef struct mk_plan_opts {
   int debug_drop_task; /* test hook: >0 removes task (value-1) from the list so its
                           counter never fires and the step returns MK_ERR_DEP_TIMEOUT;
                           0 in production */
-  int trace;         /* 1: record a per-task timeline every step (MK_DBG_TRACE) */
+  int trace;         /* 1: record a per-task timeline every step (MK_DBG_TRACE); 2: also a
+                        per-stage timeline (MK_DBG_STAGE_TRACE) */
+  int l2_ahead;      /* while its ring is full, the producer prefetches up to this many later
+                        stages into L2; <= 0 -> off (the default), at most 64 */
+  int l2_wait;       /* stages of the following routing-independent tasks prefetched into
+                        L2 while a gate/up or down task waits for routing; <= 0 -> off (the
+                        default), at most 64 */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;
@@ -158,9 +164,15 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  *   MK_DBG_TRACE         uint64 [num_tasks, 10]          globaltimer stamps (ns) per task:
  *                        consumer fetched, dependency met, activations ready, stages
  *                        consumed, done; producer first copy, last copy, start;
- *                        first and last stage landed (needs opts.trace) */
+ *                        first and last stage landed (needs opts.trace)
+ *   MK_DBG_STAGE_TRACE   uint64 [num_ctas, 4096, 6]      per CTA, its ring stages in order:
+ *                        copy issued, landed (seen by the first consumer warp), released
+ *                        (globaltimer ns, 0 = not reached), the task index, and the SM's
+ *                        clock64 at landed and released (needs opts.trace = 2; stages past
+ *                        4096 are not recorded) */
 enum { MK_DBG_HIDDEN = 1, MK_DBG_EXPERT_IDS = 2, MK_DBG_GATES = 3, MK_DBG_ROUTER_LOGITS = 4,
-       MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6, MK_DBG_TASKS = 7, MK_DBG_TRACE = 8 };
+       MK_DBG_SEQ_LENS = 5, MK_DBG_UNION = 6, MK_DBG_TASKS = 7, MK_DBG_TRACE = 8,
+       MK_DBG_STAGE_TRACE = 9 };
 int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stream stream);
 
 /* Describe the current plan (host-side numbers): writes up to `n` ints:

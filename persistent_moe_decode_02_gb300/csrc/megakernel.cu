@@ -54,6 +54,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Non-blocking probe: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -143,6 +155,11 @@ __device__ __forceinline__ Task ldg_task(const Task* t) {
   return r;
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
@@ -207,8 +224,13 @@ __device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
 
 // ------------------------------------------------------------------ shared state
 
-constexpr int WIN_ROWS = 32;                     // rows per cross-warp partial-sum window
 constexpr int MAX_UNION = MAX_BATCH * MAX_TOPK;   // distinct experts a step can select
+
+// A layer's distinct experts as the producer sees them.
+struct RouteCache {
+  int layer, U;
+  int exp[MAX_UNION];
+};
 
 struct Misc {
   uint64_t full[MAX_STAGES];
@@ -230,8 +252,8 @@ struct Misc {
   int r_tok[MAX_UNION * MAX_BATCH];
   int r_rank[MAX_UNION * MAX_BATCH];
   int r_row[MAX_UNION * MAX_BATCH];   // act row of (slot, i) in the down task
-  // per-warp partial sums of wide-row GEMVs, two windows of WIN_ROWS rows
-  float psum[2][NCW * WIN_ROWS * MAX_BATCH];
+  // the producer's copies of a layer's distinct experts, one per cursor
+  RouteCache cp_route, pf_route;
 };
 
 struct Ring {
@@ -332,21 +354,231 @@ __device__ __forceinline__ const int* route_of(const Params& p, int l) {
 
 // ------------------------------------------------------------------ producer
 
+// The producer's view of one task: how many ring stages it fills and where
+// each stage's bytes come from.  The consumer walks the same geometry.
+struct Geo {
+  int type, nst, l;
+  // row tasks
+  const uint16_t* W;
+  int K, r0, r1, rps;
+  // attention
+  int pg0, pg1, ppg, b, g;
+  uint32_t PB;
+  // gate/up and down: the routing cache the task reads
+  const RouteCache* rc;
+  long long q0, q1;
+  int pps, spe;
+};
+
+// Producer: one thread that walks the CTA's tasks and fills the ring.  It
+// keeps two cursors over the same sequence of stages: the copy cursor (bulk
+// copies into the ring, paced by the consumers' releases) and a prefetch
+// cursor that pulls later stages into L2.  The prefetch cursor moves only
+// while the copy cursor is blocked -- on a full ring (the consumers wait for
+// a dependency) or on a layer's routing -- so prefetch requests never compete
+// with copies that the consumers are waiting for, and the bytes have time to
+// land before they are copied.  It runs at most pf_ahead stages past the copy
+// cursor.  While the copy cursor waits for routing, the routing-independent
+// tasks that follow (the next layer's projections and attention) are
+// prefetched instead, up to pf_wait stages.
 struct Producer {
   const Params& p;
   Ring r;
   uint64_t pol;
   int ti = 0;
   bool first = true;
+  // prefetch cursor: task pj, next stage pst, linear stage positions
+  int pj = 0, pst = 0, t_end = 0;
+  bool pvalid = false;
+  Geo pg;
+  long long cp_lin = 0, pf_lin = 0;
 
   __device__ void mark(int k) {
     if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
   }
 
-  // Claim the next stage (waiting for its release) and arm it for `bytes`.
-  __device__ bool open(uint32_t bytes, uint8_t*& dst, uint64_t*& bar) {
+  // Routing of layer l into cache c (once per layer).  wait: block (bounded)
+  // for the router; otherwise return false if it has not finished.
+  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task) {
+    if (c->layer == l) return true;
+    if (!wait) {
+      if ((int32_t)(ld_acquire(p.ctr + (size_t)(p.cm.rdone + l) * CTR_STRIDE) - p.epoch) < 0) return false;
+    } else if (!wait_ctr(p, p.cm.rdone + l, 1, task)) {
+      return false;
+    }
+    const int* rt = route_of(p, l);
+    const int U = __ldcg(rt);
+    for (int u = 0; u < U; ++u) c->exp[u] = __ldcg(rt + 1 + u);
+    c->U = U;
+    c->layer = l;
+    return true;
+  }
+
+  // Geometry of task t; false when its routing is not known (and wait is
+  // off), on a wait that timed out, or for an unknown task type.
+  __device__ bool geo(const Task& t, Geo& q, RouteCache* c, bool wait, int task) {
+    q.type = t.type;
+    q.l = t.layer;
+    const int l = t.layer;
+    switch (t.type) {
+      case T_QKV: case T_OPROJ: case T_ROUTER: case T_LM: {
+        q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : t.type == T_ROUTER ? p.router[l] : p.lm_head;
+        q.K = t.type == T_OPROJ ? p.nq * p.d : p.H;
+        q.r0 = t.a[0];
+        q.r1 = t.a[1];
+        q.rps = rows_per_stage(p, q.K);
+        q.nst = (q.r1 - q.r0 + q.rps - 1) / q.rps;
+        return true;
+      }
+      case T_ATTN: {
+        q.b = t.a[0];
+        q.g = t.a[1];
+        const int pos = __ldcg(p.seq_len + q.b);
+        int tok0, tok1;
+        attn_range(p, t, pos, tok0, tok1);
+        q.ppg = pages_per_stage(p);
+        q.PB = (uint32_t)p.ps * p.d * 2;
+        q.pg0 = tok0 / p.ps;
+        q.pg1 = (tok1 + p.ps - 1) / p.ps;
+        q.nst = (q.pg1 - q.pg0 + q.ppg - 1) / q.ppg;
+        return true;
+      }
+      case T_GU: {
+        if (!route_ready(c, l, wait, task)) return false;
+        q.rc = c;
+        gu_range(p, t, c->U, q.q0, q.q1);
+        q.pps = pairs_per_stage(p);
+        int n = 0;
+        for (long long x = q.q0; x < q.q1;) {
+          const int u = (int)(x / p.F);
+          const int fa = (int)(x - (long long)u * p.F);
+          const int fb = (int)min((long long)p.F, q.q1 - (long long)u * p.F);
+          n += (fb - fa + q.pps - 1) / q.pps;
+          x = (long long)(u + 1) * p.F;
+        }
+        q.nst = n;
+        return true;
+      }
+      case T_DOWN: {
+        if (!route_ready(c, l, wait, task)) return false;
+        q.rc = c;
+        q.r0 = t.a[0];
+        q.r1 = t.a[1];
+        q.rps = rows_per_stage(p, p.F);
+        q.spe = (q.r1 - q.r0 + q.rps - 1) / q.rps;
+        q.nst = c->U * q.spe;
+        return true;
+      }
+      default: return false;
+    }
+  }
+
+  // Calls f(src, bytes, dst_offset) for each contiguous piece of stage s.
+  template <class F>
+  __device__ void segs(const Geo& q, int s, F f) {
+    const int l = q.l;
+    switch (q.type) {
+      case T_QKV: case T_OPROJ: case T_ROUTER: case T_LM: {
+        const int s0 = q.r0 + s * q.rps;
+        const int n = min(q.rps, q.r1 - s0);
+        f(q.W + (size_t)s0 * q.K, (uint32_t)n * q.K * 2, 0u);
+        break;
+      }
+      case T_ATTN: {
+        const int pg = q.pg0 + s * q.ppg;
+        const int n = min(q.ppg, q.pg1 - pg);
+        const int* pt = p.page_table + (size_t)q.b * p.max_pages;
+        for (int i = 0; i < n; ++i) {
+          const size_t off = ((size_t)pt[pg + i] * p.nkv + q.g) * p.ps * p.d;
+          f(p.k_pool[l] + off, q.PB, (uint32_t)i * q.PB);
+          f(p.v_pool[l] + off, q.PB, (uint32_t)(q.ppg + i) * q.PB);
+        }
+        break;
+      }
+      case T_GU: {
+        const int F = p.F, H = p.H;
+        int left = s;
+        for (long long x = q.q0; x < q.q1;) {
+          const int u = (int)(x / F);
+          const int fa = (int)(x - (long long)u * F);
+          const int fb = (int)min((long long)F, q.q1 - (long long)u * F);
+          const int ns = (fb - fa + q.pps - 1) / q.pps;
+          if (left < ns) {
+            const int f0 = fa + left * q.pps;
+            const int n = min(q.pps, fb - f0);
+            const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[u] * 2 * F * H;   // rows 2f, 2f+1
+            f(We + (size_t)2 * f0 * H, (uint32_t)n * 2 * H * 2, 0u);
+            return;
+          }
+          left -= ns;
+          x = (long long)(u + 1) * F;
+        }
+        break;
+      }
+      case T_DOWN: {
+        const int u = s / q.spe, c = s - u * q.spe;
+        const int s0 = q.r0 + c * q.rps;
+        const int n = min(q.rps, q.r1 - s0);
+        const uint16_t* We = p.w_down[l] + (size_t)q.rc->exp[u] * p.H * p.F;
+        f(We + (size_t)s0 * p.F, (uint32_t)n * p.F * 2, 0u);
+        break;
+      }
+    }
+  }
+
+  __device__ void prefetch_stage(const Geo& q, int s) {
+    segs(q, s, [&](const void* src, uint32_t bytes, uint32_t) { prefetch_l2_bulk(src, bytes); });
+  }
+
+  // Move the prefetch cursor until it is pf_ahead stages past the copy
+  // cursor (at stage s of task ti, geometry q), it reaches a task whose
+  // routing is not known yet, or the list ends.
+  __device__ void run_prefetch(int ti, int s, const Geo& q) {
+    if (pf_lin < cp_lin) {   // behind the copy cursor: restart at its position
+      pj = ti;
+      pst = s;
+      pg = q;
+      pvalid = true;
+      pf_lin = cp_lin;
+    }
+    while (pf_lin < cp_lin + p.pf_ahead) {
+      if (!pvalid) {
+        if (pj >= t_end) return;
+        if (!geo(ldg_task(p.tasks + pj), pg, &r.m->pf_route, false, pj)) return;
+        pvalid = true;
+      }
+      if (pst >= pg.nst) {
+        ++pj;
+        pst = 0;
+        pvalid = false;
+        continue;
+      }
+      prefetch_stage(pg, pst);
+      ++pst;
+      ++pf_lin;
+    }
+  }
+
+  // While task ti waits for routing: prefetch up to pf_wait stages of the
+  // routing-independent tasks that follow it.
+  __device__ void prefetch_while_routing(int ti) {
+    int budget = p.pf_wait;
+    for (int tj = ti + 1; tj < t_end && budget > 0; ++tj) {
+      const Task t = ldg_task(p.tasks + tj);
+      if (t.type == T_GU || t.type == T_DOWN) continue;
+      Geo q;
+      if (!geo(t, q, nullptr, false, tj)) return;
+      for (int s = 0; s < q.nst && budget > 0; ++s, --budget) prefetch_stage(q, s);
+    }
+  }
+
+  // Claim the next stage (waiting for its release) and arm it for `bytes`;
+  // a blocked claim first lets the prefetch cursor run (stage s of task ti).
+  __device__ bool open(uint32_t bytes, uint8_t*& dst, uint64_t*& bar, int s, const Geo& q) {
     Misc* m = r.m;
-    if (!mbar_wait(p, m, &m->empty[r.stage], (r.round & 1) ^ 1, -3)) return false;
+    const uint32_t par = (r.round & 1) ^ 1;
+    if (p.pf_ahead > 0 && !mbar_test(&m->empty[r.stage], par)) run_prefetch(ti, s, q);
+    if (!mbar_wait(p, m, &m->empty[r.stage], par, -3)) return false;
     bar = &m->full[r.stage];
     dst = r.base + (size_t)r.stage * r.sb;
     m->armed[r.stage] = r.round;
@@ -358,119 +590,42 @@ struct Producer {
     return true;
   }
 
-  __device__ bool rows(const uint16_t* W, int K, int r0, int r1) {
-    const int rps = rows_per_stage(p, K);
-    for (int s0 = r0; s0 < r1; s0 += rps) {
-      const int n = min(rps, r1 - s0);
-      const uint32_t bytes = (uint32_t)n * K * 2;
-      uint8_t* dst;
-      uint64_t* bar;
-      if (!open(bytes, dst, bar)) return false;
-      bulk_g2s(dst, W + (size_t)s0 * K, bytes, bar, pol);
-      r.advance();
-    }
-    return true;
-  }
-
-  __device__ bool attn(const Task& t) {
-    const int l = t.layer, b = t.a[0], g = t.a[1];
-    const int pos = __ldcg(p.seq_len + b);
-    int tok0, tok1;
-    attn_range(p, t, pos, tok0, tok1);
-    const int ppg = pages_per_stage(p);
-    const uint32_t PB = (uint32_t)p.ps * p.d * 2;
-    const int pg1 = (tok1 + p.ps - 1) / p.ps;
-    const int* pt = p.page_table + (size_t)b * p.max_pages;
-    const uint16_t* kp = p.k_pool[l];
-    const uint16_t* vp = p.v_pool[l];
-    for (int pg = tok0 / p.ps; pg < pg1; pg += ppg) {
-      const int n = min(ppg, pg1 - pg);
-      uint8_t* dst;
-      uint64_t* bar;
-      if (!open(2u * n * PB, dst, bar)) return false;
-      for (int i = 0; i < n; ++i) {
-        const size_t off = ((size_t)pt[pg + i] * p.nkv + g) * p.ps * p.d;
-        bulk_g2s(dst + (size_t)i * PB, kp + off, PB, bar, pol);
-        bulk_g2s(dst + (size_t)(ppg + i) * PB, vp + off, PB, bar, pol);
-      }
-      r.advance();
-    }
-    return true;
-  }
-
-  __device__ bool gu(const Task& t, int ti) {
-    const int l = t.layer;
-    if (!wait_ctr(p, p.cm.rdone + l, 1, ti)) return false;
-    const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
-    long long q0, q1;
-    gu_range(p, t, U, q0, q1);
-    const int F = p.F, H = p.H, pps = pairs_per_stage(p);
-    const uint16_t* W = p.w_gate_up[l];
-    for (long long q = q0; q < q1;) {
-      const int u = (int)(q / F);
-      const int fa = (int)(q - (long long)u * F);
-      const int fb = (int)min((long long)F, q1 - (long long)u * F);
-      const int e = __ldcg(rt + 1 + u);
-      const uint16_t* We = W + (size_t)e * 2 * F * H;   // rows 2f (gate f), 2f + 1 (up f)
-      for (int f = fa; f < fb; f += pps) {
-        const int n = min(pps, fb - f);
-        const uint32_t bytes = (uint32_t)n * 2 * H * 2;
-        uint8_t* dst;
-        uint64_t* bar;
-        if (!open(bytes, dst, bar)) return false;
-        bulk_g2s(dst, We + (size_t)2 * f * H, bytes, bar, pol);
-        r.advance();
-      }
-      q = (long long)(u + 1) * F;
-    }
-    return true;
-  }
-
-  __device__ bool down(const Task& t, int ti) {
-    const int l = t.layer;
-    if (!wait_ctr(p, p.cm.rdone + l, 1, ti)) return false;
-    const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
-    const int r0 = t.a[0], r1 = t.a[1], F = p.F, H = p.H;
-    const int rps = rows_per_stage(p, F);
-    const uint16_t* W = p.w_down[l];
-    for (int u = 0; u < U; ++u) {
-      const int e = __ldcg(rt + 1 + u);
-      const uint16_t* We = W + (size_t)e * H * F;
-      for (int s0 = r0; s0 < r1; s0 += rps) {
-        const int n = min(rps, r1 - s0);
-        uint8_t* dst;
-        uint64_t* bar;
-        if (!open((uint32_t)n * F * 2, dst, bar)) return false;
-        bulk_g2s(dst, We + (size_t)s0 * F, (uint32_t)n * F * 2, bar, pol);
-        r.advance();
-      }
-    }
-    return true;
-  }
-
   __device__ void run(int t0, int t1) {
+    r.m->cp_route.layer = -1;
+    r.m->pf_route.layer = -1;
+    t_end = t1;
+    pj = t0;
     for (ti = t0; ti < t1; ++ti) {
       if (failed(p)) return;
-      const Task t = p.tasks[ti];
-      const int l = t.layer;
-      bool ok = true;
+      const Task t = ldg_task(p.tasks + ti);
       first = true;
       mark(TR_P_START);
-      switch (t.type) {
-        case T_QKV: ok = rows(p.wqkv[l], p.H, t.a[0], t.a[1]); break;
-        case T_ATTN: ok = attn(t); break;
-        case T_OPROJ: ok = rows(p.wo[l], p.nq * p.d, t.a[0], t.a[1]); break;
-        case T_ROUTER: ok = rows(p.router[l], p.H, t.a[0], t.a[1]); break;
-        case T_GU: ok = gu(t, ti); break;
-        case T_DOWN: ok = down(t, ti); break;
-        case T_LM: ok = rows(p.lm_head, p.H, t.a[0], t.a[1]); break;
-        default: set_error(p, MK_ERR_INVALID, ti, t.type); ok = false;
+      Geo q;
+      if (!geo(t, q, &r.m->cp_route, false, ti)) {
+        if (p.pf_wait > 0) prefetch_while_routing(ti);
+        if (!geo(t, q, &r.m->cp_route, true, ti)) {
+          if (t.type < T_QKV || t.type > T_LM) set_error(p, MK_ERR_INVALID, ti, t.type);
+          r.m->abort_flag = 1;
+          return;
+        }
       }
-      if (!ok) {
-        r.m->abort_flag = 1;
-        return;
+      for (int s = 0; s < q.nst; ++s) {
+        uint32_t bytes = 0;
+        segs(q, s, [&](const void*, uint32_t b, uint32_t) { bytes += b; });
+        uint8_t* dst;
+        uint64_t* bar;
+        if (!open(bytes, dst, bar, s, q)) {
+          r.m->abort_flag = 1;
+          return;
+        }
+        segs(q, s, [&](const void* src, uint32_t b, uint32_t off) { bulk_g2s(dst + off, src, b, bar, pol); });
+        if (p.strace && cp_lin < STRACE_CAP) {
+          unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + cp_lin) * STRACE_SLOTS;
+          rec[0] = gtimer();
+          rec[3] = (unsigned long long)ti;
+        }
+        r.advance();
+        ++cp_lin;
       }
       mark(TR_P_LAST);
     }
@@ -486,6 +641,7 @@ struct Consumer {
   float* act;
   Misc* m;
   float* ydown;
+  float* psum;   // per-warp partial sums of wide-row GEMVs: [2 windows][NCW][WIN_ROWS][NB]
   int ct, cw, lane;
   int ti = 0;
 
@@ -507,12 +663,22 @@ struct Consumer {
       mark(nstage_seen == 0 ? TR_S_FIRST : TR_S_LAST);
       ++nstage_seen;
     }
+    if (p.strace && ct == 0) stage_stamp(1);
     return r.base + (size_t)r.stage * r.sb;
   }
   __device__ void release_stage(bool ab) {
     __syncwarp();
     if (!ab && lane == 0) mbar_arrive(&m->empty[r.stage]);
+    if (p.strace && ct == 0) stage_stamp(2);
     r.advance();
+  }
+  __device__ void stage_stamp(int k) {
+    const long long lin = (long long)r.round * r.nst + r.stage;
+    if (lin < STRACE_CAP) {
+      unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + lin) * STRACE_SLOTS;
+      rec[k] = gtimer();
+      rec[3 + k] = (unsigned long long)clock64();
+    }
   }
 
   // ---- activations
@@ -672,7 +838,7 @@ struct Consumer {
                 }
               }
             }
-            float* ps = m->psum[buf] + (size_t)cw * WIN_ROWS * MAX_BATCH;
+            float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
               if (j < nb) {
@@ -681,7 +847,7 @@ struct Consumer {
                 for (int q = 0; q < 8; ++q) v[q] = part[q][j];
                 const float sum = reduce8(v, lane);
                 const int q = (lane >> 2) & 7;
-                if ((lane & 3) == 0 && rb + q < n) ps[(wrow + rb + q) * MAX_BATCH + j] = sum;
+                if ((lane & 3) == 0 && rb + q < n) ps[(wrow + rb + q) * NB + j] = sum;
               }
             }
           }
@@ -691,7 +857,7 @@ struct Consumer {
         if (wrow + rps > WIN_ROWS || s0 + rps >= r1) {
           cbar();
           if (!ab) {
-            const float* pb = m->psum[buf];
+            const float* pb = psum + (size_t)buf * NCW * WIN_ROWS * NB;
             const int units = PAIRS ? wrow >> 1 : wrow;
             for (int x = ct; x < units * nb; x += NCT) {
               const int u = x / nb, j = x - u * nb;
@@ -699,14 +865,14 @@ struct Consumer {
                 float g = 0.f, up = 0.f;
 #pragma unroll
                 for (int w = 0; w < NCW; ++w) {
-                  g += pb[((size_t)w * WIN_ROWS + 2 * u) * MAX_BATCH + j];
-                  up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * MAX_BATCH + j];
+                  g += pb[((size_t)w * WIN_ROWS + 2 * u) * NB + j];
+                  up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * NB + j];
                 }
                 epi((wbase >> 1) + u, j, g, up);
               } else {
                 float s = 0.f;
 #pragma unroll
-                for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * MAX_BATCH + j];
+                for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * NB + j];
                 epi(wbase + u, j, s, 0.f);
               }
             }
@@ -1085,7 +1251,7 @@ struct Consumer {
     float* kn_s = q_s + MAX_G * d;                 // new token's key (bf16 values)
     float* vn_s = kn_s + d;
     float* mrg = vn_s + d;                         // [groups][G][RS]
-    uint32_t* pscr = reinterpret_cast<uint32_t*>(mrg + NCW * G * RS);   // [NCW][2][8][8] packed P
+    uint32_t* pscr = reinterpret_cast<uint32_t*>(mrg + p.attn_mrg_floats);   // [NCW][2][8][8] packed P
     const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
     const float2* rope = p.rope + (size_t)pos * half;
     const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
@@ -1321,56 +1487,77 @@ struct Consumer {
     ab = finish(ab);
     if (ab) return ab;
     if (ticket(p.cm.attn_idx(l, b, g), (uint32_t)t.a[6])) {
-      // Combine the nc chunks of (b, g) in chunk order: gather every chunk's
-      // (max, normaliser) in parallel, turn them into weights, then one float4
-      // of every chunk's accumulator per thread with all loads in flight.
+      // Combine the nc chunks of (b, g) in chunk order.  Every thread first
+      // issues the loads of its float4 of the first CB chunks' accumulators;
+      // meanwhile one warp per head reduces the chunks' (max, normaliser) into
+      // weights; then the weighted sums, CB chunks per round trip.
+      constexpr int CB = 10;
       const float* p0 = p.part + ((size_t)l * nslots + t.a[5]) * G * RS;
       const int nc = t.a[6];
-      float* wts = mrg;                 // [nc][G]
-      float* lsm = mrg + nc * G;        // [nc][G]
-      float* inv = q_s;                 // [G]
-      for (int idx = ct; idx < nc * G; idx += NCT) {
-        const float* pc = p0 + (size_t)idx * RS;   // idx = c * G + h
-        wts[idx] = __ldcg(pc + d);
-        lsm[idx] = __ldcg(pc + d + 1);
-      }
-      cbar();
-      if (ct < G) {
-        const int h = ct;
-        float M = -INFINITY;
-        for (int c = 0; c < nc; ++c) M = fmaxf(M, wts[c * G + h]);
-        float Ls = 0.f;
-        for (int c = 0; c < nc; ++c) {
-          const float f = exp2f(wts[c * G + h] - M);
-          wts[c * G + h] = f;
-          Ls = fmaf(lsm[c * G + h], f, Ls);
-        }
-        inv[h] = 1.0f / Ls;
-      }
-      cbar();
-      float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
+      float* wts = mrg;                 // [nc][G] chunk weights (already divided by the normaliser)
       const int d4 = d >> 2;
-      for (int idx = ct; idx < G * d4; idx += NCT) {
-        const int h = idx / d4, i4 = idx - h * d4;
+      const int oh = ct / d4, oi4 = ct - oh * d4;   // this thread's output: head oh, dims 4*oi4..+3
+      const bool has_out = ct < G * d4;
+      float4 v[CB];
+#pragma unroll
+      for (int c = 0; c < CB; ++c)
+        if (has_out && c < nc)
+          v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)c * G + oh) * RS) + oi4);
+      if (cw < G) {
+        // warp h: each lane holds the (max, normaliser) of up to 4 chunks (nc <= 128 here)
+        const int h = cw;
+        float mc[4], lc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = lane + 32 * q;
+          const float2 ml = c < nc ? __ldcg(reinterpret_cast<const float2*>(p0 + ((size_t)c * G + h) * RS + d))
+                                   : make_float2(-INFINITY, 0.f);
+          mc[q] = ml.x;
+          lc[q] = ml.y;
+        }
+        float M = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+#pragma unroll
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+        float f[4], Ls = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[q] = lane + 32 * q < nc ? exp2f(mc[q] - M) : 0.f;
+          Ls = fmaf(lc[q], f[q], Ls);
+        }
+        const float inv = 1.0f / warp_sum(Ls);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (lane + 32 * q < nc) wts[(lane + 32 * q) * G + h] = f[q] * inv;
+      }
+      cbar();
+      if (has_out) {
+        float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < nc; c0 += 8) {
-          float4 v[8];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < CB; ++c)
+          if (c < nc) {
+            const float f = wts[c * G + oh];
+            A.x = fmaf(v[c].x, f, A.x);
+            A.y = fmaf(v[c].y, f, A.y);
+            A.z = fmaf(v[c].z, f, A.z);
+            A.w = fmaf(v[c].w, f, A.w);
+          }
+        for (int c0 = CB; c0 < nc; c0 += CB) {
+#pragma unroll
+          for (int c = 0; c < CB; ++c)
             if (c0 + c < nc)
-              v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(c0 + c) * G + h) * RS) + i4);
+              v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(c0 + c) * G + oh) * RS) + oi4);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
+          for (int c = 0; c < CB; ++c)
             if (c0 + c < nc) {
-              const float f = wts[(c0 + c) * G + h];
+              const float f = wts[(c0 + c) * G + oh];
               A.x = fmaf(v[c].x, f, A.x);
               A.y = fmaf(v[c].y, f, A.y);
               A.z = fmaf(v[c].z, f, A.z);
               A.w = fmaf(v[c].w, f, A.w);
             }
         }
-        const float s = inv[h];
-        reinterpret_cast<float4*>(o + h * d)[i4] = make_float4(A.x * s, A.y * s, A.z * s, A.w * s);
+        reinterpret_cast<float4*>(o + oh * d)[oi4] = A;
       }
       ab = finish(false);
       if (!ab) signal(p.cm.combine + l);
@@ -1534,7 +1721,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
         pr.run(t0, t1);
       }
     } else {
-      Consumer<NB> c{p, ring, act, m, ydown, tid, tid >> 5, tid & 31};
+      Consumer<NB> c{p, ring, act, m, ydown, reinterpret_cast<float*>(smem + p.psum_off), tid, tid >> 5, tid & 31};
       c.run(t0, t1);
     }
   }

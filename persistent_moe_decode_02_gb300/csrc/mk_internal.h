@@ -15,7 +15,11 @@ constexpr int MAX_BATCH = 8;
 constexpr int MAX_EXPERTS = 256;
 constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
 constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
+constexpr int WIN_ROWS = 32;               // rows per cross-warp partial-sum window (wide GEMV)
 constexpr int TRACE_SLOTS = 10;            // stamps per task in the optional timeline
+constexpr int STRACE_CAP = 4096;           // ring stages per CTA in the optional stage timeline
+constexpr int STRACE_SLOTS = 6;            // per stage: copy issued, landed, released, task,
+                                           // and SM clock64 at landed and released
 // timeline slots: consumer fetched / dependency met / activations ready /
 // stages consumed / done; producer first copy / last copy / task start;
 // consumer warp 0 saw its first / last stage of the task land
@@ -106,7 +110,11 @@ struct Params {
   RouteMap rm;
   int nstages, stage_bytes;
   int act_off, act_floats, misc_off;
+  int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * WIN_ROWS * nb floats)
+  int attn_mrg_floats;   // attention page-group states in the activation region (floats)
   int allh;             // 1: the down task keeps every (request, rank) h row in smem
+  int pf_ahead;         // stages the producer's L2 prefetch runs ahead of its ring copies (0: off)
+  int pf_wait;          // stages of routing-independent tasks prefetched while routing is pending (0: off)
   int down_rows_max;
   int* seq_len;         // device [bcap]
   const int* page_table;  // device [bcap * max_pages]
@@ -130,10 +138,59 @@ struct Params {
   int lm_tiles;
   // optional per-task timeline: TRACE_SLOTS globaltimer stamps per task (nullable)
   unsigned long long* trace;
+  // optional per-stage timeline: [cta][STRACE_CAP][STRACE_SLOTS] (nullable)
+  unsigned long long* strace;
   // io
   const int* tokens;
   float* logits;        // nullable [B][V]
   int* next_token;
 };
+
+// Shared-memory layout of one CTA: [weight ring][activations][misc + down
+// sums][GEMV partial-sum windows].  The ring takes what the rest leaves of the
+// 227 KB, in 32 KB stages (16 KB when fewer than four would fit).  Returns
+// false when the shape leaves no room (fewer than two stages, or an attention
+// page split the warps cannot share evenly).
+struct SmemPlan {
+  int stage_bytes, nstages, act_floats, allh, act_off, misc_off, psum_off, attn_mrg_floats, smem;
+};
+
+inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bcap, int nb, int down_rows_max,
+                      size_t misc_struct_bytes, SmemPlan& o) {
+  const int nqd = nq * d;
+  const int widest = H > nqd ? (H > F ? H : F) : (nqd > F ? nqd : F);
+  const long long A1 = (long long)bcap * widest;
+  const int RS = d + 4;
+  int ppg32 = 32768 / (2 * ps * d * 2);
+  if (ppg32 < 1) ppg32 = 1;
+  const long long mrg = (long long)ppg32 * G * RS > 128LL * G ? (long long)ppg32 * G * RS : 128LL * G;
+  const long long A3 = (long long)MAX_G * d + 2 * d + mrg + NCW * 128;  // q, new K/V, states, P scratch
+  const long long Ah = (long long)bcap * k * F;
+  o.allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
+  long long act = A1 > A3 ? A1 : A3;
+  if (o.allh && Ah > act) act = Ah;
+  o.act_floats = (int)act;
+  o.attn_mrg_floats = (int)mrg;
+  const size_t act_bytes = ((size_t)act * 4 + 127) / 128 * 128;
+  const size_t misc = (misc_struct_bytes + (size_t)bcap * k * down_rows_max * 4 + 127) / 128 * 128;
+  const size_t psum = ((size_t)2 * NCW * WIN_ROWS * nb * 4 + 127) / 128 * 128;
+  const long long avail = (long long)SMEM_LIMIT - (long long)(act_bytes + misc + psum);
+  const int need0 = 2 * widest > 4 * H ? 2 * widest : 4 * H;
+  const int need = need0 > 2 * ps * d * 2 ? need0 : 2 * ps * d * 2;
+  int sb = avail < 4LL * 32768 ? 16384 : 32768;
+  while (sb < need) sb *= 2;
+  long long nst = avail / sb;
+  if (nst > MAX_STAGES) nst = MAX_STAGES;
+  if (nst < 2) return false;
+  const int ppg = sb / (2 * ps * d * 2) < 1 ? 1 : sb / (2 * ps * d * 2);
+  if (ppg > ppg32 || NCW % ppg != 0 || (d / 16) / (NCW / ppg) > 4) return false;
+  o.stage_bytes = sb;
+  o.nstages = (int)nst;
+  o.act_off = (int)(nst * sb);
+  o.misc_off = (int)(nst * sb + act_bytes);
+  o.psum_off = (int)(nst * sb + act_bytes + misc);
+  o.smem = (int)(nst * sb + act_bytes + misc + psum);
+  return true;
+}
 
 }  // namespace mk

@@ -115,6 +115,10 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
   for (int b = 0; b < B; ++b) total_pages += pages_for(seq_lens[b], s.ps);
   long long P = (total_pages * s.nkv + C - 1) / C;
   c.P = P < 1 ? 1 : (int)P;
+  for (int b = 0; b < B; ++b) {   // the split-KV combine takes at most 128 chunks per (request, group)
+    const int need = (pages_for(seq_lens[b], s.ps) + 127) / 128;
+    if (c.P < need) c.P = need;
+  }
   c.slots = 0;
   for (int b = 0; b < B; ++b) c.slots += (pages_for(seq_lens[b], s.ps) + c.P - 1) / c.P * s.nkv;
   int rot = 0;
@@ -311,32 +315,11 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
     return fail(MK_ERR_CAPACITY, buf);
   }
 
-  // shared-memory plan (same rule as mk_plan_create)
-  const int nqd = s.nq * s.d;
-  long long A1 = (long long)B * (s.H > nqd ? (s.H > s.F ? s.H : s.F) : (nqd > s.F ? nqd : s.F));
-  long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4) +
-                       mk::NCW * 128;  // q, new K/V, page-group states, P scratch
-  long long Ah = (long long)B * s.k * s.F;
-  const int allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
-  long long act = A1 > A3 ? A1 : A3;
-  if (allh && Ah > act) act = Ah;
-  const size_t act_bytes = ((size_t)act * 4 + 127) / 128 * 128;
-  const size_t misc = ((mk::misc_bytes() + (size_t)B * s.k * cnt.down_rows_max * 4) + 127) / 128 * 128;
-  const long long avail = (long long)mk::SMEM_LIMIT - (long long)act_bytes - (long long)misc;
-  int need = 2 * (s.H > nqd ? (s.H > s.F ? s.H : s.F) : (nqd > s.F ? nqd : s.F));
-  if (4 * s.H > need) need = 4 * s.H;
-  if (2 * s.ps * s.d * 2 > need) need = 2 * s.ps * s.d * 2;
-  int sb = avail < 4LL * 32768 ? 16384 : 32768;
-  while (sb < need) sb *= 2;
-  long long nst = avail / sb;
-  if (nst > mk::MAX_STAGES) nst = mk::MAX_STAGES;
-  if (nst < 2) return fail(MK_ERR_UNSUPPORTED, "shape leaves no room for the shared-memory ring");
-  {
-    const int ppg = sb / (2 * s.ps * s.d * 2) < 1 ? 1 : sb / (2 * s.ps * s.d * 2);
-    if (mk::NCW % ppg != 0 || (s.d / 16) / (mk::NCW / ppg) > 4)
-      return fail(MK_ERR_UNSUPPORTED, "attention page split does not fit this stage size");
-  }
-  const int smem = (int)((size_t)nst * sb + act_bytes + misc);
+  // shared-memory plan (same layout rule as mk_plan_create)
+  mk::SmemPlan sp;
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, B, nb, cnt.down_rows_max, mk::misc_bytes(), sp))
+    return fail(MK_ERR_UNSUPPORTED, "shape leaves no room for the shared-memory ring");
+  const int smem = sp.smem;
   if (mk::max_active_ctas(nb, smem) < 1) return fail(MK_ERR_CUDA, "megakernel does not fit on an SM");
 
   // fill the host staging array
@@ -401,14 +384,19 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.status = (int*)(base + d_stat);
   P.epoch = 1;
   P.timeout_ns = 2000000000ull;
+  P.pf_ahead = 0;
+  P.pf_wait = 0;
+  P.strace = nullptr;
   P.cm = cm;
   P.rm = rm;
-  P.nstages = (int)nst;
-  P.stage_bytes = sb;
-  P.act_off = (int)(nst * sb);
-  P.act_floats = (int)act;
-  P.misc_off = (int)(nst * sb + act_bytes);
-  P.allh = allh;
+  P.nstages = sp.nstages;
+  P.stage_bytes = sp.stage_bytes;
+  P.act_off = sp.act_off;
+  P.act_floats = sp.act_floats;
+  P.misc_off = sp.misc_off;
+  P.psum_off = sp.psum_off;
+  P.attn_mrg_floats = sp.attn_mrg_floats;
+  P.allh = sp.allh;
   P.down_rows_max = cnt.down_rows_max;
   P.seq_len = (int*)(base + d_blob + h_seq);
   P.page_table = (const int*)(base + d_blob + h_pt);

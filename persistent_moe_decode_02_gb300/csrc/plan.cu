@@ -135,6 +135,8 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   }
   int P = split_pages;
   if (P <= 0) P = (int)std::max<long long>(1, (total_pages * s.nkv + C - 1) / C);
+  for (int b = 0; b < B; ++b)   // the split-KV combine takes at most 128 chunks per (request, group)
+    P = std::max(P, (pages_for(seq_lens[b], s.ps) + 127) / 128);
   cnt.pages_per_chunk = P;
   std::vector<int> nch(B);
   open_start.assign(B, 0);
@@ -262,7 +264,7 @@ void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_erro
 
 struct mk_plan {
   Shape s;
-  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0;
+  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0, pf_ahead = 0, pf_wait = 0;
   int max_pages = 0, num_pages = 0, rope_npos = 0;
   int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0, allh = 0;
   int replans = 0;
@@ -290,6 +292,7 @@ struct mk_plan {
   size_t part_cap_slots = 0;
   unsigned long long* d_trace = nullptr;
   size_t trace_cap = 0;
+  unsigned long long* d_strace = nullptr;
   int* d_io_tok = nullptr;
   int* d_io_next = nullptr;
   float* d_io_logits = nullptr;
@@ -449,6 +452,9 @@ void fill_params(mk_plan* p) {
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
   P.trace = p->trace ? p->d_trace : nullptr;
+  P.strace = p->trace >= 2 ? p->d_strace : nullptr;
+  P.pf_ahead = p->pf_ahead;
+  P.pf_wait = p->pf_wait;
 }
 
 }  // namespace
@@ -534,7 +540,9 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   p->C = o.num_ctas > 0 ? std::min(o.num_ctas, sms) : sms;
   p->split_opt = o.split_pages;
   p->drop_task = o.debug_drop_task;
-  p->trace = o.trace ? 1 : 0;
+  p->trace = o.trace >= 2 ? 2 : o.trace ? 1 : 0;
+  p->pf_ahead = std::max(0, std::min(o.l2_ahead, 64));
+  p->pf_wait = std::max(0, std::min(o.l2_wait, 64));
   p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
   p->max_pages = max_pages_per_seq;
   p->num_pages = kv->num_pages;
@@ -550,37 +558,23 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   };
   g_last_error[0] = 0;
 
-  // shared-memory budget: activations + misc, the rest is the weight ring
-  const int nqd = s.nq * s.d;
-  const long long A1 = (long long)bcap * std::max(std::max(s.H, nqd), s.F);
-  const long long A3 = (long long)mk::MAX_G * s.d + 2 * s.d + (long long)mk::NCW * s.G * (s.d + 4) +
-                       mk::NCW * 128;  // q, new K/V, page-group states, P scratch
-  const long long Ah = (long long)bcap * s.k * s.F;
-  p->allh = (Ah * 4 <= 64 * 1024) ? 1 : 0;
-  p->act_floats = (int)std::max(std::max(A1, A3), p->allh ? Ah : 0LL);
+  // shared-memory budget: activations + misc + partial sums, the rest is the weight ring
   const int C = p->C;
   const int down_rows_max = (s.H + std::min(s.H, C) - 1) / std::min(s.H, C);
-  const size_t act_bytes = ((size_t)p->act_floats * 4 + 127) / 128 * 128;
-  const size_t misc = ((mk::misc_bytes() + (size_t)bcap * s.k * down_rows_max * 4) + 127) / 128 * 128;
-  const long long avail = (long long)mk::SMEM_LIMIT - (long long)act_bytes - (long long)misc;
-  const int need = std::max(std::max(2 * std::max(std::max(s.H, nqd), s.F), 4 * s.H), 2 * s.ps * s.d * 2);
-  int sb = 32768;
-  if (avail < 4LL * sb) sb = 16384;
-  while (sb < need) sb *= 2;
-  int nst = (int)std::min<long long>(mk::MAX_STAGES, avail / sb);
-  if (nst < 2) return fail(MK_ERR_UNSUPPORTED);
-  {
-    // attention: the warps split a stage's pages evenly, at most 4 output row tiles each
-    const int ppg = std::max(1, sb / (2 * s.ps * s.d * 2));
-    if (mk::NCW % ppg != 0 || (s.d / 16) / (mk::NCW / ppg) > 4) return fail(MK_ERR_UNSUPPORTED);
-  }
-  p->stage_bytes = sb;
-  p->nstages = nst;
-  p->smem = (int)((size_t)nst * sb + act_bytes + misc);
-  p->P.act_off = nst * sb;
-  p->P.act_floats = p->act_floats;
-  p->P.misc_off = (int)(nst * sb + act_bytes);
-  p->P.allh = p->allh;
+  mk::SmemPlan sp;
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, bcap, p->nb, down_rows_max, mk::misc_bytes(), sp))
+    return fail(MK_ERR_UNSUPPORTED);
+  p->allh = sp.allh;
+  p->act_floats = sp.act_floats;
+  p->stage_bytes = sp.stage_bytes;
+  p->nstages = sp.nstages;
+  p->smem = sp.smem;
+  p->P.act_off = sp.act_off;
+  p->P.act_floats = sp.act_floats;
+  p->P.misc_off = sp.misc_off;
+  p->P.psum_off = sp.psum_off;
+  p->P.attn_mrg_floats = sp.attn_mrg_floats;
+  p->P.allh = sp.allh;
   if (mk::max_active_ctas(p->nb, p->smem) < 1) {
     snprintf(g_last_error, sizeof(g_last_error), "megakernel does not fit on an SM with %d bytes of shared memory",
              p->smem);
@@ -628,7 +622,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   p->pt_cap = (size_t)bcap * max_pages_per_seq;
   ok &= dalloc(p, &p->d_pt, p->pt_cap * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &P.qkv, L * bcap * s.qkv_rows * sizeof(float)) == cudaSuccess;
-  ok &= dalloc(p, &P.o, L * bcap * nqd * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.o, L * bcap * s.nq * s.d * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_mid, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_out, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.xnf, L * bcap * s.H * sizeof(float)) == cudaSuccess;
@@ -640,6 +634,9 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;
+  if (p->trace >= 2)
+    ok &= dalloc(p, &p->d_strace, (size_t)C * mk::STRACE_CAP * mk::STRACE_SLOTS * sizeof(unsigned long long)) ==
+          cudaSuccess;
   ok &= dalloc(p, &p->d_io_tok, (size_t)bcap * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &p->d_io_next, (size_t)bcap * sizeof(int)) == cudaSuccess;
   p->rope_npos = max_pages_per_seq * s.ps;
@@ -690,6 +687,9 @@ int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next
   P.tokens = d_tokens;
   P.logits = d_logits;
   P.next_token = d_next_token;
+  if (p->d_strace &&
+      cudaMemsetAsync(p->d_strace, 0, (size_t)p->C * mk::STRACE_CAP * mk::STRACE_SLOTS * 8, st) != cudaSuccess)
+    return note_cuda(cudaGetLastError(), "stage trace reset");
   cudaError_t e = mk::launch_megakernel(P, p->nb, p->C, p->smem, st);
   if (e != cudaSuccess) return note_cuda(e, "megakernel launch");
   for (int b = 0; b < p->B; ++b) p->seq[b]++;
@@ -798,6 +798,11 @@ int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream 
       const size_t n = p->tasks.size() * mk::TRACE_SLOTS * sizeof(unsigned long long);
       if (!p->trace || !p->d_trace || bytes < n) return MK_ERR_INVALID;
       return cudaMemcpyAsync(dst, p->d_trace, n, cudaMemcpyDefault, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
+    case MK_DBG_STAGE_TRACE: {
+      const size_t n = (size_t)p->C * mk::STRACE_CAP * mk::STRACE_SLOTS * sizeof(unsigned long long);
+      if (p->trace < 2 || !p->d_strace || bytes < n) return MK_ERR_INVALID;
+      return cudaMemcpyAsync(dst, p->d_strace, n, cudaMemcpyDefault, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
     }
     case MK_DBG_UNION:
       if (bytes < L * 4) return MK_ERR_INVALID;

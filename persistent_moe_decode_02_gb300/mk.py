@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libmk.so")
 
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_DEP_TIMEOUT, MK_ERR_CAPACITY, MK_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ_LENS, MK_DBG_UNION = 1, 2, 3, 4, 5, 6
-MK_DBG_TASKS, MK_DBG_TRACE = 7, 8
+MK_DBG_TASKS, MK_DBG_TRACE, MK_DBG_STAGE_TRACE = 7, 8, 9
 TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start", "s_first", "s_last"]
 
 EXPORTS = [
@@ -47,7 +47,8 @@ class MkKv(ctypes.Structure):
 
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
-                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int)]
+                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
+                ("l2_ahead", ctypes.c_int), ("l2_wait", ctypes.c_int)]
 
 
 class MkError(RuntimeError):
@@ -164,11 +165,13 @@ class Plan:
     weights: dict with 'embed', 'final_norm', 'lm_head' tensors and per-layer
     lists 'attn_norm', 'wqkv', 'wo', 'ffn_norm', 'router', 'w_gate_up',
     'w_down' (bf16 CUDA tensors in the layout of include/mk.h).
-    k_pools / v_pools: per-layer bf16 [num_pages, nkv, page_size, d]."""
+    k_pools / v_pools: per-layer bf16 [num_pages, nkv, head_dim, page_size] (pages
+    stored transposed, slot fastest)."""
 
     def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
                  max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
-                 split_pages: int = 0, debug_drop_task: int = 0, trace: bool = False):
+                 split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0,
+                 l2_ahead: int = 0, l2_wait: int = 0):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._arrays = {k: _ptr_array(weights[k]) for k in
@@ -182,7 +185,8 @@ class Plan:
                                                               "w_gate_up", "w_down")])
         self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
         self._dims = dims_struct(D)
-        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace))
+        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace), l2_ahead,
+                          l2_wait)
         self.batch = len(seq_lens)
         pt = [int(x) for x in page_table]
         h = ctypes.c_void_p()
@@ -234,6 +238,15 @@ class Plan:
         self.read_debug(MK_DBG_TRACE, stamps, stream)
         self.sync(stream)
         return tasks, stamps
+
+    def stage_timeline(self, stream=None) -> torch.Tensor:
+        """int64 [num_ctas, 4096, 6] of the last step: per CTA and ring stage, the
+        copy issue, landing and release stamps (ns, 0 = none), the task index, and
+        the SM clock at landing and release (needs trace=2)."""
+        out = torch.empty(self.info()["num_ctas"], 4096, 6, dtype=torch.int64)
+        self.read_debug(MK_DBG_STAGE_TRACE, out, stream)
+        self.sync(stream)
+        return out
 
     def info(self) -> dict:
         buf = (ctypes.c_int * 10)()
