@@ -469,6 +469,10 @@ struct Producer {
         q.nst = c->U * q.spe;
         return true;
       }
+      case T_COMB: {   // no weights: reads only partials
+        q.nst = 0;
+        return true;
+      }
       default: return false;
     }
   }
@@ -604,7 +608,7 @@ struct Producer {
       if (!geo(t, q, &r.m->cp_route, false, ti)) {
         if (p.pf_wait > 0) prefetch_while_routing(ti);
         if (!geo(t, q, &r.m->cp_route, true, ti)) {
-          if (t.type < T_QKV || t.type > T_LM) set_error(p, MK_ERR_INVALID, ti, t.type);
+          if (t.type < T_QKV || t.type > T_LAST) set_error(p, MK_ERR_INVALID, ti, t.type);
           r.m->abort_flag = 1;
           return;
         }
@@ -683,7 +687,9 @@ struct Consumer {
 
   // ---- activations
   // act[b * H + i] = x_b[i] / sqrt(mean(x_b^2) + eps) * gamma[i] for b < B, with
-  // x_b read four floats at a time by src(b, i4).
+  // x_b read four floats at a time by src(b, i4).  The gain is read in the
+  // same pass as x (one L2 round trip): the first pass stores x * gamma and
+  // the sums of squares of x, the second scales by 1 / rms.
   template <class Src4>
   __device__ void fill_rmsnorm(const uint16_t* gamma, Src4 src) {
     const int H = p.H, H4 = H >> 2, B = p.B;
@@ -693,7 +699,8 @@ struct Consumer {
 #pragma unroll 4
       for (int i = ct; i < H4; i += NCT) {
         const float4 v = src(b, i);
-        dst[i] = v;
+        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
+        dst[i] = make_float4(v.x * bf_lo(gb.x), v.y * bf_hi(gb.x), v.z * bf_lo(gb.y), v.w * bf_hi(gb.y));
         ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
       }
       ss = warp_sum(ss);
@@ -708,12 +715,11 @@ struct Consumer {
       float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
 #pragma unroll 4
       for (int i = ct; i < H4; i += NCT) {
-        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
         float4 v = dst[i];
-        v.x = v.x * inv * bf_lo(gb.x);
-        v.y = v.y * inv * bf_hi(gb.x);
-        v.z = v.z * inv * bf_lo(gb.y);
-        v.w = v.w * inv * bf_hi(gb.y);
+        v.x *= inv;
+        v.y *= inv;
+        v.z *= inv;
+        v.w *= inv;
         dst[i] = v;
       }
     }
@@ -1237,8 +1243,7 @@ struct Consumer {
   // close to fp32 accuracy; K and V are exact bf16.  The warps of a stage take
   // its pages (NCW / pages-per-stage warps per page, splitting the d/16 output
   // row tiles); each page group keeps its own online-softmax state, merged at
-  // the end of the chunk, then the chunks of (request, KV head) are combined by
-  // the last one to finish.
+  // the end of the chunk into one partial; the combine tasks merge the chunks.
   __device__ bool attn(const Task& t, bool ab) {
     const int l = t.layer, b = t.a[0], g = t.a[1];
     const int G = p.G, d = p.d, half = d >> 1;
@@ -1485,83 +1490,83 @@ struct Consumer {
       }
     }
     ab = finish(ab);
-    if (ab) return ab;
-    if (ticket(p.cm.attn_idx(l, b, g), (uint32_t)t.a[6])) {
-      // Combine the nc chunks of (b, g) in chunk order.  Every thread first
-      // issues the loads of its float4 of the first CB chunks' accumulators;
-      // meanwhile one warp per head reduces the chunks' (max, normaliser) into
-      // weights; then the weighted sums, CB chunks per round trip.
-      constexpr int CB = 10;
-      const float* p0 = p.part + ((size_t)l * nslots + t.a[5]) * G * RS;
-      const int nc = t.a[6];
-      float* wts = mrg;                 // [nc][G] chunk weights (already divided by the normaliser)
-      const int d4 = d >> 2;
-      const int oh = ct / d4, oi4 = ct - oh * d4;   // this thread's output: head oh, dims 4*oi4..+3
-      const bool has_out = ct < G * d4;
-      float4 v[CB];
+    if (!ab) signal(p.cm.attn_idx(l, b, g));
+    return ab;
+  }
+
+  // ---- split-KV combine of query heads [a2, a2 + a3) of (request a0, KV group a1)
+  // The chunks' partials (max m, normaliser l, accumulator acc[d], in exp2
+  // units) merge by log-sum-exp.  Warp w takes chunks w, w + 8, ... in order
+  // with an online (max, normaliser, accumulator) state, CB chunks per round
+  // trip; the 8 warp states then merge in warp order, so the result does not
+  // depend on timing.
+  __device__ bool comb(const Task& t, bool ab) {
+    constexpr int CB = 8;
+    const int l = t.layer, b = t.a[0], g = t.a[1], h0 = t.a[2], nh = t.a[3], nc = t.a[6];
+    const int G = p.G, d = p.d, RS = d + 4, d4 = d >> 2;
+    const float* part = p.part + ((size_t)l * p.part_slots + t.a[5]) * G * RS;
+    float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
+    float* ws = act;                                   // [NCW][d + 4]: accumulator, max, normaliser
+    const bool has = lane < d4;                        // this lane's 4 dims
+    mark(TR_ACT);
+    for (int hh = 0; hh < nh && !ab; ++hh) {
+      const int h = h0 + hh;
+      float M = -INFINITY, Ls = 0.f;
+      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c0 = cw; c0 < nc; c0 += NCW * CB) {
+        float4 v[CB];
+        float2 ml[CB];
 #pragma unroll
-      for (int c = 0; c < CB; ++c)
-        if (has_out && c < nc)
-          v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)c * G + oh) * RS) + oi4);
-      if (cw < G) {
-        // warp h: each lane holds the (max, normaliser) of up to 4 chunks (nc <= 128 here)
-        const int h = cw;
-        float mc[4], lc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = lane + 32 * q;
-          const float2 ml = c < nc ? __ldcg(reinterpret_cast<const float2*>(p0 + ((size_t)c * G + h) * RS + d))
-                                   : make_float2(-INFINITY, 0.f);
-          mc[q] = ml.x;
-          lc[q] = ml.y;
+        for (int q = 0; q < CB; ++q) {
+          const int c = c0 + q * NCW;
+          if (c < nc) {
+            const float* pc = part + ((size_t)c * G + h) * RS;
+            ml[q] = __ldcg(reinterpret_cast<const float2*>(pc + d));
+            v[q] = has ? __ldcg(reinterpret_cast<const float4*>(pc) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        float M = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
 #pragma unroll
-        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-        float f[4], Ls = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          f[q] = lane + 32 * q < nc ? exp2f(mc[q] - M) : 0.f;
-          Ls = fmaf(lc[q], f[q], Ls);
+        for (int q = 0; q < CB; ++q) {
+          if (c0 + q * NCW < nc) {
+            const float mn = fmaxf(M, ml[q].x);
+            const float fo = exp2f(M - mn), fn = exp2f(ml[q].x - mn);   // fo = 0 while M = -inf
+            A.x = fmaf(v[q].x, fn, A.x * fo);
+            A.y = fmaf(v[q].y, fn, A.y * fo);
+            A.z = fmaf(v[q].z, fn, A.z * fo);
+            A.w = fmaf(v[q].w, fn, A.w * fo);
+            Ls = fmaf(ml[q].y, fn, Ls * fo);
+            M = mn;
+          }
         }
-        const float inv = 1.0f / warp_sum(Ls);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (lane + 32 * q < nc) wts[(lane + 32 * q) * G + h] = f[q] * inv;
+      }
+      float* mine = ws + cw * RS;
+      if (has) reinterpret_cast<float4*>(mine)[lane] = A;
+      if (lane == 0) {
+        mine[d] = M;
+        mine[d + 1] = Ls;
       }
       cbar();
-      if (has_out) {
-        float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
-        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = ct; i < d; i += NCT) {
+        float Mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < CB; ++c)
-          if (c < nc) {
-            const float f = wts[c * G + oh];
-            A.x = fmaf(v[c].x, f, A.x);
-            A.y = fmaf(v[c].y, f, A.y);
-            A.z = fmaf(v[c].z, f, A.z);
-            A.w = fmaf(v[c].w, f, A.w);
+        for (int w = 0; w < NCW; ++w) Mt = fmaxf(Mt, ws[w * RS + d]);
+        float Lt = 0.f, At = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float mw = ws[w * RS + d];
+          if (mw != -INFINITY) {
+            const float f = exp2f(mw - Mt);
+            Lt = fmaf(ws[w * RS + d + 1], f, Lt);
+            At = fmaf(ws[w * RS + i], f, At);
           }
-        for (int c0 = CB; c0 < nc; c0 += CB) {
-#pragma unroll
-          for (int c = 0; c < CB; ++c)
-            if (c0 + c < nc)
-              v[c] = __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(c0 + c) * G + oh) * RS) + oi4);
-#pragma unroll
-          for (int c = 0; c < CB; ++c)
-            if (c0 + c < nc) {
-              const float f = wts[(c0 + c) * G + oh];
-              A.x = fmaf(v[c].x, f, A.x);
-              A.y = fmaf(v[c].y, f, A.y);
-              A.z = fmaf(v[c].z, f, A.z);
-              A.w = fmaf(v[c].w, f, A.w);
-            }
         }
-        reinterpret_cast<float4*>(o + oh * d)[oi4] = A;
+        o[h * d + i] = At / Lt;
       }
-      ab = finish(false);
-      if (!ab) signal(p.cm.combine + l);
+      cbar();
     }
+    mark(TR_STAGES);
+    ab = finish(ab);
+    if (!ab) signal(p.cm.combine + l);
     return ab;
   }
 
@@ -1671,6 +1676,7 @@ struct Consumer {
         case T_GU: ab = gate_up(t, ab); break;
         case T_DOWN: ab = down(t, ab); break;
         case T_LM: ab = lm(t, ab); break;
+        case T_COMB: ab = comb(t, ab); break;
         default: ab = true;
       }
       if (ab) break;

@@ -36,7 +36,10 @@ enum TaskType : int32_t {
   T_GU = 4,      // gate/up tile a0 of a1 over the flattened (distinct expert, ffn row) space
   T_DOWN = 5,    // rows [a0,a1) of the hidden dim over every selected expert, residual add
   T_LM = 6,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
+  T_COMB = 7,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
+                 // a5 = first partial slot, a6 = chunks (waits for all of them)
 };
+constexpr int T_LAST = T_COMB;
 
 struct alignas(16) Task {
   int32_t type;

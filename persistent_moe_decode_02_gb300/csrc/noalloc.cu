@@ -91,7 +91,7 @@ inline void split_range(int n, int parts, int i, int& a, int& b) {
 }
 
 struct Counts {
-  int qkv_per_g, o, router, gu, down, lm, P, slots, down_rows_max, ntasks;
+  int qkv_per_g, o, router, gu, down, lm, P, slots, down_rows_max, ntasks, hpc, comb;
 };
 
 // Emits the step's tasks phase by phase in topological order; a phase with n
@@ -121,6 +121,14 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
   }
   c.slots = 0;
   for (int b = 0; b < B; ++b) c.slots += (pages_for(seq_lens[b], s.ps) + c.P - 1) / c.P * s.nkv;
+  // query heads per combine task: the smallest divisor of G within one task per CTA, else G
+  c.hpc = s.G;
+  for (int h = 1; h <= s.G; ++h)
+    if (s.G % h == 0 && (long long)B * s.nkv * (s.G / h) <= C) {
+      c.hpc = h;
+      break;
+    }
+  c.comb = B * s.nkv * (s.G / c.hpc);
   int rot = 0;
   auto task = [](int type, int layer, int wc, uint32_t wn) {
     mk::Task t;
@@ -165,10 +173,27 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
         }
       }
     }
+    slot = 0;
+    for (int b = 0; b < B; ++b) {
+      const int nch = (pages_for(seq_lens[b], s.ps) + c.P - 1) / c.P;
+      for (int g = 0; g < s.nkv; ++g) {
+        for (int h = 0; h < s.G; h += c.hpc) {
+          mk::Task t = task(mk::T_COMB, l, cm.attn_idx(l, b, g), (uint32_t)nch);
+          t.a[0] = b;
+          t.a[1] = g;
+          t.a[2] = h;
+          t.a[3] = c.hpc;
+          t.a[5] = slot;
+          t.a[6] = nch;
+          put(next(), t);
+        }
+        slot += nch;
+      }
+    }
     for (int i = 0; i < c.o; ++i) {
       int a, b;
       split_range(s.H, c.o, i, a, b);
-      mk::Task t = task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)(B * s.nkv));
+      mk::Task t = task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)c.comb);
       t.a[0] = a;
       t.a[1] = b;
       put(next(), t);

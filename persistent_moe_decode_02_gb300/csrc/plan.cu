@@ -58,7 +58,7 @@ int check_dims(const mk_model_dims* m, Shape& s) {
 }
 
 struct Counts {
-  int qkv_per_g = 0, attn = 0, o = 0, router = 0, gu = 0, down = 0, lm = 0;
+  int qkv_per_g = 0, attn = 0, o = 0, router = 0, gu = 0, down = 0, lm = 0, comb = 0, heads_per_comb = 1;
   int part_slots = 0, pages_per_chunk = 1, down_rows_max = 1;
 };
 
@@ -99,6 +99,22 @@ Task mk_task(int type, int layer, int wait_ctr, uint32_t wait_cnt) {
 
 // Pages covering positions [0, len] (the cached tokens plus the new one).
 inline int pages_for(int len, int ps) { return len / ps + 1; }
+
+// Query heads per split-KV combine task: the smallest divisor of G that keeps
+// the tasks (pairs x G / heads) within one per CTA, else all G heads.
+inline int comb_heads(int G, int pairs, int C) {
+  for (int h = 1; h <= G; ++h)
+    if (G % h == 0 && (long long)pairs * (G / h) <= C) return h;
+  return G;
+}
+
+// First partial slot of (request b, KV group g): slots run request by request,
+// group by group, chunk by chunk.
+inline int first_slot(const std::vector<int>& nch, int B, int nkv, int b, int g) {
+  int s = 0;
+  for (int i = 0; i < b; ++i) s += nch[i] * nkv;
+  return s + g * nch[b];
+}
 
 // Split n items into `parts` nearly equal contiguous ranges.
 inline void split_range(int n, int parts, int i, int& a, int& b) {
@@ -148,6 +164,8 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   }
   cnt.part_slots = slots;
   cnt.attn = slots;
+  cnt.heads_per_comb = comb_heads(s.G, B * s.nkv, C);
+  cnt.comb = B * s.nkv * (s.G / cnt.heads_per_comb);
   const double PB = 2.0 * s.ps * s.d * 2;
 
   for (int l = 0; l < s.L; ++l) {
@@ -188,11 +206,28 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     }
     asg.phase(ph);
     ph.clear();
+    // split-KV combine, a few query heads per task, once all chunks of (b, g) are in
+    for (int b = 0; b < B; ++b) {
+      for (int g = 0; g < s.nkv; ++g) {
+        for (int h = 0; h < s.G; h += cnt.heads_per_comb) {
+          Task t = mk_task(mk::T_COMB, l, cm.attn_idx(l, b, g), (uint32_t)nch[b]);
+          t.a[0] = b;
+          t.a[1] = g;
+          t.a[2] = h;
+          t.a[3] = cnt.heads_per_comb;
+          t.a[5] = first_slot(nch, B, s.nkv, b, g);
+          t.a[6] = nch[b];
+          ph.push_back({(double)nch[b] * cnt.heads_per_comb * (s.d + 2) * 4, t});
+        }
+      }
+    }
+    asg.phase(ph);
+    ph.clear();
     // O projection + residual
     for (int i = 0; i < cnt.o; ++i) {
       int a, b;
       split_range(s.H, cnt.o, i, a, b);
-      Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)(B * s.nkv));
+      Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)cnt.comb);
       t.a[0] = a;
       t.a[1] = b;
       ph.push_back({(double)(b - a) * nqd * 2, t});

@@ -14,7 +14,7 @@ from synth import FULL, MID, TINY, Dims
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-T_QKV, T_ATTN, T_OPROJ, T_ROUTER, T_GU, T_DOWN, T_LM = range(7)
+T_QKV, T_ATTN, T_OPROJ, T_ROUTER, T_GU, T_DOWN, T_LM, T_COMB = range(8)
 
 
 @pytest.fixture(scope="module")
@@ -84,8 +84,9 @@ def signals_per_step(D, B, tasks):
             sig[base["down"] + l] += 1
         elif typ == T_LM:
             sig[base["lm"]] += 1
+        elif typ == T_COMB:
+            sig[base["combine"] + l] += 1
     for l in range(L):
-        sig[base["combine"] + l] = B * nkv     # one per (request, group) finisher
         sig[base["rdone"] + l] = 1             # the router finisher
     return sig, base
 
@@ -146,24 +147,17 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
             out.append(base["gu"] + l)
         elif typ == T_DOWN:
             out.append(base["down"] + l)
+        elif typ == T_COMB:
+            out.append(base["combine"] + l)
         return out
 
-    # emulate with the finisher counters derived from ticket completion
-    C_ = len(cs) - 1
-    attn_need = {}
-    for t in tasks.tolist():
-        if t[0] == T_ATTN:
-            attn_need[(t[1], t[2], t[3])] = t[8]
+    # emulate with the router finisher's counter derived from ticket completion
     router_need = {t[1]: t[4] for t in tasks.tolist() if t[0] == T_ROUTER}
     got = defaultdict(int)
 
     def fires_with_finishers(t):
         out = fires(t)
         typ, l, a = t[0], t[1], t[2:10]
-        if typ == T_ATTN:
-            got[("a", l, a[0], a[1])] += 1
-            if got[("a", l, a[0], a[1])] == attn_need[(l, a[0], a[1])]:
-                out.append(base["combine"] + l)
         if typ == T_ROUTER:
             got[("r", l)] += 1
             if got[("r", l)] == router_need[l]:
@@ -191,6 +185,16 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
     cover(T_DOWN, D.hidden)
     lm = sorted((t[2], t[3]) for t in tasks.tolist() if t[0] == T_LM)
     assert lm[0][0] == 0 and lm[-1][1] == D.vocab
+    # every query head of every (request, group) is combined exactly once, from
+    # that pair's own partial slots
+    for b in range(B):
+        for g in range(nkv):
+            comb = [t for t in tasks.tolist() if t[0] == T_COMB and t[1] == 0 and t[2] == b and t[3] == g]
+            heads = sorted(h for t in comb for h in range(t[4], t[4] + t[5]))
+            assert heads == list(range(D.group))
+            chunks = sorted(t[6] for t in tasks.tolist() if t[0] == T_ATTN and t[1] == 0 and t[2] == b and t[3] == g)
+            assert all(t[7] == chunks[0] and t[8] == len(chunks) for t in comb)
+            assert chunks == list(range(chunks[0], chunks[0] + len(chunks)))
 
 
 def test_full_bs1_phases_spread_over_all_ctas(mk):
