@@ -330,6 +330,11 @@ def summarize_timeline(tasks, stamps, step_ms) -> str:
             continue
         vals = [float((S[m, b] - S[m, a]).mean()) for _, a, b in seg]
         out.append(f"{name:8s} {int(m.sum()):6d} " + "  ".join(f"{v:10.2f}" for v in vals))
+        mm = m & (S[:, 10] > 0) & (S[:, 11] > 0)
+        if S.shape[1] >= 12 and int(mm.sum()) > 0:
+            out.append(f"{'':8s} activation steps: dep>mid1 {float((S[mm, 10] - S[mm, 1]).mean()):.2f}  "
+                       f"mid1>mid2 {float((S[mm, 11] - S[mm, 10]).mean()):.2f}  "
+                       f"mid2>act {float((S[mm, 2] - S[mm, 11]).mean()):.2f}")
     L = int(lay.max()) + 1
     ends = [float(S[(typ == 5) & (lay == l), 4].max()) for l in range(L)]
     dl = [b - a for a, b in zip(ends, ends[1:])] or [ends[0]]

@@ -161,10 +161,12 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  *   MK_DBG_UNION         int32 [n_layers]                distinct experts per layer
  *   MK_DBG_TASKS         int32 [num_tasks, 12]           the task list in CTA order
  *                        (type, layer, a0..a7, wait counter, wait count)
- *   MK_DBG_TRACE         uint64 [num_tasks, 10]          globaltimer stamps (ns) per task:
+ *   MK_DBG_TRACE         uint64 [num_tasks, 12]          globaltimer stamps (ns) per task:
  *                        consumer fetched, dependency met, activations ready, stages
  *                        consumed, done; producer first copy, last copy, start;
- *                        first and last stage landed (needs opts.trace)
+ *                        first and last stage landed; two steps inside the activation
+ *                        part (gate/up: norm done, routing done); 0 = not recorded
+ *                        (needs opts.trace)
  *   MK_DBG_STAGE_TRACE   uint64 [num_ctas, 4096, 6]      per CTA, its ring stages in order:
  *                        copy issued, landed (seen by the first consumer warp), released
  *                        (globaltimer ns, 0 = not reached), the task index, and the SM's

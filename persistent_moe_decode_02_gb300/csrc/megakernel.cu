@@ -54,6 +54,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Flag handoff between this CTA's consumers and its producer thread.
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 // Non-blocking probe: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -244,8 +254,13 @@ struct Misc {
   float best_v[NCW * MAX_BATCH];
   int best_i[NCW * MAX_BATCH];
   int sel[MAX_BATCH * MAX_TOPK];
+  float selv[MAX_BATCH * MAX_TOPK];
+  float gate[MAX_BATCH * MAX_TOPK];
+  float rl[MAX_BATCH * MAX_EXPERTS];   // router logits of the layer being routed
   int slot_of[MAX_EXPERTS];
   int cnt_of[MAX_EXPERTS];
+  int r_U;                 // distinct experts of the routing in r_exp...
+  int r_layer;             // layer whose routing r_exp... holds after a gate/up task computed it (-1: none)
   // routing of the current layer, cached per task
   int r_exp[MAX_UNION];
   int r_cnt[MAX_UNION];
@@ -366,8 +381,10 @@ struct Geo {
   uint32_t PB;
   // gate/up and down: the routing cache the task reads
   const RouteCache* rc;
-  long long q0, q1;
+  int q0, q1;   // gate/up: flattened (distinct expert, ffn row) range
   int pps, spe;
+  // gate/up stage cursor: stage cs starts at pair cf of distinct expert cu
+  int cs, cu, cf;
 };
 
 // Producer: one thread that walks the CTA's tasks and fills the ring.  It
@@ -397,18 +414,47 @@ struct Producer {
     if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
   }
 
-  // Routing of layer l into cache c (once per layer).  wait: block (bounded)
-  // for the router; otherwise return false if it has not finished.
-  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task) {
+  // Routing of layer l into cache c (once per layer).  A gate/up task of this
+  // CTA computes it and hands it over in shared memory; a down task whose CTA
+  // had no gate/up task of the layer reads the table that the first gate/up
+  // task publishes in global memory.  wait: block (bounded); otherwise return
+  // false if the routing is not known yet.
+  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task, bool local_only) {
     if (c->layer == l) return true;
-    if (!wait) {
-      if ((int32_t)(ld_acquire(p.ctr + (size_t)(p.cm.rdone + l) * CTR_STRIDE) - p.epoch) < 0) return false;
-    } else if (!wait_ctr(p, p.cm.rdone + l, 1, task)) {
-      return false;
+    Misc* m = r.m;
+    if (ld_acquire_cta(&m->r_layer) != l) {
+      if (!wait && local_only) return false;
+      if (local_only) {
+        // this task's consumers compute the routing once their router inputs
+        // land; poll with plain loads (no fence per poll), acquire once seen
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1; *(volatile int*)&m->r_layer != l; ++it) {
+          if ((it & 7) == 0) {
+            if (*(volatile int*)&m->abort_flag || failed(p)) return false;
+            if (gtimer() - t0 > p.timeout_ns) {
+              set_error(p, MK_ERR_DEP_TIMEOUT, task, -5);
+              return false;
+            }
+          }
+          __nanosleep(128);
+        }
+        if (ld_acquire_cta(&m->r_layer) != l) return false;
+      } else {
+        if (!wait) {
+          if ((int32_t)(ld_acquire(p.ctr + (size_t)(p.cm.rdone + l) * CTR_STRIDE) - p.epoch) < 0) return false;
+        } else if (!wait_ctr(p, p.cm.rdone + l, 1, task)) {
+          return false;
+        }
+        const int* rt = route_of(p, l);
+        const int U = __ldcg(rt);
+        for (int u = 0; u < U; ++u) c->exp[u] = __ldcg(rt + 1 + u);
+        c->U = U;
+        c->layer = l;
+        return true;
+      }
     }
-    const int* rt = route_of(p, l);
-    const int U = __ldcg(rt);
-    for (int u = 0; u < U; ++u) c->exp[u] = __ldcg(rt + 1 + u);
+    const int U = m->r_U;
+    for (int u = 0; u < U; ++u) c->exp[u] = m->r_exp[u];
     c->U = U;
     c->layer = l;
     return true;
@@ -444,23 +490,27 @@ struct Producer {
         return true;
       }
       case T_GU: {
-        if (!route_ready(c, l, wait, task)) return false;
+        if (!route_ready(c, l, wait, task, true)) return false;
         q.rc = c;
-        gu_range(p, t, c->U, q.q0, q.q1);
+        long long g0, g1;
+        gu_range(p, t, c->U, g0, g1);
+        q.q0 = (int)g0;
+        q.q1 = (int)g1;
         q.pps = pairs_per_stage(p);
+        const int F = p.F;
         int n = 0;
-        for (long long x = q.q0; x < q.q1;) {
-          const int u = (int)(x / p.F);
-          const int fa = (int)(x - (long long)u * p.F);
-          const int fb = (int)min((long long)p.F, q.q1 - (long long)u * p.F);
+        for (int u = q.q0 / F; u * F < q.q1; ++u) {
+          const int fa = max(q.q0 - u * F, 0), fb = min(F, q.q1 - u * F);
           n += (fb - fa + q.pps - 1) / q.pps;
-          x = (long long)(u + 1) * p.F;
         }
         q.nst = n;
+        q.cs = 0;
+        q.cu = q.q0 / F;
+        q.cf = q.q0 - q.cu * F;
         return true;
       }
       case T_DOWN: {
-        if (!route_ready(c, l, wait, task)) return false;
+        if (!route_ready(c, l, wait, task, false)) return false;
         q.rc = c;
         q.r0 = t.a[0];
         q.r1 = t.a[1];
@@ -478,8 +528,10 @@ struct Producer {
   }
 
   // Calls f(src, bytes, dst_offset) for each contiguous piece of stage s.
+  // Gate/up stages are walked with a cursor kept in the geometry, so stages
+  // visited in order cost O(1) each.
   template <class F>
-  __device__ void segs(const Geo& q, int s, F f) {
+  __device__ void segs(Geo& q, int s, F f) {
     const int l = q.l;
     switch (q.type) {
       case T_QKV: case T_OPROJ: case T_ROUTER: case T_LM: {
@@ -501,22 +553,24 @@ struct Producer {
       }
       case T_GU: {
         const int F = p.F, H = p.H;
-        int left = s;
-        for (long long x = q.q0; x < q.q1;) {
-          const int u = (int)(x / F);
-          const int fa = (int)(x - (long long)u * F);
-          const int fb = (int)min((long long)F, q.q1 - (long long)u * F);
-          const int ns = (fb - fa + q.pps - 1) / q.pps;
-          if (left < ns) {
-            const int f0 = fa + left * q.pps;
-            const int n = min(q.pps, fb - f0);
-            const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[u] * 2 * F * H;   // rows 2f, 2f+1
-            f(We + (size_t)2 * f0 * H, (uint32_t)n * 2 * H * 2, 0u);
-            return;
-          }
-          left -= ns;
-          x = (long long)(u + 1) * F;
+        if (s < q.cs) {   // rewind
+          q.cs = 0;
+          q.cu = q.q0 / F;
+          q.cf = q.q0 - q.cu * F;
         }
+        while (q.cs < s) {   // advance one stage: pps pairs, or to the end of this expert's range
+          const int fb = min(F, q.q1 - q.cu * F);
+          q.cf += q.pps;
+          if (q.cf >= fb) {
+            ++q.cu;
+            q.cf = 0;
+          }
+          ++q.cs;
+        }
+        const int fb = min(F, q.q1 - q.cu * F);
+        const int n = min(q.pps, fb - q.cf);
+        const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
+        f(We + (size_t)2 * q.cf * H, (uint32_t)n * 2 * H * 2, 0u);
         break;
       }
       case T_DOWN: {
@@ -530,7 +584,7 @@ struct Producer {
     }
   }
 
-  __device__ void prefetch_stage(const Geo& q, int s) {
+  __device__ void prefetch_stage(Geo& q, int s) {
     segs(q, s, [&](const void* src, uint32_t bytes, uint32_t) { prefetch_l2_bulk(src, bytes); });
   }
 
@@ -1042,55 +1096,68 @@ struct Consumer {
     });
   }
 
-  // Top-k of every request's router logits, gates, and the distinct-expert list.
-  __device__ void route_finish(int l) {
+  // Routing of layer l from its router logits (m->rl), computed in every
+  // gate/up task the same way, so every CTA gets the same bits:
+  //  - per request, each expert's rank: how many logits are greater, or equal
+  //    with a lower index (NaN counts as -inf), so ranks are a permutation;
+  //    the top-k are the ranks below k, in rank order;
+  //  - gates: softmax over the selected logits;
+  //  - the distinct experts in ascending order, with their (request, rank)
+  //    pairs in request order (r_U, r_exp, r_cnt, r_tok, r_rank).
+  // Then the table is handed to this CTA's producer (r_layer).  With publish
+  // set it also goes to global memory (ids, gates, routing table) and the
+  // rdone counter is signalled.
+  // Expects m->rl loaded and m->cnt_of zeroed, both behind a barrier.
+  __device__ void route_local(int l, bool publish) {
     const int E = p.E, k = p.k, B = p.B;
-    int* rt = const_cast<int*>(route_of(p, l));
-    constexpr int NV = MAX_EXPERTS / 32;
-    if (cw < B) {
-      const int b = cw;
-      const float* rl = p.rlog + ((size_t)l * p.bcap + b) * E;
-      float v[NV];
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
+    const int umax = p.rm.umax, bc = p.rm.bcap;
+    // ranks: two threads per candidate when they fit, each counting half the row
+    const int split = 2 * B * E <= NCT ? 2 : 1;
+    const int per = NCT / split;
+    for (int c0 = 0; c0 < B * E; c0 += per) {
+      const int c = c0 + ct / split, half = ct & (split - 1);
+      const bool valid = c < B * E;
+      const int b = valid ? c / E : 0, e = valid ? c - b * E : 0;
+      const float* row = m->rl + b * E;
+      const float v = row[e];
+      const int e_lo = split == 2 ? half * (E >> 1) : 0, e_hi = split == 2 ? (half ? E : E >> 1) : E;
+      // four independent counts over float4 loads when every half-row starts
+      // 16-byte aligned (E a multiple of 8), else one at a time
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      int e2 = e_lo;
+      const int vec_hi = (E & 7) == 0 ? e_hi : e_lo;
+      for (; e2 + 4 <= vec_hi; e2 += 4) {
+        const float4 w = *reinterpret_cast<const float4*>(row + e2);
+        r0 += (w.x > v) || (w.x == v && e2 < e);
+        r1 += (w.y > v) || (w.y == v && e2 + 1 < e);
+        r2 += (w.z > v) || (w.z == v && e2 + 2 < e);
+        r3 += (w.w > v) || (w.w == v && e2 + 3 < e);
       }
-      float selv = 0.f, first = 0.f;
-      int mysel = 0;
-      for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float ov = __shfl_xor_sync(FULL, bv, o);
-          const int oi = __shfl_xor_sync(FULL, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-          if (lane + 32 * i == bi) v[i] = -INFINITY;
-        if (j == 0) first = bv;
-        if (lane == j) { selv = bv; mysel = bi; }
-      }
-      const float ex = lane < k ? expf(selv - first) : 0.f;
-      const float tot = warp_sum(ex);
-      if (lane < k) {
-        p.ids[((size_t)l * p.bcap + b) * k + lane] = mysel;
-        p.gates[((size_t)l * p.bcap + b) * k + lane] = ex / tot;
-        m->sel[b * k + lane] = mysel;
+      for (; e2 < e_hi; ++e2) r0 += (row[e2] > v) || (row[e2] == v && e2 < e);
+      int rank = (r0 + r1) + (r2 + r3);
+      if (split == 2) rank += __shfl_xor_sync(FULL, rank, 1);
+      if (valid && half == 0 && rank < k) {
+        m->sel[b * k + rank] = e;
+        m->selv[b * k + rank] = v;
+        atomicAdd(&m->cnt_of[e], 1);
       }
     }
-    if (ct < MAX_EXPERTS) m->cnt_of[ct] = 0;
     cbar();
-    if (ct < B * k) atomicAdd(&m->cnt_of[m->sel[ct]], 1);
-    cbar();
-    const int umax = p.rm.umax, bc = p.rm.bcap;
+    // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
+    // groups of kp consecutive lanes (kp = k rounded up to a power of two)
+    {
+      int kp = 1;
+      while (kp < k) kp <<= 1;
+      const int per_warp = 32 / kp;
+      const int b = (cw - 1) * per_warp + lane / kp, j = lane % kp;
+      const bool mine = cw >= 1 && b < B;             // uniform per warp but for the tail
+      const bool act_j = mine && j < k;
+      const float first = mine ? m->selv[b * k] : 0.f;
+      const float ex = act_j ? expf(m->selv[b * k + j] - first) : 0.f;
+      float tot = ex;
+      for (int o = 1; o < kp; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
+      if (act_j) m->gate[b * k + j] = ex / tot;
+    }
     if (cw == 0) {
       int base = 0;
       for (int c = 0; c < (E + 31) / 32; ++c) {
@@ -1100,12 +1167,12 @@ struct Consumer {
         if (pres) {
           const int u = base + __popc(mask & ((1u << lane) - 1u));
           m->slot_of[e] = u;
-          rt[1 + u] = e;
-          rt[1 + umax + u] = m->cnt_of[e];
+          m->r_exp[u] = e;
+          m->r_cnt[u] = m->cnt_of[e];
         }
         base += __popc(mask);
       }
-      if (lane == 0) rt[0] = base;
+      if (lane == 0) m->r_U = base;
     }
     cbar();
     if (ct < B * k) {
@@ -1113,14 +1180,33 @@ struct Consumer {
       int rank = 0;
       for (int q = 0; q < ct; ++q) rank += (m->sel[q] == e);
       const int u = m->slot_of[e];
-      rt[1 + 2 * umax + u * bc + rank] = ct / k;
-      rt[1 + 2 * umax + umax * bc + u * bc + rank] = ct % k;
+      m->r_tok[u * bc + rank] = ct / k;
+      m->r_rank[u * bc + rank] = ct % k;
     }
+    cbar();
+    if (ct == 0) st_release_cta(&m->r_layer, l);
+    if (!publish) return;
+    int* rt = const_cast<int*>(route_of(p, l));
+    const int U = m->r_U;
+    if (ct == 0) rt[0] = U;
+    for (int u = ct; u < U; u += NCT) {
+      rt[1 + u] = m->r_exp[u];
+      rt[1 + umax + u] = m->r_cnt[u];
+    }
+    for (int i = ct; i < U * bc; i += NCT) {
+      rt[1 + 2 * umax + i] = m->r_tok[i];
+      rt[1 + 2 * umax + umax * bc + i] = m->r_rank[i];
+    }
+    if (ct < B * k) {
+      p.ids[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->sel[ct];
+      p.gates[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->gate[ct];
+    }
+    cbar();
+    signal(p.cm.rdone + l);
   }
 
   __device__ bool router(const Task& t, bool ab) {
     const int l = t.layer;
-    // (the finisher below publishes act = rmsnorm(x_mid) * gamma for the gate/up tasks)
     if (!ab) fill_ffn_norm(l);
     cbar();
     mark(TR_ACT);
@@ -1129,17 +1215,7 @@ struct Consumer {
                      [&](int row, int j, float s, float) { rl[(size_t)j * p.E + row] = s; });
     mark(TR_STAGES);
     ab = finish(ab);
-    if (ab) return ab;
-    if (ticket(p.cm.rticket + l, (uint32_t)t.a[2])) {
-      {
-        float4* dst = reinterpret_cast<float4*>(p.xnf + (size_t)l * p.bcap * p.H);
-        const float4* src = reinterpret_cast<const float4*>(act);
-        for (int i = ct; i < (p.B * p.H) >> 2; i += NCT) dst[i] = src[i];
-      }
-      route_finish(l);
-      ab = finish(false);
-      if (!ab) signal(p.cm.rdone + l);
-    }
+    if (!ab) signal(p.cm.rticket + l);
     return ab;
   }
 
@@ -1147,11 +1223,20 @@ struct Consumer {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
     if (!ab) {
-      U = load_route(l);
-      const float4* src = reinterpret_cast<const float4*>(p.xnf + (size_t)l * p.bcap * H);
-      float4* dst = reinterpret_cast<float4*>(act);
-#pragma unroll 4
-      for (int i = ct; i < (p.B * H) >> 2; i += NCT) dst[i] = __ldcg(src + i);
+      // router logits for the local top-k, loaded in the same round trip as
+      // the norm's inputs (the fill's barrier publishes them)
+      const float* rlg = p.rlog + (size_t)l * p.bcap * p.E;
+      for (int i = ct; i < p.B * p.E; i += NCT) {
+        const float v = __ldcg(rlg + i);
+        m->rl[i] = v == v ? v : -INFINITY;
+      }
+      for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
+      fill_ffn_norm(l);
+      cbar();
+      mark(TR_MID1);
+      if (m->r_layer != l || t.a[0] == 0) route_local(l, t.a[0] == 0);
+      mark(TR_MID2);
+      U = m->r_U;
     }
     cbar();
     mark(TR_ACT);
@@ -1182,7 +1267,7 @@ struct Consumer {
     const float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
     int U = 0;
     if (!ab) {
-      U = load_route(l);
+      U = m->r_layer == l ? m->r_U : load_route(l);
       if (p.allh) {
         const float4* src = reinterpret_cast<const float4*>(hb);
         float4* dst = reinterpret_cast<float4*>(act);
@@ -1714,6 +1799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
       m->armed[s] = -1;
     }
     m->abort_flag = 0;
+    m->r_layer = -1;
     m->dead = failed(p) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }

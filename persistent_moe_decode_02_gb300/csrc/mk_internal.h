@@ -16,7 +16,7 @@ constexpr int MAX_EXPERTS = 256;
 constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
 constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
 constexpr int WIN_ROWS = 32;               // rows per cross-warp partial-sum window (wide GEMV)
-constexpr int TRACE_SLOTS = 10;            // stamps per task in the optional timeline
+constexpr int TRACE_SLOTS = 12;            // stamps per task in the optional timeline
 constexpr int STRACE_CAP = 4096;           // ring stages per CTA in the optional stage timeline
 constexpr int STRACE_SLOTS = 6;            // per stage: copy issued, landed, released, task,
                                            // and SM clock64 at landed and released
@@ -24,7 +24,7 @@ constexpr int STRACE_SLOTS = 6;            // per stage: copy issued, landed, re
 // stages consumed / done; producer first copy / last copy / task start;
 // consumer warp 0 saw its first / last stage of the task land
 enum TraceSlot { TR_FETCH = 0, TR_DEP, TR_ACT, TR_STAGES, TR_DONE, TR_P_FIRST, TR_P_LAST, TR_P_START,
-                 TR_S_FIRST, TR_S_LAST };
+                 TR_S_FIRST, TR_S_LAST, TR_MID1, TR_MID2 };   // MID1/2: steps inside a task's activation part
 
 // Task kinds in per-layer order.  Each kind signals one counter family.
 enum TaskType : int32_t {
@@ -32,8 +32,9 @@ enum TaskType : int32_t {
   T_ATTN = 1,    // request a0, KV group a1, KV pages [a2, a3) (a3 < 0: to the current end);
                  // a4 = partial slot, a5 = first slot of (a0, a1), a6 = chunks of (a0, a1)
   T_OPROJ = 2,   // rows [a0,a1) of Wo, residual add
-  T_ROUTER = 3,  // rows [a0,a1) of the router; a2 = router tiles (ticket target)
-  T_GU = 4,      // gate/up tile a0 of a1 over the flattened (distinct expert, ffn row) space
+  T_ROUTER = 3,  // rows [a0,a1) of the router
+  T_GU = 4,      // gate/up tile a0 of a1 over the flattened (distinct expert, ffn row) space;
+                 // computes the layer's routing from the router logits (tile 0 publishes it)
   T_DOWN = 5,    // rows [a0,a1) of the hidden dim over every selected expert, residual add
   T_LM = 6,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
   T_COMB = 7,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
@@ -130,7 +131,6 @@ struct Params {
   float* o;             // [L][bcap][nq*d]
   float* x_mid;         // [L][bcap][H]
   float* x_out;         // [L][bcap][H]
-  float* xnf;           // [L][bcap][H] rmsnorm(x_mid) * ffn gain, published by the router finisher
   float* rlog;          // [L][bcap][E]
   int* ids;             // [L][bcap][k]
   float* gates;         // [L][bcap][k]

@@ -204,11 +204,10 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
       mk::Task t = task(mk::T_ROUTER, l, cm.o + l, (uint32_t)c.o);
       t.a[0] = a;
       t.a[1] = b;
-      t.a[2] = c.router;
       put(next(), t);
     }
     for (int i = 0; i < c.gu; ++i) {
-      mk::Task t = task(mk::T_GU, l, cm.rdone + l, 1u);
+      mk::Task t = task(mk::T_GU, l, cm.rticket + l, (uint32_t)c.router);
       t.a[0] = i;
       t.a[1] = c.gu;
       put(next(), t);
@@ -325,7 +324,6 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_o = dc.take(L * B * s.nq * s.d * sizeof(float));
   const size_t d_xm = dc.take(L * B * s.H * sizeof(float));
   const size_t d_xo = dc.take(L * B * s.H * sizeof(float));
-  const size_t d_xn = dc.take(L * B * s.H * sizeof(float));
   const size_t d_rl = dc.take(L * B * s.E * sizeof(float));
   const size_t d_ids = dc.take(L * B * s.k * sizeof(int));
   const size_t d_gt = dc.take(L * B * s.k * sizeof(float));
@@ -433,7 +431,6 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.o = (float*)(base + d_o);
   P.x_mid = (float*)(base + d_xm);
   P.x_out = (float*)(base + d_xo);
-  P.xnf = (float*)(base + d_xn);
   P.rlog = (float*)(base + d_rl);
   P.ids = (int*)(base + d_ids);
   P.gates = (float*)(base + d_gt);

@@ -234,21 +234,20 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     }
     asg.phase(ph);
     ph.clear();
-    // router logits (last tile also takes the top-k)
+    // router logits (every gate/up task takes the top-k from them)
     for (int i = 0; i < cnt.router; ++i) {
       int a, b;
       split_range(s.E, cnt.router, i, a, b);
       Task t = mk_task(mk::T_ROUTER, l, cm.o + l, (uint32_t)cnt.o);
       t.a[0] = a;
       t.a[1] = b;
-      t.a[2] = cnt.router;
       ph.push_back({(double)(b - a) * s.H * 2, t});
     }
     asg.phase(ph);
     ph.clear();
     // expert gate/up tiles over the distinct selected experts
     for (int i = 0; i < cnt.gu; ++i) {
-      Task t = mk_task(mk::T_GU, l, cm.rdone + l, 1u);
+      Task t = mk_task(mk::T_GU, l, cm.rticket + l, (uint32_t)cnt.router);
       t.a[0] = i;
       t.a[1] = cnt.gu;
       ph.push_back({(double)umax * s.F * 4.0 * s.H / cnt.gu, t});
@@ -660,7 +659,6 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   ok &= dalloc(p, &P.o, L * bcap * s.nq * s.d * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_mid, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.x_out, L * bcap * s.H * sizeof(float)) == cudaSuccess;
-  ok &= dalloc(p, &P.xnf, L * bcap * s.H * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.rlog, L * bcap * s.E * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.ids, L * bcap * s.k * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &P.gates, L * bcap * s.k * sizeof(float)) == cudaSuccess;

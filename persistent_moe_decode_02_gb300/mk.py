@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(_HERE, "libmk.so")
 MK_OK, MK_ERR_INVALID, MK_ERR_CUDA, MK_ERR_DEP_TIMEOUT, MK_ERR_CAPACITY, MK_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 MK_DBG_HIDDEN, MK_DBG_EXPERT_IDS, MK_DBG_GATES, MK_DBG_ROUTER_LOGITS, MK_DBG_SEQ_LENS, MK_DBG_UNION = 1, 2, 3, 4, 5, 6
 MK_DBG_TASKS, MK_DBG_TRACE, MK_DBG_STAGE_TRACE = 7, 8, 9
-TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start", "s_first", "s_last"]
+TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_start", "s_first", "s_last",
+               "mid1", "mid2"]
 
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",

@@ -87,7 +87,7 @@ def signals_per_step(D, B, tasks):
         elif typ == T_COMB:
             sig[base["combine"] + l] += 1
     for l in range(L):
-        sig[base["rdone"] + l] = 1             # the router finisher
+        sig[base["rdone"] + l] = 1             # gate/up tile 0 publishes the routing table
     return sig, base
 
 
@@ -151,17 +151,10 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
             out.append(base["combine"] + l)
         return out
 
-    # emulate with the router finisher's counter derived from ticket completion
-    router_need = {t[1]: t[4] for t in tasks.tolist() if t[0] == T_ROUTER}
-    got = defaultdict(int)
-
     def fires_with_finishers(t):
         out = fires(t)
-        typ, l, a = t[0], t[1], t[2:10]
-        if typ == T_ROUTER:
-            got[("r", l)] += 1
-            if got[("r", l)] == router_need[l]:
-                out.append(base["rdone"] + l)
+        if t[0] == T_GU and t[2] == 0:
+            out.append(base["rdone"] + t[1])
         return out
 
     order = emulate(tasks, cs, fires_with_finishers)
