@@ -946,6 +946,48 @@ struct Consumer {
       for (int s0 = r0; s0 < r1; s0 += rps) {
         const int n = min(rps, r1 - s0);
         const uint8_t* st = wait_stage(ab);
+        if constexpr (!PAIRS && NB <= 2) {
+          if (st && n <= 2 * NCW) {
+            // short stage (the expert down rows of one CTA): warp w takes rows
+            // w and w + 8 whole, two independent chains, one warp sum each
+            const uint32_t sts = smem_u32(st);
+            const bool va = cw < n, vb = cw + NCW < n;
+            float pa[NB], pb[NB];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) pa[j] = pb[j] = 0.f;
+#pragma unroll 3
+            for (int gi = lane; gi < ng; gi += 32) {
+              float4 x0[NB], x1[NB];
+#pragma unroll
+              for (int j = 0; j < NB; ++j) {
+                x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+              if (va) {
+                const uint4 wv = lds128(sts + (uint32_t)cw * rowb + gi * 16);
+#pragma unroll
+                for (int j = 0; j < NB; ++j) pa[j] += dot8r(wv, x0[j], x1[j]);
+              }
+              if (vb) {
+                const uint4 wv = lds128(sts + (uint32_t)(cw + NCW) * rowb + gi * 16);
+#pragma unroll
+                for (int j = 0; j < NB; ++j) pb[j] += dot8r(wv, x0[j], x1[j]);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              if (j < nb) {
+                const float sa = warp_sum(pa[j]), sb = warp_sum(pb[j]);
+                if (lane == 0) {
+                  if (va) epi(s0 + cw, j, sa, 0.f);
+                  if (vb) epi(s0 + cw + NCW, j, sb, 0.f);
+                }
+              }
+            }
+            release_stage(ab);
+            continue;
+          }
+        }
         if (st) {
           const uint32_t sts = smem_u32(st);
           // PAIRS: warp w takes pairs w, w+8, ... (rows 2f, 2f+1); else rows w, w+8, ...
