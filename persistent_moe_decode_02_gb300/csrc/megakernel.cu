@@ -232,6 +232,24 @@ __device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
   return c;
 }
 
+// Same for 4 values: lane l returns the 32-lane sum of v[(l >> 3) & 3].
+__device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
+  float a[2];
+  const bool u16 = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u16 ? v[i] : v[i + 2];
+    const float keep = u16 ? v[i + 2] : v[i];
+    a[i] = keep + __shfl_xor_sync(FULL, send, 16);
+  }
+  const bool u8 = lane & 8;
+  float c = (u8 ? a[1] : a[0]) + __shfl_xor_sync(FULL, u8 ? a[0] : a[1], 8);
+  c += __shfl_xor_sync(FULL, c, 4);
+  c += __shfl_xor_sync(FULL, c, 2);
+  c += __shfl_xor_sync(FULL, c, 1);
+  return c;
+}
+
 // ------------------------------------------------------------------ shared state
 
 constexpr int MAX_UNION = MAX_BATCH * MAX_TOPK;   // distinct experts a step can select
@@ -851,7 +869,48 @@ struct Consumer {
         const uint8_t* st = wait_stage(ab);
         if (st) {
           const uint32_t sts = smem_u32(st);
-          for (int rb = 0; rb < n; rb += 8) {
+          bool done4 = false;
+          if constexpr (NB <= 2) {
+            if (n <= 4) {
+              // 4-row stage (K = 4096 at 32 KB): 4 chains, 4-value reduction
+              float part4[4][NB];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < NB; ++j) part4[q][j] = 0.f;
+              for (int sw = 0; sw < spw; ++sw) {
+                const int gi = (cw + NCW * sw) * 32 + lane;
+                float4 x0[NB], x1[NB];
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                uint4 wv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  wv[q] = q < n ? lds128(sts + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) part4[q][j] += dot8r(wv[q], x0[j], x1[j]);
+              }
+              float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
+#pragma unroll
+              for (int j = 0; j < NB; ++j) {
+                if (j < nb) {
+                  float v[4];
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) v[q] = part4[q][j];
+                  const float sum = reduce4(v, lane);
+                  const int q = (lane >> 3) & 3;
+                  if ((lane & 7) == 0 && q < n) ps[(wrow + q) * NB + j] = sum;
+                }
+              }
+              done4 = true;
+            }
+          }
+          for (int rb = 0; rb < n && !done4; rb += 8) {
             float part[8][NB];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
