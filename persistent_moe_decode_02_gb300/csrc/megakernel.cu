@@ -1487,37 +1487,49 @@ struct Consumer {
     mark(TR_ACT);
     const int gq = lane >> 2, tq = lane & 3;       // mma fragment coordinates
     const int nks = d >> 4;                        // 16-dim k steps (QK) = 16-dim row tiles (PV)
-    // B fragments of Q^T per k step: rows (dims) 2tq, 2tq+1 and +8, column (head) gq
-    uint32_t qh[8][2], ql[8][2];
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    // B fragments of Q^T per k step and lane (rows (dims) 2tq, 2tq+1 and +8,
+    // column (head) gq), as bf16 hi + lo pairs, in a shared table: one
+    // 16-byte read per k step instead of 32 registers held across the chunk
+    // the table takes the place of q_s (d/16 k steps x 32 lanes x 16 bytes =
+    // MAX_G * d floats): every thread reads its entry's q values first, then
+    // all write after a barrier
+    static_assert(NCT == 8 * 32, "one table entry per consumer thread");
+    uint4* qtab = reinterpret_cast<uint4*>(q_s);   // [8 k steps][32 lanes]
+    {
+      const int ks = ct >> 5, L = ct & 31, gqL = L >> 2, tqL = L & 3;
+      uint32_t w[4];
 #pragma unroll
       for (int hfi = 0; hfi < 2; ++hfi) {
         float x0 = 0.f, x1 = 0.f;
         if (ks < nks) {
-          x0 = q_s[gq * d + ks * 16 + hfi * 8 + 2 * tq];
-          x1 = q_s[gq * d + ks * 16 + hfi * 8 + 2 * tq + 1];
+          x0 = q_s[gqL * d + ks * 16 + hfi * 8 + 2 * tqL];
+          x1 = q_s[gqL * d + ks * 16 + hfi * 8 + 2 * tqL + 1];
         }
         const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
-        qh[ks][hfi] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        ql[ks][hfi] = (uint32_t)f2bf(x0 - bf2f(h0)) | ((uint32_t)f2bf(x1 - bf2f(h1)) << 16);
+        w[hfi] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        w[2 + hfi] = (uint32_t)f2bf(x0 - bf2f(h0)) | ((uint32_t)f2bf(x1 - bf2f(h1)) << 16);
       }
+      cbar();
+      if (ks < nks) qtab[ct] = make_uint4(w[0], w[1], w[2], w[3]);   // nks * 32 entries = MAX_G * d floats
     }
+    cbar();
+    const uint32_t qtab_lane = smem_u32(qtab) + (uint32_t)lane * 16;
     const int ppg = pages_per_stage(p);
-    const int wpp = NCW / ppg;                     // warps per page
-    const int grp = cw / wpp, sub = cw - grp * wpp;
-    const int mtw = nks / wpp;                     // output row tiles per warp
+    const int npar = NCW / ppg;                    // stages in flight: warp (par, grp) takes page
+    const int par = cw / ppg, grp = cw - par * ppg;  // grp of every npar-th stage, starting at par
+    const int mtw = nks;                           // output row tiles per warp (all of d)
     const uint32_t PB = (uint32_t)d * PS * 2;      // bytes of one page block
     // online-softmax state of heads 2tq, 2tq+1 (identical across gq) and O^T tiles
     float mr0 = -INFINITY, mr1 = -INFINITY, lr0 = 0.f, lr1 = 0.f;
-    float o[4][4];
+    float o[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
     uint32_t* myp = pscr + cw * 2 * 64;            // this warp's packed P^T: [hi/lo][head 8][tok/2 8]
     const int pg0 = tok0 / PS, pg1 = (tok1 + PS - 1) / PS;
-    for (int pg = pg0; pg < pg1; pg += ppg) {
+    int si = 0;                                    // stage index within the chunk
+    for (int pg = pg0; pg < pg1; pg += ppg, ++si) {
       const int npg = min(ppg, pg1 - pg);
       const uint8_t* st = wait_stage(ab);
       if (st && has_new && pos / PS >= pg && pos / PS < pg + npg) {
@@ -1545,7 +1557,7 @@ struct Consumer {
         cbar();
         cbar();
       }
-      if (st && grp < npg) {
+      if (st && si % npar == par && grp < npg) {
         const int P = pg + grp;                    // global page index of this warp's page
         const int nvalid = min(PS, tok1 - P * PS); // tokens of the page inside the chunk
         const uint32_t kpage = smem_u32(st) + grp * PB;
@@ -1559,8 +1571,9 @@ struct Consumer {
             const uint32_t addr = kpage + (uint32_t)((ks * 16 + (li >> 1) * 8 + lr) * PS * 2 + (li & 1) * 16);
             uint32_t a0, a1, a2, a3;
             ldsm_x4_trans(addr, a0, a1, a2, a3);
-            mma_bf16(s, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
-            mma_bf16(sl, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+            const uint4 qf = lds128(qtab_lane + (uint32_t)ks * 512);
+            mma_bf16(s, a0, a1, a2, a3, qf.x, qf.y);
+            mma_bf16(sl, a0, a1, a2, a3, qf.z, qf.w);
           }
         }
 #pragma unroll
@@ -1589,7 +1602,7 @@ struct Consumer {
         mr0 = mn0;
         mr1 = mn1;
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < 8; ++mt) {
           o[mt][0] *= sc0; o[mt][1] *= sc1; o[mt][2] *= sc0; o[mt][3] *= sc1;
         }
         // P^T as mma B operand: element (tok k, head n) packed per token pair;
@@ -1610,11 +1623,11 @@ struct Consumer {
         __syncwarp();
         const uint32_t bh0 = myp[gq * 8 + tq], bh1 = myp[gq * 8 + tq + 4];
         const uint32_t bl0 = myp[64 + gq * 8 + tq], bl1 = myp[64 + gq * 8 + tq + 4];
-        // O^T += V^T . P^T over this warp's row tiles (dims)
+        // O^T += V^T . P^T over all d/16 row tiles (dims)
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < 8; ++mt) {
           if (mt < mtw) {
-            const int m0 = (sub * mtw + mt) * 16;
+            const int m0 = mt * 16;
             const uint32_t addr = vpage + (uint32_t)((m0 + (li & 1) * 8 + lr) * PS * 2 + (li >> 1) * 16);
             uint32_t a0, a1, a2, a3;
             ldsm_x4(addr, a0, a1, a2, a3);
@@ -1626,27 +1639,26 @@ struct Consumer {
       release_stage(ab);
     }
     mark(TR_STAGES);
-    // merge the page groups' partial softmax states of this chunk
-    const int ngrp = ppg;
+    // merge the warps' partial softmax states of this chunk (a warp that saw
+    // no page keeps max -inf and drops out)
     if (!ab) {
-      if (sub == 0 && gq == 0) {
+      if (gq == 0) {
         if (2 * tq < G) {
-          mrg[(grp * G + 2 * tq) * RS + d] = mr0;
-          mrg[(grp * G + 2 * tq) * RS + d + 1] = lr0;
+          mrg[(cw * G + 2 * tq) * RS + d] = mr0;
+          mrg[(cw * G + 2 * tq) * RS + d + 1] = lr0;
         }
         if (2 * tq + 1 < G) {
-          mrg[(grp * G + 2 * tq + 1) * RS + d] = mr1;
-          mrg[(grp * G + 2 * tq + 1) * RS + d + 1] = lr1;
+          mrg[(cw * G + 2 * tq + 1) * RS + d] = mr1;
+          mrg[(cw * G + 2 * tq + 1) * RS + d + 1] = lr1;
         }
       }
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < 8; ++mt) {
         if (mt < mtw) {
-          const int m0 = (sub * mtw + mt) * 16;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int head = 2 * tq + (e & 1), dim = m0 + gq + 8 * (e >> 1);
-            if (head < G) mrg[(grp * G + head) * RS + dim] = o[mt][e];
+            const int head = 2 * tq + (e & 1), dim = mt * 16 + gq + 8 * (e >> 1);
+            if (head < G) mrg[(cw * G + head) * RS + dim] = o[mt][e];
           }
         }
       }
@@ -1655,25 +1667,29 @@ struct Consumer {
     if (ab) return ab;
     const int nslots = p.part_slots;
     float* part = p.part + ((size_t)l * nslots + t.a[4]) * G * RS;
-    const int ngrp_used = min(ngrp, pg1 - pg0);    // groups that saw at least one page
+    // per head: the chunk max, normaliser and each warp's weight, once
+    float* fw = reinterpret_cast<float*>(pscr);    // [NCW][G] weights (P scratch is free now)
+    if (ct < G) {
+      const int h = ct;
+      float M = -INFINITY;
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
+      float Ls = 0.f;
+      for (int w = 0; w < NCW; ++w) {
+        const float mw = mrg[(w * G + h) * RS + d];
+        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        fw[w * G + h] = f;
+        Ls = fmaf(mrg[(w * G + h) * RS + d + 1], f, Ls);
+      }
+      part[h * RS + d] = M;
+      part[h * RS + d + 1] = Ls;
+    }
+    cbar();
     for (int idx = ct; idx < G * d; idx += NCT) {
       const int h = idx / d, i = idx - h * d;
-      float M = -INFINITY;
-      for (int w = 0; w < ngrp_used; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
-      float Ls = 0.f, A = 0.f;
-      for (int w = 0; w < ngrp_used; ++w) {
-        const float mw = mrg[(w * G + h) * RS + d];
-        if (mw != -INFINITY) {
-          const float f = exp2f(mw - M);
-          Ls = fmaf(mrg[(w * G + h) * RS + d + 1], f, Ls);
-          A = fmaf(mrg[(w * G + h) * RS + i], f, A);
-        }
-      }
+      float A = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) A = fmaf(mrg[(w * G + h) * RS + i], fw[w * G + h], A);
       part[h * RS + i] = A;
-      if (i == 0) {
-        part[h * RS + d] = M;
-        part[h * RS + d + 1] = Ls;
-      }
     }
     ab = finish(ab);
     if (!ab) signal(p.cm.attn_idx(l, b, g));

@@ -166,8 +166,8 @@ inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bca
   const int RS = d + 4;
   int ppg32 = 32768 / (2 * ps * d * 2);
   if (ppg32 < 1) ppg32 = 1;
-  const long long mrg = (long long)ppg32 * G * RS > 128LL * G ? (long long)ppg32 * G * RS : 128LL * G;
-  const long long A3 = (long long)MAX_G * d + 2 * d + mrg + NCW * 128;  // q, new K/V, states, P scratch
+  const long long mrg = (long long)NCW * G * RS;   // one softmax state per consumer warp
+  const long long A3 = (long long)MAX_G * d + 2 * d + mrg + NCW * 128;  // q (then its mma table), new K/V, states, P
   const long long Ah = (long long)bcap * k * F;
   o.allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
   long long act = A1 > A3 ? A1 : A3;
@@ -186,7 +186,7 @@ inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bca
   if (nst > MAX_STAGES) nst = MAX_STAGES;
   if (nst < 2) return false;
   const int ppg = sb / (2 * ps * d * 2) < 1 ? 1 : sb / (2 * ps * d * 2);
-  if (ppg > ppg32 || NCW % ppg != 0 || (d / 16) / (NCW / ppg) > 4) return false;
+  if (ppg > ppg32 || NCW % ppg != 0 || d / 16 > 8) return false;
   o.stage_bytes = sb;
   o.nstages = (int)nst;
   o.act_off = (int)(nst * sb);
