@@ -306,7 +306,7 @@ def our_arm(args, wl):
         dist.destroy_process_group()
 
 
-PHASES = ["QKV", "ATTN", "OPROJ", "ROUTER", "GATE_UP", "DOWN", "LM", "COMBINE"]
+PHASES = ["QKV", "ATTN", "OPROJ", "ROUTER", "EXPERT", "REDUCE", "LM", "COMBINE"]
 
 
 def summarize_timeline(tasks, stamps, step_ms) -> str:

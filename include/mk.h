@@ -64,7 +64,10 @@ typedef struct mk_model_dims {
  *   router[l]   [n_experts, hidden]
  *   w_gate_up[l][n_experts, 2*expert_ffn, hidden]: rows interleaved per ffn
  *               unit f: row 2f = gate row f, row 2f+1 = up row f
- *   w_down[l]   [n_experts, hidden, expert_ffn]
+ *   w_down[l]   [n_experts, expert_ffn, hidden]: the down projection stored
+ *               transposed per expert, row f = the hidden-size column of ffn
+ *               unit f (W_down[e][:, f]), so an expert tile reads the down
+ *               weights of its ffn units as contiguous rows
  * Every pointer must be 16-byte aligned. */
 typedef struct mk_weights {
   const void* embed;

@@ -284,7 +284,6 @@ struct Misc {
   int r_cnt[MAX_UNION];
   int r_tok[MAX_UNION * MAX_BATCH];
   int r_rank[MAX_UNION * MAX_BATCH];
-  int r_row[MAX_UNION * MAX_BATCH];   // act row of (slot, i) in the down task
   // the producer's copies of a layer's distinct experts, one per cursor
   RouteCache cp_route, pf_route;
 };
@@ -397,12 +396,14 @@ struct Geo {
   // attention
   int pg0, pg1, ppg, b, g;
   uint32_t PB;
-  // gate/up and down: the routing cache the task reads
+  // expert tile: the routing cache it reads, its flattened (distinct expert,
+  // ffn unit) range, gate/up stages first (pps units each), then down stages
+  // (rpw units each, rows of the transposed down matrix)
   const RouteCache* rc;
-  int q0, q1;   // gate/up: flattened (distinct expert, ffn row) range
-  int pps, spe;
-  // gate/up stage cursor: stage cs starts at pair cf of distinct expert cu
-  int cs, cu, cf;
+  int q0, q1;
+  int pps, rpw, nst_gu;
+  int cs, cu, cf;   // gate/up cursor: stage cs starts at unit cf of distinct expert cu
+  int ws, wu, wf;   // down cursor, the same for down stage ws
 };
 
 // Producer: one thread that walks the CTA's tasks and fills the ring.  It
@@ -432,44 +433,27 @@ struct Producer {
     if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
   }
 
-  // Routing of layer l into cache c (once per layer).  A gate/up task of this
-  // CTA computes it and hands it over in shared memory; a down task whose CTA
-  // had no gate/up task of the layer reads the table that the first gate/up
-  // task publishes in global memory.  wait: block (bounded); otherwise return
-  // false if the routing is not known yet.
-  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task, bool local_only) {
+  // Routing of layer l into cache c (once per layer): this CTA's expert
+  // tile computes it and hands it over in shared memory.  wait: block
+  // (bounded); otherwise return false if it is not known yet.
+  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task) {
     if (c->layer == l) return true;
     Misc* m = r.m;
     if (ld_acquire_cta(&m->r_layer) != l) {
-      if (!wait && local_only) return false;
-      if (local_only) {
-        // this task's consumers compute the routing once their router inputs
-        // land; poll with plain loads (no fence per poll), acquire once seen
-        const uint64_t t0 = gtimer();
-        for (uint32_t it = 1; *(volatile int*)&m->r_layer != l; ++it) {
-          if ((it & 7) == 0) {
-            if (*(volatile int*)&m->abort_flag || failed(p)) return false;
-            if (gtimer() - t0 > p.timeout_ns) {
-              set_error(p, MK_ERR_DEP_TIMEOUT, task, -5);
-              return false;
-            }
+      if (!wait) return false;
+      // poll with plain loads (no fence per poll), acquire once seen
+      const uint64_t t0 = gtimer();
+      for (uint32_t it = 1; *(volatile int*)&m->r_layer != l; ++it) {
+        if ((it & 7) == 0) {
+          if (*(volatile int*)&m->abort_flag || failed(p)) return false;
+          if (gtimer() - t0 > p.timeout_ns) {
+            set_error(p, MK_ERR_DEP_TIMEOUT, task, -5);
+            return false;
           }
-          __nanosleep(128);
         }
-        if (ld_acquire_cta(&m->r_layer) != l) return false;
-      } else {
-        if (!wait) {
-          if ((int32_t)(ld_acquire(p.ctr + (size_t)(p.cm.rdone + l) * CTR_STRIDE) - p.epoch) < 0) return false;
-        } else if (!wait_ctr(p, p.cm.rdone + l, 1, task)) {
-          return false;
-        }
-        const int* rt = route_of(p, l);
-        const int U = __ldcg(rt);
-        for (int u = 0; u < U; ++u) c->exp[u] = __ldcg(rt + 1 + u);
-        c->U = U;
-        c->layer = l;
-        return true;
+        __nanosleep(128);
       }
+      if (ld_acquire_cta(&m->r_layer) != l) return false;
     }
     const int U = m->r_U;
     for (int u = 0; u < U; ++u) c->exp[u] = m->r_exp[u];
@@ -507,36 +491,30 @@ struct Producer {
         q.nst = (q.pg1 - q.pg0 + q.ppg - 1) / q.ppg;
         return true;
       }
-      case T_GU: {
-        if (!route_ready(c, l, wait, task, true)) return false;
+      case T_MOE: {
+        if (!route_ready(c, l, wait, task)) return false;
         q.rc = c;
         long long g0, g1;
         gu_range(p, t, c->U, g0, g1);
         q.q0 = (int)g0;
         q.q1 = (int)g1;
         q.pps = pairs_per_stage(p);
+        q.rpw = rows_per_stage(p, p.H);
         const int F = p.F;
-        int n = 0;
+        int ngu = 0, nwd = 0;
         for (int u = q.q0 / F; u * F < q.q1; ++u) {
           const int fa = max(q.q0 - u * F, 0), fb = min(F, q.q1 - u * F);
-          n += (fb - fa + q.pps - 1) / q.pps;
+          ngu += (fb - fa + q.pps - 1) / q.pps;
+          nwd += (fb - fa + q.rpw - 1) / q.rpw;
         }
-        q.nst = n;
-        q.cs = 0;
-        q.cu = q.q0 / F;
-        q.cf = q.q0 - q.cu * F;
+        q.nst_gu = ngu;
+        q.nst = ngu + nwd;
+        q.cs = q.ws = 0;
+        q.cu = q.wu = q.q0 / F;
+        q.cf = q.wf = q.q0 - q.cu * F;
         return true;
       }
-      case T_DOWN: {
-        if (!route_ready(c, l, wait, task, false)) return false;
-        q.rc = c;
-        q.r0 = t.a[0];
-        q.r1 = t.a[1];
-        q.rps = rows_per_stage(p, p.F);
-        q.spe = (q.r1 - q.r0 + q.rps - 1) / q.rps;
-        q.nst = c->U * q.spe;
-        return true;
-      }
+      case T_RED:      // no weights: reads only the expert tiles' partials
       case T_COMB: {   // no weights: reads only partials
         q.nst = 0;
         return true;
@@ -569,34 +547,48 @@ struct Producer {
         }
         break;
       }
-      case T_GU: {
+      case T_MOE: {
         const int F = p.F, H = p.H;
-        if (s < q.cs) {   // rewind
-          q.cs = 0;
-          q.cu = q.q0 / F;
-          q.cf = q.q0 - q.cu * F;
-        }
-        while (q.cs < s) {   // advance one stage: pps pairs, or to the end of this expert's range
-          const int fb = min(F, q.q1 - q.cu * F);
-          q.cf += q.pps;
-          if (q.cf >= fb) {
-            ++q.cu;
-            q.cf = 0;
+        if (s < q.nst_gu) {
+          if (s < q.cs) {   // rewind
+            q.cs = 0;
+            q.cu = q.q0 / F;
+            q.cf = q.q0 - q.cu * F;
           }
-          ++q.cs;
+          while (q.cs < s) {   // advance one stage: pps units, or to the end of this expert's range
+            const int fb = min(F, q.q1 - q.cu * F);
+            q.cf += q.pps;
+            if (q.cf >= fb) {
+              ++q.cu;
+              q.cf = 0;
+            }
+            ++q.cs;
+          }
+          const int fb = min(F, q.q1 - q.cu * F);
+          const int n = min(q.pps, fb - q.cf);
+          const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
+          f(We + (size_t)2 * q.cf * H, (uint32_t)n * 2 * H * 2, 0u);
+        } else {
+          const int s2 = s - q.nst_gu;
+          if (s2 < q.ws) {
+            q.ws = 0;
+            q.wu = q.q0 / F;
+            q.wf = q.q0 - q.wu * F;
+          }
+          while (q.ws < s2) {
+            const int fb = min(F, q.q1 - q.wu * F);
+            q.wf += q.rpw;
+            if (q.wf >= fb) {
+              ++q.wu;
+              q.wf = 0;
+            }
+            ++q.ws;
+          }
+          const int fb = min(F, q.q1 - q.wu * F);
+          const int n = min(q.rpw, fb - q.wf);
+          const uint16_t* Wd = p.w_down[l] + ((size_t)q.rc->exp[q.wu] * F + q.wf) * H;   // [E][F][H]
+          f(Wd, (uint32_t)n * H * 2, 0u);
         }
-        const int fb = min(F, q.q1 - q.cu * F);
-        const int n = min(q.pps, fb - q.cf);
-        const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
-        f(We + (size_t)2 * q.cf * H, (uint32_t)n * 2 * H * 2, 0u);
-        break;
-      }
-      case T_DOWN: {
-        const int u = s / q.spe, c = s - u * q.spe;
-        const int s0 = q.r0 + c * q.rps;
-        const int n = min(q.rps, q.r1 - s0);
-        const uint16_t* We = p.w_down[l] + (size_t)q.rc->exp[u] * p.H * p.F;
-        f(We + (size_t)s0 * p.F, (uint32_t)n * p.F * 2, 0u);
         break;
       }
     }
@@ -641,7 +633,7 @@ struct Producer {
     int budget = p.pf_wait;
     for (int tj = ti + 1; tj < t_end && budget > 0; ++tj) {
       const Task t = ldg_task(p.tasks + tj);
-      if (t.type == T_GU || t.type == T_DOWN) continue;
+      if (t.type == T_MOE) continue;
       Geo q;
       if (!geo(t, q, nullptr, false, tj)) return;
       for (int s = 0; s < q.nst && budget > 0; ++s, --budget) prefetch_stage(q, s);
@@ -716,7 +708,7 @@ struct Consumer {
   Ring r;
   float* act;
   Misc* m;
-  float* ydown;
+  float* scr;      // after the misc struct: an H-row tile's residual rows, or an expert tile's coefficients
   float* psum;   // per-warp partial sums of wide-row GEMVs: [2 windows][NCW][WIN_ROWS][NB]
   int ct, cw, lane;
   int ti = 0;
@@ -1135,23 +1127,6 @@ struct Consumer {
     return m->ticket_last != 0;
   }
 
-  // Routing of layer l (written by that layer's router finisher) into smem;
-  // the caller's next barrier publishes it.  Returns the distinct-expert count.
-  __device__ int load_route(int l) {
-    const int* rt = route_of(p, l);
-    const int umax = p.rm.umax, bc = p.rm.bcap;
-    // fixed bounds, so every load is in flight at once (entries past U are unused)
-    for (int i = ct; i < umax; i += NCT) {
-      m->r_exp[i] = __ldcg(rt + 1 + i);
-      m->r_cnt[i] = __ldcg(rt + 1 + umax + i);
-    }
-    for (int i = ct; i < umax * bc; i += NCT) {
-      m->r_tok[i] = __ldcg(rt + 1 + 2 * umax + i);
-      m->r_rank[i] = __ldcg(rt + 1 + 2 * umax + umax * bc + i);
-    }
-    return __ldcg(rt);
-  }
-
   // ------------------------------------------------------------ tasks
 
   __device__ bool qkv(const Task& t, bool ab) {
@@ -1170,7 +1145,7 @@ struct Consumer {
 
   __device__ bool oproj(const Task& t, bool ab) {
     const int l = t.layer, K = p.nq * p.d, r0 = t.a[0], nr = t.a[1] - r0;
-    float* xres = ydown;  // residual rows of this tile, [B][nr]
+    float* xres = scr;    // residual rows of this tile, [B][nr]
     if (!ab) {
       const float4* o = reinterpret_cast<const float4*>(p.o + (size_t)l * p.bcap * K);
       float4* dst = reinterpret_cast<float4*>(act);
@@ -1320,7 +1295,15 @@ struct Consumer {
     return ab;
   }
 
-  __device__ bool gate_up(const Task& t, bool ab) {
+  // ---- expert tile: the layer's routing, then for this tile's (distinct
+  // expert, ffn unit) pairs the gate/up rows, giving per token slot the
+  // coefficient c = gate x silu(gate row . xn) x (up row . xn), then the same
+  // units' rows of the transposed down matrix: y_b += c x Wd^T[unit] for the
+  // token's request b.  y is this tile's gated partial of the layer output
+  // (moe_part); the reduce tasks add the residual and all tiles' partials.
+  // No other CTA's gate/up results are needed, so the tile streams its
+  // gate/up and down weights back to back.
+  __device__ bool moe(const Task& t, bool ab) {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
     if (!ab) {
@@ -1341,81 +1324,129 @@ struct Consumer {
     }
     cbar();
     mark(TR_ACT);
-    long long q0, q1;
-    gu_range(p, t, U, q0, q1);
-    float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
-    for (long long q = q0; q < q1;) {
-      const int u = (int)(q / F);
-      const int fa = (int)(q - (long long)u * F);
-      const int fb = (int)min((long long)F, q1 - (long long)u * F);
+    long long g0, g1;
+    gu_range(p, t, U, g0, g1);
+    const int q0 = (int)g0, q1 = (int)g1;
+    float* cf = scr;   // [unit - q0][token slot] coefficients
+    for (int q = q0; q < q1;) {
+      const int u = q / F, fa = q - u * F, fb = min(F, q1 - u * F);
       const int nt = m->r_cnt[u];
       const int* toks = m->r_tok + u * bc;
       const int* ranks = m->r_rank + u * bc;
       ab = gemv<true>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, [&](int f, int j, float g, float up) {
-        hb[((size_t)toks[j] * k + ranks[j]) * F + f] = g / (1.0f + expf(-g)) * up;
+        cf[(u * F + f - q0) * bc + j] = m->gate[toks[j] * k + ranks[j]] * (g / (1.0f + expf(-g)) * up);
       });
-      q = (long long)(u + 1) * F;
+      q = (u + 1) * F;
+    }
+    cbar();   // coefficients complete; the activation region is free
+    const int rpw = rows_per_stage(p, H);
+    const bool col = ct * 8 < H;                 // this thread's 8 output columns
+    const uint32_t coff = (uint32_t)ct * 16;
+    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // batch 1: request 0 in registers
+    if constexpr (NB > 1) {                      // else: y per request in the activation region,
+      if (col) {                                 // each thread owning its 8 columns of every row
+        for (int b = 0; b < p.B; ++b) {
+          float4* yb = reinterpret_cast<float4*>(act + (size_t)b * H) + 2 * ct;
+          yb[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          yb[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+    for (int q = q0; q < q1;) {
+      const int u = q / F, fa = q - u * F, fb = min(F, q1 - u * F);
+      const int nt = m->r_cnt[u];
+      const int* toks = m->r_tok + u * bc;
+      for (int f0 = fa; f0 < fb; f0 += rpw) {
+        const int n = min(rpw, fb - f0);
+        const uint8_t* st = wait_stage(ab);
+        if (st && col) {
+          const uint32_t sts = smem_u32(st) + coff;
+          const float* cu = cf + (size_t)(u * F + f0 - q0) * bc;
+          for (int i = 0; i < n; ++i) {
+            const uint4 w = lds128(sts + (uint32_t)i * H * 2);
+            if constexpr (NB == 1) {
+              const float c = cu[i * bc];
+              y[0] = fmaf(c, bf_lo(w.x), y[0]);
+              y[1] = fmaf(c, bf_hi(w.x), y[1]);
+              y[2] = fmaf(c, bf_lo(w.y), y[2]);
+              y[3] = fmaf(c, bf_hi(w.y), y[3]);
+              y[4] = fmaf(c, bf_lo(w.z), y[4]);
+              y[5] = fmaf(c, bf_hi(w.z), y[5]);
+              y[6] = fmaf(c, bf_lo(w.w), y[6]);
+              y[7] = fmaf(c, bf_hi(w.w), y[7]);
+            } else {
+              for (int j = 0; j < nt; ++j) {
+                const float c = cu[i * bc + j];
+                float4* yb = reinterpret_cast<float4*>(act + (size_t)toks[j] * H) + 2 * ct;
+                float4 a0 = yb[0], a1 = yb[1];
+                a0.x = fmaf(c, bf_lo(w.x), a0.x);
+                a0.y = fmaf(c, bf_hi(w.x), a0.y);
+                a0.z = fmaf(c, bf_lo(w.y), a0.z);
+                a0.w = fmaf(c, bf_hi(w.y), a0.w);
+                a1.x = fmaf(c, bf_lo(w.z), a1.x);
+                a1.y = fmaf(c, bf_hi(w.z), a1.y);
+                a1.z = fmaf(c, bf_lo(w.w), a1.z);
+                a1.w = fmaf(c, bf_hi(w.w), a1.w);
+                yb[0] = a0;
+                yb[1] = a1;
+              }
+            }
+          }
+        }
+        release_stage(ab);
+      }
+      q = (u + 1) * F;
     }
     mark(TR_STAGES);
+    if (!ab && col) {
+      float* part = p.moe_part + (size_t)t.a[0] * p.bcap * H;
+      for (int b = 0; b < p.B; ++b) {
+        float4* dst = reinterpret_cast<float4*>(part + (size_t)b * H) + 2 * ct;
+        if constexpr (NB == 1) {
+          dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+          dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(act + (size_t)b * H) + 2 * ct;
+          dst[0] = src[0];
+          dst[1] = src[1];
+        }
+      }
+    }
     ab = finish(ab);
     if (!ab) signal(p.cm.gu + l);
     return ab;
   }
 
-  __device__ bool down(const Task& t, bool ab) {
-    const int l = t.layer, F = p.F, k = p.k, B = p.B, bc = p.rm.bcap;
-    const int r0 = t.a[0], r1 = t.a[1], nr = r1 - r0, drm = p.down_rows_max;
-    const float* hb = p.hbuf + (size_t)l * p.bcap * k * F;
-    int U = 0;
-    if (!ab) {
-      U = m->r_layer == l ? m->r_U : load_route(l);
-      if (p.allh) {
-        const float4* src = reinterpret_cast<const float4*>(hb);
-        float4* dst = reinterpret_cast<float4*>(act);
-#pragma unroll 4
-        for (int i = ct; i < (B * k * F) >> 2; i += NCT) dst[i] = __ldcg(src + i);
-      }
-    }
-    U = __shfl_sync(FULL, U, 0);
-    cbar();
-    if (!ab && p.allh) {
-      for (int i = ct; i < U * bc; i += NCT) m->r_row[i] = m->r_tok[i] * k + m->r_rank[i];
-      cbar();
-    }
+  // ---- reduce: rows [a0, a1) of the hidden dim, x_out = x_mid + the a2 expert
+  // tiles' partials, summed in tile order (strided chunks, then chunk order)
+  __device__ bool red(const Task& t, bool ab) {
+    const int l = t.layer, r0 = t.a[0], nr = t.a[1] - r0, ntiles = t.a[2], B = p.B, H = p.H;
+    const int no = B * nr;
+    const int nch = no > 0 ? max(1, NCT / no) : 1;
+    float* rs = act;                                   // [output][chunk] sums
     mark(TR_ACT);
-    for (int u = 0; u < U; ++u) {
-      const int nt = m->r_cnt[u];
-      const int* toks = m->r_tok + u * bc;
-      const int* ranks = m->r_rank + u * bc;
-      if (!p.allh) {
-        cbar();  // the previous expert's rows are done with act
-        if (!ab) {
-          for (int i = ct; i < nt * F; i += NCT) {
-            const int j = i / F;
-            act[i] = __ldcg(hb + ((size_t)toks[j] * k + ranks[j]) * F + (i - j * F));
-          }
-        }
-        cbar();
+    if (!ab) {
+      for (int x = ct; x < no * nch; x += NCT) {
+        const int o = x / nch, c = x - o * nch, b = o / nr, h = r0 + (o - b * nr);
+        const float* src = p.moe_part + (size_t)b * H + h;
+        float s = 0.f;
+#pragma unroll 4
+        for (int ti = c; ti < ntiles; ti += nch) s += __ldcg(src + (size_t)ti * p.bcap * H);
+        rs[o * nch + c] = s;
       }
-      ab = gemv<false>(F, r0, r1, act, F, p.allh ? m->r_row + u * bc : nullptr, nt, ab,
-                       [&](int row, int j, float s, float) {
-                         ydown[((size_t)toks[j] * k + ranks[j]) * drm + (row - r0)] = s;
-                       });
+    }
+    cbar();
+    if (!ab) {
+      const float* xm = p.x_mid + (size_t)l * p.bcap * H;
+      float* xo = p.x_out + (size_t)l * p.bcap * H;
+      for (int o = ct; o < no; o += NCT) {
+        const int b = o / nr, h = r0 + (o - b * nr);
+        float s = __ldcg(xm + (size_t)b * H + h);
+        for (int c = 0; c < nch; ++c) s += rs[o * nch + c];
+        xo[(size_t)b * H + h] = s;
+      }
     }
     mark(TR_STAGES);
-    cbar();
-    if (!ab) {
-      const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
-      float* xo = p.x_out + (size_t)l * p.bcap * p.H;
-      const float* gt = p.gates + (size_t)l * p.bcap * k;
-      for (int i = ct; i < B * nr; i += NCT) {
-        const int b = i / nr, rr = i - b * nr;
-        float x = __ldcg(xm + (size_t)b * p.H + r0 + rr);
-        for (int j = 0; j < k; ++j)
-          x = fmaf(__ldcg(gt + b * k + j), ydown[((size_t)b * k + j) * drm + rr], x);
-        xo[(size_t)b * p.H + r0 + rr] = x;
-      }
-    }
     ab = finish(ab);
     if (!ab) signal(p.cm.down + l);
     return ab;
@@ -1875,8 +1906,8 @@ struct Consumer {
         case T_ATTN: ab = attn(t, ab); break;
         case T_OPROJ: ab = oproj(t, ab); break;
         case T_ROUTER: ab = router(t, ab); break;
-        case T_GU: ab = gate_up(t, ab); break;
-        case T_DOWN: ab = down(t, ab); break;
+        case T_MOE: ab = moe(t, ab); break;
+        case T_RED: ab = red(t, ab); break;
         case T_LM: ab = lm(t, ab); break;
         case T_COMB: ab = comb(t, ab); break;
         default: ab = true;
@@ -1907,7 +1938,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
   extern __shared__ __align__(128) uint8_t smem[];
   Misc* m = reinterpret_cast<Misc*>(smem + p.misc_off);
   float* act = reinterpret_cast<float*>(smem + p.act_off);
-  float* ydown = reinterpret_cast<float*>(smem + p.misc_off + sizeof(Misc));
+  float* scr = reinterpret_cast<float*>(smem + p.misc_off + sizeof(Misc));
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < p.nstages; ++s) {
@@ -1930,7 +1961,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
         pr.run(t0, t1);
       }
     } else {
-      Consumer<NB> c{p, ring, act, m, ydown, reinterpret_cast<float*>(smem + p.psum_off), tid, tid >> 5, tid & 31};
+      Consumer<NB> c{p, ring, act, m, scr, reinterpret_cast<float*>(smem + p.psum_off), tid, tid >> 5, tid & 31};
       c.run(t0, t1);
     }
   }

@@ -33,9 +33,11 @@ enum TaskType : int32_t {
                  // a4 = partial slot, a5 = first slot of (a0, a1), a6 = chunks of (a0, a1)
   T_OPROJ = 2,   // rows [a0,a1) of Wo, residual add
   T_ROUTER = 3,  // rows [a0,a1) of the router
-  T_GU = 4,      // gate/up tile a0 of a1 over the flattened (distinct expert, ffn row) space;
-                 // computes the layer's routing from the router logits (tile 0 publishes it)
-  T_DOWN = 5,    // rows [a0,a1) of the hidden dim over every selected expert, residual add
+  T_MOE = 4,     // expert tile a0 of a1 over the flattened (distinct expert, ffn unit) space:
+                 // routing from the router logits (tile 0 publishes it), the tile's gate/up
+                 // rows, then the same units' rows of the transposed down matrix, into a
+                 // gated partial of the layer output
+  T_RED = 5,     // rows [a0,a1) of the hidden dim: residual + the a2 expert tiles' partials
   T_LM = 6,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
   T_COMB = 7,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
                  // a5 = first partial slot, a6 = chunks (waits for all of them)
@@ -116,10 +118,10 @@ struct Params {
   int act_off, act_floats, misc_off;
   int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * WIN_ROWS * nb floats)
   int attn_mrg_floats;   // attention page-group states in the activation region (floats)
-  int allh;             // 1: the down task keeps every (request, rank) h row in smem
   int pf_ahead;         // stages the producer's L2 prefetch runs ahead of its ring copies (0: off)
   int pf_wait;          // stages of routing-independent tasks prefetched while routing is pending (0: off)
-  int down_rows_max;
+  int down_rows_max;    // most rows of an H-row tile (O projection, reduce)
+  int cf_pairs;         // most (expert, unit) pairs of one expert tile
   int* seq_len;         // device [bcap]
   const int* page_table;  // device [bcap * max_pages]
   const float2* rope;   // [max_pos][d/2] (cos, sin)
@@ -135,7 +137,7 @@ struct Params {
   int* ids;             // [L][bcap][k]
   float* gates;         // [L][bcap][k]
   int* route;           // [L][rm.ints]
-  float* hbuf;          // [L][bcap][k][F]
+  float* moe_part;      // [expert tiles][bcap][H] gated partial outputs (reused by every layer)
   float* lm_val;        // [bcap][lm_tiles]
   int* lm_idx;          // [bcap][lm_tiles]
   int lm_tiles;
@@ -155,11 +157,40 @@ struct Params {
 // false when the shape leaves no room (fewer than two stages, or an attention
 // page split the warps cannot share evenly).
 struct SmemPlan {
-  int stage_bytes, nstages, act_floats, allh, act_off, misc_off, psum_off, attn_mrg_floats, smem;
+  int stage_bytes, nstages, act_floats, act_off, misc_off, psum_off, attn_mrg_floats, smem;
 };
 
+// Per-expert-tile coefficients (gate x silu(gate row) x up row, per token slot)
+// kept in shared memory between the tile's gate/up and down parts: at most
+// CF_FLOATS, else what one tile per CTA needs at this capacity.
+constexpr int CF_FLOATS = 2048;
+
+inline int cf_floats(int E, int k, int F, int C, int bcap) {
+  const long long umax = E < bcap * k ? E : (long long)bcap * k;
+  const long long pairs = umax * F;
+  const long long tiles = pairs < C ? (pairs > 0 ? pairs : 1) : C;
+  const long long need = (pairs + tiles - 1) / tiles * bcap;
+  return (int)(need < CF_FLOATS ? need : CF_FLOATS);
+}
+
+// Expert tiles per layer for umax distinct experts: one per CTA (at most one
+// per (expert, unit) pair), but enough that each tile's pairs x capacity
+// coefficients fit cf floats.
+inline int moe_tiles(int umax, int F, int C, int bcap, int cf) {
+  const long long pairs = (long long)umax * F;
+  long long cap = cf / bcap;
+  if (cap < 1) cap = 1;
+  long long t = pairs < C ? pairs : C;
+  if (t < 1) t = 1;
+  const long long need = (pairs + cap - 1) / cap;
+  return (int)(t > need ? t : need);
+}
+
+// Shared-memory layout: [weight ring][activations][misc struct + scratch][GEMV partial sums].
+// The scratch holds an H-row tile's residual rows or an expert tile's coefficients.
 inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bcap, int nb, int down_rows_max,
-                      size_t misc_struct_bytes, SmemPlan& o) {
+                      int cf, size_t misc_struct_bytes, SmemPlan& o) {
+  (void)k;
   const int nqd = nq * d;
   const int widest = H > nqd ? (H > F ? H : F) : (nqd > F ? nqd : F);
   const long long A1 = (long long)bcap * widest;
@@ -168,14 +199,12 @@ inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bca
   if (ppg32 < 1) ppg32 = 1;
   const long long mrg = (long long)NCW * G * RS;   // one softmax state per consumer warp
   const long long A3 = (long long)MAX_G * d + 2 * d + mrg + NCW * 128;  // q (then its mma table), new K/V, states, P
-  const long long Ah = (long long)bcap * k * F;
-  o.allh = Ah * 4 <= 64 * 1024 ? 1 : 0;
   long long act = A1 > A3 ? A1 : A3;
-  if (o.allh && Ah > act) act = Ah;
   o.act_floats = (int)act;
   o.attn_mrg_floats = (int)mrg;
   const size_t act_bytes = ((size_t)act * 4 + 127) / 128 * 128;
-  const size_t misc = (misc_struct_bytes + (size_t)bcap * k * down_rows_max * 4 + 127) / 128 * 128;
+  const long long scr = (long long)bcap * down_rows_max > cf ? (long long)bcap * down_rows_max : cf;
+  const size_t misc = (misc_struct_bytes + (size_t)scr * 4 + 127) / 128 * 128;
   const size_t psum = ((size_t)2 * NCW * WIN_ROWS * nb * 4 + 127) / 128 * 128;
   const long long avail = (long long)SMEM_LIMIT - (long long)(act_bytes + misc + psum);
   const int need0 = 2 * widest > 4 * H ? 2 * widest : 4 * H;
@@ -187,6 +216,7 @@ inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bca
   if (nst < 2) return false;
   const int ppg = sb / (2 * ps * d * 2) < 1 ? 1 : sb / (2 * ps * d * 2);
   if (ppg > ppg32 || NCW % ppg != 0 || d / 16 > 8) return false;
+  if (H > 8 * NCW * 32 || H % 8 != 0) return false;   // the expert tile's down part: 8 columns per thread
   o.stage_bytes = sb;
   o.nstages = (int)nst;
   o.act_off = (int)(nst * sb);

@@ -107,7 +107,7 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
   if (c.qkv_per_g > Rg) c.qkv_per_g = Rg;
   c.o = C < s.H ? C : s.H;
   c.router = s.E < 32 ? s.E : 32;
-  c.gu = C < umax * s.F ? C : umax * s.F;
+  c.gu = mk::moe_tiles(umax, s.F, C, B, mk::cf_floats(s.E, s.k, s.F, C, B));
   c.down = C < s.H ? C : s.H;
   c.lm = 4 * C < s.V ? 4 * C : s.V;
   c.down_rows_max = (s.H + c.down - 1) / c.down;
@@ -207,7 +207,7 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
       put(next(), t);
     }
     for (int i = 0; i < c.gu; ++i) {
-      mk::Task t = task(mk::T_GU, l, cm.rticket + l, (uint32_t)c.router);
+      mk::Task t = task(mk::T_MOE, l, cm.rticket + l, (uint32_t)c.router);
       t.a[0] = i;
       t.a[1] = c.gu;
       put(next(), t);
@@ -215,9 +215,10 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
     for (int i = 0; i < c.down; ++i) {
       int a, b;
       split_range(s.H, c.down, i, a, b);
-      mk::Task t = task(mk::T_DOWN, l, cm.gu + l, (uint32_t)c.gu);
+      mk::Task t = task(mk::T_RED, l, cm.gu + l, (uint32_t)c.gu);
       t.a[0] = a;
       t.a[1] = b;
+      t.a[2] = c.gu;
       put(next(), t);
     }
   }
@@ -328,7 +329,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_ids = dc.take(L * B * s.k * sizeof(int));
   const size_t d_gt = dc.take(L * B * s.k * sizeof(float));
   const size_t d_route = dc.take(L * rm.ints * sizeof(int));
-  const size_t d_h = dc.take(L * B * s.k * s.F * sizeof(float));
+  const size_t d_mp = dc.take((size_t)cnt.gu * B * s.H * sizeof(float));
   const size_t d_lmv = dc.take((size_t)B * cnt.lm * sizeof(float));
   const size_t d_lmi = dc.take((size_t)B * cnt.lm * sizeof(int));
   if (dc.off > kScratchBytes) {
@@ -340,7 +341,8 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
 
   // shared-memory plan (same layout rule as mk_plan_create)
   mk::SmemPlan sp;
-  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, B, nb, cnt.down_rows_max, mk::misc_bytes(), sp))
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, B, nb, cnt.down_rows_max,
+                     mk::cf_floats(s.E, s.k, s.F, C, B), mk::misc_bytes(), sp))
     return fail(MK_ERR_UNSUPPORTED, "shape leaves no room for the shared-memory ring");
   const int smem = sp.smem;
   if (mk::max_active_ctas(nb, smem) < 1) return fail(MK_ERR_CUDA, "megakernel does not fit on an SM");
@@ -419,8 +421,8 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.misc_off = sp.misc_off;
   P.psum_off = sp.psum_off;
   P.attn_mrg_floats = sp.attn_mrg_floats;
-  P.allh = sp.allh;
   P.down_rows_max = cnt.down_rows_max;
+  P.cf_pairs = mk::cf_floats(s.E, s.k, s.F, C, B) / B > 0 ? mk::cf_floats(s.E, s.k, s.F, C, B) / B : 1;
   P.seq_len = (int*)(base + d_blob + h_seq);
   P.page_table = (const int*)(base + d_blob + h_pt);
   P.rope = (const float2*)(base + d_rope);
@@ -435,7 +437,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.ids = (int*)(base + d_ids);
   P.gates = (float*)(base + d_gt);
   P.route = (int*)(base + d_route);
-  P.hbuf = (float*)(base + d_h);
+  P.moe_part = (float*)(base + d_mp);
   P.lm_val = (float*)(base + d_lmv);
   P.lm_idx = (int*)(base + d_lmi);
   P.lm_tiles = cnt.lm;

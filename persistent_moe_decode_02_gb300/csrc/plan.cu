@@ -100,6 +100,7 @@ Task mk_task(int type, int layer, int wait_ctr, uint32_t wait_cnt) {
 // Pages covering positions [0, len] (the cached tokens plus the new one).
 inline int pages_for(int len, int ps) { return len / ps + 1; }
 
+
 // Query heads per split-KV combine task: the smallest divisor of G that keeps
 // the tasks (pairs x G / heads) within one per CTA, else all G heads.
 inline int comb_heads(int G, int pairs, int C) {
@@ -139,7 +140,7 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   cnt.o = std::max(1, std::min(s.H, C));
   cnt.router = std::max(1, std::min(s.E, 32));
   const int umax = std::min(s.E, B * s.k);
-  cnt.gu = std::max(1, std::min(C, umax * s.F));
+  cnt.gu = mk::moe_tiles(umax, s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   cnt.down = std::max(1, std::min(s.H, C));
   cnt.lm = std::max(1, std::min(s.V, 4 * C));
   cnt.down_rows_max = (s.H + cnt.down - 1) / cnt.down;
@@ -245,23 +246,24 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     }
     asg.phase(ph);
     ph.clear();
-    // expert gate/up tiles over the distinct selected experts
+    // expert tiles over the distinct selected experts: gate/up + down slices
     for (int i = 0; i < cnt.gu; ++i) {
-      Task t = mk_task(mk::T_GU, l, cm.rticket + l, (uint32_t)cnt.router);
+      Task t = mk_task(mk::T_MOE, l, cm.rticket + l, (uint32_t)cnt.router);
       t.a[0] = i;
       t.a[1] = cnt.gu;
-      ph.push_back({(double)umax * s.F * 4.0 * s.H / cnt.gu, t});
+      ph.push_back({(double)umax * s.F * 6.0 * s.H / cnt.gu, t});
     }
     asg.phase(ph);
     ph.clear();
-    // expert down tiles + weighted combine + residual
+    // reduce: residual + the expert tiles' partials, row tiles of the hidden dim
     for (int i = 0; i < cnt.down; ++i) {
       int a, b;
       split_range(s.H, cnt.down, i, a, b);
-      Task t = mk_task(mk::T_DOWN, l, cm.gu + l, (uint32_t)cnt.gu);
+      Task t = mk_task(mk::T_RED, l, cm.gu + l, (uint32_t)cnt.gu);
       t.a[0] = a;
       t.a[1] = b;
-      ph.push_back({(double)(b - a) * umax * s.F * 2, t});
+      t.a[2] = cnt.gu;
+      ph.push_back({(double)(b - a) * cnt.gu * B * 4, t});
     }
     asg.phase(ph);
   }
@@ -300,7 +302,7 @@ struct mk_plan {
   Shape s;
   int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0, pf_ahead = 0, pf_wait = 0;
   int max_pages = 0, num_pages = 0, rope_npos = 0;
-  int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0, allh = 0;
+  int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0;
   int replans = 0;
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 0;
@@ -485,6 +487,7 @@ void fill_params(mk_plan* p) {
   P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
+  P.cf_pairs = std::max(1, mk::cf_floats(s.E, s.k, s.F, p->C, p->bcap) / p->bcap);
   P.trace = p->trace ? p->d_trace : nullptr;
   P.strace = p->trace >= 2 ? p->d_strace : nullptr;
   P.pf_ahead = p->pf_ahead;
@@ -596,9 +599,9 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   const int C = p->C;
   const int down_rows_max = (s.H + std::min(s.H, C) - 1) / std::min(s.H, C);
   mk::SmemPlan sp;
-  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, bcap, p->nb, down_rows_max, mk::misc_bytes(), sp))
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, bcap, p->nb, down_rows_max,
+                     mk::cf_floats(s.E, s.k, s.F, C, bcap), mk::misc_bytes(), sp))
     return fail(MK_ERR_UNSUPPORTED);
-  p->allh = sp.allh;
   p->act_floats = sp.act_floats;
   p->stage_bytes = sp.stage_bytes;
   p->nstages = sp.nstages;
@@ -608,7 +611,6 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   p->P.misc_off = sp.misc_off;
   p->P.psum_off = sp.psum_off;
   p->P.attn_mrg_floats = sp.attn_mrg_floats;
-  p->P.allh = sp.allh;
   if (mk::max_active_ctas(p->nb, p->smem) < 1) {
     snprintf(g_last_error, sizeof(g_last_error), "megakernel does not fit on an SM with %d bytes of shared memory",
              p->smem);
@@ -663,7 +665,9 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   ok &= dalloc(p, &P.ids, L * bcap * s.k * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &P.gates, L * bcap * s.k * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.route, L * p->rm.ints * sizeof(int)) == cudaSuccess;
-  ok &= dalloc(p, &P.hbuf, L * bcap * s.k * s.F * sizeof(float)) == cudaSuccess;
+  // expert-tile partials, sized for the most tiles any batch up to the capacity needs
+  const int moe_max = mk::moe_tiles(std::min(s.E, bcap * s.k), s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
+  ok &= dalloc(p, &P.moe_part, (size_t)moe_max * bcap * s.H * sizeof(float)) == cudaSuccess;
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;

@@ -54,7 +54,14 @@ class DeviceModel:
                 gu[e, :, 0].copy_(fill_normal_(tmp, seed, wname("gate", l), start=e * F * H))
                 gu[e, :, 1].copy_(fill_normal_(tmp, seed, wname("up", l), start=e * F * H))
             self.w_gate_up.append(gu.view(E, 2 * F, H))
-            self.w_down.append(normal((E, H, F), seed, wname("down", l), device=dev))
+            # down projection stored transposed per expert, [E, F, H]: row f holds
+            # the H output coefficients of ffn unit f (values keyed by the logical
+            # [E, H, F] index, so the oracle's view is unchanged)
+            wd = torch.empty(E, F, H, dtype=torch.bfloat16, device=dev)
+            tmpd = torch.empty(H, F, dtype=torch.bfloat16, device=dev)
+            for e in range(E):
+                wd[e].copy_(fill_normal_(tmpd, seed, wname("down", l), start=e * H * F).t())
+            self.w_down.append(wd)
 
     def weights(self) -> dict:
         return {"embed": self.embed, "final_norm": self.final_norm, "lm_head": self.lm_head,

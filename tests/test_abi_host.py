@@ -14,7 +14,7 @@ from synth import FULL, MID, TINY, Dims
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-T_QKV, T_ATTN, T_OPROJ, T_ROUTER, T_GU, T_DOWN, T_LM, T_COMB = range(8)
+T_QKV, T_ATTN, T_OPROJ, T_ROUTER, T_MOE, T_RED, T_LM, T_COMB = range(8)
 
 
 @pytest.fixture(scope="module")
@@ -78,9 +78,9 @@ def signals_per_step(D, B, tasks):
             sig[base["o"] + l] += 1
         elif typ == T_ROUTER:
             sig[base["rticket"] + l] += 1
-        elif typ == T_GU:
+        elif typ == T_MOE:
             sig[base["gu"] + l] += 1
-        elif typ == T_DOWN:
+        elif typ == T_RED:
             sig[base["down"] + l] += 1
         elif typ == T_LM:
             sig[base["lm"]] += 1
@@ -143,9 +143,9 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
             out.append(base["o"] + l)
         elif typ == T_ROUTER:
             out.append(base["rticket"] + l)
-        elif typ == T_GU:
+        elif typ == T_MOE:
             out.append(base["gu"] + l)
-        elif typ == T_DOWN:
+        elif typ == T_RED:
             out.append(base["down"] + l)
         elif typ == T_COMB:
             out.append(base["combine"] + l)
@@ -153,7 +153,7 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
 
     def fires_with_finishers(t):
         out = fires(t)
-        if t[0] == T_GU and t[2] == 0:
+        if t[0] == T_MOE and t[2] == 0:
             out.append(base["rdone"] + t[1])
         return out
 
@@ -175,7 +175,7 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
     cover(T_QKV, D.n_kv_heads * (D.group + 2) * D.head_dim)
     cover(T_OPROJ, D.hidden)
     cover(T_ROUTER, D.n_experts)
-    cover(T_DOWN, D.hidden)
+    cover(T_RED, D.hidden)
     lm = sorted((t[2], t[3]) for t in tasks.tolist() if t[0] == T_LM)
     assert lm[0][0] == 0 and lm[-1][1] == D.vocab
     # every query head of every (request, group) is combined exactly once, from
@@ -197,7 +197,7 @@ def test_full_bs1_phases_spread_over_all_ctas(mk):
         for t in tasks[cs[c]:cs[c + 1]].tolist():
             if t[1] == 5:
                 per_cta[t[0]][c] += 1
-    for typ in (T_QKV, T_OPROJ, T_GU, T_DOWN):
+    for typ in (T_QKV, T_OPROJ, T_MOE, T_RED):
         assert len(per_cta[typ]) == 152, typ          # every CTA takes part in each big phase
         assert max(per_cta[typ].values()) == 1, typ   # and takes one tile of it
     # 513 pages x 4 groups in 14-page chunks: 148 chunks, at most one per CTA
