@@ -702,6 +702,38 @@ struct Producer {
 
 // ------------------------------------------------------------------ consumer pieces
 
+// GEMV epilogue shared by the projection and expert tasks, so that one GEMV
+// body (inlined at one call site per row kind) serves all of them:
+//   STORE:  out[j * ld + row] = s
+//   RESID:  out[j * ld + row] = res[j * res_ld + row - res_r0] + s
+//   SWIGLU: (rows are gate/up pairs: row = ffn unit f, s = gate, s2 = up)
+//           out[(f + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * silu(s) * s2
+struct GemvEpi {
+  enum Kind { STORE, RESID, SWIGLU };
+  int kind;
+  float* out;
+  int ld;
+  const float* res;
+  int res_ld, res_r0;
+  int base, k;
+  const int* toks;
+  const int* ranks;
+  const float* gate_w;
+  __device__ __forceinline__ void operator()(int row, int j, float s, float s2) const {
+    switch (kind) {
+      case STORE: out[(size_t)j * ld + row] = s; break;
+      case RESID: out[(size_t)j * ld + row] = res[j * res_ld + row - res_r0] + s; break;
+      default: out[(size_t)(row + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * (s / (1.0f + expf(-s)) * s2);
+    }
+  }
+};
+
+// A projection task's GEMV: rows [r0, r1) of a K-wide matrix against the activations.
+struct ProjGemv {
+  int K, r0, r1;
+  GemvEpi epi;
+};
+
 template <int NB>
 struct Consumer {
   const Params& p;
@@ -1129,21 +1161,24 @@ struct Consumer {
 
   // ------------------------------------------------------------ tasks
 
-  __device__ bool qkv(const Task& t, bool ab) {
+  // ---- projections: QKV, O (+ residual), router logits.  prep_* builds the
+  // activations and the GEMV's range and epilogue; the caller runs the GEMV;
+  // post_proj signals the task's counter.
+  __device__ bool prep_qkv(const Task& t, bool ab, ProjGemv& g) {
     const int l = t.layer;
     if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i4) { return x_in4(l, b, i4); });
     cbar();
-    mark(TR_ACT);
-    float* out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
-    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab,
-                     [&](int row, int j, float s, float) { out[(size_t)j * p.qkv_rows + row] = s; });
-    mark(TR_STAGES);
-    ab = finish(ab);
-    if (!ab) signal(p.cm.qkv + l * p.nkv + t.a[2]);
+    g.K = p.H;
+    g.r0 = t.a[0];
+    g.r1 = t.a[1];
+    g.epi = GemvEpi{};
+    g.epi.kind = GemvEpi::STORE;
+    g.epi.out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
+    g.epi.ld = p.qkv_rows;
     return ab;
   }
 
-  __device__ bool oproj(const Task& t, bool ab) {
+  __device__ bool prep_oproj(const Task& t, bool ab, ProjGemv& g) {
     const int l = t.layer, K = p.nq * p.d, r0 = t.a[0], nr = t.a[1] - r0;
     float* xres = scr;    // residual rows of this tile, [B][nr]
     if (!ab) {
@@ -1154,14 +1189,41 @@ struct Consumer {
       for (int i = ct; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
     }
     cbar();
-    mark(TR_ACT);
-    float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
-    ab = gemv<false>(K, r0, t.a[1], act, K, nullptr, p.B, ab, [&](int row, int j, float s, float) {
-      xm[(size_t)j * p.H + row] = xres[j * nr + row - r0] + s;
-    });
-    mark(TR_STAGES);
+    g.K = K;
+    g.r0 = r0;
+    g.r1 = t.a[1];
+    g.epi = GemvEpi{};
+    g.epi.kind = GemvEpi::RESID;
+    g.epi.out = p.x_mid + (size_t)l * p.bcap * p.H;
+    g.epi.ld = p.H;
+    g.epi.res = xres;
+    g.epi.res_ld = nr;
+    g.epi.res_r0 = r0;
+    return ab;
+  }
+
+  __device__ bool prep_router(const Task& t, bool ab, ProjGemv& g) {
+    const int l = t.layer;
+    if (!ab) fill_ffn_norm(l);
+    cbar();
+    g.K = p.H;
+    g.r0 = t.a[0];
+    g.r1 = t.a[1];
+    g.epi = GemvEpi{};
+    g.epi.kind = GemvEpi::STORE;
+    g.epi.out = p.rlog + (size_t)l * p.bcap * p.E;
+    g.epi.ld = p.E;
+    return ab;
+  }
+
+  __device__ bool post_proj(const Task& t, bool ab) {
+    const int l = t.layer;
     ab = finish(ab);
-    if (!ab) signal(p.cm.o + l);
+    if (!ab) {
+      if (t.type == T_QKV) signal(p.cm.qkv + l * p.nkv + t.a[2]);
+      else if (t.type == T_OPROJ) signal(p.cm.o + l);
+      else signal(p.cm.rticket + l);
+    }
     return ab;
   }
 
@@ -1281,20 +1343,6 @@ struct Consumer {
     signal(p.cm.rdone + l);
   }
 
-  __device__ bool router(const Task& t, bool ab) {
-    const int l = t.layer;
-    if (!ab) fill_ffn_norm(l);
-    cbar();
-    mark(TR_ACT);
-    float* rl = p.rlog + (size_t)l * p.bcap * p.E;
-    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, p.B, ab,
-                     [&](int row, int j, float s, float) { rl[(size_t)j * p.E + row] = s; });
-    mark(TR_STAGES);
-    ab = finish(ab);
-    if (!ab) signal(p.cm.rticket + l);
-    return ab;
-  }
-
   // ---- expert tile: the layer's routing, then for this tile's (distinct
   // expert, ffn unit) pairs the gate/up rows, giving per token slot the
   // coefficient c = gate x silu(gate row . xn) x (up row . xn), then the same
@@ -1333,9 +1381,16 @@ struct Consumer {
       const int nt = m->r_cnt[u];
       const int* toks = m->r_tok + u * bc;
       const int* ranks = m->r_rank + u * bc;
-      ab = gemv<true>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, [&](int f, int j, float g, float up) {
-        cf[(u * F + f - q0) * bc + j] = m->gate[toks[j] * k + ranks[j]] * (g / (1.0f + expf(-g)) * up);
-      });
+      GemvEpi e{};
+      e.kind = GemvEpi::SWIGLU;
+      e.out = cf;
+      e.ld = bc;
+      e.base = u * F - q0;
+      e.k = k;
+      e.toks = toks;
+      e.ranks = ranks;
+      e.gate_w = m->gate;
+      ab = gemv<true>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, e);
       q = (u + 1) * F;
     }
     cbar();   // coefficients complete; the activation region is free
@@ -1902,10 +1957,18 @@ struct Consumer {
       if (ab) break;
       mark(TR_DEP);
       switch (t.type) {
-        case T_QKV: ab = qkv(t, ab); break;
+        case T_QKV:
+        case T_OPROJ:
+        case T_ROUTER: {
+          ProjGemv g;
+          ab = t.type == T_QKV ? prep_qkv(t, ab, g) : t.type == T_OPROJ ? prep_oproj(t, ab, g) : prep_router(t, ab, g);
+          mark(TR_ACT);
+          ab = gemv<false>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
+          mark(TR_STAGES);
+          ab = post_proj(t, ab);
+          break;
+        }
         case T_ATTN: ab = attn(t, ab); break;
-        case T_OPROJ: ab = oproj(t, ab); break;
-        case T_ROUTER: ab = router(t, ab); break;
         case T_MOE: ab = moe(t, ab); break;
         case T_RED: ab = red(t, ab); break;
         case T_LM: ab = lm(t, ab); break;
