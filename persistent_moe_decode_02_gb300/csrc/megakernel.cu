@@ -34,6 +34,10 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int NCT = NCW * 32;  // consumer threads
+// Column-slice GEMV: consume two ring stages per pass, per call site.  It pays
+// off in the LM head's long tiles; in the short projection and expert tiles
+// waiting for the second stage before any math costs more than it saves.
+constexpr bool SP_PROJ = false, SP_MOE = false, SP_LM = true;
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -772,6 +776,19 @@ struct Consumer {
     if (p.strace && ct == 0) stage_stamp(2);
     r.advance();
   }
+  // Release an earlier stage (slot `stage` of round `round`) without moving the ring.
+  __device__ void release_at(bool ab, int stage, int round) {
+    __syncwarp();
+    if (!ab && lane == 0) mbar_arrive(&m->empty[stage]);
+    if (p.strace && ct == 0) {
+      const long long lin = (long long)round * r.nst + stage;
+      if (lin < STRACE_CAP) {
+        unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + lin) * STRACE_SLOTS;
+        rec[2] = gtimer();
+        rec[5] = (unsigned long long)clock64();
+      }
+    }
+  }
   __device__ void stage_stamp(int k) {
     const long long lin = (long long)r.round * r.nst + r.stage;
     if (lin < STRACE_CAP) {
@@ -876,7 +893,34 @@ struct Consumer {
   //
   // PAIRS: rows come as (gate, up) pairs 2f, 2f+1 and the epilogue is
   // epi(f, j, gate_sum, up_sum); otherwise epi(row, j, sum).
-  template <bool PAIRS, class Epi>
+  // Window flush of the column-slice GEMV: sum the 8 warps' partials of the
+  // window's rows in warp order and hand each (row or pair, batch row) to the epilogue.
+  template <class Epi>
+  __device__ __forceinline__ void gemv_flush(bool pairs, bool ab, int buf, int wbase, int wrow, int nb, Epi& epi) {
+    cbar();
+    if (ab) return;
+    const float* pb = psum + (size_t)buf * NCW * WIN_ROWS * NB;
+    const int units = pairs ? wrow >> 1 : wrow;
+    for (int x = ct; x < units * nb; x += NCT) {
+      const int u = x / nb, j = x - u * nb;
+      if (pairs) {
+        float g = 0.f, up = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          g += pb[((size_t)w * WIN_ROWS + 2 * u) * NB + j];
+          up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * NB + j];
+        }
+        epi((wbase >> 1) + u, j, g, up);
+      } else {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * NB + j];
+        epi(wbase + u, j, s, 0.f);
+      }
+    }
+  }
+
+  template <bool PAIRS, bool SP, class Epi>
   __device__ bool gemv(int K, int r0, int r1, const float* a, int stride, const int* map, int nb, bool ab,
                        Epi epi) {
     const int rps = PAIRS ? 2 * pairs_per_stage(p) : rows_per_stage(p, K);
@@ -888,8 +932,115 @@ struct Consumer {
     if ((K & 2047) == 0) {
       const int spw = K >> 11;  // granules per lane per row
       int wbase = r0, wrow = 0, buf = 0;
-      for (int s0 = r0; s0 < r1; s0 += rps) {
+      for (int s0 = r0; s0 < r1;) {
         const int n = min(rps, r1 - s0);
+        if constexpr (SP && NB <= 2) {
+          // two stages per pass when a second one follows and both fit the
+          // window: twice the independent work between reductions
+          const int n2 = min(rps, r1 - s0 - rps);
+          if ((rps == 8 || rps == 4) && n == rps && n2 > 0 && wrow + n + n2 <= WIN_ROWS) {
+            const uint8_t* sa = wait_stage(ab);
+            const int ga = r.stage, ra = r.round;
+            r.advance();
+            const uint8_t* sb = wait_stage(ab);
+            if (sa && sb) {
+              const uint32_t ta = smem_u32(sa), tb = smem_u32(sb);
+              float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
+              if (rps == 8) {
+                // 16 rows: 8 from each stage, one granule column per lane (K = 2048)
+                float part[16][NB];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
+                for (int sw = 0; sw < spw; ++sw) {
+                  const int gi = (cw + NCW * sw) * 32 + lane;
+                  float4 x0[NB], x1[NB];
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) {
+                    x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+                  uint4 wv[16];
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) wv[q] = lds128(ta + (uint32_t)q * rowb + gi * 16);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+                    wv[8 + q] = q < n2 ? lds128(tb + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                  for (int q = 0; q < 16; ++q)
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                  if (j < nb) {
+                    float v[8], w2[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                      v[q] = part[q][j];
+                      w2[q] = part[8 + q][j];
+                    }
+                    const float sum = reduce8(v, lane), sum2 = reduce8(w2, lane);
+                    const int q = (lane >> 2) & 7;
+                    if ((lane & 3) == 0) {
+                      ps[(wrow + q) * NB + j] = sum;
+                      if (q < n2) ps[(wrow + 8 + q) * NB + j] = sum2;
+                    }
+                  }
+                }
+              } else {
+                // 8 rows: 4 from each stage (K = 4096, two granule columns per lane)
+                float part[8][NB];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
+                for (int sw = 0; sw < spw; ++sw) {
+                  const int gi = (cw + NCW * sw) * 32 + lane;
+                  float4 x0[NB], x1[NB];
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) {
+                    x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+                  uint4 wv[8];
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) wv[q] = lds128(ta + (uint32_t)q * rowb + gi * 16);
+#pragma unroll
+                  for (int q = 0; q < 4; ++q)
+                    wv[4 + q] = q < n2 ? lds128(tb + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                  if (j < nb) {
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = part[q][j];
+                    const float sum = reduce8(v, lane);
+                    const int q = (lane >> 2) & 7;
+                    if ((lane & 3) == 0 && q < 4 + n2) ps[(wrow + q) * NB + j] = sum;
+                  }
+                }
+              }
+            }
+            release_at(ab, ga, ra);
+            release_stage(ab);
+            wrow += n + n2;
+            s0 += n + n2;
+            if (wrow + rps > WIN_ROWS || s0 >= r1) {
+              gemv_flush(PAIRS, ab, buf, wbase, wrow, nb, epi);
+              buf ^= 1;
+              wbase = s0;
+              wrow = 0;
+            }
+            continue;
+          }
+        }
         const uint8_t* st = wait_stage(ab);
         if (st) {
           const uint32_t sts = smem_u32(st);
@@ -997,31 +1148,11 @@ struct Consumer {
         }
         release_stage(ab);
         wrow += n;
-        if (wrow + rps > WIN_ROWS || s0 + rps >= r1) {
-          cbar();
-          if (!ab) {
-            const float* pb = psum + (size_t)buf * NCW * WIN_ROWS * NB;
-            const int units = PAIRS ? wrow >> 1 : wrow;
-            for (int x = ct; x < units * nb; x += NCT) {
-              const int u = x / nb, j = x - u * nb;
-              if (PAIRS) {
-                float g = 0.f, up = 0.f;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) {
-                  g += pb[((size_t)w * WIN_ROWS + 2 * u) * NB + j];
-                  up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * NB + j];
-                }
-                epi((wbase >> 1) + u, j, g, up);
-              } else {
-                float s = 0.f;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * NB + j];
-                epi(wbase + u, j, s, 0.f);
-              }
-            }
-          }
+        s0 += n;
+        if (wrow + rps > WIN_ROWS || s0 >= r1) {
+          gemv_flush(PAIRS, ab, buf, wbase, wrow, nb, epi);
           buf ^= 1;
-          wbase = s0 + n;
+          wbase = s0;
           wrow = 0;
         }
       }
@@ -1390,7 +1521,7 @@ struct Consumer {
       e.toks = toks;
       e.ranks = ranks;
       e.gate_w = m->gate;
-      ab = gemv<true>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, e);
+      ab = gemv<true, SP_MOE>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, e);
       q = (u + 1) * F;
     }
     cbar();   // coefficients complete; the activation region is free
@@ -1877,7 +2008,7 @@ struct Consumer {
       bi[j] = 0x7fffffff;
     }
     float* lg = p.logits;
-    ab = gemv<false>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s, float) {
+    ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s, float) {
       if (lg) lg[(size_t)j * p.V + row] = s;
 #pragma unroll
       for (int jj = 0; jj < NB; ++jj)
@@ -1963,7 +2094,7 @@ struct Consumer {
           ProjGemv g;
           ab = t.type == T_QKV ? prep_qkv(t, ab, g) : t.type == T_OPROJ ? prep_oproj(t, ab, g) : prep_router(t, ab, g);
           mark(TR_ACT);
-          ab = gemv<false>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
+          ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
           mark(TR_STAGES);
           ab = post_proj(t, ab);
           break;
