@@ -306,7 +306,7 @@ def our_arm(args, wl):
         dist.destroy_process_group()
 
 
-PHASES = ["QKV", "ATTN", "OPROJ", "ROUTER", "EXPERT", "REDUCE", "LM", "COMBINE"]
+PHASES = ["QKV", "ATTN", "OPROJ", "EXPERT", "REDUCE", "LM", "COMBINE"]
 
 
 def summarize_timeline(tasks, stamps, step_ms) -> str:
@@ -336,18 +336,21 @@ def summarize_timeline(tasks, stamps, step_ms) -> str:
                        f"mid1>mid2 {float((S[mm, 11] - S[mm, 10]).mean()):.2f}  "
                        f"mid2>act {float((S[mm, 2] - S[mm, 11]).mean()):.2f}")
     L = int(lay.max()) + 1
-    ends = [float(S[(typ == 5) & (lay == l), 4].max()) for l in range(L)]
+    red, lmk = PHASES.index("REDUCE"), PHASES.index("LM")
+    ends = [float(S[(typ == red) & (lay == l), 4].max()) for l in range(L)]
     dl = [b - a for a, b in zip(ends, ends[1:])] or [ends[0]]
     out.append(f"per-layer time us: median {st.median(dl):.2f} min {min(dl):.2f} max {max(dl):.2f}")
     l = L // 2
     out.append(f"layer {l} phase windows (us): dependency met first..last | done last | producer first copy")
-    for k in range(6):
+    for k in range(len(PHASES)):
         m = (typ == k) & (lay == l)
+        if k == lmk:
+            continue
         if int(m.sum()) == 0:
             continue
         out.append(f"  {PHASES[k]:8s} dep {float(S[m, 1].min()):9.1f}..{float(S[m, 1].max()):9.1f} | done "
                    f"{float(S[m, 4].max()):9.1f} | prod {float(S[m, 5].min()):9.1f}..{float(S[m, 5].max()):9.1f}")
-    m = typ == 6
+    m = typ == lmk
     out.append(f"LM head: start {float(S[m, 1].min()):.1f} end {float(S[m, 4].max()):.1f}")
     return "\n".join(out)
 

@@ -61,7 +61,10 @@ typedef struct mk_model_dims {
  *               rows grouped per KV head g: the G query heads of group g
  *               (G*head_dim rows), then key head g, then value head g
  *   wo[l]       [hidden, n_q_heads * head_dim]
- *   router[l]   [n_experts, hidden]
+ *   router[l]   [hidden, n_experts]: the router stored transposed, row h =
+ *               the n_experts weights of hidden unit h (W_router[:, h]), so
+ *               an O-projection tile reads the router rows of its own hidden
+ *               rows contiguously (n_experts must be a multiple of 4)
  *   w_gate_up[l][n_experts, 2*expert_ffn, hidden]: rows interleaved per ffn
  *               unit f: row 2f = gate row f, row 2f+1 = up row f
  *   w_down[l]   [n_experts, expert_ffn, hidden]: the down projection stored
@@ -168,7 +171,8 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  *                        consumer fetched, dependency met, activations ready, stages
  *                        consumed, done; producer first copy, last copy, start;
  *                        first and last stage landed; two steps inside the activation
- *                        part (gate/up: norm done, routing done); 0 = not recorded
+ *                        part (expert tile: norm and router logits done, routing done);
+ *                        0 = not recorded
  *                        (needs opts.trace)
  *   MK_DBG_STAGE_TRACE   uint64 [num_ctas, 4096, 6]      per CTA, its ring stages in order:
  *                        copy issued, landed (seen by the first consumer warp), released

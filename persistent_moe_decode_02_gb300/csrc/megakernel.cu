@@ -273,6 +273,7 @@ struct Misc {
   int ticket_last;
   int pad;
   float red[NCW * MAX_BATCH];
+  float inv[MAX_BATCH];    // 1 / rms of each activation row of the last norm (its GEMV epilogue scales by it)
   float best_v[NCW * MAX_BATCH];
   int best_i[NCW * MAX_BATCH];
   int sel[MAX_BATCH * MAX_TOPK];
@@ -379,9 +380,14 @@ __device__ __forceinline__ void attn_range(const Params& p, const Task& t, int p
 // Flattened (distinct expert, ffn row) range of gate/up tile a0 of a1.
 __device__ __forceinline__ void gu_range(const Params& p, const Task& t, int U, long long& q0,
                                          long long& q1) {
-  const long long tot = (long long)U * p.F;
-  q0 = tot * t.a[0] / t.a[1];
-  q1 = tot * (t.a[0] + 1) / t.a[1];
+  const unsigned tot = (unsigned)U * (unsigned)p.F, i = (unsigned)t.a[0], n = (unsigned)t.a[1];
+  if ((unsigned long long)tot * n < (1ull << 32)) {   // 32-bit division: the common case
+    q0 = tot * i / n;
+    q1 = tot * (i + 1) / n;
+  } else {
+    q0 = (long long)tot * i / n;
+    q1 = (long long)tot * (i + 1) / n;
+  }
 }
 
 __device__ __forceinline__ const int* route_of(const Params& p, int l) {
@@ -396,6 +402,7 @@ struct Geo {
   int type, nst, l;
   // row tasks
   const uint16_t* W;
+  const uint16_t* W2;   // expert tile: the layer's down matrix (W: its gate/up matrix)
   int K, r0, r1, rps;
   // attention
   int pg0, pg1, ppg, b, g;
@@ -445,17 +452,17 @@ struct Producer {
     Misc* m = r.m;
     if (ld_acquire_cta(&m->r_layer) != l) {
       if (!wait) return false;
-      // poll with plain loads (no fence per poll), acquire once seen
+      // poll with plain loads (no fence, no sleep: the table is a few hundred
+      // cycles away and the first copies wait on it), acquire once seen
       const uint64_t t0 = gtimer();
       for (uint32_t it = 1; *(volatile int*)&m->r_layer != l; ++it) {
-        if ((it & 7) == 0) {
+        if ((it & 63) == 0) {
           if (*(volatile int*)&m->abort_flag || failed(p)) return false;
           if (gtimer() - t0 > p.timeout_ns) {
             set_error(p, MK_ERR_DEP_TIMEOUT, task, -5);
             return false;
           }
         }
-        __nanosleep(128);
       }
       if (ld_acquire_cta(&m->r_layer) != l) return false;
     }
@@ -473,13 +480,13 @@ struct Producer {
     q.l = t.layer;
     const int l = t.layer;
     switch (t.type) {
-      case T_QKV: case T_OPROJ: case T_ROUTER: case T_LM: {
-        q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : t.type == T_ROUTER ? p.router[l] : p.lm_head;
+      case T_QKV: case T_OPROJ: case T_LM: {
+        q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : p.lm_head;
         q.K = t.type == T_OPROJ ? p.nq * p.d : p.H;
         q.r0 = t.a[0];
         q.r1 = t.a[1];
         q.rps = rows_per_stage(p, q.K);
-        q.nst = (q.r1 - q.r0 + q.rps - 1) / q.rps;
+        q.nst = (q.r1 - q.r0 + q.rps - 1) / q.rps + (t.type == T_OPROJ ? 1 : 0);   // + the router stage
         return true;
       }
       case T_ATTN: {
@@ -496,6 +503,10 @@ struct Producer {
         return true;
       }
       case T_MOE: {
+        // the layer's expert matrices first: their pointer loads overlap the routing wait
+        q.W = p.w_gate_up[l];
+        q.W2 = p.w_down[l];
+        asm volatile("" ::"l"(q.W), "l"(q.W2));
         if (!route_ready(c, l, wait, task)) return false;
         q.rc = c;
         long long g0, g1;
@@ -534,7 +545,16 @@ struct Producer {
   __device__ void segs(Geo& q, int s, F f) {
     const int l = q.l;
     switch (q.type) {
-      case T_QKV: case T_OPROJ: case T_ROUTER: case T_LM: {
+      case T_QKV: case T_OPROJ: case T_LM: {
+        if (q.type == T_OPROJ && s == q.nst - 1) {
+          // the O tile's router stage: rows [r0, r1) of the transposed router,
+          // then the 16-byte window of the FFN norm's gain around the same rows
+          const int nr = q.r1 - q.r0;
+          f(p.router[l] + (size_t)q.r0 * p.E, (uint32_t)nr * p.E * 2, 0u);
+          const uint32_t w0 = (uint32_t)q.r0 * 2 / 16 * 16, w1 = ((uint32_t)q.r1 * 2 + 15) / 16 * 16;
+          f(reinterpret_cast<const uint8_t*>(p.ffn_norm[l]) + w0, w1 - w0, (uint32_t)router_stage_gain_off(nr, p.E));
+          break;
+        }
         const int s0 = q.r0 + s * q.rps;
         const int n = min(q.rps, q.r1 - s0);
         f(q.W + (size_t)s0 * q.K, (uint32_t)n * q.K * 2, 0u);
@@ -570,7 +590,7 @@ struct Producer {
           }
           const int fb = min(F, q.q1 - q.cu * F);
           const int n = min(q.pps, fb - q.cf);
-          const uint16_t* We = p.w_gate_up[l] + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
+          const uint16_t* We = q.W + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
           f(We + (size_t)2 * q.cf * H, (uint32_t)n * 2 * H * 2, 0u);
         } else {
           const int s2 = s - q.nst_gu;
@@ -590,7 +610,7 @@ struct Producer {
           }
           const int fb = min(F, q.q1 - q.wu * F);
           const int n = min(q.rpw, fb - q.wf);
-          const uint16_t* Wd = p.w_down[l] + ((size_t)q.rc->exp[q.wu] * F + q.wf) * H;   // [E][F][H]
+          const uint16_t* Wd = q.W2 + ((size_t)q.rc->exp[q.wu] * F + q.wf) * H;   // [E][F][H]
           f(Wd, (uint32_t)n * H * 2, 0u);
         }
         break;
@@ -707,27 +727,41 @@ struct Producer {
 // ------------------------------------------------------------------ consumer pieces
 
 // GEMV epilogue shared by the projection and expert tasks, so that one GEMV
-// body (inlined at one call site per row kind) serves all of them:
-//   STORE:  out[j * ld + row] = s
-//   RESID:  out[j * ld + row] = res[j * res_ld + row - res_r0] + s
-//   SWIGLU: (rows are gate/up pairs: row = ffn unit f, s = gate, s2 = up)
-//           out[(f + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * silu(s) * s2
+// body (inlined at one call site per row kind) serves all of them.  inv holds
+// the RMS-norm scale of each activation row (the GEMV ran on x * gain):
+//   STORE:  out[j * ld + row] = inv[j] * s
+//   RESID:  out[j * ld + row] = res[j * res_ld + row - res_r0] += s   (no norm; the
+//           sum also replaces the residual in res, for the O tile's router share)
+//   SWIGLU: (rows are gate/up pairs: row = ffn unit f, s = gate, s2 = up; the
+//           token slot j reads activation row toks[j], c = inv[toks[j]])
+//           out[(f + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * silu(c * s) * (c * s2)
 struct GemvEpi {
   enum Kind { STORE, RESID, SWIGLU };
   int kind;
   float* out;
   int ld;
-  const float* res;
+  float* res;
   int res_ld, res_r0;
   int base, k;
   const int* toks;
   const int* ranks;
   const float* gate_w;
+  const float* inv;
   __device__ __forceinline__ void operator()(int row, int j, float s, float s2) const {
     switch (kind) {
-      case STORE: out[(size_t)j * ld + row] = s; break;
-      case RESID: out[(size_t)j * ld + row] = res[j * res_ld + row - res_r0] + s; break;
-      default: out[(size_t)(row + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * (s / (1.0f + expf(-s)) * s2);
+      case STORE: out[(size_t)j * ld + row] = inv[j] * s; break;
+      case RESID: {
+        float* r = res + j * res_ld + row - res_r0;
+        const float v = *r + s;
+        *r = v;
+        out[(size_t)j * ld + row] = v;
+        break;
+      }
+      default: {
+        const int tj = toks[j];
+        const float c = inv[tj], g = c * s;
+        out[(size_t)(row + base) * ld + j] = gate_w[tj * k + ranks[j]] * (g / (1.0f + expf(-g)) * (c * s2));
+      }
     }
   }
 };
@@ -799,10 +833,12 @@ struct Consumer {
   }
 
   // ---- activations
-  // act[b * H + i] = x_b[i] / sqrt(mean(x_b^2) + eps) * gamma[i] for b < B, with
-  // x_b read four floats at a time by src(b, i4).  The gain is read in the
-  // same pass as x (one L2 round trip): the first pass stores x * gamma and
-  // the sums of squares of x, the second scales by 1 / rms.
+  // act[b * H + i] = x_b[i] * gamma[i] for b < B, with x_b read four floats at
+  // a time by src(b, i4), and m->inv[b] = 1 / sqrt(mean(x_b^2) + eps): the
+  // norm's scale is applied to the GEMV sums (the map is linear), so the gain
+  // and x come in one L2 round trip and the activations are written once.
+  // m->inv is written after a barrier; every caller passes another barrier
+  // before its GEMV reads it.
   template <class Src4>
   __device__ void fill_rmsnorm(const uint16_t* gamma, Src4 src) {
     const int H = p.H, H4 = H >> 2, B = p.B;
@@ -820,21 +856,11 @@ struct Consumer {
       if (lane == 0) m->red[b * NCW + cw] = ss;
     }
     cbar();
-    for (int b = 0; b < B; ++b) {
+    if (ct < B) {
       float tot = 0.f;
 #pragma unroll
-      for (int w = 0; w < NCW; ++w) tot += m->red[b * NCW + w];
-      const float inv = 1.0f / sqrtf(tot / (float)H + p.eps);
-      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
-#pragma unroll 4
-      for (int i = ct; i < H4; i += NCT) {
-        float4 v = dst[i];
-        v.x *= inv;
-        v.y *= inv;
-        v.z *= inv;
-        v.w *= inv;
-        dst[i] = v;
-      }
+      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
+      m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
     }
   }
 
@@ -1306,6 +1332,7 @@ struct Consumer {
     g.epi.kind = GemvEpi::STORE;
     g.epi.out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
     g.epi.ld = p.qkv_rows;
+    g.epi.inv = m->inv;
     return ab;
   }
 
@@ -1333,28 +1360,38 @@ struct Consumer {
     return ab;
   }
 
-  __device__ bool prep_router(const Task& t, bool ab, ProjGemv& g) {
-    const int l = t.layer;
-    if (!ab) fill_ffn_norm(l);
-    cbar();
-    g.K = p.H;
-    g.r0 = t.a[0];
-    g.r1 = t.a[1];
-    g.epi = GemvEpi{};
-    g.epi.kind = GemvEpi::STORE;
-    g.epi.out = p.rlog + (size_t)l * p.bcap * p.E;
-    g.epi.ld = p.E;
-    return ab;
-  }
-
   __device__ bool post_proj(const Task& t, bool ab) {
     const int l = t.layer;
+    if (t.type == T_OPROJ) ab = router_part(t, ab);
     ab = finish(ab);
     if (!ab) {
       if (t.type == T_QKV) signal(p.cm.qkv + l * p.nkv + t.a[2]);
-      else if (t.type == T_OPROJ) signal(p.cm.o + l);
-      else signal(p.cm.rticket + l);
+      else signal(p.cm.o + l);
     }
+    return ab;
+  }
+
+  // The O tile's share of the router logits over its hidden rows h in [r0, r1):
+  //   part[b][e] = sum_h WrT[h][e] * gain[h] * x_mid[b][h]
+  // (the logits are inv_rms(x_mid_b) times the sum of every tile's part), from
+  // the x_mid rows the residual epilogue left in the scratch and the router stage.
+  __device__ bool router_part(const Task& t, bool ab) {
+    const int r0 = t.a[0], nr = t.a[1] - r0, E = p.E;
+    const uint8_t* st = wait_stage(ab);
+    cbar();   // every x_mid row of the tile is in the scratch
+    if (st) {
+      const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
+      const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
+      float* out = p.rpart + (size_t)t.a[2] * p.bcap * E;
+      for (int x = ct; x < p.B * E; x += NCT) {
+        const int b = x / E, e = x - b * E;
+        const float* xr = scr + b * nr;
+        float acc = 0.f;
+        for (int i = 0; i < nr; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
+        out[(size_t)b * E + e] = acc;
+      }
+    }
+    release_stage(ab);
     return ab;
   }
 
@@ -1373,7 +1410,8 @@ struct Consumer {
   //  - gates: softmax over the selected logits;
   //  - the distinct experts in ascending order, with their (request, rank)
   //    pairs in request order (r_U, r_exp, r_cnt, r_tok, r_rank).
-  // Then the table is handed to this CTA's producer (r_layer).  With publish
+  // The distinct experts go to this CTA's producer (r_layer) as soon as they
+  // are known, before the token lists.  With publish
   // set it also goes to global memory (ids, gates, routing table) and the
   // rdone counter is signalled.
   // Expects m->rl loaded and m->cnt_of zeroed, both behind a barrier.
@@ -1395,12 +1433,13 @@ struct Consumer {
       int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
       int e2 = e_lo;
       const int vec_hi = (E & 7) == 0 ? e_hi : e_lo;
-      for (; e2 + 4 <= vec_hi; e2 += 4) {
+#pragma unroll 8
+      for (; e2 + 4 <= vec_hi; e2 += 4) {   // branch-free: (w > v) | (w == v & index < e)
         const float4 w = *reinterpret_cast<const float4*>(row + e2);
-        r0 += (w.x > v) || (w.x == v && e2 < e);
-        r1 += (w.y > v) || (w.y == v && e2 + 1 < e);
-        r2 += (w.z > v) || (w.z == v && e2 + 2 < e);
-        r3 += (w.w > v) || (w.w == v && e2 + 3 < e);
+        r0 += (w.x > v) | ((w.x == v) & (e2 < e));
+        r1 += (w.y > v) | ((w.y == v) & (e2 + 1 < e));
+        r2 += (w.z > v) | ((w.z == v) & (e2 + 2 < e));
+        r3 += (w.w > v) | ((w.w == v) & (e2 + 3 < e));
       }
       for (; e2 < e_hi; ++e2) r0 += (row[e2] > v) || (row[e2] == v && e2 < e);
       int rank = (r0 + r1) + (r2 + r3);
@@ -1444,6 +1483,7 @@ struct Consumer {
       if (lane == 0) m->r_U = base;
     }
     cbar();
+    if (ct == 0) st_release_cta(&m->r_layer, l);   // the producer needs only r_U and r_exp
     if (ct < B * k) {
       const int e = m->sel[ct];
       int rank = 0;
@@ -1453,7 +1493,6 @@ struct Consumer {
       m->r_rank[u * bc + rank] = ct % k;
     }
     cbar();
-    if (ct == 0) st_release_cta(&m->r_layer, l);
     if (!publish) return;
     int* rt = const_cast<int*>(route_of(p, l));
     const int U = m->r_U;
@@ -1470,8 +1509,79 @@ struct Consumer {
       p.ids[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->sel[ct];
       p.gates[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->gate[ct];
     }
+    for (int i = ct; i < B * E; i += NCT) p.rlog[((size_t)l * p.bcap + i / E) * E + i % E] = m->rl[i];
     cbar();
     signal(p.cm.rdone + l);
+  }
+
+  // The expert tile's activations: act = x_mid * FFN gain with m->inv (as
+  // fill_rmsnorm), and the layer's router logits m->rl[b * E + e] = inv[b] *
+  // (the sum of the O tiles' partials in a fixed order), NaN ranked as -inf.
+  // With the (request, expert) float4 columns no more than the threads, G
+  // groups of threads take every G-th tile (a group reads consecutive columns
+  // of a tile: coalesced) and the group sums are added in group order; else
+  // thread t sums whole columns t, t + 256, ...  The first BT partial loads are
+  // issued before the norm's loads, so the two arrive in one round trip.
+  __device__ void moe_act(int l) {
+    constexpr int BT = 10;
+    const int E = p.E, ncol = (p.B * E) >> 2, T = p.o_tiles;
+    const float4* rp = reinterpret_cast<const float4*>(p.rpart);
+    const size_t ts = ((size_t)p.bcap * E) >> 2;   // float4 per tile
+    float4* rl4 = reinterpret_cast<float4*>(m->rl);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool grp = ncol <= NCT;
+    const int G = grp ? NCT / ncol : 1, g = grp ? ct / ncol : 0, c = grp ? ct - g * ncol : ct;
+    const bool mine = g < G && c < ncol;
+    auto add4 = [](float4& a, const float4 b) {
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    };
+    // tiles g + G * i for i in [i0, T): BT loads in flight, added in tile order
+    auto sum_from = [&](float4 acc, int col, int i0) {
+      for (int tb = g + i0 * G; tb < T; tb += BT * G) {
+        float4 v[BT];
+#pragma unroll
+        for (int r = 0; r < BT; ++r) {
+          const int tt = tb + r * G;
+          v[r] = tt < T ? __ldcg(rp + tt * ts + col) : z4;
+        }
+#pragma unroll
+        for (int r = 0; r < BT; ++r) add4(acc, v[r]);
+      }
+      return acc;
+    };
+    for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
+    fill_ffn_norm(l);   // m->inv is published by the next barrier
+    float4 acc = z4;
+    if (mine) acc = sum_from(acc, c, 0);
+    auto scaled = [&](float4 a, int col) {   // column col holds request (4 col) / E
+      const float inv = m->inv[(col << 2) / E];
+      a.x *= inv;
+      a.y *= inv;
+      a.z *= inv;
+      a.w *= inv;
+      a.x = a.x == a.x ? a.x : -INFINITY;
+      a.y = a.y == a.y ? a.y : -INFINITY;
+      a.z = a.z == a.z ? a.z : -INFINITY;
+      a.w = a.w == a.w ? a.w : -INFINITY;
+      return a;
+    };
+    if (grp) {
+      if (mine) rl4[g * ncol + c] = acc;   // staging: G * ncol <= 256 float4
+      cbar();
+      float4 s4 = z4;
+      if (ct < ncol)
+        for (int q = 0; q < G; ++q) add4(s4, rl4[q * ncol + ct]);
+      cbar();
+      if (ct < ncol) rl4[ct] = scaled(s4, ct);
+    } else {
+      rl4[ct] = acc;
+      for (int c2 = ct + NCT; c2 < ncol; c2 += NCT) rl4[c2] = sum_from(z4, c2, 0);
+      cbar();
+      for (int c2 = ct; c2 < ncol; c2 += NCT) rl4[c2] = scaled(rl4[c2], c2);
+    }
   }
 
   // ---- expert tile: the layer's routing, then for this tile's (distinct
@@ -1486,15 +1596,7 @@ struct Consumer {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
     if (!ab) {
-      // router logits for the local top-k, loaded in the same round trip as
-      // the norm's inputs (the fill's barrier publishes them)
-      const float* rlg = p.rlog + (size_t)l * p.bcap * p.E;
-      for (int i = ct; i < p.B * p.E; i += NCT) {
-        const float v = __ldcg(rlg + i);
-        m->rl[i] = v == v ? v : -INFINITY;
-      }
-      for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
-      fill_ffn_norm(l);
+      moe_act(l);
       cbar();
       mark(TR_MID1);
       if (m->r_layer != l || t.a[0] == 0) route_local(l, t.a[0] == 0);
@@ -1521,6 +1623,7 @@ struct Consumer {
       e.toks = toks;
       e.ranks = ranks;
       e.gate_w = m->gate;
+      e.inv = m->inv;
       ab = gemv<true, SP_MOE>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, e);
       q = (u + 1) * F;
     }
@@ -2008,7 +2111,8 @@ struct Consumer {
       bi[j] = 0x7fffffff;
     }
     float* lg = p.logits;
-    ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s, float) {
+    ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s0, float) {
+      const float s = m->inv[j] * s0;
       if (lg) lg[(size_t)j * p.V + row] = s;
 #pragma unroll
       for (int jj = 0; jj < NB; ++jj)
@@ -2089,10 +2193,9 @@ struct Consumer {
       mark(TR_DEP);
       switch (t.type) {
         case T_QKV:
-        case T_OPROJ:
-        case T_ROUTER: {
+        case T_OPROJ: {
           ProjGemv g;
-          ab = t.type == T_QKV ? prep_qkv(t, ab, g) : t.type == T_OPROJ ? prep_oproj(t, ab, g) : prep_router(t, ab, g);
+          ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g);
           mark(TR_ACT);
           ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
           mark(TR_STAGES);

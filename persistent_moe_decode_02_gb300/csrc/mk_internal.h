@@ -31,15 +31,16 @@ enum TaskType : int32_t {
   T_QKV = 0,     // rows [a0,a1) of the grouped QKV matrix, all requests; a2 = KV group
   T_ATTN = 1,    // request a0, KV group a1, KV pages [a2, a3) (a3 < 0: to the current end);
                  // a4 = partial slot, a5 = first slot of (a0, a1), a6 = chunks of (a0, a1)
-  T_OPROJ = 2,   // rows [a0,a1) of Wo, residual add
-  T_ROUTER = 3,  // rows [a0,a1) of the router
-  T_MOE = 4,     // expert tile a0 of a1 over the flattened (distinct expert, ffn unit) space:
-                 // routing from the router logits (tile 0 publishes it), the tile's gate/up
-                 // rows, then the same units' rows of the transposed down matrix, into a
-                 // gated partial of the layer output
-  T_RED = 5,     // rows [a0,a1) of the hidden dim: residual + the a2 expert tiles' partials
-  T_LM = 6,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
-  T_COMB = 7,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
+  T_OPROJ = 2,   // rows [a0,a1) of Wo, residual add, then the same hidden rows' share of
+                 // the router logits (rows [a0,a1) of the transposed router, times the
+                 // FFN norm's gain): partial a2 of the layer's router logits
+  T_MOE = 3,     // expert tile a0 of a1 over the flattened (distinct expert, ffn unit) space:
+                 // router logits from the O tiles' partials, routing (tile 0 publishes it),
+                 // the tile's gate/up rows, then the same units' rows of the transposed
+                 // down matrix, into a gated partial of the layer output
+  T_RED = 4,     // rows [a0,a1) of the hidden dim: residual + the a2 expert tiles' partials
+  T_LM = 5,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
+  T_COMB = 6,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
                  // a5 = first partial slot, a6 = chunks (waits for all of them)
 };
 constexpr int T_LAST = T_COMB;
@@ -57,7 +58,7 @@ static_assert(sizeof(Task) == 48, "task record is 48 bytes");
 // satisfied when counter >= epoch * cnt (epoch = 1, 2, ... since the last reset).
 struct CtrMap {
   int L, nkv, bcap;
-  int qkv, attn, combine, o, rticket, rdone, gu, down, lm, total;
+  int qkv, attn, combine, o, rdone, gu, down, lm, total;
 
   void init(int L_, int nkv_, int bcap_) {
     L = L_; nkv = nkv_; bcap = bcap_;
@@ -66,7 +67,6 @@ struct CtrMap {
     attn = c; c += L * bcap * nkv;
     combine = c; c += L;
     o = c; c += L;
-    rticket = c; c += L;
     rdone = c; c += L;
     gu = c; c += L;
     down = c; c += L;
@@ -138,6 +138,9 @@ struct Params {
   float* gates;         // [L][bcap][k]
   int* route;           // [L][rm.ints]
   float* moe_part;      // [expert tiles][bcap][H] gated partial outputs (reused by every layer)
+  float* rpart;         // [o_tiles][bcap][E] router-logit partials of the O tiles (reused by every
+                        // layer: the next layer's O tiles start after every expert tile of this one)
+  int o_tiles;
   float* lm_val;        // [bcap][lm_tiles]
   int* lm_idx;          // [bcap][lm_tiles]
   int lm_tiles;
@@ -186,11 +189,19 @@ inline int moe_tiles(int umax, int F, int C, int bcap, int cf) {
   return (int)(t > need ? t : need);
 }
 
+// The router stage of an O tile of nr hidden rows: the rows of the transposed
+// router ([nr][E] bf16), then, 16-byte aligned, the 16-byte window of the FFN
+// norm's gain that covers the nr entries (at most nr * 2 + 30 bytes).
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+inline int router_stage_gain_off(int nr, int E) { return (nr * E * 2 + 15) / 16 * 16; }
+inline int router_stage_bytes(int nr, int E) { return router_stage_gain_off(nr, E) + (nr * 2 + 30 + 15) / 16 * 16; }
+
 // Shared-memory layout: [weight ring][activations][misc struct + scratch][GEMV partial sums].
 // The scratch holds an H-row tile's residual rows or an expert tile's coefficients.
-inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bcap, int nb, int down_rows_max,
+inline bool plan_smem(int H, int nq, int d, int G, int E, int F, int ps, int bcap, int nb, int down_rows_max,
                       int cf, size_t misc_struct_bytes, SmemPlan& o) {
-  (void)k;
   const int nqd = nq * d;
   const int widest = H > nqd ? (H > F ? H : F) : (nqd > F ? nqd : F);
   const long long A1 = (long long)bcap * widest;
@@ -217,6 +228,8 @@ inline bool plan_smem(int H, int nq, int d, int G, int k, int F, int ps, int bca
   const int ppg = sb / (2 * ps * d * 2) < 1 ? 1 : sb / (2 * ps * d * 2);
   if (ppg > ppg32 || NCW % ppg != 0 || d / 16 > 8) return false;
   if (H > 8 * NCW * 32 || H % 8 != 0) return false;   // the expert tile's down part: 8 columns per thread
+  // an O tile's router rows and gain window share one stage; logits are summed four at a time
+  if (E % 4 != 0 || router_stage_bytes(down_rows_max, E) > sb) return false;
   o.stage_bytes = sb;
   o.nstages = (int)nst;
   o.act_off = (int)(nst * sb);

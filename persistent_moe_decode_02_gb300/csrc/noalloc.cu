@@ -91,7 +91,7 @@ inline void split_range(int n, int parts, int i, int& a, int& b) {
 }
 
 struct Counts {
-  int qkv_per_g, o, router, gu, down, lm, P, slots, down_rows_max, ntasks, hpc, comb;
+  int qkv_per_g, o, gu, down, lm, P, slots, down_rows_max, ntasks, hpc, comb;
 };
 
 // Emits the step's tasks phase by phase in topological order; a phase with n
@@ -106,7 +106,6 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
   c.qkv_per_g = (C + s.nkv - 1) / s.nkv;
   if (c.qkv_per_g > Rg) c.qkv_per_g = Rg;
   c.o = C < s.H ? C : s.H;
-  c.router = s.E < 32 ? s.E : 32;
   c.gu = mk::moe_tiles(umax, s.F, C, B, mk::cf_floats(s.E, s.k, s.F, C, B));
   c.down = C < s.H ? C : s.H;
   c.lm = 4 * C < s.V ? 4 * C : s.V;
@@ -196,18 +195,11 @@ void emit(const Shape& s, int B, const int* seq_lens, int C, Counts& c, Put put)
       mk::Task t = task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)c.comb);
       t.a[0] = a;
       t.a[1] = b;
-      put(next(), t);
-    }
-    for (int i = 0; i < c.router; ++i) {
-      int a, b;
-      split_range(s.E, c.router, i, a, b);
-      mk::Task t = task(mk::T_ROUTER, l, cm.o + l, (uint32_t)c.o);
-      t.a[0] = a;
-      t.a[1] = b;
+      t.a[2] = i;
       put(next(), t);
     }
     for (int i = 0; i < c.gu; ++i) {
-      mk::Task t = task(mk::T_MOE, l, cm.rticket + l, (uint32_t)c.router);
+      mk::Task t = task(mk::T_MOE, l, cm.o + l, (uint32_t)c.o);
       t.a[0] = i;
       t.a[1] = c.gu;
       put(next(), t);
@@ -330,6 +322,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_gt = dc.take(L * B * s.k * sizeof(float));
   const size_t d_route = dc.take(L * rm.ints * sizeof(int));
   const size_t d_mp = dc.take((size_t)cnt.gu * B * s.H * sizeof(float));
+  const size_t d_rp = dc.take((size_t)cnt.o * B * s.E * sizeof(float));
   const size_t d_lmv = dc.take((size_t)B * cnt.lm * sizeof(float));
   const size_t d_lmi = dc.take((size_t)B * cnt.lm * sizeof(int));
   if (dc.off > kScratchBytes) {
@@ -341,7 +334,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
 
   // shared-memory plan (same layout rule as mk_plan_create)
   mk::SmemPlan sp;
-  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, B, nb, cnt.down_rows_max,
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.E, s.F, s.ps, B, nb, cnt.down_rows_max,
                      mk::cf_floats(s.E, s.k, s.F, C, B), mk::misc_bytes(), sp))
     return fail(MK_ERR_UNSUPPORTED, "shape leaves no room for the shared-memory ring");
   const int smem = sp.smem;
@@ -438,6 +431,8 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.gates = (float*)(base + d_gt);
   P.route = (int*)(base + d_route);
   P.moe_part = (float*)(base + d_mp);
+  P.rpart = (float*)(base + d_rp);
+  P.o_tiles = cnt.o;
   P.lm_val = (float*)(base + d_lmv);
   P.lm_idx = (int*)(base + d_lmi);
   P.lm_tiles = cnt.lm;

@@ -58,7 +58,7 @@ int check_dims(const mk_model_dims* m, Shape& s) {
 }
 
 struct Counts {
-  int qkv_per_g = 0, attn = 0, o = 0, router = 0, gu = 0, down = 0, lm = 0, comb = 0, heads_per_comb = 1;
+  int qkv_per_g = 0, attn = 0, o = 0, gu = 0, down = 0, lm = 0, comb = 0, heads_per_comb = 1;
   int part_slots = 0, pages_per_chunk = 1, down_rows_max = 1;
 };
 
@@ -138,7 +138,6 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   // tile counts
   cnt.qkv_per_g = std::max(1, std::min(Rg, (C + s.nkv - 1) / s.nkv));
   cnt.o = std::max(1, std::min(s.H, C));
-  cnt.router = std::max(1, std::min(s.E, 32));
   const int umax = std::min(s.E, B * s.k);
   cnt.gu = mk::moe_tiles(umax, s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   cnt.down = std::max(1, std::min(s.H, C));
@@ -224,31 +223,22 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     }
     asg.phase(ph);
     ph.clear();
-    // O projection + residual
+    // O projection + residual, each tile with its hidden rows' share of the router logits
     for (int i = 0; i < cnt.o; ++i) {
       int a, b;
       split_range(s.H, cnt.o, i, a, b);
       Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)cnt.comb);
       t.a[0] = a;
       t.a[1] = b;
-      ph.push_back({(double)(b - a) * nqd * 2, t});
+      t.a[2] = i;
+      ph.push_back({(double)(b - a) * (nqd + s.E) * 2, t});
     }
     asg.phase(ph);
     ph.clear();
-    // router logits (every gate/up task takes the top-k from them)
-    for (int i = 0; i < cnt.router; ++i) {
-      int a, b;
-      split_range(s.E, cnt.router, i, a, b);
-      Task t = mk_task(mk::T_ROUTER, l, cm.o + l, (uint32_t)cnt.o);
-      t.a[0] = a;
-      t.a[1] = b;
-      ph.push_back({(double)(b - a) * s.H * 2, t});
-    }
-    asg.phase(ph);
-    ph.clear();
-    // expert tiles over the distinct selected experts: gate/up + down slices
+    // expert tiles over the distinct selected experts (every tile routes from the
+    // O tiles' logit partials): gate/up + down slices
     for (int i = 0; i < cnt.gu; ++i) {
-      Task t = mk_task(mk::T_MOE, l, cm.rticket + l, (uint32_t)cnt.router);
+      Task t = mk_task(mk::T_MOE, l, cm.o + l, (uint32_t)cnt.o);
       t.a[0] = i;
       t.a[1] = cnt.gu;
       ph.push_back({(double)umax * s.F * 6.0 * s.H / cnt.gu, t});
@@ -487,6 +477,7 @@ void fill_params(mk_plan* p) {
   P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
+  P.o_tiles = p->cnt.o;
   P.cf_pairs = std::max(1, mk::cf_floats(s.E, s.k, s.F, p->C, p->bcap) / p->bcap);
   P.trace = p->trace ? p->d_trace : nullptr;
   P.strace = p->trace >= 2 ? p->d_strace : nullptr;
@@ -599,7 +590,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   const int C = p->C;
   const int down_rows_max = (s.H + std::min(s.H, C) - 1) / std::min(s.H, C);
   mk::SmemPlan sp;
-  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.k, s.F, s.ps, bcap, p->nb, down_rows_max,
+  if (!mk::plan_smem(s.H, s.nq, s.d, s.G, s.E, s.F, s.ps, bcap, p->nb, down_rows_max,
                      mk::cf_floats(s.E, s.k, s.F, C, bcap), mk::misc_bytes(), sp))
     return fail(MK_ERR_UNSUPPORTED);
   p->act_floats = sp.act_floats;
@@ -668,6 +659,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   // expert-tile partials, sized for the most tiles any batch up to the capacity needs
   const int moe_max = mk::moe_tiles(std::min(s.E, bcap * s.k), s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   ok &= dalloc(p, &P.moe_part, (size_t)moe_max * bcap * s.H * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.rpart, (size_t)std::min(s.H, C) * bcap * s.E * sizeof(float)) == cudaSuccess;
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;

@@ -47,7 +47,8 @@ class DeviceModel:
             self.wqkv.append(w)
             self.wo.append(normal((H, D.n_q_heads * d), seed, wname("wo", l), device=dev))
             self.ffn_norm.append(normal((H,), seed, wname("ffn_norm", l), mean=1.0, device=dev))
-            self.router.append(normal((E, H), seed, wname("router", l), device=dev))
+            # router stored transposed, [H, E] (values keyed by the logical [E, H] index)
+            self.router.append(normal((E, H), seed, wname("router", l), device=dev).t().contiguous())
             gu = torch.empty(E, F, 2, H, dtype=torch.bfloat16, device=dev)
             tmp = torch.empty(F, H, dtype=torch.bfloat16, device=dev)
             for e in range(E):

@@ -14,7 +14,7 @@ from synth import FULL, MID, TINY, Dims
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-T_QKV, T_ATTN, T_OPROJ, T_ROUTER, T_MOE, T_RED, T_LM, T_COMB = range(8)
+T_QKV, T_ATTN, T_OPROJ, T_MOE, T_RED, T_LM, T_COMB = range(7)
 
 
 @pytest.fixture(scope="module")
@@ -63,7 +63,7 @@ def signals_per_step(D, B, tasks):
     # same layout as the device counter map
     base = {}
     c = 0
-    for name, n in (("qkv", L * nkv), ("attn", L * B * nkv), ("combine", L), ("o", L), ("rticket", L),
+    for name, n in (("qkv", L * nkv), ("attn", L * B * nkv), ("combine", L), ("o", L),
                     ("rdone", L), ("gu", L), ("down", L), ("lm", 1)):
         base[name] = c
         c += n
@@ -76,8 +76,6 @@ def signals_per_step(D, B, tasks):
             sig[base["attn"] + (l * B + a[0]) * nkv + a[1]] += 1
         elif typ == T_OPROJ:
             sig[base["o"] + l] += 1
-        elif typ == T_ROUTER:
-            sig[base["rticket"] + l] += 1
         elif typ == T_MOE:
             sig[base["gu"] + l] += 1
         elif typ == T_RED:
@@ -141,8 +139,6 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
             out.append(base["attn"] + (l * B + a[0]) * nkv + a[1])
         elif typ == T_OPROJ:
             out.append(base["o"] + l)
-        elif typ == T_ROUTER:
-            out.append(base["rticket"] + l)
         elif typ == T_MOE:
             out.append(base["gu"] + l)
         elif typ == T_RED:
@@ -174,8 +170,10 @@ def test_planner_lists_complete_without_deadlock(mk, D, ctx, C):
         assert all(x[1] == y[0] for x, y in zip(rows, rows[1:]))
     cover(T_QKV, D.n_kv_heads * (D.group + 2) * D.head_dim)
     cover(T_OPROJ, D.hidden)
-    cover(T_ROUTER, D.n_experts)
     cover(T_RED, D.hidden)
+    # the O tiles carry distinct router-partial indices 0 .. tiles - 1
+    oi = sorted(t[4] for t in tasks.tolist() if t[0] == T_OPROJ and t[1] == 0)
+    assert oi == list(range(len(oi)))
     lm = sorted((t[2], t[3]) for t in tasks.tolist() if t[0] == T_LM)
     assert lm[0][0] == 0 and lm[-1][1] == D.vocab
     # every query head of every (request, group) is combined exactly once, from
