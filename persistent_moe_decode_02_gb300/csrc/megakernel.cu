@@ -467,10 +467,41 @@ struct Producer {
       if (ld_acquire_cta(&m->r_layer) != l) return false;
     }
     const int U = m->r_U;
-    for (int u = 0; u < U; ++u) c->exp[u] = m->r_exp[u];
+    for (int u0 = 0; u0 < U; u0 += 8) {   // eight loads in flight
+      int e[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) e[i] = u0 + i < U ? m->r_exp[u0 + i] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (u0 + i < U) c->exp[u0 + i] = e[i];
+    }
     c->U = U;
     c->layer = l;
     return true;
+  }
+
+  // Stage layout of expert tile t for U distinct experts: its flattened (distinct
+  // expert, ffn unit) range, gate/up stages of pps units, then down stages of
+  // rpw units, each within one expert; both cursors at their first stage.
+  __device__ void moe_layout(const Task& t, Geo& q, int U) {
+    long long g0, g1;
+    gu_range(p, t, U, g0, g1);
+    q.q0 = (int)g0;
+    q.q1 = (int)g1;
+    q.pps = pairs_per_stage(p);
+    q.rpw = rows_per_stage(p, p.H);
+    const int F = p.F;
+    int ngu = 0, nwd = 0;
+    for (int u = q.q0 / F; u * F < q.q1; ++u) {
+      const int fa = max(q.q0 - u * F, 0), fb = min(F, q.q1 - u * F);
+      ngu += (fb - fa + q.pps - 1) / q.pps;
+      nwd += (fb - fa + q.rpw - 1) / q.rpw;
+    }
+    q.nst_gu = ngu;
+    q.nst = ngu + nwd;
+    q.cs = q.ws = 0;
+    q.cu = q.wu = q.q0 / F;
+    q.cf = q.wf = q.q0 - q.cu * F;
   }
 
   // Geometry of task t; false when its routing is not known (and wait is
@@ -503,30 +534,18 @@ struct Producer {
         return true;
       }
       case T_MOE: {
-        // the layer's expert matrices first: their pointer loads overlap the routing wait
+        // Everything but the expert ids depends on the routing only through U,
+        // the number of distinct experts: lay out the stages for the largest U
+        // the batch can have (always the U of one request) and load the layer's
+        // expert matrices before the wait; redo the layout if U differs.
         q.W = p.w_gate_up[l];
         q.W2 = p.w_down[l];
         asm volatile("" ::"l"(q.W), "l"(q.W2));
+        const int Ug = min(p.E, p.B * p.k);
+        moe_layout(t, q, Ug);
         if (!route_ready(c, l, wait, task)) return false;
         q.rc = c;
-        long long g0, g1;
-        gu_range(p, t, c->U, g0, g1);
-        q.q0 = (int)g0;
-        q.q1 = (int)g1;
-        q.pps = pairs_per_stage(p);
-        q.rpw = rows_per_stage(p, p.H);
-        const int F = p.F;
-        int ngu = 0, nwd = 0;
-        for (int u = q.q0 / F; u * F < q.q1; ++u) {
-          const int fa = max(q.q0 - u * F, 0), fb = min(F, q.q1 - u * F);
-          ngu += (fb - fa + q.pps - 1) / q.pps;
-          nwd += (fb - fa + q.rpw - 1) / q.rpw;
-        }
-        q.nst_gu = ngu;
-        q.nst = ngu + nwd;
-        q.cs = q.ws = 0;
-        q.cu = q.wu = q.q0 / F;
-        q.cf = q.wf = q.q0 - q.cu * F;
+        if (c->U != Ug) moe_layout(t, q, c->U);
         return true;
       }
       case T_RED:      // no weights: reads only the expert tiles' partials
@@ -1395,13 +1414,6 @@ struct Consumer {
     return ab;
   }
 
-  __device__ void fill_ffn_norm(int l) {
-    const float* xm = p.x_mid + (size_t)l * p.bcap * p.H;
-    fill_rmsnorm(p.ffn_norm[l], [&](int b, int i4) {
-      return __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * p.H) + i4);
-    });
-  }
-
   // Routing of layer l from its router logits (m->rl), computed in every
   // gate/up task the same way, so every CTA gets the same bits:
   //  - per request, each expert's rank: how many logits are greater, or equal
@@ -1521,7 +1533,7 @@ struct Consumer {
   // groups of threads take every G-th tile (a group reads consecutive columns
   // of a tile: coalesced) and the group sums are added in group order; else
   // thread t sums whole columns t, t + 256, ...  The first BT partial loads are
-  // issued before the norm's loads, so the two arrive in one round trip.
+  // issued right after the norm's loads, so the two arrive in one round trip.
   __device__ void moe_act(int l) {
     constexpr int BT = 10;
     const int E = p.E, ncol = (p.B * E) >> 2, T = p.o_tiles;
@@ -1553,9 +1565,52 @@ struct Consumer {
       return acc;
     };
     for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
-    fill_ffn_norm(l);   // m->inv is published by the next barrier
+    // the norm (as fill_rmsnorm): request 0's inputs (at most two float4 per
+    // thread: H <= 2048) are loaded, then the first BT partials, then both used
+    const int H = p.H, H4 = H >> 2;
+    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
+    const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
+    float4 x0[2];
+    uint2 g0[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = ct + h * NCT;
+      x0[h] = i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm) + i) : z4;
+      g0[h] = i < H4 ? __ldg(gam + i) : make_uint2(0u, 0u);
+    }
+    float4 v[BT];
+#pragma unroll
+    for (int r = 0; r < BT; ++r) {
+      const int tt = g + r * G;
+      v[r] = mine && tt < T ? __ldcg(rp + tt * ts + c) : z4;
+    }
+    for (int b = 0; b < p.B; ++b) {
+      float ss = 0.f;
+      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = ct + h * NCT;
+        if (i < H4) {
+          const float4 xv = b == 0 ? x0[h] : __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i);
+          const uint2 gb = b == 0 ? g0[h] : __ldg(gam + i);
+          dst[i] = make_float4(xv.x * bf_lo(gb.x), xv.y * bf_hi(gb.x), xv.z * bf_lo(gb.y), xv.w * bf_hi(gb.y));
+          ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) m->red[b * NCW + cw] = ss;
+    }
     float4 acc = z4;
-    if (mine) acc = sum_from(acc, c, 0);
+#pragma unroll
+    for (int r = 0; r < BT; ++r) add4(acc, v[r]);
+    if (mine) acc = sum_from(acc, c, BT);
+    cbar();
+    if (ct < p.B) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
+      m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
+    }
     auto scaled = [&](float4 a, int col) {   // column col holds request (4 col) / E
       const float inv = m->inv[(col << 2) / E];
       a.x *= inv;
