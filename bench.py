@@ -219,8 +219,7 @@ def our_arm(args, wl):
     max_pages = max((c + total_steps + ps) // ps for c in wl.ctx) + 1
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, total_steps) + 4, max_pages, wl.seed)
     reqs = [kv.admit(rid, c, total_steps) for rid, c in enumerate(wl.ctx)]
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
-                   l2_ahead=args.l2_ahead, l2_wait=args.l2_wait)
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages)
     B = wl.batch
     tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -369,7 +368,7 @@ def timeline_arm(args, wl):
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, steps + 2) + 4, max_pages, wl.seed)
     reqs = [kv.admit(i, c, steps + 2) for i, c in enumerate(wl.ctx)]
     plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
-                   trace=2 if args.stage_trace else 1, l2_ahead=args.l2_ahead, l2_wait=args.l2_wait)
+                   trace=2 if args.stage_trace else 1)
     tok = torch.tensor(initial_tokens(wl, list(range(wl.batch))), dtype=torch.int32, device="cuda")
     times = []
     for _ in range(steps):
@@ -404,10 +403,6 @@ def main():
                     help="trace --steps steps per task and write a summary to this path ('-': print only)")
     ap.add_argument("--stage-trace", action="store_true",
                     help="with --timeline: also record every ring stage (saved beside the summary)")
-    ap.add_argument("--l2-ahead", type=int, default=0,
-                    help="stages the producer prefetches into L2 while its ring is full (0: off)")
-    ap.add_argument("--l2-wait", type=int, default=0,
-                    help="stages prefetched into L2 while routing is pending (0: off)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     import synth

@@ -109,11 +109,6 @@ typedef struct mk_plan_opts {
                           0 in production */
   int trace;         /* 1: record a per-task timeline every step (MK_DBG_TRACE); 2: also a
                         per-stage timeline (MK_DBG_STAGE_TRACE) */
-  int l2_ahead;      /* while its ring is full, the producer prefetches up to this many later
-                        stages into L2; <= 0 -> off (the default), at most 64 */
-  int l2_wait;       /* stages of the following routing-independent tasks prefetched into
-                        L2 while a gate/up or down task waits for routing; <= 0 -> off (the
-                        default), at most 64 */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;

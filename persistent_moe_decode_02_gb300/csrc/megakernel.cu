@@ -49,9 +49,9 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
+// Announce bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -69,17 +69,6 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
 }
 
 // Non-blocking probe: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -169,10 +158,6 @@ __device__ __forceinline__ Task ldg_task(const Task* t) {
   return r;
 }
 
-// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
@@ -290,7 +275,7 @@ struct Misc {
   int r_tok[MAX_UNION * MAX_BATCH];
   int r_rank[MAX_UNION * MAX_BATCH];
   // the producer's copies of a layer's distinct experts, one per cursor
-  RouteCache cp_route, pf_route;
+  RouteCache cp_route;
 };
 
 struct Ring {
@@ -417,41 +402,27 @@ struct Geo {
   int ws, wu, wf;   // down cursor, the same for down stage ws
 };
 
-// Producer: one thread that walks the CTA's tasks and fills the ring.  It
-// keeps two cursors over the same sequence of stages: the copy cursor (bulk
-// copies into the ring, paced by the consumers' releases) and a prefetch
-// cursor that pulls later stages into L2.  The prefetch cursor moves only
-// while the copy cursor is blocked -- on a full ring (the consumers wait for
-// a dependency) or on a layer's routing -- so prefetch requests never compete
-// with copies that the consumers are waiting for, and the bytes have time to
-// land before they are copied.  It runs at most pf_ahead stages past the copy
-// cursor.  While the copy cursor waits for routing, the routing-independent
-// tasks that follow (the next layer's projections and attention) are
-// prefetched instead, up to pf_wait stages.
+// Producer: one thread that walks the CTA's tasks and fills the ring with
+// bulk copies, paced by the consumers' releases: a task's weights are in
+// flight as soon as ring slots free up, long before its activations exist.
+// Kept small: the SM's instruction cache is shared with the consumer warps.
 struct Producer {
   const Params& p;
   Ring r;
   uint64_t pol;
   int ti = 0;
-  bool first = true;
-  // prefetch cursor: task pj, next stage pst, linear stage positions
-  int pj = 0, pst = 0, t_end = 0;
-  bool pvalid = false;
-  Geo pg;
-  long long cp_lin = 0, pf_lin = 0;
+  long long cp_lin = 0;   // ring stages filled so far (stage timeline index)
 
   __device__ void mark(int k) {
     if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
   }
 
   // Routing of layer l into cache c (once per layer): this CTA's expert
-  // tile computes it and hands it over in shared memory.  wait: block
-  // (bounded); otherwise return false if it is not known yet.
-  __device__ bool route_ready(RouteCache* c, int l, bool wait, int task) {
+  // tile computes it and hands it over in shared memory (bounded wait).
+  __device__ bool route_ready(RouteCache* c, int l, int task) {
     if (c->layer == l) return true;
     Misc* m = r.m;
     if (ld_acquire_cta(&m->r_layer) != l) {
-      if (!wait) return false;
       // poll with plain loads (no fence, no sleep: the table is a few hundred
       // cycles away and the first copies wait on it), acquire once seen
       const uint64_t t0 = gtimer();
@@ -504,9 +475,9 @@ struct Producer {
     q.cf = q.wf = q.q0 - q.cu * F;
   }
 
-  // Geometry of task t; false when its routing is not known (and wait is
-  // off), on a wait that timed out, or for an unknown task type.
-  __device__ bool geo(const Task& t, Geo& q, RouteCache* c, bool wait, int task) {
+  // Geometry of task t; false on a routing wait that timed out or gave up,
+  // or for an unknown task type.
+  __device__ bool geo(const Task& t, Geo& q, RouteCache* c, int task) {
     q.type = t.type;
     q.l = t.layer;
     const int l = t.layer;
@@ -543,7 +514,7 @@ struct Producer {
         asm volatile("" ::"l"(q.W), "l"(q.W2));
         const int Ug = min(p.E, p.B * p.k);
         moe_layout(t, q, Ug);
-        if (!route_ready(c, l, wait, task)) return false;
+        if (!route_ready(c, l, task)) return false;
         q.rc = c;
         if (c->U != Ug) moe_layout(t, q, c->U);
         return true;
@@ -637,99 +608,37 @@ struct Producer {
     }
   }
 
-  __device__ void prefetch_stage(Geo& q, int s) {
-    segs(q, s, [&](const void* src, uint32_t bytes, uint32_t) { prefetch_l2_bulk(src, bytes); });
-  }
-
-  // Move the prefetch cursor until it is pf_ahead stages past the copy
-  // cursor (at stage s of task ti, geometry q), it reaches a task whose
-  // routing is not known yet, or the list ends.
-  __device__ void run_prefetch(int ti, int s, const Geo& q) {
-    if (pf_lin < cp_lin) {   // behind the copy cursor: restart at its position
-      pj = ti;
-      pst = s;
-      pg = q;
-      pvalid = true;
-      pf_lin = cp_lin;
-    }
-    while (pf_lin < cp_lin + p.pf_ahead) {
-      if (!pvalid) {
-        if (pj >= t_end) return;
-        if (!geo(ldg_task(p.tasks + pj), pg, &r.m->pf_route, false, pj)) return;
-        pvalid = true;
-      }
-      if (pst >= pg.nst) {
-        ++pj;
-        pst = 0;
-        pvalid = false;
-        continue;
-      }
-      prefetch_stage(pg, pst);
-      ++pst;
-      ++pf_lin;
-    }
-  }
-
-  // While task ti waits for routing: prefetch up to pf_wait stages of the
-  // routing-independent tasks that follow it.
-  __device__ void prefetch_while_routing(int ti) {
-    int budget = p.pf_wait;
-    for (int tj = ti + 1; tj < t_end && budget > 0; ++tj) {
-      const Task t = ldg_task(p.tasks + tj);
-      if (t.type == T_MOE) continue;
-      Geo q;
-      if (!geo(t, q, nullptr, false, tj)) return;
-      for (int s = 0; s < q.nst && budget > 0; ++s, --budget) prefetch_stage(q, s);
-    }
-  }
-
-  // Claim the next stage (waiting for its release) and arm it for `bytes`;
-  // a blocked claim first lets the prefetch cursor run (stage s of task ti).
-  __device__ bool open(uint32_t bytes, uint8_t*& dst, uint64_t*& bar, int s, const Geo& q) {
-    Misc* m = r.m;
-    const uint32_t par = (r.round & 1) ^ 1;
-    if (p.pf_ahead > 0 && !mbar_test(&m->empty[r.stage], par)) run_prefetch(ti, s, q);
-    if (!mbar_wait(p, m, &m->empty[r.stage], par, -3)) return false;
-    bar = &m->full[r.stage];
-    dst = r.base + (size_t)r.stage * r.sb;
-    m->armed[r.stage] = r.round;
-    mbar_expect_tx(bar, bytes);
-    if (first) {
-      mark(TR_P_FIRST);
-      first = false;
-    }
-    return true;
-  }
-
   __device__ void run(int t0, int t1) {
-    r.m->cp_route.layer = -1;
-    r.m->pf_route.layer = -1;
-    t_end = t1;
-    pj = t0;
+    Misc* m = r.m;
+    m->cp_route.layer = -1;
     for (ti = t0; ti < t1; ++ti) {
       if (failed(p)) return;
       const Task t = ldg_task(p.tasks + ti);
-      first = true;
       mark(TR_P_START);
       Geo q;
-      if (!geo(t, q, &r.m->cp_route, false, ti)) {
-        if (p.pf_wait > 0) prefetch_while_routing(ti);
-        if (!geo(t, q, &r.m->cp_route, true, ti)) {
-          if (t.type < T_QKV || t.type > T_LAST) set_error(p, MK_ERR_INVALID, ti, t.type);
-          r.m->abort_flag = 1;
-          return;
-        }
+      if (!geo(t, q, &m->cp_route, ti)) {
+        if (t.type < T_QKV || t.type > T_LAST) set_error(p, MK_ERR_INVALID, ti, t.type);
+        m->abort_flag = 1;
+        return;
       }
       for (int s = 0; s < q.nst; ++s) {
-        uint32_t bytes = 0;
-        segs(q, s, [&](const void*, uint32_t b, uint32_t) { bytes += b; });
-        uint8_t* dst;
-        uint64_t* bar;
-        if (!open(bytes, dst, bar, s, q)) {
-          r.m->abort_flag = 1;
+        // claim the slot once the consumers released it, then for each piece
+        // announce its bytes before the copy; the closing arrival completes
+        // the phase when the last byte lands
+        const uint32_t par = (r.round & 1) ^ 1;
+        if (!mbar_wait(p, m, &m->empty[r.stage], par, -3)) {
+          m->abort_flag = 1;
           return;
         }
-        segs(q, s, [&](const void* src, uint32_t b, uint32_t off) { bulk_g2s(dst + off, src, b, bar, pol); });
+        if (s == 0) mark(TR_P_FIRST);
+        uint64_t* bar = &m->full[r.stage];
+        uint8_t* dst = r.base + (size_t)r.stage * r.sb;
+        m->armed[r.stage] = r.round;
+        segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
+          mbar_expect_tx_only(bar, b);
+          bulk_g2s(dst + off, src, b, bar, pol);
+        });
+        mbar_arrive(bar);
         if (p.strace && cp_lin < STRACE_CAP) {
           unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + cp_lin) * STRACE_SLOTS;
           rec[0] = gtimer();

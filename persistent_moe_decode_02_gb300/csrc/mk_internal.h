@@ -118,8 +118,6 @@ struct Params {
   int act_off, act_floats, misc_off;
   int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * WIN_ROWS * nb floats)
   int attn_mrg_floats;   // attention page-group states in the activation region (floats)
-  int pf_ahead;         // stages the producer's L2 prefetch runs ahead of its ring copies (0: off)
-  int pf_wait;          // stages of routing-independent tasks prefetched while routing is pending (0: off)
   int down_rows_max;    // most rows of an H-row tile (O projection, reduce)
   int cf_pairs;         // most (expert, unit) pairs of one expert tile
   int* seq_len;         // device [bcap]

@@ -402,8 +402,6 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.status = (int*)(base + d_stat);
   P.epoch = 1;
   P.timeout_ns = 2000000000ull;
-  P.pf_ahead = 0;
-  P.pf_wait = 0;
   P.strace = nullptr;
   P.cm = cm;
   P.rm = rm;

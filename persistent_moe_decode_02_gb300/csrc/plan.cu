@@ -290,7 +290,7 @@ void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_erro
 
 struct mk_plan {
   Shape s;
-  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0, pf_ahead = 0, pf_wait = 0;
+  int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0;
   int max_pages = 0, num_pages = 0, rope_npos = 0;
   int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0;
   int replans = 0;
@@ -481,8 +481,6 @@ void fill_params(mk_plan* p) {
   P.cf_pairs = std::max(1, mk::cf_floats(s.E, s.k, s.F, p->C, p->bcap) / p->bcap);
   P.trace = p->trace ? p->d_trace : nullptr;
   P.strace = p->trace >= 2 ? p->d_strace : nullptr;
-  P.pf_ahead = p->pf_ahead;
-  P.pf_wait = p->pf_wait;
 }
 
 }  // namespace
@@ -569,8 +567,6 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   p->split_opt = o.split_pages;
   p->drop_task = o.debug_drop_task;
   p->trace = o.trace >= 2 ? 2 : o.trace ? 1 : 0;
-  p->pf_ahead = std::max(0, std::min(o.l2_ahead, 64));
-  p->pf_wait = std::max(0, std::min(o.l2_wait, 64));
   p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
   p->max_pages = max_pages_per_seq;
   p->num_pages = kv->num_pages;

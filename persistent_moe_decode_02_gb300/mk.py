@@ -48,8 +48,7 @@ class MkKv(ctypes.Structure):
 
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
-                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
-                ("l2_ahead", ctypes.c_int), ("l2_wait", ctypes.c_int)]
+                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int)]
 
 
 class MkError(RuntimeError):
@@ -171,8 +170,7 @@ class Plan:
 
     def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
                  max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
-                 split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0,
-                 l2_ahead: int = 0, l2_wait: int = 0):
+                 split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._arrays = {k: _ptr_array(weights[k]) for k in
@@ -186,8 +184,7 @@ class Plan:
                                                               "w_gate_up", "w_down")])
         self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
         self._dims = dims_struct(D)
-        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace), l2_ahead,
-                          l2_wait)
+        opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace))
         self.batch = len(seq_lens)
         pt = [int(x) for x in page_table]
         h = ctypes.c_void_p()

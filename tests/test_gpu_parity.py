@@ -142,20 +142,6 @@ def test_full_b8_long_sampled_requests():
     rep.assert_ok()
 
 
-def test_l2_prefetch_options_keep_results():
-    # the producer's L2 prefetch (ring-full and routing-wait) moves no data
-    # the consumers see: results stay within the oracle bars and bit-equal
-    # to a run without it
-    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 37, 95], steps=4)
-    rep = run_and_check(wl, steps=4, split_pages=2, l2_ahead=6, l2_wait=8)
-    rep.assert_ok()
-    a = GpuRun(wl)
-    b = GpuRun(wl, model=a.model, l2_ahead=3, l2_wait=12)
-    for _ in range(3):
-        x, y = a.step(), b.step()
-        assert torch.equal(x.logits, y.logits) and torch.equal(x.next_tok, y.next_tok)
-
-
 def test_stage_timeline_is_ordered():
     wl = dataclasses.replace(synth.workload("tiny"), steps=2)
     run = GpuRun(wl, trace=2)
