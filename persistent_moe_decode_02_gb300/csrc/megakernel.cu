@@ -1311,12 +1311,19 @@ struct Consumer {
       const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
       const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
       float* out = p.rpart + (size_t)t.a[2] * p.bcap * E;
-      for (int x = ct; x < p.B * E; x += NCT) {
-        const int b = x / E, e = x - b * E;
+      // two neighbouring threads per (b, e), each half the rows, then one shuffle
+      const int n2 = 2 * p.B * E, hr = (nr + 1) >> 1;
+      for (int x0 = 0; x0 < n2; x0 += NCT) {
+        const int x = x0 + ct, half = x & 1, be = x >> 1;
+        const bool ok = x < n2;
+        const int b = ok ? be / E : 0, e = ok ? be - b * E : 0;
         const float* xr = scr + b * nr;
+        const int i0 = half ? hr : 0, i1 = half ? nr : hr;
         float acc = 0.f;
-        for (int i = 0; i < nr; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
-        out[(size_t)b * E + e] = acc;
+        if (ok)
+          for (int i = i0; i < i1; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
+        const float other = __shfl_xor_sync(FULL, acc, 1);
+        if (ok && half == 0) out[(size_t)b * E + e] = acc + other;
       }
     }
     release_stage(ab);
@@ -1678,23 +1685,36 @@ struct Consumer {
     const int nch = no > 0 ? max(1, NCT / no) : 1;
     float* rs = act;                                   // [output][chunk] sums
     mark(TR_ACT);
+    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
+    // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)
+    const float xres = !ab && ct < no ? __ldcg(xm + (size_t)(ct / nr) * H + r0 + ct % nr) : 0.f;
     if (!ab) {
+      // thread x takes output o = x % no and every nch-th tile from chunk c = x / no,
+      // so a warp reads consecutive rows of a tile; up to BT loads in flight
+      constexpr int BT = 10;
       for (int x = ct; x < no * nch; x += NCT) {
-        const int o = x / nch, c = x - o * nch, b = o / nr, h = r0 + (o - b * nr);
+        const int c = x / no, o = x - c * no, b = o / nr, h = r0 + (o - b * nr);
         const float* src = p.moe_part + (size_t)b * H + h;
         float s = 0.f;
-#pragma unroll 4
-        for (int ti = c; ti < ntiles; ti += nch) s += __ldcg(src + (size_t)ti * p.bcap * H);
+        for (int t0 = c; t0 < ntiles; t0 += BT * nch) {
+          float v[BT];
+#pragma unroll
+          for (int i = 0; i < BT; ++i) {
+            const int ti = t0 + i * nch;
+            v[i] = ti < ntiles ? __ldcg(src + (size_t)ti * p.bcap * H) : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < BT; ++i) s += v[i];
+        }
         rs[o * nch + c] = s;
       }
     }
     cbar();
     if (!ab) {
-      const float* xm = p.x_mid + (size_t)l * p.bcap * H;
       float* xo = p.x_out + (size_t)l * p.bcap * H;
       for (int o = ct; o < no; o += NCT) {
         const int b = o / nr, h = r0 + (o - b * nr);
-        float s = __ldcg(xm + (size_t)b * H + h);
+        float s = o == ct ? xres : __ldcg(xm + (size_t)b * H + h);
         for (int c = 0; c < nch; ++c) s += rs[o * nch + c];
         xo[(size_t)b * H + h] = s;
       }
@@ -1704,6 +1724,7 @@ struct Consumer {
     if (!ab) signal(p.cm.down + l);
     return ab;
   }
+
 
   // ---- split-KV attention chunk on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc)
   // Pages hold K and V transposed ([d][16 slots]).  Per page (16 tokens):
@@ -1953,19 +1974,25 @@ struct Consumer {
     float* part = p.part + ((size_t)l * nslots + t.a[4]) * G * RS;
     // per head: the chunk max, normaliser and each warp's weight, once
     float* fw = reinterpret_cast<float*>(pscr);    // [NCW][G] weights (P scratch is free now)
-    if (ct < G) {
-      const int h = ct;
-      float M = -INFINITY;
-      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mrg[(w * G + h) * RS + d]);
-      float Ls = 0.f;
-      for (int w = 0; w < NCW; ++w) {
-        const float mw = mrg[(w * G + h) * RS + d];
-        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    static_assert(NCW == 8 && MAX_G * NCW <= NCT, "eight lanes per head, one per warp state");
+    if (ct < MAX_G * NCW) {   // lanes 8h .. 8h + 7: head h, warp state w (butterflies within the 8)
+      const int h = ct >> 3, w = ct & 7;
+      const bool hv = h < G;
+      const float mw = hv ? mrg[(w * G + h) * RS + d] : -INFINITY;
+      float M = mw;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      float Ls = hv ? mrg[(w * G + h) * RS + d + 1] * f : 0.f;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) Ls += __shfl_xor_sync(FULL, Ls, o);
+      if (hv) {
         fw[w * G + h] = f;
-        Ls = fmaf(mrg[(w * G + h) * RS + d + 1], f, Ls);
+        if (w == 0) {
+          part[h * RS + d] = M;
+          part[h * RS + d + 1] = Ls;
+        }
       }
-      part[h * RS + d] = M;
-      part[h * RS + d + 1] = Ls;
     }
     cbar();
     for (int idx = ct; idx < G * d; idx += NCT) {
