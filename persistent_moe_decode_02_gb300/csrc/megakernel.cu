@@ -1268,11 +1268,15 @@ struct Consumer {
     const int l = t.layer, K = p.nq * p.d, r0 = t.a[0], nr = t.a[1] - r0;
     float* xres = scr;    // residual rows of this tile, [B][nr]
     if (!ab) {
+      // the residual rows' loads go out first, with the attention output's
+      const bool r1st = ct < p.B * nr;
+      const float x1st = r1st ? x_in(l, ct / nr, r0 + ct % nr) : 0.f;
       const float4* o = reinterpret_cast<const float4*>(p.o + (size_t)l * p.bcap * K);
       float4* dst = reinterpret_cast<float4*>(act);
 #pragma unroll 4
       for (int i = ct; i < (p.B * K) >> 2; i += NCT) dst[i] = __ldcg(o + i);
-      for (int i = ct; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
+      if (r1st) xres[ct] = x1st;
+      for (int i = ct + NCT; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
     }
     cbar();
     g.K = K;
