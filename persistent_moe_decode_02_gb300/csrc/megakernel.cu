@@ -708,6 +708,7 @@ struct Consumer {
   Misc* m;
   float* scr;      // after the misc struct: an H-row tile's residual rows, or an expert tile's coefficients
   float* psum;   // per-warp partial sums of wide-row GEMVs: [2 windows][NCW][WIN_ROWS][NB]
+  static constexpr int WIN_ROWS = win_rows(NB);
   int ct, cw, lane;
   int ti = 0;
 

@@ -15,7 +15,9 @@ constexpr int MAX_BATCH = 8;
 constexpr int MAX_EXPERTS = 256;
 constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
 constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
-constexpr int WIN_ROWS = 32;               // rows per cross-warp partial-sum window (wide GEMV)
+// rows per cross-warp partial-sum window of the wide GEMV: 64 at batch <= 2 (a
+// projection tile's rows in one window: one flush), else 32 (shared memory)
+constexpr int win_rows(int nb) { return nb <= 2 ? 64 : 32; }
 constexpr int TRACE_SLOTS = 12;            // stamps per task in the optional timeline
 constexpr int STRACE_CAP = 4096;           // ring stages per CTA in the optional stage timeline
 constexpr int STRACE_SLOTS = 6;            // per stage: copy issued, landed, released, task,
@@ -116,7 +118,7 @@ struct Params {
   RouteMap rm;
   int nstages, stage_bytes;
   int act_off, act_floats, misc_off;
-  int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * WIN_ROWS * nb floats)
+  int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * win_rows(nb) * nb floats)
   int attn_mrg_floats;   // attention page-group states in the activation region (floats)
   int down_rows_max;    // most rows of an H-row tile (O projection, reduce)
   int cf_pairs;         // most (expert, unit) pairs of one expert tile
@@ -214,7 +216,7 @@ inline bool plan_smem(int H, int nq, int d, int G, int E, int F, int ps, int bca
   const size_t act_bytes = ((size_t)act * 4 + 127) / 128 * 128;
   const long long scr = (long long)bcap * down_rows_max > cf ? (long long)bcap * down_rows_max : cf;
   const size_t misc = (misc_struct_bytes + (size_t)scr * 4 + 127) / 128 * 128;
-  const size_t psum = ((size_t)2 * NCW * WIN_ROWS * nb * 4 + 127) / 128 * 128;
+  const size_t psum = ((size_t)2 * NCW * win_rows(nb) * nb * 4 + 127) / 128 * 128;
   const long long avail = (long long)SMEM_LIMIT - (long long)(act_bytes + misc + psum);
   const int need0 = 2 * widest > 4 * H ? 2 * widest : 4 * H;
   const int need = need0 > 2 * ps * d * 2 ? need0 : 2 * ps * d * 2;
