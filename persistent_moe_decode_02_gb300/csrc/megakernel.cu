@@ -711,6 +711,7 @@ struct Consumer {
   static constexpr int WIN_ROWS = win_rows(NB);
   int ct, cw, lane;
   int ti = 0;
+  int lm_done = 0;   // LM-head tiles this CTA finished in this launch (its last task is the last of them)
 
   __device__ void mark(int k) {
     if (p.trace && ct == 0) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
@@ -1235,11 +1236,11 @@ struct Consumer {
     if (ct == 0) atom_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
   }
 
-  // Uniform "am I the last of n producers this step" for counter ctr.
-  __device__ bool ticket(int ctr, uint32_t n) {
+  // Uniform "do my add signals complete the n of this step" for counter ctr.
+  __device__ bool ticket(int ctr, uint32_t n, uint32_t add) {
     if (ct == 0) {
-      const uint32_t old = atom_add_acq_rel(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
-      m->ticket_last = (old == p.epoch * n - 1u) ? 1 : 0;
+      const uint32_t old = atom_add_acq_rel(p.ctr + (size_t)ctr * CTR_STRIDE, add);
+      m->ticket_last = (old + add == p.epoch * n) ? 1 : 0;
     }
     cbar();
     return m->ticket_last != 0;
@@ -1384,48 +1385,76 @@ struct Consumer {
       }
     }
     cbar();
-    // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
-    // groups of kp consecutive lanes (kp = k rounded up to a power of two)
-    {
-      int kp = 1;
-      while (kp < k) kp <<= 1;
-      const int per_warp = 32 / kp;
-      const int b = (cw - 1) * per_warp + lane / kp, j = lane % kp;
-      const bool mine = cw >= 1 && b < B;             // uniform per warp but for the tail
-      const bool act_j = mine && j < k;
-      const float first = mine ? m->selv[b * k] : 0.f;
-      const float ex = act_j ? expf(m->selv[b * k + j] - first) : 0.f;
-      float tot = ex;
-      for (int o = 1; o < kp; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
-      if (act_j) m->gate[b * k + j] = ex / tot;
-    }
-    if (cw == 0) {
-      int base = 0;
-      for (int c = 0; c < (E + 31) / 32; ++c) {
-        const int e = c * 32 + lane;
-        const bool pres = e < E && m->cnt_of[e] > 0;
-        const unsigned mask = __ballot_sync(FULL, pres);
-        if (pres) {
-          const int u = base + __popc(mask & ((1u << lane) - 1u));
-          m->slot_of[e] = u;
-          m->r_exp[u] = e;
-          m->r_cnt[u] = m->cnt_of[e];
+    if (B == 1) {
+      // one request: its k experts are distinct.  Warp 0 holds them in lanes
+      // 0 .. k-1: the gates (softmax over the selected; the butterfly over all
+      // 32 lanes adds only zeros past k), and each expert's place in ascending
+      // id order gives the distinct-expert table, one token slot each.
+      if (cw == 0) {
+        const bool on = lane < k;
+        const int e = on ? m->sel[lane] : 0;
+        const float v = on ? m->selv[lane] : 0.f;
+        const float ex = on ? expf(v - m->selv[0]) : 0.f;
+        float tot = ex;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        int pos = 0;
+        for (int j = 0; j < k; ++j) pos += m->sel[j] < e;
+        if (on) {
+          m->gate[lane] = ex / tot;
+          m->r_exp[pos] = e;
+          m->r_cnt[pos] = 1;
+          m->r_tok[pos * bc] = 0;
+          m->r_rank[pos * bc] = lane;
         }
-        base += __popc(mask);
+        if (lane == 0) m->r_U = k;
       }
-      if (lane == 0) m->r_U = base;
+      cbar();
+      if (ct == 0) st_release_cta(&m->r_layer, l);
+    } else {
+      // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
+      // groups of kp consecutive lanes (kp = k rounded up to a power of two)
+      {
+        int kp = 1;
+        while (kp < k) kp <<= 1;
+        const int per_warp = 32 / kp;
+        const int b = (cw - 1) * per_warp + lane / kp, j = lane % kp;
+        const bool mine = cw >= 1 && b < B;             // uniform per warp but for the tail
+        const bool act_j = mine && j < k;
+        const float first = mine ? m->selv[b * k] : 0.f;
+        const float ex = act_j ? expf(m->selv[b * k + j] - first) : 0.f;
+        float tot = ex;
+        for (int o = 1; o < kp; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        if (act_j) m->gate[b * k + j] = ex / tot;
+      }
+      if (cw == 0) {
+        int base = 0;
+        for (int c = 0; c < (E + 31) / 32; ++c) {
+          const int e = c * 32 + lane;
+          const bool pres = e < E && m->cnt_of[e] > 0;
+          const unsigned mask = __ballot_sync(FULL, pres);
+          if (pres) {
+            const int u = base + __popc(mask & ((1u << lane) - 1u));
+            m->slot_of[e] = u;
+            m->r_exp[u] = e;
+            m->r_cnt[u] = m->cnt_of[e];
+          }
+          base += __popc(mask);
+        }
+        if (lane == 0) m->r_U = base;
+      }
+      cbar();
+      if (ct == 0) st_release_cta(&m->r_layer, l);   // the producer needs only r_U and r_exp
+      if (ct < B * k) {
+        const int e = m->sel[ct];
+        int rank = 0;
+        for (int q = 0; q < ct; ++q) rank += (m->sel[q] == e);
+        const int u = m->slot_of[e];
+        m->r_tok[u * bc + rank] = ct / k;
+        m->r_rank[u * bc + rank] = ct % k;
+      }
+      cbar();
     }
-    cbar();
-    if (ct == 0) st_release_cta(&m->r_layer, l);   // the producer needs only r_U and r_exp
-    if (ct < B * k) {
-      const int e = m->sel[ct];
-      int rank = 0;
-      for (int q = 0; q < ct; ++q) rank += (m->sel[q] == e);
-      const int u = m->slot_of[e];
-      m->r_tok[u * bc + rank] = ct / k;
-      m->r_rank[u * bc + rank] = ct % k;
-    }
-    cbar();
     if (!publish) return;
     int* rt = const_cast<int*>(route_of(p, l));
     const int U = m->r_U;
@@ -2088,15 +2117,19 @@ struct Consumer {
     return ab;
   }
 
-  __device__ bool lm(const Task& t, bool ab) {
+  // LM-head tile.  A CTA's LM tiles are the last tasks of its list: the first
+  // fills the final norm's activations (kept by the later tiles), and only the
+  // last takes the ticket, for all of this CTA's tiles at once.
+  __device__ bool lm(const Task& t, bool ab, bool last) {
     const int L = p.L, B = p.B;
-    if (!ab) {
+    if (!ab && lm_done == 0) {
       const float* xo = p.x_out + (size_t)(L - 1) * p.bcap * p.H;
       fill_rmsnorm(p.final_norm, [&](int b, int i4) {
         return __ldcg(reinterpret_cast<const float4*>(xo + (size_t)b * p.H) + i4);
       });
     }
     cbar();
+    ++lm_done;
     mark(TR_ACT);
     // each thread keeps, per activation row, the best (value, lowest index) it saw
     float bv[NB];
@@ -2148,9 +2181,10 @@ struct Consumer {
       p.lm_val[(size_t)ct * tiles + tile] = v;
       p.lm_idx[(size_t)ct * tiles + tile] = ix;
     }
+    if (!last) return ab;   // the last tile's barrier orders these writes before its ticket
     ab = finish(ab);
     if (ab) return ab;
-    if (ticket(p.cm.lm, (uint32_t)t.a[3])) {
+    if (ticket(p.cm.lm, (uint32_t)t.a[3], (uint32_t)lm_done)) {
       if (cw < B) {
         const int b = cw;
         float v = -INFINITY;
@@ -2201,7 +2235,7 @@ struct Consumer {
         case T_ATTN: ab = attn(t, ab); break;
         case T_MOE: ab = moe(t, ab); break;
         case T_RED: ab = red(t, ab); break;
-        case T_LM: ab = lm(t, ab); break;
+        case T_LM: ab = lm(t, ab, ti + 1 == t1); break;
         case T_COMB: ab = comb(t, ab); break;
         default: ab = true;
       }
