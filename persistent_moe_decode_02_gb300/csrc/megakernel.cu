@@ -163,6 +163,14 @@ __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
+// 32.32 fixed point for the router-logit sums (two's complement in 64 bits).
+__device__ __forceinline__ unsigned long long to_fixed(float v) {
+  return (unsigned long long)__double2ll_rn((double)v * 4294967296.0);
+}
+__device__ __forceinline__ float from_fixed(unsigned long long q) {
+  return (float)((double)(long long)q * 2.3283064365386963e-10);
+}
+
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -1308,7 +1316,9 @@ struct Consumer {
   // The O tile's share of the router logits over its hidden rows h in [r0, r1):
   //   part[b][e] = sum_h WrT[h][e] * gain[h] * x_mid[b][h]
   // (the logits are inv_rms(x_mid_b) times the sum of every tile's part), from
-  // the x_mid rows the residual epilogue left in the scratch and the router stage.
+  // the x_mid rows the residual epilogue left in the scratch and the router
+  // stage.  The parts are added as 32.32 fixed-point integers: the sum is
+  // exact, so its bits do not depend on the order the tiles arrive in.
   __device__ bool router_part(const Task& t, bool ab) {
     const int r0 = t.a[0], nr = t.a[1] - r0, E = p.E;
     const uint8_t* st = wait_stage(ab);
@@ -1316,7 +1326,7 @@ struct Consumer {
     if (st) {
       const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
       const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
-      float* out = p.rpart + (size_t)t.a[2] * p.bcap * E;
+      unsigned long long* out = p.rlsum + (size_t)t.layer * p.bcap * E;
       // two neighbouring threads per (b, e), each half the rows, then one shuffle
       const int n2 = 2 * p.B * E, hr = (nr + 1) >> 1;
       for (int x0 = 0; x0 < n2; x0 += NCT) {
@@ -1329,7 +1339,7 @@ struct Consumer {
         if (ok)
           for (int i = i0; i < i1; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
         const float other = __shfl_xor_sync(FULL, acc, 1);
-        if (ok && half == 0) out[(size_t)b * E + e] = acc + other;
+        if (ok && half == 0) atomicAdd(out + (size_t)b * E + e, to_fixed(acc + other));
       }
     }
     release_stage(ab);
@@ -1478,48 +1488,16 @@ struct Consumer {
 
   // The expert tile's activations: act = x_mid * FFN gain with m->inv (as
   // fill_rmsnorm), and the layer's router logits m->rl[b * E + e] = inv[b] *
-  // (the sum of the O tiles' partials in a fixed order), NaN ranked as -inf.
-  // With the (request, expert) float4 columns no more than the threads, G
-  // groups of threads take every G-th tile (a group reads consecutive columns
-  // of a tile: coalesced) and the group sums are added in group order; else
-  // thread t sums whole columns t, t + 256, ...  The first BT partial loads are
-  // issued right after the norm's loads, so the two arrive in one round trip.
+  // (the O tiles' fixed-point sum), NaN ranked as -inf.  The sums' loads go
+  // out first and the norm's inputs (at most two float4 per thread: H <= 2048)
+  // right after, so both arrive in one round trip.
   __device__ void moe_act(int l) {
-    constexpr int BT = 10;
-    const int E = p.E, ncol = (p.B * E) >> 2, T = p.o_tiles;
-    const float4* rp = reinterpret_cast<const float4*>(p.rpart);
-    const size_t ts = ((size_t)p.bcap * E) >> 2;   // float4 per tile
-    float4* rl4 = reinterpret_cast<float4*>(m->rl);
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool grp = ncol <= NCT;
-    const int G = grp ? NCT / ncol : 1, g = grp ? ct / ncol : 0, c = grp ? ct - g * ncol : ct;
-    const bool mine = g < G && c < ncol;
-    auto add4 = [](float4& a, const float4 b) {
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
-    };
-    // tiles g + G * i for i in [i0, T): BT loads in flight, added in tile order
-    auto sum_from = [&](float4 acc, int col, int i0) {
-      for (int tb = g + i0 * G; tb < T; tb += BT * G) {
-        float4 v[BT];
-#pragma unroll
-        for (int r = 0; r < BT; ++r) {
-          const int tt = tb + r * G;
-          v[r] = tt < T ? __ldcg(rp + tt * ts + col) : z4;
-        }
-#pragma unroll
-        for (int r = 0; r < BT; ++r) add4(acc, v[r]);
-      }
-      return acc;
-    };
-    for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
-    // the norm (as fill_rmsnorm): request 0's inputs (at most two float4 per
-    // thread: H <= 2048) are loaded, then the first BT partials, then both used
-    const int H = p.H, H4 = H >> 2;
+    const int H = p.H, H4 = H >> 2, E = p.E, BE = p.B * E;
+    const unsigned long long* rs = p.rlsum + (size_t)l * p.bcap * E;
+    const unsigned long long q0 = ct < BE ? __ldcg(rs + ct) : 0ull;
     const float* xm = p.x_mid + (size_t)l * p.bcap * H;
     const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 x0[2];
     uint2 g0[2];
 #pragma unroll
@@ -1528,12 +1506,7 @@ struct Consumer {
       x0[h] = i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm) + i) : z4;
       g0[h] = i < H4 ? __ldg(gam + i) : make_uint2(0u, 0u);
     }
-    float4 v[BT];
-#pragma unroll
-    for (int r = 0; r < BT; ++r) {
-      const int tt = g + r * G;
-      v[r] = mine && tt < T ? __ldcg(rp + tt * ts + c) : z4;
-    }
+    for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
     for (int b = 0; b < p.B; ++b) {
       float ss = 0.f;
       float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
@@ -1550,10 +1523,6 @@ struct Consumer {
       ss = warp_sum(ss);
       if (lane == 0) m->red[b * NCW + cw] = ss;
     }
-    float4 acc = z4;
-#pragma unroll
-    for (int r = 0; r < BT; ++r) add4(acc, v[r]);
-    if (mine) acc = sum_from(acc, c, BT);
     cbar();
     if (ct < p.B) {
       float tot = 0.f;
@@ -1561,31 +1530,10 @@ struct Consumer {
       for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
       m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
     }
-    auto scaled = [&](float4 a, int col) {   // column col holds request (4 col) / E
-      const float inv = m->inv[(col << 2) / E];
-      a.x *= inv;
-      a.y *= inv;
-      a.z *= inv;
-      a.w *= inv;
-      a.x = a.x == a.x ? a.x : -INFINITY;
-      a.y = a.y == a.y ? a.y : -INFINITY;
-      a.z = a.z == a.z ? a.z : -INFINITY;
-      a.w = a.w == a.w ? a.w : -INFINITY;
-      return a;
-    };
-    if (grp) {
-      if (mine) rl4[g * ncol + c] = acc;   // staging: G * ncol <= 256 float4
-      cbar();
-      float4 s4 = z4;
-      if (ct < ncol)
-        for (int q = 0; q < G; ++q) add4(s4, rl4[q * ncol + ct]);
-      cbar();
-      if (ct < ncol) rl4[ct] = scaled(s4, ct);
-    } else {
-      rl4[ct] = acc;
-      for (int c2 = ct + NCT; c2 < ncol; c2 += NCT) rl4[c2] = sum_from(z4, c2, 0);
-      cbar();
-      for (int c2 = ct; c2 < ncol; c2 += NCT) rl4[c2] = scaled(rl4[c2], c2);
+    cbar();
+    for (int i = ct; i < BE; i += NCT) {
+      const float v = from_fixed(i == ct ? q0 : __ldcg(rs + i)) * m->inv[i / E];
+      m->rl[i] = v == v ? v : -INFINITY;
     }
   }
 
@@ -1720,6 +1668,11 @@ struct Consumer {
     float* rs = act;                                   // [output][chunk] sums
     mark(TR_ACT);
     const float* xm = p.x_mid + (size_t)l * p.bcap * H;
+    if (!ab) {   // every expert tile of the layer has read the router sums: zero this task's share
+      const long long n = (long long)p.bcap * p.E;
+      unsigned long long* rs = p.rlsum + (size_t)l * n;
+      for (long long i = r0 * n / H + ct; i < (long long)t.a[1] * n / H; i += NCT) rs[i] = 0ull;
+    }
     // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)
     const float xres = !ab && ct < no ? __ldcg(xm + (size_t)(ct / nr) * H + r0 + ct % nr) : 0.f;
     if (!ab) {

@@ -138,9 +138,10 @@ struct Params {
   float* gates;         // [L][bcap][k]
   int* route;           // [L][rm.ints]
   float* moe_part;      // [expert tiles][bcap][H] gated partial outputs (reused by every layer)
-  float* rpart;         // [o_tiles][bcap][E] router-logit partials of the O tiles (reused by every
-                        // layer: the next layer's O tiles start after every expert tile of this one)
-  int o_tiles;
+  unsigned long long* rlsum;   // [L][bcap][E] router-logit sums in 32.32 fixed point: the O tiles
+                               // add their shares (integer adds: exact, any order), the expert
+                               // tiles read them, the layer's reduce tasks zero them for the next
+                               // step (and every replan zeroes all)
   float* lm_val;        // [bcap][lm_tiles]
   int* lm_idx;          // [bcap][lm_tiles]
   int lm_tiles;

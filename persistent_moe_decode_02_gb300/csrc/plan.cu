@@ -446,6 +446,9 @@ int replan(mk_plan* p, cudaStream_t st) {
   p->d_cta = (int*)((uint8_t*)p->d_tasks + tasks.size() * sizeof(Task));
   if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) != cudaSuccess)
     return MK_ERR_CUDA;
+  if (cudaMemsetAsync(p->P.rlsum, 0, (size_t)p->s.L * p->bcap * p->s.E * sizeof(unsigned long long), st) !=
+      cudaSuccess)
+    return MK_ERR_CUDA;
   p->epoch = 0;
   p->tasks.swap(tasks);
   p->cta_start.swap(cs);
@@ -477,7 +480,6 @@ void fill_params(mk_plan* p) {
   P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
-  P.o_tiles = p->cnt.o;
   P.cf_pairs = std::max(1, mk::cf_floats(s.E, s.k, s.F, p->C, p->bcap) / p->bcap);
   P.trace = p->trace ? p->d_trace : nullptr;
   P.strace = p->trace >= 2 ? p->d_strace : nullptr;
@@ -655,7 +657,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   // expert-tile partials, sized for the most tiles any batch up to the capacity needs
   const int moe_max = mk::moe_tiles(std::min(s.E, bcap * s.k), s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   ok &= dalloc(p, &P.moe_part, (size_t)moe_max * bcap * s.H * sizeof(float)) == cudaSuccess;
-  ok &= dalloc(p, &P.rpart, (size_t)std::min(s.H, C) * bcap * s.E * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.rlsum, L * bcap * s.E * sizeof(unsigned long long)) == cudaSuccess;
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;
