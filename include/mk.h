@@ -102,7 +102,11 @@ typedef struct mk_kv {
 typedef struct mk_plan_opts {
   int timeout_us;    /* limit of every device spin-wait; 0 -> 2,000,000 us */
   int num_ctas;      /* persistent CTAs; 0 -> one per SM */
-  int max_batch;     /* batch capacity for mk_plan_update; 0 -> batch */
+  int max_batch;     /* batch capacity for mk_plan_update; 0 -> batch.  Above 8 the plan
+                        is a group of sub-plans of at most 8 requests each (requests
+                        8i .. 8i + 7 in sub-plan i); a step runs one megakernel launch
+                        per sub-plan that holds requests, one after another on the
+                        stream, and each launch streams the weights it needs */
   int split_pages;   /* KV pages per attention task; 0 -> balance over the CTAs */
   int debug_drop_task; /* test hook: >0 removes task (value-1) from the list so its
                           counter never fires and the step returns MK_ERR_DEP_TIMEOUT;
@@ -153,7 +157,9 @@ int mk_plan_update(mk_plan* plan, int batch, const int* seq_lens, const int* pag
 int mk_plan_sync(mk_plan* plan, mk_stream stream);
 
 /* Copy a per-step intermediate of the most recent step into dst (device or
- * host memory, `bytes` long), on `stream`:
+ * host memory, `bytes` long), on `stream`.  A plan with a capacity above 8
+ * answers the per-request kinds (HIDDEN, EXPERT_IDS, GATES, ROUTER_LOGITS,
+ * SEQ_LENS) and returns MK_ERR_UNSUPPORTED for the others:
  *   MK_DBG_HIDDEN        fp32 [batch, n_layers, hidden]  x after each layer
  *   MK_DBG_EXPERT_IDS    int32 [batch, n_layers, top_k]  rank order
  *   MK_DBG_GATES         fp32 [batch, n_layers, top_k]

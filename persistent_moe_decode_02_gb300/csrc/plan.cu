@@ -289,6 +289,12 @@ void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_erro
 // ------------------------------------------------------------------ the plan
 
 struct mk_plan {
+  // A batch capacity above mk::MAX_BATCH makes a group: sub-plan i holds
+  // requests [8i, 8i + 8) and the group's calls run the sub-plans one after
+  // another on the caller's stream.  A sub-plan with no requests is idle.
+  std::vector<mk_plan*> subs;
+  std::vector<int> sub_B;
+  int group_B = 0;
   Shape s;
   int B = 0, bcap = 0, C = 0, nb = 1, split_opt = 0, drop_task = 0, trace = 0;
   int max_pages = 0, num_pages = 0, rope_npos = 0;
@@ -528,9 +534,11 @@ int mk_plan_inspect(const mk_model_dims* dims, int batch, const int* seq_lens, i
   return (int)tasks.size();
 }
 
-int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
-                   const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                   const mk_plan_opts* opts, mk_plan** out) {
+static void destroy_one(mk_plan* p);
+
+static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
+                      const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                      const mk_plan_opts* opts, mk_plan** out) {
   if (!out) return MK_ERR_INVALID;
   *out = nullptr;
   Shape s;
@@ -579,7 +587,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
 
   auto fail = [&](int code) {
     if (code == MK_ERR_CUDA && !g_last_error[0]) note_cuda(cudaGetLastError(), "mk_plan_create");
-    mk_plan_destroy(p);
+    destroy_one(p);
     return code;
   };
   g_last_error[0] = 0;
@@ -686,7 +694,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   return MK_OK;
 }
 
-int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
+static int step_one(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
   if (!p || !d_tokens || !d_next_token) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const Shape& s = p->s;
@@ -723,7 +731,7 @@ int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next
   return MK_OK;
 }
 
-int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
+static int step_host_one(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
   if (!p || !h_tokens || !h_next_token) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const size_t tb = (size_t)p->B * sizeof(int);
@@ -731,7 +739,7 @@ int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h
     if (dalloc(p, &p->d_io_logits, (size_t)p->bcap * p->s.V * sizeof(float)) != cudaSuccess) return MK_ERR_CUDA;
   }
   if (cudaMemcpyAsync(p->d_io_tok, h_tokens, tb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MK_ERR_CUDA;
-  int rc = mk_decode_step(p, p->d_io_tok, h_logits ? p->d_io_logits : nullptr, p->d_io_next, stream);
+  int rc = step_one(p, p->d_io_tok, h_logits ? p->d_io_logits : nullptr, p->d_io_next, stream);
   if (rc != MK_OK) return rc;
   if (cudaMemcpyAsync(h_next_token, p->d_io_next, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MK_ERR_CUDA;
@@ -745,8 +753,8 @@ int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h
   return p->h_status[0];
 }
 
-int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                   mk_stream stream) {
+static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                      mk_stream stream) {
   if (!p || batch < 1) return MK_ERR_INVALID;
   if (batch > p->bcap) return MK_ERR_CAPACITY;
   cudaStream_t st = (cudaStream_t)stream;
@@ -781,7 +789,7 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
   return MK_OK;
 }
 
-int mk_plan_sync(mk_plan* p, mk_stream stream) {
+static int sync_one(mk_plan* p, mk_stream stream) {
   if (!p) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaMemcpyAsync(p->h_status, p->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st);
@@ -791,7 +799,7 @@ int mk_plan_sync(mk_plan* p, mk_stream stream) {
   return p->h_status[0];
 }
 
-int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream stream) {
+static int read_debug_one(mk_plan* p, int what, void* dst, size_t bytes, mk_stream stream) {
   if (!p || !dst) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const Shape& s = p->s;
@@ -849,7 +857,7 @@ int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream 
   return MK_OK;
 }
 
-int mk_plan_info(const mk_plan* p, int* out, int n) {
+static int info_one(const mk_plan* p, int* out, int n) {
   if (!p || !out) return MK_ERR_INVALID;
   const int v[10] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
                      p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans};
@@ -857,7 +865,7 @@ int mk_plan_info(const mk_plan* p, int* out, int n) {
   return MK_OK;
 }
 
-void mk_plan_destroy(mk_plan* p) {
+static void destroy_one(mk_plan* p) {
   if (!p) return;
   for (void* v : p->allocs) cudaFree(v);
   p->allocs.clear();
@@ -865,6 +873,150 @@ void mk_plan_destroy(mk_plan* p) {
   if (p->h_status) cudaFreeHost(p->h_status);
   if (p->ev_stage) cudaEventDestroy(p->ev_stage);
   delete p;
+}
+
+// ---- the public entry points: one plan, or a group of sub-plans
+
+static void destroy_group(mk_plan* g) {
+  for (mk_plan* sp : g->subs) destroy_one(sp);
+  delete g;
+}
+
+int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
+                   const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   const mk_plan_opts* opts, mk_plan** out) {
+  if (!out) return MK_ERR_INVALID;
+  *out = nullptr;
+  mk_plan_opts o = {};
+  if (opts) o = *opts;
+  const int bcap = o.max_batch > 0 ? o.max_batch : batch;
+  if (bcap <= mk::MAX_BATCH) return create_one(dims, w, kv, batch, seq_lens, page_table, max_pages_per_seq, opts, out);
+  if (batch < 1 || batch > bcap || !seq_lens || !page_table || max_pages_per_seq < 1) return MK_ERR_INVALID;
+  mk_plan* g = new (std::nothrow) mk_plan();
+  if (!g) return MK_ERR_CUDA;
+  const int M = mk::MAX_BATCH;
+  for (int i = 0; i * M < bcap; ++i) {
+    const int n = std::max(0, std::min(M, batch - i * M));
+    mk_plan_opts so = o;
+    so.max_batch = std::min(M, bcap - i * M);
+    // an idle sub-plan is built over the group's first request and stepped
+    // only once an update gives it requests of its own
+    const int* sl = n > 0 ? seq_lens + (size_t)i * M : seq_lens;
+    const int* pt = n > 0 ? page_table + (size_t)i * M * max_pages_per_seq : page_table;
+    mk_plan* sp = nullptr;
+    const int rc = create_one(dims, w, kv, n > 0 ? n : 1, sl, pt, max_pages_per_seq, &so, &sp);
+    if (rc != MK_OK) {
+      destroy_group(g);
+      return rc;
+    }
+    g->subs.push_back(sp);
+    g->sub_B.push_back(n);
+  }
+  g->s = g->subs[0]->s;
+  g->B = g->group_B = batch;
+  g->bcap = bcap;
+  *out = g;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
+  if (!p || p->subs.empty()) return step_one(p, d_tokens, d_logits, d_next_token, stream);
+  if (!d_tokens || !d_next_token) return MK_ERR_INVALID;
+  const size_t M = mk::MAX_BATCH, V = p->s.V;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = step_one(p->subs[i], d_tokens + i * M, d_logits ? d_logits + i * M * V : nullptr,
+                            d_next_token + i * M, stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
+int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
+  if (!p || p->subs.empty()) return step_host_one(p, h_tokens, h_logits, h_next_token, stream);
+  if (!h_tokens || !h_next_token) return MK_ERR_INVALID;
+  const size_t M = mk::MAX_BATCH, V = p->s.V;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = step_host_one(p->subs[i], h_tokens + i * M, h_logits ? h_logits + i * M * V : nullptr,
+                                 h_next_token + i * M, stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
+int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   mk_stream stream) {
+  if (!p || p->subs.empty()) return update_one(p, batch, seq_lens, page_table, max_pages_per_seq, stream);
+  if (batch < 1 || !seq_lens || !page_table || max_pages_per_seq < 1) return MK_ERR_INVALID;
+  if (batch > p->bcap) return MK_ERR_CAPACITY;
+  const int M = mk::MAX_BATCH;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    const int n = std::max(0, std::min(M, batch - (int)i * M));
+    if (n > 0) {
+      const int rc = update_one(p->subs[i], n, seq_lens + i * M, page_table + i * M * max_pages_per_seq,
+                                max_pages_per_seq, stream);
+      if (rc != MK_OK) return rc;
+    }
+    p->sub_B[i] = n;
+  }
+  p->B = p->group_B = batch;
+  return MK_OK;
+}
+
+int mk_plan_sync(mk_plan* p, mk_stream stream) {
+  if (!p || p->subs.empty()) return sync_one(p, stream);
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = sync_one(p->subs[i], stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
+int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream stream) {
+  if (!p || p->subs.empty()) return read_debug_one(p, what, dst, bytes, stream);
+  if (!dst) return MK_ERR_INVALID;
+  const size_t L = p->s.L;
+  size_t per = 0;   // bytes per request
+  switch (what) {
+    case MK_DBG_HIDDEN: per = L * p->s.H * 4; break;
+    case MK_DBG_EXPERT_IDS: case MK_DBG_GATES: per = L * p->s.k * 4; break;
+    case MK_DBG_ROUTER_LOGITS: per = L * p->s.E * 4; break;
+    case MK_DBG_SEQ_LENS: per = 4; break;
+    default: return MK_ERR_UNSUPPORTED;   // per-plan records: read them from a plan of at most 8 requests
+  }
+  if (bytes < (size_t)p->group_B * per) return MK_ERR_INVALID;
+  const size_t M = mk::MAX_BATCH;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = read_debug_one(p->subs[i], what, (uint8_t*)dst + i * M * per, (size_t)p->sub_B[i] * per, stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
+int mk_plan_info(const mk_plan* p, int* out, int n) {
+  if (!p || p->subs.empty()) return info_one(p, out, n);
+  if (!out) return MK_ERR_INVALID;
+  int v[10] = {0};
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    int w[10];
+    info_one(p->subs[i], w, 10);
+    if (i == 0)
+      for (int j = 0; j < 10; ++j) v[j] = w[j];
+    else
+      for (int j : {1, 6, 7, 8, 9}) v[j] += w[j];   // tasks, attention / expert / LM tiles, replans
+  }
+  v[5] = p->group_B;
+  for (int i = 0; i < n && i < 10; ++i) out[i] = v[i];
+  return MK_OK;
+}
+
+void mk_plan_destroy(mk_plan* p) {
+  if (!p) return;
+  if (p->subs.empty()) destroy_one(p);
+  else destroy_group(p);
 }
 
 }  // extern "C"

@@ -47,18 +47,20 @@ class GpuRun:
     """A workload's model, paged cache and plan on cuda:0."""
 
     def __init__(self, wl: synth.Workload, steps: Optional[int] = None, model: Optional[DeviceModel] = None,
-                 rids: Optional[List[int]] = None, perm_salt: int = 0, poison: bool = False, **plan_kw):
+                 rids: Optional[List[int]] = None, perm_salt: int = 0, poison: bool = False,
+                 extra_requests: int = 0, extra_ctx: int = 0, **plan_kw):
         from persistent_moe_decode_02_gb300 import mk
         D = wl.dims
         self.wl, self.D = wl, D
         self.steps = wl.steps if steps is None else steps
         self.model = model if model is not None else DeviceModel(D, wl.seed)
         ps = D.page_size
-        max_pages = max((c + self.steps + 1 + ps - 1) // ps for c in wl.ctx) + 1
-        num_pages = kv_pages_needed(D, wl.ctx, self.steps) + 4
+        max_pages = max((c + self.steps + 1 + ps - 1) // ps for c in wl.ctx + [extra_ctx]) + 1
+        num_pages = kv_pages_needed(D, wl.ctx, self.steps, extra_requests, extra_ctx) + 4
         self.kv = PagedKV(D, num_pages, max_pages, wl.seed, perm_salt=perm_salt, poison=poison)
         rids = list(range(wl.batch)) if rids is None else rids
         self.reqs = [self.kv.admit(rid, c, self.steps + 1) for rid, c in zip(rids, wl.ctx)]
+        self.next_rid = max(rids) + 1
         self.max_pages = max_pages
         self.plan = mk.Plan(D, self.model.weights(), self.kv.k, self.kv.v, [r.length for r in self.reqs],
                             self.kv.page_table(self.reqs), max_pages, **plan_kw)
@@ -90,6 +92,22 @@ class GpuRun:
             r.length += 1
         self.tokens = nxt
         return rec
+
+    def churn(self, leave: int, join: int, join_ctx: int) -> list:
+        """Continuous batching: the `leave` oldest requests finish, `join` new
+        ones (fresh request ids) join at `join_ctx` cached tokens, and the plan
+        is updated.  Returns the new requests."""
+        for r in self.reqs[:leave]:
+            self.kv.release(r)
+        keep_tok = self.tokens[leave:]
+        self.reqs = self.reqs[leave:]
+        new = [self.kv.admit(self.next_rid + i, join_ctx, self.steps + 1) for i in range(join)]
+        self.next_rid += join
+        self.reqs += new
+        new_tok = torch.tensor(initial_tokens(self.wl, [r.rid for r in new]), dtype=torch.int32, device="cuda")
+        self.tokens = torch.cat([keep_tok, new_tok])
+        self.plan.update([r.length for r in self.reqs], self.kv.page_table(self.reqs), self.max_pages)
+        return new
 
 
 @dataclass
@@ -195,5 +213,30 @@ def run_and_check(wl: synth.Workload, steps: int, oracle_steps: Optional[int] = 
         rr = OracleReplay(wl, run.reqs[b].rid, wl.ctx[b], W=W, cache_prior=cache_prior, n_layers=n_layers)
         for s in range(oracle_steps):
             rr.step(recs[s], b, rep)
+    run.plan.close()
+    return rep
+
+
+def run_churn_and_check(wl: synth.Workload, capacity: int, steps: int, leave: int, join: int, join_ctx: int,
+                        sample: Optional[List[int]] = None, n_layers: Optional[int] = None,
+                        cache_prior: bool = True, **plan_kw) -> Report:
+    """Run `steps` GPU steps with `leave` requests finishing and `join` joining
+    after each step (batch capacity `capacity`), then replay every request
+    (or the request ids in `sample`) in the oracle over the steps it took part in."""
+    run = GpuRun(wl, steps=steps, max_batch=capacity, extra_requests=join * steps, extra_ctx=join_ctx, **plan_kw)
+    prior = {r.rid: r.prior_len for r in run.reqs}
+    recs = []
+    for s in range(steps):
+        recs.append(run.step())
+        if s + 1 < steps:
+            for r in run.churn(leave, join, join_ctx):
+                prior[r.rid] = join_ctx
+    rep = Report()
+    W = synth.SynthWeights(wl.dims, wl.seed)
+    for rid in (sorted(prior) if sample is None else sample):
+        rr = OracleReplay(wl, rid, prior[rid], W=W, cache_prior=cache_prior, n_layers=n_layers)
+        for rec in recs:
+            if rid in rec.rids:
+                rr.step(rec, rec.rids.index(rid), rep)
     run.plan.close()
     return rep

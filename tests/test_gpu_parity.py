@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import synth
-from tests.gpu_util import GpuRun, Report, run_and_check, rel_l2
+from tests.gpu_util import GpuRun, Report, rel_l2, run_and_check, run_churn_and_check
 
 pytestmark = pytest.mark.gpu
 
@@ -135,11 +135,31 @@ def test_full_b1_256k_first_layers():
 
 
 @pytest.mark.slow
+def test_full_b32_churn_sampled_requests():
+    # batch 32, contexts log-uniform in [512, 32768], 2 finish / 2 join at 512 per step
+    wl = synth.workload("full_b32_churn")
+    rep = run_churn_and_check(wl, capacity=32, steps=2, leave=wl.churn_leave, join=wl.churn_leave,
+                              join_ctx=wl.churn_join_ctx, sample=[2, 17, 31, 32], n_layers=2, cache_prior=False)
+    print(rep)
+    rep.assert_ok()
+
+
+@pytest.mark.slow
 def test_full_b8_long_sampled_requests():
     wl = synth.workload("full_b8_long")
     rep = run_and_check(wl, steps=1, requests=[0, 2], n_layers=2, cache_prior=False)
     print(rep)
     rep.assert_ok()
+
+
+def test_tiny_batch_12_churn_over_two_sub_plans():
+    # a batch capacity above 8 runs as sub-plans of up to 8 requests; two leave
+    # and two join after every step, so requests move between sub-plans
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 37, 95, 5, 300, 16, 64, 200, 77, 0, 21], steps=3)
+    rep = run_churn_and_check(wl, capacity=12, steps=3, leave=2, join=2, join_ctx=20)
+    print(rep)
+    rep.assert_ok()
+    assert rep.steps >= 30
 
 
 def test_stage_timeline_is_ordered():
