@@ -249,9 +249,11 @@ def our_arm(args, wl):
         t = torch.tensor([elapsed_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t)
-    union = torch.zeros(D.n_layers, dtype=torch.int32)
-    plan.read_debug(mk.MK_DBG_UNION, union)
+    # distinct experts per layer over the whole batch (the experts a step must read)
+    ids = torch.zeros(B, D.n_layers, D.top_k, dtype=torch.int32)
+    plan.read_debug(mk.MK_DBG_EXPERT_IDS, ids)
     plan.sync()
+    union = torch.tensor([len(set(ids[:, l, :].flatten().tolist())) for l in range(D.n_layers)])
     nbytes = 0
     for s in range(args.steps):
         nbytes += step_bytes(D, [c + s for c in ctx_at_start], union_per_layer=union.tolist())["total"]

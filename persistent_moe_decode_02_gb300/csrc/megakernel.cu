@@ -1326,7 +1326,8 @@ struct Consumer {
     if (st) {
       const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
       const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
-      unsigned long long* out = p.rlsum + (size_t)t.layer * p.bcap * E;
+      // copy t % RL_COPIES of the sums: eight times fewer tiles contend for each address
+      unsigned long long* out = p.rlsum + ((size_t)t.layer * RL_COPIES + t.a[2] % RL_COPIES) * p.bcap * E;
       // two neighbouring threads per (b, e), each half the rows, then one shuffle
       const int n2 = 2 * p.B * E, hr = (nr + 1) >> 1;
       for (int x0 = 0; x0 < n2; x0 += NCT) {
@@ -1493,8 +1494,20 @@ struct Consumer {
   // right after, so both arrive in one round trip.
   __device__ void moe_act(int l) {
     const int H = p.H, H4 = H >> 2, E = p.E, BE = p.B * E;
-    const unsigned long long* rs = p.rlsum + (size_t)l * p.bcap * E;
-    const unsigned long long q0 = ct < BE ? __ldcg(rs + ct) : 0ull;
+    const size_t cs = (size_t)p.bcap * E;   // one copy of the sums
+    const unsigned long long* rs = p.rlsum + (size_t)l * RL_COPIES * cs;
+    auto load_sum = [&](int i) {   // the copies' integer sum: exact in any order
+      unsigned long long v[RL_COPIES];
+#pragma unroll
+      for (int c = 0; c < RL_COPIES; ++c) v[c] = __ldcg(rs + c * cs + i);
+      unsigned long long q = 0;
+#pragma unroll
+      for (int c = 0; c < RL_COPIES; ++c) q += v[c];
+      return q;
+    };
+    unsigned long long v0[RL_COPIES];   // this thread's first sum: its loads go out now, the adds come later
+#pragma unroll
+    for (int c = 0; c < RL_COPIES; ++c) v0[c] = ct < BE ? __ldcg(rs + c * cs + ct) : 0ull;
     const float* xm = p.x_mid + (size_t)l * p.bcap * H;
     const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1531,8 +1544,11 @@ struct Consumer {
       m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
     }
     cbar();
+    unsigned long long q0 = 0;
+#pragma unroll
+    for (int c = 0; c < RL_COPIES; ++c) q0 += v0[c];
     for (int i = ct; i < BE; i += NCT) {
-      const float v = from_fixed(i == ct ? q0 : __ldcg(rs + i)) * m->inv[i / E];
+      const float v = from_fixed(i == ct ? q0 : load_sum(i)) * m->inv[i / E];
       m->rl[i] = v == v ? v : -INFINITY;
     }
   }
@@ -1669,7 +1685,7 @@ struct Consumer {
     mark(TR_ACT);
     const float* xm = p.x_mid + (size_t)l * p.bcap * H;
     if (!ab) {   // every expert tile of the layer has read the router sums: zero this task's share
-      const long long n = (long long)p.bcap * p.E;
+      const long long n = (long long)RL_COPIES * p.bcap * p.E;
       unsigned long long* rs = p.rlsum + (size_t)l * n;
       for (long long i = r0 * n / H + ct; i < (long long)t.a[1] * n / H; i += NCT) rs[i] = 0ull;
     }

@@ -18,6 +18,7 @@ constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
 // rows per cross-warp partial-sum window of the wide GEMV: 64 at batch <= 2 (a
 // projection tile's rows in one window: one flush), else 32 (shared memory)
 constexpr int win_rows(int nb) { return nb <= 2 ? 64 : 32; }
+constexpr int RL_COPIES = 8;               // copies of the router-logit sums (O tile i adds to copy i % 8)
 constexpr int TRACE_SLOTS = 12;            // stamps per task in the optional timeline
 constexpr int STRACE_CAP = 4096;           // ring stages per CTA in the optional stage timeline
 constexpr int STRACE_SLOTS = 6;            // per stage: copy issued, landed, released, task,
@@ -138,7 +139,7 @@ struct Params {
   float* gates;         // [L][bcap][k]
   int* route;           // [L][rm.ints]
   float* moe_part;      // [expert tiles][bcap][H] gated partial outputs (reused by every layer)
-  unsigned long long* rlsum;   // [L][bcap][E] router-logit sums in 32.32 fixed point: the O tiles
+  unsigned long long* rlsum;   // [L][RL_COPIES][bcap][E] router-logit sums in 32.32 fixed point: the O tiles
                                // add their shares (integer adds: exact, any order), the expert
                                // tiles read them, the layer's reduce tasks zero them for the next
                                // step (and every replan zeroes all)

@@ -322,7 +322,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_gt = dc.take(L * B * s.k * sizeof(float));
   const size_t d_route = dc.take(L * rm.ints * sizeof(int));
   const size_t d_mp = dc.take((size_t)cnt.gu * B * s.H * sizeof(float));
-  const size_t d_rp = dc.take(L * B * s.E * sizeof(unsigned long long));
+  const size_t d_rp = dc.take(L * mk::RL_COPIES * B * s.E * sizeof(unsigned long long));
   const size_t d_lmv = dc.take((size_t)B * cnt.lm * sizeof(float));
   const size_t d_lmi = dc.take((size_t)B * cnt.lm * sizeof(int));
   if (dc.off > kScratchBytes) {
@@ -375,7 +375,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(counters)");
   e = cudaMemsetAsync(base + d_route, 0, L * rm.ints * sizeof(int), st);
   if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(routing)");
-  e = cudaMemsetAsync(base + d_rp, 0, L * B * s.E * sizeof(unsigned long long), st);
+  e = cudaMemsetAsync(base + d_rp, 0, L * mk::RL_COPIES * B * s.E * sizeof(unsigned long long), st);
   if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(router sums)");
   e = mk::launch_rope_table((float2*)(base + d_rope), npos, s.d, (double)dims->rope_theta, st);
   if (e != cudaSuccess) return fail_cuda(e, "RoPE table launch");

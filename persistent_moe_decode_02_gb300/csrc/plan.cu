@@ -452,7 +452,7 @@ int replan(mk_plan* p, cudaStream_t st) {
   p->d_cta = (int*)((uint8_t*)p->d_tasks + tasks.size() * sizeof(Task));
   if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) != cudaSuccess)
     return MK_ERR_CUDA;
-  if (cudaMemsetAsync(p->P.rlsum, 0, (size_t)p->s.L * p->bcap * p->s.E * sizeof(unsigned long long), st) !=
+  if (cudaMemsetAsync(p->P.rlsum, 0, (size_t)p->s.L * mk::RL_COPIES * p->bcap * p->s.E * sizeof(unsigned long long), st) !=
       cudaSuccess)
     return MK_ERR_CUDA;
   p->epoch = 0;
@@ -665,7 +665,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   // expert-tile partials, sized for the most tiles any batch up to the capacity needs
   const int moe_max = mk::moe_tiles(std::min(s.E, bcap * s.k), s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   ok &= dalloc(p, &P.moe_part, (size_t)moe_max * bcap * s.H * sizeof(float)) == cudaSuccess;
-  ok &= dalloc(p, &P.rlsum, L * bcap * s.E * sizeof(unsigned long long)) == cudaSuccess;
+  ok &= dalloc(p, &P.rlsum, L * mk::RL_COPIES * bcap * s.E * sizeof(unsigned long long)) == cudaSuccess;
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
   ok &= dalloc(p, &P.lm_idx, (size_t)bcap * lm_tiles * sizeof(int)) == cudaSuccess;
