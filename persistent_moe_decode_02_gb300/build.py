@@ -38,7 +38,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(lg)
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.run(["nvcc", "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp,
-                    "-lcudart"], check=True)
+                    "-lcudart", "-lpthread"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

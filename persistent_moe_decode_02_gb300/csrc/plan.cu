@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "mk.h"
@@ -64,25 +65,51 @@ struct Counts {
 
 // Phase-balanced assignment: tasks of one phase go, largest first, to the CTA
 // with the least work in this phase (ties: least work so far, then lowest id).
+// The CTAs sit in a binary min-heap ordered by exactly that key; a task only
+// raises the root's key, so one sift-down per task: O(n log C) per phase.
 struct Assigner {
+  struct Key {
+    double ph, tot;
+    int c;
+  };
+  static bool before(const Key& a, const Key& b) {   // a is the better choice than b
+    if (a.ph != b.ph) return a.ph < b.ph;
+    if (a.tot != b.tot) return a.tot < b.tot;
+    return a.c < b.c;
+  }
   int C;
   std::vector<std::vector<Task>> per_cta;
   std::vector<double> total;
+  std::vector<Key> heap;
   explicit Assigner(int c) : C(c), per_cta(c), total(c, 0.0) {}
+  void sift_down(size_t i) {
+    const size_t n = heap.size();
+    const Key k = heap[i];
+    for (;;) {
+      size_t ch = 2 * i + 1;
+      if (ch >= n) break;
+      if (ch + 1 < n && before(heap[ch + 1], heap[ch])) ++ch;
+      if (!before(heap[ch], k)) break;
+      heap[i] = heap[ch];
+      i = ch;
+    }
+    heap[i] = k;
+  }
   void phase(std::vector<std::pair<double, Task>>& ts) {
     std::stable_sort(ts.begin(), ts.end(),
                      [](const std::pair<double, Task>& a, const std::pair<double, Task>& b) {
                        return a.first > b.first;
                      });
-    std::vector<double> ph(C, 0.0);
+    heap.resize(C);
+    for (int c = 0; c < C; ++c) heap[c] = {0.0, total[c], c};
+    for (size_t i = heap.size() / 2; i-- > 0;) sift_down(i);
     for (auto& t : ts) {
-      int best = 0;
-      for (int c = 1; c < C; ++c) {
-        if (ph[c] < ph[best] || (ph[c] == ph[best] && total[c] < total[best])) best = c;
-      }
-      ph[best] += t.first;
-      total[best] += t.first;
-      per_cta[best].push_back(t.second);
+      Key& k = heap[0];
+      k.ph += t.first;
+      total[k.c] += t.first;
+      k.tot = total[k.c];
+      per_cta[k.c].push_back(t.second);
+      sift_down(0);
     }
   }
 };
@@ -167,6 +194,11 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   cnt.heads_per_comb = comb_heads(s.G, B * s.nkv, C);
   cnt.comb = B * s.nkv * (s.G / cnt.heads_per_comb);
   const double PB = 2.0 * s.ps * s.d * 2;
+  {   // room for every CTA's share up front (the lists grow by one task at a time)
+    const long long per_layer = (long long)cnt.qkv_per_g * s.nkv + cnt.attn + cnt.comb + cnt.o + cnt.gu + cnt.down;
+    const long long est = (per_layer * s.L + cnt.lm) / C + 2 * s.L + 8;
+    for (auto& v : asg.per_cta) v.reserve((size_t)est);
+  }
 
   for (int l = 0; l < s.L; ++l) {
     std::vector<std::pair<double, Task>> ph;
@@ -271,6 +303,9 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   asg.phase(ph);
 
   out.clear();
+  size_t ntot = 0;
+  for (int c = 0; c < C; ++c) ntot += asg.per_cta[c].size();
+  out.reserve(ntot);
   cta_start.assign(C + 1, 0);
   for (int c = 0; c < C; ++c) {
     cta_start[c] = (int)out.size();
@@ -329,9 +364,12 @@ struct mk_plan {
   int* d_io_next = nullptr;
   float* d_io_logits = nullptr;
   // pinned staging for uploads, protected by an event
-  void* h_stage = nullptr;
-  size_t h_stage_cap = 0;
-  cudaEvent_t ev_stage = nullptr;
+  // two pinned staging buffers used in turn: an upload waits only for the one
+  // two updates back, never for the step in flight
+  void* h_stage[2] = {nullptr, nullptr};
+  size_t h_stage_cap[2] = {0, 0};
+  cudaEvent_t ev_stage[2] = {nullptr, nullptr};
+  int stage_i = 0;
   int* h_status = nullptr;
 };
 
@@ -375,43 +413,78 @@ int validate_batch(const Shape& s, int B, const int* seq_lens, const int* page_t
 }
 
 // Stage the bytes in pinned memory and enqueue the copy to `dst` on `st`.
-cudaError_t upload(mk_plan* p, void* dst, const void* src, size_t bytes, cudaStream_t st) {
-  if (bytes == 0) return cudaSuccess;
+// Host -> device copies of one update, through the next pinned staging buffer
+// (each piece at a 16-byte aligned offset).
+struct Up {
+  void* dst;
+  const void* src;
+  size_t bytes;
+};
+cudaError_t upload_many(mk_plan* p, cudaStream_t st, const Up* u, int n) {
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += (u[i].bytes + 15) / 16 * 16;
+  if (total == 0) return cudaSuccess;
+  const int k = p->stage_i ^ 1;
   cudaError_t e;
-  if (p->ev_stage) {
-    e = cudaEventSynchronize(p->ev_stage);  // previous upload no longer reads the staging buffer
+  if (p->ev_stage[k]) {
+    e = cudaEventSynchronize(p->ev_stage[k]);   // the update two back no longer reads this buffer
     if (e != cudaSuccess) return e;
   }
-  if (bytes > p->h_stage_cap) {
-    if (p->h_stage) cudaFreeHost(p->h_stage);
-    p->h_stage = nullptr;
-    e = cudaMallocHost(&p->h_stage, bytes);
+  if (total > p->h_stage_cap[k]) {
+    if (p->h_stage[k]) cudaFreeHost(p->h_stage[k]);
+    p->h_stage[k] = nullptr;
+    p->h_stage_cap[k] = 0;
+    e = cudaMallocHost(&p->h_stage[k], total + total / 2);
     if (e != cudaSuccess) return e;
-    p->h_stage_cap = bytes;
+    p->h_stage_cap[k] = total + total / 2;
   }
-  memcpy(p->h_stage, src, bytes);
-  e = cudaMemcpyAsync(dst, p->h_stage, bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return e;
-  return cudaEventRecord(p->ev_stage, st);
+  uint8_t* h = (uint8_t*)p->h_stage[k];
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    if (u[i].bytes == 0) continue;
+    memcpy(h + off, u[i].src, u[i].bytes);
+    e = cudaMemcpyAsync(u[i].dst, h + off, u[i].bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+    off += (u[i].bytes + 15) / 16 * 16;
+  }
+  p->stage_i = k;
+  return cudaEventRecord(p->ev_stage[k], st);
 }
 
-// Rebuild tasks for the plan's current lengths, upload them, reset counters.
-int replan(mk_plan* p, cudaStream_t st) {
+cudaError_t upload(mk_plan* p, void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  const Up u = {dst, src, bytes};
+  return upload_many(p, st, &u, 1);
+}
+
+// A replan in two halves.  build_for is host work only (the task list for the
+// plan's current lengths), so a group builds its sub-plans' lists on parallel
+// threads.  commit_built grows device buffers if needed, uploads the list (with
+// the lengths and page table when with_batch), and resets the counters.
+struct Built {
   std::vector<Task> tasks;
-  std::vector<int> cs;
+  std::vector<int> cs, open;
   Counts cnt;
-  std::vector<int> open;
-  int rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, tasks, cs, cnt, open);
-  if (rc != MK_OK) return rc;
-  if (p->drop_task > 0 && p->drop_task - 1 < (int)tasks.size()) {
+  int rc = MK_OK;
+};
+
+void build_for(const mk_plan* p, Built& b) {
+  b.rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open);
+  if (b.rc != MK_OK) return;
+  if (p->drop_task > 0 && p->drop_task - 1 < (int)b.tasks.size()) {
     const int victim = p->drop_task - 1;
-    tasks.erase(tasks.begin() + victim);
+    b.tasks.erase(b.tasks.begin() + victim);
     for (int c = 0; c <= p->C; ++c)
-      if (cs[c] > victim) cs[c]--;
+      if (b.cs[c] > victim) b.cs[c]--;
   }
+}
+
+int commit_built(mk_plan* p, Built& b, cudaStream_t st, bool with_batch) {
+  if (b.rc != MK_OK) return b.rc;
+  std::vector<Task>& tasks = b.tasks;
+  std::vector<int>& cs = b.cs;
   cudaError_t e;
   // one device blob: tasks, then the C + 1 CTA offsets (48-byte tasks keep it 16-byte aligned)
-  const size_t blob_bytes = tasks.size() * sizeof(Task) + cs.size() * sizeof(int);
+  const size_t tbytes = tasks.size() * sizeof(Task), blob_bytes = tbytes + cs.size() * sizeof(int);
   if (blob_bytes > p->tasks_cap) {
     if (p->d_tasks) {
       if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
@@ -433,23 +506,28 @@ int replan(mk_plan* p, cudaStream_t st) {
       return MK_ERR_CUDA;
     p->trace_cap = cap;
   }
-  if ((size_t)cnt.part_slots > p->part_cap_slots) {
+  if ((size_t)b.cnt.part_slots > p->part_cap_slots) {
     // grow the attention partial buffer (rare: only when a replan adds chunks)
     if (p->d_part) {
       if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
       dfree(p, p->d_part);
       p->d_part = nullptr;
     }
-    size_t cap = (size_t)cnt.part_slots * 2 + 16;
+    size_t cap = (size_t)b.cnt.part_slots * 2 + 16;
     if (dalloc(p, &p->d_part, (size_t)p->s.L * cap * p->s.G * (p->s.d + 4) * sizeof(float)) != cudaSuccess)
       return MK_ERR_CUDA;
     p->part_cap_slots = cap;
   }
-  std::vector<uint8_t> blob(blob_bytes);
-  memcpy(blob.data(), tasks.data(), tasks.size() * sizeof(Task));
-  memcpy(blob.data() + tasks.size() * sizeof(Task), cs.data(), cs.size() * sizeof(int));
-  if (upload(p, p->d_tasks, blob.data(), blob_bytes, st) != cudaSuccess) return MK_ERR_CUDA;
-  p->d_cta = (int*)((uint8_t*)p->d_tasks + tasks.size() * sizeof(Task));
+  Up ups[4];
+  int nu = 0;
+  ups[nu++] = {p->d_tasks, tasks.data(), tbytes};
+  ups[nu++] = {(uint8_t*)p->d_tasks + tbytes, cs.data(), cs.size() * sizeof(int)};
+  if (with_batch) {
+    ups[nu++] = {p->d_seq, p->seq.data(), (size_t)p->B * sizeof(int)};
+    ups[nu++] = {p->d_pt, p->pt.data(), p->pt.size() * sizeof(int)};
+  }
+  if (upload_many(p, st, ups, nu) != cudaSuccess) return MK_ERR_CUDA;
+  p->d_cta = (int*)((uint8_t*)p->d_tasks + tbytes);
   if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) != cudaSuccess)
     return MK_ERR_CUDA;
   if (cudaMemsetAsync(p->P.rlsum, 0, (size_t)p->s.L * mk::RL_COPIES * p->bcap * p->s.E * sizeof(unsigned long long), st) !=
@@ -458,10 +536,17 @@ int replan(mk_plan* p, cudaStream_t st) {
   p->epoch = 0;
   p->tasks.swap(tasks);
   p->cta_start.swap(cs);
-  p->cnt = cnt;
-  p->open_start.swap(open);
+  p->cnt = b.cnt;
+  p->open_start.swap(b.open);
   p->replans++;
   return MK_OK;
+}
+
+// Rebuild tasks for the plan's current lengths, upload them, reset counters.
+int replan(mk_plan* p, cudaStream_t st) {
+  Built b;
+  build_for(p, b);
+  return commit_built(p, b, st, false);
 }
 
 bool needs_replan(const mk_plan* p) {
@@ -677,16 +762,19 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->rope_npos = max_pages_per_seq * s.ps;
   ok &= dalloc(p, &p->d_rope, (size_t)p->rope_npos * (s.d / 2) * sizeof(float2)) == cudaSuccess;
   if (!ok) return fail(MK_ERR_CUDA);
-  if (cudaEventCreateWithFlags(&p->ev_stage, cudaEventDisableTiming) != cudaSuccess) return fail(MK_ERR_CUDA);
+  for (int k = 0; k < 2; ++k)
+    if (cudaEventCreateWithFlags(&p->ev_stage[k], cudaEventDisableTiming) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMallocHost(&p->h_status, 4 * sizeof(int)) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMemsetAsync(P.route, 0, L * p->rm.ints * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (mk::launch_rope_table(p->d_rope, p->rope_npos, s.d, (double)s.theta, st) != cudaSuccess)
     return fail(MK_ERR_CUDA);
-  if (upload(p, p->d_seq, p->seq.data(), (size_t)batch * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
-  if (upload(p, p->d_pt, p->pt.data(), p->pt.size() * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
-  rc = replan(p, st);
-  if (rc != MK_OK) return fail(rc);
+  {
+    Built b;
+    build_for(p, b);
+    rc = commit_built(p, b, st, true);
+    if (rc != MK_OK) return fail(rc);
+  }
   p->replans = 0;
   if (cudaStreamSynchronize(st) != cudaSuccess) return fail(MK_ERR_CUDA);
   fill_params(p);
@@ -753,11 +841,12 @@ static int step_host_one(mk_plan* p, const int* h_tokens, float* h_logits, int* 
   return p->h_status[0];
 }
 
-static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                      mk_stream stream) {
+// The first half of an update: checks, device capacity, and the new batch on
+// the host side of the plan.
+static int update_prepare(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                          cudaStream_t st) {
   if (!p || batch < 1) return MK_ERR_INVALID;
   if (batch > p->bcap) return MK_ERR_CAPACITY;
-  cudaStream_t st = (cudaStream_t)stream;
   int rc = validate_batch(p->s, batch, seq_lens, page_table, max_pages_per_seq, p->num_pages);
   if (rc != MK_OK) return rc;
   if ((size_t)p->bcap * max_pages_per_seq > p->pt_cap || max_pages_per_seq * p->s.ps > p->rope_npos) {
@@ -780,13 +869,26 @@ static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* pag
   p->max_pages = max_pages_per_seq;
   p->seq.assign(seq_lens, seq_lens + batch);
   p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
-  if (upload(p, p->d_seq, p->seq.data(), (size_t)batch * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
-  if (upload(p, p->d_pt, p->pt.data(), p->pt.size() * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
-  if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
-  rc = replan(p, st);
+  return MK_OK;
+}
+
+// The last half: upload the built list with the batch, clear the status word.
+static int update_commit(mk_plan* p, Built& b, cudaStream_t st) {
+  int rc = commit_built(p, b, st, true);
   if (rc != MK_OK) return rc;
+  if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return MK_ERR_CUDA;
   fill_params(p);
   return MK_OK;
+}
+
+static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                      mk_stream stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  int rc = update_prepare(p, batch, seq_lens, page_table, max_pages_per_seq, st);
+  if (rc != MK_OK) return rc;
+  Built b;
+  build_for(p, b);
+  return update_commit(p, b, st);
 }
 
 static int sync_one(mk_plan* p, mk_stream stream) {
@@ -869,9 +971,11 @@ static void destroy_one(mk_plan* p) {
   if (!p) return;
   for (void* v : p->allocs) cudaFree(v);
   p->allocs.clear();
-  if (p->h_stage) cudaFreeHost(p->h_stage);
+  for (int k = 0; k < 2; ++k) {
+    if (p->h_stage[k]) cudaFreeHost(p->h_stage[k]);
+    if (p->ev_stage[k]) cudaEventDestroy(p->ev_stage[k]);
+  }
   if (p->h_status) cudaFreeHost(p->h_status);
-  if (p->ev_stage) cudaEventDestroy(p->ev_stage);
   delete p;
 }
 
@@ -950,15 +1054,29 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
   if (!p || p->subs.empty()) return update_one(p, batch, seq_lens, page_table, max_pages_per_seq, stream);
   if (batch < 1 || !seq_lens || !page_table || max_pages_per_seq < 1) return MK_ERR_INVALID;
   if (batch > p->bcap) return MK_ERR_CAPACITY;
+  cudaStream_t st = (cudaStream_t)stream;
   const int M = mk::MAX_BATCH;
-  for (size_t i = 0; i < p->subs.size(); ++i) {
-    const int n = std::max(0, std::min(M, batch - (int)i * M));
-    if (n > 0) {
-      const int rc = update_one(p->subs[i], n, seq_lens + i * M, page_table + i * M * max_pages_per_seq,
-                                max_pages_per_seq, stream);
+  const size_t n = p->subs.size();
+  std::vector<int> nb(n);
+  for (size_t i = 0; i < n; ++i) {
+    nb[i] = std::max(0, std::min(M, batch - (int)i * M));
+    if (nb[i] == 0) continue;
+    const int rc = update_prepare(p->subs[i], nb[i], seq_lens + i * M, page_table + i * M * max_pages_per_seq,
+                                  max_pages_per_seq, st);
+    if (rc != MK_OK) return rc;
+  }
+  // the task lists are host work: one thread per sub-plan that holds requests
+  std::vector<Built> built(n);
+  std::vector<std::thread> th;
+  for (size_t i = 0; i < n; ++i)
+    if (nb[i] > 0) th.emplace_back([&, i] { build_for(p->subs[i], built[i]); });
+  for (auto& t : th) t.join();
+  for (size_t i = 0; i < n; ++i) {
+    if (nb[i] > 0) {
+      const int rc = update_commit(p->subs[i], built[i], st);
       if (rc != MK_OK) return rc;
     }
-    p->sub_B[i] = n;
+    p->sub_B[i] = nb[i];
   }
   p->B = p->group_B = batch;
   return MK_OK;

@@ -9,6 +9,7 @@ import ctypes
 import os
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -210,8 +211,11 @@ class Plan:
         return lib().mk_decode_step_host(self.h, tp, lp, np_, _stream(stream))
 
     def update(self, seq_lens: Sequence[int], page_table, max_pages: int, stream=None) -> None:
-        pt = [int(x) for x in page_table]
-        rc = lib().mk_plan_update(self.h, len(seq_lens), _int_array(seq_lens), _int_array(pt), max_pages,
+        # int32 host arrays handed over by pointer (a numpy array or CPU tensor is not copied)
+        sl = np.ascontiguousarray(np.asarray(seq_lens), dtype=np.int32)
+        pt = np.ascontiguousarray(np.asarray(page_table), dtype=np.int32)
+        p_int = ctypes.POINTER(ctypes.c_int)
+        rc = lib().mk_plan_update(self.h, len(sl), sl.ctypes.data_as(p_int), pt.ctypes.data_as(p_int), max_pages,
                                   _stream(stream))
         if rc != MK_OK:
             raise MkError("mk_plan_update", rc)
