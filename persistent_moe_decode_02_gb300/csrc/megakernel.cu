@@ -396,7 +396,7 @@ struct Geo {
   // row tasks
   const uint16_t* W;
   const uint16_t* W2;   // expert tile: the layer's down matrix (W: its gate/up matrix)
-  int K, r0, r1, rps;
+  int K, r0, r1, rps, halves;
   // attention
   int pg0, pg1, ppg, b, g;
   uint32_t PB;
@@ -414,7 +414,9 @@ struct Geo {
 // bulk copies, paced by the consumers' releases: a task's weights are in
 // flight as soon as ring slots free up, long before its activations exist.
 // Kept small: the SM's instruction cache is shared with the consumer warps.
+template <int NB>
 struct Producer {
+  static constexpr bool kSplit = NB > 2;   // the O projection may run in K halves only above batch 2
   const Params& p;
   Ring r;
   uint64_t pol;
@@ -492,11 +494,13 @@ struct Producer {
     switch (t.type) {
       case T_QKV: case T_OPROJ: case T_LM: {
         q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : p.lm_head;
-        q.K = t.type == T_OPROJ ? p.nq * p.d : p.H;
+        // the O projection's K halves (o_halves = 2) stream one after the other
+        q.halves = kSplit && t.type == T_OPROJ ? p.o_halves : 1;
+        q.K = t.type == T_OPROJ ? p.nq * p.d / q.halves : p.H;
         q.r0 = t.a[0];
         q.r1 = t.a[1];
         q.rps = rows_per_stage(p, q.K);
-        q.nst = (q.r1 - q.r0 + q.rps - 1) / q.rps + (t.type == T_OPROJ ? 1 : 0);   // + the router stage
+        q.nst = q.halves * ((q.r1 - q.r0 + q.rps - 1) / q.rps) + (t.type == T_OPROJ ? 1 : 0);   // + the router stage
         return true;
       }
       case T_ATTN: {
@@ -553,9 +557,17 @@ struct Producer {
           f(reinterpret_cast<const uint8_t*>(p.ffn_norm[l]) + w0, w1 - w0, (uint32_t)router_stage_gain_off(nr, p.E));
           break;
         }
-        const int s0 = q.r0 + s * q.rps;
-        const int n = min(q.rps, q.r1 - s0);
-        f(q.W + (size_t)s0 * q.K, (uint32_t)n * q.K * 2, 0u);
+        if (!kSplit || q.halves == 1) {
+          const int s0 = q.r0 + s * q.rps;
+          const int n = min(q.rps, q.r1 - s0);
+          f(q.W + (size_t)s0 * q.K, (uint32_t)n * q.K * 2, 0u);
+        } else {   // K half h of rows s0 .. s0 + n: one copy per row
+          const int per = (q.r1 - q.r0 + q.rps - 1) / q.rps, h = s / per;
+          const int s0 = q.r0 + (s - h * per) * q.rps;
+          const int n = min(q.rps, q.r1 - s0);
+          for (int i = 0; i < n; ++i)
+            f(q.W + (size_t)(s0 + i) * q.K * q.halves + (size_t)h * q.K, (uint32_t)q.K * 2, (uint32_t)i * q.K * 2);
+        }
         break;
       }
       case T_ATTN: {
@@ -1274,19 +1286,35 @@ struct Consumer {
     return ab;
   }
 
-  __device__ bool prep_oproj(const Task& t, bool ab, ProjGemv& g) {
-    const int l = t.layer, K = p.nq * p.d, r0 = t.a[0], nr = t.a[1] - r0;
+  // K half h of the O projection (h = 0 only, unless o_halves = 2): the
+  // attention output's columns of that half as the activations; the residual
+  // epilogue accumulates the halves in the scratch rows.
+  __device__ bool prep_oproj(const Task& t, bool ab, ProjGemv& g, int h) {
+    const int l = t.layer, KF = p.nq * p.d, K = NB > 2 ? KF / p.o_halves : KF, r0 = t.a[0], nr = t.a[1] - r0;
     float* xres = scr;    // residual rows of this tile, [B][nr]
+    if (h > 0) cbar();    // the previous half's GEMV is done with the activations
     if (!ab) {
       // the residual rows' loads go out first, with the attention output's
-      const bool r1st = ct < p.B * nr;
+      const bool r1st = h == 0 && ct < p.B * nr;
       const float x1st = r1st ? x_in(l, ct / nr, r0 + ct % nr) : 0.f;
-      const float4* o = reinterpret_cast<const float4*>(p.o + (size_t)l * p.bcap * K);
-      float4* dst = reinterpret_cast<float4*>(act);
+      const float* o = p.o + (size_t)l * p.bcap * KF + (size_t)h * K;
+      if (NB <= 2 || K == KF) {   // whole rows: one contiguous copy
+        const float4* o4 = reinterpret_cast<const float4*>(o);
+        float4* dst = reinterpret_cast<float4*>(act);
 #pragma unroll 4
-      for (int i = ct; i < (p.B * K) >> 2; i += NCT) dst[i] = __ldcg(o + i);
+        for (int i = ct; i < (p.B * K) >> 2; i += NCT) dst[i] = __ldcg(o4 + i);
+      } else {
+        const int K4 = K >> 2;
+#pragma unroll 4
+        for (int i = ct; i < p.B * K4; i += NCT) {
+          const int b = i / K4, c = i - b * K4;
+          reinterpret_cast<float4*>(act + (size_t)b * K)[c] =
+              __ldcg(reinterpret_cast<const float4*>(o + (size_t)b * KF) + c);
+        }
+      }
       if (r1st) xres[ct] = x1st;
-      for (int i = ct + NCT; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
+      if (h == 0)
+        for (int i = ct + NCT; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
     }
     cbar();
     g.K = K;
@@ -2194,9 +2222,18 @@ struct Consumer {
         case T_QKV:
         case T_OPROJ: {
           ProjGemv g;
-          ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g);
-          mark(TR_ACT);
-          ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
+          if constexpr (NB > 2) {   // the O projection may run in K halves
+            const int parts = t.type == T_OPROJ ? p.o_halves : 1;
+            for (int h = 0; h < parts; ++h) {
+              ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g, h);
+              if (h == 0) mark(TR_ACT);
+              ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
+            }
+          } else {
+            ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g, 0);
+            mark(TR_ACT);
+            ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
+          }
           mark(TR_STAGES);
           ab = post_proj(t, ab);
           break;
@@ -2253,7 +2290,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
     Ring ring{smem, m, p.nstages, p.stage_bytes, 0, 0};
     if (tid >= NCT) {
       if (tid == NCT) {
-        Producer pr{p, ring, evict_first_policy()};
+        Producer<NB> pr{p, ring, evict_first_policy()};
         pr.run(t0, t1);
       }
     } else {

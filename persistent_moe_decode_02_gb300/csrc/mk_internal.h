@@ -16,8 +16,9 @@ constexpr int MAX_EXPERTS = 256;
 constexpr int CTR_STRIDE = 8;              // uint32 slots per counter (32 B apart)
 constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
 // rows per cross-warp partial-sum window of the wide GEMV: 64 at batch <= 2 (a
-// projection tile's rows in one window: one flush), else 32 (shared memory)
-constexpr int win_rows(int nb) { return nb <= 2 ? 64 : 32; }
+// projection tile's rows in one window: one flush), fewer for larger batches
+// (shared memory)
+constexpr int win_rows(int nb) { return nb <= 2 ? 64 : nb <= 4 ? 32 : 16; }
 constexpr int RL_COPIES = 8;               // copies of the router-logit sums (O tile i adds to copy i % 8)
 constexpr int TRACE_SLOTS = 12;            // stamps per task in the optional timeline
 constexpr int STRACE_CAP = 4096;           // ring stages per CTA in the optional stage timeline
@@ -122,6 +123,8 @@ struct Params {
   int psum_off;          // smem offset of the GEMV partial-sum windows (2 * NCW * win_rows(nb) * nb floats)
   int attn_mrg_floats;   // attention page-group states in the activation region (floats)
   int down_rows_max;    // most rows of an H-row tile (O projection, reduce)
+  int o_halves;         // 2: the O projection runs over two K halves (its input in shared memory
+                        // half at a time, so larger batches keep a deep weight ring), else 1
   int cf_pairs;         // most (expert, unit) pairs of one expert tile
   int* seq_len;         // device [bcap]
   const int* page_table;  // device [bcap * max_pages]
@@ -162,7 +165,7 @@ struct Params {
 // false when the shape leaves no room (fewer than two stages, or an attention
 // page split the warps cannot share evenly).
 struct SmemPlan {
-  int stage_bytes, nstages, act_floats, act_off, misc_off, psum_off, attn_mrg_floats, smem;
+  int stage_bytes, nstages, act_floats, act_off, misc_off, psum_off, attn_mrg_floats, smem, o_halves;
 };
 
 // Per-expert-tile coefficients (gate x silu(gate row) x up row, per token slot)
@@ -205,7 +208,10 @@ inline int router_stage_bytes(int nr, int E) { return router_stage_gain_off(nr, 
 inline bool plan_smem(int H, int nq, int d, int G, int E, int F, int ps, int bcap, int nb, int down_rows_max,
                       int cf, size_t misc_struct_bytes, SmemPlan& o) {
   const int nqd = nq * d;
-  const int widest = H > nqd ? (H > F ? H : F) : (nqd > F ? nqd : F);
+  // above batch 2 the O projection's input (the widest) goes in two K halves
+  o.o_halves = nb > 2 && nqd > H && (nqd / 2) % 2048 == 0 ? 2 : 1;
+  const int kin = nqd / o.o_halves;
+  const int widest = H > kin ? (H > F ? H : F) : (kin > F ? kin : F);
   const long long A1 = (long long)bcap * widest;
   const int RS = d + 4;
   int ppg32 = 32768 / (2 * ps * d * 2);

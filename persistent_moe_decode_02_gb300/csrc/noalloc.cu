@@ -414,6 +414,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.misc_off = sp.misc_off;
   P.psum_off = sp.psum_off;
   P.attn_mrg_floats = sp.attn_mrg_floats;
+  P.o_halves = sp.o_halves;
   P.down_rows_max = cnt.down_rows_max;
   P.cf_pairs = mk::cf_floats(s.E, s.k, s.F, C, B) / B > 0 ? mk::cf_floats(s.E, s.k, s.F, C, B) / B : 1;
   P.seq_len = (int*)(base + d_blob + h_seq);

@@ -693,6 +693,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->P.misc_off = sp.misc_off;
   p->P.psum_off = sp.psum_off;
   p->P.attn_mrg_floats = sp.attn_mrg_floats;
+  p->P.o_halves = sp.o_halves;
   if (mk::max_active_ctas(p->nb, p->smem) < 1) {
     snprintf(g_last_error, sizeof(g_last_error), "megakernel does not fit on an SM with %d bytes of shared memory",
              p->smem);
