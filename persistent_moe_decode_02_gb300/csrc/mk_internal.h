@@ -171,7 +171,7 @@ struct SmemPlan {
 // Per-expert-tile coefficients (gate x silu(gate row) x up row, per token slot)
 // kept in shared memory between the tile's gate/up and down parts: at most
 // CF_FLOATS, else what one tile per CTA needs at this capacity.
-constexpr int CF_FLOATS = 2048;
+constexpr int CF_FLOATS = 3072;
 
 inline int cf_floats(int E, int k, int F, int C, int bcap) {
   const long long umax = E < bcap * k ? E : (long long)bcap * k;
