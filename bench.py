@@ -393,6 +393,84 @@ def timeline_arm(args, wl):
     plan.close()
 
 
+def serve_arm(args, wl):
+    """The continuous-batching loop (mk_serve_step) on the workload's model:
+    a seeded stream of requests (prompt and output lengths log-uniform), half
+    queued at the start and the rest after a quarter of the expected steps,
+    prompts fed through decode steps into an empty cache.  Prints one JSON
+    line: tokens through the model per second of wall time, and per step the
+    wall time and the stream time of the same calls (CUDA events around each
+    mk_serve_step; the difference is host time the GPU does not overlap)."""
+    import torch
+
+    from persistent_moe_decode_02_gb300 import mk
+    from synth.device import DeviceModel
+    D = wl.dims
+    cap = args.serve_batch
+    n_req = 4 * cap
+    plen = synth_lengths(n_req, 16, 256, wl.seed, "serve prompt")
+    olen = synth_lengths(n_req, 16, 128, wl.seed, "serve output")
+    ps = D.page_size
+    max_pages = (256 + 128 + ps - 1) // ps
+    num_pages = cap * max_pages
+    shape = (num_pages, D.n_kv_heads, D.head_dim, ps)
+    model = DeviceModel(D, wl.seed)
+    k = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
+    v = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
+    import synth
+    toks = synth.uniform_ints(int(sum(plen)), D.vocab, wl.seed, "serve tokens").tolist()
+    prompts, o = [], 0
+    for n in plen:
+        prompts.append(toks[o:o + n])
+        o += n
+    srv = mk.Server(D, model.weights(), k, v, max_batch=cap, max_pages=max_pages)
+    half = n_req // 2
+    for i in range(half):
+        srv.submit(i, prompts[i], olen[i])
+    expected = sum(p + m - 1 for p, m in zip(plen, olen)) // cap
+    stream = torch.cuda.current_stream()
+    steps, tokens, gpu_ms, wall, rest = 0, 0, 0.0, 0.0, False
+    torch.cuda.synchronize()
+    while True:
+        if not rest and steps >= expected // 4:
+            for i in range(half, n_req):
+                srv.submit(i, prompts[i], olen[i])
+            rest = True
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        b = srv.step(stream)
+        e1.record(stream)
+        e1.synchronize()
+        wall += time.perf_counter() - t0
+        if b == 0:
+            if rest:
+                break
+            for i in range(half, n_req):   # the first half finished early: queue the rest now
+                srv.submit(i, prompts[i], olen[i])
+            rest = True
+            continue
+        gpu_ms += e0.elapsed_time(e1)
+        steps += 1
+        tokens += b
+    st = srv.sched.stats()
+    assert st["retired"] == n_req and st["free_pages"] == num_pages, st
+    gen = int(sum(olen))
+    out = {"metric": "serving loop tokens/s (prompt and output tokens through the model, wall time)",
+           "value": tokens / wall, "unit": "tok/s", "generated_tok_s": gen / wall, "requests": n_req,
+           "max_batch": cap, "steps": steps, "ms_per_step_wall": 1e3 * wall / steps,
+           "ms_per_step_stream": gpu_ms / steps, "mean_batch": tokens / steps,
+           "config": {"workload": wl.name, "layers": D.n_layers, "prompt_tokens": "16-256 log-uniform",
+                      "output_tokens": "16-128 log-uniform", "weights": "bf16 random-init", "data": "synthetic"}}
+    print(json.dumps(out))
+    srv.close()
+
+
+def synth_lengths(n, lo, hi, seed, name):
+    import synth
+    return synth.log_uniform_lengths(n, lo, hi, seed, name)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,6 +483,9 @@ def main():
                     help="trace --steps steps per task and write a summary to this path ('-': print only)")
     ap.add_argument("--stage-trace", action="store_true",
                     help="with --timeline: also record every ring stage (saved beside the summary)")
+    ap.add_argument("--serve", action="store_true",
+                    help="time the continuous-batching loop (mk_serve_step) on the workload's model")
+    ap.add_argument("--serve-batch", type=int, default=8)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     import synth
@@ -413,6 +494,10 @@ def main():
         import __graft_entry__
         __graft_entry__.build()
         timeline_arm(args, wl)
+    elif args.serve:
+        import __graft_entry__
+        __graft_entry__.build()
+        serve_arm(args, wl)
     elif args.impl == "reference":
         reference_arm(args, wl)
     else:

@@ -234,6 +234,92 @@ int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weights* w, const
                            const int* d_tokens, float* d_logits, int* d_next_token, int* d_status,
                            mk_stream stream);
 
+/* ---- Continuous batching: request scheduler with a KV page allocator ----
+ *
+ * The pages describe the megakernel as the engine of a server that admits
+ * requests continuously into a paged KV cache with ragged lengths ("Cohere
+ * Publishes One-Kernel Server for North Mini Code", "A hand-built approach
+ * to a specialized server"; "Inside the Megakernel Serving Engine for North
+ * Mini Code", architecture paragraph).  mk_sched is the host side of that
+ * loop; the pages leave its policy open, and this one is the plainest:
+ *   - pages: a free list over the pool's num_pages pages; a request is
+ *     admitted only with the pages of its whole sequence (prompt_len +
+ *     max_new_tokens - 1 cached positions) reserved, so an admitted request
+ *     never waits for a page and nothing is ever preempted;
+ *   - admission: first come, first served, while a batch slot (max_batch) is
+ *     free and the request at the head of the queue fits in the free pages;
+ *   - every step feeds each admitted request one token: its prompt tokens in
+ *     order (the prediction of a prompt step is discarded, except after the
+ *     last prompt token: that one is the first output), then its own
+ *     previous output.  The prompt's K/V thus come from decode steps;
+ *   - retirement: after max_new_tokens outputs, or right after the request
+ *     outputs eos_token (eos_token < 0: none); its pages and slot are freed
+ *     at once, and the batch keeps the order of the requests that remain.
+ * The mk_sched_* calls are host-only (no CUDA call) and not thread-safe: one
+ * thread per scheduler. */
+typedef struct mk_sched mk_sched;
+
+/* A scheduler over a KV pool of num_pages pages of page_size tokens, for at
+ * most max_batch requests per step, each with a page-table row of
+ * max_pages_per_seq entries.  MK_ERR_INVALID for a non-positive argument. */
+int mk_sched_create(int num_pages, int page_size, int max_batch, int max_pages_per_seq, mk_sched** out);
+
+/* Queue request `rid` (unique among the requests the scheduler holds) with
+ * n_prompt >= 1 prompt tokens (host int32, copied; each >= 0) and
+ * max_new_tokens >= 1.  MK_ERR_INVALID for a bad argument or a repeated rid;
+ * MK_ERR_CAPACITY when its sequence needs more pages than a page-table row
+ * or the whole pool holds (it could never be admitted). */
+int mk_sched_submit(mk_sched* s, long long rid, const int* prompt, int n_prompt, int max_new_tokens,
+                    int eos_token);
+
+/* Admit what fits, then describe the next step's batch in host arrays sized
+ * for max_batch requests: *batch, seq_lens[b] (tokens cached), page_table[b *
+ * max_pages_per_seq + i] (-1 past the request's pages), tokens[b] (the input
+ * token) and rids[b]; *changed = 1 when the requests differ from the
+ * previous batch (a plan must then be updated), else 0.  *batch = 0: nothing
+ * to run.  A non-empty batch must be committed (or abandoned) before the
+ * next call, else MK_ERR_INVALID. */
+int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                  int* changed);
+
+/* The step of the last mk_sched_next ran: next_tokens[b] (host int32) is
+ * request b's greedy output.  Advances every request by one position,
+ * records outputs and retires finished requests.  MK_ERR_INVALID when no
+ * batch is pending. */
+int mk_sched_commit(mk_sched* s, const int* next_tokens);
+
+/* The step of the last mk_sched_next did not run: forget the batch (no
+ * request advances; the next batch reports changed = 1).  MK_ERR_INVALID
+ * when no batch is pending. */
+int mk_sched_abandon(mk_sched* s);
+
+/* Outputs of request rid so far: copies min(cap, count) tokens to `tokens`
+ * (host, may be NULL when cap == 0), the count to *n_tokens and 1 to *done
+ * once it retired.  MK_ERR_INVALID for an unknown rid. */
+int mk_sched_result(const mk_sched* s, long long rid, int* tokens, int cap, int* n_tokens, int* done);
+
+/* Drop a retired request's record (its outputs); MK_ERR_INVALID if rid is
+ * unknown or not retired. */
+int mk_sched_forget(mk_sched* s, long long rid);
+
+/* Counters: out[0] queued, [1] admitted, [2] retired (not forgotten), [3]
+ * free pages, [4] steps committed.  Writes min(n, 5) values. */
+int mk_sched_stats(const mk_sched* s, int* out, int n);
+
+void mk_sched_destroy(mk_sched* s);
+
+/* One step of the serving loop on `stream`: mk_sched_next; when *plan is
+ * NULL, mk_plan_create with that batch (capacity opts->max_batch, or the
+ * scheduler's max_batch when 0; a smaller capacity is MK_ERR_INVALID), else
+ * mk_plan_update when the requests changed; mk_decode_step_host; then
+ * mk_sched_commit.  dims, w and kv are read only when the plan is created
+ * (kv->num_pages must be at least the scheduler's pool).  Returns the batch
+ * size that ran (0: nothing queued or admitted) or an error; on an error the
+ * batch is abandoned, so the same requests run again on the next call (after
+ * a device error, only once the caller has dealt with it). */
+int mk_serve_step(mk_sched* s, mk_plan** plan, const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv,
+                  const mk_plan_opts* opts, mk_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

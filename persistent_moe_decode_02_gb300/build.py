@@ -7,7 +7,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["megakernel.cu", "plan.cu", "noalloc.cu"]
+SOURCES = ["megakernel.cu", "plan.cu", "noalloc.cu", "serve.cu"]
 HEADERS = [os.path.join(CSRC, "mk_internal.h"), os.path.join(ROOT, "include", "mk.h")]
 NVFLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
            "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CSRC]

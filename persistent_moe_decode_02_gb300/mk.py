@@ -24,7 +24,9 @@ TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
     "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
-    "mk_last_error", "mk_decode_step_noalloc",
+    "mk_last_error", "mk_decode_step_noalloc", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
+    "mk_sched_commit", "mk_sched_abandon", "mk_sched_result", "mk_sched_forget", "mk_sched_stats",
+    "mk_sched_destroy", "mk_serve_step",
 ]
 
 
@@ -87,8 +89,23 @@ def lib():
         L.mk_plan_inspect.argtypes = [ctypes.POINTER(MkModelDims), i32, p_int, i32, i32, p_int, i32, p_int]
         L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights),
                                              ctypes.POINTER(MkKv), i32, p_int, p_int, i32, vp, vp, vp, vp, vp]
+        i64, p_i64 = ctypes.c_longlong, ctypes.POINTER(ctypes.c_longlong)
+        L.mk_sched_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.mk_sched_submit.argtypes = [vp, i64, p_int, i32, i32, i32]
+        L.mk_sched_next.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
+        L.mk_sched_commit.argtypes = [vp, p_int]
+        L.mk_sched_abandon.argtypes = [vp]
+        L.mk_sched_result.argtypes = [vp, i64, p_int, i32, p_int, p_int]
+        L.mk_sched_forget.argtypes = [vp, i64]
+        L.mk_sched_stats.argtypes = [vp, p_int, i32]
+        L.mk_sched_destroy.argtypes = [vp]
+        L.mk_sched_destroy.restype = None
+        L.mk_serve_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights),
+                                    ctypes.POINTER(MkKv), ctypes.POINTER(MkPlanOpts), vp]
         for f in ("mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
-                  "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc"):
+                  "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc",
+                  "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
+                  "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -261,6 +278,132 @@ class Plan:
         if getattr(self, "h", None):
             lib().mk_plan_destroy(self.h)
             self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Scheduler:
+    """Owns an mk_sched: the host-side request queue, batch and KV page
+    allocator of continuous batching (include/mk.h describes the policy)."""
+
+    def __init__(self, num_pages: int, page_size: int, max_batch: int, max_pages: int):
+        h = ctypes.c_void_p()
+        rc = lib().mk_sched_create(num_pages, page_size, max_batch, max_pages, ctypes.byref(h))
+        if rc != MK_OK:
+            raise MkError("mk_sched_create", rc)
+        self.h, self.max_batch, self.max_pages = h, max_batch, max_pages
+
+    def submit(self, rid: int, prompt: Sequence[int], max_new_tokens: int, eos_token: int = -1) -> None:
+        rc = lib().mk_sched_submit(self.h, rid, _int_array(prompt), len(prompt), max_new_tokens, eos_token)
+        if rc != MK_OK:
+            raise MkError("mk_sched_submit", rc)
+
+    def next(self):
+        """The next batch as a dict (seq_lens, page_table, tokens, rids, changed), or None when idle."""
+        cap, mp = self.max_batch, self.max_pages
+        b, ch = ctypes.c_int(), ctypes.c_int()
+        sl, pt, tk = (ctypes.c_int * cap)(), (ctypes.c_int * (cap * mp))(), (ctypes.c_int * cap)()
+        rids = (ctypes.c_longlong * cap)()
+        rc = lib().mk_sched_next(self.h, ctypes.byref(b), sl, pt, tk, rids, ctypes.byref(ch))
+        if rc != MK_OK:
+            raise MkError("mk_sched_next", rc)
+        n = b.value
+        if n == 0:
+            return None
+        return {"seq_lens": list(sl[:n]), "page_table": list(pt[:n * mp]), "tokens": list(tk[:n]),
+                "rids": list(rids[:n]), "changed": bool(ch.value)}
+
+    def commit(self, next_tokens: Sequence[int]) -> None:
+        rc = lib().mk_sched_commit(self.h, _int_array(next_tokens))
+        if rc != MK_OK:
+            raise MkError("mk_sched_commit", rc)
+
+    def abandon(self) -> None:
+        rc = lib().mk_sched_abandon(self.h)
+        if rc != MK_OK:
+            raise MkError("mk_sched_abandon", rc)
+
+    def result(self, rid: int):
+        """(output tokens, done) of request rid."""
+        n, d = ctypes.c_int(), ctypes.c_int()
+        rc = lib().mk_sched_result(self.h, rid, None, 0, ctypes.byref(n), ctypes.byref(d))
+        if rc != MK_OK:
+            raise MkError("mk_sched_result", rc)
+        buf = (ctypes.c_int * max(1, n.value))()
+        rc = lib().mk_sched_result(self.h, rid, buf, n.value, ctypes.byref(n), ctypes.byref(d))
+        if rc != MK_OK:
+            raise MkError("mk_sched_result", rc)
+        return list(buf[:n.value]), bool(d.value)
+
+    def forget(self, rid: int) -> None:
+        rc = lib().mk_sched_forget(self.h, rid)
+        if rc != MK_OK:
+            raise MkError("mk_sched_forget", rc)
+
+    def stats(self) -> dict:
+        buf = (ctypes.c_int * 5)()
+        lib().mk_sched_stats(self.h, buf, 5)
+        return dict(zip(["queued", "active", "retired", "free_pages", "steps"], list(buf)))
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().mk_sched_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Server:
+    """The serving loop: a Scheduler plus the plan it drives (created by the
+    first mk_serve_step).  k_pools / v_pools: the KV pool the scheduler's
+    pages index (every page of it is the scheduler's)."""
+
+    def __init__(self, D, weights: dict, k_pools, v_pools, max_batch: int, max_pages: int, timeout_us: int = 0,
+                 num_ctas: int = 0, split_pages: int = 0):
+        self.D = D
+        self._keep = (weights, k_pools, v_pools)
+        self._w, self._kv, self._arrays = _weight_structs(D, weights, k_pools, v_pools)
+        self._dims = dims_struct(D)
+        self._opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, 0, 0)
+        self.sched = Scheduler(int(k_pools[0].shape[0]), D.page_size, max_batch, max_pages)
+        self.plan = ctypes.c_void_p()
+
+    def submit(self, rid: int, prompt: Sequence[int], max_new_tokens: int, eos_token: int = -1) -> None:
+        self.sched.submit(rid, prompt, max_new_tokens, eos_token)
+
+    def step(self, stream=None) -> int:
+        """One serving step; returns the batch size that ran (0: idle)."""
+        rc = lib().mk_serve_step(self.sched.h, ctypes.byref(self.plan), ctypes.byref(self._dims),
+                                 ctypes.byref(self._w), ctypes.byref(self._kv), ctypes.byref(self._opts),
+                                 _stream(stream))
+        if rc < 0:
+            raise MkError("mk_serve_step", rc)
+        return rc
+
+    def run(self, max_steps: int = 1 << 30, stream=None) -> int:
+        """Step until nothing is queued or admitted (or max_steps); returns the steps run."""
+        n = 0
+        while n < max_steps and self.step(stream) > 0:
+            n += 1
+        return n
+
+    def result(self, rid: int):
+        return self.sched.result(rid)
+
+    def close(self):
+        if getattr(self, "plan", None) and self.plan.value:
+            lib().mk_plan_destroy(self.plan)
+            self.plan = ctypes.c_void_p()
+        if getattr(self, "sched", None) is not None:
+            self.sched.close()
 
     def __del__(self):
         try:

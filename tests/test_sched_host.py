@@ -1,0 +1,197 @@
+"""Host-only tests of the continuous-batching scheduler (mk_sched_*, no GPU).
+
+The scheduler is driven with a fake model (the next token is a fixed function
+of the request and its position) and compared step by step with a plain
+Python restatement of the policy include/mk.h documents: pages reserved for
+prompt + max_new - 1 positions at admission, first come first served with
+head-of-line blocking, prompt tokens fed in order with their predictions
+discarded except after the last one, retirement after max_new outputs or on
+the end token, pages and slots freed at once, batch order kept."""
+import random
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def mk():
+    from persistent_moe_decode_02_gb300 import build, mk as m
+    build.build()
+    return m
+
+
+def fake_next(rid: int, pos: int, vocab: int = 50) -> int:
+    return (rid * 7919 + pos * 104729) % vocab
+
+
+class PolicyModel:
+    """The documented policy, restated independently of the C++."""
+
+    def __init__(self, num_pages, ps, max_batch, max_pages):
+        self.free, self.ps, self.max_batch, self.max_pages = num_pages, ps, max_batch, max_pages
+        self.queue, self.active, self.reqs = [], [], {}
+
+    def submit(self, rid, prompt, max_new, eos):
+        self.reqs[rid] = dict(prompt=list(prompt), max_new=max_new, eos=eos, out=[], len=0, done=False,
+                              pages=-(-(len(prompt) + max_new - 1) // self.ps))
+        self.queue.append(rid)
+
+    def next(self):
+        while self.queue and len(self.active) < self.max_batch and self.reqs[self.queue[0]]["pages"] <= self.free:
+            rid = self.queue.pop(0)
+            self.free -= self.reqs[rid]["pages"]
+            self.active.append(rid)
+        batch = []
+        for rid in self.active:
+            r = self.reqs[rid]
+            tok = r["prompt"][r["len"]] if r["len"] < len(r["prompt"]) else r["out"][-1]
+            batch.append((rid, r["len"], tok))
+        return batch
+
+    def commit(self, nxt):
+        keep = []
+        for rid, tok in zip(self.active, nxt):
+            r = self.reqs[rid]
+            r["len"] += 1
+            if r["len"] >= len(r["prompt"]):
+                r["out"].append(tok)
+                if len(r["out"]) >= r["max_new"] or (r["eos"] >= 0 and tok == r["eos"]):
+                    r["done"] = True
+            if r["done"]:
+                self.free += r["pages"]
+            else:
+                keep.append(rid)
+        self.active = keep
+
+
+def drive(mk, num_pages, ps, max_batch, max_pages, requests, arrivals=None, max_steps=500):
+    """Run scheduler and policy model side by side; returns the scheduler."""
+    s = mk.Scheduler(num_pages, ps, max_batch, max_pages)
+    ref = PolicyModel(num_pages, ps, max_batch, max_pages)
+    arrivals = arrivals or {0: list(range(len(requests)))}
+    step = 0
+    prev = None
+    while step < max_steps:
+        for i in arrivals.get(step, []):
+            rid, prompt, max_new, eos = requests[i]
+            s.submit(rid, prompt, max_new, eos)
+            ref.submit(rid, prompt, max_new, eos)
+        b = s.next()
+        want = ref.next()
+        if b is None:
+            assert want == []
+            if step > max(arrivals):
+                break
+            step += 1
+            continue
+        assert list(zip(b["rids"], b["seq_lens"], b["tokens"])) == want
+        assert b["changed"] == (prev != b["rids"])
+        prev = b["rids"]
+        # page rows: distinct pages across the batch, each row covers the request's reservation
+        rows = [b["page_table"][i * max_pages:(i + 1) * max_pages] for i in range(len(b["rids"]))]
+        held = [p for row in rows for p in row if p >= 0]
+        assert len(held) == len(set(held)) and all(0 <= p < num_pages for p in held)
+        for rid, row in zip(b["rids"], rows):
+            n = ref.reqs[rid]["pages"]
+            assert all(p >= 0 for p in row[:n]) and all(p == -1 for p in row[n:])
+        assert s.stats()["free_pages"] == ref.free
+        nxt = [fake_next(rid, pos) for rid, pos, _ in want]
+        s.commit(nxt)
+        ref.commit(nxt)
+        step += 1
+    for rid, r in ref.reqs.items():
+        out, done = s.result(rid)
+        assert (out, done) == (r["out"], r["done"]), rid
+    return s, ref
+
+
+def test_prompts_then_outputs_in_one_batch(mk):
+    reqs = [(10, [1, 2, 3], 4, -1), (11, [5], 3, -1), (12, [7, 8, 9, 10, 11, 12], 2, -1)]
+    s, ref = drive(mk, 64, 16, 4, 8, reqs)
+    for rid, prompt, max_new, _ in reqs:
+        out, done = s.result(rid)
+        assert done and len(out) == max_new
+        # the first output is the prediction after the last prompt token, then each output feeds the next step
+        assert out[0] == fake_next(rid, len(prompt) - 1)
+        assert all(out[i + 1] == fake_next(rid, len(prompt) + i) for i in range(max_new - 1))
+    st = s.stats()
+    assert st["queued"] == 0 and st["active"] == 0 and st["retired"] == 3 and st["free_pages"] == 64
+
+
+def test_slots_and_pages_limit_admission_fifo(mk):
+    rng = random.Random(5)
+    reqs = [(100 + i, [rng.randrange(50) for _ in range(rng.randrange(1, 26))], rng.randrange(1, 16), -1)
+            for i in range(24)]
+    arrivals = {0: list(range(8)), 3: list(range(8, 16)), 9: list(range(16, 24))}
+    s, ref = drive(mk, 12, 4, 3, 16, reqs, arrivals)
+    assert all(r["done"] for r in ref.reqs.values())
+    assert s.stats()["free_pages"] == 12
+
+
+def test_head_of_line_request_blocks_until_pages_free(mk):
+    # 8 pages of 4 tokens: the second request needs all 8 and must wait for the first
+    reqs = [(1, [3] * 5, 4, -1), (2, [4] * 20, 13, -1), (3, [5], 1, -1)]
+    s = mk.Scheduler(8, 4, 4, 8)
+    for r in reqs:
+        s.submit(*r)
+    b = s.next()
+    assert b["rids"] == [1]          # request 2 needs 8 pages, 6 are free; request 3 waits behind it
+    st = s.stats()
+    assert st["queued"] == 2 and st["free_pages"] == 6
+    s.commit([0])
+    s, ref = drive(mk, 8, 4, 4, 8, reqs)
+    assert all(r["done"] for r in ref.reqs.values())
+
+
+def test_end_token_retires_early(mk):
+    eos = fake_next(7, 2)              # the first output of request 7 (prompt of 3 tokens)
+    reqs = [(7, [1, 1, 1], 10, eos), (8, [2, 2], 3, eos)]
+    s, ref = drive(mk, 32, 16, 2, 4, reqs)
+    out, done = s.result(7)
+    assert done and out == [eos]
+
+
+def test_abandon_repeats_the_batch(mk):
+    s = mk.Scheduler(16, 16, 2, 2)
+    s.submit(1, [4, 5], 3)
+    b1 = s.next()
+    assert b1["changed"]
+    s.abandon()
+    b2 = s.next()
+    assert b2["changed"] and (b2["rids"], b2["seq_lens"], b2["tokens"]) == (b1["rids"], b1["seq_lens"], b1["tokens"])
+    s.commit([9])
+    b3 = s.next()
+    assert not b3["changed"] and b3["seq_lens"] == [1] and b3["tokens"] == [5]
+
+
+def test_errors(mk):
+    s = mk.Scheduler(4, 16, 2, 2)
+    s.submit(1, [1], 2)
+    with pytest.raises(mk.MkError) as e:
+        s.submit(1, [1], 2)                     # repeated id
+    assert e.value.code == mk.MK_ERR_INVALID
+    with pytest.raises(mk.MkError) as e:
+        s.submit(2, [1] * 30, 4)                # 33 positions: 3 pages, a row holds 2
+    assert e.value.code == mk.MK_ERR_CAPACITY
+    for bad in ([], [-1]):
+        with pytest.raises(mk.MkError) as e:
+            s.submit(3, bad, 2)
+        assert e.value.code == mk.MK_ERR_INVALID
+    with pytest.raises(mk.MkError):
+        s.submit(4, [1], 0)
+    with pytest.raises(mk.MkError):
+        s.commit([0])                           # nothing pending
+    s.next()
+    with pytest.raises(mk.MkError):
+        s.next()                                # previous batch not committed
+    s.commit([0])
+    with pytest.raises(mk.MkError):
+        s.forget(1)                             # not finished yet
+    s.next()
+    s.commit([0])
+    assert s.result(1) == ([0, 0], True)
+    s.forget(1)
+    with pytest.raises(mk.MkError):
+        s.result(1)
+    with pytest.raises(mk.MkError):
+        mk.Scheduler(0, 16, 1, 1)
+    assert s.next() is None
