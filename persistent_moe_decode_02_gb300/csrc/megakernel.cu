@@ -1097,13 +1097,22 @@ struct Consumer {
                   }
                 }
               } else {
+                // rows in two groups of 4 held in registers; each activation
+                // row is read once per group instead of once per weight row
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  if (rb + q < n) {
-                    const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
+                for (int h = 0; h < 8; h += 4) {
+                  uint4 wv[4];
 #pragma unroll
-                    for (int j = 0; j < NB; ++j)
-                      if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
+                  for (int q = 0; q < 4; ++q)
+                    wv[q] = rb + h + q < n ? lds128(sts + (uint32_t)(rb + h + q) * rowb + gi * 16)
+                                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                  for (int j = 0; j < NB; ++j) {
+                    if (j < nb) {
+                      const float4 x0 = lds128f(aoff[j] + gi * 32), x1 = lds128f(aoff[j] + gi * 32 + 16);
+#pragma unroll
+                      for (int q = 0; q < 4; ++q) part[h + q][j] += dot8r(wv[q], x0, x1);
+                    }
                   }
                 }
               }
