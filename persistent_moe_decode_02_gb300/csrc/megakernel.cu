@@ -792,18 +792,45 @@ struct Consumer {
   template <class Src4>
   __device__ void fill_rmsnorm(const uint16_t* gamma, Src4 src) {
     const int H = p.H, H4 = H >> 2, B = p.B;
-    for (int b = 0; b < B; ++b) {
+    if constexpr (NB == 1) {
       float ss = 0.f;
-      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
+      float4* dst = reinterpret_cast<float4*>(act);
 #pragma unroll 4
       for (int i = ct; i < H4; i += NCT) {
-        const float4 v = src(b, i);
+        const float4 v = src(0, i);
         const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
         dst[i] = make_float4(v.x * bf_lo(gb.x), v.y * bf_hi(gb.x), v.z * bf_lo(gb.y), v.w * bf_hi(gb.y));
         ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
       }
       ss = warp_sum(ss);
-      if (lane == 0) m->red[b * NCW + cw] = ss;
+      if (lane == 0) m->red[cw] = ss;
+    } else {
+      // every request's loads of a column group go out together: one round trip, not B
+      float ss[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+      for (int i = ct; i < H4; i += NCT) {
+        float4 v[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) v[b] = b < B ? src(b, i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
+        const float g0 = bf_lo(gb.x), g1 = bf_hi(gb.x), g2 = bf_lo(gb.y), g3 = bf_hi(gb.y);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b < B) {
+            reinterpret_cast<float4*>(act + (size_t)b * H)[i] =
+                make_float4(v[b].x * g0, v[b].y * g1, v[b].z * g2, v[b].w * g3);
+            ss[b] = fmaf(v[b].x, v[b].x, fmaf(v[b].y, v[b].y, fmaf(v[b].z, v[b].z, fmaf(v[b].w, v[b].w, ss[b]))));
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < B) {
+          const float t = warp_sum(ss[b]);
+          if (lane == 0) m->red[b * NCW + cw] = t;
+        }
+      }
     }
     cbar();
     if (ct < B) {
@@ -1557,21 +1584,58 @@ struct Consumer {
       g0[h] = i < H4 ? __ldg(gam + i) : make_uint2(0u, 0u);
     }
     for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
-    for (int b = 0; b < p.B; ++b) {
+    if constexpr (NB == 1) {
       float ss = 0.f;
-      float4* dst = reinterpret_cast<float4*>(act + (size_t)b * H);
+      float4* dst = reinterpret_cast<float4*>(act);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = ct + h * NCT;
         if (i < H4) {
-          const float4 xv = b == 0 ? x0[h] : __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i);
-          const uint2 gb = b == 0 ? g0[h] : __ldg(gam + i);
+          const float4 xv = x0[h];
+          const uint2 gb = g0[h];
           dst[i] = make_float4(xv.x * bf_lo(gb.x), xv.y * bf_hi(gb.x), xv.z * bf_lo(gb.y), xv.w * bf_hi(gb.y));
           ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
         }
       }
       ss = warp_sum(ss);
-      if (lane == 0) m->red[b * NCW + cw] = ss;
+      if (lane == 0) m->red[cw] = ss;
+    } else {
+      // the other requests' rows: all loads out together (one round trip, not B - 1)
+      float4 xv[2][NB];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = ct + h * NCT;
+        xv[h][0] = x0[h];
+#pragma unroll
+        for (int b = 1; b < NB; ++b)
+          xv[h][b] = b < p.B && i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i) : z4;
+      }
+      float ss[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = ct + h * NCT;
+        if (i < H4) {
+          const uint2 gb = g0[h];
+          const float ga = bf_lo(gb.x), gc = bf_hi(gb.x), ge = bf_lo(gb.y), gg = bf_hi(gb.y);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (b < p.B) {
+              const float4 v = xv[h][b];
+              reinterpret_cast<float4*>(act + (size_t)b * H)[i] = make_float4(v.x * ga, v.y * gc, v.z * ge, v.w * gg);
+              ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < p.B) {
+          const float t = warp_sum(ss[b]);
+          if (lane == 0) m->red[b * NCW + cw] = t;
+        }
+      }
     }
     cbar();
     if (ct < p.B) {
@@ -1584,9 +1648,38 @@ struct Consumer {
     unsigned long long q0 = 0;
 #pragma unroll
     for (int c = 0; c < RL_COPIES; ++c) q0 += v0[c];
-    for (int i = ct; i < BE; i += NCT) {
-      const float v = from_fixed(i == ct ? q0 : load_sum(i)) * m->inv[i / E];
-      m->rl[i] = v == v ? v : -INFINITY;
+    if constexpr (NB == 1) {
+      for (int i = ct; i < BE; i += NCT) {
+        const float v = from_fixed(i == ct ? q0 : load_sum(i)) * m->inv[i / E];
+        m->rl[i] = v == v ? v : -INFINITY;
+      }
+    } else {
+      if (ct < BE) {
+        const float v = from_fixed(q0) * m->inv[ct / E];
+        m->rl[ct] = v == v ? v : -INFINITY;
+      }
+      // the rest two sums at a time, both sets of loads in flight together
+      for (int i = ct + NCT; i < BE; i += 2 * NCT) {
+        const int i2 = i + NCT;
+        unsigned long long a[RL_COPIES], c2[RL_COPIES];
+#pragma unroll
+        for (int c = 0; c < RL_COPIES; ++c) {
+          a[c] = __ldcg(rs + c * cs + i);
+          c2[c] = i2 < BE ? __ldcg(rs + c * cs + i2) : 0ull;
+        }
+        unsigned long long qa = 0, qb = 0;
+#pragma unroll
+        for (int c = 0; c < RL_COPIES; ++c) {
+          qa += a[c];
+          qb += c2[c];
+        }
+        const float va = from_fixed(qa) * m->inv[i / E];
+        m->rl[i] = va == va ? va : -INFINITY;
+        if (i2 < BE) {
+          const float vb = from_fixed(qb) * m->inv[i2 / E];
+          m->rl[i2] = vb == vb ? vb : -INFINITY;
+        }
+      }
     }
   }
 
@@ -1657,9 +1750,39 @@ struct Consumer {
         if (st && col) {
           const uint32_t sts = smem_u32(st) + coff;
           const float* cu = cf + (size_t)(u * F + f0 - q0) * bc;
-          for (int i = 0; i < n; ++i) {
-            const uint4 w = lds128(sts + (uint32_t)i * H * 2);
-            if constexpr (NB == 1) {
+          if constexpr (NB > 1) {
+            // every row of the stage is a unit of expert u, so all share its
+            // token slots: up to 8 rows in registers, then each token's 8
+            // output columns read and written once for all of them
+            for (int i0 = 0; i0 < n; i0 += 8) {
+              const int ni = min(8, n - i0);
+              uint4 w8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                w8[i] = i < ni ? lds128(sts + (uint32_t)(i0 + i) * H * 2) : make_uint4(0, 0, 0, 0);
+              for (int j = 0; j < nt; ++j) {
+                float4* yb = reinterpret_cast<float4*>(act + (size_t)toks[j] * H) + 2 * ct;
+                float4 a0 = yb[0], a1 = yb[1];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float c = i < ni ? cu[(i0 + i) * bc + j] : 0.f;
+                  const uint4 w = w8[i];
+                  a0.x = fmaf(c, bf_lo(w.x), a0.x);
+                  a0.y = fmaf(c, bf_hi(w.x), a0.y);
+                  a0.z = fmaf(c, bf_lo(w.y), a0.z);
+                  a0.w = fmaf(c, bf_hi(w.y), a0.w);
+                  a1.x = fmaf(c, bf_lo(w.z), a1.x);
+                  a1.y = fmaf(c, bf_hi(w.z), a1.y);
+                  a1.z = fmaf(c, bf_lo(w.w), a1.z);
+                  a1.w = fmaf(c, bf_hi(w.w), a1.w);
+                }
+                yb[0] = a0;
+                yb[1] = a1;
+              }
+            }
+          } else {
+            for (int i = 0; i < n; ++i) {
+              const uint4 w = lds128(sts + (uint32_t)i * H * 2);
               const float c = cu[i * bc];
               y[0] = fmaf(c, bf_lo(w.x), y[0]);
               y[1] = fmaf(c, bf_hi(w.x), y[1]);
@@ -1669,22 +1792,6 @@ struct Consumer {
               y[5] = fmaf(c, bf_hi(w.z), y[5]);
               y[6] = fmaf(c, bf_lo(w.w), y[6]);
               y[7] = fmaf(c, bf_hi(w.w), y[7]);
-            } else {
-              for (int j = 0; j < nt; ++j) {
-                const float c = cu[i * bc + j];
-                float4* yb = reinterpret_cast<float4*>(act + (size_t)toks[j] * H) + 2 * ct;
-                float4 a0 = yb[0], a1 = yb[1];
-                a0.x = fmaf(c, bf_lo(w.x), a0.x);
-                a0.y = fmaf(c, bf_hi(w.x), a0.y);
-                a0.z = fmaf(c, bf_lo(w.y), a0.z);
-                a0.w = fmaf(c, bf_hi(w.y), a0.w);
-                a1.x = fmaf(c, bf_lo(w.z), a1.x);
-                a1.y = fmaf(c, bf_hi(w.z), a1.y);
-                a1.z = fmaf(c, bf_lo(w.w), a1.z);
-                a1.w = fmaf(c, bf_hi(w.w), a1.w);
-                yb[0] = a0;
-                yb[1] = a1;
-              }
             }
           }
         }
