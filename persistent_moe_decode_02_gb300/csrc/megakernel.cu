@@ -383,6 +383,45 @@ __device__ __forceinline__ void gu_range(const Params& p, const Task& t, int U, 
   }
 }
 
+// Above batch 1 the distinct experts serve different numbers of token slots,
+// and a unit's work grows with them: the ranges are cut by cost instead, a
+// unit of expert u costing GU_UNIT_COST + cnt[u] (its weight rows, then one per
+// slot).  When the cut could give some tile more units than its coefficient
+// scratch holds (cf_pairs), the plain even cut is kept.  Producer and
+// consumers call this with the same routing, so they agree.
+constexpr long long GU_UNIT_COST = 1;
+
+__device__ __forceinline__ long long gu_cut(int U, int F, const int* cnt, long long T) {
+  long long acc = 0;
+  for (int u = 0; u < U; ++u) {
+    const long long w = GU_UNIT_COST + cnt[u], span = (long long)F * w;
+    if (T <= acc + span) return (long long)u * F + min((long long)F, (T - acc + w - 1) / w);
+    acc += span;
+  }
+  return (long long)U * F;
+}
+
+template <int NB>
+__device__ __forceinline__ void gu_range_w(const Params& p, const Task& t, int U, const int* cnt, long long& q0,
+                                           long long& q1) {
+  if constexpr (NB > 1) {
+    long long tot = 0;
+    int cmin = 1 << 30;
+    for (int u = 0; u < U; ++u) {
+      tot += GU_UNIT_COST + cnt[u];
+      cmin = min(cmin, cnt[u]);
+    }
+    tot *= p.F;
+    const long long n = t.a[1], i = t.a[0];
+    if (U > 0 && tot / (n * (GU_UNIT_COST + cmin)) + 2 <= p.cf_pairs) {
+      q0 = gu_cut(U, p.F, cnt, tot * i / n);
+      q1 = gu_cut(U, p.F, cnt, tot * (i + 1) / n);
+      return;
+    }
+  }
+  gu_range(p, t, U, q0, q1);
+}
+
 __device__ __forceinline__ const int* route_of(const Params& p, int l) {
   return p.route + (size_t)l * p.rm.ints;
 }
@@ -464,9 +503,9 @@ struct Producer {
   // Stage layout of expert tile t for U distinct experts: its flattened (distinct
   // expert, ffn unit) range, gate/up stages of pps units, then down stages of
   // rpw units, each within one expert; both cursors at their first stage.
-  __device__ void moe_layout(const Task& t, Geo& q, int U) {
+  __device__ void moe_layout(const Task& t, Geo& q, int U, const int* cnt) {
     long long g0, g1;
-    gu_range(p, t, U, g0, g1);
+    gu_range_w<NB>(p, t, U, cnt, g0, g1);
     q.q0 = (int)g0;
     q.q1 = (int)g1;
     q.pps = pairs_per_stage(p);
@@ -525,10 +564,16 @@ struct Producer {
         q.W2 = p.w_down[l];
         asm volatile("" ::"l"(q.W), "l"(q.W2));
         const int Ug = min(p.E, p.B * p.k);
-        moe_layout(t, q, Ug);
+        if constexpr (NB == 1) moe_layout(t, q, Ug, nullptr);
         if (!route_ready(c, l, task)) return false;
         q.rc = c;
-        if (c->U != Ug) moe_layout(t, q, c->U);
+        if constexpr (NB == 1) {
+          if (c->U != Ug) moe_layout(t, q, c->U, nullptr);
+        } else {
+          // the cut depends on the token counts: the consumers' table (r_cnt)
+          // holds this layer's until this CTA's next expert task routes
+          moe_layout(t, q, c->U, r.m->r_cnt);
+        }
         return true;
       }
       case T_RED:      // no weights: reads only the expert tiles' partials
@@ -1705,7 +1750,7 @@ struct Consumer {
     cbar();
     mark(TR_ACT);
     long long g0, g1;
-    gu_range(p, t, U, g0, g1);
+    gu_range_w<NB>(p, t, U, m->r_cnt, g0, g1);
     const int q0 = (int)g0, q1 = (int)g1;
     float* cf = scr;   // [unit - q0][token slot] coefficients
     for (int q = q0; q < q1;) {
