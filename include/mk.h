@@ -156,6 +156,20 @@ int mk_plan_update(mk_plan* plan, int batch, const int* seq_lens, const int* pag
  * a step recorded). */
 int mk_plan_sync(mk_plan* plan, mk_stream stream);
 
+/* Sampling beyond greedy for the following steps (the pages stop at the next
+ * token; this is the plainest sampler).  temperature 0 (the default) is
+ * greedy; above 0 the next token of request b is a draw from
+ * softmax(logits / temperature), made by the Gumbel-max construction: the
+ * argmax over rows v of logit_v / temperature - log(-log(u_v)), with u_v =
+ * ((x >> 9) + 1/2) * 2^-23 and x word 0 of Philox4x32-10 (Salmon et al.,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011) with key (seed mod
+ * 2^32, seed >> 32) and counter (v, the request's position, b, 0); b counts
+ * across a group's sub-plans.  Draws are therefore reproducible from (seed,
+ * batch slot, position).  Logits written by a step stay unscaled.
+ * MK_ERR_INVALID for a negative or non-finite temperature.  Takes effect at
+ * the next step; mk_decode_step_noalloc is always greedy. */
+int mk_plan_set_sampling(mk_plan* plan, float temperature, unsigned long long seed);
+
 /* Copy a per-step intermediate of the most recent step into dst (device or
  * host memory, `bytes` long), on `stream`.  A plan with a capacity above 8
  * answers the per-request kinds (HIDDEN, EXPERT_IDS, GATES, ROUTER_LOGITS,

@@ -171,6 +171,38 @@ __device__ __forceinline__ float from_fixed(unsigned long long q) {
   return (float)((double)(long long)q * 2.3283064365386963e-10);
 }
 
+// Word 0 of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit
+// products, the key advanced by the Weyl constants before every round but
+// the first.
+__device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return c0;
+}
+
+// Standard Gumbel noise -log(-log(u)) for vocabulary row `row` of the request
+// in batch slot `slot` at position `pos`, u = ((x >> 9) + 1/2) * 2^-23 in
+// (0, 1) (exact in float32).  Kept out of line: only sampled steps call it.
+__device__ __noinline__ float gumbel_noise(uint32_t row, uint32_t pos, uint32_t slot, uint32_t k0, uint32_t k1) {
+  const uint32_t x = philox_w0(row, pos, slot, 0u, k0, k1);
+  const float u = ((float)(x >> 9) + 0.5f) * 1.1920928955078125e-07f;
+  return -logf(-logf(u));
+}
+
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -2286,6 +2318,9 @@ struct Consumer {
         return __ldcg(reinterpret_cast<const float4*>(xo + (size_t)b * p.H) + i4);
       });
     }
+    const bool sampled = p.inv_temp > 0.f;
+    int* pos = reinterpret_cast<int*>(scr);   // each request's position: the noise counter
+    if (sampled && ct < B) pos[ct] = __ldcg(p.seq_len + ct);
     cbar();
     ++lm_done;
     mark(TR_ACT);
@@ -2299,8 +2334,11 @@ struct Consumer {
     }
     float* lg = p.logits;
     ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s0, float) {
-      const float s = m->inv[j] * s0;
+      float s = m->inv[j] * s0;
       if (lg) lg[(size_t)j * p.V + row] = s;
+      if (sampled)   // Gumbel-max: the argmax of the perturbed, scaled logits is a draw from softmax(logits / T)
+        s = fmaf(s, p.inv_temp,
+                 gumbel_noise((uint32_t)row, (uint32_t)pos[j], (uint32_t)(p.slot0 + j), p.seed_lo, p.seed_hi));
 #pragma unroll
       for (int jj = 0; jj < NB; ++jj)
         if (jj == j && (s > bv[jj] || (s == bv[jj] && row < bi[jj]))) {

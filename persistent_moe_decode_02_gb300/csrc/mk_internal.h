@@ -157,6 +157,12 @@ struct Params {
   const int* tokens;
   float* logits;        // nullable [B][V]
   int* next_token;
+  // temperature sampling (inv_temp = 1 / T; 0: greedy): the next token is the
+  // argmax of logit * inv_temp + Gumbel noise drawn by Philox4x32-10 with key
+  // (seed_lo, seed_hi) and counter (vocab row, position, slot0 + request, 0)
+  float inv_temp;
+  uint32_t seed_lo, seed_hi;
+  int slot0;
 };
 
 // Shared-memory layout of one CTA: [weight ring][activations][misc + down

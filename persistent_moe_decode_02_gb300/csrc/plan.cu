@@ -336,6 +336,9 @@ struct mk_plan {
   int smem = 0, nstages = 0, stage_bytes = 0, act_floats = 0;
   int replans = 0;
   uint32_t epoch = 0;
+  float inv_temp = 0.f;            // temperature sampling: 1 / T, 0 = greedy
+  unsigned long long seed = 0;
+  int slot0 = 0;                   // batch slot of the first request (sub-plan i of a group: 8 i)
   unsigned long long timeout_ns = 0;
   std::vector<int> seq, pt, open_start;
   std::vector<Task> tasks;
@@ -808,6 +811,10 @@ static int step_one(mk_plan* p, const int* d_tokens, float* d_logits, int* d_nex
   fill_params(p);
   mk::Params P = p->P;
   P.epoch = p->epoch;
+  P.inv_temp = p->inv_temp;
+  P.seed_lo = (uint32_t)(p->seed & 0xffffffffull);
+  P.seed_hi = (uint32_t)(p->seed >> 32);
+  P.slot0 = p->slot0;
   P.tokens = d_tokens;
   P.logits = d_logits;
   P.next_token = d_next_token;
@@ -1014,6 +1021,7 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
       destroy_group(g);
       return rc;
     }
+    sp->slot0 = i * M;
     g->subs.push_back(sp);
     g->sub_B.push_back(n);
   }
@@ -1080,6 +1088,21 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
     p->sub_B[i] = nb[i];
   }
   p->B = p->group_B = batch;
+  return MK_OK;
+}
+
+int mk_plan_set_sampling(mk_plan* p, float temperature, unsigned long long seed) {
+  if (!p || !(temperature >= 0.f) || temperature > 1e30f) {
+    mk::set_last_error("mk_plan_set_sampling: temperature must be finite and >= 0");
+    return MK_ERR_INVALID;
+  }
+  const float it = temperature > 0.f ? 1.0f / temperature : 0.f;
+  p->inv_temp = it;
+  p->seed = seed;
+  for (mk_plan* s : p->subs) {
+    s->inv_temp = it;
+    s->seed = seed;
+  }
   return MK_OK;
 }
 

@@ -24,7 +24,7 @@ TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_
 EXPORTS = [
     "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
     "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
-    "mk_last_error", "mk_decode_step_noalloc", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
+    "mk_last_error", "mk_decode_step_noalloc", "mk_plan_set_sampling", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
     "mk_sched_commit", "mk_sched_abandon", "mk_sched_result", "mk_sched_forget", "mk_sched_stats",
     "mk_sched_destroy", "mk_serve_step",
 ]
@@ -90,6 +90,7 @@ def lib():
         L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights),
                                              ctypes.POINTER(MkKv), i32, p_int, p_int, i32, vp, vp, vp, vp, vp]
         i64, p_i64 = ctypes.c_longlong, ctypes.POINTER(ctypes.c_longlong)
+        L.mk_plan_set_sampling.argtypes = [vp, ctypes.c_float, ctypes.c_ulonglong]
         L.mk_sched_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
         L.mk_sched_submit.argtypes = [vp, i64, p_int, i32, i32, i32]
         L.mk_sched_next.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
@@ -104,7 +105,7 @@ def lib():
                                     ctypes.POINTER(MkKv), ctypes.POINTER(MkPlanOpts), vp]
         for f in ("mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
                   "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc",
-                  "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
+                  "mk_plan_set_sampling", "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
                   "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -240,6 +241,12 @@ class Plan:
 
     def sync(self, stream=None) -> int:
         return lib().mk_plan_sync(self.h, _stream(stream))
+
+    def set_sampling(self, temperature: float, seed: int = 0) -> None:
+        """Temperature sampling for the following steps (0: greedy); see include/mk.h."""
+        rc = lib().mk_plan_set_sampling(self.h, float(temperature), int(seed) & (2 ** 64 - 1))
+        if rc != MK_OK:
+            raise MkError("mk_plan_set_sampling", rc)
 
     def read_debug(self, what: int, out: torch.Tensor, stream=None) -> torch.Tensor:
         rc = lib().mk_plan_read_debug(self.h, what, ctypes.c_void_p(out.data_ptr()),

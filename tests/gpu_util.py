@@ -155,7 +155,11 @@ class OracleReplay:
         self.L = self.D.n_layers if n_layers is None else n_layers
         self.req = O.OracleRequest(rid, prior_len, make_prior(self.D, wl.seed, cache_prior), self.D.n_layers)
 
-    def step(self, rec: StepRecord, b: int, rep: Report) -> None:
+    def step(self, rec: StepRecord, b: int, rep: Report, sampling: Optional[tuple] = None) -> None:
+        """sampling = (temperature, seed, batch slot): the expected token is the
+        oracle's temperature draw (oracle/sample.py) instead of the greedy one,
+        and a difference is excused when the GPU token's oracle key is within
+        NEAR_TIE of the largest key."""
         O, D = self.O, self.D
         pos = self.req.length
         x = O.widen(self.W.embed_rows([int(rec.tok_in[b])])[0])
@@ -189,8 +193,14 @@ class OracleReplay:
             rep.max_logit_rel = max(rep.max_logit_rel, rel_l2(g, logits))
             rep.max_logit_abs = max(rep.max_logit_abs, float((g - logits).abs().max()))
         gt = int(rec.next_tok[b])
+        score = logits
+        if sampling is not None:
+            from oracle import sample as OS
+            T, seed, slot = sampling
+            score = OS.sample_keys(logits, T, seed, slot, pos)
+            nxt = OS.sample_token(logits, T, seed, slot, pos)
         if gt != nxt:
-            if float(logits[gt]) >= float(logits.max()) - NEAR_TIE:
+            if float(score[gt]) >= float(score.max()) - NEAR_TIE:
                 rep.token_excused += 1
             else:
                 rep.token_unexcused += 1

@@ -229,3 +229,36 @@ def test_serving_loop_matches_oracle_greedy(max_batch, n_req):
             tok = out[j]     # the oracle follows the GPU's choice after an excused near-tie
     assert excused <= 1
     srv.close()
+
+
+@pytest.mark.parametrize("capacity", [0, 10])
+def test_temperature_sampling_matches_oracle(capacity):
+    # Sampled decoding: each step's token is the Gumbel-max draw from
+    # softmax(logits / T) with Philox noise keyed by (seed, batch slot,
+    # position); the oracle draws from its own float64 logits with its own
+    # generator.  Ragged batch of 3 on a plain plan; with capacity 10 the same
+    # 10 requests run as a group of two sub-plans (slots 8 and 9 in the second).
+    from tests.gpu_util import OracleReplay
+    n = 3 if capacity == 0 else 10
+    ctx = [128, 37, 95, 16, 1, 60, 77, 5, 130, 40][:n]
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=ctx, steps=5)
+    T, seed = 0.8, 0x123456789
+    run = GpuRun(wl, steps=5, **({"max_batch": capacity} if capacity else {}))
+    run.plan.set_sampling(T, seed)
+    recs = [run.step() for _ in range(5)]
+    rep = Report()
+    W = synth.SynthWeights(wl.dims, wl.seed)
+    greedy_differs = 0
+    for b in range(n):
+        rr = OracleReplay(wl, run.reqs[b].rid, ctx[b], W=W)
+        for rec in recs:
+            rr.step(rec, b, rep, sampling=(T, seed, b))
+            greedy_differs += int(rec.next_tok[b]) != int(torch.argmax(rec.logits[b]))
+    print(rep)
+    rep.assert_ok()
+    assert rep.token_excused <= 1
+    assert greedy_differs > 0            # the draws are not the greedy tokens
+    run.plan.set_sampling(0.0)           # back to greedy: the next token is the argmax
+    rec = run.step()
+    assert all(int(rec.next_tok[b]) == int(torch.argmax(rec.logits[b])) for b in range(n))
+    run.plan.close()
