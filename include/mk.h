@@ -113,6 +113,8 @@ typedef struct mk_plan_opts {
                           0 in production */
   int trace;         /* 1: record a per-task timeline every step (MK_DBG_TRACE); 2: also a
                         per-stage timeline (MK_DBG_STAGE_TRACE) */
+  float temperature; /* sampling from the first step, as mk_plan_set_sampling; 0 -> greedy */
+  unsigned long long seed;
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;

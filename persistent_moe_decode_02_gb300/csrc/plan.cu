@@ -650,6 +650,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   }
   rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages);
   if (rc != MK_OK) return rc;
+  if (!(o.temperature >= 0.f) || o.temperature > 1e30f) return MK_ERR_INVALID;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
@@ -664,6 +665,8 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->C = o.num_ctas > 0 ? std::min(o.num_ctas, sms) : sms;
   p->split_opt = o.split_pages;
   p->drop_task = o.debug_drop_task;
+  p->inv_temp = o.temperature > 0.f ? 1.0f / o.temperature : 0.f;
+  p->seed = o.seed;
   p->trace = o.trace >= 2 ? 2 : o.trace ? 1 : 0;
   p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
   p->max_pages = max_pages_per_seq;

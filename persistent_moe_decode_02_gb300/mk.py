@@ -51,7 +51,8 @@ class MkKv(ctypes.Structure):
 
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
-                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int)]
+                ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
+                ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong)]
 
 
 class MkError(RuntimeError):
@@ -374,12 +375,13 @@ class Server:
     pages index (every page of it is the scheduler's)."""
 
     def __init__(self, D, weights: dict, k_pools, v_pools, max_batch: int, max_pages: int, timeout_us: int = 0,
-                 num_ctas: int = 0, split_pages: int = 0):
+                 num_ctas: int = 0, split_pages: int = 0, temperature: float = 0.0, seed: int = 0):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._w, self._kv, self._arrays = _weight_structs(D, weights, k_pools, v_pools)
         self._dims = dims_struct(D)
-        self._opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, 0, 0)
+        self._opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, 0, 0, float(temperature),
+                                int(seed) & (2 ** 64 - 1))
         self.sched = Scheduler(int(k_pools[0].shape[0]), D.page_size, max_batch, max_pages)
         self.plan = ctypes.c_void_p()
 
