@@ -48,6 +48,23 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest x over the ranks of the process group (x itself on one rank):
+    the job's time is its slowest replica's."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def job_tok_s(world: int, batch: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every replica decodes `batch` tokens per step."""
+    return world * batch * steps / seconds
+
+
 def ncu_traffic(workload: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
@@ -244,11 +261,7 @@ def our_arm(args, wl):
     st = plan.sync()
     assert st == 0, mk.status_string(st)
     per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    elapsed_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t)
+    elapsed_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world)
     # distinct experts per layer over the whole batch (the experts a step must read)
     ids = torch.zeros(B, D.n_layers, D.top_k, dtype=torch.int32)
     plan.read_debug(mk.MK_DBG_EXPERT_IDS, ids)
@@ -261,7 +274,7 @@ def our_arm(args, wl):
     mean_launch_ms = statistics.mean(per_launch)
     achieved = bytes_per_launch / (mean_launch_ms * 1e-3) / 1e9
     peaks = measured_peaks()
-    value = world * B * args.steps / (elapsed_ms * 1e-3)
+    value = job_tok_s(world, B, args.steps, elapsed_ms * 1e-3)
 
     # end to end through the host-buffer entry point: H2D tokens, step, D2H next tokens, sync
     h_tok = torch.tensor(tok.cpu().tolist(), dtype=torch.int32).pin_memory()
@@ -273,12 +286,8 @@ def our_arm(args, wl):
         assert rc == 0, mk.status_string(rc)
         h_tok.copy_(h_next)
     t1 = time.perf_counter()
-    e2e_s = t1 - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t)
-    e2e = {"value": world * B * e2e_steps / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+    e2e_s = max_over_ranks(t1 - t0, world)
+    e2e = {"value": job_tok_s(world, B, e2e_steps, e2e_s), "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
            "d2h_bytes_per_step": 4 * B + 16, "steps": e2e_steps}
 
     cpu = None
