@@ -20,6 +20,13 @@ position `pos`, with seed s (64 bits):
 and the token is the lowest index among the maxima of the float32-rounded
 keys logits / T + g (the kernel's precision for the decision).  T = 0 is
 greedy decoding.
+
+Nucleus (top-p) sampling restricts the draw to the nucleus: rows sorted by
+logit (descending, lower index first among equal logits), the shortest
+prefix whose softmax(logits / T) mass reaches p.  Gumbel-max over a subset
+draws from the distribution renormalised to that subset, so the token is the
+argmax of the same keys over the nucleus only.  p = 1 is plain temperature
+sampling.
 """
 from __future__ import annotations
 
@@ -68,8 +75,30 @@ def sample_keys(logits: torch.Tensor, temperature: float, seed: int, slot: int, 
     return logits.double() / temperature + torch.from_numpy(g)
 
 
-def sample_token(logits: torch.Tensor, temperature: float, seed: int, slot: int, pos: int) -> int:
-    """The next token: greedy at T = 0, else argmax of the float32 keys (lowest index on ties)."""
+def nucleus(logits: torch.Tensor, temperature: float, top_p: float) -> torch.Tensor:
+    """Row indices of the nucleus for T > 0 and 0 < top_p <= 1 (float64 mass)."""
+    l = logits.double()
+    order = sorted(range(l.shape[0]), key=lambda v: (-float(l[v]), v))
+    prob = torch.softmax(l / temperature, 0)
+    mass, keep = 0.0, []
+    for v in order:
+        keep.append(v)
+        mass += float(prob[v])
+        if mass >= top_p:
+            break
+    return torch.tensor(keep, dtype=torch.long)
+
+
+def sample_token(logits: torch.Tensor, temperature: float, seed: int, slot: int, pos: int,
+                 top_p: float = 1.0) -> int:
+    """The next token: greedy at T = 0, else the argmax of the float32 keys
+    (lowest index on ties), over the nucleus when top_p < 1."""
     if temperature == 0:
         return int(torch.argmax(logits.to(torch.float32)))
-    return int(torch.argmax(sample_keys(logits, temperature, seed, slot, pos).to(torch.float32)))
+    keys = sample_keys(logits, temperature, seed, slot, pos).to(torch.float32)
+    if top_p >= 1.0:
+        return int(torch.argmax(keys))
+    rows = nucleus(logits, temperature, top_p)
+    sub = keys[rows]
+    best = float(sub.max())
+    return int(rows[sub == best].min())

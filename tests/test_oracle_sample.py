@@ -71,3 +71,45 @@ def test_tiny_temperature_is_greedy_and_noise_is_keyed():
     # the Gumbel law: mean = Euler-Mascheroni constant, variance = pi^2 / 6
     z = S.gumbel(np.arange(200000), pos=0, slot=0, seed=77)
     assert abs(z.mean() - 0.5772156649) < 0.01 and abs(z.var() - math.pi ** 2 / 6) < 0.03
+
+
+def test_nucleus_is_the_shortest_prefix_reaching_p():
+    g = torch.Generator().manual_seed(9)
+    for trial in range(20):
+        logits = torch.randn(12, generator=g, dtype=torch.float64) * 2
+        logits[3] = logits[7]                       # an exact tie: the lower index comes first
+        T = 0.5 + trial * 0.1
+        p = 0.05 + 0.045 * trial
+        rows = S.nucleus(logits, T, p).tolist()
+        prob = torch.softmax(logits / T, 0)
+        # brute force: the full order by (logit desc, index asc), then the shortest prefix with mass >= p
+        order = sorted(range(12), key=lambda v: (-float(logits[v]), v))
+        k = next(i for i in range(1, 13) if float(prob[order[:i]].sum()) >= p)
+        assert rows == order[:k]
+        assert float(prob[rows].sum()) >= p and (k == 1 or float(prob[rows[:-1]].sum()) < p)
+
+
+def test_nucleus_draws_follow_the_renormalised_truncated_softmax():
+    logits = torch.tensor([1.0, 0.2, -0.5, 2.0, 0.0, -1.0], dtype=torch.float64)
+    T, p = 1.1, 0.8
+    keep = S.nucleus(logits, T, p).tolist()
+    prob = torch.softmax(logits / T, 0)
+    want = np.zeros(6)
+    want[keep] = (prob[keep] / prob[keep].sum()).numpy()
+    n = 30000
+    counts = np.zeros(6)
+    for pos in range(n):
+        counts[S.sample_token(logits, T, seed=5, slot=pos % 4, pos=pos, top_p=p)] += 1
+    assert counts[[v for v in range(6) if v not in keep]].sum() == 0
+    chi2 = float(sum((counts[v] - n * want[v]) ** 2 / (n * want[v]) for v in keep))
+    assert chi2 < 25.0, (counts, n * want, chi2)
+
+
+def test_nucleus_limits():
+    g = torch.Generator().manual_seed(4)
+    logits = torch.randn(300, generator=g, dtype=torch.float64)
+    for pos in range(30):
+        # a nucleus that is the whole vocabulary draws exactly the plain temperature sample
+        assert S.sample_token(logits, 0.9, 3, 1, pos, top_p=1 - 1e-12) == S.sample_token(logits, 0.9, 3, 1, pos)
+        # a vanishing nucleus is the greedy token
+        assert S.sample_token(logits, 0.9, 3, 1, pos, top_p=1e-9) == int(torch.argmax(logits))
