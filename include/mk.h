@@ -2,7 +2,8 @@
  *
  * One decode step of a pre-norm MoE transformer (RMSNorm, QKV projection with
  * RoPE, KV append into a paged cache, split-KV paged GQA attention, O
- * projection, softmax/top-k router, SwiGLU experts, LM head, greedy argmax)
+ * projection, softmax/top-k router, SwiGLU experts, LM head, greedy argmax or
+ * a temperature draw)
  * runs as ONE persistent kernel: one CTA per SM walks a host-prepared list of
  * tile tasks, and counters in global memory say when a tile's inputs are
  * ready, so a tile starts as soon as its own inputs land while immutable
