@@ -412,13 +412,14 @@ def serve_arm(args, wl):
     mk_serve_step; the difference is host time the GPU does not overlap)."""
     import torch
 
+    import synth
     from persistent_moe_decode_02_gb300 import mk
     from synth.device import DeviceModel
     D = wl.dims
     cap = args.serve_batch
     n_req = 4 * cap
-    plen = synth_lengths(n_req, 16, 256, wl.seed, "serve prompt")
-    olen = synth_lengths(n_req, 16, 128, wl.seed, "serve output")
+    plen = synth.log_uniform_lengths(n_req, 16, 256, wl.seed, "serve prompt")
+    olen = synth.log_uniform_lengths(n_req, 16, 128, wl.seed, "serve output")
     ps = D.page_size
     max_pages = (256 + 128 + ps - 1) // ps
     num_pages = cap * max_pages
@@ -426,7 +427,6 @@ def serve_arm(args, wl):
     model = DeviceModel(D, wl.seed)
     k = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
     v = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
-    import synth
     toks = synth.uniform_ints(int(sum(plen)), D.vocab, wl.seed, "serve tokens").tolist()
     prompts, o = [], 0
     for n in plen:
@@ -473,11 +473,6 @@ def serve_arm(args, wl):
                       "output_tokens": "16-128 log-uniform", "weights": "bf16 random-init", "data": "synthetic"}}
     print(json.dumps(out))
     srv.close()
-
-
-def synth_lengths(n, lo, hi, seed, name):
-    import synth
-    return synth.log_uniform_lengths(n, lo, hi, seed, name)
 
 
 def main():
