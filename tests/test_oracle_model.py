@@ -261,3 +261,73 @@ def test_batch_is_independent_requests():
     O.decode_step(W, D, b1, 6)
     ra2 = O.decode_step(W, D, a2, 4)
     assert torch.equal(ra.logits, ra2.logits)
+
+
+def _prior_scores_closed_form(q, K, pos, dims):
+    """Scores of the rotated query against stored keys, written through the
+    rotation angle instead of a rotated vector: for the rotate-half pair
+    (i, i + d/2) with angle phi_i = pos * theta^(-2i/d),
+      <R(phi) q, k> = sum_i (q_i k_i + q_j k_j) cos phi_i + (q_i k_j - q_j k_i) sin phi_i,
+    j = i + d/2, scaled by 1/sqrt(d).  q [d] floats, K [T][d] floats."""
+    d = len(q)
+    half = d // 2
+    out = []
+    for k in K:
+        s = 0.0
+        for i in range(half):
+            j = i + half
+            phi = pos * dims.rope_theta ** (-2.0 * i / d)
+            s += (q[i] * k[i] + q[j] * k[j]) * math.cos(phi) + (q[i] * k[j] - q[j] * k[i]) * math.sin(phi)
+        out.append(s / math.sqrt(d))
+    return out
+
+
+def _x_mid_from_scores(W, x, data, T, scores_of, dims):
+    """x + Wo o with o_h = sum_t p_t V_t over the T prior tokens and a new
+    token whose key and value are zero (score 0, value 0)."""
+    G, d = dims.group, dims.head_dim
+    K0, V0 = data[0]
+    o = []
+    for h in range(dims.n_q_heads):
+        g = h // G
+        s = scores_of(h, [[float(v) for v in K0[t, g]] for t in range(T)])
+        z = 1.0 + sum(math.exp(v) for v in s)              # the new token adds exp(0)
+        for i in range(d):
+            o.append(sum(math.exp(s[t]) * float(V0[t, g, i]) for t in range(T)) / z)
+    return [x[r] + dot(W.t[("wo", 0)][r], o) for r in range(dims.hidden)]
+
+
+def test_query_is_rotated_at_the_decode_position():
+    # Non-zero Wq with Wk = Wv = 0: the new token scores 0 and carries a zero
+    # value, so the layer-0 output depends on the query only through its
+    # scores against the stored prior keys.  Those follow the closed form in
+    # cos/sin of the decode position; an unrotated query, a query rotated one
+    # position off, or the opposite rotation direction each give a different
+    # x_mid (phi is linear in the position, so the opposite direction is
+    # position -T), checked below so the pin cannot pass vacuously.
+    zeros_k = torch.zeros(D.n_kv_heads * D.head_dim, D.hidden, dtype=BF)
+    for T in (5, 11):
+        over = {}
+        for l in range(D.n_layers):
+            over[("wk", l)] = zeros_k
+            over[("wv", l)] = zeros_k
+        W = DictWeights(D, seed=4, over=over)
+        r, data = req(D, T, seed=12)
+        tok = 6
+        out = O.decode_step(W, D, r, tok)
+        x = [float(v) for v in W.t["embed"][tok]]
+        ms = sum(v * v for v in x) / len(x)
+        xn = [v / math.sqrt(ms + D.rms_eps) * float(gm) for v, gm in zip(x, W.t[("attn_norm", 0)])]
+        d = D.head_dim
+        q = [dot(W.t[("wq", 0)][i], xn) for i in range(D.n_q_heads * d)]
+
+        def at(pos):
+            return lambda h, K: _prior_scores_closed_form(q[h * d:(h + 1) * d], K, pos, D)
+
+        want = _x_mid_from_scores(W, x, data, T, at(T), D)
+        got = out.layers[0].x_mid
+        assert torch.allclose(got, torch.tensor(want, dtype=F64), rtol=1e-10, atol=1e-12)
+        # the wrong readings are far away
+        for wrong_pos in (0, T - 1, T + 1, -T):
+            wrong = _x_mid_from_scores(W, x, data, T, at(wrong_pos), D)
+            assert float((got - torch.tensor(wrong, dtype=F64)).abs().max()) > 1e-3
