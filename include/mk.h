@@ -120,7 +120,14 @@ typedef struct mk_plan_opts {
 
 typedef struct mk_plan mk_plan;
 
-/* Build the task list and dependency counters for `batch` requests whose
+/* Defined by: "Cohere Publishes One-Kernel Server for North Mini Code",
+ * "One resident program, many small tasks" (the host prepares a list of small
+ * tasks per SM and readiness lives in counters in global memory) and "What
+ * the scheduling change is meant to avoid" (tile-level scheduling, no false
+ * dependencies); "Inside the Megakernel Serving Engine for North Mini Code",
+ * architecture paragraph (a task list per SM).
+ *
+ * Build the task list and dependency counters for `batch` requests whose
  * caches hold seq_lens[b] tokens (host array), with the host page table
  * page_table[b * max_pages_per_seq + i] (page ids of request b in order).
  * Every page that covers positions [0, seq_lens[b]] must be present and in
@@ -130,7 +137,15 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
                    const int* seq_lens, const int* page_table, int max_pages_per_seq,
                    const mk_plan_opts* opts, mk_plan** out);
 
-/* One decode step, enqueued on `stream`: request b decodes d_tokens[b] (device
+/* Defined by: "Cohere Publishes One-Kernel Server for North Mini Code",
+ * "The delay is between operations" (one decode step: normalization,
+ * projections, attention and expert routing, run without kernel boundaries)
+ * and "One resident program, many small tasks" (one resident block per SM
+ * walks its tasks); "Inside the Megakernel Serving Engine for North Mini
+ * Code", architecture paragraph (QKV, then attention, then the MoE, as one
+ * program); "Cohere fuses an entire decode step into one GPU program".
+ *
+ * One decode step, enqueued on `stream`: request b decodes d_tokens[b] (device
  * int32[batch]) at position seq_len[b], writes its K/V there, and the greedy
  * next token to d_next_token[b] (device int32[batch]); d_logits (device
  * fp32[batch, vocab]) is written when non-NULL.  d_tokens may alias
@@ -147,7 +162,12 @@ int mk_decode_step(mk_plan* plan, const int* d_tokens, float* d_logits, int* d_n
 int mk_decode_step_host(mk_plan* plan, const int* h_tokens, float* h_logits, int* h_next_token,
                         mk_stream stream);
 
-/* Continuous batching: replace the batch (requests joining or leaving) with
+/* Defined by: "Cohere Publishes One-Kernel Server for North Mini Code",
+ * introduction (the engine serves with continuous batching, paged attention
+ * and ragged sequence lengths) and "A hand-built approach to a specialized
+ * server".
+ *
+ * Continuous batching: replace the batch (requests joining or leaving) with
  * `batch` requests (<= the plan's capacity), their cached lengths and page
  * table (host arrays, same layout as mk_plan_create).  Rebuilds the task list,
  * uploads it with the lengths and page table on `stream`, resets counters and
@@ -169,7 +189,9 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  * 2^32, seed >> 32) and counter (v, the request's position, b, 0); b counts
  * across a group's sub-plans.  Draws are therefore reproducible from (seed,
  * batch slot, position).  Logits written by a step stay unscaled.
- * MK_ERR_INVALID for a negative or non-finite temperature.  Takes effect at
+ * MK_ERR_INVALID for a negative, NaN or infinite temperature, or a positive
+ * one so small that its inverse overflows (below about 2.9e-39); mk_plan_create
+ * applies the same rule to opts->temperature.  Takes effect at
  * the next step; mk_decode_step_noalloc is always greedy. */
 int mk_plan_set_sampling(mk_plan* plan, float temperature, unsigned long long seed);
 

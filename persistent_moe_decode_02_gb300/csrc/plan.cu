@@ -622,6 +622,15 @@ int mk_plan_inspect(const mk_model_dims* dims, int batch, const int* seq_lens, i
   return (int)tasks.size();
 }
 
+// A usable sampling temperature: 0 (greedy), or finite and positive with a
+// finite inverse (the LM tiles scale logits by 1 / T; below about 2.9e-39 the
+// inverse overflows to infinity and every key would be NaN or infinite).
+static bool temperature_ok(float t) {
+  if (t == 0.f) return true;
+  return t > 0.f && std::isfinite(t) && std::isfinite(1.0f / t);
+}
+
+
 static void destroy_one(mk_plan* p);
 
 static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
@@ -650,7 +659,10 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   }
   rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages);
   if (rc != MK_OK) return rc;
-  if (!(o.temperature >= 0.f) || o.temperature > 1e30f) return MK_ERR_INVALID;
+  if (!temperature_ok(o.temperature)) {
+    mk::set_last_error("mk_plan_create: temperature must be 0 (greedy) or a finite value whose inverse is finite");
+    return MK_ERR_INVALID;
+  }
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
@@ -1095,8 +1107,8 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
 }
 
 int mk_plan_set_sampling(mk_plan* p, float temperature, unsigned long long seed) {
-  if (!p || !(temperature >= 0.f) || temperature > 1e30f) {
-    mk::set_last_error("mk_plan_set_sampling: temperature must be finite and >= 0");
+  if (!p || !temperature_ok(temperature)) {
+    mk::set_last_error("mk_plan_set_sampling: temperature must be 0 (greedy) or a finite value whose inverse is finite");
     return MK_ERR_INVALID;
   }
   const float it = temperature > 0.f ? 1.0f / temperature : 0.f;

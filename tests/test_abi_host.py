@@ -200,3 +200,43 @@ def test_full_bs1_phases_spread_over_all_ctas(mk):
         assert max(per_cta[typ].values()) == 1, typ   # and takes one tile of it
     # 513 pages x 4 groups in 14-page chunks: 148 chunks, at most one per CTA
     assert len(per_cta[T_ATTN]) == 148 and max(per_cta[T_ATTN].values()) == 1
+
+
+def test_plan_create_rejects_unusable_temperatures(mk):
+    # The temperature is checked before any CUDA call, so fake (aligned,
+    # never dereferenced) device addresses are enough here.  Negative, NaN,
+    # infinite and denormal-small temperatures (whose inverse overflows) are
+    # MK_ERR_INVALID; the message names the rule.
+    class Fake:
+        def __init__(self, addr):
+            self.addr = addr
+
+        def data_ptr(self):
+            return self.addr
+
+    D = TINY
+    L = D.n_layers
+    addr = iter(range(1 << 20, 1 << 30, 1 << 12))
+    weights = {k: Fake(next(addr)) for k in ("embed", "final_norm", "lm_head")}
+    for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down"):
+        weights[k] = [Fake(next(addr)) for _ in range(L)]
+    pools = [Fake(next(addr)) for _ in range(L)]
+
+    class Pool(Fake):
+        shape = (64,)
+
+    kp = [Pool(p.addr) for p in pools]
+    w, kv, keep = mk._weight_structs(D, weights, kp, kp)
+    dims = mk.dims_struct(D)
+    lens = mk._int_array([20])
+    pt = mk._int_array(list(range(4)))
+    out = ctypes.c_void_p()
+    for T in (-1.0, float("nan"), float("inf"), 1e-39):
+        opts = mk.MkPlanOpts()
+        opts.temperature = T
+        rc = mk.lib().mk_plan_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(kv), 1, lens, pt, 4,
+                                     ctypes.byref(opts), ctypes.byref(out))
+        assert rc == mk.MK_ERR_INVALID, T
+        assert b"inverse" in mk.lib().mk_last_error(), T
+        assert not out.value
+    del keep

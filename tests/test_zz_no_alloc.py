@@ -20,9 +20,12 @@ from tests.gpu_util import LOGIT_MAX_ABS, LOGIT_REL_L2, rel_l2
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_matches_plan_step_on_two_calls(built):
+@pytest.mark.parametrize("ctx", [[128, 45], [300, 17, 160]])
+def test_noalloc_matches_plan_step_on_two_calls(built, ctx):
+    # batch 2, and batch 3 (kernel capacity rounded up to 4) whose contexts
+    # split into several KV chunks per (request, group) with a combine each
     from persistent_moe_decode_02_gb300 import mk
-    wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 45], steps=2)
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=ctx, steps=2)
     D = wl.dims
     model = DeviceModel(D, wl.seed)
     max_pages = max((c + 3 + D.page_size) // D.page_size for c in wl.ctx) + 1
@@ -38,7 +41,7 @@ def test_noalloc_matches_plan_step_on_two_calls(built):
     pt = kv_a.page_table(reqs_a)
     lens = [r.length for r in reqs_a]
     plan = mk.Plan(D, model.weights(), kv_a.k, kv_a.v, lens, pt, max_pages)
-    tok_a = torch.tensor(initial_tokens(wl, [0, 1]), dtype=torch.int32, device="cuda")
+    tok_a = torch.tensor(initial_tokens(wl, list(range(wl.batch))), dtype=torch.int32, device="cuda")
     tok_b = tok_a.clone()
     B = wl.batch
     for step in range(2):
@@ -77,5 +80,6 @@ def test_noalloc_rejects_oversized_step(built):
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = mk.decode_step_noalloc(D, model_like, pools * D.n_layers, pools * D.n_layers, [ctx],
                                 list(range(pages)), pages, tok, tok)
-    assert rc in (mk.MK_ERR_CAPACITY, mk.MK_ERR_INVALID)
-    assert mk.lib().mk_last_error().decode()
+    assert rc == mk.MK_ERR_CAPACITY
+    msg = mk.lib().mk_last_error().decode()
+    assert "bytes of scratch" in msg and str(64 << 20) in msg, msg
