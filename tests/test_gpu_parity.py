@@ -119,37 +119,50 @@ def test_capacity_error_when_no_page_for_next_position():
 
 
 @pytest.mark.slow
-def test_full_bs1_8k_two_steps_and_determinism():
+def test_full_bs1_8k_16_steps():
+    # the headline workload: 48 layers, 128 experts top-8, batch 1, 8192
+    # cached tokens; 16 greedy steps, every layer and the logits compared
     wl = synth.workload("full_bs1_8k")
-    rep = run_and_check(wl, steps=2, cache_prior=False)
+    rep = run_and_check(wl, steps=16)
     print(rep)
     rep.assert_ok()
+    assert rep.steps == 16 and rep.layers_checked == 16 * 48
 
 
 @pytest.mark.slow
-def test_full_b1_256k_first_layers():
+def test_full_b1_256k_whole_step():
+    # batch 1 at 262,144 cached tokens (about 26 GB of paged K/V): all 48
+    # layers, the logits and the greedy token of one step
     wl = synth.workload("full_b1_256k")
-    rep = run_and_check(wl, steps=1, n_layers=2, cache_prior=False)
+    rep = run_and_check(wl, steps=1, cache_prior=False)
     print(rep)
     rep.assert_ok()
+    assert rep.steps == 1 and rep.layers_checked == 48
 
 
 @pytest.mark.slow
-def test_full_b32_churn_sampled_requests():
-    # batch 32, contexts log-uniform in [512, 32768], 2 finish / 2 join at 512 per step
+def test_full_b32_churn_whole_steps():
+    # batch 32, contexts log-uniform in [512, 32768]; after every step the 2
+    # oldest requests finish and 2 new ones join at 512 tokens.  Four steps,
+    # every layer and the logits of requests that stay throughout (17, 31),
+    # leave early (2) or joined later (32 from step 2, 35 from step 3).
     wl = synth.workload("full_b32_churn")
-    rep = run_churn_and_check(wl, capacity=32, steps=2, leave=wl.churn_leave, join=wl.churn_leave,
-                              join_ctx=wl.churn_join_ctx, sample=[2, 17, 31, 32], n_layers=2, cache_prior=False)
+    rep = run_churn_and_check(wl, capacity=32, steps=4, leave=wl.churn_leave, join=wl.churn_leave,
+                              join_ctx=wl.churn_join_ctx, sample=[2, 17, 31, 32, 35], cache_prior=False)
     print(rep)
     rep.assert_ok()
+    assert rep.steps == 2 + 4 + 4 + 3 + 2
 
 
 @pytest.mark.slow
-def test_full_b8_long_sampled_requests():
+def test_full_b8_long_whole_step():
+    # batch 8, contexts log-uniform in [8192, 262144]: every request, all 48
+    # layers, the logits and the greedy tokens of one step
     wl = synth.workload("full_b8_long")
-    rep = run_and_check(wl, steps=1, requests=[0, 2], n_layers=2, cache_prior=False)
+    rep = run_and_check(wl, steps=1, cache_prior=False)
     print(rep)
     rep.assert_ok()
+    assert rep.steps == 8 and rep.layers_checked == 8 * 48
 
 
 def test_tiny_batch_12_churn_over_two_sub_plans():
