@@ -265,7 +265,8 @@ def our_arm(args, wl):
     D = wl.dims
     model = DeviceModel(D, wl.seed)
     e2e_steps = max(3, args.steps // 4)
-    total_steps = args.warmup + args.steps + e2e_steps + 2
+    total_steps = args.warmup + args.steps + e2e_steps + 2 + (args.steps + args.steps_per_launch
+                                                               if args.steps_per_launch > 1 else 0)
     ps = D.page_size
     max_pages = max((c + total_steps + ps) // ps for c in wl.ctx) + 1
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, total_steps) + 4, max_pages, wl.seed)
@@ -310,6 +311,32 @@ def our_arm(args, wl):
     peaks = measured_peaks()
     value = job_tok_s(world, B, args.steps, elapsed_ms * 1e-3)
 
+    # several steps per launch (tokens fed back on the device): the same
+    # number of steps, timed the same way
+    K = max(1, args.steps_per_launch)
+    multi = None
+    if K > 1:
+        n_launch = max(1, args.steps // K)
+        # two row buffers in turn: a launch reads the last row of the other
+        rows = [torch.empty(K, B, dtype=torch.int32, device="cuda") for _ in range(2)]
+        rows[1][-1].copy_(tok)
+        rc = plan.steps(rows[1][-1], K, rows[0])   # warm-up launch
+        assert rc == 0, mk.status_string(rc)
+        evm = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        barrier()
+        torch.cuda.synchronize()
+        evm[0].record(stream)
+        for i in range(n_launch):
+            plan.steps(rows[i % 2][-1], K, rows[(i + 1) % 2])
+        evm[1].record(stream)
+        torch.cuda.synchronize()
+        st = plan.sync()
+        assert st == 0, mk.status_string(st)
+        ms = max_over_ranks(evm[0].elapsed_time(evm[1]), world)
+        multi = {"steps_per_launch": K, "launches": n_launch, "value": job_tok_s(world, B, n_launch * K, ms * 1e-3),
+                 "unit": "tok/s", "ms_per_step": ms / (n_launch * K)}
+        tok.copy_(rows[n_launch % 2][-1])
+
     # end to end through the host-buffer entry point: H2D tokens, step, D2H next tokens, sync
     h_tok = torch.tensor(tok.cpu().tolist(), dtype=torch.int32).pin_memory()
     h_next = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -343,7 +370,7 @@ def our_arm(args, wl):
                             "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                             "traffic": ncu_traffic(wl.name), "algorithmic_bytes_per_launch": bytes_per_launch,
                             "kernel": "mk_megakernel", "mean_launch_ms": mean_launch_ms},
-               "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+               "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "multi_step": multi,
                "clocks": clk.summary(), "plan": info, "kernel_hash": kernel_hash()}
         print(json.dumps(out), flush=True)
     plan.close()
@@ -518,6 +545,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steps-per-launch", type=int, default=8,
+                    help="also time this many decode steps per launch (tokens fed back on the device); 1: off")
     ap.add_argument("--timeline", default=None,
                     help="trace --steps steps per task and write a summary to this path ('-': print only)")
     ap.add_argument("--stage-trace", action="store_true",

@@ -116,6 +116,7 @@ typedef struct mk_plan_opts {
                         per-stage timeline (MK_DBG_STAGE_TRACE) */
   float temperature; /* sampling from the first step, as mk_plan_set_sampling; 0 -> greedy */
   unsigned long long seed;
+  float top_p;       /* nucleus sampling from the first step, as mk_plan_set_top_p; 0 -> 1 (off) */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;
@@ -156,6 +157,27 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
 int mk_decode_step(mk_plan* plan, const int* d_tokens, float* d_logits, int* d_next_token,
                    mk_stream stream);
 
+/* Defined by: "Cohere Publishes One-Kernel Server for North Mini Code", "The
+ * delay is between operations" (time lost where one kernel ends and the next
+ * begins), here at the boundary between decode steps; the pages stop at one
+ * step, and running several in one launch is this library's reading of it.
+ *
+ * n_steps >= 1 decode steps in ONE launch of the persistent kernel, each
+ * step's greedy (or sampled) tokens fed to the next on the device: step 0
+ * decodes d_tokens[b] (device int32[batch]); step s >= 1 decodes the tokens
+ * step s - 1 wrote.  Step s writes request b's next token to
+ * d_next_tokens[s * batch + b] (device int32[n_steps, batch]) and, when
+ * d_logits is non-NULL, its logits to d_logits[(s * batch + b) * vocab ...]
+ * (device fp32[n_steps, batch, vocab]).  Request b's step s runs at position
+ * seq_len[b] + s; every one of those positions needs a page (else
+ * MK_ERR_CAPACITY, nothing enqueued).  Afterwards the plan's lengths are
+ * seq_len + n_steps.  d_tokens may alias the first row of d_next_tokens.
+ * The results equal n_steps calls of mk_decode_step.  A group plan (capacity
+ * above 8) runs one such launch per sub-plan; the rows stay [n_steps, batch].
+ * Errors as mk_decode_step. */
+int mk_decode_steps(mk_plan* plan, const int* d_tokens, int n_steps, float* d_logits, int* d_next_tokens,
+                    mk_stream stream);
+
 /* The same step with HOST buffers: copies h_tokens in, runs the step, copies
  * the next tokens (and logits when h_logits != NULL) out, and waits for the
  * stream.  Host buffers may be pageable or pinned. */
@@ -194,6 +216,24 @@ int mk_plan_sync(mk_plan* plan, mk_stream stream);
  * applies the same rule to opts->temperature.  Takes effect at
  * the next step; mk_decode_step_noalloc is always greedy. */
 int mk_plan_set_sampling(mk_plan* plan, float temperature, unsigned long long seed);
+
+/* Nucleus (top-p) sampling for the following sampled steps: with a
+ * temperature above 0 and 0 < top_p < 1, the draw of mk_plan_set_sampling is
+ * restricted to the nucleus: the rows ordered by logit (descending, the lower
+ * index first among equal logits), cut at the shortest prefix whose mass
+ * reaches top_p of the total.  A row's mass is w = exp((logit - max logit) /
+ * temperature) in float32, held as the integer round(w * 2^32), so the sums
+ * are exact and independent of the order of the adds; the cut is the first
+ * prefix whose integer mass reaches ceil(top_p * total).  The token is then
+ * the argmax of the same keys as mk_plan_set_sampling (logit / temperature
+ * plus Gumbel noise keyed by seed, batch slot and position) over the nucleus
+ * only.  The pages stop at the next token; this is the standard sampler
+ * restricted as its usual definition says.  top_p = 1 (the default) turns it
+ * off; temperature 0 stays greedy whatever top_p is.  The first step after
+ * the setting changes between on and off rebuilds the task list (one draw
+ * task per request after the LM head).  MK_ERR_INVALID outside (0, 1].
+ * mk_decode_step_noalloc is always greedy. */
+int mk_plan_set_top_p(mk_plan* plan, float top_p);
 
 /* Copy a per-step intermediate of the most recent step into dst (device or
  * host memory, `bytes` long), on `stream`.  A plan with a capacity above 8

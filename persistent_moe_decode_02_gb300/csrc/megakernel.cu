@@ -316,6 +316,11 @@ struct Misc {
   int r_rank[MAX_UNION * MAX_BATCH];
   // the producer's copies of a layer's distinct experts, one per cursor
   RouteCache cp_route;
+  // nucleus draw (T_SAMPLE): target and running mass, key prefix, digit, cut, max logit
+  unsigned long long smp_tgt, smp_before;
+  uint32_t smp_prefix;
+  int smp_digit, smp_cut;
+  float smp_max;
 };
 
 struct Ring {
@@ -344,10 +349,10 @@ __device__ void set_error(const Params& p, int code, int task, int info) {
 }
 
 // Wait until counter `ctr` holds epoch * cnt signals (bounded).
-__device__ bool wait_ctr(const Params& p, int ctr, uint32_t cnt, int task) {
+__device__ bool wait_ctr(const Params& p, int ctr, uint32_t epoch, uint32_t cnt, int task) {
   if (ctr < 0) return true;
   const uint32_t* c = p.ctr + (size_t)ctr * CTR_STRIDE;
-  const uint32_t target = p.epoch * cnt;
+  const uint32_t target = epoch * cnt;
   if ((int32_t)(ld_acquire(c) - target) >= 0) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; ++it) {
@@ -492,15 +497,18 @@ struct Producer {
   Ring r;
   uint64_t pol;
   int ti = 0;
+  int step = 0;           // step of this launch being walked (0 .. nsteps - 1)
   long long cp_lin = 0;   // ring stages filled so far (stage timeline index)
 
   __device__ void mark(int k) {
     if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
   }
 
-  // Routing of layer l into cache c (once per layer): this CTA's expert
-  // tile computes it and hands it over in shared memory (bounded wait).
-  __device__ bool route_ready(RouteCache* c, int l, int task) {
+  // Routing of layer l into cache c (once per layer and step): this CTA's
+  // expert tile computes it and hands it over in shared memory (bounded
+  // wait), tagged with the layer's index counted over the launch's steps.
+  __device__ bool route_ready(RouteCache* c, int l0, int task) {
+    const int l = step * p.L + l0;
     if (c->layer == l) return true;
     Misc* m = r.m;
     if (ld_acquire_cta(&m->r_layer) != l) {
@@ -577,7 +585,7 @@ struct Producer {
       case T_ATTN: {
         q.b = t.a[0];
         q.g = t.a[1];
-        const int pos = __ldcg(p.seq_len + q.b);
+        const int pos = __ldcg(p.seq_len + q.b) + step;
         int tok0, tok1;
         attn_range(p, t, pos, tok0, tok1);
         q.ppg = pages_per_stage(p);
@@ -609,6 +617,7 @@ struct Producer {
         return true;
       }
       case T_RED:      // no weights: reads only the expert tiles' partials
+      case T_SAMPLE:   // no weights: reads the kept logits
       case T_COMB: {   // no weights: reads only partials
         q.nst = 0;
         return true;
@@ -705,18 +714,45 @@ struct Producer {
     }
   }
 
+  // Before a later step's first KV page copy: the previous step's K/V appends
+  // must be visible to the bulk-copy engine.  Wait (bounded) for that step's
+  // done counter, then order the async proxy after it.
+  __device__ bool kv_ready(int task) {
+    if (!wait_ctr(p, p.cm.sdone, p.epoch + (uint32_t)step - 1u, (uint32_t)p.sdone_cnt, task)) return false;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+  }
+
   __device__ void run(int t0, int t1) {
     Misc* m = r.m;
     m->cp_route.layer = -1;
-    for (ti = t0; ti < t1; ++ti) {
-      if (failed(p)) return;
+    for (step = 0; step < p.nsteps; ++step) {
+      bool kv_seen = step == 0;
+      for (ti = t0; ti < t1; ++ti) {
+        if (!run_task(ti, kv_seen)) return;
+      }
+    }
+  }
+
+  __device__ bool run_task(int ti_, bool& kv_seen) {
+    Misc* m = r.m;
+    ti = ti_;
+    {
+      if (failed(p)) return false;
       const Task t = ldg_task(p.tasks + ti);
       mark(TR_P_START);
       Geo q;
       if (!geo(t, q, &m->cp_route, ti)) {
         if (t.type < T_QKV || t.type > T_LAST) set_error(p, MK_ERR_INVALID, ti, t.type);
         m->abort_flag = 1;
-        return;
+        return false;
+      }
+      if (t.type == T_ATTN && q.nst > 0 && !kv_seen) {
+        if (!kv_ready(ti)) {
+          m->abort_flag = 1;
+          return false;
+        }
+        kv_seen = true;
       }
       for (int s = 0; s < q.nst; ++s) {
         // claim the slot once the consumers released it, then for each piece
@@ -725,7 +761,7 @@ struct Producer {
         const uint32_t par = (r.round & 1) ^ 1;
         if (!mbar_wait(p, m, &m->empty[r.stage], par, -3)) {
           m->abort_flag = 1;
-          return;
+          return false;
         }
         if (s == 0) mark(TR_P_FIRST);
         uint64_t* bar = &m->full[r.stage];
@@ -746,6 +782,7 @@ struct Producer {
       }
       mark(TR_P_LAST);
     }
+    return true;
   }
 };
 
@@ -808,7 +845,9 @@ struct Consumer {
   static constexpr int WIN_ROWS = win_rows(NB);
   int ct, cw, lane;
   int ti = 0;
-  int lm_done = 0;   // LM-head tiles this CTA finished in this launch (its last task is the last of them)
+  int step = 0;      // step of this launch being run (0 .. nsteps - 1)
+  uint32_t epoch = 0;   // its counter epoch: p.epoch + step
+  int lm_done = 0;   // LM-head tiles this CTA finished in this step (its last task is the last of them)
 
   __device__ void mark(int k) {
     if (p.trace && ct == 0) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
@@ -921,7 +960,7 @@ struct Consumer {
   // Token id of request b, checked: an id outside [0, vocab) records
   // MK_ERR_INVALID and reads row 0 instead of faulting.
   __device__ int token(int b) const {
-    const int tok = __ldcg(p.tokens + b);
+    const int tok = step == 0 ? __ldcg(p.tokens + b) : __ldcg(p.next_token + (size_t)(step - 1) * p.io_stride + b);
     if (tok < 0 || tok >= p.V) {
       set_error(p, MK_ERR_INVALID, -1, tok);
       return 0;
@@ -1373,7 +1412,7 @@ struct Consumer {
   __device__ bool ticket(int ctr, uint32_t n, uint32_t add) {
     if (ct == 0) {
       const uint32_t old = atom_add_acq_rel(p.ctr + (size_t)ctr * CTR_STRIDE, add);
-      m->ticket_last = (old + add == p.epoch * n) ? 1 : 0;
+      m->ticket_last = (old + add == epoch * n) ? 1 : 0;
     }
     cbar();
     return m->ticket_last != 0;
@@ -1562,7 +1601,7 @@ struct Consumer {
         if (lane == 0) m->r_U = k;
       }
       cbar();
-      if (ct == 0) st_release_cta(&m->r_layer, l);
+      if (ct == 0) st_release_cta(&m->r_layer, step * p.L + l);
     } else {
       // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
       // groups of kp consecutive lanes (kp = k rounded up to a power of two)
@@ -1596,7 +1635,7 @@ struct Consumer {
         if (lane == 0) m->r_U = base;
       }
       cbar();
-      if (ct == 0) st_release_cta(&m->r_layer, l);   // the producer needs only r_U and r_exp
+      if (ct == 0) st_release_cta(&m->r_layer, step * p.L + l);   // the producer needs only r_U and r_exp
       if (ct < B * k) {
         const int e = m->sel[ct];
         int rank = 0;
@@ -1775,7 +1814,7 @@ struct Consumer {
       moe_act(l);
       cbar();
       mark(TR_MID1);
-      if (m->r_layer != l || t.a[0] == 0) route_local(l, t.a[0] == 0);
+      if (m->r_layer != step * p.L + l || t.a[0] == 0) route_local(l, t.a[0] == 0);
       mark(TR_MID2);
       U = m->r_U;
     }
@@ -1963,7 +2002,7 @@ struct Consumer {
     const int l = t.layer, b = t.a[0], g = t.a[1];
     const int G = p.G, d = p.d, half = d >> 1;
     constexpr int PS = 16;                         // page size (tokens)
-    const int pos = __ldcg(p.seq_len + b);
+    const int pos = __ldcg(p.seq_len + b) + step;
     int tok0, tok1;
     attn_range(p, t, pos, tok0, tok1);
     const int RS = d + 4;                          // partial row: acc[d], m, l, pad (16-byte rows)
@@ -2307,6 +2346,203 @@ struct Consumer {
     return ab;
   }
 
+  // Nucleus (top-p) draw of request b = t.a[0] from the logits its LM tiles
+  // kept.  Rows are ordered by logit, descending, the lower index first among
+  // equal logits.  Each row's mass is w = exp((logit - max) / T) in float32,
+  // held as the integer round(w * 2^32), so every sum below is exact and does
+  // not depend on the order of the adds.  The nucleus is the shortest prefix
+  // of the order whose mass reaches ceil(top_p * total).  It is found by a
+  // radix search over a 32-bit key that sorts rows the same way (four 8-bit
+  // digits, one pass over the logits each), then, for equal logits at the
+  // cut, by index.  The token is the Gumbel-max draw of the temperature
+  // sampler restricted to the nucleus: the argmax of logit / T + noise over it.
+  __device__ static uint32_t desc_key(float l) {
+    const uint32_t u = __float_as_uint(l + 0.0f);   // -0 -> +0
+    return (u & 0x80000000u) ? u : (~u & 0x7fffffffu);
+  }
+
+  __device__ bool sample(const Task& t, bool ab) {
+    if (ab) return ab;
+    const int b = t.a[0], V = p.V, tiles = p.lm_tiles;
+    const float* lg = p.lg_keep + (size_t)b * V;
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(act);   // [256] masses
+    unsigned int* hcnt = reinterpret_cast<unsigned int*>(hist + 256);       // [256] row counts
+    unsigned long long* red = reinterpret_cast<unsigned long long*>(hcnt + 256);   // [NCT] scan / sums
+    unsigned long long& s_tgt = m->smp_tgt;
+    unsigned long long& s_before = m->smp_before;
+    uint32_t& s_prefix = m->smp_prefix;
+    int& s_digit = m->smp_digit;
+    int& s_cut = m->smp_cut;
+    float& s_max = m->smp_max;
+    const int pos = __ldcg(p.seq_len + b) + step;
+    const float it = p.inv_temp;
+    // the largest logit, from the tiles' maxima
+    if (cw == 0) {
+      float v = -INFINITY;
+      for (int i = lane; i < tiles; i += 32) v = fmaxf(v, __ldcg(p.lm_val + (size_t)b * tiles + i));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+      if (lane == 0) s_max = v;
+    }
+    cbar();
+    const float mx = s_max;
+    auto mass = [&](float l) -> unsigned long long {
+      return __float2ull_rn(expf((l - mx) * it) * 4294967296.0f);
+    };
+    // the total mass, then the target
+    {
+      unsigned long long z = 0;
+      for (int v = ct; v < V; v += NCT) z += mass(__ldcg(lg + v));
+      red[ct] = z;
+      cbar();
+      if (ct == 0) {
+        unsigned long long tot = 0;
+        for (int i = 0; i < NCT; ++i) tot += red[i];
+        unsigned long long tg = (unsigned long long)ceil((double)p.top_p * (double)tot);
+        s_tgt = tg < 1ull ? 1ull : (tg > tot ? tot : tg);
+        s_before = 0;
+        s_prefix = 0;
+      }
+      cbar();
+    }
+    // four digit passes: the digit where the running mass reaches the target
+    for (int pass = 0; pass < 4; ++pass) {
+      const int sh = 24 - 8 * pass;
+      for (int i = ct; i < 256; i += NCT) {
+        hist[i] = 0;
+        hcnt[i] = 0;
+      }
+      cbar();
+      const uint32_t pre = s_prefix;
+      for (int v = ct; v < V; v += NCT) {
+        const float l = __ldcg(lg + v);
+        const uint32_t k = desc_key(l);
+        if (pass > 0 && (k >> (sh + 8)) != pre) continue;
+        const int dg = (k >> sh) & 0xff;
+        atomicAdd(&hist[dg], mass(l));
+        atomicAdd(&hcnt[dg], 1u);
+      }
+      cbar();
+      if (cw == 0) {
+        // lane i holds digits 8i .. 8i + 7; an exclusive scan over lanes finds the digit
+        unsigned long long loc[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          loc[j] = hist[lane * 8 + j];
+          sum += loc[j];
+        }
+        unsigned long long inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long y = __shfl_up_sync(FULL, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const unsigned long long before = s_before, tgt = s_tgt;
+        unsigned long long run = before + inc - sum;   // mass of every digit below this lane's first
+        int found = -1;
+        unsigned long long found_before = 0;
+        for (int j = 0; j < 8; ++j) {
+          if (found < 0 && run + loc[j] >= tgt) {
+            found = lane * 8 + j;
+            found_before = run;
+          }
+          run += loc[j];
+        }
+        const unsigned ok = __ballot_sync(FULL, found >= 0);
+        const int src = ok ? __ffs(ok) - 1 : 31;
+        const int dsel = __shfl_sync(FULL, ok ? found : 255, src);
+        const unsigned long long bsel = __shfl_sync(FULL, ok ? found_before : before, src);
+        const unsigned long long all = __shfl_sync(FULL, inc, 31);   // this pass's whole mass
+        if (lane == 0) {
+          // the digits' masses always reach the target (they add up to the
+          // digit chosen by the pass before); kept safe regardless: the last
+          // occupied digit
+          int d = dsel;
+          unsigned long long bb = bsel;
+          if (!ok) {
+            d = 255;
+            while (d > 0 && hcnt[d] == 0) --d;
+            bb = before + all - hist[d];
+          }
+          s_digit = d;
+          s_before = bb;
+          s_prefix = (s_prefix << 8) | (uint32_t)d;
+        }
+      }
+      cbar();
+    }
+    const uint32_t kcut = s_prefix;
+    // equal logits at the cut: rows in index order until the target is reached
+    int vcut = V;
+    if (hcnt[s_digit] > 1) {
+      const int per = (V + NCT - 1) / NCT, v0 = ct * per, v1 = min(V, v0 + per);
+      unsigned long long mine = 0;
+      for (int v = v0; v < v1; ++v) {
+        const float l = __ldcg(lg + v);
+        if (desc_key(l) == kcut) mine += mass(l);
+      }
+      red[ct] = mine;
+      cbar();
+      if (ct == 0) {
+        unsigned long long run = s_before;
+        int owner = NCT - 1;
+        for (int i = 0; i < NCT; ++i) {
+          if (run + red[i] >= s_tgt) { owner = i; break; }
+          run += red[i];
+        }
+        s_cut = owner;
+        red[NCT - 1] = run;   // mass before the owner's range (the owner reads it back)
+      }
+      cbar();
+      if (ct == s_cut) {
+        unsigned long long run = red[NCT - 1];
+        int c = v1 - 1;
+        for (int v = v0; v < v1; ++v) {
+          const float l = __ldcg(lg + v);
+          if (desc_key(l) != kcut) continue;
+          run += mass(l);
+          if (run >= s_tgt) { c = v; break; }
+        }
+        s_cut = c;
+      }
+      cbar();
+      vcut = s_cut;
+    }
+    // the draw: argmax of the temperature keys over the nucleus
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int v = ct; v < V; v += NCT) {
+      const float l = __ldcg(lg + v);
+      const uint32_t k = desc_key(l);
+      if (k > kcut || (k == kcut && v > vcut)) continue;
+      const float sv = fmaf(l, it, gumbel_noise((uint32_t)v, (uint32_t)pos, (uint32_t)(p.slot0 + b), p.seed_lo,
+                                                p.seed_hi));
+      if (sv > bv || (sv == bv && v < bi)) { bv = sv; bi = v; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(FULL, bv, o);
+      const int oi = __shfl_xor_sync(FULL, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) {
+      m->best_v[cw] = bv;
+      m->best_i[cw] = bi;
+    }
+    cbar();
+    if (ct == 0) {
+      float v = -INFINITY;
+      int ix = 0x7fffffff;
+      for (int w = 0; w < NCW; ++w)
+        if (m->best_v[w] > v || (m->best_v[w] == v && m->best_i[w] < ix)) { v = m->best_v[w]; ix = m->best_i[w]; }
+      p.next_token[(size_t)step * p.io_stride + b] = ix;
+      if (step + 1 == p.nsteps) p.seq_len[b] = __ldcg(p.seq_len + b) + p.nsteps;
+    }
+    ab = finish(false);
+    if (!ab) signal(p.cm.sdone);
+    return ab;
+  }
+
   // LM-head tile.  A CTA's LM tiles are the last tasks of its list: the first
   // fills the final norm's activations (kept by the later tiles), and only the
   // last takes the ticket, for all of this CTA's tiles at once.
@@ -2318,9 +2554,12 @@ struct Consumer {
         return __ldcg(reinterpret_cast<const float4*>(xo + (size_t)b * p.H) + i4);
       });
     }
-    const bool sampled = p.inv_temp > 0.f;
+    // nucleus sampling: this tile keeps its logits and finds their plain
+    // maximum; the request's T_SAMPLE task draws from them afterwards
+    const bool keep = p.lg_keep != nullptr;
+    const bool sampled = p.inv_temp > 0.f && !keep;
     int* pos = reinterpret_cast<int*>(scr);   // each request's position: the noise counter
-    if (sampled && ct < B) pos[ct] = __ldcg(p.seq_len + ct);
+    if (sampled && ct < B) pos[ct] = __ldcg(p.seq_len + ct) + step;
     cbar();
     ++lm_done;
     mark(TR_ACT);
@@ -2332,10 +2571,11 @@ struct Consumer {
       bv[j] = -INFINITY;
       bi[j] = 0x7fffffff;
     }
-    float* lg = p.logits;
+    float* lg = p.logits ? p.logits + (size_t)step * p.io_stride * p.V : nullptr;
     ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s0, float) {
       float s = m->inv[j] * s0;
       if (lg) lg[(size_t)j * p.V + row] = s;
+      if (keep) p.lg_keep[(size_t)j * p.V + row] = s;
       if (sampled)   // Gumbel-max: the argmax of the perturbed, scaled logits is a draw from softmax(logits / T)
         s = fmaf(s, p.inv_temp,
                  gumbel_noise((uint32_t)row, (uint32_t)pos[j], (uint32_t)(p.slot0 + j), p.seed_lo, p.seed_hi));
@@ -2380,7 +2620,7 @@ struct Consumer {
     if (!last) return ab;   // the last tile's barrier orders these writes before its ticket
     ab = finish(ab);
     if (ab) return ab;
-    if (ticket(p.cm.lm, (uint32_t)t.a[3], (uint32_t)lm_done)) {
+    if (ticket(p.cm.lm, (uint32_t)t.a[3], (uint32_t)lm_done) && !keep) {
       if (cw < B) {
         const int b = cw;
         float v = -INFINITY;
@@ -2397,25 +2637,42 @@ struct Consumer {
           if (ov > v || (ov == v && oi < ix)) { v = ov; ix = oi; }
         }
         if (lane == 0) {
-          p.next_token[b] = ix;
-          p.seq_len[b] = __ldcg(p.seq_len + b) + 1;
+          p.next_token[(size_t)step * p.io_stride + b] = ix;
+          // positions stay those of the launch's start until its last step is done
+          if (step + 1 == p.nsteps) p.seq_len[b] = __ldcg(p.seq_len + b) + p.nsteps;
         }
       }
       ab = finish(false);
+      if (!ab) signal(p.cm.sdone);   // the next step's first layer may read these tokens
     }
     return ab;
   }
 
   __device__ void run(int t0, int t1) {
+    for (step = 0; step < p.nsteps; ++step) {
+      epoch = p.epoch + (uint32_t)step;
+      lm_done = 0;
+      if (!run_step(t0, t1)) return;
+    }
+  }
+
+  // One pass over this CTA's tasks for step `step`; false once a wait gave up.
+  __device__ bool run_step(int t0, int t1) {
     for (ti = t0; ti < t1; ++ti) {
       const Task t = ldg_task(p.tasks + ti);
       if (ti + 1 < t1) prefetch_l1(p.tasks + ti + 1);   // the next record arrives while this task runs
       bool ab = false;
       nstage_seen = 0;
       mark(TR_FETCH);
-      if (ct == 0) ab = !wait_ctr(p, t.wait_ctr, t.wait_cnt, ti);
+      if (ct == 0) {
+        // the first layer of a later step starts from the previous step's tokens
+        if (t.wait_ctr < 0 && step > 0)
+          ab = !wait_ctr(p, p.cm.sdone, epoch - 1u, (uint32_t)p.sdone_cnt, ti);
+        else
+          ab = !wait_ctr(p, t.wait_ctr, epoch, t.wait_cnt, ti);
+      }
       ab = cbar_or(ab);
-      if (ab) break;
+      if (ab) return false;
       mark(TR_DEP);
       switch (t.type) {
         case T_QKV:
@@ -2440,13 +2697,15 @@ struct Consumer {
         case T_ATTN: ab = attn(t, ab); break;
         case T_MOE: ab = moe(t, ab); break;
         case T_RED: ab = red(t, ab); break;
-        case T_LM: ab = lm(t, ab, ti + 1 == t1); break;
+        case T_LM: ab = lm(t, ab, ti + 1 == t1 || ldg_task(p.tasks + ti + 1).type != T_LM); break;
         case T_COMB: ab = comb(t, ab); break;
+        case T_SAMPLE: ab = sample(t, ab); break;
         default: ab = true;
       }
-      if (ab) break;
+      if (ab) return false;
       mark(TR_DONE);
     }
+    return true;
   }
 };
 

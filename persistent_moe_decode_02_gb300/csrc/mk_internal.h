@@ -46,8 +46,9 @@ enum TaskType : int32_t {
   T_LM = 5,      // rows [a0,a1) of the LM head; a2 = tile index, a3 = tiles (ticket target)
   T_COMB = 6,    // split-KV combine of query heads [a2, a2 + a3) of request a0, KV group a1:
                  // a5 = first partial slot, a6 = chunks (waits for all of them)
+  T_SAMPLE = 7,  // nucleus (top-p) draw of request a0 from its logits, once every LM tile is done
 };
-constexpr int T_LAST = T_COMB;
+constexpr int T_LAST = T_SAMPLE;
 
 struct alignas(16) Task {
   int32_t type;
@@ -62,7 +63,7 @@ static_assert(sizeof(Task) == 48, "task record is 48 bytes");
 // satisfied when counter >= epoch * cnt (epoch = 1, 2, ... since the last reset).
 struct CtrMap {
   int L, nkv, bcap;
-  int qkv, attn, combine, o, rdone, gu, down, lm, total;
+  int qkv, attn, combine, o, rdone, gu, down, lm, sdone, total;
 
   void init(int L_, int nkv_, int bcap_) {
     L = L_; nkv = nkv_; bcap = bcap_;
@@ -75,6 +76,7 @@ struct CtrMap {
     gu = c; c += L;
     down = c; c += L;
     lm = c; c += 1;
+    sdone = c; c += 1;   // a step's next tokens are written (one signal per step)
     total = c;
   }
 #if defined(__CUDACC__)
@@ -114,7 +116,9 @@ struct Params {
   const int* cta_start;
   uint32_t* ctr;
   int* status;          // [0] code, [1] task, [2] cta, [3] info
-  uint32_t epoch;
+  uint32_t epoch;        // epoch of the launch's first step; step s waits for epoch + s
+  int nsteps;            // decode steps this launch runs (>= 1), each fed the previous one's tokens
+  int io_stride;         // requests between two steps' rows of next_token (and logits): the group's batch
   unsigned long long timeout_ns;
   CtrMap cm;
   RouteMap rm;
@@ -153,16 +157,25 @@ struct Params {
   unsigned long long* trace;
   // optional per-stage timeline: [cta][STRACE_CAP][STRACE_SLOTS] (nullable)
   unsigned long long* strace;
-  // io
+  // io: step 0 reads tokens[b]; step s >= 1 reads next_token[(s - 1) * io_stride + b];
+  // step s writes next_token[s * io_stride + b] and, when logits is set,
+  // logits[(s * io_stride + b) * V ...]
   const int* tokens;
-  float* logits;        // nullable [B][V]
-  int* next_token;
+  float* logits;        // nullable [nsteps][io_stride][V]
+  int* next_token;      // [nsteps][io_stride]
   // temperature sampling (inv_temp = 1 / T; 0: greedy): the next token is the
   // argmax of logit * inv_temp + Gumbel noise drawn by Philox4x32-10 with key
   // (seed_lo, seed_hi) and counter (vocab row, position, slot0 + request, 0)
   float inv_temp;
   uint32_t seed_lo, seed_hi;
   int slot0;
+  // nucleus sampling (top_p < 1 with inv_temp > 0): the LM tiles keep every
+  // logit in lg_keep and the per-tile maximum logit in lm_val; T_SAMPLE task b
+  // draws request b's token from the nucleus and signals sdone (sdone_cnt
+  // signals per step: B with nucleus sampling, else 1, the LM finisher's)
+  float top_p;
+  float* lg_keep;       // [bcap][V] or null
+  int sdone_cnt;
 };
 
 // Shared-memory layout of one CTA: [weight ring][activations][misc + down

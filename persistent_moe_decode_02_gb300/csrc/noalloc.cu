@@ -403,6 +403,11 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.ctr = (uint32_t*)(base + d_ctr);
   P.status = (int*)(base + d_stat);
   P.epoch = 1;
+  P.nsteps = 1;
+  P.io_stride = B;
+  P.top_p = 1.f;
+  P.lg_keep = nullptr;
+  P.sdone_cnt = 1;
   P.timeout_ns = 2000000000ull;
   P.strace = nullptr;
   P.cm = cm;

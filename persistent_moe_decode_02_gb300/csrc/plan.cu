@@ -155,7 +155,7 @@ inline void split_range(int n, int parts, int i, int& a, int& b) {
 // topological order, so with all CTAs resident the step cannot deadlock.
 int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int split_pages,
                 std::vector<Task>& out, std::vector<int>& cta_start, Counts& cnt,
-                std::vector<int>& open_start) {
+                std::vector<int>& open_start, bool nucleus = false) {
   if (B < 1 || B > bcap || C < 1) return MK_ERR_INVALID;
   mk::CtrMap cm;
   cm.init(s.L, s.nkv, bcap);
@@ -301,6 +301,15 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     ph.push_back({(double)(b - a) * s.H * 2, t});
   }
   asg.phase(ph);
+  if (nucleus) {   // one nucleus draw per request, once every LM tile is done
+    ph.clear();
+    for (int b = 0; b < B; ++b) {
+      Task t = mk_task(mk::T_SAMPLE, s.L - 1, cm.lm, (uint32_t)cnt.lm);
+      t.a[0] = b;
+      ph.push_back({(double)s.V * 4 * 6, t});
+    }
+    asg.phase(ph);
+  }
 
   out.clear();
   size_t ntot = 0;
@@ -337,6 +346,9 @@ struct mk_plan {
   int replans = 0;
   uint32_t epoch = 0;
   float inv_temp = 0.f;            // temperature sampling: 1 / T, 0 = greedy
+  float top_p = 1.f;               // nucleus sampling below 1 (with inv_temp > 0)
+  bool nucleus_built = false;      // the task list holds the nucleus draw tasks
+  float* d_lg_keep = nullptr;      // [bcap][V] logits kept for the draw
   unsigned long long seed = 0;
   int slot0 = 0;                   // batch slot of the first request (sub-plan i of a group: 8 i)
   unsigned long long timeout_ns = 0;
@@ -468,10 +480,15 @@ struct Built {
   std::vector<int> cs, open;
   Counts cnt;
   int rc = MK_OK;
+  bool nucleus = false;
 };
 
+bool nucleus_on(const mk_plan* p) { return p->inv_temp > 0.f && p->top_p < 1.f; }
+
 void build_for(const mk_plan* p, Built& b) {
-  b.rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open);
+  b.rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open,
+                     nucleus_on(p));
+  b.nucleus = nucleus_on(p);
   if (b.rc != MK_OK) return;
   if (p->drop_task > 0 && p->drop_task - 1 < (int)b.tasks.size()) {
     const int victim = p->drop_task - 1;
@@ -541,6 +558,7 @@ int commit_built(mk_plan* p, Built& b, cudaStream_t st, bool with_batch) {
   p->cta_start.swap(cs);
   p->cnt = b.cnt;
   p->open_start.swap(b.open);
+  p->nucleus_built = b.nucleus;
   p->replans++;
   return MK_OK;
 }
@@ -663,6 +681,10 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
     mk::set_last_error("mk_plan_create: temperature must be 0 (greedy) or a finite value whose inverse is finite");
     return MK_ERR_INVALID;
   }
+  if (!(o.top_p == 0.f || (o.top_p > 0.f && o.top_p <= 1.f))) {
+    mk::set_last_error("mk_plan_create: top_p must be in (0, 1] (0: off)");
+    return MK_ERR_INVALID;
+  }
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
@@ -678,6 +700,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->split_opt = o.split_pages;
   p->drop_task = o.debug_drop_task;
   p->inv_temp = o.temperature > 0.f ? 1.0f / o.temperature : 0.f;
+  p->top_p = o.top_p == 0.f ? 1.f : o.top_p;
   p->seed = o.seed;
   p->trace = o.trace >= 2 ? 2 : o.trace ? 1 : 0;
   p->timeout_ns = (unsigned long long)(o.timeout_us > 0 ? o.timeout_us : 2000000) * 1000ull;
@@ -801,35 +824,47 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   return MK_OK;
 }
 
-static int step_one(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
-  if (!p || !d_tokens || !d_next_token) return MK_ERR_INVALID;
+// n_steps decode steps in one launch; step s's next tokens go to row s of
+// d_next_token (rows io_stride apart) and feed step s + 1 on the device.
+static int steps_one(mk_plan* p, const int* d_tokens, int n_steps, float* d_logits, int* d_next_token,
+                     int io_stride, mk_stream stream) {
+  if (!p || !d_tokens || !d_next_token || n_steps < 1 || io_stride < p->B) return MK_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const Shape& s = p->s;
-  for (int b = 0; b < p->B; ++b) {
-    const int pos = p->seq[b];
-    if (pos / s.ps >= p->max_pages || pos >= p->rope_npos) return MK_ERR_CAPACITY;
-    const int pg = p->pt[(size_t)b * p->max_pages + pos / s.ps];
-    if (pg < 0 || pg >= p->num_pages) return MK_ERR_CAPACITY;
+  for (int b = 0; b < p->B; ++b) {   // every position this launch writes needs its page
+    for (int k = 0; k < n_steps; ++k) {
+      const int pos = p->seq[b] + k;
+      if (pos / s.ps >= p->max_pages || pos >= p->rope_npos) return MK_ERR_CAPACITY;
+      const int pg = p->pt[(size_t)b * p->max_pages + pos / s.ps];
+      if (pg < 0 || pg >= p->num_pages) return MK_ERR_CAPACITY;
+    }
   }
-  if (needs_replan(p)) {
+  if (needs_replan(p) || p->nucleus_built != nucleus_on(p)) {
     int rc = replan(p, st);
     if (rc != MK_OK) return rc;
   }
+  if (p->nucleus_built && !p->d_lg_keep &&
+      dalloc(p, &p->d_lg_keep, (size_t)p->bcap * s.V * sizeof(float)) != cudaSuccess)
+    return note_cuda(cudaGetLastError(), "nucleus logits buffer");
   // keep epoch * count far from 32-bit wrap-around
-  if ((unsigned long long)(p->epoch + 1) * 1024ull * 1024ull > 0x7fffffffull) {
+  if ((unsigned long long)(p->epoch + n_steps) * 1024ull * 1024ull > 0x7fffffffull) {
     if (cudaMemsetAsync(p->d_ctr, 0, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t), st) !=
         cudaSuccess)
       return MK_ERR_CUDA;
     p->epoch = 0;
   }
-  p->epoch++;
   fill_params(p);
   mk::Params P = p->P;
-  P.epoch = p->epoch;
+  P.epoch = p->epoch + 1;
+  P.nsteps = n_steps;
+  P.io_stride = io_stride;
   P.inv_temp = p->inv_temp;
   P.seed_lo = (uint32_t)(p->seed & 0xffffffffull);
   P.seed_hi = (uint32_t)(p->seed >> 32);
   P.slot0 = p->slot0;
+  P.top_p = p->top_p;
+  P.lg_keep = p->nucleus_built ? p->d_lg_keep : nullptr;
+  P.sdone_cnt = p->nucleus_built ? p->B : 1;
   P.tokens = d_tokens;
   P.logits = d_logits;
   P.next_token = d_next_token;
@@ -838,8 +873,14 @@ static int step_one(mk_plan* p, const int* d_tokens, float* d_logits, int* d_nex
     return note_cuda(cudaGetLastError(), "stage trace reset");
   cudaError_t e = mk::launch_megakernel(P, p->nb, p->C, p->smem, st);
   if (e != cudaSuccess) return note_cuda(e, "megakernel launch");
-  for (int b = 0; b < p->B; ++b) p->seq[b]++;
+  p->epoch += (uint32_t)n_steps;
+  for (int b = 0; b < p->B; ++b) p->seq[b] += n_steps;
   return MK_OK;
+}
+
+static int step_one(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
+  if (!p) return MK_ERR_INVALID;
+  return steps_one(p, d_tokens, 1, d_logits, d_next_token, p->B, stream);
 }
 
 static int step_host_one(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
@@ -1060,6 +1101,23 @@ int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next
   return MK_OK;
 }
 
+int mk_decode_steps(mk_plan* p, const int* d_tokens, int n_steps, float* d_logits, int* d_next_tokens,
+                    mk_stream stream) {
+  if (!p || p->subs.empty()) return steps_one(p, d_tokens, n_steps, d_logits, d_next_tokens, p ? p->B : 0, stream);
+  if (!d_tokens || !d_next_tokens || n_steps < 1) return MK_ERR_INVALID;
+  // requests of different sub-plans are independent: each sub-plan runs its
+  // n_steps in one launch of its own, writing its columns of the rows
+  const size_t M = mk::MAX_BATCH, V = p->s.V;
+  const int stride = p->group_B;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = steps_one(p->subs[i], d_tokens + i * M, n_steps, d_logits ? d_logits + i * M * V : nullptr,
+                             d_next_tokens + i * M, stride, stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
 int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
   if (!p || p->subs.empty()) return step_host_one(p, h_tokens, h_logits, h_next_token, stream);
   if (!h_tokens || !h_next_token) return MK_ERR_INVALID;
@@ -1118,6 +1176,16 @@ int mk_plan_set_sampling(mk_plan* p, float temperature, unsigned long long seed)
     s->inv_temp = it;
     s->seed = seed;
   }
+  return MK_OK;
+}
+
+int mk_plan_set_top_p(mk_plan* p, float top_p) {
+  if (!p || !(top_p > 0.f && top_p <= 1.f)) {
+    mk::set_last_error("mk_plan_set_top_p: top_p must be in (0, 1]");
+    return MK_ERR_INVALID;
+  }
+  p->top_p = top_p;
+  for (mk_plan* s : p->subs) s->top_p = top_p;
   return MK_OK;
 }
 

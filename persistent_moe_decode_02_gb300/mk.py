@@ -22,9 +22,9 @@ TRACE_SLOTS = ["fetch", "dep", "act", "stages", "done", "p_first", "p_last", "p_
                "mid1", "mid2"]
 
 EXPORTS = [
-    "mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
+    "mk_plan_create", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
     "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
-    "mk_last_error", "mk_decode_step_noalloc", "mk_plan_set_sampling", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
+    "mk_last_error", "mk_decode_step_noalloc", "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
     "mk_sched_commit", "mk_sched_abandon", "mk_sched_result", "mk_sched_forget", "mk_sched_stats",
     "mk_sched_destroy", "mk_serve_step",
 ]
@@ -52,7 +52,7 @@ class MkKv(ctypes.Structure):
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
-                ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong)]
+                ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("top_p", ctypes.c_float)]
 
 
 class MkError(RuntimeError):
@@ -76,6 +76,7 @@ def lib():
         L.mk_plan_create.argtypes = [ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights), ctypes.POINTER(MkKv),
                                      i32, p_int, p_int, i32, ctypes.POINTER(MkPlanOpts), ctypes.POINTER(vp)]
         L.mk_decode_step.argtypes = [vp, vp, vp, vp, vp]
+        L.mk_decode_steps.argtypes = [vp, vp, i32, vp, vp, vp]
         L.mk_decode_step_host.argtypes = [vp, p_int, ctypes.POINTER(ctypes.c_float), p_int, vp]
         L.mk_plan_update.argtypes = [vp, i32, p_int, p_int, i32, vp]
         L.mk_plan_sync.argtypes = [vp, vp]
@@ -92,6 +93,7 @@ def lib():
                                              ctypes.POINTER(MkKv), i32, p_int, p_int, i32, vp, vp, vp, vp, vp]
         i64, p_i64 = ctypes.c_longlong, ctypes.POINTER(ctypes.c_longlong)
         L.mk_plan_set_sampling.argtypes = [vp, ctypes.c_float, ctypes.c_ulonglong]
+        L.mk_plan_set_top_p.argtypes = [vp, ctypes.c_float]
         L.mk_sched_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
         L.mk_sched_submit.argtypes = [vp, i64, p_int, i32, i32, i32]
         L.mk_sched_next.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
@@ -104,9 +106,9 @@ def lib():
         L.mk_sched_destroy.restype = None
         L.mk_serve_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(MkModelDims), ctypes.POINTER(MkWeights),
                                     ctypes.POINTER(MkKv), ctypes.POINTER(MkPlanOpts), vp]
-        for f in ("mk_plan_create", "mk_decode_step", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
+        for f in ("mk_plan_create", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
                   "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc",
-                  "mk_plan_set_sampling", "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
+                  "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
                   "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -222,6 +224,15 @@ class Plan:
                                     ctypes.c_void_p(logits.data_ptr() if logits is not None else 0),
                                     ctypes.c_void_p(next_token.data_ptr()), _stream(stream))
 
+    def steps(self, tokens: torch.Tensor, n_steps: int, next_tokens: torch.Tensor,
+              logits: Optional[torch.Tensor] = None, stream=None) -> int:
+        """Enqueue n_steps decode steps in one launch (device buffers):
+        next_tokens int32 [n_steps, batch], logits float32 [n_steps, batch,
+        vocab] or None.  Returns the status code."""
+        return lib().mk_decode_steps(self.h, ctypes.c_void_p(tokens.data_ptr()), int(n_steps),
+                                     ctypes.c_void_p(logits.data_ptr() if logits is not None else 0),
+                                     ctypes.c_void_p(next_tokens.data_ptr()), _stream(stream))
+
     def step_host(self, tokens, next_token, logits=None, stream=None) -> int:
         """One step with host buffers (int32 / float32 CPU tensors, contiguous)."""
         tp = ctypes.cast(tokens.data_ptr(), ctypes.POINTER(ctypes.c_int))
@@ -248,6 +259,12 @@ class Plan:
         rc = lib().mk_plan_set_sampling(self.h, float(temperature), int(seed) & (2 ** 64 - 1))
         if rc != MK_OK:
             raise MkError("mk_plan_set_sampling", rc)
+
+    def set_top_p(self, top_p: float) -> None:
+        """Nucleus sampling (0 < top_p < 1) for the following sampled steps; 1: off."""
+        rc = lib().mk_plan_set_top_p(self.h, float(top_p))
+        if rc != MK_OK:
+            raise MkError("mk_plan_set_top_p", rc)
 
     def read_debug(self, what: int, out: torch.Tensor, stream=None) -> torch.Tensor:
         rc = lib().mk_plan_read_debug(self.h, what, ctypes.c_void_p(out.data_ptr()),

@@ -22,6 +22,7 @@ import synth
 from synth.device import DeviceModel, PagedKV, initial_tokens, kv_pages_needed
 
 NEAR_TIE = 1e-3
+NUCLEUS_MASS_TOL = 2e-3   # nucleus cut: mass tolerance between float32 (GPU) and float64 (oracle) masses
 LOGIT_REL_L2 = 1e-2
 LOGIT_MAX_ABS = 5e-2
 HIDDEN_REL_L2 = 1e-2
@@ -156,10 +157,12 @@ class OracleReplay:
         self.req = O.OracleRequest(rid, prior_len, make_prior(self.D, wl.seed, cache_prior), self.D.n_layers)
 
     def step(self, rec: StepRecord, b: int, rep: Report, sampling: Optional[tuple] = None) -> None:
-        """sampling = (temperature, seed, batch slot): the expected token is the
-        oracle's temperature draw (oracle/sample.py) instead of the greedy one,
-        and a difference is excused when the GPU token's oracle key is within
-        NEAR_TIE of the largest key."""
+        """sampling = (temperature, seed, batch slot[, top_p]): the expected
+        token is the oracle's temperature draw (oracle/sample.py), over the
+        nucleus when top_p < 1, instead of the greedy one.  A difference is
+        excused when the GPU token's oracle key is within NEAR_TIE of the
+        largest key, or (top_p < 1) when it is the draw over a nucleus whose
+        mass is within NUCLEUS_MASS_TOL of top_p."""
         O, D = self.O, self.D
         pos = self.req.length
         x = O.widen(self.W.embed_rows([int(rec.tok_in[b])])[0])
@@ -194,13 +197,31 @@ class OracleReplay:
             rep.max_logit_abs = max(rep.max_logit_abs, float((g - logits).abs().max()))
         gt = int(rec.next_tok[b])
         score = logits
+        allowed = None
         if sampling is not None:
             from oracle import sample as OS
-            T, seed, slot = sampling
+            T, seed, slot = sampling[:3]
+            top_p = sampling[3] if len(sampling) > 3 else 1.0
             score = OS.sample_keys(logits, T, seed, slot, pos)
-            nxt = OS.sample_token(logits, T, seed, slot, pos)
+            nxt = OS.sample_token(logits, T, seed, slot, pos, top_p=top_p)
+            if top_p < 1.0:
+                # the draw is over the nucleus; its cut depends on masses the
+                # two sides compute in different precisions, so every cut
+                # whose mass lies within NUCLEUS_MASS_TOL of top_p is allowed
+                lo = OS.nucleus(logits, T, max(top_p - NUCLEUS_MASS_TOL, 1e-12)).shape[0]
+                order = OS.nucleus(logits, T, min(top_p + NUCLEUS_MASS_TOL, 1.0)).tolist()
+                keys32 = score.to(torch.float32)
+                allowed = set()
+                for n in range(lo, len(order) + 1):
+                    sub = keys32[order[:n]]
+                    best = float(sub.max())
+                    allowed.add(min(v for v, k in zip(order[:n], sub.tolist()) if k == best))
+                score = torch.full_like(score, -math.inf)
+                score[order] = OS.sample_keys(logits, T, seed, slot, pos)[order]
         if gt != nxt:
-            if float(score[gt]) >= float(score.max()) - NEAR_TIE:
+            if allowed is not None and gt in allowed:
+                rep.token_excused += 1
+            elif float(score[gt]) >= float(score.max()) - NEAR_TIE:
                 rep.token_excused += 1
             else:
                 rep.token_unexcused += 1

@@ -277,6 +277,49 @@ def test_temperature_sampling_matches_oracle(capacity):
     run.plan.close()
 
 
+@pytest.mark.parametrize("capacity,T,top_p", [(0, 0.8, 0.5), (0, 0.05, 0.9), (10, 0.8, 0.7)])
+def test_nucleus_sampling_matches_oracle(capacity, T, top_p):
+    # Nucleus (top-p) sampling: the draw is the Gumbel-max of the temperature
+    # sampler restricted to the shortest prefix of rows (by logit) whose mass
+    # reaches top_p.  T = 0.8 leaves a wide distribution (the nucleus holds
+    # many rows and often excludes the plain draw); T = 0.05 a peaked one (a
+    # few rows).  Capacity 10: the same over a group of two sub-plans.
+    from oracle import sample as OS
+    from tests.gpu_util import OracleReplay
+    n = 3 if capacity == 0 else 10
+    ctx = [128, 37, 95, 16, 1, 60, 77, 5, 130, 40][:n]
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=ctx, steps=6)
+    seed = 0xABCDEF12345
+    run = GpuRun(wl, steps=6, **({"max_batch": capacity} if capacity else {}))
+    run.plan.set_sampling(T, seed)
+    run.plan.set_top_p(top_p)
+    recs = [run.step() for _ in range(6)]
+    rep = Report()
+    W = synth.SynthWeights(wl.dims, wl.seed)
+    plain_differs = 0
+    for b in range(n):
+        rr = OracleReplay(wl, run.reqs[b].rid, ctx[b], W=W)
+        for rec in recs:
+            pos = rr.req.length
+            rr.step(rec, b, rep, sampling=(T, seed, b, top_p))
+            lg = rec.logits[b].double()
+            plain_differs += int(rec.next_tok[b]) != OS.sample_token(lg, T, seed, b, pos)
+            assert int(rec.next_tok[b]) in OS.nucleus(lg, T, min(1.0, top_p + 2e-3)).tolist()
+    print(rep, "plain draw differs:", plain_differs)
+    rep.assert_ok()
+    assert rep.token_excused <= 2
+    if T >= 0.5:
+        assert plain_differs > 0          # the nucleus excludes some plain draws
+    run.plan.set_top_p(1.0)               # back to plain temperature sampling
+    rec = run.step()
+    for b in range(n):
+        want = OS.sample_token(rec.logits[b].double(), T, seed, b, run.reqs[b].length - 1)
+        keys = OS.sample_keys(rec.logits[b].double(), T, seed, b, run.reqs[b].length - 1)
+        got = int(rec.next_tok[b])
+        assert got == want or float(keys[got]) >= float(keys.max()) - 1e-3
+    run.plan.close()
+
+
 def test_serving_loop_sampling_is_reproducible():
     # The serving loop with temperature sampling set at plan creation: the
     # same requests and seed give the same outputs on a fresh server; another
@@ -310,3 +353,63 @@ def test_serving_loop_sampling_is_reproducible():
     assert serve(1.0, 42) == a
     assert serve(1.0, 43) != a
     assert serve(0.0, 42) != a
+
+
+def _multi_step_pair(wl, n, plan_kw=None, sampling=None, capacity=0, top_p=1.0):
+    """Two identical runs of `wl`: one of n single-step launches, one of a
+    single n-step launch.  Returns (tokens, logits, hidden) of each."""
+    from persistent_moe_decode_02_gb300 import mk
+    plan_kw = dict(plan_kw or {})
+    if capacity:
+        plan_kw["max_batch"] = capacity
+    out = []
+    for multi in (False, True):
+        run = GpuRun(wl, steps=n, **plan_kw)
+        if sampling is not None:
+            run.plan.set_sampling(*sampling)
+        if top_p < 1.0:
+            run.plan.set_top_p(top_p)
+        B, V = len(run.reqs), wl.dims.vocab
+        toks = torch.empty(n, B, dtype=torch.int32, device="cuda")
+        lg = torch.empty(n, B, V, dtype=torch.float32, device="cuda")
+        if multi:
+            assert run.plan.steps(run.tokens, n, toks, lg) == mk.MK_OK
+        else:
+            tok = run.tokens
+            for s in range(n):
+                assert run.plan.step(tok, toks[s], lg[s]) == mk.MK_OK
+                tok = toks[s]
+        assert run.plan.sync() == mk.MK_OK
+        hid = torch.empty(B, wl.dims.n_layers, wl.dims.hidden, dtype=torch.float32, device="cuda")
+        run.plan.read_debug(mk.MK_DBG_HIDDEN, hid)
+        lens = torch.empty(B, dtype=torch.int32, device="cuda")
+        run.plan.read_debug(mk.MK_DBG_SEQ_LENS, lens)
+        assert run.plan.sync() == mk.MK_OK
+        out.append((toks.cpu(), lg.cpu(), hid.cpu(), lens.cpu()))
+        run.plan.close()
+    return out
+
+
+@pytest.mark.parametrize("case", ["ragged_split", "group_12", "sampled", "nucleus", "mid"])
+def test_multi_step_launch_equals_single_steps(case):
+    # n decode steps in one launch, tokens fed back on the device, give the
+    # same bits as n launches of one step each: every token, every step's
+    # logits, the last step's hidden states and the lengths.  The ragged case
+    # crosses a page boundary inside the launch (request 0 at 31 tokens).
+    if case == "ragged_split":
+        wl = dataclasses.replace(synth.workload("tiny"), ctx=[31, 128, 60], steps=6)
+        (a, b) = _multi_step_pair(wl, 6, plan_kw={"split_pages": 2})
+    elif case == "group_12":
+        wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 37, 95, 5, 300, 16, 64, 200, 77, 0, 21], steps=3)
+        (a, b) = _multi_step_pair(wl, 3, capacity=12)
+    elif case == "sampled":
+        wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 45], steps=5)
+        (a, b) = _multi_step_pair(wl, 5, sampling=(0.8, 77))
+    elif case == "nucleus":
+        wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 45, 3], steps=5)
+        (a, b) = _multi_step_pair(wl, 5, sampling=(0.8, 77), top_p=0.6)
+    else:
+        wl = dataclasses.replace(synth.workload("mid"), steps=4)
+        (a, b) = _multi_step_pair(wl, 4)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
