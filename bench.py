@@ -27,7 +27,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode tok/s (bs1, 8K ctx) and achieved HBM GB/s as % of speed-of-light"
-KERNEL_SOURCES = ["persistent_moe_decode_02_gb300/csrc/megakernel.cu",
+KERNEL_SOURCES = ["persistent_moe_decode_02_gb300/csrc/megakernel.cuh",
+                  "persistent_moe_decode_02_gb300/csrc/megakernel.cu",
                   "persistent_moe_decode_02_gb300/csrc/mk_internal.h",
                   "persistent_moe_decode_02_gb300/csrc/plan.cu"]
 

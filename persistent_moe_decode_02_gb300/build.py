@@ -7,8 +7,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["megakernel.cu", "plan.cu", "noalloc.cu", "serve.cu"]
-HEADERS = [os.path.join(CSRC, "mk_internal.h"), os.path.join(ROOT, "include", "mk.h")]
+SOURCES = ["megakernel.cu", "megakernel_nuc.cu", "plan.cu", "noalloc.cu", "serve.cu"]
+HEADERS = [os.path.join(CSRC, "mk_internal.h"), os.path.join(CSRC, "megakernel.cuh"), os.path.join(ROOT, "include", "mk.h")]
 NVFLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
            "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 

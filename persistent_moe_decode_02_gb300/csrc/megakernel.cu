@@ -1,2764 +1,13 @@
-// Persistent MoE decode megakernel for GB300 (sm_103a).
-//
-// One CTA per SM stays resident for the whole decode step and walks its slice
-// of a host-prepared task list ("Cohere Publishes One-Kernel Server for North
-// Mini Code" — "One resident program, many small tasks"; "Inside the
-// Megakernel Serving Engine for North Mini Code" — architecture paragraph).
-//
-// Inside a CTA:
-//   * warp 8 (one lane) is the producer: it walks the CTA's tasks in order and
-//     streams each task's weight rows (or cached KV pages) into a ring of
-//     shared-memory stages with bulk async copies (cp.async.bulk, completion
-//     on an mbarrier).  It never waits for a task's activations, so immutable
-//     bytes land while the dependency is still pending ("What the scheduling
-//     change is meant to avoid", third bullet).  Only expert tiles wait, for
-//     the router's choice, since their addresses depend on it.
-//   * warps 0-7 are consumers: per task they wait on a global-memory
-//     dependency counter, load the small fp32 activation into shared memory,
-//     consume the ring stages (bf16 x fp32 dot products on CUDA cores, or
-//     online-softmax attention), write the outputs and bump the task's
-//     counter.  A tile starts when its own inputs are ready, not when a whole
-//     op is done ("False dependencies" bullet).
-// Every spin-wait has a time limit; on expiry the kernel records
-// MK_ERR_DEP_TIMEOUT in the status word, all CTAs drain and return.
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <math.h>
-#include <stdint.h>
-
-#include "mk.h"
-#include "mk_internal.h"
+// Host entry points of the megakernel: the launches, the RoPE table and the
+// shared-memory bookkeeping.  The device code is in megakernel.cuh; the
+// kernel instances with the nucleus-draw tasks are built in megakernel_nuc.cu,
+// so the greedy and temperature kernels carry none of that code.
+#include "megakernel.cuh"
 
 namespace mk {
+cudaError_t launch_megakernel_nuc(const Params& p, int nb, int grid, int smem, cudaStream_t st);
+int max_active_ctas_nuc(int nb, int smem);
 namespace {
-
-constexpr unsigned FULL = 0xffffffffu;
-constexpr int NCT = NCW * 32;  // consumer threads
-// Column-slice GEMV: consume two ring stages per pass, per call site.  It pays
-// off in the LM head's long tiles; in the short projection and expert tiles
-// waiting for the second stage before any math costs more than it saves.
-constexpr bool SP_PROJ = false, SP_MOE = false, SP_LM = true;
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-// Announce bytes of the current phase without arriving.
-__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Flag handoff between this CTA's consumers and its producer thread.
-__device__ __forceinline__ void st_release_cta(int* p, int v) {
-  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_cta(const int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
-// Non-blocking probe: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// Global -> shared bulk copy; completion counted on `bar` in bytes.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint32_t atom_add_release(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// Explicit shared-memory loads (32-bit shared addresses), so the hot loops
-// never go through generic addressing.  Volatile keeps them behind the
-// mbarrier waits that publish the data.
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float4 lds128f(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-  return v;
-}
-// Tensor-core helpers: 8x8 b16 matrix loads from shared memory and the
-// m16n8k16 bf16 MMA with fp32 accumulation (d += a . b).
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Task records are read-only during a step: read them through the L1.
-__device__ __forceinline__ Task ldg_task(const Task* t) {
-  const int4* q = reinterpret_cast<const int4*>(t);
-  const int4 a = __ldg(q), b = __ldg(q + 1), c = __ldg(q + 2);
-  Task r;
-  r.type = a.x; r.layer = a.y; r.a[0] = a.z; r.a[1] = a.w;
-  r.a[2] = b.x; r.a[3] = b.y; r.a[4] = b.z; r.a[5] = b.w;
-  r.a[6] = c.x; r.a[7] = c.y; r.wait_ctr = c.z; r.wait_cnt = (uint32_t)c.w;
-  return r;
-}
-
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
-// 32.32 fixed point for the router-logit sums (two's complement in 64 bits).
-__device__ __forceinline__ unsigned long long to_fixed(float v) {
-  return (unsigned long long)__double2ll_rn((double)v * 4294967296.0);
-}
-__device__ __forceinline__ float from_fixed(unsigned long long q) {
-  return (float)((double)(long long)q * 2.3283064365386963e-10);
-}
-
-// Word 0 of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
-// Numbers: As Easy as 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit
-// products, the key advanced by the Weyl constants before every round but
-// the first.
-__device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                              uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-    c0 = n0;
-    c1 = lo1;
-    c2 = n2;
-    c3 = lo0;
-  }
-  return c0;
-}
-
-// Standard Gumbel noise -log(-log(u)) for vocabulary row `row` of the request
-// in batch slot `slot` at position `pos`, u = ((x >> 9) + 1/2) * 2^-23 in
-// (0, 1) (exact in float32).  Kept out of line: only sampled steps call it.
-__device__ __noinline__ float gumbel_noise(uint32_t row, uint32_t pos, uint32_t slot, uint32_t k0, uint32_t k1) {
-  const uint32_t x = philox_w0(row, pos, slot, 0u, k0, k1);
-  const float u = ((float)(x >> 9) + 0.5f) * 1.1920928955078125e-07f;
-  return -logf(-logf(u));
-}
-
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Barrier over the 256 consumer threads (named barrier 1).
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// Same barrier, returning the OR of every consumer thread's predicate.
-__device__ __forceinline__ bool cbar_or(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
-__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-  return v;
-}
-
-// Sum of v[h] over the 32 lanes for the head h = (lane >> 2) & 7, by halving
-// exchanges (9 shuffles for 8 values instead of 40).
-__device__ __forceinline__ float reduce8(const float (&v)[8], int lane) {
-  float a[4];
-  const bool u16 = lane & 16;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float send = u16 ? v[i] : v[i + 4];
-    float keep = u16 ? v[i + 4] : v[i];
-    a[i] = keep + __shfl_xor_sync(FULL, send, 16);
-  }
-  float b[2];
-  const bool u8 = lane & 8;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    float send = u8 ? a[i] : a[i + 2];
-    float keep = u8 ? a[i + 2] : a[i];
-    b[i] = keep + __shfl_xor_sync(FULL, send, 8);
-  }
-  const bool u4 = lane & 4;
-  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(FULL, u4 ? b[0] : b[1], 4);
-  c += __shfl_xor_sync(FULL, c, 2);
-  c += __shfl_xor_sync(FULL, c, 1);
-  return c;
-}
-
-// Same for 4 values: lane l returns the 32-lane sum of v[(l >> 3) & 3].
-__device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
-  float a[2];
-  const bool u16 = lane & 16;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = u16 ? v[i] : v[i + 2];
-    const float keep = u16 ? v[i + 2] : v[i];
-    a[i] = keep + __shfl_xor_sync(FULL, send, 16);
-  }
-  const bool u8 = lane & 8;
-  float c = (u8 ? a[1] : a[0]) + __shfl_xor_sync(FULL, u8 ? a[0] : a[1], 8);
-  c += __shfl_xor_sync(FULL, c, 4);
-  c += __shfl_xor_sync(FULL, c, 2);
-  c += __shfl_xor_sync(FULL, c, 1);
-  return c;
-}
-
-// ------------------------------------------------------------------ shared state
-
-constexpr int MAX_UNION = MAX_BATCH * MAX_TOPK;   // distinct experts a step can select
-
-// A layer's distinct experts as the producer sees them.
-struct RouteCache {
-  int layer, U;
-  int exp[MAX_UNION];
-};
-
-struct Misc {
-  uint64_t full[MAX_STAGES];
-  uint64_t empty[MAX_STAGES];
-  int armed[MAX_STAGES];   // round in which the producer last armed a stage, -1 never
-  int dead;                // the status word was already set at kernel entry
-  int abort_flag;          // a warp of this CTA gave up
-  int ticket_last;
-  int pad;
-  float red[NCW * MAX_BATCH];
-  float inv[MAX_BATCH];    // 1 / rms of each activation row of the last norm (its GEMV epilogue scales by it)
-  float best_v[NCW * MAX_BATCH];
-  int best_i[NCW * MAX_BATCH];
-  int sel[MAX_BATCH * MAX_TOPK];
-  float selv[MAX_BATCH * MAX_TOPK];
-  float gate[MAX_BATCH * MAX_TOPK];
-  float rl[MAX_BATCH * MAX_EXPERTS];   // router logits of the layer being routed
-  int slot_of[MAX_EXPERTS];
-  int cnt_of[MAX_EXPERTS];
-  int r_U;                 // distinct experts of the routing in r_exp...
-  int r_layer;             // layer whose routing r_exp... holds after a gate/up task computed it (-1: none)
-  // routing of the current layer, cached per task
-  int r_exp[MAX_UNION];
-  int r_cnt[MAX_UNION];
-  int r_tok[MAX_UNION * MAX_BATCH];
-  int r_rank[MAX_UNION * MAX_BATCH];
-  // the producer's copies of a layer's distinct experts, one per cursor
-  RouteCache cp_route;
-  // nucleus draw (T_SAMPLE): target and running mass, key prefix, digit, cut, max logit
-  unsigned long long smp_tgt, smp_before;
-  uint32_t smp_prefix;
-  int smp_digit, smp_cut;
-  float smp_max;
-};
-
-struct Ring {
-  uint8_t* base;
-  Misc* m;
-  int nst, sb;
-  int stage, round;
-  __device__ void advance() {
-    if (++stage == nst) { stage = 0; ++round; }
-  }
-};
-
-// ------------------------------------------------------------------ failure handling
-
-__device__ __forceinline__ bool failed(const Params& p) {
-  return *(volatile int*)p.status != 0;
-}
-
-__device__ void set_error(const Params& p, int code, int task, int info) {
-  if (atomicCAS(p.status, 0, code) == 0) {
-    p.status[1] = task;
-    p.status[2] = blockIdx.x;
-    p.status[3] = info;
-    __threadfence();
-  }
-}
-
-// Wait until counter `ctr` holds epoch * cnt signals (bounded).
-__device__ bool wait_ctr(const Params& p, int ctr, uint32_t epoch, uint32_t cnt, int task) {
-  if (ctr < 0) return true;
-  const uint32_t* c = p.ctr + (size_t)ctr * CTR_STRIDE;
-  const uint32_t target = epoch * cnt;
-  if ((int32_t)(ld_acquire(c) - target) >= 0) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 1;; ++it) {
-    if ((int32_t)(ld_acquire(c) - target) >= 0) return true;
-    if ((it & 31) == 0) {
-      if (failed(p)) return false;
-      if (gtimer() - t0 > p.timeout_ns) {
-        set_error(p, MK_ERR_DEP_TIMEOUT, task, ctr);
-        return false;
-      }
-    }
-    if (it > 256) __nanosleep(100);
-  }
-}
-
-// Bounded mbarrier parity wait; gives up when this CTA or any CTA failed.
-__device__ bool mbar_wait(const Params& p, Misc* m, uint64_t* bar, uint32_t parity, int info) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15) == 0) {
-      if (*(volatile int*)&m->abort_flag || failed(p)) return false;
-      if (gtimer() - t0 > p.timeout_ns) {
-        set_error(p, MK_ERR_DEP_TIMEOUT, -1, info);
-        return false;
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ stage geometry
-// Producer and consumers derive the same stage sequence from the task and the
-// same device state, so they agree on what every stage holds.
-
-__device__ __forceinline__ int rows_per_stage(const Params& p, int K) {
-  return max(1, p.stage_bytes / (K * 2));
-}
-
-__device__ __forceinline__ int pages_per_stage(const Params& p) {
-  return max(1, p.stage_bytes / (2 * p.ps * p.d * 2));
-}
-
-__device__ __forceinline__ int pairs_per_stage(const Params& p) {
-  return max(1, p.stage_bytes / (4 * p.H));
-}
-
-// Token range [tok0, tok1) of an attention task at the current lengths.
-__device__ __forceinline__ void attn_range(const Params& p, const Task& t, int pos, int& tok0,
-                                           int& tok1) {
-  tok0 = t.a[2] * p.ps;
-  tok1 = (t.a[3] < 0) ? pos + 1 : min(t.a[3] * p.ps, pos + 1);
-}
-
-// Flattened (distinct expert, ffn row) range of gate/up tile a0 of a1.
-__device__ __forceinline__ void gu_range(const Params& p, const Task& t, int U, long long& q0,
-                                         long long& q1) {
-  const unsigned tot = (unsigned)U * (unsigned)p.F, i = (unsigned)t.a[0], n = (unsigned)t.a[1];
-  if ((unsigned long long)tot * n < (1ull << 32)) {   // 32-bit division: the common case
-    q0 = tot * i / n;
-    q1 = tot * (i + 1) / n;
-  } else {
-    q0 = (long long)tot * i / n;
-    q1 = (long long)tot * (i + 1) / n;
-  }
-}
-
-// Above batch 1 the distinct experts serve different numbers of token slots,
-// and a unit's work grows with them: the ranges are cut by cost instead, a
-// unit of expert u costing GU_UNIT_COST + cnt[u] (its weight rows, then one per
-// slot).  When the cut could give some tile more units than its coefficient
-// scratch holds (cf_pairs), the plain even cut is kept.  Producer and
-// consumers call this with the same routing, so they agree.
-constexpr long long GU_UNIT_COST = 1;
-
-__device__ __forceinline__ long long gu_cut(int U, int F, const int* cnt, long long T) {
-  long long acc = 0;
-  for (int u = 0; u < U; ++u) {
-    const long long w = GU_UNIT_COST + cnt[u], span = (long long)F * w;
-    if (T <= acc + span) return (long long)u * F + min((long long)F, (T - acc + w - 1) / w);
-    acc += span;
-  }
-  return (long long)U * F;
-}
-
-template <int NB>
-__device__ __forceinline__ void gu_range_w(const Params& p, const Task& t, int U, const int* cnt, long long& q0,
-                                           long long& q1) {
-  if constexpr (NB > 1) {
-    long long tot = 0;
-    int cmin = 1 << 30;
-    for (int u = 0; u < U; ++u) {
-      tot += GU_UNIT_COST + cnt[u];
-      cmin = min(cmin, cnt[u]);
-    }
-    tot *= p.F;
-    const long long n = t.a[1], i = t.a[0];
-    if (U > 0 && tot / (n * (GU_UNIT_COST + cmin)) + 2 <= p.cf_pairs) {
-      q0 = gu_cut(U, p.F, cnt, tot * i / n);
-      q1 = gu_cut(U, p.F, cnt, tot * (i + 1) / n);
-      return;
-    }
-  }
-  gu_range(p, t, U, q0, q1);
-}
-
-__device__ __forceinline__ const int* route_of(const Params& p, int l) {
-  return p.route + (size_t)l * p.rm.ints;
-}
-
-// ------------------------------------------------------------------ producer
-
-// The producer's view of one task: how many ring stages it fills and where
-// each stage's bytes come from.  The consumer walks the same geometry.
-struct Geo {
-  int type, nst, l;
-  // row tasks
-  const uint16_t* W;
-  const uint16_t* W2;   // expert tile: the layer's down matrix (W: its gate/up matrix)
-  int K, r0, r1, rps, halves;
-  // attention
-  int pg0, pg1, ppg, b, g;
-  uint32_t PB;
-  // expert tile: the routing cache it reads, its flattened (distinct expert,
-  // ffn unit) range, gate/up stages first (pps units each), then down stages
-  // (rpw units each, rows of the transposed down matrix)
-  const RouteCache* rc;
-  int q0, q1;
-  int pps, rpw, nst_gu;
-  int cs, cu, cf;   // gate/up cursor: stage cs starts at unit cf of distinct expert cu
-  int ws, wu, wf;   // down cursor, the same for down stage ws
-};
-
-// Producer: one thread that walks the CTA's tasks and fills the ring with
-// bulk copies, paced by the consumers' releases: a task's weights are in
-// flight as soon as ring slots free up, long before its activations exist.
-// Kept small: the SM's instruction cache is shared with the consumer warps.
-template <int NB>
-struct Producer {
-  static constexpr bool kSplit = NB > 2;   // the O projection may run in K halves only above batch 2
-  const Params& p;
-  Ring r;
-  uint64_t pol;
-  int ti = 0;
-  int step = 0;           // step of this launch being walked (0 .. nsteps - 1)
-  long long cp_lin = 0;   // ring stages filled so far (stage timeline index)
-
-  __device__ void mark(int k) {
-    if (p.trace) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
-  }
-
-  // Routing of layer l into cache c (once per layer and step): this CTA's
-  // expert tile computes it and hands it over in shared memory (bounded
-  // wait), tagged with the layer's index counted over the launch's steps.
-  __device__ bool route_ready(RouteCache* c, int l0, int task) {
-    const int l = step * p.L + l0;
-    if (c->layer == l) return true;
-    Misc* m = r.m;
-    if (ld_acquire_cta(&m->r_layer) != l) {
-      // poll with plain loads (no fence, no sleep: the table is a few hundred
-      // cycles away and the first copies wait on it), acquire once seen
-      const uint64_t t0 = gtimer();
-      for (uint32_t it = 1; *(volatile int*)&m->r_layer != l; ++it) {
-        if ((it & 63) == 0) {
-          if (*(volatile int*)&m->abort_flag || failed(p)) return false;
-          if (gtimer() - t0 > p.timeout_ns) {
-            set_error(p, MK_ERR_DEP_TIMEOUT, task, -5);
-            return false;
-          }
-        }
-      }
-      if (ld_acquire_cta(&m->r_layer) != l) return false;
-    }
-    const int U = m->r_U;
-    for (int u0 = 0; u0 < U; u0 += 8) {   // eight loads in flight
-      int e[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) e[i] = u0 + i < U ? m->r_exp[u0 + i] : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (u0 + i < U) c->exp[u0 + i] = e[i];
-    }
-    c->U = U;
-    c->layer = l;
-    return true;
-  }
-
-  // Stage layout of expert tile t for U distinct experts: its flattened (distinct
-  // expert, ffn unit) range, gate/up stages of pps units, then down stages of
-  // rpw units, each within one expert; both cursors at their first stage.
-  __device__ void moe_layout(const Task& t, Geo& q, int U, const int* cnt) {
-    long long g0, g1;
-    gu_range_w<NB>(p, t, U, cnt, g0, g1);
-    q.q0 = (int)g0;
-    q.q1 = (int)g1;
-    q.pps = pairs_per_stage(p);
-    q.rpw = rows_per_stage(p, p.H);
-    const int F = p.F;
-    int ngu = 0, nwd = 0;
-    for (int u = q.q0 / F; u * F < q.q1; ++u) {
-      const int fa = max(q.q0 - u * F, 0), fb = min(F, q.q1 - u * F);
-      ngu += (fb - fa + q.pps - 1) / q.pps;
-      nwd += (fb - fa + q.rpw - 1) / q.rpw;
-    }
-    q.nst_gu = ngu;
-    q.nst = ngu + nwd;
-    q.cs = q.ws = 0;
-    q.cu = q.wu = q.q0 / F;
-    q.cf = q.wf = q.q0 - q.cu * F;
-  }
-
-  // Geometry of task t; false on a routing wait that timed out or gave up,
-  // or for an unknown task type.
-  __device__ bool geo(const Task& t, Geo& q, RouteCache* c, int task) {
-    q.type = t.type;
-    q.l = t.layer;
-    const int l = t.layer;
-    switch (t.type) {
-      case T_QKV: case T_OPROJ: case T_LM: {
-        q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : p.lm_head;
-        // the O projection's K halves (o_halves = 2) stream one after the other
-        q.halves = kSplit && t.type == T_OPROJ ? p.o_halves : 1;
-        q.K = t.type == T_OPROJ ? p.nq * p.d / q.halves : p.H;
-        q.r0 = t.a[0];
-        q.r1 = t.a[1];
-        q.rps = rows_per_stage(p, q.K);
-        q.nst = q.halves * ((q.r1 - q.r0 + q.rps - 1) / q.rps) + (t.type == T_OPROJ ? 1 : 0);   // + the router stage
-        return true;
-      }
-      case T_ATTN: {
-        q.b = t.a[0];
-        q.g = t.a[1];
-        const int pos = __ldcg(p.seq_len + q.b) + step;
-        int tok0, tok1;
-        attn_range(p, t, pos, tok0, tok1);
-        q.ppg = pages_per_stage(p);
-        q.PB = (uint32_t)p.ps * p.d * 2;
-        q.pg0 = tok0 / p.ps;
-        q.pg1 = (tok1 + p.ps - 1) / p.ps;
-        q.nst = (q.pg1 - q.pg0 + q.ppg - 1) / q.ppg;
-        return true;
-      }
-      case T_MOE: {
-        // Everything but the expert ids depends on the routing only through U,
-        // the number of distinct experts: lay out the stages for the largest U
-        // the batch can have (always the U of one request) and load the layer's
-        // expert matrices before the wait; redo the layout if U differs.
-        q.W = p.w_gate_up[l];
-        q.W2 = p.w_down[l];
-        asm volatile("" ::"l"(q.W), "l"(q.W2));
-        const int Ug = min(p.E, p.B * p.k);
-        if constexpr (NB == 1) moe_layout(t, q, Ug, nullptr);
-        if (!route_ready(c, l, task)) return false;
-        q.rc = c;
-        if constexpr (NB == 1) {
-          if (c->U != Ug) moe_layout(t, q, c->U, nullptr);
-        } else {
-          // the cut depends on the token counts: the consumers' table (r_cnt)
-          // holds this layer's until this CTA's next expert task routes
-          moe_layout(t, q, c->U, r.m->r_cnt);
-        }
-        return true;
-      }
-      case T_RED:      // no weights: reads only the expert tiles' partials
-      case T_SAMPLE:   // no weights: reads the kept logits
-      case T_COMB: {   // no weights: reads only partials
-        q.nst = 0;
-        return true;
-      }
-      default: return false;
-    }
-  }
-
-  // Calls f(src, bytes, dst_offset) for each contiguous piece of stage s.
-  // Gate/up stages are walked with a cursor kept in the geometry, so stages
-  // visited in order cost O(1) each.
-  template <class F>
-  __device__ void segs(Geo& q, int s, F f) {
-    const int l = q.l;
-    switch (q.type) {
-      case T_QKV: case T_OPROJ: case T_LM: {
-        if (q.type == T_OPROJ && s == q.nst - 1) {
-          // the O tile's router stage: rows [r0, r1) of the transposed router,
-          // then the 16-byte window of the FFN norm's gain around the same rows
-          const int nr = q.r1 - q.r0;
-          f(p.router[l] + (size_t)q.r0 * p.E, (uint32_t)nr * p.E * 2, 0u);
-          const uint32_t w0 = (uint32_t)q.r0 * 2 / 16 * 16, w1 = ((uint32_t)q.r1 * 2 + 15) / 16 * 16;
-          f(reinterpret_cast<const uint8_t*>(p.ffn_norm[l]) + w0, w1 - w0, (uint32_t)router_stage_gain_off(nr, p.E));
-          break;
-        }
-        if (!kSplit || q.halves == 1) {
-          const int s0 = q.r0 + s * q.rps;
-          const int n = min(q.rps, q.r1 - s0);
-          f(q.W + (size_t)s0 * q.K, (uint32_t)n * q.K * 2, 0u);
-        } else {   // K half h of rows s0 .. s0 + n: one copy per row
-          const int per = (q.r1 - q.r0 + q.rps - 1) / q.rps, h = s / per;
-          const int s0 = q.r0 + (s - h * per) * q.rps;
-          const int n = min(q.rps, q.r1 - s0);
-          for (int i = 0; i < n; ++i)
-            f(q.W + (size_t)(s0 + i) * q.K * q.halves + (size_t)h * q.K, (uint32_t)q.K * 2, (uint32_t)i * q.K * 2);
-        }
-        break;
-      }
-      case T_ATTN: {
-        const int pg = q.pg0 + s * q.ppg;
-        const int n = min(q.ppg, q.pg1 - pg);
-        const int* pt = p.page_table + (size_t)q.b * p.max_pages;
-        for (int i = 0; i < n; ++i) {
-          const size_t off = ((size_t)pt[pg + i] * p.nkv + q.g) * p.ps * p.d;
-          f(p.k_pool[l] + off, q.PB, (uint32_t)i * q.PB);
-          f(p.v_pool[l] + off, q.PB, (uint32_t)(q.ppg + i) * q.PB);
-        }
-        break;
-      }
-      case T_MOE: {
-        const int F = p.F, H = p.H;
-        if (s < q.nst_gu) {
-          if (s < q.cs) {   // rewind
-            q.cs = 0;
-            q.cu = q.q0 / F;
-            q.cf = q.q0 - q.cu * F;
-          }
-          while (q.cs < s) {   // advance one stage: pps units, or to the end of this expert's range
-            const int fb = min(F, q.q1 - q.cu * F);
-            q.cf += q.pps;
-            if (q.cf >= fb) {
-              ++q.cu;
-              q.cf = 0;
-            }
-            ++q.cs;
-          }
-          const int fb = min(F, q.q1 - q.cu * F);
-          const int n = min(q.pps, fb - q.cf);
-          const uint16_t* We = q.W + (size_t)q.rc->exp[q.cu] * 2 * F * H;   // rows 2f, 2f+1
-          f(We + (size_t)2 * q.cf * H, (uint32_t)n * 2 * H * 2, 0u);
-        } else {
-          const int s2 = s - q.nst_gu;
-          if (s2 < q.ws) {
-            q.ws = 0;
-            q.wu = q.q0 / F;
-            q.wf = q.q0 - q.wu * F;
-          }
-          while (q.ws < s2) {
-            const int fb = min(F, q.q1 - q.wu * F);
-            q.wf += q.rpw;
-            if (q.wf >= fb) {
-              ++q.wu;
-              q.wf = 0;
-            }
-            ++q.ws;
-          }
-          const int fb = min(F, q.q1 - q.wu * F);
-          const int n = min(q.rpw, fb - q.wf);
-          const uint16_t* Wd = q.W2 + ((size_t)q.rc->exp[q.wu] * F + q.wf) * H;   // [E][F][H]
-          f(Wd, (uint32_t)n * H * 2, 0u);
-        }
-        break;
-      }
-    }
-  }
-
-  // Before a later step's first KV page copy: the previous step's K/V appends
-  // must be visible to the bulk-copy engine.  Wait (bounded) for that step's
-  // done counter, then order the async proxy after it.
-  __device__ bool kv_ready(int task) {
-    if (!wait_ctr(p, p.cm.sdone, p.epoch + (uint32_t)step - 1u, (uint32_t)p.sdone_cnt, task)) return false;
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return true;
-  }
-
-  __device__ void run(int t0, int t1) {
-    Misc* m = r.m;
-    m->cp_route.layer = -1;
-    for (step = 0; step < p.nsteps; ++step) {
-      bool kv_seen = step == 0;
-      for (ti = t0; ti < t1; ++ti) {
-        if (!run_task(ti, kv_seen)) return;
-      }
-    }
-  }
-
-  __device__ bool run_task(int ti_, bool& kv_seen) {
-    Misc* m = r.m;
-    ti = ti_;
-    {
-      if (failed(p)) return false;
-      const Task t = ldg_task(p.tasks + ti);
-      mark(TR_P_START);
-      Geo q;
-      if (!geo(t, q, &m->cp_route, ti)) {
-        if (t.type < T_QKV || t.type > T_LAST) set_error(p, MK_ERR_INVALID, ti, t.type);
-        m->abort_flag = 1;
-        return false;
-      }
-      if (t.type == T_ATTN && q.nst > 0 && !kv_seen) {
-        if (!kv_ready(ti)) {
-          m->abort_flag = 1;
-          return false;
-        }
-        kv_seen = true;
-      }
-      for (int s = 0; s < q.nst; ++s) {
-        // claim the slot once the consumers released it, then for each piece
-        // announce its bytes before the copy; the closing arrival completes
-        // the phase when the last byte lands
-        const uint32_t par = (r.round & 1) ^ 1;
-        if (!mbar_wait(p, m, &m->empty[r.stage], par, -3)) {
-          m->abort_flag = 1;
-          return false;
-        }
-        if (s == 0) mark(TR_P_FIRST);
-        uint64_t* bar = &m->full[r.stage];
-        uint8_t* dst = r.base + (size_t)r.stage * r.sb;
-        m->armed[r.stage] = r.round;
-        segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
-          mbar_expect_tx_only(bar, b);
-          bulk_g2s(dst + off, src, b, bar, pol);
-        });
-        mbar_arrive(bar);
-        if (p.strace && cp_lin < STRACE_CAP) {
-          unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + cp_lin) * STRACE_SLOTS;
-          rec[0] = gtimer();
-          rec[3] = (unsigned long long)ti;
-        }
-        r.advance();
-        ++cp_lin;
-      }
-      mark(TR_P_LAST);
-    }
-    return true;
-  }
-};
-
-// ------------------------------------------------------------------ consumer pieces
-
-// GEMV epilogue shared by the projection and expert tasks, so that one GEMV
-// body (inlined at one call site per row kind) serves all of them.  inv holds
-// the RMS-norm scale of each activation row (the GEMV ran on x * gain):
-//   STORE:  out[j * ld + row] = inv[j] * s
-//   RESID:  out[j * ld + row] = res[j * res_ld + row - res_r0] += s   (no norm; the
-//           sum also replaces the residual in res, for the O tile's router share)
-//   SWIGLU: (rows are gate/up pairs: row = ffn unit f, s = gate, s2 = up; the
-//           token slot j reads activation row toks[j], c = inv[toks[j]])
-//           out[(f + base) * ld + j] = gate_w[toks[j] * k + ranks[j]] * silu(c * s) * (c * s2)
-struct GemvEpi {
-  enum Kind { STORE, RESID, SWIGLU };
-  int kind;
-  float* out;
-  int ld;
-  float* res;
-  int res_ld, res_r0;
-  int base, k;
-  const int* toks;
-  const int* ranks;
-  const float* gate_w;
-  const float* inv;
-  __device__ __forceinline__ void operator()(int row, int j, float s, float s2) const {
-    switch (kind) {
-      case STORE: out[(size_t)j * ld + row] = inv[j] * s; break;
-      case RESID: {
-        float* r = res + j * res_ld + row - res_r0;
-        const float v = *r + s;
-        *r = v;
-        out[(size_t)j * ld + row] = v;
-        break;
-      }
-      default: {
-        const int tj = toks[j];
-        const float c = inv[tj], g = c * s;
-        out[(size_t)(row + base) * ld + j] = gate_w[tj * k + ranks[j]] * (g / (1.0f + expf(-g)) * (c * s2));
-      }
-    }
-  }
-};
-
-// A projection task's GEMV: rows [r0, r1) of a K-wide matrix against the activations.
-struct ProjGemv {
-  int K, r0, r1;
-  GemvEpi epi;
-};
-
-template <int NB>
-struct Consumer {
-  const Params& p;
-  Ring r;
-  float* act;
-  Misc* m;
-  float* scr;      // after the misc struct: an H-row tile's residual rows, or an expert tile's coefficients
-  float* psum;   // per-warp partial sums of wide-row GEMVs: [2 windows][NCW][WIN_ROWS][NB]
-  static constexpr int WIN_ROWS = win_rows(NB);
-  int ct, cw, lane;
-  int ti = 0;
-  int step = 0;      // step of this launch being run (0 .. nsteps - 1)
-  uint32_t epoch = 0;   // its counter epoch: p.epoch + step
-  int lm_done = 0;   // LM-head tiles this CTA finished in this step (its last task is the last of them)
-
-  __device__ void mark(int k) {
-    if (p.trace && ct == 0) p.trace[(size_t)ti * TRACE_SLOTS + k] = gtimer();
-  }
-
-  // ---- ring access (per warp)
-  int nstage_seen = 0;   // stages of the current task seen by this warp (timeline only)
-
-  __device__ const uint8_t* wait_stage(bool& ab) {
-    if (ab) return nullptr;
-    if (!mbar_wait(p, m, &m->full[r.stage], r.round & 1, -4)) {
-      ab = true;
-      m->abort_flag = 1;
-      return nullptr;
-    }
-    if (p.trace) {
-      mark(nstage_seen == 0 ? TR_S_FIRST : TR_S_LAST);
-      ++nstage_seen;
-    }
-    if (p.strace && ct == 0) stage_stamp(1);
-    return r.base + (size_t)r.stage * r.sb;
-  }
-  __device__ void release_stage(bool ab) {
-    __syncwarp();
-    if (!ab && lane == 0) mbar_arrive(&m->empty[r.stage]);
-    if (p.strace && ct == 0) stage_stamp(2);
-    r.advance();
-  }
-  // Release an earlier stage (slot `stage` of round `round`) without moving the ring.
-  __device__ void release_at(bool ab, int stage, int round) {
-    __syncwarp();
-    if (!ab && lane == 0) mbar_arrive(&m->empty[stage]);
-    if (p.strace && ct == 0) {
-      const long long lin = (long long)round * r.nst + stage;
-      if (lin < STRACE_CAP) {
-        unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + lin) * STRACE_SLOTS;
-        rec[2] = gtimer();
-        rec[5] = (unsigned long long)clock64();
-      }
-    }
-  }
-  __device__ void stage_stamp(int k) {
-    const long long lin = (long long)r.round * r.nst + r.stage;
-    if (lin < STRACE_CAP) {
-      unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + lin) * STRACE_SLOTS;
-      rec[k] = gtimer();
-      rec[3 + k] = (unsigned long long)clock64();
-    }
-  }
-
-  // ---- activations
-  // act[b * H + i] = x_b[i] * gamma[i] for b < B, with x_b read four floats at
-  // a time by src(b, i4), and m->inv[b] = 1 / sqrt(mean(x_b^2) + eps): the
-  // norm's scale is applied to the GEMV sums (the map is linear), so the gain
-  // and x come in one L2 round trip and the activations are written once.
-  // m->inv is written after a barrier; every caller passes another barrier
-  // before its GEMV reads it.
-  template <class Src4>
-  __device__ void fill_rmsnorm(const uint16_t* gamma, Src4 src) {
-    const int H = p.H, H4 = H >> 2, B = p.B;
-    if constexpr (NB == 1) {
-      float ss = 0.f;
-      float4* dst = reinterpret_cast<float4*>(act);
-#pragma unroll 4
-      for (int i = ct; i < H4; i += NCT) {
-        const float4 v = src(0, i);
-        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
-        dst[i] = make_float4(v.x * bf_lo(gb.x), v.y * bf_hi(gb.x), v.z * bf_lo(gb.y), v.w * bf_hi(gb.y));
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) m->red[cw] = ss;
-    } else {
-      // every request's loads of a column group go out together: one round trip, not B
-      float ss[NB];
-#pragma unroll
-      for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-      for (int i = ct; i < H4; i += NCT) {
-        float4 v[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) v[b] = b < B ? src(b, i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gamma) + i);
-        const float g0 = bf_lo(gb.x), g1 = bf_hi(gb.x), g2 = bf_lo(gb.y), g3 = bf_hi(gb.y);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b < B) {
-            reinterpret_cast<float4*>(act + (size_t)b * H)[i] =
-                make_float4(v[b].x * g0, v[b].y * g1, v[b].z * g2, v[b].w * g3);
-            ss[b] = fmaf(v[b].x, v[b].x, fmaf(v[b].y, v[b].y, fmaf(v[b].z, v[b].z, fmaf(v[b].w, v[b].w, ss[b]))));
-          }
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (b < B) {
-          const float t = warp_sum(ss[b]);
-          if (lane == 0) m->red[b * NCW + cw] = t;
-        }
-      }
-    }
-    cbar();
-    if (ct < B) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
-      m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
-    }
-  }
-
-  // Token id of request b, checked: an id outside [0, vocab) records
-  // MK_ERR_INVALID and reads row 0 instead of faulting.
-  __device__ int token(int b) const {
-    const int tok = step == 0 ? __ldcg(p.tokens + b) : __ldcg(p.next_token + (size_t)(step - 1) * p.io_stride + b);
-    if (tok < 0 || tok >= p.V) {
-      set_error(p, MK_ERR_INVALID, -1, tok);
-      return 0;
-    }
-    return tok;
-  }
-
-  __device__ float4 x_in4(int l, int b, int i4) const {
-    if (l == 0) {
-      const int tok = token(b);
-      const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.embed + (size_t)tok * p.H) + i4);
-      return make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
-    }
-    return __ldcg(reinterpret_cast<const float4*>(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H) + i4);
-  }
-
-  __device__ float x_in(int l, int b, int i) const {
-    if (l == 0) return bf2f(p.embed[(size_t)token(b) * p.H + i]);
-    return __ldcg(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H + i);
-  }
-
-  // dot of one 16-byte bf16 granule with 8 activations
-  __device__ __forceinline__ static float dot8(const uint4 wv, uint32_t a) {
-    return dot8r(wv, lds128f(a), lds128f(a + 16));
-  }
-  __device__ __forceinline__ static float dot8r(const uint4 wv, const float4 x0, const float4 x1) {
-    float s0 = bf_lo(wv.x) * x0.x;
-    float s1 = bf_hi(wv.x) * x0.y;
-    s0 = fmaf(bf_lo(wv.y), x0.z, s0);
-    s1 = fmaf(bf_hi(wv.y), x0.w, s1);
-    s0 = fmaf(bf_lo(wv.z), x1.x, s0);
-    s1 = fmaf(bf_hi(wv.z), x1.y, s1);
-    s0 = fmaf(bf_lo(wv.w), x1.z, s0);
-    s1 = fmaf(bf_hi(wv.w), x1.w, s1);
-    return s0 + s1;
-  }
-
-  // ---- GEMV over rows [r0, r1) of a K-wide bf16 matrix streamed through the
-  // ring, against nb activation rows (act row map[j], or j when map is null).
-  //
-  // Wide rows (K a multiple of 2048, the model's hidden and attention widths):
-  // warp w owns the 256-column slices w, w+8, ...; per stage it accumulates up
-  // to 8 rows at once (independent chains), reduces them across its lanes and
-  // parks one partial per (warp, row) in a 32-row smem window.  When a window
-  // fills (or the range ends) the consumer threads sum the 8 warp partials in
-  // warp order -- the same order every run -- and call the epilogue.
-  // Narrow rows (other K): warp w owns rows w, w+8, ..., up to 8 at a time,
-  // its lanes span the whole row, and it calls the epilogue itself.
-  //
-  // PAIRS: rows come as (gate, up) pairs 2f, 2f+1 and the epilogue is
-  // epi(f, j, gate_sum, up_sum); otherwise epi(row, j, sum).
-  // Window flush of the column-slice GEMV: sum the 8 warps' partials of the
-  // window's rows in warp order and hand each (row or pair, batch row) to the epilogue.
-  template <class Epi>
-  __device__ __forceinline__ void gemv_flush(bool pairs, bool ab, int buf, int wbase, int wrow, int nb, Epi& epi) {
-    cbar();
-    if (ab) return;
-    const float* pb = psum + (size_t)buf * NCW * WIN_ROWS * NB;
-    const int units = pairs ? wrow >> 1 : wrow;
-    for (int x = ct; x < units * nb; x += NCT) {
-      const int u = x / nb, j = x - u * nb;
-      if (pairs) {
-        float g = 0.f, up = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-          g += pb[((size_t)w * WIN_ROWS + 2 * u) * NB + j];
-          up += pb[((size_t)w * WIN_ROWS + 2 * u + 1) * NB + j];
-        }
-        epi((wbase >> 1) + u, j, g, up);
-      } else {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) s += pb[((size_t)w * WIN_ROWS + u) * NB + j];
-        epi(wbase + u, j, s, 0.f);
-      }
-    }
-  }
-
-  template <bool PAIRS, bool SP, class Epi>
-  __device__ bool gemv(int K, int r0, int r1, const float* a, int stride, const int* map, int nb, bool ab,
-                       Epi epi) {
-    const int rps = PAIRS ? 2 * pairs_per_stage(p) : rows_per_stage(p, K);
-    const int ng = K >> 3;
-    const uint32_t rowb = (uint32_t)K * 2;
-    uint32_t aoff[NB];  // shared address of each activation row
-#pragma unroll
-    for (int j = 0; j < NB; ++j) aoff[j] = smem_u32(a) + (uint32_t)((j < nb ? (map ? map[j] : j) : 0) * stride * 4);
-    if ((K & 2047) == 0) {
-      const int spw = K >> 11;  // granules per lane per row
-      int wbase = r0, wrow = 0, buf = 0;
-      for (int s0 = r0; s0 < r1;) {
-        const int n = min(rps, r1 - s0);
-        if constexpr (SP && NB <= 2) {
-          // two stages per pass when a second one follows and both fit the
-          // window: twice the independent work between reductions
-          const int n2 = min(rps, r1 - s0 - rps);
-          if ((rps == 8 || rps == 4) && n == rps && n2 > 0 && wrow + n + n2 <= WIN_ROWS) {
-            const uint8_t* sa = wait_stage(ab);
-            const int ga = r.stage, ra = r.round;
-            r.advance();
-            const uint8_t* sb = wait_stage(ab);
-            if (sa && sb) {
-              const uint32_t ta = smem_u32(sa), tb = smem_u32(sb);
-              float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
-              if (rps == 8) {
-                // 16 rows: 8 from each stage, one granule column per lane (K = 2048)
-                float part[16][NB];
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
-                for (int sw = 0; sw < spw; ++sw) {
-                  const int gi = (cw + NCW * sw) * 32 + lane;
-                  float4 x0[NB], x1[NB];
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) {
-                    x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  }
-                  uint4 wv[16];
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) wv[q] = lds128(ta + (uint32_t)q * rowb + gi * 16);
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-                    wv[8 + q] = q < n2 ? lds128(tb + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                  for (int q = 0; q < 16; ++q)
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                  if (j < nb) {
-                    float v[8], w2[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                      v[q] = part[q][j];
-                      w2[q] = part[8 + q][j];
-                    }
-                    const float sum = reduce8(v, lane), sum2 = reduce8(w2, lane);
-                    const int q = (lane >> 2) & 7;
-                    if ((lane & 3) == 0) {
-                      ps[(wrow + q) * NB + j] = sum;
-                      if (q < n2) ps[(wrow + 8 + q) * NB + j] = sum2;
-                    }
-                  }
-                }
-              } else {
-                // 8 rows: 4 from each stage (K = 4096, two granule columns per lane)
-                float part[8][NB];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
-                for (int sw = 0; sw < spw; ++sw) {
-                  const int gi = (cw + NCW * sw) * 32 + lane;
-                  float4 x0[NB], x1[NB];
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) {
-                    x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  }
-                  uint4 wv[8];
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) wv[q] = lds128(ta + (uint32_t)q * rowb + gi * 16);
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    wv[4 + q] = q < n2 ? lds128(tb + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                  if (j < nb) {
-                    float v[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = part[q][j];
-                    const float sum = reduce8(v, lane);
-                    const int q = (lane >> 2) & 7;
-                    if ((lane & 3) == 0 && q < 4 + n2) ps[(wrow + q) * NB + j] = sum;
-                  }
-                }
-              }
-            }
-            release_at(ab, ga, ra);
-            release_stage(ab);
-            wrow += n + n2;
-            s0 += n + n2;
-            if (wrow + rps > WIN_ROWS || s0 >= r1) {
-              gemv_flush(PAIRS, ab, buf, wbase, wrow, nb, epi);
-              buf ^= 1;
-              wbase = s0;
-              wrow = 0;
-            }
-            continue;
-          }
-        }
-        const uint8_t* st = wait_stage(ab);
-        if (st) {
-          const uint32_t sts = smem_u32(st);
-          bool done4 = false;
-          if constexpr (NB <= 2) {
-            if (n <= 4) {
-              // 4-row stage (K = 4096 at 32 KB): 4 chains, 4-value reduction
-              float part4[4][NB];
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int j = 0; j < NB; ++j) part4[q][j] = 0.f;
-              for (int sw = 0; sw < spw; ++sw) {
-                const int gi = (cw + NCW * sw) * 32 + lane;
-                float4 x0[NB], x1[NB];
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                uint4 wv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  wv[q] = q < n ? lds128(sts + (uint32_t)q * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) part4[q][j] += dot8r(wv[q], x0[j], x1[j]);
-              }
-              float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
-#pragma unroll
-              for (int j = 0; j < NB; ++j) {
-                if (j < nb) {
-                  float v[4];
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) v[q] = part4[q][j];
-                  const float sum = reduce4(v, lane);
-                  const int q = (lane >> 3) & 3;
-                  if ((lane & 7) == 0 && q < n) ps[(wrow + q) * NB + j] = sum;
-                }
-              }
-              done4 = true;
-            }
-          }
-          for (int rb = 0; rb < n && !done4; rb += 8) {
-            float part[8][NB];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-#pragma unroll
-              for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
-            for (int sw = 0; sw < spw; ++sw) {
-              const int gi = (cw + NCW * sw) * 32 + lane;
-              if constexpr (NB <= 4) {
-                // this warp's 8 activation columns are the same for every row of the batch
-                float4 x0[NB], x1[NB];
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                if constexpr (NB <= 2) {
-                  uint4 wv[8];
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-                    wv[q] = rb + q < n ? lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv[q], x0[j], x1[j]);
-                } else {
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) {
-                    if (rb + q < n) {
-                      const uint4 wv = lds128(sts + (uint32_t)(rb + q) * rowb + gi * 16);
-#pragma unroll
-                      for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv, x0[j], x1[j]);
-                    }
-                  }
-                }
-              } else {
-                // rows in two groups of 4 held in registers; each activation
-                // row is read once per group instead of once per weight row
-#pragma unroll
-                for (int h = 0; h < 8; h += 4) {
-                  uint4 wv[4];
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    wv[q] = rb + h + q < n ? lds128(sts + (uint32_t)(rb + h + q) * rowb + gi * 16)
-                                           : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                  for (int j = 0; j < NB; ++j) {
-                    if (j < nb) {
-                      const float4 x0 = lds128f(aoff[j] + gi * 32), x1 = lds128f(aoff[j] + gi * 32 + 16);
-#pragma unroll
-                      for (int q = 0; q < 4; ++q) part[h + q][j] += dot8r(wv[q], x0, x1);
-                    }
-                  }
-                }
-              }
-            }
-            float* ps = psum + ((size_t)buf * NCW + cw) * WIN_ROWS * NB;
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              if (j < nb) {
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = part[q][j];
-                const float sum = reduce8(v, lane);
-                const int q = (lane >> 2) & 7;
-                if ((lane & 3) == 0 && rb + q < n) ps[(wrow + rb + q) * NB + j] = sum;
-              }
-            }
-          }
-        }
-        release_stage(ab);
-        wrow += n;
-        s0 += n;
-        if (wrow + rps > WIN_ROWS || s0 >= r1) {
-          gemv_flush(PAIRS, ab, buf, wbase, wrow, nb, epi);
-          buf ^= 1;
-          wbase = s0;
-          wrow = 0;
-        }
-      }
-    } else {
-      for (int s0 = r0; s0 < r1; s0 += rps) {
-        const int n = min(rps, r1 - s0);
-        const uint8_t* st = wait_stage(ab);
-        if constexpr (!PAIRS && NB <= 2) {
-          if (st && n <= 2 * NCW) {
-            // short stage (the expert down rows of one CTA): warp w takes rows
-            // w and w + 8 whole, two independent chains, one warp sum each
-            const uint32_t sts = smem_u32(st);
-            const bool va = cw < n, vb = cw + NCW < n;
-            float pa[NB], pb[NB];
-#pragma unroll
-            for (int j = 0; j < NB; ++j) pa[j] = pb[j] = 0.f;
-#pragma unroll 3
-            for (int gi = lane; gi < ng; gi += 32) {
-              float4 x0[NB], x1[NB];
-#pragma unroll
-              for (int j = 0; j < NB; ++j) {
-                x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-              if (va) {
-                const uint4 wv = lds128(sts + (uint32_t)cw * rowb + gi * 16);
-#pragma unroll
-                for (int j = 0; j < NB; ++j) pa[j] += dot8r(wv, x0[j], x1[j]);
-              }
-              if (vb) {
-                const uint4 wv = lds128(sts + (uint32_t)(cw + NCW) * rowb + gi * 16);
-#pragma unroll
-                for (int j = 0; j < NB; ++j) pb[j] += dot8r(wv, x0[j], x1[j]);
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              if (j < nb) {
-                const float sa = warp_sum(pa[j]), sb = warp_sum(pb[j]);
-                if (lane == 0) {
-                  if (va) epi(s0 + cw, j, sa, 0.f);
-                  if (vb) epi(s0 + cw + NCW, j, sb, 0.f);
-                }
-              }
-            }
-            release_stage(ab);
-            continue;
-          }
-        }
-        if (st) {
-          const uint32_t sts = smem_u32(st);
-          // PAIRS: warp w takes pairs w, w+8, ... (rows 2f, 2f+1); else rows w, w+8, ...
-          const int unit = PAIRS ? 2 : 1;
-          const int per = 8 / unit;  // units per batch of 8 rows
-          for (int u0 = cw; u0 * unit < n; u0 += NCW * per) {
-            float part[8][NB];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-#pragma unroll
-              for (int j = 0; j < NB; ++j) part[q][j] = 0.f;
-            if constexpr (NB <= 2) {
-              for (int gi = lane; gi < ng; gi += 32) {
-                float4 x0[NB], x1[NB];
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                  x0[j] = j < nb ? lds128f(aoff[j] + gi * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  x1[j] = j < nb ? lds128f(aoff[j] + gi * 32 + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
-                  if (row < n) {
-                    const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) part[q][j] += dot8r(wv, x0[j], x1[j]);
-                  }
-                }
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const int row = (u0 + NCW * (q / unit)) * unit + (q % unit);
-                if (row < n) {
-                  for (int gi = lane; gi < ng; gi += 32) {
-                    const uint4 wv = lds128(sts + (uint32_t)row * rowb + gi * 16);
-#pragma unroll
-                    for (int j = 0; j < NB; ++j)
-                      if (j < nb) part[q][j] += dot8(wv, aoff[j] + gi * 32);
-                  }
-                }
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              if (j < nb) {
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = part[q][j];
-                const float sum = reduce8(v, lane);
-                const int q = (lane >> 2) & 7;
-                if (PAIRS) {
-                  const float other = __shfl_down_sync(FULL, sum, 4);  // group q+1 = the up row
-                  const int row = (u0 + NCW * (q / 2)) * 2;
-                  if ((lane & 7) == 0 && row < n) epi((s0 + row) >> 1, j, sum, other);
-                } else {
-                  const int row = u0 + NCW * q;
-                  if ((lane & 3) == 0 && row < n) epi(s0 + row, j, sum, 0.f);
-                }
-              }
-            }
-          }
-        }
-        release_stage(ab);
-      }
-    }
-    return ab;
-  }
-
-  // End of a task: agree on failure.  The barrier orders every consumer
-  // thread's writes before thread 0's release (atom.release.gpu is cumulative),
-  // so the signal publishes them without a fence in every thread.
-  __device__ bool finish(bool ab) { return cbar_or(ab); }
-
-  __device__ void signal(int ctr) {
-    if (ct == 0) atom_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
-  }
-
-  // Uniform "do my add signals complete the n of this step" for counter ctr.
-  __device__ bool ticket(int ctr, uint32_t n, uint32_t add) {
-    if (ct == 0) {
-      const uint32_t old = atom_add_acq_rel(p.ctr + (size_t)ctr * CTR_STRIDE, add);
-      m->ticket_last = (old + add == epoch * n) ? 1 : 0;
-    }
-    cbar();
-    return m->ticket_last != 0;
-  }
-
-  // ------------------------------------------------------------ tasks
-
-  // ---- projections: QKV, O (+ residual), router logits.  prep_* builds the
-  // activations and the GEMV's range and epilogue; the caller runs the GEMV;
-  // post_proj signals the task's counter.
-  __device__ bool prep_qkv(const Task& t, bool ab, ProjGemv& g) {
-    const int l = t.layer;
-    if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i4) { return x_in4(l, b, i4); });
-    cbar();
-    g.K = p.H;
-    g.r0 = t.a[0];
-    g.r1 = t.a[1];
-    g.epi = GemvEpi{};
-    g.epi.kind = GemvEpi::STORE;
-    g.epi.out = p.qkv + (size_t)l * p.bcap * p.qkv_rows;
-    g.epi.ld = p.qkv_rows;
-    g.epi.inv = m->inv;
-    return ab;
-  }
-
-  // K half h of the O projection (h = 0 only, unless o_halves = 2): the
-  // attention output's columns of that half as the activations; the residual
-  // epilogue accumulates the halves in the scratch rows.
-  __device__ bool prep_oproj(const Task& t, bool ab, ProjGemv& g, int h) {
-    const int l = t.layer, KF = p.nq * p.d, K = NB > 2 ? KF / p.o_halves : KF, r0 = t.a[0], nr = t.a[1] - r0;
-    float* xres = scr;    // residual rows of this tile, [B][nr]
-    if (h > 0) cbar();    // the previous half's GEMV is done with the activations
-    if (!ab) {
-      // the residual rows' loads go out first, with the attention output's
-      const bool r1st = h == 0 && ct < p.B * nr;
-      const float x1st = r1st ? x_in(l, ct / nr, r0 + ct % nr) : 0.f;
-      const float* o = p.o + (size_t)l * p.bcap * KF + (size_t)h * K;
-      if (NB <= 2 || K == KF) {   // whole rows: one contiguous copy
-        const float4* o4 = reinterpret_cast<const float4*>(o);
-        float4* dst = reinterpret_cast<float4*>(act);
-#pragma unroll 4
-        for (int i = ct; i < (p.B * K) >> 2; i += NCT) dst[i] = __ldcg(o4 + i);
-      } else {
-        const int K4 = K >> 2;
-#pragma unroll 4
-        for (int i = ct; i < p.B * K4; i += NCT) {
-          const int b = i / K4, c = i - b * K4;
-          reinterpret_cast<float4*>(act + (size_t)b * K)[c] =
-              __ldcg(reinterpret_cast<const float4*>(o + (size_t)b * KF) + c);
-        }
-      }
-      if (r1st) xres[ct] = x1st;
-      if (h == 0)
-        for (int i = ct + NCT; i < p.B * nr; i += NCT) xres[i] = x_in(l, i / nr, r0 + i % nr);
-    }
-    cbar();
-    g.K = K;
-    g.r0 = r0;
-    g.r1 = t.a[1];
-    g.epi = GemvEpi{};
-    g.epi.kind = GemvEpi::RESID;
-    g.epi.out = p.x_mid + (size_t)l * p.bcap * p.H;
-    g.epi.ld = p.H;
-    g.epi.res = xres;
-    g.epi.res_ld = nr;
-    g.epi.res_r0 = r0;
-    return ab;
-  }
-
-  __device__ bool post_proj(const Task& t, bool ab) {
-    const int l = t.layer;
-    if (t.type == T_OPROJ) ab = router_part(t, ab);
-    ab = finish(ab);
-    if (!ab) {
-      if (t.type == T_QKV) signal(p.cm.qkv + l * p.nkv + t.a[2]);
-      else signal(p.cm.o + l);
-    }
-    return ab;
-  }
-
-  // The O tile's share of the router logits over its hidden rows h in [r0, r1):
-  //   part[b][e] = sum_h WrT[h][e] * gain[h] * x_mid[b][h]
-  // (the logits are inv_rms(x_mid_b) times the sum of every tile's part), from
-  // the x_mid rows the residual epilogue left in the scratch and the router
-  // stage.  The parts are added as 32.32 fixed-point integers: the sum is
-  // exact, so its bits do not depend on the order the tiles arrive in.
-  __device__ bool router_part(const Task& t, bool ab) {
-    const int r0 = t.a[0], nr = t.a[1] - r0, E = p.E;
-    const uint8_t* st = wait_stage(ab);
-    cbar();   // every x_mid row of the tile is in the scratch
-    if (st) {
-      const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
-      const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
-      // copy t % RL_COPIES of the sums: eight times fewer tiles contend for each address
-      unsigned long long* out = p.rlsum + ((size_t)t.layer * RL_COPIES + t.a[2] % RL_COPIES) * p.bcap * E;
-      // two neighbouring threads per (b, e), each half the rows, then one shuffle
-      const int n2 = 2 * p.B * E, hr = (nr + 1) >> 1;
-      for (int x0 = 0; x0 < n2; x0 += NCT) {
-        const int x = x0 + ct, half = x & 1, be = x >> 1;
-        const bool ok = x < n2;
-        const int b = ok ? be / E : 0, e = ok ? be - b * E : 0;
-        const float* xr = scr + b * nr;
-        const int i0 = half ? hr : 0, i1 = half ? nr : hr;
-        float acc = 0.f;
-        if (ok)
-          for (int i = i0; i < i1; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
-        const float other = __shfl_xor_sync(FULL, acc, 1);
-        if (ok && half == 0) atomicAdd(out + (size_t)b * E + e, to_fixed(acc + other));
-      }
-    }
-    release_stage(ab);
-    return ab;
-  }
-
-  // Routing of layer l from its router logits (m->rl), computed in every
-  // gate/up task the same way, so every CTA gets the same bits:
-  //  - per request, each expert's rank: how many logits are greater, or equal
-  //    with a lower index (NaN counts as -inf), so ranks are a permutation;
-  //    the top-k are the ranks below k, in rank order;
-  //  - gates: softmax over the selected logits;
-  //  - the distinct experts in ascending order, with their (request, rank)
-  //    pairs in request order (r_U, r_exp, r_cnt, r_tok, r_rank).
-  // The distinct experts go to this CTA's producer (r_layer) as soon as they
-  // are known, before the token lists.  With publish
-  // set it also goes to global memory (ids, gates, routing table) and the
-  // rdone counter is signalled.
-  // Expects m->rl loaded and m->cnt_of zeroed, both behind a barrier.
-  __device__ void route_local(int l, bool publish) {
-    const int E = p.E, k = p.k, B = p.B;
-    const int umax = p.rm.umax, bc = p.rm.bcap;
-    // ranks: two threads per candidate when they fit, each counting half the row
-    const int split = 2 * B * E <= NCT ? 2 : 1;
-    const int per = NCT / split;
-    for (int c0 = 0; c0 < B * E; c0 += per) {
-      const int c = c0 + ct / split, half = ct & (split - 1);
-      const bool valid = c < B * E;
-      const int b = valid ? c / E : 0, e = valid ? c - b * E : 0;
-      const float* row = m->rl + b * E;
-      const float v = row[e];
-      const int e_lo = split == 2 ? half * (E >> 1) : 0, e_hi = split == 2 ? (half ? E : E >> 1) : E;
-      // four independent counts over float4 loads when every half-row starts
-      // 16-byte aligned (E a multiple of 8), else one at a time
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-      int e2 = e_lo;
-      const int vec_hi = (E & 7) == 0 ? e_hi : e_lo;
-#pragma unroll 8
-      for (; e2 + 4 <= vec_hi; e2 += 4) {   // branch-free: (w > v) | (w == v & index < e)
-        const float4 w = *reinterpret_cast<const float4*>(row + e2);
-        r0 += (w.x > v) | ((w.x == v) & (e2 < e));
-        r1 += (w.y > v) | ((w.y == v) & (e2 + 1 < e));
-        r2 += (w.z > v) | ((w.z == v) & (e2 + 2 < e));
-        r3 += (w.w > v) | ((w.w == v) & (e2 + 3 < e));
-      }
-      for (; e2 < e_hi; ++e2) r0 += (row[e2] > v) || (row[e2] == v && e2 < e);
-      int rank = (r0 + r1) + (r2 + r3);
-      if (split == 2) rank += __shfl_xor_sync(FULL, rank, 1);
-      if (valid && half == 0 && rank < k) {
-        m->sel[b * k + rank] = e;
-        m->selv[b * k + rank] = v;
-        atomicAdd(&m->cnt_of[e], 1);
-      }
-    }
-    cbar();
-    if (B == 1) {
-      // one request: its k experts are distinct.  Warp 0 holds them in lanes
-      // 0 .. k-1: the gates (softmax over the selected; the butterfly over all
-      // 32 lanes adds only zeros past k), and each expert's place in ascending
-      // id order gives the distinct-expert table, one token slot each.
-      if (cw == 0) {
-        const bool on = lane < k;
-        const int e = on ? m->sel[lane] : 0;
-        const float v = on ? m->selv[lane] : 0.f;
-        const float ex = on ? expf(v - m->selv[0]) : 0.f;
-        float tot = ex;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
-        int pos = 0;
-        for (int j = 0; j < k; ++j) pos += m->sel[j] < e;
-        if (on) {
-          m->gate[lane] = ex / tot;
-          m->r_exp[pos] = e;
-          m->r_cnt[pos] = 1;
-          m->r_tok[pos * bc] = 0;
-          m->r_rank[pos * bc] = lane;
-        }
-        if (lane == 0) m->r_U = k;
-      }
-      cbar();
-      if (ct == 0) st_release_cta(&m->r_layer, step * p.L + l);
-    } else {
-      // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
-      // groups of kp consecutive lanes (kp = k rounded up to a power of two)
-      {
-        int kp = 1;
-        while (kp < k) kp <<= 1;
-        const int per_warp = 32 / kp;
-        const int b = (cw - 1) * per_warp + lane / kp, j = lane % kp;
-        const bool mine = cw >= 1 && b < B;             // uniform per warp but for the tail
-        const bool act_j = mine && j < k;
-        const float first = mine ? m->selv[b * k] : 0.f;
-        const float ex = act_j ? expf(m->selv[b * k + j] - first) : 0.f;
-        float tot = ex;
-        for (int o = 1; o < kp; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
-        if (act_j) m->gate[b * k + j] = ex / tot;
-      }
-      if (cw == 0) {
-        int base = 0;
-        for (int c = 0; c < (E + 31) / 32; ++c) {
-          const int e = c * 32 + lane;
-          const bool pres = e < E && m->cnt_of[e] > 0;
-          const unsigned mask = __ballot_sync(FULL, pres);
-          if (pres) {
-            const int u = base + __popc(mask & ((1u << lane) - 1u));
-            m->slot_of[e] = u;
-            m->r_exp[u] = e;
-            m->r_cnt[u] = m->cnt_of[e];
-          }
-          base += __popc(mask);
-        }
-        if (lane == 0) m->r_U = base;
-      }
-      cbar();
-      if (ct == 0) st_release_cta(&m->r_layer, step * p.L + l);   // the producer needs only r_U and r_exp
-      if (ct < B * k) {
-        const int e = m->sel[ct];
-        int rank = 0;
-        for (int q = 0; q < ct; ++q) rank += (m->sel[q] == e);
-        const int u = m->slot_of[e];
-        m->r_tok[u * bc + rank] = ct / k;
-        m->r_rank[u * bc + rank] = ct % k;
-      }
-      cbar();
-    }
-    if (!publish) return;
-    int* rt = const_cast<int*>(route_of(p, l));
-    const int U = m->r_U;
-    if (ct == 0) rt[0] = U;
-    for (int u = ct; u < U; u += NCT) {
-      rt[1 + u] = m->r_exp[u];
-      rt[1 + umax + u] = m->r_cnt[u];
-    }
-    for (int i = ct; i < U * bc; i += NCT) {
-      rt[1 + 2 * umax + i] = m->r_tok[i];
-      rt[1 + 2 * umax + umax * bc + i] = m->r_rank[i];
-    }
-    if (ct < B * k) {
-      p.ids[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->sel[ct];
-      p.gates[((size_t)l * p.bcap + ct / k) * k + ct % k] = m->gate[ct];
-    }
-    for (int i = ct; i < B * E; i += NCT) p.rlog[((size_t)l * p.bcap + i / E) * E + i % E] = m->rl[i];
-    cbar();
-    signal(p.cm.rdone + l);
-  }
-
-  // The expert tile's activations: act = x_mid * FFN gain with m->inv (as
-  // fill_rmsnorm), and the layer's router logits m->rl[b * E + e] = inv[b] *
-  // (the O tiles' fixed-point sum), NaN ranked as -inf.  The sums' loads go
-  // out first and the norm's inputs (at most two float4 per thread: H <= 2048)
-  // right after, so both arrive in one round trip.
-  __device__ void moe_act(int l) {
-    const int H = p.H, H4 = H >> 2, E = p.E, BE = p.B * E;
-    const size_t cs = (size_t)p.bcap * E;   // one copy of the sums
-    const unsigned long long* rs = p.rlsum + (size_t)l * RL_COPIES * cs;
-    auto load_sum = [&](int i) {   // the copies' integer sum: exact in any order
-      unsigned long long v[RL_COPIES];
-#pragma unroll
-      for (int c = 0; c < RL_COPIES; ++c) v[c] = __ldcg(rs + c * cs + i);
-      unsigned long long q = 0;
-#pragma unroll
-      for (int c = 0; c < RL_COPIES; ++c) q += v[c];
-      return q;
-    };
-    unsigned long long v0[RL_COPIES];   // this thread's first sum: its loads go out now, the adds come later
-#pragma unroll
-    for (int c = 0; c < RL_COPIES; ++c) v0[c] = ct < BE ? __ldcg(rs + c * cs + ct) : 0ull;
-    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
-    const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 x0[2];
-    uint2 g0[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = ct + h * NCT;
-      x0[h] = i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm) + i) : z4;
-      g0[h] = i < H4 ? __ldg(gam + i) : make_uint2(0u, 0u);
-    }
-    for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
-    if constexpr (NB == 1) {
-      float ss = 0.f;
-      float4* dst = reinterpret_cast<float4*>(act);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = ct + h * NCT;
-        if (i < H4) {
-          const float4 xv = x0[h];
-          const uint2 gb = g0[h];
-          dst[i] = make_float4(xv.x * bf_lo(gb.x), xv.y * bf_hi(gb.x), xv.z * bf_lo(gb.y), xv.w * bf_hi(gb.y));
-          ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
-        }
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) m->red[cw] = ss;
-    } else {
-      // the other requests' rows: all loads out together (one round trip, not B - 1)
-      float4 xv[2][NB];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = ct + h * NCT;
-        xv[h][0] = x0[h];
-#pragma unroll
-        for (int b = 1; b < NB; ++b)
-          xv[h][b] = b < p.B && i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i) : z4;
-      }
-      float ss[NB];
-#pragma unroll
-      for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = ct + h * NCT;
-        if (i < H4) {
-          const uint2 gb = g0[h];
-          const float ga = bf_lo(gb.x), gc = bf_hi(gb.x), ge = bf_lo(gb.y), gg = bf_hi(gb.y);
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (b < p.B) {
-              const float4 v = xv[h][b];
-              reinterpret_cast<float4*>(act + (size_t)b * H)[i] = make_float4(v.x * ga, v.y * gc, v.z * ge, v.w * gg);
-              ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (b < p.B) {
-          const float t = warp_sum(ss[b]);
-          if (lane == 0) m->red[b * NCW + cw] = t;
-        }
-      }
-    }
-    cbar();
-    if (ct < p.B) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
-      m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
-    }
-    cbar();
-    unsigned long long q0 = 0;
-#pragma unroll
-    for (int c = 0; c < RL_COPIES; ++c) q0 += v0[c];
-    if constexpr (NB == 1) {
-      for (int i = ct; i < BE; i += NCT) {
-        const float v = from_fixed(i == ct ? q0 : load_sum(i)) * m->inv[i / E];
-        m->rl[i] = v == v ? v : -INFINITY;
-      }
-    } else {
-      if (ct < BE) {
-        const float v = from_fixed(q0) * m->inv[ct / E];
-        m->rl[ct] = v == v ? v : -INFINITY;
-      }
-      // the rest two sums at a time, both sets of loads in flight together
-      for (int i = ct + NCT; i < BE; i += 2 * NCT) {
-        const int i2 = i + NCT;
-        unsigned long long a[RL_COPIES], c2[RL_COPIES];
-#pragma unroll
-        for (int c = 0; c < RL_COPIES; ++c) {
-          a[c] = __ldcg(rs + c * cs + i);
-          c2[c] = i2 < BE ? __ldcg(rs + c * cs + i2) : 0ull;
-        }
-        unsigned long long qa = 0, qb = 0;
-#pragma unroll
-        for (int c = 0; c < RL_COPIES; ++c) {
-          qa += a[c];
-          qb += c2[c];
-        }
-        const float va = from_fixed(qa) * m->inv[i / E];
-        m->rl[i] = va == va ? va : -INFINITY;
-        if (i2 < BE) {
-          const float vb = from_fixed(qb) * m->inv[i2 / E];
-          m->rl[i2] = vb == vb ? vb : -INFINITY;
-        }
-      }
-    }
-  }
-
-  // ---- expert tile: the layer's routing, then for this tile's (distinct
-  // expert, ffn unit) pairs the gate/up rows, giving per token slot the
-  // coefficient c = gate x silu(gate row . xn) x (up row . xn), then the same
-  // units' rows of the transposed down matrix: y_b += c x Wd^T[unit] for the
-  // token's request b.  y is this tile's gated partial of the layer output
-  // (moe_part); the reduce tasks add the residual and all tiles' partials.
-  // No other CTA's gate/up results are needed, so the tile streams its
-  // gate/up and down weights back to back.
-  __device__ bool moe(const Task& t, bool ab) {
-    const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
-    int U = 0;
-    if (!ab) {
-      moe_act(l);
-      cbar();
-      mark(TR_MID1);
-      if (m->r_layer != step * p.L + l || t.a[0] == 0) route_local(l, t.a[0] == 0);
-      mark(TR_MID2);
-      U = m->r_U;
-    }
-    cbar();
-    mark(TR_ACT);
-    long long g0, g1;
-    gu_range_w<NB>(p, t, U, m->r_cnt, g0, g1);
-    const int q0 = (int)g0, q1 = (int)g1;
-    float* cf = scr;   // [unit - q0][token slot] coefficients
-    for (int q = q0; q < q1;) {
-      const int u = q / F, fa = q - u * F, fb = min(F, q1 - u * F);
-      const int nt = m->r_cnt[u];
-      const int* toks = m->r_tok + u * bc;
-      const int* ranks = m->r_rank + u * bc;
-      GemvEpi e{};
-      e.kind = GemvEpi::SWIGLU;
-      e.out = cf;
-      e.ld = bc;
-      e.base = u * F - q0;
-      e.k = k;
-      e.toks = toks;
-      e.ranks = ranks;
-      e.gate_w = m->gate;
-      e.inv = m->inv;
-      ab = gemv<true, SP_MOE>(H, 2 * fa, 2 * fb, act, H, toks, nt, ab, e);
-      q = (u + 1) * F;
-    }
-    cbar();   // coefficients complete; the activation region is free
-    const int rpw = rows_per_stage(p, H);
-    const bool col = ct * 8 < H;                 // this thread's 8 output columns
-    const uint32_t coff = (uint32_t)ct * 16;
-    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // batch 1: request 0 in registers
-    if constexpr (NB > 1) {                      // else: y per request in the activation region,
-      if (col) {                                 // each thread owning its 8 columns of every row
-        for (int b = 0; b < p.B; ++b) {
-          float4* yb = reinterpret_cast<float4*>(act + (size_t)b * H) + 2 * ct;
-          yb[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-          yb[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-    }
-    for (int q = q0; q < q1;) {
-      const int u = q / F, fa = q - u * F, fb = min(F, q1 - u * F);
-      const int nt = m->r_cnt[u];
-      const int* toks = m->r_tok + u * bc;
-      for (int f0 = fa; f0 < fb; f0 += rpw) {
-        const int n = min(rpw, fb - f0);
-        const uint8_t* st = wait_stage(ab);
-        if (st && col) {
-          const uint32_t sts = smem_u32(st) + coff;
-          const float* cu = cf + (size_t)(u * F + f0 - q0) * bc;
-          if constexpr (NB > 1) {
-            // every row of the stage is a unit of expert u, so all share its
-            // token slots: up to 8 rows in registers, then each token's 8
-            // output columns read and written once for all of them
-            for (int i0 = 0; i0 < n; i0 += 8) {
-              const int ni = min(8, n - i0);
-              uint4 w8[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                w8[i] = i < ni ? lds128(sts + (uint32_t)(i0 + i) * H * 2) : make_uint4(0, 0, 0, 0);
-              for (int j = 0; j < nt; ++j) {
-                float4* yb = reinterpret_cast<float4*>(act + (size_t)toks[j] * H) + 2 * ct;
-                float4 a0 = yb[0], a1 = yb[1];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float c = i < ni ? cu[(i0 + i) * bc + j] : 0.f;
-                  const uint4 w = w8[i];
-                  a0.x = fmaf(c, bf_lo(w.x), a0.x);
-                  a0.y = fmaf(c, bf_hi(w.x), a0.y);
-                  a0.z = fmaf(c, bf_lo(w.y), a0.z);
-                  a0.w = fmaf(c, bf_hi(w.y), a0.w);
-                  a1.x = fmaf(c, bf_lo(w.z), a1.x);
-                  a1.y = fmaf(c, bf_hi(w.z), a1.y);
-                  a1.z = fmaf(c, bf_lo(w.w), a1.z);
-                  a1.w = fmaf(c, bf_hi(w.w), a1.w);
-                }
-                yb[0] = a0;
-                yb[1] = a1;
-              }
-            }
-          } else {
-            for (int i = 0; i < n; ++i) {
-              const uint4 w = lds128(sts + (uint32_t)i * H * 2);
-              const float c = cu[i * bc];
-              y[0] = fmaf(c, bf_lo(w.x), y[0]);
-              y[1] = fmaf(c, bf_hi(w.x), y[1]);
-              y[2] = fmaf(c, bf_lo(w.y), y[2]);
-              y[3] = fmaf(c, bf_hi(w.y), y[3]);
-              y[4] = fmaf(c, bf_lo(w.z), y[4]);
-              y[5] = fmaf(c, bf_hi(w.z), y[5]);
-              y[6] = fmaf(c, bf_lo(w.w), y[6]);
-              y[7] = fmaf(c, bf_hi(w.w), y[7]);
-            }
-          }
-        }
-        release_stage(ab);
-      }
-      q = (u + 1) * F;
-    }
-    mark(TR_STAGES);
-    if (!ab && col) {
-      float* part = p.moe_part + (size_t)t.a[0] * p.bcap * H;
-      for (int b = 0; b < p.B; ++b) {
-        float4* dst = reinterpret_cast<float4*>(part + (size_t)b * H) + 2 * ct;
-        if constexpr (NB == 1) {
-          dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-          dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-        } else {
-          const float4* src = reinterpret_cast<const float4*>(act + (size_t)b * H) + 2 * ct;
-          dst[0] = src[0];
-          dst[1] = src[1];
-        }
-      }
-    }
-    ab = finish(ab);
-    if (!ab) signal(p.cm.gu + l);
-    return ab;
-  }
-
-  // ---- reduce: rows [a0, a1) of the hidden dim, x_out = x_mid + the a2 expert
-  // tiles' partials, summed in tile order (strided chunks, then chunk order)
-  __device__ bool red(const Task& t, bool ab) {
-    const int l = t.layer, r0 = t.a[0], nr = t.a[1] - r0, ntiles = t.a[2], B = p.B, H = p.H;
-    const int no = B * nr;
-    const int nch = no > 0 ? max(1, NCT / no) : 1;
-    float* rs = act;                                   // [output][chunk] sums
-    mark(TR_ACT);
-    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
-    if (!ab) {   // every expert tile of the layer has read the router sums: zero this task's share
-      const long long n = (long long)RL_COPIES * p.bcap * p.E;
-      unsigned long long* rs = p.rlsum + (size_t)l * n;
-      for (long long i = r0 * n / H + ct; i < (long long)t.a[1] * n / H; i += NCT) rs[i] = 0ull;
-    }
-    // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)
-    const float xres = !ab && ct < no ? __ldcg(xm + (size_t)(ct / nr) * H + r0 + ct % nr) : 0.f;
-    if (!ab) {
-      // thread x takes output o = x % no and every nch-th tile from chunk c = x / no,
-      // so a warp reads consecutive rows of a tile; up to BT loads in flight
-      constexpr int BT = 10;
-      for (int x = ct; x < no * nch; x += NCT) {
-        const int c = x / no, o = x - c * no, b = o / nr, h = r0 + (o - b * nr);
-        const float* src = p.moe_part + (size_t)b * H + h;
-        float s = 0.f;
-        for (int t0 = c; t0 < ntiles; t0 += BT * nch) {
-          float v[BT];
-#pragma unroll
-          for (int i = 0; i < BT; ++i) {
-            const int ti = t0 + i * nch;
-            v[i] = ti < ntiles ? __ldcg(src + (size_t)ti * p.bcap * H) : 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < BT; ++i) s += v[i];
-        }
-        rs[o * nch + c] = s;
-      }
-    }
-    cbar();
-    if (!ab) {
-      float* xo = p.x_out + (size_t)l * p.bcap * H;
-      for (int o = ct; o < no; o += NCT) {
-        const int b = o / nr, h = r0 + (o - b * nr);
-        float s = o == ct ? xres : __ldcg(xm + (size_t)b * H + h);
-        for (int c = 0; c < nch; ++c) s += rs[o * nch + c];
-        xo[(size_t)b * H + h] = s;
-      }
-    }
-    mark(TR_STAGES);
-    ab = finish(ab);
-    if (!ab) signal(p.cm.down + l);
-    return ab;
-  }
-
-
-  // ---- split-KV attention chunk on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc)
-  // Pages hold K and V transposed ([d][16 slots]).  Per page (16 tokens):
-  //   S  [16 tok x 8 heads] = K [tok x d] . Q^T            (A = K via ldmatrix.trans, B = q regs)
-  //   O^T[16 dim x 8 heads] += V^T [dim x tok] . P^T       (A = V^T via ldmatrix, B = P via smem)
-  // q and P enter as bf16 hi + lo pairs (two MMAs each), so the products keep
-  // close to fp32 accuracy; K and V are exact bf16.  The warps of a stage take
-  // its pages (NCW / pages-per-stage warps per page, splitting the d/16 output
-  // row tiles); each page group keeps its own online-softmax state, merged at
-  // the end of the chunk into one partial; the combine tasks merge the chunks.
-  __device__ bool attn(const Task& t, bool ab) {
-    const int l = t.layer, b = t.a[0], g = t.a[1];
-    const int G = p.G, d = p.d, half = d >> 1;
-    constexpr int PS = 16;                         // page size (tokens)
-    const int pos = __ldcg(p.seq_len + b) + step;
-    int tok0, tok1;
-    attn_range(p, t, pos, tok0, tok1);
-    const int RS = d + 4;                          // partial row: acc[d], m, l, pad (16-byte rows)
-    float* q_s = act;                              // [MAX_G][d] rotated, scaled q
-    float* kn_s = q_s + MAX_G * d;                 // new token's key (bf16 values)
-    float* vn_s = kn_s + d;
-    float* mrg = vn_s + d;                         // [groups][G][RS]
-    uint32_t* pscr = reinterpret_cast<uint32_t*>(mrg + p.attn_mrg_floats);   // [NCW][2][8][8] packed P
-    const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
-    const float2* rope = p.rope + (size_t)pos * half;
-    const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
-    const bool has_new = pos >= tok0 && pos < tok1;
-    if (!ab) {
-      for (int idx = ct; idx < MAX_G * half; idx += NCT) {
-        const int h = idx / half, i = idx - h * half;
-        float qa = 0.f, qb = 0.f;
-        if (h < G) {
-          const float2 cs = rope[i];
-          const float a = __ldcg(qkv + h * d + i), c = __ldcg(qkv + h * d + i + half);
-          qa = (a * cs.x - c * cs.y) * qscale;
-          qb = (c * cs.x + a * cs.y) * qscale;
-        }
-        q_s[h * d + i] = qa;
-        q_s[h * d + i + half] = qb;
-      }
-      if (has_new) {
-        const float* kr = qkv + (size_t)G * d;
-        const float* vr = kr + d;
-        const size_t base =
-            ((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * d * PS + pos % PS;
-        uint16_t* kd = p.k_pool[l] + base;
-        uint16_t* vd = p.v_pool[l] + base;
-        for (int i = ct; i < half; i += NCT) {
-          const float2 cs = rope[i];
-          const float a = __ldcg(kr + i), c = __ldcg(kr + i + half);
-          const uint16_t k0 = f2bf(a * cs.x - c * cs.y), k1 = f2bf(c * cs.x + a * cs.y);
-          kd[(size_t)i * PS] = k0;
-          kd[(size_t)(i + half) * PS] = k1;
-          kn_s[i] = bf2f(k0);
-          kn_s[i + half] = bf2f(k1);
-        }
-        for (int i = ct; i < d; i += NCT) {
-          const uint16_t v0 = f2bf(__ldcg(vr + i));
-          vd[(size_t)i * PS] = v0;
-          vn_s[i] = bf2f(v0);
-        }
-      }
-    }
-    cbar();
-    mark(TR_ACT);
-    const int gq = lane >> 2, tq = lane & 3;       // mma fragment coordinates
-    const int nks = d >> 4;                        // 16-dim k steps (QK) = 16-dim row tiles (PV)
-    // B fragments of Q^T per k step and lane (rows (dims) 2tq, 2tq+1 and +8,
-    // column (head) gq), as bf16 hi + lo pairs, in a shared table: one
-    // 16-byte read per k step instead of 32 registers held across the chunk
-    // the table takes the place of q_s (d/16 k steps x 32 lanes x 16 bytes =
-    // MAX_G * d floats): every thread reads its entry's q values first, then
-    // all write after a barrier
-    static_assert(NCT == 8 * 32, "one table entry per consumer thread");
-    uint4* qtab = reinterpret_cast<uint4*>(q_s);   // [8 k steps][32 lanes]
-    {
-      const int ks = ct >> 5, L = ct & 31, gqL = L >> 2, tqL = L & 3;
-      uint32_t w[4];
-#pragma unroll
-      for (int hfi = 0; hfi < 2; ++hfi) {
-        float x0 = 0.f, x1 = 0.f;
-        if (ks < nks) {
-          x0 = q_s[gqL * d + ks * 16 + hfi * 8 + 2 * tqL];
-          x1 = q_s[gqL * d + ks * 16 + hfi * 8 + 2 * tqL + 1];
-        }
-        const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
-        w[hfi] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        w[2 + hfi] = (uint32_t)f2bf(x0 - bf2f(h0)) | ((uint32_t)f2bf(x1 - bf2f(h1)) << 16);
-      }
-      cbar();
-      if (ks < nks) qtab[ct] = make_uint4(w[0], w[1], w[2], w[3]);   // nks * 32 entries = MAX_G * d floats
-    }
-    cbar();
-    const uint32_t qtab_lane = smem_u32(qtab) + (uint32_t)lane * 16;
-    const int ppg = pages_per_stage(p);
-    const int npar = NCW / ppg;                    // stages in flight: warp (par, grp) takes page
-    const int par = cw / ppg, grp = cw - par * ppg;  // grp of every npar-th stage, starting at par
-    const int mtw = nks;                           // output row tiles per warp (all of d)
-    const uint32_t PB = (uint32_t)d * PS * 2;      // bytes of one page block
-    // online-softmax state of heads 2tq, 2tq+1 (identical across gq) and O^T tiles
-    float mr0 = -INFINITY, mr1 = -INFINITY, lr0 = 0.f, lr1 = 0.f;
-    float o[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
-    uint32_t* myp = pscr + cw * 2 * 64;            // this warp's packed P^T: [hi/lo][head 8][tok/2 8]
-    const int pg0 = tok0 / PS, pg1 = (tok1 + PS - 1) / PS;
-    int si = 0;                                    // stage index within the chunk
-    for (int pg = pg0; pg < pg1; pg += ppg, ++si) {
-      const int npg = min(ppg, pg1 - pg);
-      const uint8_t* st = wait_stage(ab);
-      if (st && has_new && pos / PS >= pg && pos / PS < pg + npg) {
-        // put the new token's K and V into its stage slot before anyone reads the
-        // page, and zero the page's later slots: they hold no token yet, and
-        // although their scores are masked, their V still enters the P.V product
-        // (0 * NaN would poison the output)
-        cbar();
-        const int pi = pos / PS - pg, slot = pos % PS;
-        uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
-        uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
-        for (int i = ct; i < d * PS; i += NCT) {
-          const int dim = i / PS, sl = i - dim * PS;
-          if (sl == slot) {
-            kp[i] = f2bf(kn_s[dim]);
-            vp[i] = f2bf(vn_s[dim]);
-          } else if (sl > slot) {
-            kp[i] = 0;
-            vp[i] = 0;
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        cbar();
-      } else if (has_new && pos / PS >= pg && pos / PS < pg + npg) {
-        cbar();
-        cbar();
-      }
-      if (st && si % npar == par && grp < npg) {
-        const int P = pg + grp;                    // global page index of this warp's page
-        const int nvalid = min(PS, tok1 - P * PS); // tokens of the page inside the chunk
-        const uint32_t kpage = smem_u32(st) + grp * PB;
-        const uint32_t vpage = kpage + ppg * PB;
-        // S = K . Q^T : A tiles of K^T-stored rows via ldmatrix.trans
-        float s[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-        const int li = lane >> 3, lr = lane & 7;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          if (ks < nks) {
-            const uint32_t addr = kpage + (uint32_t)((ks * 16 + (li >> 1) * 8 + lr) * PS * 2 + (li & 1) * 16);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(addr, a0, a1, a2, a3);
-            const uint4 qf = lds128(qtab_lane + (uint32_t)ks * 512);
-            mma_bf16(s, a0, a1, a2, a3, qf.x, qf.y);
-            mma_bf16(sl, a0, a1, a2, a3, qf.z, qf.w);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[e] += sl[e];
-        // s[0]: (tok gq, head 2tq) s[1]: (tok gq, head 2tq+1) s[2]/s[3]: tok gq+8
-        if (gq >= nvalid) { s[0] = -INFINITY; s[1] = -INFINITY; }
-        if (gq + 8 >= nvalid) { s[2] = -INFINITY; s[3] = -INFINITY; }
-        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, off));
-        }
-        const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
-        const float sc0 = exp2f(mr0 - mn0), sc1 = exp2f(mr1 - mn1);   // 0 on the first page
-        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
-        float ps0 = p0 + p2, ps1 = p1 + p3;
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          ps0 += __shfl_xor_sync(FULL, ps0, off);
-          ps1 += __shfl_xor_sync(FULL, ps1, off);
-        }
-        lr0 = lr0 * sc0 + ps0;
-        lr1 = lr1 * sc1 + ps1;
-        mr0 = mn0;
-        mr1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= sc0; o[mt][1] *= sc1; o[mt][2] *= sc0; o[mt][3] *= sc1;
-        }
-        // P^T as mma B operand: element (tok k, head n) packed per token pair;
-        // store [hi/lo][head][tok/2] as bf16x2 words
-        __syncwarp();
-        {
-          uint16_t* ph = reinterpret_cast<uint16_t*>(myp);
-          uint16_t* pl = reinterpret_cast<uint16_t*>(myp + 64);
-          const float pv[4] = {p0, p1, p2, p3};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int head = 2 * tq + (e & 1), tok = gq + 8 * (e >> 1);
-            const uint16_t hb = f2bf(pv[e]);
-            ph[head * 16 + tok] = hb;
-            pl[head * 16 + tok] = f2bf(pv[e] - bf2f(hb));
-          }
-        }
-        __syncwarp();
-        const uint32_t bh0 = myp[gq * 8 + tq], bh1 = myp[gq * 8 + tq + 4];
-        const uint32_t bl0 = myp[64 + gq * 8 + tq], bl1 = myp[64 + gq * 8 + tq + 4];
-        // O^T += V^T . P^T over all d/16 row tiles (dims)
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          if (mt < mtw) {
-            const int m0 = mt * 16;
-            const uint32_t addr = vpage + (uint32_t)((m0 + (li & 1) * 8 + lr) * PS * 2 + (li >> 1) * 16);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
-          }
-        }
-      }
-      release_stage(ab);
-    }
-    mark(TR_STAGES);
-    // merge the warps' partial softmax states of this chunk (a warp that saw
-    // no page keeps max -inf and drops out)
-    if (!ab) {
-      if (gq == 0) {
-        if (2 * tq < G) {
-          mrg[(cw * G + 2 * tq) * RS + d] = mr0;
-          mrg[(cw * G + 2 * tq) * RS + d + 1] = lr0;
-        }
-        if (2 * tq + 1 < G) {
-          mrg[(cw * G + 2 * tq + 1) * RS + d] = mr1;
-          mrg[(cw * G + 2 * tq + 1) * RS + d + 1] = lr1;
-        }
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        if (mt < mtw) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int head = 2 * tq + (e & 1), dim = mt * 16 + gq + 8 * (e >> 1);
-            if (head < G) mrg[(cw * G + head) * RS + dim] = o[mt][e];
-          }
-        }
-      }
-    }
-    ab = cbar_or(ab);
-    if (ab) return ab;
-    const int nslots = p.part_slots;
-    float* part = p.part + ((size_t)l * nslots + t.a[4]) * G * RS;
-    // per head: the chunk max, normaliser and each warp's weight, once
-    float* fw = reinterpret_cast<float*>(pscr);    // [NCW][G] weights (P scratch is free now)
-    static_assert(NCW == 8 && MAX_G * NCW <= NCT, "eight lanes per head, one per warp state");
-    if (ct < MAX_G * NCW) {   // lanes 8h .. 8h + 7: head h, warp state w (butterflies within the 8)
-      const int h = ct >> 3, w = ct & 7;
-      const bool hv = h < G;
-      const float mw = hv ? mrg[(w * G + h) * RS + d] : -INFINITY;
-      float M = mw;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      float Ls = hv ? mrg[(w * G + h) * RS + d + 1] * f : 0.f;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) Ls += __shfl_xor_sync(FULL, Ls, o);
-      if (hv) {
-        fw[w * G + h] = f;
-        if (w == 0) {
-          part[h * RS + d] = M;
-          part[h * RS + d + 1] = Ls;
-        }
-      }
-    }
-    cbar();
-    for (int idx = ct; idx < G * d; idx += NCT) {
-      const int h = idx / d, i = idx - h * d;
-      float A = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) A = fmaf(mrg[(w * G + h) * RS + i], fw[w * G + h], A);
-      part[h * RS + i] = A;
-    }
-    ab = finish(ab);
-    if (!ab) signal(p.cm.attn_idx(l, b, g));
-    return ab;
-  }
-
-  // ---- split-KV combine of query heads [a2, a2 + a3) of (request a0, KV group a1)
-  // The chunks' partials (max m, normaliser l, accumulator acc[d], in exp2
-  // units) merge by log-sum-exp.  Warp w takes chunks w, w + 8, ... in order
-  // with an online (max, normaliser, accumulator) state, CB chunks per round
-  // trip; the 8 warp states then merge in warp order, so the result does not
-  // depend on timing.
-  __device__ bool comb(const Task& t, bool ab) {
-    constexpr int CB = 8;
-    const int l = t.layer, b = t.a[0], g = t.a[1], h0 = t.a[2], nh = t.a[3], nc = t.a[6];
-    const int G = p.G, d = p.d, RS = d + 4, d4 = d >> 2;
-    const float* part = p.part + ((size_t)l * p.part_slots + t.a[5]) * G * RS;
-    float* o = p.o + ((size_t)l * p.bcap + b) * p.nq * d + (size_t)g * G * d;
-    float* ws = act;                                   // [NCW][d + 4]: accumulator, max, normaliser
-    const bool has = lane < d4;                        // this lane's 4 dims
-    mark(TR_ACT);
-    for (int hh = 0; hh < nh && !ab; ++hh) {
-      const int h = h0 + hh;
-      float M = -INFINITY, Ls = 0.f;
-      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c0 = cw; c0 < nc; c0 += NCW * CB) {
-        float4 v[CB];
-        float2 ml[CB];
-#pragma unroll
-        for (int q = 0; q < CB; ++q) {
-          const int c = c0 + q * NCW;
-          if (c < nc) {
-            const float* pc = part + ((size_t)c * G + h) * RS;
-            ml[q] = __ldcg(reinterpret_cast<const float2*>(pc + d));
-            v[q] = has ? __ldcg(reinterpret_cast<const float4*>(pc) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < CB; ++q) {
-          if (c0 + q * NCW < nc) {
-            const float mn = fmaxf(M, ml[q].x);
-            const float fo = exp2f(M - mn), fn = exp2f(ml[q].x - mn);   // fo = 0 while M = -inf
-            A.x = fmaf(v[q].x, fn, A.x * fo);
-            A.y = fmaf(v[q].y, fn, A.y * fo);
-            A.z = fmaf(v[q].z, fn, A.z * fo);
-            A.w = fmaf(v[q].w, fn, A.w * fo);
-            Ls = fmaf(ml[q].y, fn, Ls * fo);
-            M = mn;
-          }
-        }
-      }
-      float* mine = ws + cw * RS;
-      if (has) reinterpret_cast<float4*>(mine)[lane] = A;
-      if (lane == 0) {
-        mine[d] = M;
-        mine[d + 1] = Ls;
-      }
-      cbar();
-      for (int i = ct; i < d; i += NCT) {
-        float Mt = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) Mt = fmaxf(Mt, ws[w * RS + d]);
-        float Lt = 0.f, At = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-          const float mw = ws[w * RS + d];
-          if (mw != -INFINITY) {
-            const float f = exp2f(mw - Mt);
-            Lt = fmaf(ws[w * RS + d + 1], f, Lt);
-            At = fmaf(ws[w * RS + i], f, At);
-          }
-        }
-        o[h * d + i] = At / Lt;
-      }
-      cbar();
-    }
-    mark(TR_STAGES);
-    ab = finish(ab);
-    if (!ab) signal(p.cm.combine + l);
-    return ab;
-  }
-
-  // Nucleus (top-p) draw of request b = t.a[0] from the logits its LM tiles
-  // kept.  Rows are ordered by logit, descending, the lower index first among
-  // equal logits.  Each row's mass is w = exp((logit - max) / T) in float32,
-  // held as the integer round(w * 2^32), so every sum below is exact and does
-  // not depend on the order of the adds.  The nucleus is the shortest prefix
-  // of the order whose mass reaches ceil(top_p * total).  It is found by a
-  // radix search over a 32-bit key that sorts rows the same way (four 8-bit
-  // digits, one pass over the logits each), then, for equal logits at the
-  // cut, by index.  The token is the Gumbel-max draw of the temperature
-  // sampler restricted to the nucleus: the argmax of logit / T + noise over it.
-  __device__ static uint32_t desc_key(float l) {
-    const uint32_t u = __float_as_uint(l + 0.0f);   // -0 -> +0
-    return (u & 0x80000000u) ? u : (~u & 0x7fffffffu);
-  }
-
-  __device__ bool sample(const Task& t, bool ab) {
-    if (ab) return ab;
-    const int b = t.a[0], V = p.V, tiles = p.lm_tiles;
-    const float* lg = p.lg_keep + (size_t)b * V;
-    unsigned long long* hist = reinterpret_cast<unsigned long long*>(act);   // [256] masses
-    unsigned int* hcnt = reinterpret_cast<unsigned int*>(hist + 256);       // [256] row counts
-    unsigned long long* red = reinterpret_cast<unsigned long long*>(hcnt + 256);   // [NCT] scan / sums
-    unsigned long long& s_tgt = m->smp_tgt;
-    unsigned long long& s_before = m->smp_before;
-    uint32_t& s_prefix = m->smp_prefix;
-    int& s_digit = m->smp_digit;
-    int& s_cut = m->smp_cut;
-    float& s_max = m->smp_max;
-    const int pos = __ldcg(p.seq_len + b) + step;
-    const float it = p.inv_temp;
-    // the largest logit, from the tiles' maxima
-    if (cw == 0) {
-      float v = -INFINITY;
-      for (int i = lane; i < tiles; i += 32) v = fmaxf(v, __ldcg(p.lm_val + (size_t)b * tiles + i));
-#pragma unroll
-      for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
-      if (lane == 0) s_max = v;
-    }
-    cbar();
-    const float mx = s_max;
-    auto mass = [&](float l) -> unsigned long long {
-      return __float2ull_rn(expf((l - mx) * it) * 4294967296.0f);
-    };
-    // the total mass, then the target
-    {
-      unsigned long long z = 0;
-      for (int v = ct; v < V; v += NCT) z += mass(__ldcg(lg + v));
-      red[ct] = z;
-      cbar();
-      if (ct == 0) {
-        unsigned long long tot = 0;
-        for (int i = 0; i < NCT; ++i) tot += red[i];
-        unsigned long long tg = (unsigned long long)ceil((double)p.top_p * (double)tot);
-        s_tgt = tg < 1ull ? 1ull : (tg > tot ? tot : tg);
-        s_before = 0;
-        s_prefix = 0;
-      }
-      cbar();
-    }
-    // four digit passes: the digit where the running mass reaches the target
-    for (int pass = 0; pass < 4; ++pass) {
-      const int sh = 24 - 8 * pass;
-      for (int i = ct; i < 256; i += NCT) {
-        hist[i] = 0;
-        hcnt[i] = 0;
-      }
-      cbar();
-      const uint32_t pre = s_prefix;
-      for (int v = ct; v < V; v += NCT) {
-        const float l = __ldcg(lg + v);
-        const uint32_t k = desc_key(l);
-        if (pass > 0 && (k >> (sh + 8)) != pre) continue;
-        const int dg = (k >> sh) & 0xff;
-        atomicAdd(&hist[dg], mass(l));
-        atomicAdd(&hcnt[dg], 1u);
-      }
-      cbar();
-      if (cw == 0) {
-        // lane i holds digits 8i .. 8i + 7; an exclusive scan over lanes finds the digit
-        unsigned long long loc[8], sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          loc[j] = hist[lane * 8 + j];
-          sum += loc[j];
-        }
-        unsigned long long inc = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long y = __shfl_up_sync(FULL, inc, o);
-          if (lane >= o) inc += y;
-        }
-        const unsigned long long before = s_before, tgt = s_tgt;
-        unsigned long long run = before + inc - sum;   // mass of every digit below this lane's first
-        int found = -1;
-        unsigned long long found_before = 0;
-        for (int j = 0; j < 8; ++j) {
-          if (found < 0 && run + loc[j] >= tgt) {
-            found = lane * 8 + j;
-            found_before = run;
-          }
-          run += loc[j];
-        }
-        const unsigned ok = __ballot_sync(FULL, found >= 0);
-        const int src = ok ? __ffs(ok) - 1 : 31;
-        const int dsel = __shfl_sync(FULL, ok ? found : 255, src);
-        const unsigned long long bsel = __shfl_sync(FULL, ok ? found_before : before, src);
-        const unsigned long long all = __shfl_sync(FULL, inc, 31);   // this pass's whole mass
-        if (lane == 0) {
-          // the digits' masses always reach the target (they add up to the
-          // digit chosen by the pass before); kept safe regardless: the last
-          // occupied digit
-          int d = dsel;
-          unsigned long long bb = bsel;
-          if (!ok) {
-            d = 255;
-            while (d > 0 && hcnt[d] == 0) --d;
-            bb = before + all - hist[d];
-          }
-          s_digit = d;
-          s_before = bb;
-          s_prefix = (s_prefix << 8) | (uint32_t)d;
-        }
-      }
-      cbar();
-    }
-    const uint32_t kcut = s_prefix;
-    // equal logits at the cut: rows in index order until the target is reached
-    int vcut = V;
-    if (hcnt[s_digit] > 1) {
-      const int per = (V + NCT - 1) / NCT, v0 = ct * per, v1 = min(V, v0 + per);
-      unsigned long long mine = 0;
-      for (int v = v0; v < v1; ++v) {
-        const float l = __ldcg(lg + v);
-        if (desc_key(l) == kcut) mine += mass(l);
-      }
-      red[ct] = mine;
-      cbar();
-      if (ct == 0) {
-        unsigned long long run = s_before;
-        int owner = NCT - 1;
-        for (int i = 0; i < NCT; ++i) {
-          if (run + red[i] >= s_tgt) { owner = i; break; }
-          run += red[i];
-        }
-        s_cut = owner;
-        red[NCT - 1] = run;   // mass before the owner's range (the owner reads it back)
-      }
-      cbar();
-      if (ct == s_cut) {
-        unsigned long long run = red[NCT - 1];
-        int c = v1 - 1;
-        for (int v = v0; v < v1; ++v) {
-          const float l = __ldcg(lg + v);
-          if (desc_key(l) != kcut) continue;
-          run += mass(l);
-          if (run >= s_tgt) { c = v; break; }
-        }
-        s_cut = c;
-      }
-      cbar();
-      vcut = s_cut;
-    }
-    // the draw: argmax of the temperature keys over the nucleus
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int v = ct; v < V; v += NCT) {
-      const float l = __ldcg(lg + v);
-      const uint32_t k = desc_key(l);
-      if (k > kcut || (k == kcut && v > vcut)) continue;
-      const float sv = fmaf(l, it, gumbel_noise((uint32_t)v, (uint32_t)pos, (uint32_t)(p.slot0 + b), p.seed_lo,
-                                                p.seed_hi));
-      if (sv > bv || (sv == bv && v < bi)) { bv = sv; bi = v; }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(FULL, bv, o);
-      const int oi = __shfl_xor_sync(FULL, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) {
-      m->best_v[cw] = bv;
-      m->best_i[cw] = bi;
-    }
-    cbar();
-    if (ct == 0) {
-      float v = -INFINITY;
-      int ix = 0x7fffffff;
-      for (int w = 0; w < NCW; ++w)
-        if (m->best_v[w] > v || (m->best_v[w] == v && m->best_i[w] < ix)) { v = m->best_v[w]; ix = m->best_i[w]; }
-      p.next_token[(size_t)step * p.io_stride + b] = ix;
-      if (step + 1 == p.nsteps) p.seq_len[b] = __ldcg(p.seq_len + b) + p.nsteps;
-    }
-    ab = finish(false);
-    if (!ab) signal(p.cm.sdone);
-    return ab;
-  }
-
-  // LM-head tile.  A CTA's LM tiles are the last tasks of its list: the first
-  // fills the final norm's activations (kept by the later tiles), and only the
-  // last takes the ticket, for all of this CTA's tiles at once.
-  __device__ bool lm(const Task& t, bool ab, bool last) {
-    const int L = p.L, B = p.B;
-    if (!ab && lm_done == 0) {
-      const float* xo = p.x_out + (size_t)(L - 1) * p.bcap * p.H;
-      fill_rmsnorm(p.final_norm, [&](int b, int i4) {
-        return __ldcg(reinterpret_cast<const float4*>(xo + (size_t)b * p.H) + i4);
-      });
-    }
-    // nucleus sampling: this tile keeps its logits and finds their plain
-    // maximum; the request's T_SAMPLE task draws from them afterwards
-    const bool keep = p.lg_keep != nullptr;
-    const bool sampled = p.inv_temp > 0.f && !keep;
-    int* pos = reinterpret_cast<int*>(scr);   // each request's position: the noise counter
-    if (sampled && ct < B) pos[ct] = __ldcg(p.seq_len + ct) + step;
-    cbar();
-    ++lm_done;
-    mark(TR_ACT);
-    // each thread keeps, per activation row, the best (value, lowest index) it saw
-    float bv[NB];
-    int bi[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      bv[j] = -INFINITY;
-      bi[j] = 0x7fffffff;
-    }
-    float* lg = p.logits ? p.logits + (size_t)step * p.io_stride * p.V : nullptr;
-    ab = gemv<false, SP_LM>(p.H, t.a[0], t.a[1], act, p.H, nullptr, B, ab, [&](int row, int j, float s0, float) {
-      float s = m->inv[j] * s0;
-      if (lg) lg[(size_t)j * p.V + row] = s;
-      if (keep) p.lg_keep[(size_t)j * p.V + row] = s;
-      if (sampled)   // Gumbel-max: the argmax of the perturbed, scaled logits is a draw from softmax(logits / T)
-        s = fmaf(s, p.inv_temp,
-                 gumbel_noise((uint32_t)row, (uint32_t)pos[j], (uint32_t)(p.slot0 + j), p.seed_lo, p.seed_hi));
-#pragma unroll
-      for (int jj = 0; jj < NB; ++jj)
-        if (jj == j && (s > bv[jj] || (s == bv[jj] && row < bi[jj]))) {
-          bv[jj] = s;
-          bi[jj] = row;
-        }
-    });
-    mark(TR_STAGES);
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(FULL, bv[j], o);
-        const int oi = __shfl_xor_sync(FULL, bi[j], o);
-        if (ov > bv[j] || (ov == bv[j] && oi < bi[j])) {
-          bv[j] = ov;
-          bi[j] = oi;
-        }
-      }
-      if (!ab && lane == 0 && j < B) {
-        m->best_v[cw * MAX_BATCH + j] = bv[j];
-        m->best_i[cw * MAX_BATCH + j] = bi[j];
-      }
-    }
-    ab = cbar_or(ab);
-    if (ab) return ab;
-    const int tiles = p.lm_tiles, tile = t.a[2];
-    if (ct < B) {
-      float v = -INFINITY;
-      int ix = 0x7fffffff;
-      for (int w = 0; w < NCW; ++w) {
-        const float wv = m->best_v[w * MAX_BATCH + ct];
-        const int wi = m->best_i[w * MAX_BATCH + ct];
-        if (wv > v || (wv == v && wi < ix)) { v = wv; ix = wi; }
-      }
-      p.lm_val[(size_t)ct * tiles + tile] = v;
-      p.lm_idx[(size_t)ct * tiles + tile] = ix;
-    }
-    if (!last) return ab;   // the last tile's barrier orders these writes before its ticket
-    ab = finish(ab);
-    if (ab) return ab;
-    if (ticket(p.cm.lm, (uint32_t)t.a[3], (uint32_t)lm_done) && !keep) {
-      if (cw < B) {
-        const int b = cw;
-        float v = -INFINITY;
-        int ix = 0x7fffffff;
-        for (int i = lane; i < tiles; i += 32) {
-          const float tv = __ldcg(p.lm_val + (size_t)b * tiles + i);
-          const int tix = __ldcg(p.lm_idx + (size_t)b * tiles + i);
-          if (tv > v || (tv == v && tix < ix)) { v = tv; ix = tix; }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float ov = __shfl_xor_sync(FULL, v, o);
-          const int oi = __shfl_xor_sync(FULL, ix, o);
-          if (ov > v || (ov == v && oi < ix)) { v = ov; ix = oi; }
-        }
-        if (lane == 0) {
-          p.next_token[(size_t)step * p.io_stride + b] = ix;
-          // positions stay those of the launch's start until its last step is done
-          if (step + 1 == p.nsteps) p.seq_len[b] = __ldcg(p.seq_len + b) + p.nsteps;
-        }
-      }
-      ab = finish(false);
-      if (!ab) signal(p.cm.sdone);   // the next step's first layer may read these tokens
-    }
-    return ab;
-  }
-
-  __device__ void run(int t0, int t1) {
-    for (step = 0; step < p.nsteps; ++step) {
-      epoch = p.epoch + (uint32_t)step;
-      lm_done = 0;
-      if (!run_step(t0, t1)) return;
-    }
-  }
-
-  // One pass over this CTA's tasks for step `step`; false once a wait gave up.
-  __device__ bool run_step(int t0, int t1) {
-    for (ti = t0; ti < t1; ++ti) {
-      const Task t = ldg_task(p.tasks + ti);
-      if (ti + 1 < t1) prefetch_l1(p.tasks + ti + 1);   // the next record arrives while this task runs
-      bool ab = false;
-      nstage_seen = 0;
-      mark(TR_FETCH);
-      if (ct == 0) {
-        // the first layer of a later step starts from the previous step's tokens
-        if (t.wait_ctr < 0 && step > 0)
-          ab = !wait_ctr(p, p.cm.sdone, epoch - 1u, (uint32_t)p.sdone_cnt, ti);
-        else
-          ab = !wait_ctr(p, t.wait_ctr, epoch, t.wait_cnt, ti);
-      }
-      ab = cbar_or(ab);
-      if (ab) return false;
-      mark(TR_DEP);
-      switch (t.type) {
-        case T_QKV:
-        case T_OPROJ: {
-          ProjGemv g;
-          if constexpr (NB > 2) {   // the O projection may run in K halves
-            const int parts = t.type == T_OPROJ ? p.o_halves : 1;
-            for (int h = 0; h < parts; ++h) {
-              ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g, h);
-              if (h == 0) mark(TR_ACT);
-              ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
-            }
-          } else {
-            ab = t.type == T_QKV ? prep_qkv(t, ab, g) : prep_oproj(t, ab, g, 0);
-            mark(TR_ACT);
-            ab = gemv<false, SP_PROJ>(g.K, g.r0, g.r1, act, g.K, nullptr, p.B, ab, g.epi);   // the one plain call site
-          }
-          mark(TR_STAGES);
-          ab = post_proj(t, ab);
-          break;
-        }
-        case T_ATTN: ab = attn(t, ab); break;
-        case T_MOE: ab = moe(t, ab); break;
-        case T_RED: ab = red(t, ab); break;
-        case T_LM: ab = lm(t, ab, ti + 1 == t1 || ldg_task(p.tasks + ti + 1).type != T_LM); break;
-        case T_COMB: ab = comb(t, ab); break;
-        case T_SAMPLE: ab = sample(t, ab); break;
-        default: ab = true;
-      }
-      if (ab) return false;
-      mark(TR_DONE);
-    }
-    return true;
-  }
-};
-
-// Wait (bounded) for every bulk copy still in flight before the CTA exits.
-__device__ void drain(const Params& p, Misc* m, int nst) {
-  for (int s = 0; s < nst; ++s) {
-    const int rd = m->armed[s];
-    if (rd < 0) continue;
-    const uint64_t t0 = gtimer();
-    while (!mbar_try_wait(&m->full[s], rd & 1)) {
-      if (gtimer() - t0 > p.timeout_ns) {
-        set_error(p, MK_ERR_DEP_TIMEOUT, -1, -5);
-        break;
-      }
-    }
-  }
-}
-
-template <int NB>
-__global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  Misc* m = reinterpret_cast<Misc*>(smem + p.misc_off);
-  float* act = reinterpret_cast<float*>(smem + p.act_off);
-  float* scr = reinterpret_cast<float*>(smem + p.misc_off + sizeof(Misc));
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int s = 0; s < p.nstages; ++s) {
-      mbar_init(&m->full[s], 1);
-      mbar_init(&m->empty[s], NCW);
-      m->armed[s] = -1;
-    }
-    m->abort_flag = 0;
-    m->r_layer = -1;
-    m->dead = failed(p) ? 1 : 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  if (!m->dead) {
-    const int t0 = p.cta_start[blockIdx.x], t1 = p.cta_start[blockIdx.x + 1];
-    Ring ring{smem, m, p.nstages, p.stage_bytes, 0, 0};
-    if (tid >= NCT) {
-      if (tid == NCT) {
-        Producer<NB> pr{p, ring, evict_first_policy()};
-        pr.run(t0, t1);
-      }
-    } else {
-      Consumer<NB> c{p, ring, act, m, scr, reinterpret_cast<float*>(smem + p.psum_off), tid, tid >> 5, tid & 31};
-      c.run(t0, t1);
-    }
-  }
-  __syncthreads();
-  if (tid == 0) drain(p, m, p.nstages);
-}
 
 __global__ void k_rope_table(float2* tab, int npos, int half, int d, double theta) {
   const long long n = (long long)npos * half;
@@ -2772,48 +21,17 @@ __global__ void k_rope_table(float2* tab, int npos, int half, int d, double thet
   }
 }
 
-template <int NB>
-cudaError_t set_smem_attr() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(mk_megakernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
-  if (e == cudaSuccess) done = true;
-  return e;
-}
-
-template <int NB>
-cudaError_t launch_nb(const Params& p, int grid, int smem, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<NB>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mk_megakernel<NB>, p);
-}
-
-template <int NB>
-int occupancy(int smem) {
-  if (set_smem_attr<NB>() != cudaSuccess) return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mk_megakernel<NB>, NTHREADS, smem) != cudaSuccess) return 0;
-  return n;
-}
-
 }  // namespace
 
+// The nucleus-draw instance runs only when the LM tiles keep their logits
+// for the draw tasks; every other step takes the plain instance.
 cudaError_t launch_megakernel(const Params& p, int nb, int grid, int smem, cudaStream_t st) {
+  if (p.lg_keep) return launch_megakernel_nuc(p, nb, grid, smem, st);
   switch (nb) {
-    case 1: return launch_nb<1>(p, grid, smem, st);
-    case 2: return launch_nb<2>(p, grid, smem, st);
-    case 4: return launch_nb<4>(p, grid, smem, st);
-    case 8: return launch_nb<8>(p, grid, smem, st);
+    case 1: return launch_nb<1, false>(p, grid, smem, st);
+    case 2: return launch_nb<2, false>(p, grid, smem, st);
+    case 4: return launch_nb<4, false>(p, grid, smem, st);
+    case 8: return launch_nb<8, false>(p, grid, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -2828,14 +46,18 @@ cudaError_t launch_rope_table(float2* tab, int npos, int d, double theta, cudaSt
   return cudaGetLastError();
 }
 
+// Resident CTAs per SM of both instances (the smaller of the two).
 int max_active_ctas(int nb, int smem) {
+  int n = 0;
   switch (nb) {
-    case 1: return occupancy<1>(smem);
-    case 2: return occupancy<2>(smem);
-    case 4: return occupancy<4>(smem);
-    case 8: return occupancy<8>(smem);
+    case 1: n = occupancy<1, false>(smem); break;
+    case 2: n = occupancy<2, false>(smem); break;
+    case 4: n = occupancy<4, false>(smem); break;
+    case 8: n = occupancy<8, false>(smem); break;
     default: return 0;
   }
+  const int m = max_active_ctas_nuc(nb, smem);
+  return n < m ? n : m;
 }
 
 size_t misc_bytes() { return sizeof(Misc); }
