@@ -117,6 +117,7 @@ typedef struct mk_plan_opts {
   float temperature; /* sampling from the first step, as mk_plan_set_sampling; 0 -> greedy */
   unsigned long long seed;
   float top_p;       /* nucleus sampling from the first step, as mk_plan_set_top_p; 0 -> 1 (off) */
+  const int* chunk_first; /* prefill chunks of the first batch, as mk_plan_update_rows (host, nullable) */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;
@@ -196,6 +197,24 @@ int mk_decode_step_host(mk_plan* plan, const int* h_tokens, float* h_logits, int
  * clears a recorded device error.  No kernel is launched. */
 int mk_plan_update(mk_plan* plan, int batch, const int* seq_lens, const int* page_table,
                    int max_pages_per_seq, mk_stream stream);
+
+/* Prefill: the same update where some rows are prefill chunks (the pages
+ * speak of serving prompts, not of how they enter the cache; here a prompt
+ * enters the paged cache through the decode tasks, up to 8 tokens per launch).
+ * chunk_first[b] (host int32[batch], NULL = every row its own request) is
+ * the first row of the chunk row b belongs to: rows chunk_first[b] .. b are
+ * consecutive prompt tokens of ONE request, row b at position seq_lens[b] =
+ * seq_lens[b - 1] + 1, with the same page-table row (the request's pages;
+ * a page for the last row's position must be there).  Each row appends its
+ * token's K/V and attends causally to the request's cache and the chunk's
+ * earlier rows; its next token is the model's prediction after it (the last
+ * row's is the first output).  Rows of different chunks or requests may not
+ * share a page; in a plan with a capacity above 8 a chunk may not cross a
+ * multiple of 8 rows (one sub-plan).  A batch with chunks runs exactly one
+ * mk_decode_step (MK_ERR_INVALID for a second step or mk_decode_steps with
+ * n_steps > 1) before the next update.  MK_ERR_INVALID for a malformed chunk. */
+int mk_plan_update_rows(mk_plan* plan, int batch, const int* seq_lens, const int* page_table,
+                        int max_pages_per_seq, const int* chunk_first, mk_stream stream);
 
 /* Wait for `stream`, then return the device status (MK_OK or the first error
  * a step recorded). */
@@ -330,7 +349,11 @@ int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weights* w, const
  *   - every step feeds each admitted request one token: its prompt tokens in
  *     order (the prediction of a prompt step is discarded, except after the
  *     last prompt token: that one is the first output), then its own
- *     previous output.  The prompt's K/V thus come from decode steps;
+ *     previous output.  With prefill chunks (mk_sched_set_prefill) a request
+ *     still in its prompt may take several rows of the step: after one row
+ *     per admitted request, the spare rows go to prompts in batch order, up
+ *     to the chunk size and the prompt's remaining tokens each (above 8 rows
+ *     a chunk also ends at the next multiple of 8);
  *   - retirement: after max_new_tokens outputs, or right after the request
  *     outputs eos_token (eos_token < 0: none); its pages and slot are freed
  *     at once, and the batch keeps the order of the requests that remain.
@@ -351,6 +374,21 @@ int mk_sched_create(int num_pages, int page_size, int max_batch, int max_pages_p
 int mk_sched_submit(mk_sched* s, long long rid, const int* prompt, int n_prompt, int max_new_tokens,
                     int eos_token);
 
+/* Prefill chunks: a request still in its prompt may feed up to max_chunk
+ * (1 .. 8) prompt tokens in one step, as consecutive rows (see
+ * mk_plan_update_rows).  1, the default, is one token per step.  Set it
+ * between steps (MK_ERR_INVALID while a batch is pending). */
+int mk_sched_set_prefill(mk_sched* s, int max_chunk);
+
+/* The next step's rows (mk_sched_next with prefill chunks): like
+ * mk_sched_next, with rows instead of requests (*rows of them, row arrays
+ * sized for max_batch rows) and chunk_first[r] = the first row of row r's
+ * request in this batch (r itself for a single row); a request's rows carry
+ * its consecutive positions and its page row.  *changed is also 1 whenever
+ * this batch or the previous one holds a chunk of several rows. */
+int mk_sched_next_rows(mk_sched* s, int* rows, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                       int* chunk_first, int* changed);
+
 /* Admit what fits, then describe the next step's batch in host arrays sized
  * for max_batch requests: *batch, seq_lens[b] (tokens cached), page_table[b *
  * max_pages_per_seq + i] (-1 past the request's pages), tokens[b] (the input
@@ -359,10 +397,11 @@ int mk_sched_submit(mk_sched* s, long long rid, const int* prompt, int n_prompt,
  * to run.  A non-empty batch must be committed (or abandoned) before the
  * next call, else MK_ERR_INVALID. */
 int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* tokens, long long* rids,
-                  int* changed);
+                  int* changed);   /* MK_ERR_INVALID with prefill chunks above 1 */
 
 /* The step of the last mk_sched_next ran: next_tokens[b] (host int32) is
- * request b's greedy output.  Advances every request by one position,
+ * the output of row b (request b without prefill chunks; the prediction
+ * after a request's last row is its output).  Advances every request by one position,
  * records outputs and retires finished requests.  MK_ERR_INVALID when no
  * batch is pending. */
 int mk_sched_commit(mk_sched* s, const int* next_tokens);
@@ -387,10 +426,10 @@ int mk_sched_stats(const mk_sched* s, int* out, int n);
 
 void mk_sched_destroy(mk_sched* s);
 
-/* One step of the serving loop on `stream`: mk_sched_next; when *plan is
- * NULL, mk_plan_create with that batch (capacity opts->max_batch, or the
+/* One step of the serving loop on `stream`: mk_sched_next_rows; when *plan
+ * is NULL, mk_plan_create with that batch (capacity opts->max_batch, or the
  * scheduler's max_batch when 0; a smaller capacity is MK_ERR_INVALID), else
- * mk_plan_update when the requests changed; mk_decode_step_host; then
+ * mk_plan_update_rows when the rows changed; mk_decode_step_host; then
  * mk_sched_commit.  dims, w and kv are read only when the plan is created
  * (kv->num_pages must be at least the scheduler's pool).  Returns the batch
  * size that ran (0: nothing queued or admitted) or an error; on an error the

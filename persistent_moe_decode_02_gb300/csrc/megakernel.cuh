@@ -2019,6 +2019,13 @@ struct Consumer {
     const float2* rope = p.rope + (size_t)pos * half;
     const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
     const bool has_new = pos >= tok0 && pos < tok1;
+    // a prefill row also sees the earlier rows of its chunk: their tokens sit
+    // at positions [pos - nprev, pos) of the same pages, written by their own
+    // attention tasks of this step, so their K (rotated at its position) and V
+    // are patched into the stages here from the QKV outputs, like the row's own
+    const int nprev = p.chunk0 ? b - __ldcg(p.chunk0 + b) : 0;
+    const int pq0 = max(tok0, pos - nprev), pq1 = min(tok1, pos + 1);   // patched positions
+    const float* qkv_rows = p.qkv + (size_t)l * p.bcap * p.qkv_rows + (size_t)g * (G + 2) * d + (size_t)G * d;
     if (!ab) {
       for (int idx = ct; idx < MAX_G * half; idx += NCT) {
         const int h = idx / half, i = idx - h * half;
@@ -2104,28 +2111,38 @@ struct Consumer {
     for (int pg = pg0; pg < pg1; pg += ppg, ++si) {
       const int npg = min(ppg, pg1 - pg);
       const uint8_t* st = wait_stage(ab);
-      if (st && has_new && pos / PS >= pg && pos / PS < pg + npg) {
-        // put the new token's K and V into its stage slot before anyone reads the
-        // page, and zero the page's later slots: they hold no token yet, and
-        // although their scores are masked, their V still enters the P.V product
-        // (0 * NaN would poison the output)
+      const bool patch = pq0 < pq1 && pq0 / PS < pg + npg && (pq1 - 1) / PS >= pg;
+      if (st && patch) {
+        // put the new token's K and V (and those of the earlier rows of a
+        // prefill chunk) into their stage slots before anyone reads the pages,
+        // and zero the slots after the new token: they hold no token yet, and
+        // although their scores are masked, their V still enters the P.V
+        // product (0 * NaN would poison the output)
         cbar();
-        const int pi = pos / PS - pg, slot = pos % PS;
-        uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
-        uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
-        for (int i = ct; i < d * PS; i += NCT) {
-          const int dim = i / PS, sl = i - dim * PS;
-          if (sl == slot) {
-            kp[i] = f2bf(kn_s[dim]);
-            vp[i] = f2bf(vn_s[dim]);
-          } else if (sl > slot) {
-            kp[i] = 0;
-            vp[i] = 0;
+        const int pa = max(pg, pq0 / PS), pb = min(pg + npg - 1, (pq1 - 1) / PS);
+        for (int i = ct; i < (pb - pa + 1) * d * PS; i += NCT) {
+          const int pi = pa - pg + i / (d * PS), e = i % (d * PS);
+          const int dim = e / PS, sl = e - dim * PS, q = (pg + pi) * PS + sl;
+          uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
+          uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
+          if (q == pos) {
+            kp[e] = f2bf(kn_s[dim]);
+            vp[e] = f2bf(vn_s[dim]);
+          } else if (q > pos) {
+            kp[e] = 0;
+            vp[e] = 0;
+          } else if (q >= pq0) {   // an earlier row of the chunk, b - (pos - q)
+            const float* kr = qkv_rows + (size_t)(b - (pos - q)) * p.qkv_rows;
+            const int i0 = dim < half ? dim : dim - half;
+            const float2 cs = p.rope[(size_t)q * half + i0];
+            const float a = __ldcg(kr + i0), c = __ldcg(kr + i0 + half);
+            kp[e] = f2bf(dim < half ? a * cs.x - c * cs.y : c * cs.x + a * cs.y);
+            vp[e] = f2bf(__ldcg(kr + d + dim));
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         cbar();
-      } else if (has_new && pos / PS >= pg && pos / PS < pg + npg) {
+      } else if (patch) {
         cbar();
         cbar();
       }

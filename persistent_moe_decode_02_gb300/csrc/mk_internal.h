@@ -132,6 +132,11 @@ struct Params {
   int cf_pairs;         // most (expert, unit) pairs of one expert tile
   int* seq_len;         // device [bcap]
   const int* page_table;  // device [bcap * max_pages]
+  // prefill chunks: row b belongs to the chunk of one request that starts at
+  // row chunk0[b] <= b (rows chunk0[b] .. b hold the request's consecutive
+  // prompt positions seq_len[b] - (b - chunk0[b]) .. seq_len[b] and share its
+  // page row); null: every row is a request of its own
+  const int* chunk0;
   const float2* rope;   // [max_pos][d/2] (cos, sin)
   int rope_npos;
   // per-layer scratch (fp32 unless noted), all strided by bcap

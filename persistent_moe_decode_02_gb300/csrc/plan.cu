@@ -353,6 +353,9 @@ struct mk_plan {
   int slot0 = 0;                   // batch slot of the first request (sub-plan i of a group: 8 i)
   unsigned long long timeout_ns = 0;
   std::vector<int> seq, pt, open_start;
+  std::vector<int> chunk0;         // rows' prefill chunk starts (empty: no chunks)
+  int* d_chunk0 = nullptr;
+  bool chunk_stepped = false;      // a step ran on a batch with prefill chunks (an update must come next)
   std::vector<Task> tasks;
   std::vector<int> cta_start;
   Counts cnt;
@@ -409,18 +412,35 @@ void dfree(mk_plan* p, void* ptr) {
 
 bool aligned16(const void* q) { return q && ((uintptr_t)q % 16) == 0; }
 
+// chunk_first (nullable): row b is part of the prefill chunk that starts at
+// row chunk_first[b] <= b.  A chunk's rows are consecutive, hold consecutive
+// positions of one request and the same page row; rows of different chunks
+// may not share a page.  group: rows per sub-plan (a chunk stays inside one).
 int validate_batch(const Shape& s, int B, const int* seq_lens, const int* page_table, int max_pages,
-                   int num_pages) {
+                   int num_pages, const int* chunk_first = nullptr, int group = 0) {
   if (!seq_lens || !page_table || max_pages < 1) return MK_ERR_INVALID;
   std::vector<char> used((size_t)num_pages, 0);
   for (int b = 0; b < B; ++b) {
     if (seq_lens[b] < 0) return MK_ERR_INVALID;
     const int np = pages_for(seq_lens[b], s.ps);
     if (np > max_pages) return MK_ERR_CAPACITY;
+    const int c = chunk_first ? chunk_first[b] : b;
+    if (c != b) {   // a later row of a chunk: the previous row's request, one position on
+      if (c < 0 || c > b || chunk_first[b - 1] != c || seq_lens[b] != seq_lens[b - 1] + 1) return MK_ERR_INVALID;
+      if (group > 0 && c / group != b / group) return MK_ERR_INVALID;
+      for (int i = 0; i < np; ++i) {
+        const int pg = page_table[(size_t)b * max_pages + i];
+        if (pg < 0 || pg >= num_pages) return MK_ERR_INVALID;
+        const int pc = i < pages_for(seq_lens[b - 1], s.ps) ? page_table[(size_t)(b - 1) * max_pages + i] : -1;
+        if (pc >= 0 ? pg != pc : used[pg] != 0) return MK_ERR_INVALID;   // same pages as the chunk, new ones unused
+        used[pg] = 1;
+      }
+      continue;
+    }
     for (int i = 0; i < np; ++i) {
       const int pg = page_table[(size_t)b * max_pages + i];
       if (pg < 0 || pg >= num_pages) return MK_ERR_INVALID;
-      if (used[pg]) return MK_ERR_INVALID;  // two positions may not share a page
+      if (used[pg]) return MK_ERR_INVALID;  // two requests may not share a page
       used[pg] = 1;
     }
   }
@@ -538,12 +558,13 @@ int commit_built(mk_plan* p, Built& b, cudaStream_t st, bool with_batch) {
       return MK_ERR_CUDA;
     p->part_cap_slots = cap;
   }
-  Up ups[4];
+  Up ups[5];
   int nu = 0;
   ups[nu++] = {p->d_tasks, tasks.data(), tbytes};
   ups[nu++] = {(uint8_t*)p->d_tasks + tbytes, cs.data(), cs.size() * sizeof(int)};
   if (with_batch) {
     ups[nu++] = {p->d_seq, p->seq.data(), (size_t)p->B * sizeof(int)};
+    if (!p->chunk0.empty()) ups[nu++] = {p->d_chunk0, p->chunk0.data(), (size_t)p->B * sizeof(int)};
     ups[nu++] = {p->d_pt, p->pt.data(), p->pt.size() * sizeof(int)};
   }
   if (upload_many(p, st, ups, nu) != cudaSuccess) return MK_ERR_CUDA;
@@ -590,6 +611,7 @@ void fill_params(mk_plan* p) {
   P.timeout_ns = p->timeout_ns; P.cm = p->cm; P.rm = p->rm;
   P.nstages = p->nstages; P.stage_bytes = p->stage_bytes;
   P.seq_len = p->d_seq; P.page_table = p->d_pt; P.rope = p->d_rope; P.rope_npos = p->rope_npos;
+  P.chunk0 = p->chunk0.empty() ? nullptr : p->d_chunk0;
   P.part = p->d_part; P.part_slots = (int)p->part_cap_slots;
   P.lm_tiles = p->cnt.lm; P.down_rows_max = p->cnt.down_rows_max;
   P.cf_pairs = std::max(1, mk::cf_floats(s.E, s.k, s.F, p->C, p->bcap) / p->bcap);
@@ -649,6 +671,16 @@ static bool temperature_ok(float t) {
 }
 
 
+// The rows' prefill chunk starts, kept only when some row continues a chunk.
+static void set_chunks(mk_plan* p, int batch, const int* chunk_first) {
+  p->chunk0.clear();
+  p->chunk_stepped = false;
+  if (!chunk_first) return;
+  bool any = false;
+  for (int b = 0; b < batch; ++b) any |= chunk_first[b] != b;
+  if (any) p->chunk0.assign(chunk_first, chunk_first + batch);
+}
+
 static void destroy_one(mk_plan* p);
 
 static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
@@ -675,7 +707,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
         !aligned16(w->w_down[l]) || !aligned16(kv->k_pool[l]) || !aligned16(kv->v_pool[l]))
       return MK_ERR_INVALID;
   }
-  rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages);
+  rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages, o.chunk_first);
   if (rc != MK_OK) return rc;
   if (!temperature_ok(o.temperature)) {
     mk::set_last_error("mk_plan_create: temperature must be 0 (greedy) or a finite value whose inverse is finite");
@@ -708,6 +740,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->num_pages = kv->num_pages;
   p->seq.assign(seq_lens, seq_lens + batch);
   p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
+  set_chunks(p, batch, o.chunk_first);
   p->cm.init(s.L, s.nkv, bcap);
   p->rm.init(std::min(s.E, bcap * s.k), bcap);
 
@@ -779,6 +812,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   ok &= dalloc(p, &p->d_ctr, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t)) == cudaSuccess;
   ok &= dalloc(p, &p->d_status, 4 * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &p->d_seq, (size_t)bcap * sizeof(int)) == cudaSuccess;
+  ok &= dalloc(p, &p->d_chunk0, (size_t)bcap * sizeof(int)) == cudaSuccess;
   p->pt_cap = (size_t)bcap * max_pages_per_seq;
   ok &= dalloc(p, &p->d_pt, p->pt_cap * sizeof(int)) == cudaSuccess;
   ok &= dalloc(p, &P.qkv, L * bcap * s.qkv_rows * sizeof(float)) == cudaSuccess;
@@ -826,10 +860,13 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
 
 // n_steps decode steps in one launch; step s's next tokens go to row s of
 // d_next_token (rows io_stride apart) and feed step s + 1 on the device.
-static int steps_one(mk_plan* p, const int* d_tokens, int n_steps, float* d_logits, int* d_next_token,
-                     int io_stride, mk_stream stream) {
-  if (!p || !d_tokens || !d_next_token || n_steps < 1 || io_stride < p->B) return MK_ERR_INVALID;
-  cudaStream_t st = (cudaStream_t)stream;
+// The checks of a launch of n_steps, with no side effect: a group checks
+// every sub-plan before it launches any.
+static int steps_check(const mk_plan* p, int n_steps) {
+  if (!p->chunk0.empty() && (n_steps > 1 || p->chunk_stepped)) {
+    mk::set_last_error("a batch with prefill chunks runs one step, then needs mk_plan_update_rows");
+    return MK_ERR_INVALID;
+  }
   const Shape& s = p->s;
   for (int b = 0; b < p->B; ++b) {   // every position this launch writes needs its page
     for (int k = 0; k < n_steps; ++k) {
@@ -839,6 +876,16 @@ static int steps_one(mk_plan* p, const int* d_tokens, int n_steps, float* d_logi
       if (pg < 0 || pg >= p->num_pages) return MK_ERR_CAPACITY;
     }
   }
+  return MK_OK;
+}
+
+static int steps_one(mk_plan* p, const int* d_tokens, int n_steps, float* d_logits, int* d_next_token,
+                     int io_stride, mk_stream stream) {
+  if (!p || !d_tokens || !d_next_token || n_steps < 1 || io_stride < p->B) return MK_ERR_INVALID;
+  int rc0 = steps_check(p, n_steps);
+  if (rc0 != MK_OK) return rc0;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Shape& s = p->s;
   if (needs_replan(p) || p->nucleus_built != nucleus_on(p)) {
     int rc = replan(p, st);
     if (rc != MK_OK) return rc;
@@ -875,6 +922,7 @@ static int steps_one(mk_plan* p, const int* d_tokens, int n_steps, float* d_logi
   if (e != cudaSuccess) return note_cuda(e, "megakernel launch");
   p->epoch += (uint32_t)n_steps;
   for (int b = 0; b < p->B; ++b) p->seq[b] += n_steps;
+  if (!p->chunk0.empty()) p->chunk_stepped = true;
   return MK_OK;
 }
 
@@ -908,10 +956,10 @@ static int step_host_one(mk_plan* p, const int* h_tokens, float* h_logits, int* 
 // The first half of an update: checks, device capacity, and the new batch on
 // the host side of the plan.
 static int update_prepare(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                          cudaStream_t st) {
+                          cudaStream_t st, const int* chunk_first = nullptr) {
   if (!p || batch < 1) return MK_ERR_INVALID;
   if (batch > p->bcap) return MK_ERR_CAPACITY;
-  int rc = validate_batch(p->s, batch, seq_lens, page_table, max_pages_per_seq, p->num_pages);
+  int rc = validate_batch(p->s, batch, seq_lens, page_table, max_pages_per_seq, p->num_pages, chunk_first);
   if (rc != MK_OK) return rc;
   if ((size_t)p->bcap * max_pages_per_seq > p->pt_cap || max_pages_per_seq * p->s.ps > p->rope_npos) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
@@ -933,6 +981,7 @@ static int update_prepare(mk_plan* p, int batch, const int* seq_lens, const int*
   p->max_pages = max_pages_per_seq;
   p->seq.assign(seq_lens, seq_lens + batch);
   p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
+  set_chunks(p, batch, chunk_first);
   return MK_OK;
 }
 
@@ -946,9 +995,9 @@ static int update_commit(mk_plan* p, Built& b, cudaStream_t st) {
 }
 
 static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                      mk_stream stream) {
+                      mk_stream stream, const int* chunk_first = nullptr) {
   cudaStream_t st = (cudaStream_t)stream;
-  int rc = update_prepare(p, batch, seq_lens, page_table, max_pages_per_seq, st);
+  int rc = update_prepare(p, batch, seq_lens, page_table, max_pages_per_seq, st, chunk_first);
   if (rc != MK_OK) return rc;
   Built b;
   build_for(p, b);
@@ -1060,13 +1109,28 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   const int bcap = o.max_batch > 0 ? o.max_batch : batch;
   if (bcap <= mk::MAX_BATCH) return create_one(dims, w, kv, batch, seq_lens, page_table, max_pages_per_seq, opts, out);
   if (batch < 1 || batch > bcap || !seq_lens || !page_table || max_pages_per_seq < 1) return MK_ERR_INVALID;
+  const int M = mk::MAX_BATCH;
+  if (o.chunk_first) {   // prefill chunks: each stays inside one sub-plan
+    Shape s;
+    int rc = check_dims(dims, s);
+    if (rc != MK_OK) return rc;
+    if (!kv) return MK_ERR_INVALID;
+    rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages, o.chunk_first, M);
+    if (rc != MK_OK) return rc;
+  }
   mk_plan* g = new (std::nothrow) mk_plan();
   if (!g) return MK_ERR_CUDA;
-  const int M = mk::MAX_BATCH;
   for (int i = 0; i * M < bcap; ++i) {
     const int n = std::max(0, std::min(M, batch - i * M));
     mk_plan_opts so = o;
     so.max_batch = std::min(M, bcap - i * M);
+    std::vector<int> cf;
+    so.chunk_first = nullptr;
+    if (o.chunk_first && n > 0) {
+      cf.resize(n);
+      for (int b = 0; b < n; ++b) cf[b] = o.chunk_first[i * M + b] - i * M;
+      so.chunk_first = cf.data();
+    }
     // an idle sub-plan is built over the group's first request and stepped
     // only once an update gives it requests of its own
     const int* sl = n > 0 ? seq_lens + (size_t)i * M : seq_lens;
@@ -1088,9 +1152,21 @@ int mk_plan_create(const mk_model_dims* dims, const mk_weights* w, const mk_kv* 
   return MK_OK;
 }
 
+// A group's sub-plans that hold requests all pass their checks, or none runs.
+static int group_check(const mk_plan* p, int n_steps) {
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = steps_check(p->subs[i], n_steps);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
 int mk_decode_step(mk_plan* p, const int* d_tokens, float* d_logits, int* d_next_token, mk_stream stream) {
   if (!p || p->subs.empty()) return step_one(p, d_tokens, d_logits, d_next_token, stream);
   if (!d_tokens || !d_next_token) return MK_ERR_INVALID;
+  const int rc0 = group_check(p, 1);
+  if (rc0 != MK_OK) return rc0;
   const size_t M = mk::MAX_BATCH, V = p->s.V;
   for (size_t i = 0; i < p->subs.size(); ++i) {
     if (p->sub_B[i] == 0) continue;
@@ -1105,6 +1181,8 @@ int mk_decode_steps(mk_plan* p, const int* d_tokens, int n_steps, float* d_logit
                     mk_stream stream) {
   if (!p || p->subs.empty()) return steps_one(p, d_tokens, n_steps, d_logits, d_next_tokens, p ? p->B : 0, stream);
   if (!d_tokens || !d_next_tokens || n_steps < 1) return MK_ERR_INVALID;
+  const int rc0 = group_check(p, n_steps);
+  if (rc0 != MK_OK) return rc0;
   // requests of different sub-plans are independent: each sub-plan runs its
   // n_steps in one launch of its own, writing its columns of the rows
   const size_t M = mk::MAX_BATCH, V = p->s.V;
@@ -1121,6 +1199,8 @@ int mk_decode_steps(mk_plan* p, const int* d_tokens, int n_steps, float* d_logit
 int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h_next_token, mk_stream stream) {
   if (!p || p->subs.empty()) return step_host_one(p, h_tokens, h_logits, h_next_token, stream);
   if (!h_tokens || !h_next_token) return MK_ERR_INVALID;
+  const int rc0 = group_check(p, 1);
+  if (rc0 != MK_OK) return rc0;
   const size_t M = mk::MAX_BATCH, V = p->s.V;
   for (size_t i = 0; i < p->subs.size(); ++i) {
     if (p->sub_B[i] == 0) continue;
@@ -1131,20 +1211,30 @@ int mk_decode_step_host(mk_plan* p, const int* h_tokens, float* h_logits, int* h
   return MK_OK;
 }
 
-int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
-                   mk_stream stream) {
-  if (!p || p->subs.empty()) return update_one(p, batch, seq_lens, page_table, max_pages_per_seq, stream);
+int mk_plan_update_rows(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                        const int* chunk_first, mk_stream stream) {
+  if (!p || p->subs.empty())
+    return update_one(p, batch, seq_lens, page_table, max_pages_per_seq, stream, chunk_first);
   if (batch < 1 || !seq_lens || !page_table || max_pages_per_seq < 1) return MK_ERR_INVALID;
   if (batch > p->bcap) return MK_ERR_CAPACITY;
-  cudaStream_t st = (cudaStream_t)stream;
   const int M = mk::MAX_BATCH;
+  // whole-batch check first: pages are shared only within a chunk, and a
+  // chunk stays inside one sub-plan
+  int rc = validate_batch(p->s, batch, seq_lens, page_table, max_pages_per_seq, p->subs[0]->num_pages, chunk_first, M);
+  if (rc != MK_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
   const size_t n = p->subs.size();
   std::vector<int> nb(n);
+  std::vector<std::vector<int>> cf(n);
   for (size_t i = 0; i < n; ++i) {
     nb[i] = std::max(0, std::min(M, batch - (int)i * M));
     if (nb[i] == 0) continue;
-    const int rc = update_prepare(p->subs[i], nb[i], seq_lens + i * M, page_table + i * M * max_pages_per_seq,
-                                  max_pages_per_seq, st);
+    if (chunk_first) {
+      cf[i].resize(nb[i]);
+      for (int b = 0; b < nb[i]; ++b) cf[i][b] = chunk_first[i * M + b] - (int)i * M;
+    }
+    rc = update_prepare(p->subs[i], nb[i], seq_lens + i * M, page_table + i * M * max_pages_per_seq,
+                        max_pages_per_seq, st, chunk_first ? cf[i].data() : nullptr);
     if (rc != MK_OK) return rc;
   }
   // the task lists are host work: one thread per sub-plan that holds requests
@@ -1155,13 +1245,18 @@ int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_t
   for (auto& t : th) t.join();
   for (size_t i = 0; i < n; ++i) {
     if (nb[i] > 0) {
-      const int rc = update_commit(p->subs[i], built[i], st);
+      rc = update_commit(p->subs[i], built[i], st);
       if (rc != MK_OK) return rc;
     }
     p->sub_B[i] = nb[i];
   }
   p->B = p->group_B = batch;
   return MK_OK;
+}
+
+int mk_plan_update(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
+                   mk_stream stream) {
+  return mk_plan_update_rows(p, batch, seq_lens, page_table, max_pages_per_seq, nullptr, stream);
 }
 
 int mk_plan_set_sampling(mk_plan* p, float temperature, unsigned long long seed) {

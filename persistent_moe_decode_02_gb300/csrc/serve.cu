@@ -8,8 +8,9 @@
 // megakernel as the engine of a server that admits requests continuously
 // into a paged KV cache with ragged lengths.  They leave the host policy
 // open; this one reserves each request's pages at admission, admits first
-// come first served, feeds the prompt through decode steps and retires on a
-// token budget or an end token (see include/mk.h).
+// come first served, feeds the prompt through the decode tasks (one token per
+// step, or prefill chunks of several rows) and retires on a token budget or an
+// end token (see include/mk.h).
 #include <algorithm>
 #include <deque>
 #include <unordered_map>
@@ -31,6 +32,9 @@ struct mk_sched {
     bool done = false;
   };
   int num_pages = 0, ps = 0, max_batch = 0, max_pages = 0;
+  int max_chunk = 1;                    // prompt tokens a request may feed in one step (rows)
+  bool had_chunks = false;              // the last batch handed out held a multi-row chunk
+  std::vector<int> rows_of;             // rows each active request took in the pending batch
   std::vector<int> free_pages;          // a stack of free page ids
   std::deque<long long> queue;          // submitted, not admitted (arrival order)
   std::vector<long long> active;        // admitted, in batch order
@@ -89,10 +93,17 @@ int mk_sched_submit(mk_sched* s, long long rid, const int* prompt, int n_prompt,
   return MK_OK;
 }
 
-int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* tokens, long long* rids,
-                  int* changed) {
-  if (!s || !batch || !seq_lens || !page_table || !tokens || !rids || !changed)
-    return fail(MK_ERR_INVALID, "mk_sched_next: null argument");
+int mk_sched_set_prefill(mk_sched* s, int max_chunk) {
+  if (!s || max_chunk < 1 || max_chunk > 8) return fail(MK_ERR_INVALID, "mk_sched_set_prefill: max_chunk in 1 .. 8");
+  if (s->pending) return fail(MK_ERR_INVALID, "mk_sched_set_prefill: a batch is pending");
+  s->max_chunk = max_chunk;
+  return MK_OK;
+}
+
+int mk_sched_next_rows(mk_sched* s, int* rows, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                       int* chunk_first, int* changed) {
+  if (!s || !rows || !seq_lens || !page_table || !tokens || !rids || !chunk_first || !changed)
+    return fail(MK_ERR_INVALID, "mk_sched_next_rows: null argument");
   if (s->pending) return fail(MK_ERR_INVALID, "mk_sched_next: the previous batch was neither committed nor abandoned");
   // admission: first come, first served, while a slot and the head's pages are free
   while (!s->queue.empty() && (int)s->active.size() < s->max_batch) {
@@ -106,23 +117,54 @@ int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* 
     s->queue.pop_front();
     s->changed = true;
   }
-  const int B = (int)s->active.size();
-  for (int b = 0; b < B; ++b) {
-    const mk_sched::Req& r = s->reqs.at(s->active[b]);
-    const int np = (int)r.prompt.size();
-    seq_lens[b] = r.len;
-    tokens[b] = r.len < np ? r.prompt[r.len] : r.out.back();
-    rids[b] = s->active[b];
-    int* row = page_table + (size_t)b * s->max_pages;
-    for (int i = 0; i < s->max_pages; ++i) row[i] = i < (int)r.pages.size() ? r.pages[i] : -1;
+  // rows: one per request, then the spare rows to requests still in their
+  // prompt, in batch order, up to max_chunk each and the prompt's remaining
+  // tokens; above 8 rows a chunk ends at the next multiple of 8 (one launch)
+  const int A = (int)s->active.size();
+  s->rows_of.assign(A, 1);
+  int spare = s->max_batch - A;
+  for (int a = 0; a < A && spare > 0; ++a) {
+    const mk_sched::Req& r = s->reqs.at(s->active[a]);
+    const int left = (int)r.prompt.size() - r.len;
+    const int extra = std::min(spare, std::min(s->max_chunk, left) - 1);
+    if (extra > 0) {
+      s->rows_of[a] += extra;
+      spare -= extra;
+    }
   }
-  *batch = B;
-  *changed = B > 0 && s->changed ? 1 : 0;
-  if (B > 0) {
+  int row = 0;
+  bool chunks = false;
+  for (int a = 0; a < A; ++a) {
+    if (s->max_batch > 8) s->rows_of[a] = std::min(s->rows_of[a], 8 - row % 8);
+    const mk_sched::Req& r = s->reqs.at(s->active[a]);
+    const int np = (int)r.prompt.size();
+    for (int j = 0; j < s->rows_of[a]; ++j, ++row) {
+      seq_lens[row] = r.len + j;
+      tokens[row] = r.len + j < np ? r.prompt[r.len + j] : r.out.back();
+      rids[row] = s->active[a];
+      chunk_first[row] = row - j;
+      int* pr = page_table + (size_t)row * s->max_pages;
+      for (int i = 0; i < s->max_pages; ++i) pr[i] = i < (int)r.pages.size() ? r.pages[i] : -1;
+    }
+    chunks |= s->rows_of[a] > 1;
+  }
+  *rows = row;
+  *changed = row > 0 && (s->changed || chunks || s->had_chunks) ? 1 : 0;
+  if (row > 0) {
     s->pending = true;
     s->changed = false;
+    s->had_chunks = chunks;
   }
   return MK_OK;
+}
+
+int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                  int* changed) {
+  if (!s || !batch || !seq_lens || !page_table || !tokens || !rids || !changed)
+    return fail(MK_ERR_INVALID, "mk_sched_next: null argument");
+  if (s->max_chunk != 1) return fail(MK_ERR_INVALID, "mk_sched_next: prefill chunks need mk_sched_next_rows");
+  std::vector<int> cf(s->max_batch);
+  return mk_sched_next_rows(s, batch, seq_lens, page_table, tokens, rids, cf.data(), changed);
 }
 
 int mk_sched_commit(mk_sched* s, const int* next_tokens) {
@@ -130,11 +172,14 @@ int mk_sched_commit(mk_sched* s, const int* next_tokens) {
   if (!s->pending) return fail(MK_ERR_INVALID, "mk_sched_commit: no batch is pending");
   std::vector<long long> keep;
   keep.reserve(s->active.size());
+  int row = 0;
   for (size_t b = 0; b < s->active.size(); ++b) {
     mk_sched::Req& r = s->reqs.at(s->active[b]);
-    r.len += 1;
-    if (r.len >= (int)r.prompt.size()) {   // the input was the last prompt token or an output
-      const int tok = next_tokens[b];
+    const int n = s->rows_of[b];
+    r.len += n;
+    row += n;
+    if (r.len >= (int)r.prompt.size()) {   // the last row's input was the last prompt token or an output
+      const int tok = next_tokens[row - 1];
       r.out.push_back(tok);
       if ((int)r.out.size() >= r.max_new || (r.eos >= 0 && tok == r.eos)) r.done = true;
     }
@@ -199,10 +244,10 @@ int mk_serve_step(mk_sched* s, mk_plan** plan, const mk_model_dims* dims, const 
   if (!s || !plan) return fail(MK_ERR_INVALID, "mk_serve_step: null argument");
   if (!*plan && (!dims || !w || !kv)) return fail(MK_ERR_INVALID, "mk_serve_step: a new plan needs dims, w and kv");
   const int cap = s->max_batch;
-  std::vector<int> seq(cap), pt((size_t)cap * s->max_pages), tok(cap), nxt(cap);
+  std::vector<int> seq(cap), pt((size_t)cap * s->max_pages), tok(cap), nxt(cap), cf(cap);
   std::vector<long long> rid(cap);
   int B = 0, changed = 0;
-  int rc = mk_sched_next(s, &B, seq.data(), pt.data(), tok.data(), rid.data(), &changed);
+  int rc = mk_sched_next_rows(s, &B, seq.data(), pt.data(), tok.data(), rid.data(), cf.data(), &changed);
   if (rc != MK_OK || B == 0) return rc;
   if (!*plan) {
     mk_plan_opts o{};
@@ -212,9 +257,10 @@ int mk_serve_step(mk_sched* s, mk_plan** plan, const mk_model_dims* dims, const 
       mk_sched_abandon(s);
       return fail(MK_ERR_INVALID, "mk_serve_step: plan capacity below max_batch, or KV pool smaller than the scheduler's");
     }
+    o.chunk_first = cf.data();
     rc = mk_plan_create(dims, w, kv, B, seq.data(), pt.data(), s->max_pages, &o, plan);
   } else if (changed) {
-    rc = mk_plan_update(*plan, B, seq.data(), pt.data(), s->max_pages, stream);
+    rc = mk_plan_update_rows(*plan, B, seq.data(), pt.data(), s->max_pages, cf.data(), stream);
   }
   if (rc == MK_OK) rc = mk_decode_step_host(*plan, tok.data(), nullptr, nxt.data(), stream);
   if (rc != MK_OK) {

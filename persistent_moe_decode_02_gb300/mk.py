@@ -26,7 +26,7 @@ EXPORTS = [
     "mk_plan_read_debug", "mk_plan_info", "mk_plan_destroy", "mk_status_string", "mk_plan_inspect",
     "mk_last_error", "mk_decode_step_noalloc", "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
     "mk_sched_commit", "mk_sched_abandon", "mk_sched_result", "mk_sched_forget", "mk_sched_stats",
-    "mk_sched_destroy", "mk_serve_step",
+    "mk_sched_destroy", "mk_serve_step", "mk_sched_next_rows", "mk_sched_set_prefill", "mk_plan_update_rows",
 ]
 
 
@@ -52,7 +52,8 @@ class MkKv(ctypes.Structure):
 class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
-                ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("top_p", ctypes.c_float)]
+                ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("top_p", ctypes.c_float),
+                ("chunk_first", ctypes.POINTER(ctypes.c_int))]
 
 
 class MkError(RuntimeError):
@@ -97,6 +98,9 @@ def lib():
         L.mk_sched_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
         L.mk_sched_submit.argtypes = [vp, i64, p_int, i32, i32, i32]
         L.mk_sched_next.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
+        L.mk_sched_next_rows.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int, p_int]
+        L.mk_sched_set_prefill.argtypes = [vp, i32]
+        L.mk_plan_update_rows.argtypes = [vp, i32, p_int, p_int, i32, p_int, vp]
         L.mk_sched_commit.argtypes = [vp, p_int]
         L.mk_sched_abandon.argtypes = [vp]
         L.mk_sched_result.argtypes = [vp, i64, p_int, i32, p_int, p_int]
@@ -109,7 +113,8 @@ def lib():
         for f in ("mk_plan_create", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_plan_update", "mk_plan_sync",
                   "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc",
                   "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
-                  "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step"):
+                  "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step", "mk_sched_next_rows",
+                  "mk_sched_set_prefill", "mk_plan_update_rows"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -240,6 +245,16 @@ class Plan:
         lp = ctypes.cast(logits.data_ptr(), ctypes.POINTER(ctypes.c_float)) if logits is not None else None
         return lib().mk_decode_step_host(self.h, tp, lp, np_, _stream(stream))
 
+    def update_rows(self, seq_lens: Sequence[int], page_table, max_pages: int, chunk_first: Sequence[int],
+                    stream=None) -> None:
+        """Replace the batch with rows of which some are prefill chunks (include/mk.h)."""
+        self.batch = len(seq_lens)
+        pt = [int(x) for x in page_table]
+        rc = lib().mk_plan_update_rows(self.h, self.batch, _int_array(seq_lens), _int_array(pt), max_pages,
+                                       _int_array(chunk_first), _stream(stream))
+        if rc != MK_OK:
+            raise MkError("mk_plan_update_rows", rc)
+
     def update(self, seq_lens: Sequence[int], page_table, max_pages: int, stream=None) -> None:
         # int32 host arrays handed over by pointer (a numpy array or CPU tensor is not copied)
         sl = np.ascontiguousarray(np.asarray(seq_lens), dtype=np.int32)
@@ -327,20 +342,27 @@ class Scheduler:
         if rc != MK_OK:
             raise MkError("mk_sched_submit", rc)
 
+    def set_prefill(self, max_chunk: int) -> None:
+        """Prompt tokens a request may feed per step as consecutive rows (1: one token per step)."""
+        rc = lib().mk_sched_set_prefill(self.h, int(max_chunk))
+        if rc != MK_OK:
+            raise MkError("mk_sched_set_prefill", rc)
+
     def next(self):
-        """The next batch as a dict (seq_lens, page_table, tokens, rids, changed), or None when idle."""
+        """The next batch's rows as a dict (seq_lens, page_table, tokens, rids,
+        chunk_first, changed), or None when idle."""
         cap, mp = self.max_batch, self.max_pages
         b, ch = ctypes.c_int(), ctypes.c_int()
         sl, pt, tk = (ctypes.c_int * cap)(), (ctypes.c_int * (cap * mp))(), (ctypes.c_int * cap)()
-        rids = (ctypes.c_longlong * cap)()
-        rc = lib().mk_sched_next(self.h, ctypes.byref(b), sl, pt, tk, rids, ctypes.byref(ch))
+        rids, cf = (ctypes.c_longlong * cap)(), (ctypes.c_int * cap)()
+        rc = lib().mk_sched_next_rows(self.h, ctypes.byref(b), sl, pt, tk, rids, cf, ctypes.byref(ch))
         if rc != MK_OK:
-            raise MkError("mk_sched_next", rc)
+            raise MkError("mk_sched_next_rows", rc)
         n = b.value
         if n == 0:
             return None
         return {"seq_lens": list(sl[:n]), "page_table": list(pt[:n * mp]), "tokens": list(tk[:n]),
-                "rids": list(rids[:n]), "changed": bool(ch.value)}
+                "rids": list(rids[:n]), "chunk_first": list(cf[:n]), "changed": bool(ch.value)}
 
     def commit(self, next_tokens: Sequence[int]) -> None:
         rc = lib().mk_sched_commit(self.h, _int_array(next_tokens))
@@ -392,7 +414,8 @@ class Server:
     pages index (every page of it is the scheduler's)."""
 
     def __init__(self, D, weights: dict, k_pools, v_pools, max_batch: int, max_pages: int, timeout_us: int = 0,
-                 num_ctas: int = 0, split_pages: int = 0, temperature: float = 0.0, seed: int = 0):
+                 num_ctas: int = 0, split_pages: int = 0, temperature: float = 0.0, seed: int = 0,
+                 prefill: int = 8):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._w, self._kv, self._arrays = _weight_structs(D, weights, k_pools, v_pools)
@@ -400,6 +423,8 @@ class Server:
         self._opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, 0, 0, float(temperature),
                                 int(seed) & (2 ** 64 - 1))
         self.sched = Scheduler(int(k_pools[0].shape[0]), D.page_size, max_batch, max_pages)
+        if prefill > 1:   # prompts enter the cache in chunks of up to `prefill` tokens per step
+            self.sched.set_prefill(min(prefill, 8))
         self.plan = ctypes.c_void_p()
 
     def submit(self, rid: int, prompt: Sequence[int], max_new_tokens: int, eos_token: int = -1) -> None:

@@ -188,14 +188,14 @@ def test_stage_timeline_is_ordered():
     assert bool((st[..., 3][rec] < n_tasks).all())
 
 
-@pytest.mark.parametrize("max_batch,n_req", [(3, 7), (10, 12)])
-def test_serving_loop_matches_oracle_greedy(max_batch, n_req):
+@pytest.mark.parametrize("max_batch,n_req,prefill", [(3, 7, 1), (10, 12, 1), (3, 7, 8), (8, 9, 4), (10, 12, 8)])
+def test_serving_loop_matches_oracle_greedy(max_batch, n_req, prefill):
     # The continuous-batching loop end to end: requests arrive over time,
-    # their prompts go through decode steps into an empty (NaN-poisoned)
-    # cache, outputs feed back, and finished requests free their pages and
-    # slots for the queue.  Each request's outputs must be the oracle's
-    # greedy continuation of its prompt.  With a capacity of 10 the plan is a
-    # group of two sub-plans.
+    # their prompts go into an empty (NaN-poisoned) cache one token per step
+    # (prefill 1) or in prefill chunks of several rows (4, 8), outputs feed
+    # back, and finished requests free their pages and slots for the queue.
+    # Each request's outputs must be the oracle's greedy continuation of its
+    # prompt.  With a capacity of 10 the plan is a group of two sub-plans.
     import random
 
     from oracle import decode as O
@@ -212,7 +212,7 @@ def test_serving_loop_matches_oracle_greedy(max_batch, n_req):
     rng = random.Random(11)
     reqs = [(100 + i, [rng.randrange(D.vocab) for _ in range(rng.randrange(1, 21))], rng.randrange(1, 7))
             for i in range(n_req)]
-    srv = mk.Server(D, model.weights(), k, v, max_batch=max_batch, max_pages=max_pages)
+    srv = mk.Server(D, model.weights(), k, v, max_batch=max_batch, max_pages=max_pages, prefill=prefill)
     first = n_req // 2
     for rid, prompt, max_new in reqs[:first]:
         srv.submit(rid, prompt, max_new)
@@ -413,3 +413,71 @@ def test_multi_step_launch_equals_single_steps(case):
         (a, b) = _multi_step_pair(wl, 4)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("capacity", [8, 16])
+def test_prefill_chunk_rows_match_per_token_decode(capacity):
+    # One launch with prefill chunks: request B decodes one token, A feeds 4
+    # prompt tokens at positions 45..48 (crossing a page boundary), C feeds 3
+    # at 14..16 (across a page boundary and, with split_pages=1, across
+    # attention tasks).  Every row must equal the oracle decoding those tokens
+    # one at a time: per-layer hidden states, expert ids, logits and the
+    # predicted tokens.  With capacity 16 seven plain decode rows come first,
+    # so A's and C's chunks sit in the second sub-plan (rows 8..14).
+    from persistent_moe_decode_02_gb300 import mk
+    from synth.device import DeviceModel, PagedKV
+    from tests.gpu_util import OracleReplay, StepRecord
+    wl = synth.workload("tiny")
+    D = wl.dims
+    model = DeviceModel(D, wl.seed)
+    lead = [] if capacity == 8 else [20, 33, 7, 50, 61, 2, 90]       # plain decode rows first
+    ctx = lead + [30, 45, 14]                                         # ... then B, A, C
+    kv = PagedKV(D, 96, 8, wl.seed)
+    reqs = [kv.admit(rid, c, 8) for rid, c in enumerate(ctx)]
+    nl = len(lead)
+    plan_rows = [(i, 1) for i in range(nl)] + [(nl, 1), (nl + 1, 4), (nl + 2, 3)]
+    g = torch.Generator().manual_seed(3)
+    seq, pt, toks, cf, owner = [], [], [], [], []
+    for ri, n in plan_rows:
+        r = reqs[ri]
+        first = len(seq)
+        for j in range(n):
+            seq.append(r.length + j)
+            pt += r.pages + [-1] * (kv.max_pages - len(r.pages))
+            toks.append(int(torch.randint(0, D.vocab, (1,), generator=g)))
+            cf.append(first)
+            owner.append(ri)
+    B = len(seq)
+    assert B <= capacity
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs),
+                   kv.max_pages, split_pages=1, max_batch=capacity)
+    plan.update_rows(seq, pt, kv.max_pages, cf)
+    tok = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    lg = torch.empty(B, D.vocab, device="cuda")
+    assert plan.step(tok, nxt, lg) == mk.MK_OK
+    hid = torch.empty(B, D.n_layers, D.hidden, device="cuda")
+    ids = torch.empty(B, D.n_layers, D.top_k, dtype=torch.int32, device="cuda")
+    rl = torch.empty(B, D.n_layers, D.n_experts, device="cuda")
+    plan.read_debug(mk.MK_DBG_HIDDEN, hid)
+    plan.read_debug(mk.MK_DBG_EXPERT_IDS, ids)
+    plan.read_debug(mk.MK_DBG_ROUTER_LOGITS, rl)
+    assert plan.sync() == mk.MK_OK
+    rec = StepRecord(tok.cpu(), nxt.cpu(), lg.cpu(), hid.cpu(), ids.cpu().long(), rl.cpu(), list(range(B)))
+    # a batch with chunks runs one step, then needs an update; a group checks
+    # every sub-plan before it launches any, so nothing ran
+    again = torch.zeros(B, dtype=torch.int32, device="cuda")
+    assert plan.step(nxt, again) == mk.MK_ERR_INVALID
+    assert plan.sync() == mk.MK_OK and int(again.abs().sum()) == 0
+    rep = Report()
+    W = synth.SynthWeights(D, wl.seed)
+    for ri in range(len(reqs)):
+        rr = OracleReplay(wl, ri, ctx[ri], W=W)
+        for b in range(B):
+            if owner[b] == ri:
+                assert rr.req.length == seq[b]
+                rr.step(rec, b, rep)
+    print(rep)
+    rep.assert_ok()
+    assert rep.steps == B
+    plan.close()

@@ -6,7 +6,11 @@ Python restatement of the policy include/mk.h documents: pages reserved for
 prompt + max_new - 1 positions at admission, first come first served with
 head-of-line blocking, prompt tokens fed in order with their predictions
 discarded except after the last one, retirement after max_new outputs or on
-the end token, pages and slots freed at once, batch order kept."""
+the end token, pages and slots freed at once, batch order kept.  With prefill
+chunks a prompt may take several consecutive rows of a step: one row per
+request first, then the spare rows to prompts in batch order, up to the chunk
+size and the prompt's remaining tokens (above 8 rows a chunk ends at the next
+multiple of 8)."""
 import random
 
 import pytest
@@ -26,9 +30,11 @@ def fake_next(rid: int, pos: int, vocab: int = 50) -> int:
 class PolicyModel:
     """The documented policy, restated independently of the C++."""
 
-    def __init__(self, num_pages, ps, max_batch, max_pages):
+    def __init__(self, num_pages, ps, max_batch, max_pages, max_chunk=1):
         self.free, self.ps, self.max_batch, self.max_pages = num_pages, ps, max_batch, max_pages
+        self.max_chunk = max_chunk
         self.queue, self.active, self.reqs = [], [], {}
+        self.rows_of = []
 
     def submit(self, rid, prompt, max_new, eos):
         self.reqs[rid] = dict(prompt=list(prompt), max_new=max_new, eos=eos, out=[], len=0, done=False,
@@ -40,18 +46,34 @@ class PolicyModel:
             rid = self.queue.pop(0)
             self.free -= self.reqs[rid]["pages"]
             self.active.append(rid)
-        batch = []
-        for rid in self.active:
+        rows_of = [1] * len(self.active)
+        spare = self.max_batch - len(self.active)
+        for i, rid in enumerate(self.active):
             r = self.reqs[rid]
-            tok = r["prompt"][r["len"]] if r["len"] < len(r["prompt"]) else r["out"][-1]
-            batch.append((rid, r["len"], tok))
+            extra = min(spare, min(self.max_chunk, len(r["prompt"]) - r["len"]) - 1)
+            if extra > 0:
+                rows_of[i] += extra
+                spare -= extra
+        batch, row = [], 0
+        for i, rid in enumerate(self.active):
+            if self.max_batch > 8:
+                rows_of[i] = min(rows_of[i], 8 - row % 8)
+            r = self.reqs[rid]
+            for j in range(rows_of[i]):
+                pos = r["len"] + j
+                tok = r["prompt"][pos] if pos < len(r["prompt"]) else r["out"][-1]
+                batch.append((rid, pos, tok))
+                row += 1
+        self.rows_of = rows_of
         return batch
 
     def commit(self, nxt):
-        keep = []
-        for rid, tok in zip(self.active, nxt):
+        keep, row = [], 0
+        for rid, n in zip(self.active, self.rows_of):
             r = self.reqs[rid]
-            r["len"] += 1
+            r["len"] += n
+            row += n
+            tok = nxt[row - 1]
             if r["len"] >= len(r["prompt"]):
                 r["out"].append(tok)
                 if len(r["out"]) >= r["max_new"] or (r["eos"] >= 0 and tok == r["eos"]):
@@ -63,13 +85,16 @@ class PolicyModel:
         self.active = keep
 
 
-def drive(mk, num_pages, ps, max_batch, max_pages, requests, arrivals=None, max_steps=500):
+def drive(mk, num_pages, ps, max_batch, max_pages, requests, arrivals=None, max_steps=500, max_chunk=1):
     """Run scheduler and policy model side by side; returns the scheduler."""
     s = mk.Scheduler(num_pages, ps, max_batch, max_pages)
-    ref = PolicyModel(num_pages, ps, max_batch, max_pages)
+    if max_chunk > 1:
+        s.set_prefill(max_chunk)
+    ref = PolicyModel(num_pages, ps, max_batch, max_pages, max_chunk)
     arrivals = arrivals or {0: list(range(len(requests)))}
     step = 0
     prev = None
+    prev_chunks = False
     while step < max_steps:
         for i in arrivals.get(step, []):
             rid, prompt, max_new, eos = requests[i]
@@ -84,11 +109,22 @@ def drive(mk, num_pages, ps, max_batch, max_pages, requests, arrivals=None, max_
             step += 1
             continue
         assert list(zip(b["rids"], b["seq_lens"], b["tokens"])) == want
-        assert b["changed"] == (prev != b["rids"])
-        prev = b["rids"]
-        # page rows: distinct pages across the batch, each row covers the request's reservation
+        chunks = max(ref.rows_of) > 1
+        assert b["changed"] == (prev != b["rids"] or chunks or prev_chunks)
+        prev, prev_chunks = b["rids"], chunks
+        # chunk starts: each row points at the first row of its request
+        first = {}
+        for i, rid in enumerate(b["rids"]):
+            first.setdefault(rid, i)
+            assert b["chunk_first"][i] == first[rid]
+            if max_batch > 8:
+                assert first[rid] // 8 == i // 8          # a chunk stays inside one launch of 8 rows
+        # page rows: a request's rows share its pages, distinct across requests
         rows = [b["page_table"][i * max_pages:(i + 1) * max_pages] for i in range(len(b["rids"]))]
-        held = [p for row in rows for p in row if p >= 0]
+        per_req = {}
+        for rid, row in zip(b["rids"], rows):
+            assert per_req.setdefault(rid, row) == row
+        held = [p for row in per_req.values() for p in row if p >= 0]
         assert len(held) == len(set(held)) and all(0 <= p < num_pages for p in held)
         for rid, row in zip(b["rids"], rows):
             n = ref.reqs[rid]["pages"]
@@ -115,6 +151,39 @@ def test_prompts_then_outputs_in_one_batch(mk):
         assert all(out[i + 1] == fake_next(rid, len(prompt) + i) for i in range(max_new - 1))
     st = s.stats()
     assert st["queued"] == 0 and st["active"] == 0 and st["retired"] == 3 and st["free_pages"] == 64
+
+
+@pytest.mark.parametrize("max_batch,max_chunk", [(4, 4), (4, 8), (12, 8), (8, 3)])
+def test_prefill_chunks_follow_the_policy(mk, max_batch, max_chunk):
+    rng = random.Random(17 + max_chunk)
+    reqs = [(200 + i, [rng.randrange(50) for _ in range(rng.randrange(1, 30))], rng.randrange(1, 12), -1)
+            for i in range(20)]
+    arrivals = {0: list(range(6)), 4: list(range(6, 14)), 11: list(range(14, 20))}
+    s, ref = drive(mk, 48, 4, max_batch, 16, reqs, arrivals, max_chunk=max_chunk)
+    assert all(r["done"] for r in ref.reqs.values())
+    assert s.stats()["free_pages"] == 48
+    # prefill shortens the run: fewer steps than feeding one prompt token per step
+    s1, _ = drive(mk, 48, 4, max_batch, 16, reqs, arrivals, max_chunk=1)
+    assert s.stats()["steps"] < s1.stats()["steps"]
+
+
+def test_prefill_setting_is_checked(mk):
+    s = mk.Scheduler(16, 16, 4, 2)
+    for bad in (0, 9):
+        with pytest.raises(mk.MkError):
+            s.set_prefill(bad)
+    s.set_prefill(4)
+    s.submit(1, [1, 2, 3, 4, 5, 6], 2)
+    b = s.next()
+    assert b["rids"] == [1] * 4 and b["seq_lens"] == [0, 1, 2, 3] and b["chunk_first"] == [0] * 4
+    with pytest.raises(mk.MkError):
+        s.set_prefill(2)                        # a batch is pending
+    s.commit([0, 0, 0, 9])                      # no output yet: the prompt has 6 tokens
+    assert s.result(1) == ([], False)
+    b = s.next()
+    assert b["seq_lens"] == [4, 5] and b["tokens"] == [5, 6]
+    s.commit([0, 7])                            # the prediction after the last prompt token
+    assert s.result(1) == ([7], False)
 
 
 def test_slots_and_pages_limit_admission_fifo(mk):
