@@ -106,10 +106,10 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t atom_add_release(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+// Release-ordered add without a returned value: the signalling thread does
+// not wait for the atomic's round trip.
+__device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
@@ -1409,7 +1409,7 @@ struct Consumer {
   __device__ bool finish(bool ab) { return cbar_or(ab); }
 
   __device__ void signal(int ctr) {
-    if (ct == 0) atom_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
+    if (ct == 0) red_add_release(p.ctr + (size_t)ctr * CTR_STRIDE, 1u);
   }
 
   // Uniform "do my add signals complete the n of this step" for counter ctr.
@@ -2111,33 +2111,43 @@ struct Consumer {
     for (int pg = pg0; pg < pg1; pg += ppg, ++si) {
       const int npg = min(ppg, pg1 - pg);
       const uint8_t* st = wait_stage(ab);
-      const bool patch = pq0 < pq1 && pq0 / PS < pg + npg && (pq1 - 1) / PS >= pg;
+      const bool own = has_new && pos / PS >= pg && pos / PS < pg + npg;
+      const bool patch = own || (nprev > 0 && pq0 < pq1 && pq0 / PS < pg + npg && (pq1 - 1) / PS >= pg);
       if (st && patch) {
-        // put the new token's K and V (and those of the earlier rows of a
-        // prefill chunk) into their stage slots before anyone reads the pages,
-        // and zero the slots after the new token: they hold no token yet, and
-        // although their scores are masked, their V still enters the P.V
-        // product (0 * NaN would poison the output)
+        // put the new token's K and V into its stage slot before anyone reads the
+        // page, and zero the page's later slots: they hold no token yet, and
+        // although their scores are masked, their V still enters the P.V product
+        // (0 * NaN would poison the output)
         cbar();
-        const int pa = max(pg, pq0 / PS), pb = min(pg + npg - 1, (pq1 - 1) / PS);
-        for (int i = ct; i < (pb - pa + 1) * d * PS; i += NCT) {
-          const int pi = pa - pg + i / (d * PS), e = i % (d * PS);
-          const int dim = e / PS, sl = e - dim * PS, q = (pg + pi) * PS + sl;
+        if (own) {
+          const int pi = pos / PS - pg, slot = pos % PS;
           uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
           uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
-          if (q == pos) {
-            kp[e] = f2bf(kn_s[dim]);
-            vp[e] = f2bf(vn_s[dim]);
-          } else if (q > pos) {
-            kp[e] = 0;
-            vp[e] = 0;
-          } else if (q >= pq0) {   // an earlier row of the chunk, b - (pos - q)
-            const float* kr = qkv_rows + (size_t)(b - (pos - q)) * p.qkv_rows;
+          for (int i = ct; i < d * PS; i += NCT) {
+            const int dim = i / PS, sl = i - dim * PS;
+            if (sl == slot) {
+              kp[i] = f2bf(kn_s[dim]);
+              vp[i] = f2bf(vn_s[dim]);
+            } else if (sl > slot) {
+              kp[i] = 0;
+              vp[i] = 0;
+            }
+          }
+        }
+        if (nprev > 0) {
+          // the chunk's earlier rows at positions [pq0, min(pq1, pos)) of this stage's pages
+          const int qa = max(pq0, pg * PS), qb = min(min(pq1, pos), (pg + npg) * PS);
+          for (int i = ct; i < (qb - qa) * d; i += NCT) {
+            const int q = qa + i / d, dim = i - (i / d) * d;
+            const int pi = q / PS - pg, sl = q % PS;
+            uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
+            uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
+            const float* kr = qkv_rows + (size_t)(b - (pos - q)) * p.qkv_rows;   // row b - (pos - q)
             const int i0 = dim < half ? dim : dim - half;
             const float2 cs = p.rope[(size_t)q * half + i0];
             const float a = __ldcg(kr + i0), c = __ldcg(kr + i0 + half);
-            kp[e] = f2bf(dim < half ? a * cs.x - c * cs.y : c * cs.x + a * cs.y);
-            vp[e] = f2bf(__ldcg(kr + d + dim));
+            kp[dim * PS + sl] = f2bf(dim < half ? a * cs.x - c * cs.y : c * cs.x + a * cs.y);
+            vp[dim * PS + sl] = f2bf(__ldcg(kr + d + dim));
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
