@@ -379,6 +379,116 @@ def our_arm(args, wl):
         dist.destroy_process_group()
 
 
+def churn_arm(args, wl):
+    """Continuous batching inside the timed loop (workloads with churn, e.g.
+    batch 32 with 2 requests leaving and 2 joining at 512 tokens every step):
+    each timed step is one decode step of the whole batch followed by the
+    plan update for the next batch (the leaving requests' pages released, the
+    joiners' rows added: host task-list rebuild and upload).  The joiners'
+    pages and their synthetic prior K/V are written before the clock starts
+    (input preparation, like every other workload's cache)."""
+    import torch
+
+    from persistent_moe_decode_02_gb300 import mk
+    from persistent_moe_decode_02_gb300.roofline import step_bytes
+    from synth.device import DeviceModel, PagedKV, initial_tokens, kv_pages_needed
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    D, B = wl.dims, wl.batch
+    leave, jctx = wl.churn_leave, wl.churn_join_ctx
+    e2e_steps = max(3, args.steps // 4)
+    n_steps = args.warmup + args.steps + e2e_steps
+    n_join = leave * n_steps
+    ps = D.page_size
+    max_pages = max((c + n_steps + ps) // ps for c in wl.ctx + [jctx]) + 1
+    model = DeviceModel(D, wl.seed)
+    kv = PagedKV(D, kv_pages_needed(D, wl.ctx, n_steps, n_join, jctx) + 4, max_pages, wl.seed)
+    live = [kv.admit(rid, c, n_steps + 1) for rid, c in enumerate(wl.ctx)]
+    joiners = [kv.admit(B + i, jctx, n_steps + 1) for i in range(n_join)]
+    join_tok = torch.tensor(initial_tokens(wl, [r.rid for r in joiners]), dtype=torch.int32, device="cuda")
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in live], kv.page_table(live), max_pages,
+                   max_batch=B)
+    tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    state = {"j": 0, "lens": []}
+
+    def churn_step(tokens_in, tokens_out):
+        rc = plan.step(tokens_in, tokens_out)
+        assert rc == 0, mk.status_string(rc)
+        state["lens"].append([r.length for r in live])
+        for r in live:
+            r.length += 1
+        del live[:leave]
+        j = state["j"]
+        live.extend(joiners[j:j + leave])
+        state["j"] = j + leave
+        # next inputs: the staying requests' outputs, then the joiners' first tokens
+        tokens_in[:B - leave].copy_(tokens_out[leave:])
+        tokens_in[B - leave:].copy_(join_tok[j:j + leave])
+        plan.update([r.length for r in live], kv.page_table(live), max_pages)
+
+    for _ in range(args.warmup):
+        churn_step(tok, nxt)
+    assert plan.sync() == 0
+    state["lens"].clear()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with ClockSampler(0) as clk:
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            churn_step(tok, nxt)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t0
+    st = plan.sync()
+    assert st == 0, mk.status_string(st)
+    elapsed_ms = ev[0].elapsed_time(ev[1])
+    ids = torch.zeros(B, D.n_layers, D.top_k, dtype=torch.int32)
+    plan.read_debug(mk.MK_DBG_EXPERT_IDS, ids)
+    plan.sync()
+    union = [len(set(ids[:, l, :].flatten().tolist())) for l in range(D.n_layers)]
+    nbytes = sum(step_bytes(D, lens, union_per_layer=union)["total"] for lens in state["lens"]) / args.steps
+    ms = elapsed_ms / args.steps
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    # end to end: the same churn loop through the host-buffer entry point
+    h_tok = torch.tensor(tok.cpu().tolist(), dtype=torch.int32).pin_memory()
+    h_next = torch.empty(B, dtype=torch.int32).pin_memory()
+    t1 = time.perf_counter()
+    for _ in range(e2e_steps):
+        rc = plan.step_host(h_tok, h_next)
+        assert rc == 0, mk.status_string(rc)
+        for r in live:
+            r.length += 1
+        del live[:leave]
+        j = state["j"]
+        live.extend(joiners[j:j + leave])
+        state["j"] = j + leave
+        h_tok[:B - leave].copy_(h_next[leave:])
+        h_tok[B - leave:].copy_(join_tok[j:j + leave].cpu())
+        plan.update([r.length for r in live], kv.page_table(live), max_pages)
+    e2e_s = time.perf_counter() - t1
+    out = {"metric": METRIC, "value": B * args.steps / (elapsed_ms * 1e-3), "unit": "tok/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(wl),
+           "churn": {"leave_per_step": leave, "join_per_step": leave, "join_ctx": jctx,
+                     "in_timed_loop": "decode step + plan update (host rebuild and upload) every step",
+                     "wall_ms_per_step": 1e3 * wall_s / args.steps},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"], "traffic": None,
+                        "algorithmic_bytes_per_launch": nbytes, "kernel": "mk_megakernel",
+                        "note": "bytes per step from the steps' actual lengths and the last step's expert union; "
+                                "the batch runs as 4 launches of 8 requests"},
+           "cpu_baseline": None,
+           "e2e": {"value": B * e2e_steps / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+                   "d2h_bytes_per_step": 4 * B + 16, "steps": e2e_steps},
+           "gpu_launches": args.steps * ((B + 7) // 8), "clocks": clk.summary(), "kernel_hash": kernel_hash()}
+    print(json.dumps(out), flush=True)
+    plan.close()
+
+
 PHASES = ["QKV", "ATTN", "OPROJ", "EXPERT", "REDUCE", "LM", "COMBINE"]
 
 
@@ -569,6 +679,10 @@ def main():
         serve_arm(args, wl)
     elif args.impl == "reference":
         reference_arm(args, wl)
+    elif wl.churn_leave > 0:
+        import __graft_entry__
+        __graft_entry__.build()
+        churn_arm(args, wl)
     else:
         import __graft_entry__
         __graft_entry__.build()
