@@ -433,15 +433,15 @@ def churn_arm(args, wl):
     assert plan.sync() == 0
     state["lens"].clear()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with ClockSampler(0) as clk:
+        t0 = time.perf_counter()
         ev[0].record(stream)
         for _ in range(args.steps):
             churn_step(tok, nxt)
         ev[1].record(stream)
         torch.cuda.synchronize()
-    wall_s = time.perf_counter() - t0
+        wall_s = time.perf_counter() - t0
     st = plan.sync()
     assert st == 0, mk.status_string(st)
     elapsed_ms = ev[0].elapsed_time(ev[1])
