@@ -389,6 +389,14 @@ int mk_sched_set_prefill(mk_sched* s, int max_chunk);
 int mk_sched_next_rows(mk_sched* s, int* rows, int* seq_lens, int* page_table, int* tokens, long long* rids,
                        int* chunk_first, int* changed);
 
+/* The rows mk_sched_next_rows would hand out next if the pending batch (if
+ * any) were committed with outputs that end no request early (no end token).
+ * Changes nothing.  A serving loop uses it to prepare the next step (its task
+ * list) while the current one runs on the GPU; the prediction misses only
+ * when a request outputs its end token. */
+int mk_sched_peek_rows(const mk_sched* s, int* rows, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                       int* chunk_first);
+
 /* Admit what fits, then describe the next step's batch in host arrays sized
  * for max_batch requests: *batch, seq_lens[b] (tokens cached), page_table[b *
  * max_pages_per_seq + i] (-1 past the request's pages), tokens[b] (the input
@@ -429,7 +437,10 @@ void mk_sched_destroy(mk_sched* s);
 /* One step of the serving loop on `stream`: mk_sched_next_rows; when *plan
  * is NULL, mk_plan_create with that batch (capacity opts->max_batch, or the
  * scheduler's max_batch when 0; a smaller capacity is MK_ERR_INVALID), else
- * mk_plan_update_rows when the rows changed; mk_decode_step_host; then
+ * mk_plan_update_rows when the rows changed; the step from host buffers
+ * (as mk_decode_step_host), during which the host builds the task list of
+ * the batch mk_sched_peek_rows predicts, so the next call's update only
+ * uploads it when the prediction holds; then
  * mk_sched_commit.  dims, w and kv are read only when the plan is created
  * (kv->num_pages must be at least the scheduler's pool).  Returns the batch
  * size that ran (0: nothing queued or admitted) or an error; on an error the

@@ -332,6 +332,10 @@ void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_erro
 
 // ------------------------------------------------------------------ the plan
 
+namespace {
+struct Built;
+}
+
 struct mk_plan {
   // A batch capacity above mk::MAX_BATCH makes a group: sub-plan i holds
   // requests [8i, 8i + 8) and the group's calls run the sub-plans one after
@@ -389,6 +393,13 @@ struct mk_plan {
   cudaEvent_t ev_stage[2] = {nullptr, nullptr};
   int stage_i = 0;
   int* h_status = nullptr;
+  int* h_next = nullptr;           // pinned [bcap]: next tokens of a step enqueued without waiting
+  int* h_tok = nullptr;            // pinned [bcap]: that step's input tokens
+  // a task list built ahead for the lengths `pre_seq` (the serving loop builds
+  // the next batch's list while the GPU runs the current step)
+  bool pre_valid = false;
+  std::vector<int> pre_seq;
+  Built* pre = nullptr;
 };
 
 namespace {
@@ -505,9 +516,12 @@ struct Built {
 
 bool nucleus_on(const mk_plan* p) { return p->inv_temp > 0.f && p->top_p < 1.f; }
 
-void build_for(const mk_plan* p, Built& b) {
-  b.rc = build_tasks(p->s, p->B, p->bcap, p->seq.data(), p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open,
-                     nucleus_on(p));
+void build_for(const mk_plan* p, Built& b, int B = -1, const int* seq = nullptr) {
+  if (B < 0) {
+    B = p->B;
+    seq = p->seq.data();
+  }
+  b.rc = build_tasks(p->s, B, p->bcap, seq, p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open, nucleus_on(p));
   b.nucleus = nucleus_on(p);
   if (b.rc != MK_OK) return;
   if (p->drop_task > 0 && p->drop_task - 1 < (int)b.tasks.size()) {
@@ -841,6 +855,8 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   for (int k = 0; k < 2; ++k)
     if (cudaEventCreateWithFlags(&p->ev_stage[k], cudaEventDisableTiming) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMallocHost(&p->h_status, 4 * sizeof(int)) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaMallocHost(&p->h_next, (size_t)bcap * sizeof(int)) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaMallocHost(&p->h_tok, (size_t)bcap * sizeof(int)) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaMemsetAsync(P.route, 0, L * p->rm.ints * sizeof(int), st) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (mk::launch_rope_table(p->d_rope, p->rope_npos, s.d, (double)s.theta, st) != cudaSuccess)
@@ -953,6 +969,15 @@ static int step_host_one(mk_plan* p, const int* h_tokens, float* h_logits, int* 
   return p->h_status[0];
 }
 
+// A task list built ahead (mk::plan_prebuild) for exactly the plan's new
+// lengths; it is used once.
+static bool take_prebuilt(mk_plan* p, Built& b) {
+  const bool hit = p->pre_valid && p->pre && p->pre->nucleus == nucleus_on(p) && p->pre_seq == p->seq;
+  p->pre_valid = false;
+  if (hit) b = std::move(*p->pre);
+  return hit;
+}
+
 // The first half of an update: checks, device capacity, and the new batch on
 // the host side of the plan.
 static int update_prepare(mk_plan* p, int batch, const int* seq_lens, const int* page_table, int max_pages_per_seq,
@@ -1000,7 +1025,7 @@ static int update_one(mk_plan* p, int batch, const int* seq_lens, const int* pag
   int rc = update_prepare(p, batch, seq_lens, page_table, max_pages_per_seq, st, chunk_first);
   if (rc != MK_OK) return rc;
   Built b;
-  build_for(p, b);
+  if (!take_prebuilt(p, b)) build_for(p, b);
   return update_commit(p, b, st);
 }
 
@@ -1089,6 +1114,9 @@ static void destroy_one(mk_plan* p) {
     if (p->ev_stage[k]) cudaEventDestroy(p->ev_stage[k]);
   }
   if (p->h_status) cudaFreeHost(p->h_status);
+  if (p->h_next) cudaFreeHost(p->h_next);
+  if (p->h_tok) cudaFreeHost(p->h_tok);
+  delete p->pre;
   delete p;
 }
 
@@ -1241,7 +1269,7 @@ int mk_plan_update_rows(mk_plan* p, int batch, const int* seq_lens, const int* p
   std::vector<Built> built(n);
   std::vector<std::thread> th;
   for (size_t i = 0; i < n; ++i)
-    if (nb[i] > 0) th.emplace_back([&, i] { build_for(p->subs[i], built[i]); });
+    if (nb[i] > 0 && !take_prebuilt(p->subs[i], built[i])) th.emplace_back([&, i] { build_for(p->subs[i], built[i]); });
   for (auto& t : th) t.join();
   for (size_t i = 0; i < n; ++i) {
     if (nb[i] > 0) {
@@ -1340,3 +1368,83 @@ void mk_plan_destroy(mk_plan* p) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ serving-loop helpers
+// Used by mk_serve_step: a step enqueued from host tokens without waiting
+// for it, the wait, and a task list built ahead for the next batch's lengths
+// while the GPU runs the current step.
+namespace mk {
+
+static int step_host_begin_one(mk_plan* q, const int* h_tokens, mk_stream stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t tb = (size_t)q->B * sizeof(int);
+  memcpy(q->h_tok, h_tokens, tb);
+  if (cudaMemcpyAsync(q->d_io_tok, q->h_tok, tb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MK_ERR_CUDA;
+  const int rc = step_one(q, q->d_io_tok, nullptr, q->d_io_next, stream);
+  if (rc != MK_OK) return rc;
+  if (cudaMemcpyAsync(q->h_next, q->d_io_next, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MK_ERR_CUDA;
+  if (cudaMemcpyAsync(q->h_status, q->d_status, 4 * sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MK_ERR_CUDA;
+  return MK_OK;
+}
+
+int plan_step_host_begin(mk_plan* p, const int* h_tokens, mk_stream stream) {
+  if (!p || !h_tokens) return MK_ERR_INVALID;
+  if (p->subs.empty()) return step_host_begin_one(p, h_tokens, stream);
+  const int rc0 = group_check(p, 1);
+  if (rc0 != MK_OK) return rc0;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    const int rc = step_host_begin_one(p->subs[i], h_tokens + i * MAX_BATCH, stream);
+    if (rc != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
+int plan_step_host_end(mk_plan* p, int* h_next, mk_stream stream) {
+  if (!p || !h_next) return MK_ERR_INVALID;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return note_cuda(cudaGetLastError(), "serve step");
+  if (p->subs.empty()) {
+    memcpy(h_next, p->h_next, (size_t)p->B * sizeof(int));
+    return p->h_status[0];
+  }
+  int st = MK_OK;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    if (p->sub_B[i] == 0) continue;
+    memcpy(h_next + i * MAX_BATCH, p->subs[i]->h_next, (size_t)p->sub_B[i] * sizeof(int));
+    if (st == MK_OK) st = p->subs[i]->h_status[0];
+  }
+  return st;
+}
+
+static void prebuild_one(mk_plan* q, int batch, const int* seq_lens) {
+  q->pre_valid = false;
+  if (batch < 1 || batch > q->bcap) return;
+  if (!q->pre) q->pre = new (std::nothrow) Built();
+  if (!q->pre) return;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 0) return;
+  build_for(q, *q->pre, batch, seq_lens);
+  q->pre_seq.assign(seq_lens, seq_lens + batch);
+  q->pre_valid = q->pre->rc == MK_OK;
+}
+
+void plan_prebuild(mk_plan* p, int batch, const int* seq_lens) {
+  if (!p || !seq_lens) return;
+  if (p->subs.empty()) {
+    prebuild_one(p, batch, seq_lens);
+    return;
+  }
+  std::vector<std::thread> th;
+  for (size_t i = 0; i < p->subs.size(); ++i) {
+    const int nb = std::max(0, std::min(MAX_BATCH, batch - (int)i * MAX_BATCH));
+    if (nb == 0) {
+      p->subs[i]->pre_valid = false;
+      continue;
+    }
+    th.emplace_back([p, i, nb, seq_lens] { prebuild_one(p->subs[i], nb, seq_lens + i * MAX_BATCH); });
+  }
+  for (auto& t : th) t.join();
+}
+
+}  // namespace mk

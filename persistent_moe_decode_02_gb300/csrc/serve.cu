@@ -20,6 +20,11 @@
 
 namespace mk {
 void set_last_error(const char* msg);
+// plan.cu: a step enqueued from host tokens without waiting, its wait, and a
+// task list built ahead for a batch's lengths
+int plan_step_host_begin(mk_plan* p, const int* h_tokens, mk_stream stream);
+int plan_step_host_end(mk_plan* p, int* h_next, mk_stream stream);
+void plan_prebuild(mk_plan* p, int batch, const int* seq_lens);
 }
 
 struct mk_sched {
@@ -167,6 +172,21 @@ int mk_sched_next(mk_sched* s, int* batch, int* seq_lens, int* page_table, int* 
   return mk_sched_next_rows(s, batch, seq_lens, page_table, tokens, rids, cf.data(), changed);
 }
 
+int mk_sched_peek_rows(const mk_sched* s, int* rows, int* seq_lens, int* page_table, int* tokens, long long* rids,
+                       int* chunk_first) {
+  if (!s || !rows || !seq_lens || !page_table || !tokens || !rids || !chunk_first)
+    return fail(MK_ERR_INVALID, "mk_sched_peek_rows: null argument");
+  mk_sched c = *s;   // the prediction runs on a copy; the scheduler itself does not change
+  if (c.pending) {
+    // commit the pending batch with outputs that are no request's end token
+    std::vector<int> fake(c.rows_of.empty() ? 1 : (size_t)c.max_batch, -2);
+    const int rc = mk_sched_commit(&c, fake.data());
+    if (rc != MK_OK) return rc;
+  }
+  int changed = 0;
+  return mk_sched_next_rows(&c, rows, seq_lens, page_table, tokens, rids, chunk_first, &changed);
+}
+
 int mk_sched_commit(mk_sched* s, const int* next_tokens) {
   if (!s || !next_tokens) return fail(MK_ERR_INVALID, "mk_sched_commit: null argument");
   if (!s->pending) return fail(MK_ERR_INVALID, "mk_sched_commit: no batch is pending");
@@ -262,7 +282,17 @@ int mk_serve_step(mk_sched* s, mk_plan** plan, const mk_model_dims* dims, const 
   } else if (changed) {
     rc = mk_plan_update_rows(*plan, B, seq.data(), pt.data(), s->max_pages, cf.data(), stream);
   }
-  if (rc == MK_OK) rc = mk_decode_step_host(*plan, tok.data(), nullptr, nxt.data(), stream);
+  if (rc == MK_OK) rc = mk::plan_step_host_begin(*plan, tok.data(), stream);
+  if (rc == MK_OK) {
+    // while the GPU runs this step, build the task list of the batch the
+    // next call will most likely run (no request ending on its end token)
+    std::vector<int> pseq(cap), ppt((size_t)cap * s->max_pages), ptok(cap), pcf(cap);
+    std::vector<long long> prid(cap);
+    int PB = 0;
+    if (mk_sched_peek_rows(s, &PB, pseq.data(), ppt.data(), ptok.data(), prid.data(), pcf.data()) == MK_OK && PB > 0)
+      mk::plan_prebuild(*plan, PB, pseq.data());
+    rc = mk::plan_step_host_end(*plan, nxt.data(), stream);
+  }
   if (rc != MK_OK) {
     mk_sched_abandon(s);
     return rc;

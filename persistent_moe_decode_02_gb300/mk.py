@@ -27,6 +27,7 @@ EXPORTS = [
     "mk_last_error", "mk_decode_step_noalloc", "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next",
     "mk_sched_commit", "mk_sched_abandon", "mk_sched_result", "mk_sched_forget", "mk_sched_stats",
     "mk_sched_destroy", "mk_serve_step", "mk_sched_next_rows", "mk_sched_set_prefill", "mk_plan_update_rows",
+    "mk_sched_peek_rows",
 ]
 
 
@@ -100,6 +101,7 @@ def lib():
         L.mk_sched_next.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
         L.mk_sched_next_rows.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int, p_int]
         L.mk_sched_set_prefill.argtypes = [vp, i32]
+        L.mk_sched_peek_rows.argtypes = [vp, p_int, p_int, p_int, p_int, p_i64, p_int]
         L.mk_plan_update_rows.argtypes = [vp, i32, p_int, p_int, i32, p_int, vp]
         L.mk_sched_commit.argtypes = [vp, p_int]
         L.mk_sched_abandon.argtypes = [vp]
@@ -114,7 +116,7 @@ def lib():
                   "mk_plan_read_debug", "mk_plan_info", "mk_plan_inspect", "mk_decode_step_noalloc",
                   "mk_plan_set_sampling", "mk_plan_set_top_p", "mk_sched_create", "mk_sched_submit", "mk_sched_next", "mk_sched_commit", "mk_sched_abandon",
                   "mk_sched_result", "mk_sched_forget", "mk_sched_stats", "mk_serve_step", "mk_sched_next_rows",
-                  "mk_sched_set_prefill", "mk_plan_update_rows"):
+                  "mk_sched_set_prefill", "mk_plan_update_rows", "mk_sched_peek_rows"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -363,6 +365,21 @@ class Scheduler:
             return None
         return {"seq_lens": list(sl[:n]), "page_table": list(pt[:n * mp]), "tokens": list(tk[:n]),
                 "rids": list(rids[:n]), "chunk_first": list(cf[:n]), "changed": bool(ch.value)}
+
+    def peek(self):
+        """The rows next() would return after the pending batch committed with no end token, or None."""
+        cap, mp = self.max_batch, self.max_pages
+        b = ctypes.c_int()
+        sl, pt, tk = (ctypes.c_int * cap)(), (ctypes.c_int * (cap * mp))(), (ctypes.c_int * cap)()
+        rids, cf = (ctypes.c_longlong * cap)(), (ctypes.c_int * cap)()
+        rc = lib().mk_sched_peek_rows(self.h, ctypes.byref(b), sl, pt, tk, rids, cf)
+        if rc != MK_OK:
+            raise MkError("mk_sched_peek_rows", rc)
+        n = b.value
+        if n == 0:
+            return None
+        return {"seq_lens": list(sl[:n]), "page_table": list(pt[:n * mp]), "tokens": list(tk[:n]),
+                "rids": list(rids[:n]), "chunk_first": list(cf[:n])}
 
     def commit(self, next_tokens: Sequence[int]) -> None:
         rc = lib().mk_sched_commit(self.h, _int_array(next_tokens))

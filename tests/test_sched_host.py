@@ -131,8 +131,22 @@ def drive(mk, num_pages, ps, max_batch, max_pages, requests, arrivals=None, max_
             assert all(p >= 0 for p in row[:n]) and all(p == -1 for p in row[n:])
         assert s.stats()["free_pages"] == ref.free
         nxt = [fake_next(rid, pos) for rid, pos, _ in want]
+        before = s.stats()
+        ahead = s.peek()                      # the prediction made while the step "runs"
+        assert s.stats() == before            # peeking changes nothing
         s.commit(nxt)
         ref.commit(nxt)
+        ends = any(r["eos"] >= 0 for r in ref.reqs.values())
+        if not ends and step + 1 not in arrivals:
+            # with no end token and no arrival the prediction is the next batch
+            # (its rows and lengths: what the task list depends on; a decode
+            # row's input token is unknown until the step ends)
+            nb = s.peek()
+            if ahead is None:
+                assert nb is None
+            else:
+                for k in ("rids", "seq_lens", "page_table", "chunk_first"):
+                    assert ahead[k] == nb[k], k
         step += 1
     for rid, r in ref.reqs.items():
         out, done = s.result(rid)
