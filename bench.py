@@ -272,7 +272,8 @@ def our_arm(args, wl):
     max_pages = max((c + total_steps + ps) // ps for c in wl.ctx) + 1
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, total_steps) + 4, max_pages, wl.seed)
     reqs = [kv.admit(rid, c, total_steps) for rid, c in enumerate(wl.ctx)]
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages)
+    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
+                   tc_off=args.tc_off)
     B = wl.batch
     tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -407,7 +408,7 @@ def churn_arm(args, wl):
     joiners = [kv.admit(B + i, jctx, n_steps + 1) for i in range(n_join)]
     join_tok = torch.tensor(initial_tokens(wl, [r.rid for r in joiners]), dtype=torch.int32, device="cuda")
     plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in live], kv.page_table(live), max_pages,
-                   max_batch=B)
+                   max_batch=B, tc_off=args.tc_off)
     tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
     nxt = torch.empty(B, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -656,6 +657,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tc-off", action="store_true",
+                    help="expert gate/up of batches 5-8 on the CUDA cores instead of the tensor cores")
     ap.add_argument("--steps-per-launch", type=int, default=8,
                     help="also time this many decode steps per launch (tokens fed back on the device); 1: off")
     ap.add_argument("--timeline", default=None,

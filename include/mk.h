@@ -118,6 +118,9 @@ typedef struct mk_plan_opts {
   unsigned long long seed;
   float top_p;       /* nucleus sampling from the first step, as mk_plan_set_top_p; 0 -> 1 (off) */
   const int* chunk_first; /* prefill chunks of the first batch, as mk_plan_update_rows (host, nullable) */
+  int tc_off;        /* 1: the expert gate/up of batches 5-8 on the CUDA cores; 0 (default): on the
+                        tensor cores (tcgen05, TMEM accumulators, TMA tiles) when hidden is a multiple
+                        of 128 and expert_ffn of 64 */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;
@@ -285,7 +288,7 @@ int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stre
 
 /* Describe the current plan (host-side numbers): writes up to `n` ints:
  * [num_ctas, num_tasks, nstages, stage_bytes, smem_bytes, batch, n_attn_tasks,
- *  n_gu_tasks, n_lm_tiles, replans]. */
+ *  n_gu_tasks, n_lm_tiles, replans, expert gate/up on the tensor cores (1/0)]. */
 int mk_plan_info(const mk_plan* plan, int* out, int n);
 
 void mk_plan_destroy(mk_plan* plan);

@@ -100,6 +100,67 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- tensor-core (tcgen05) helpers: 2-D TMA tile loads, shared-memory
+// matrix descriptors, TMEM allocation, MMA issue / commit and TMEM loads.
+
+// 2-D tiled bulk tensor copy global -> shared, completion on `bar` in bytes.
+// x (the inner, K coordinate) is always a multiple of 64 bf16 (128 bytes).
+__device__ __forceinline__ void tma_g2s_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout (8-row groups of 128-byte rows, 1024 bytes apart).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                  // leading-dimension offset (not used by swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride between 8-row groups
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = 16.
+constexpr uint32_t UMMA_IDESC_M128_N16 = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t)(16 >> 3) << 17 |
+                                         (uint32_t)(128 >> 4) << 24;
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued is complete.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32 (w % 4) .. + 31).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -320,6 +381,11 @@ struct Misc {
   int r_rank[MAX_UNION * MAX_BATCH];
   // the producer's copies of a layer's distinct experts, one per cursor
   RouteCache cp_route;
+  // tensor-core gate/up: accumulator-ready barrier (one commit per 64-unit
+  // tile), final-completion barrier, and the TMEM base address
+  uint64_t acc_bar;
+  uint64_t tc_fin;
+  uint32_t tmem;
   // nucleus draw (T_SAMPLE): target and running mass, key prefix, digit, cut, max logit
   unsigned long long smp_tgt, smp_before;
   uint32_t smp_prefix;
@@ -442,9 +508,27 @@ __device__ __forceinline__ long long gu_cut(int U, int F, const int* cnt, long l
   return (long long)U * F;
 }
 
+// Whether expert tile t's gate/up runs on the tensor cores: the batch-8
+// instance with tensor maps, when the layer's 64-unit blocks, cut evenly
+// over the tiles, fit the coefficient scratch (the producer and the
+// consumers decide alike from the same routing).
+__device__ __forceinline__ bool tc_layer(const Params& p, const Task& t, int U) {
+  if (!p.tm_gu) return false;
+  const long long T = (long long)U * p.F / TC_UNITS, n = t.a[1];
+  return (T + n - 1) / n * TC_UNITS <= p.cf_pairs;
+}
+
 template <int NB>
 __device__ __forceinline__ void gu_range_w(const Params& p, const Task& t, int U, const int* cnt, long long& q0,
                                            long long& q1) {
+  if constexpr (NB == 8) {
+    if (tc_layer(p, t, U)) {   // tensor-core gate/up: whole 64-unit blocks, evenly
+      const long long T = (long long)U * p.F / TC_UNITS, i = t.a[0], n = t.a[1];
+      q0 = T * i / n * TC_UNITS;
+      q1 = T * (i + 1) / n * TC_UNITS;
+      return;
+    }
+  }
   if constexpr (NB > 1) {
     long long tot = 0;
     int cmin = 1 << 30;
@@ -488,6 +572,7 @@ struct Geo {
   int pps, rpw, nst_gu;
   int cs, cu, cf;   // gate/up cursor: stage cs starts at unit cf of distinct expert cu
   int ws, wu, wf;   // down cursor, the same for down stage ws
+  bool tc;          // gate/up stages are tensor-core tiles (128 rows x 64 columns per 16 KB)
 };
 
 // Producer: one thread that walks the CTA's tasks and fills the ring with
@@ -561,6 +646,8 @@ struct Producer {
       ngu += (fb - fa + q.pps - 1) / q.pps;
       nwd += (fb - fa + q.rpw - 1) / q.rpw;
     }
+    q.tc = NB == 8 && tc_layer(p, t, U);
+    if (q.tc) ngu = (q.q1 - q.q0) / TC_UNITS * (p.H / (64 * (p.stage_bytes / TC_BOX)));   // 128-row tiles
     q.nst_gu = ngu;
     q.nst = ngu + nwd;
     q.cs = q.ws = 0;
@@ -771,10 +858,21 @@ struct Producer {
         uint64_t* bar = &m->full[r.stage];
         uint8_t* dst = r.base + (size_t)r.stage * r.sb;
         m->armed[r.stage] = r.round;
-        segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
-          mbar_expect_tx_only(bar, b);
-          bulk_g2s(dst + off, src, b, bar, pol);
-        });
+        if (NB == 8 && q.type == T_MOE && q.tc && s < q.nst_gu) {
+          // tensor-core gate/up tile: 128 interleaved gate/up rows (64 units of
+          // one expert) x 64 columns per 16 KB box of the stage
+          const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox), mt = s / kst, ks = s - mt * kst;
+          const int qa = q.q0 + mt * TC_UNITS, u = qa / p.F, f = qa - u * p.F;
+          const int y = q.rc->exp[u] * 2 * p.F + 2 * f;
+          const void* tm = reinterpret_cast<const uint8_t*>(p.tm_gu) + (size_t)q.l * 128;
+          mbar_expect_tx_only(bar, (uint32_t)nbox * TC_BOX);
+          for (int h = 0; h < nbox; ++h) tma_g2s_2d(dst + h * TC_BOX, tm, (ks * nbox + h) * 64, y, bar, pol);
+        } else {
+          segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
+            mbar_expect_tx_only(bar, b);
+            bulk_g2s(dst + off, src, b, bar, pol);
+          });
+        }
         mbar_arrive(bar);
         if (p.strace && cp_lin < STRACE_CAP) {
           unsigned long long* rec = p.strace + ((size_t)blockIdx.x * STRACE_CAP + cp_lin) * STRACE_SLOTS;
@@ -1741,11 +1839,16 @@ struct Consumer {
           const float ga = bf_lo(gb.x), gc = bf_hi(gb.x), ge = bf_lo(gb.y), gg = bf_hi(gb.y);
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
-            if (b < p.B) {
-              const float4 v = xv[h][b];
-              reinterpret_cast<float4*>(act + (size_t)b * H)[i] = make_float4(v.x * ga, v.y * gc, v.z * ge, v.w * gg);
-              ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
+            const float4 v = xv[h][b];
+            const float4 y = make_float4(v.x * ga, v.y * gc, v.z * ge, v.w * gg);
+            if (NB == 8 && p.tm_gu) {
+              // the tensor cores' B operand: bf16 hi (row b) and lo (row 8 + b)
+              // of x * gain, K-major, 128-byte swizzled (zero rows past the batch)
+              store_b_operand(b, 4 * i, b < p.B ? y : z4);
+            } else if (b < p.B) {
+              reinterpret_cast<float4*>(act + (size_t)b * H)[i] = y;
             }
+            if (b < p.B) ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
           }
         }
       }
@@ -1756,6 +1859,7 @@ struct Consumer {
           if (lane == 0) m->red[b * NCW + cw] = t;
         }
       }
+      if (NB == 8 && p.tm_gu) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor cores
     }
     cbar();
     if (ct < p.B) {
@@ -1811,6 +1915,100 @@ struct Consumer {
   // (moe_part); the reduce tasks add the residual and all tiles' partials.
   // No other CTA's gate/up results are needed, so the tile streams its
   // gate/up and down weights back to back.
+  // Element k .. k + 3 of B-operand rows `b` (bf16 hi) and 8 + b (bf16 lo) in
+  // the K-major 128-byte swizzled layout: 64-column slices of 16 rows x 128
+  // bytes (2 KB), rows in two 8-row groups of 1024 bytes, the 16-byte chunk c
+  // of row r stored at chunk c ^ r.
+  __device__ __forceinline__ void store_b_operand(int b, int k, float4 y) {
+    const uint16_t h0 = f2bf(y.x), h1 = f2bf(y.y), h2 = f2bf(y.z), h3 = f2bf(y.w);
+    const uint16_t l0 = f2bf(y.x - bf2f(h0)), l1 = f2bf(y.y - bf2f(h1)), l2 = f2bf(y.z - bf2f(h2)),
+                   l3 = f2bf(y.w - bf2f(h3));
+    const int sl = k >> 6, c = (k & 63) >> 3, half = k & 4;
+    uint8_t* base = reinterpret_cast<uint8_t*>(act) + sl * 2048 + b * 128 + ((c ^ b) << 4) + half * 2;
+    *reinterpret_cast<uint2*>(base) = make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
+    *reinterpret_cast<uint2*>(base + 1024) =
+        make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
+  }
+
+  // The gate/up part of an expert tile on the tensor cores (batch instance 8):
+  // units [q0, q1) are whole 64-unit blocks.  Per block, 128 gate/up rows x
+  // H columns stream through the ring as 128 x 128 tiles; one thread issues
+  // M = 128, N = 16, K = 16 MMAs (A: the weight tile, B: the batch's
+  // activations as bf16 hi + lo rows) accumulating in TMEM, and commits each
+  // stage's release to the ring's empty barrier.  Warps 0-3 then read the
+  // accumulator (one TMEM lane per row), add the hi and lo columns of each
+  // request, pair gate and up rows and write the SwiGLU coefficients of the
+  // expert's token slots, as the CUDA-core epilogue does.
+  uint32_t acc_ph = 0;
+  __device__ bool gu_tc(int q0, int q1, bool ab, float* cf) {
+    const int F = p.F, k = p.k, bc = p.rm.bcap;
+    const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox), nmt = (q1 - q0) / TC_UNITS;
+    const uint32_t bsm = smem_u32(act), tmem = m->tmem;
+    for (int mt = 0; mt < nmt; ++mt) {
+      const int qa = q0 + mt * TC_UNITS, u = qa / F, f0 = qa - u * F;
+      for (int ks = 0; ks < kst; ++ks) {
+        const uint8_t* st = wait_stage(ab);
+        if (cw == 0) {
+          if (lane == 0) {
+            if (st) {
+              tc_fence_after();
+              const uint32_t sa = smem_u32(st);
+              for (int h = 0; h < nbox; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_f16(tmem, umma_desc_sw128(sa + h * TC_BOX + kk * 32),
+                           umma_desc_sw128(bsm + (nbox * ks + h) * 2048 + kk * 32), UMMA_IDESC_M128_N16,
+                           (ks | h | kk) != 0);
+              umma_commit(&m->empty[r.stage]);   // the stage is free once its MMAs are done
+              if (ks == kst - 1) umma_commit(&m->acc_bar);
+            } else {
+              mbar_arrive(&m->empty[r.stage]);
+            }
+          }
+          __syncwarp();
+          if (p.strace && ct == 0) stage_stamp(2);
+          r.advance();
+        } else {
+          release_stage(ab);
+        }
+      }
+      ab = cbar_or(ab);
+      if (!ab && cw < 4) {
+        if (!mbar_wait(p, m, &m->acc_bar, acc_ph, -6)) ab = true;
+        tc_fence_after();
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(cw * 32) << 16), v);
+        float gsum[8], usum[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gsum[j] = v[j] + v[8 + j];   // hi + lo of request j
+#pragma unroll
+        for (int j = 0; j < 8; ++j) usum[j] = __shfl_down_sync(FULL, gsum[j], 1);   // the up row below
+        if (!ab && (lane & 1) == 0) {
+          const int f = f0 + ((cw * 32 + lane) >> 1);
+          const int nt = m->r_cnt[u];
+          const int* toks = m->r_tok + u * bc;
+          const int* ranks = m->r_rank + u * bc;
+          for (int j = 0; j < nt; ++j) {
+            const int tj = toks[j];
+            float gs = 0.f, us = 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+              if (b == tj) {
+                gs = gsum[b];
+                us = usum[b];
+              }
+            const float c = m->inv[tj], g = c * gs;
+            cf[(size_t)(u * F + f - q0) * bc + j] = m->gate[tj * k + ranks[j]] * (g / (1.0f + expf(-g)) * (c * us));
+          }
+        }
+      }
+      acc_ph ^= 1;
+      tc_fence_before();
+      ab = cbar_or(ab);   // the accumulator is read before the next block's MMAs overwrite it
+    }
+    return ab;
+  }
+
   __device__ bool moe(const Task& t, bool ab) {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
@@ -1828,7 +2026,28 @@ struct Consumer {
     gu_range_w<NB>(p, t, U, m->r_cnt, g0, g1);
     const int q0 = (int)g0, q1 = (int)g1;
     float* cf = scr;   // [unit - q0][token slot] coefficients
-    for (int q = q0; q < q1;) {
+    bool tc = false;
+    if constexpr (NB == 8) {
+      tc = tc_layer(p, t, U);
+      if (tc) {
+        ab = gu_tc(q0, q1, ab, cf);
+      } else if (p.tm_gu && !ab) {
+        // this layer's blocks do not fit the coefficient scratch: the CUDA
+        // cores take it, from fp32 activations in place of the B operand
+        const int H4 = H >> 2;
+        const float* xm = p.x_mid + (size_t)l * p.bcap * H;
+        const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
+        for (int x = ct; x < p.B * H4; x += NCT) {
+          const int b = x / H4, i = x - b * H4;
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i);
+          const uint2 gb = __ldg(gam + i);
+          reinterpret_cast<float4*>(act + (size_t)b * H)[i] =
+              make_float4(v.x * bf_lo(gb.x), v.y * bf_hi(gb.x), v.z * bf_lo(gb.y), v.w * bf_hi(gb.y));
+        }
+        cbar();
+      }
+    }
+    for (int q = tc ? q1 : q0; q < q1;) {
       const int u = q / F, fa = q - u * F, fb = min(F, q1 - u * F);
       const int nt = m->r_cnt[u];
       const int* toks = m->r_tok + u * bc;
@@ -2765,7 +2984,7 @@ __device__ void drain(const Params& p, Misc* m, int nst) {
 
 template <int NB, bool NUC>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   Misc* m = reinterpret_cast<Misc*>(smem + p.misc_off);
   float* act = reinterpret_cast<float*>(smem + p.act_off);
   float* scr = reinterpret_cast<float*>(smem + p.misc_off + sizeof(Misc));
@@ -2779,9 +2998,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
     m->abort_flag = 0;
     m->r_layer = -1;
     m->dead = failed(p) ? 1 : 0;
+    if constexpr (NB == 8) {
+      if (p.tm_gu) {
+        mbar_init(&m->acc_bar, 1);
+        mbar_init(&m->tc_fin, 1);
+      }
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (NB == 8) {
+    if (p.tm_gu && tid < 32) {   // consumer warp 0 holds 32 TMEM columns for the launch
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(smem_u32(&m->tmem))
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+  }
   __syncthreads();
+  if constexpr (NB == 8) tc_fence_after();
   if (!m->dead) {
     const int t0 = p.cta_start[blockIdx.x], t1 = p.cta_start[blockIdx.x + 1];
     Ring ring{smem, m, p.nstages, p.stage_bytes, 0, 0};
@@ -2798,6 +3032,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_megakernel(const __grid_consta
   }
   __syncthreads();
   if (tid == 0) drain(p, m, p.nstages);
+  if constexpr (NB == 8) {
+  if (p.tm_gu && tid < 32) {
+    // every MMA of the launch is complete before the TMEM columns go back
+    if (tid == 0) {
+      umma_commit(&m->tc_fin);
+      const uint64_t t0 = gtimer();
+      while (!mbar_try_wait(&m->tc_fin, 0))
+        if (gtimer() - t0 > p.timeout_ns) {
+          set_error(p, MK_ERR_DEP_TIMEOUT, -1, -7);
+          break;
+        }
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(m->tmem) : "memory");
+  }
+  }
 }
 
 template <int NB, bool NUC>

@@ -181,7 +181,19 @@ struct Params {
   float top_p;
   float* lg_keep;       // [bcap][V] or null
   int sdone_cnt;
+  // expert gate/up on the tensor cores (kernel instances of batch 4 and 8):
+  // per layer a TMA tensor map (bf16 [E * 2F rows, H columns], 64 x 128 boxes,
+  // 128-byte swizzle) of w_gate_up, in device memory; null: CUDA cores
+  const void* tm_gu;
 };
+
+// Expert gate/up on the tensor cores: a stage is a tile of 128 of an
+// expert's interleaved gate/up rows (64 ffn units) by 64 columns per 16 KB of
+// stage (one or two 64-column boxes); an expert tile's range is a run of whole
+// 64-unit blocks.
+constexpr int TC_UNITS = 64;     // ffn units (gate + up row pairs) per tensor-core tile
+constexpr int TC_BOX = 16384;    // bytes of one 128-row x 64-column box
+inline bool tc_moe_shape(int H, int F) { return H % 128 == 0 && F % TC_UNITS == 0; }
 
 // Shared-memory layout of one CTA: [weight ring][activations][misc + down
 // sums][GEMV partial-sum windows].  The ring takes what the rest leaves of the

@@ -2,6 +2,8 @@
 // gets a task list, and dependencies are tracked with counters in global
 // memory" — "Inside the Megakernel Serving Engine for North Mini Code",
 // architecture paragraph) and the C ABI of include/mk.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -695,6 +697,32 @@ static void set_chunks(mk_plan* p, int batch, const int* chunk_first) {
   if (any) p->chunk0.assign(chunk_first, chunk_first + batch);
 }
 
+// TMA tensor maps of every layer's gate/up matrix for the tensor-core expert
+// path (batch instance 8): bf16 [E * 2F rows, H columns], 64 x 128 boxes,
+// 128-byte swizzle.  Uploaded to `dst` (device, L x 128 bytes).  False when
+// the driver's encoder is unavailable or refuses a map: the expert tiles then
+// run on the CUDA cores.
+static bool encode_gate_up_maps(const Shape& s, const mk_weights* w, void* dst) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      !fn || q != cudaDriverEntryPointSuccess)
+    return false;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  std::vector<CUtensorMap> maps((size_t)s.L);
+  const cuuint64_t gdim[2] = {(cuuint64_t)s.H, (cuuint64_t)s.E * 2 * s.F};
+  const cuuint64_t gstr[1] = {(cuuint64_t)s.H * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  for (int l = 0; l < s.L; ++l) {
+    if (enc(&maps[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w->w_gate_up[l]), gdim, gstr, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return cudaMemcpy(dst, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess;
+}
+
 static void destroy_one(mk_plan* p);
 
 static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_kv* kv, int batch,
@@ -821,6 +849,14 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
     P.embed = (const uint16_t*)w->embed;
     P.final_norm = (const uint16_t*)w->final_norm;
     P.lm_head = (const uint16_t*)w->lm_head;
+  }
+  // the batch-8 instance's expert gate/up on the tensor cores
+  P.tm_gu = nullptr;
+  if (p->nb == 8 && mk::tc_moe_shape(s.H, s.F) && !o.tc_off && p->stage_bytes % mk::TC_BOX == 0 &&
+      s.H % (64 * (p->stage_bytes / mk::TC_BOX)) == 0 && (long long)p->act_floats * 4 >= 32LL * s.H) {
+    void* maps = nullptr;
+    if (dalloc(p, (uint8_t**)&maps, L * sizeof(CUtensorMap)) != cudaSuccess) return fail(MK_ERR_CUDA);
+    if (encode_gate_up_maps(s, w, maps)) P.tm_gu = maps;
   }
   bool ok = true;
   ok &= dalloc(p, &p->d_ctr, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t)) == cudaSuccess;
@@ -1099,9 +1135,9 @@ static int read_debug_one(mk_plan* p, int what, void* dst, size_t bytes, mk_stre
 
 static int info_one(const mk_plan* p, int* out, int n) {
   if (!p || !out) return MK_ERR_INVALID;
-  const int v[10] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
-                     p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans};
-  for (int i = 0; i < n && i < 10; ++i) out[i] = v[i];
+  const int v[11] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
+                     p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans, p->P.tm_gu ? 1 : 0};
+  for (int i = 0; i < n && i < 11; ++i) out[i] = v[i];
   return MK_OK;
 }
 
@@ -1347,17 +1383,17 @@ int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream 
 int mk_plan_info(const mk_plan* p, int* out, int n) {
   if (!p || p->subs.empty()) return info_one(p, out, n);
   if (!out) return MK_ERR_INVALID;
-  int v[10] = {0};
+  int v[11] = {0};
   for (size_t i = 0; i < p->subs.size(); ++i) {
-    int w[10];
-    info_one(p->subs[i], w, 10);
+    int w[11];
+    info_one(p->subs[i], w, 11);
     if (i == 0)
-      for (int j = 0; j < 10; ++j) v[j] = w[j];
+      for (int j = 0; j < 11; ++j) v[j] = w[j];
     else
       for (int j : {1, 6, 7, 8, 9}) v[j] += w[j];   // tasks, attention / expert / LM tiles, replans
   }
   v[5] = p->group_B;
-  for (int i = 0; i < n && i < 10; ++i) out[i] = v[i];
+  for (int i = 0; i < n && i < 11; ++i) out[i] = v[i];
   return MK_OK;
 }
 

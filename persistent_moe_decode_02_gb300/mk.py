@@ -54,7 +54,7 @@ class MkPlanOpts(ctypes.Structure):
     _fields_ = [("timeout_us", ctypes.c_int), ("num_ctas", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("split_pages", ctypes.c_int), ("debug_drop_task", ctypes.c_int), ("trace", ctypes.c_int),
                 ("temperature", ctypes.c_float), ("seed", ctypes.c_ulonglong), ("top_p", ctypes.c_float),
-                ("chunk_first", ctypes.POINTER(ctypes.c_int))]
+                ("chunk_first", ctypes.POINTER(ctypes.c_int)), ("tc_off", ctypes.c_int)]
 
 
 class MkError(RuntimeError):
@@ -199,7 +199,7 @@ class Plan:
 
     def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
                  max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
-                 split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0):
+                 split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0, tc_off: bool = False):
         self.D = D
         self._keep = (weights, k_pools, v_pools)
         self._arrays = {k: _ptr_array(weights[k]) for k in
@@ -214,6 +214,7 @@ class Plan:
         self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
         self._dims = dims_struct(D)
         opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace))
+        opts.tc_off = int(bool(tc_off))
         self.batch = len(seq_lens)
         pt = [int(x) for x in page_table]
         h = ctypes.c_void_p()
@@ -310,10 +311,10 @@ class Plan:
         return out
 
     def info(self) -> dict:
-        buf = (ctypes.c_int * 10)()
-        lib().mk_plan_info(self.h, buf, 10)
+        buf = (ctypes.c_int * 11)()
+        lib().mk_plan_info(self.h, buf, 11)
         keys = ["num_ctas", "num_tasks", "nstages", "stage_bytes", "smem_bytes", "batch", "attn_tasks",
-                "gu_tasks", "lm_tiles", "replans"]
+                "gu_tasks", "lm_tiles", "replans", "tc_gate_up"]
         return dict(zip(keys, list(buf)))
 
     def close(self):
