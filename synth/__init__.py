@@ -200,13 +200,16 @@ def workload(name: str) -> Workload:
                         note="full shape, batch 32, ctx log-uniform [512, 32768], 2 leave / 2 join at 512 per step")
     if name == "full_b1_256k":
         return Workload(name, FULL, [262144], 16, note="full shape, batch 1, ctx 262144")
+    if name == "mid_b8":
+        return Workload(name, MID, log_uniform_lengths(8, 512, 4096, 0, "ctx.mid_b8"), 4,
+                        note="mid shape, batch 8, ctx log-uniform [512, 4096] (a few GB on the device: profiling case)")
     if name == "full_b8_long":
         return Workload(name, FULL, log_uniform_lengths(8, 8192, 262144, 0, "ctx.b8"), 16,
                         note="full shape, batch 8, ctx log-uniform [8192, 262144]")
     raise KeyError(name)
 
 
-WORKLOADS = ["tiny", "mid", "full_bs1_8k", "full_b32_churn", "full_b1_256k", "full_b8_long"]
+WORKLOADS = ["tiny", "mid", "mid_b8", "full_bs1_8k", "full_b32_churn", "full_b1_256k", "full_b8_long"]
 
 
 def first_token(dims: Dims, seed: int, rid: int) -> int:
