@@ -1528,7 +1528,9 @@ struct Consumer {
   __device__ bool prep_qkv(const Task& t, bool ab, ProjGemv& g) {
     const int l = t.layer;
     if (!ab) fill_rmsnorm(p.attn_norm[l], [&](int b, int i4) { return x_in4(l, b, i4); });
-    cbar();
+    // the column-slice GEMV (K a multiple of 2048) reads the scale only after its
+    // window barrier; the narrow-row path calls the epilogue without one
+    if (p.H & 2047) cbar();
     g.K = p.H;
     g.r0 = t.a[0];
     g.r1 = t.a[1];
@@ -1862,22 +1864,29 @@ struct Consumer {
       if (NB == 8 && p.tm_gu) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor cores
     }
     cbar();
-    if (ct < p.B) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
-      m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
-    }
-    cbar();
     unsigned long long q0 = 0;
 #pragma unroll
     for (int c = 0; c < RL_COPIES; ++c) q0 += v0[c];
     if constexpr (NB == 1) {
+      // one request: every thread forms the scale itself (the same sum in the
+      // same order, so the same bits); the routing's barrier orders m->inv[0]
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) tot += m->red[w];
+      const float inv0 = 1.0f / sqrtf(tot / (float)H + p.eps);
+      if (ct == 0) m->inv[0] = inv0;
       for (int i = ct; i < BE; i += NCT) {
-        const float v = from_fixed(i == ct ? q0 : load_sum(i)) * m->inv[i / E];
+        const float v = from_fixed(i == ct ? q0 : load_sum(i)) * inv0;
         m->rl[i] = v == v ? v : -INFINITY;
       }
     } else {
+      if (ct < p.B) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
+        m->inv[ct] = 1.0f / sqrtf(tot / (float)H + p.eps);
+      }
+      cbar();
       if (ct < BE) {
         const float v = from_fixed(q0) * m->inv[ct / E];
         m->rl[ct] = v == v ? v : -INFINITY;
