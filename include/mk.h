@@ -288,7 +288,8 @@ int mk_plan_read_debug(mk_plan* plan, int what, void* dst, size_t bytes, mk_stre
 
 /* Describe the current plan (host-side numbers): writes up to `n` ints:
  * [num_ctas, num_tasks, nstages, stage_bytes, smem_bytes, batch, n_attn_tasks,
- *  n_gu_tasks, n_lm_tiles, replans, expert gate/up on the tensor cores (1/0)]. */
+ *  n_gu_tasks, n_lm_tiles, replans, expert gate/up on the tensor cores (1/0),
+ *  QKV and O projections on the tensor cores (1/0)]. */
 int mk_plan_info(const mk_plan* plan, int* out, int n);
 
 void mk_plan_destroy(mk_plan* plan);

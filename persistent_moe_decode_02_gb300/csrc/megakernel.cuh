@@ -573,6 +573,10 @@ struct Geo {
   int cs, cu, cf;   // gate/up cursor: stage cs starts at unit cf of distinct expert cu
   int ws, wu, wf;   // down cursor, the same for down stage ws
   bool tc;          // gate/up stages are tensor-core tiles (128 rows x 64 columns per 16 KB)
+  // projection on the tensor cores: rows [r0, r0 + 128), nw stages of 128
+  // columns from K stage ks0 (then, for O, the router stage)
+  bool tcp;
+  int ks0, nw;
 };
 
 // Producer: one thread that walks the CTA's tasks and fills the ring with
@@ -660,9 +664,21 @@ struct Producer {
   __device__ bool geo(const Task& t, Geo& q, RouteCache* c, int task) {
     q.type = t.type;
     q.l = t.layer;
+    q.tcp = false;
     const int l = t.layer;
     switch (t.type) {
       case T_QKV: case T_OPROJ: case T_LM: {
+        if constexpr (NB == 8) {
+          if (p.tm_qkv && t.type != T_LM) {
+            q.tcp = true;
+            q.r0 = t.a[0];
+            q.r1 = t.a[1];
+            q.ks0 = t.a[3];
+            q.nw = t.a[4] - t.a[3];
+            q.nst = q.nw + (t.type == T_OPROJ ? 1 : 0);   // + the router stage
+            return true;
+          }
+        }
         q.W = t.type == T_QKV ? p.wqkv[l] : t.type == T_OPROJ ? p.wo[l] : p.lm_head;
         // the O projection's K halves (o_halves = 2) stream one after the other
         q.halves = kSplit && t.type == T_OPROJ ? p.o_halves : 1;
@@ -867,6 +883,18 @@ struct Producer {
           const void* tm = reinterpret_cast<const uint8_t*>(p.tm_gu) + (size_t)q.l * 128;
           mbar_expect_tx_only(bar, (uint32_t)nbox * TC_BOX);
           for (int h = 0; h < nbox; ++h) tma_g2s_2d(dst + h * TC_BOX, tm, (ks * nbox + h) * 64, y, bar, pol);
+        } else if (NB == 8 && q.tcp) {
+          if (s < q.nw) {
+            // projection tile: 128 rows x 128 columns (two 64-column boxes) of K stage ks0 + s
+            const void* tm = reinterpret_cast<const uint8_t*>(q.type == T_QKV ? p.tm_qkv : p.tm_o) + (size_t)q.l * 128;
+            mbar_expect_tx_only(bar, 2u * TC_BOX);
+            for (int h = 0; h < 2; ++h) tma_g2s_2d(dst + h * TC_BOX, tm, (q.ks0 + s) * 128 + h * 64, q.r0, bar, pol);
+          } else {
+            // the O tile's router stage: its 128 rows of the transposed router
+            const uint32_t nb = 128u * p.E * 2;
+            mbar_expect_tx_only(bar, nb);
+            bulk_g2s(dst, p.router[q.l] + (size_t)q.r0 * p.E, nb, bar, pol);
+          }
         } else {
           segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
             mbar_expect_tx_only(bar, b);
@@ -1082,6 +1110,36 @@ struct Consumer {
   __device__ float x_in(int l, int b, int i) const {
     if (l == 0) return bf2f(p.embed[(size_t)token(b) * p.H + i]);
     return __ldcg(p.x_out + ((size_t)(l - 1) * p.bcap + b) * p.H + i);
+  }
+
+  // Element `off` of the QKV outputs: fp32, or the tensor-core tiles'
+  // fixed-point sums.
+  __device__ __forceinline__ float qkv_at(size_t off) const {
+    if constexpr (NB == 8) {
+      if (p.qkv_fx) return from_fixed(__ldcg(p.qkv_fx + off));
+    }
+    return __ldcg(p.qkv + off);
+  }
+
+  // x_mid of layer l (after the O projection and residual), request b: four
+  // columns from i4 * 4, or column i; fp32 or fixed-point sums as qkv_at.
+  __device__ __forceinline__ float4 xmid4(int l, int b, int i4) const {
+    const size_t off = ((size_t)l * p.bcap + b) * p.H + 4 * (size_t)i4;
+    if constexpr (NB == 8) {
+      if (p.xmid_fx) {
+        const ulonglong2 a = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off));
+        const ulonglong2 c = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off) + 1);
+        return make_float4(from_fixed(a.x), from_fixed(a.y), from_fixed(c.x), from_fixed(c.y));
+      }
+    }
+    return __ldcg(reinterpret_cast<const float4*>(p.x_mid + off));
+  }
+  __device__ __forceinline__ float xmid1(int l, int b, int i) const {
+    const size_t off = ((size_t)l * p.bcap + b) * p.H + i;
+    if constexpr (NB == 8) {
+      if (p.xmid_fx) return from_fixed(__ldcg(p.xmid_fx + off));
+    }
+    return __ldcg(p.x_mid + off);
   }
 
   // dot of one 16-byte bf16 granule with 8 activations
@@ -1792,7 +1850,6 @@ struct Consumer {
     unsigned long long v0[RL_COPIES];   // this thread's first sum: its loads go out now, the adds come later
 #pragma unroll
     for (int c = 0; c < RL_COPIES; ++c) v0[c] = ct < BE ? __ldcg(rs + c * cs + ct) : 0ull;
-    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
     const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 x0[2];
@@ -1800,7 +1857,7 @@ struct Consumer {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = ct + h * NCT;
-      x0[h] = i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm) + i) : z4;
+      x0[h] = i < H4 ? xmid4(l, 0, i) : z4;
       g0[h] = i < H4 ? __ldg(gam + i) : make_uint2(0u, 0u);
     }
     for (int i = ct; i < MAX_EXPERTS; i += NCT) m->cnt_of[i] = 0;
@@ -1828,7 +1885,7 @@ struct Consumer {
         xv[h][0] = x0[h];
 #pragma unroll
         for (int b = 1; b < NB; ++b)
-          xv[h][b] = b < p.B && i < H4 ? __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i) : z4;
+          xv[h][b] = b < p.B && i < H4 ? xmid4(l, b, i) : z4;
       }
       float ss[NB];
 #pragma unroll
@@ -1929,14 +1986,180 @@ struct Consumer {
   // bytes (2 KB), rows in two 8-row groups of 1024 bytes, the 16-byte chunk c
   // of row r stored at chunk c ^ r.
   __device__ __forceinline__ void store_b_operand(int b, int k, float4 y) {
+    store_b_at(reinterpret_cast<uint8_t*>(act), b, k, y);
+  }
+  // The same into the slices from `at` (column k counted from there).
+  __device__ __forceinline__ static void store_b_at(uint8_t* at, int b, int k, float4 y) {
     const uint16_t h0 = f2bf(y.x), h1 = f2bf(y.y), h2 = f2bf(y.z), h3 = f2bf(y.w);
     const uint16_t l0 = f2bf(y.x - bf2f(h0)), l1 = f2bf(y.y - bf2f(h1)), l2 = f2bf(y.z - bf2f(h2)),
                    l3 = f2bf(y.w - bf2f(h3));
     const int sl = k >> 6, c = (k & 63) >> 3, half = k & 4;
-    uint8_t* base = reinterpret_cast<uint8_t*>(act) + sl * 2048 + b * 128 + ((c ^ b) << 4) + half * 2;
+    uint8_t* base = at + sl * 2048 + b * 128 + ((c ^ b) << 4) + half * 2;
     *reinterpret_cast<uint2*>(base) = make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
     *reinterpret_cast<uint2*>(base + 1024) =
         make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
+  }
+
+  // A QKV or O projection task on the tensor cores (batch instance 8): rows
+  // [row0, row0 + 128) of the matrix over its 128-column K stages [ks0, ks1).
+  // B operand slot j (4 KB: two 64-column slices of 16 rows, bf16 hi then lo
+  // of the 8 requests' activations, K-major, 128-byte swizzled) holds the
+  // columns of stage ks0 + j.  One thread issues each stage's M = 128, N = 16,
+  // K = 16 MMAs into TMEM and releases the stage by tcgen05.commit; warps 0-3
+  // then read the accumulator (one TMEM lane per row), add each request's hi
+  // and lo columns and add the part to the rows' 32.32 fixed-point sums:
+  //   QKV: the part times the request's RMS-norm scale (the B rows are x * gain);
+  //   O:   the part, plus the residual x in the task that holds K stage 0, and
+  //        the part's share of the router logits, sum_r WrT[r][e] gain[r] part[b][r]
+  //        (linear in x_mid, so the tasks of a row add theirs separately), from
+  //        the router stage that follows the weight stages.
+  // The O tasks also clear the layer's QKV sums (the attention has read them).
+  __device__ bool proj_tc(const Task& t, bool ab) {
+    const int l = t.layer, row0 = t.a[0], ks0 = t.a[3], nu = t.a[4] - t.a[3], B = p.B;
+    const bool isq = t.type == T_QKV;
+    uint8_t* bs = reinterpret_cast<uint8_t*>(act);
+    const int c0 = ks0 * 128, nc = nu * 128;   // the B slots' columns
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!ab) {
+      if (isq) {
+        // the norm needs whole rows; the B slots take columns [c0, c0 + nc)
+        const int H4 = p.H >> 2;
+        float ss[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) ss[b] = 0.f;
+        for (int i = ct; i < H4; i += NCT) {
+          float4 v[8];
+#pragma unroll
+          for (int b = 0; b < 8; ++b) v[b] = b < B ? x_in4(l, b, i) : z4;
+          const int c = 4 * i - c0;
+          const bool inb = c >= 0 && c < nc;
+          const uint2 gb = inb ? __ldg(reinterpret_cast<const uint2*>(p.attn_norm[l]) + i) : make_uint2(0u, 0u);
+          const float g0 = bf_lo(gb.x), g1 = bf_hi(gb.x), g2 = bf_lo(gb.y), g3 = bf_hi(gb.y);
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            ss[b] = fmaf(v[b].x, v[b].x, fmaf(v[b].y, v[b].y, fmaf(v[b].z, v[b].z, fmaf(v[b].w, v[b].w, ss[b]))));
+            if (inb)
+              store_b_at(bs + (c >> 7) * 4096, b, c & 127,
+                         make_float4(v[b].x * g0, v[b].y * g1, v[b].z * g2, v[b].w * g3));
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const float tt = warp_sum(ss[b]);
+          if (lane == 0) m->red[b * NCW + cw] = tt;
+        }
+      } else {
+        // the attention output's columns [c0, c0 + nc) of every request
+        const int KF = p.nq * p.d, n4 = nc >> 2;
+        const float* o = p.o + (size_t)l * p.bcap * KF + c0;
+        for (int x = ct; x < 8 * n4; x += NCT) {
+          const int b = x / n4, i = x - b * n4;
+          const float4 y = b < B ? __ldcg(reinterpret_cast<const float4*>(o + (size_t)b * KF) + i) : z4;
+          store_b_at(bs + (i >> 5) * 4096, b, (4 * i) & 127, y);
+        }
+        // every attention task of the layer is done: clear this task's share of the QKV sums
+        const long long n = (long long)B * p.qkv_rows;
+        unsigned long long* qs = p.qkv_fx + (size_t)l * p.bcap * p.qkv_rows;
+        for (long long i = n * t.a[2] / t.a[5] + ct; i < n * (t.a[2] + 1) / t.a[5]; i += NCT) qs[i] = 0ull;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor cores
+    }
+    cbar();
+    if (isq && !ab && ct < B) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) tot += m->red[ct * NCW + w];
+      m->inv[ct] = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+    }
+    mark(TR_ACT);
+    const uint32_t bsm = smem_u32(bs), tmem = m->tmem;
+    for (int j = 0; j < nu; ++j) {
+      const uint8_t* st = wait_stage(ab);
+      if (cw == 0) {
+        if (lane == 0) {
+          if (st) {
+            tc_fence_after();
+            const uint32_t sa = smem_u32(st);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16(tmem, umma_desc_sw128(sa + h * TC_BOX + kk * 32),
+                         umma_desc_sw128(bsm + j * 4096 + h * 2048 + kk * 32), UMMA_IDESC_M128_N16,
+                         (j | h | kk) != 0);
+            umma_commit(&m->empty[r.stage]);   // the stage is free once its MMAs are done
+            if (j == nu - 1) umma_commit(&m->acc_bar);
+          } else {
+            mbar_arrive(&m->empty[r.stage]);
+          }
+        }
+        __syncwarp();
+        if (p.strace && ct == 0) stage_stamp(2);
+        r.advance();
+      } else {
+        release_stage(ab);
+      }
+    }
+    const uint8_t* rst = isq ? nullptr : wait_stage(ab);   // the O task's router rows [128][E] bf16
+    ab = cbar_or(ab);
+    float* vb = psum;   // O: [128 rows][8 requests] part * gain, the router share's input
+    if (!ab && cw < 4) {
+      const int r = cw * 32 + lane, row = row0 + r;
+      float xr[8];   // the residual's loads go out before the accumulator wait
+#pragma unroll
+      for (int b = 0; b < 8; ++b) xr[b] = !isq && ks0 == 0 && b < B ? x_in(l, b, row) : 0.f;
+      if (!mbar_wait(p, m, &m->acc_bar, acc_ph, -7)) ab = true;
+      tc_fence_after();
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(cw * 32) << 16), v);
+      if (isq) {
+        unsigned long long* out = p.qkv_fx + (size_t)l * p.bcap * p.qkv_rows + row;
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          if (!ab && b < B) atomicAdd(out + (size_t)b * p.qkv_rows, to_fixed((v[b] + v[8 + b]) * m->inv[b]));
+      } else {
+        const float gn = bf2f(p.ffn_norm[l][row]);
+        unsigned long long* out = p.xmid_fx + (size_t)l * p.bcap * p.H + row;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const float x = v[b] + v[8 + b] + xr[b];
+          if (!ab && b < B) atomicAdd(out + (size_t)b * p.H, to_fixed(x));
+          vb[r * 8 + b] = b < B ? x * gn : 0.f;
+        }
+      }
+    }
+    acc_ph ^= 1;
+    tc_fence_before();
+    ab = cbar_or(ab);   // the accumulator is read before the next task's MMAs overwrite it
+    if (!isq) {
+      if (!ab && rst) {
+        // router share: thread (request half bh, expert e) over the tile's 128 rows
+        const uint16_t* wr = reinterpret_cast<const uint16_t*>(rst);
+        const int E = p.E;
+        unsigned long long* out = p.rlsum + ((size_t)l * RL_COPIES + t.a[2] % RL_COPIES) * p.bcap * E;
+        for (int x = ct; x < 2 * E; x += NCT) {
+          const int bh = x / E, e = x - bh * E;
+          if (4 * bh < B) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < 128; ++r) {
+              const float w = bf2f(wr[r * E + e]);
+              const float4 xv = *reinterpret_cast<const float4*>(vb + r * 8 + 4 * bh);
+              a0 = fmaf(w, xv.x, a0);
+              a1 = fmaf(w, xv.y, a1);
+              a2 = fmaf(w, xv.z, a2);
+              a3 = fmaf(w, xv.w, a3);
+            }
+            const float a[4] = {a0, a1, a2, a3};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (4 * bh + q < B) atomicAdd(out + (size_t)(4 * bh + q) * E + e, to_fixed(a[q]));
+          }
+        }
+      }
+      release_stage(ab);
+    }
+    return ab;
   }
 
   // The gate/up part of an expert tile on the tensor cores (batch instance 8):
@@ -2044,11 +2267,10 @@ struct Consumer {
         // this layer's blocks do not fit the coefficient scratch: the CUDA
         // cores take it, from fp32 activations in place of the B operand
         const int H4 = H >> 2;
-        const float* xm = p.x_mid + (size_t)l * p.bcap * H;
         const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
         for (int x = ct; x < p.B * H4; x += NCT) {
           const int b = x / H4, i = x - b * H4;
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(xm + (size_t)b * H) + i);
+          const float4 v = xmid4(l, b, i);
           const uint2 gb = __ldg(gam + i);
           reinterpret_cast<float4*>(act + (size_t)b * H)[i] =
               make_float4(v.x * bf_lo(gb.x), v.y * bf_hi(gb.x), v.z * bf_lo(gb.y), v.w * bf_hi(gb.y));
@@ -2175,14 +2397,13 @@ struct Consumer {
     const int nch = no > 0 ? max(1, NCT / no) : 1;
     float* rs = act;                                   // [output][chunk] sums
     mark(TR_ACT);
-    const float* xm = p.x_mid + (size_t)l * p.bcap * H;
     if (!ab) {   // every expert tile of the layer has read the router sums: zero this task's share
       const long long n = (long long)RL_COPIES * p.bcap * p.E;
       unsigned long long* rs = p.rlsum + (size_t)l * n;
       for (long long i = r0 * n / H + ct; i < (long long)t.a[1] * n / H; i += NCT) rs[i] = 0ull;
     }
     // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)
-    const float xres = !ab && ct < no ? __ldcg(xm + (size_t)(ct / nr) * H + r0 + ct % nr) : 0.f;
+    const float xres = !ab && ct < no ? xmid1(l, ct / nr, r0 + ct % nr) : 0.f;
     if (!ab) {
       // thread x takes output o = x % no and every nch-th tile from chunk c = x / no,
       // so a warp reads consecutive rows of a tile; up to BT loads in flight
@@ -2209,9 +2430,12 @@ struct Consumer {
       float* xo = p.x_out + (size_t)l * p.bcap * H;
       for (int o = ct; o < no; o += NCT) {
         const int b = o / nr, h = r0 + (o - b * nr);
-        float s = o == ct ? xres : __ldcg(xm + (size_t)b * H + h);
+        float s = o == ct ? xres : xmid1(l, b, h);
         for (int c = 0; c < nch; ++c) s += rs[o * nch + c];
         xo[(size_t)b * H + h] = s;
+        if constexpr (NB == 8) {   // the last reader of the fixed-point x_mid: clear it for the next step
+          if (p.xmid_fx) p.xmid_fx[((size_t)l * p.bcap + b) * H + h] = 0ull;
+        }
       }
     }
     mark(TR_STAGES);
@@ -2243,7 +2467,7 @@ struct Consumer {
     float* vn_s = kn_s + d;
     float* mrg = vn_s + d;                         // [groups][G][RS]
     uint32_t* pscr = reinterpret_cast<uint32_t*>(mrg + p.attn_mrg_floats);   // [NCW][2][8][8] packed P
-    const float* qkv = p.qkv + ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;
+    const size_t qo = ((size_t)l * p.bcap + b) * p.qkv_rows + (size_t)g * (G + 2) * d;   // this group's q rows
     const float2* rope = p.rope + (size_t)pos * half;
     const float qscale = 1.4426950408889634f / sqrtf((float)d);  // log2(e)/sqrt(d): exp2 softmax
     const bool has_new = pos >= tok0 && pos < tok1;
@@ -2253,14 +2477,14 @@ struct Consumer {
     // are patched into the stages here from the QKV outputs, like the row's own
     const int nprev = p.chunk0 ? b - __ldcg(p.chunk0 + b) : 0;
     const int pq0 = max(tok0, pos - nprev), pq1 = min(tok1, pos + 1);   // patched positions
-    const float* qkv_rows = p.qkv + (size_t)l * p.bcap * p.qkv_rows + (size_t)g * (G + 2) * d + (size_t)G * d;
+    const size_t qro = (size_t)l * p.bcap * p.qkv_rows + (size_t)g * (G + 2) * d + (size_t)G * d;   // row 0's k
     if (!ab) {
       for (int idx = ct; idx < MAX_G * half; idx += NCT) {
         const int h = idx / half, i = idx - h * half;
         float qa = 0.f, qb = 0.f;
         if (h < G) {
           const float2 cs = rope[i];
-          const float a = __ldcg(qkv + h * d + i), c = __ldcg(qkv + h * d + i + half);
+          const float a = qkv_at(qo + h * d + i), c = qkv_at(qo + h * d + i + half);
           qa = (a * cs.x - c * cs.y) * qscale;
           qb = (c * cs.x + a * cs.y) * qscale;
         }
@@ -2268,15 +2492,14 @@ struct Consumer {
         q_s[h * d + i + half] = qb;
       }
       if (has_new) {
-        const float* kr = qkv + (size_t)G * d;
-        const float* vr = kr + d;
+        const size_t kr = qo + (size_t)G * d, vr = kr + d;
         const size_t base =
             ((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * d * PS + pos % PS;
         uint16_t* kd = p.k_pool[l] + base;
         uint16_t* vd = p.v_pool[l] + base;
         for (int i = ct; i < half; i += NCT) {
           const float2 cs = rope[i];
-          const float a = __ldcg(kr + i), c = __ldcg(kr + i + half);
+          const float a = qkv_at(kr + i), c = qkv_at(kr + i + half);
           const uint16_t k0 = f2bf(a * cs.x - c * cs.y), k1 = f2bf(c * cs.x + a * cs.y);
           kd[(size_t)i * PS] = k0;
           kd[(size_t)(i + half) * PS] = k1;
@@ -2284,7 +2507,7 @@ struct Consumer {
           kn_s[i + half] = bf2f(k1);
         }
         for (int i = ct; i < d; i += NCT) {
-          const uint16_t v0 = f2bf(__ldcg(vr + i));
+          const uint16_t v0 = f2bf(qkv_at(vr + i));
           vd[(size_t)i * PS] = v0;
           vn_s[i] = bf2f(v0);
         }
@@ -2370,12 +2593,12 @@ struct Consumer {
             const int pi = q / PS - pg, sl = q % PS;
             uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
             uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
-            const float* kr = qkv_rows + (size_t)(b - (pos - q)) * p.qkv_rows;   // row b - (pos - q)
+            const size_t kr = qro + (size_t)(b - (pos - q)) * p.qkv_rows;   // row b - (pos - q)
             const int i0 = dim < half ? dim : dim - half;
             const float2 cs = p.rope[(size_t)q * half + i0];
-            const float a = __ldcg(kr + i0), c = __ldcg(kr + i0 + half);
+            const float a = qkv_at(kr + i0), c = qkv_at(kr + i0 + half);
             kp[dim * PS + sl] = f2bf(dim < half ? a * cs.x - c * cs.y : c * cs.x + a * cs.y);
-            vp[dim * PS + sl] = f2bf(__ldcg(kr + d + dim));
+            vp[dim * PS + sl] = f2bf(qkv_at(kr + d + dim));
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -2936,6 +3159,15 @@ struct Consumer {
       switch (t.type) {
         case T_QKV:
         case T_OPROJ: {
+          if constexpr (NB == 8) {
+            if (p.tm_qkv) {   // tensor cores: one 128-row tile over a run of K stages
+              ab = proj_tc(t, ab);
+              mark(TR_STAGES);
+              ab = finish(ab);
+              if (!ab) signal(t.type == T_QKV ? p.cm.qkv + t.layer * p.nkv + t.a[2] : p.cm.o + t.layer);
+              break;
+            }
+          }
           ProjGemv g;
           if constexpr (NB > 2) {   // the O projection may run in K halves
             const int parts = t.type == T_OPROJ ? p.o_halves : 1;

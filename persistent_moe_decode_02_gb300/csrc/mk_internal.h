@@ -185,6 +185,17 @@ struct Params {
   // per layer a TMA tensor map (bf16 [E * 2F rows, H columns], 64 x 128 boxes,
   // 128-byte swizzle) of w_gate_up, in device memory; null: CUDA cores
   const void* tm_gu;
+  // QKV and O projections on the tensor cores (batch instance 8, with tm_gu):
+  // per layer a TMA tensor map of wqkv (bf16 [qkv_rows, H]) and of wo (bf16
+  // [H, nq * d]), 64 x 128 boxes, 128-byte swizzle, in device memory.  A task
+  // is one 128-row tile of the matrix over a run of its 128-column K stages;
+  // the tiles of a row add their parts in 32.32 fixed point (integer adds:
+  // exact, so the bits do not depend on the order), the readers convert.
+  // null: CUDA cores, fp32 outputs in qkv and x_mid
+  const void* tm_qkv;
+  const void* tm_o;
+  unsigned long long* qkv_fx;    // [L][bcap][qkv_rows]; zeroed after use by the layer's O tiles
+  unsigned long long* xmid_fx;   // [L][bcap][H]; zeroed after use by the layer's reduce tasks
 };
 
 // Expert gate/up on the tensor cores: a stage is a tile of 128 of an
@@ -194,6 +205,15 @@ struct Params {
 constexpr int TC_UNITS = 64;     // ffn units (gate + up row pairs) per tensor-core tile
 constexpr int TC_BOX = 16384;    // bytes of one 128-row x 64-column box
 inline bool tc_moe_shape(int H, int F) { return H % 128 == 0 && F % TC_UNITS == 0; }
+// The projections on the tensor cores: 128-row tiles that never straddle a KV
+// group's rows, 128-column K stages, and an O tile's router rows ([128][E]
+// bf16) in one stage.  TC_PROJ_UNITS bounds a task's K stages (their B operand
+// slots, 4 KB each, share the activation region).
+constexpr int TC_PROJ_UNITS = 16;
+inline bool tc_proj_shape(int H, int nq, int d, int G, int E, int stage_bytes) {
+  return H % 128 == 0 && (nq * d) % 128 == 0 && ((G + 2) * d) % 128 == 0 && E % 4 == 0 &&
+         128 * E * 2 <= stage_bytes && stage_bytes == 2 * TC_BOX;
+}
 
 // Shared-memory layout of one CTA: [weight ring][activations][misc + down
 // sums][GEMV partial-sum windows].  The ring takes what the rest leaves of the

@@ -408,7 +408,9 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.top_p = 1.f;
   P.lg_keep = nullptr;
   P.sdone_cnt = 1;
-  P.tm_gu = nullptr;     // the expert gate/up on CUDA cores here
+  P.tm_gu = nullptr;     // the expert gate/up and the projections on CUDA cores here
+  P.tm_qkv = P.tm_o = nullptr;
+  P.qkv_fx = P.xmid_fx = nullptr;
   P.timeout_ns = 2000000000ull;
   P.strace = nullptr;
   P.cm = cm;

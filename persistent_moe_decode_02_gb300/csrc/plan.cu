@@ -157,7 +157,7 @@ inline void split_range(int n, int parts, int i, int& a, int& b) {
 // topological order, so with all CTAs resident the step cannot deadlock.
 int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int split_pages,
                 std::vector<Task>& out, std::vector<int>& cta_start, Counts& cnt,
-                std::vector<int>& open_start, bool nucleus = false) {
+                std::vector<int>& open_start, bool nucleus = false, bool tcp = false) {
   if (B < 1 || B > bcap || C < 1) return MK_ERR_INVALID;
   mk::CtrMap cm;
   cm.init(s.L, s.nkv, bcap);
@@ -167,6 +167,17 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   // tile counts
   cnt.qkv_per_g = std::max(1, std::min(Rg, (C + s.nkv - 1) / s.nkv));
   cnt.o = std::max(1, std::min(s.H, C));
+  // tensor-core projections: each 128-row tile split into kq (QKV) or ko (O)
+  // runs of its 128-column K stages, as many as the CTAs allow, each run at
+  // most TC_PROJ_UNITS stages
+  const int kst_q = s.H / 128, kst_o = nqd / 128, mt_q = s.qkv_rows / 128, mt_o = s.H / 128;
+  int kq = 1, ko = 1;
+  if (tcp) {
+    kq = std::min(kst_q, std::max(std::max(1, C / mt_q), (kst_q + mk::TC_PROJ_UNITS - 1) / mk::TC_PROJ_UNITS));
+    ko = std::min(kst_o, std::max(std::max(1, C / mt_o), (kst_o + mk::TC_PROJ_UNITS - 1) / mk::TC_PROJ_UNITS));
+    cnt.qkv_per_g = Rg / 128 * kq;
+    cnt.o = mt_o * ko;
+  }
   const int umax = std::min(s.E, B * s.k);
   cnt.gu = mk::moe_tiles(umax, s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   cnt.down = std::max(1, std::min(s.H, C));
@@ -205,7 +216,20 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
   for (int l = 0; l < s.L; ++l) {
     std::vector<std::pair<double, Task>> ph;
     // QKV projection tiles, per KV group
-    for (int g = 0; g < s.nkv; ++g) {
+    for (int mt = 0; tcp && mt < mt_q; ++mt) {
+      for (int i = 0; i < kq; ++i) {   // tensor cores: (128-row tile, run of K stages)
+        int a, b;
+        split_range(kst_q, kq, i, a, b);
+        Task t = mk_task(mk::T_QKV, l, l == 0 ? -1 : cm.down + l - 1, (uint32_t)cnt.down);
+        t.a[0] = mt * 128;
+        t.a[1] = mt * 128 + 128;
+        t.a[2] = mt * 128 / Rg;
+        t.a[3] = a;
+        t.a[4] = b;
+        ph.push_back({(double)(b - a) * 128 * 128 * 2, t});
+      }
+    }
+    for (int g = 0; !tcp && g < s.nkv; ++g) {
       for (int i = 0; i < cnt.qkv_per_g; ++i) {
         int a, b;
         split_range(Rg, cnt.qkv_per_g, i, a, b);
@@ -258,7 +282,19 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
     asg.phase(ph);
     ph.clear();
     // O projection + residual, each tile with its hidden rows' share of the router logits
-    for (int i = 0; i < cnt.o; ++i) {
+    for (int i = 0; tcp && i < cnt.o; ++i) {   // tensor cores: (128-row tile, run of K stages)
+      int a, b;
+      split_range(kst_o, ko, i % ko, a, b);
+      Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)cnt.comb);
+      t.a[0] = i / ko * 128;
+      t.a[1] = i / ko * 128 + 128;
+      t.a[2] = i;
+      t.a[3] = a;
+      t.a[4] = b;
+      t.a[5] = cnt.o;
+      ph.push_back({(double)(b - a + 1) * 128 * 128 * 2, t});
+    }
+    for (int i = 0; !tcp && i < cnt.o; ++i) {
       int a, b;
       split_range(s.H, cnt.o, i, a, b);
       Task t = mk_task(mk::T_OPROJ, l, cm.combine + l, (uint32_t)cnt.comb);
@@ -523,7 +559,8 @@ void build_for(const mk_plan* p, Built& b, int B = -1, const int* seq = nullptr)
     B = p->B;
     seq = p->seq.data();
   }
-  b.rc = build_tasks(p->s, B, p->bcap, seq, p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open, nucleus_on(p));
+  b.rc = build_tasks(p->s, B, p->bcap, seq, p->C, p->split_opt, b.tasks, b.cs, b.cnt, b.open, nucleus_on(p),
+                     p->P.tm_qkv != nullptr);
   b.nucleus = nucleus_on(p);
   if (b.rc != MK_OK) return;
   if (p->drop_task > 0 && p->drop_task - 1 < (int)b.tasks.size()) {
@@ -589,6 +626,12 @@ int commit_built(mk_plan* p, Built& b, cudaStream_t st, bool with_batch) {
     return MK_ERR_CUDA;
   if (cudaMemsetAsync(p->P.rlsum, 0, (size_t)p->s.L * mk::RL_COPIES * p->bcap * p->s.E * sizeof(unsigned long long), st) !=
       cudaSuccess)
+    return MK_ERR_CUDA;
+  if (p->P.tm_qkv &&
+      (cudaMemsetAsync(p->P.qkv_fx, 0, (size_t)p->s.L * p->bcap * p->s.qkv_rows * sizeof(unsigned long long), st) !=
+           cudaSuccess ||
+       cudaMemsetAsync(p->P.xmid_fx, 0, (size_t)p->s.L * p->bcap * p->s.H * sizeof(unsigned long long), st) !=
+           cudaSuccess))
     return MK_ERR_CUDA;
   p->epoch = 0;
   p->tasks.swap(tasks);
@@ -697,12 +740,12 @@ static void set_chunks(mk_plan* p, int batch, const int* chunk_first) {
   if (any) p->chunk0.assign(chunk_first, chunk_first + batch);
 }
 
-// TMA tensor maps of every layer's gate/up matrix for the tensor-core expert
-// path (batch instance 8): bf16 [E * 2F rows, H columns], 64 x 128 boxes,
-// 128-byte swizzle.  Uploaded to `dst` (device, L x 128 bytes).  False when
-// the driver's encoder is unavailable or refuses a map: the expert tiles then
-// run on the CUDA cores.
-static bool encode_gate_up_maps(const Shape& s, const mk_weights* w, void* dst) {
+// TMA tensor maps of one weight matrix per layer for the tensor-core paths
+// (batch instance 8): bf16 [rows, cols] row-major, 64 x 128 boxes, 128-byte
+// swizzle.  Uploaded to `dst` (device, L x 128 bytes).  False when the
+// driver's encoder is unavailable or refuses a map: the CUDA cores then take
+// the work.
+static bool encode_maps(const Shape& s, const void* const* mats, long long rows, long long cols, void* dst) {
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -710,12 +753,12 @@ static bool encode_gate_up_maps(const Shape& s, const mk_weights* w, void* dst) 
     return false;
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   std::vector<CUtensorMap> maps((size_t)s.L);
-  const cuuint64_t gdim[2] = {(cuuint64_t)s.H, (cuuint64_t)s.E * 2 * s.F};
-  const cuuint64_t gstr[1] = {(cuuint64_t)s.H * 2};
+  const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t gstr[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {64, 128};
   const cuuint32_t es[2] = {1, 1};
   for (int l = 0; l < s.L; ++l) {
-    if (enc(&maps[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w->w_gate_up[l]), gdim, gstr, box, es,
+    if (enc(&maps[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(mats[l]), gdim, gstr, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
@@ -851,12 +894,31 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
     P.lm_head = (const uint16_t*)w->lm_head;
   }
   // the batch-8 instance's expert gate/up on the tensor cores
-  P.tm_gu = nullptr;
+  P.tm_gu = P.tm_qkv = P.tm_o = nullptr;
+  P.qkv_fx = P.xmid_fx = nullptr;
   if (p->nb == 8 && mk::tc_moe_shape(s.H, s.F) && !o.tc_off && p->stage_bytes % mk::TC_BOX == 0 &&
       s.H % (64 * (p->stage_bytes / mk::TC_BOX)) == 0 && (long long)p->act_floats * 4 >= 32LL * s.H) {
     void* maps = nullptr;
     if (dalloc(p, (uint8_t**)&maps, L * sizeof(CUtensorMap)) != cudaSuccess) return fail(MK_ERR_CUDA);
-    if (encode_gate_up_maps(s, w, maps)) P.tm_gu = maps;
+    if (encode_maps(s, (const void* const*)w->w_gate_up, (long long)s.E * 2 * s.F, s.H, maps)) P.tm_gu = maps;
+  }
+  // and the QKV and O projections: B operand slots of a task's K stages (4 KB
+  // each) in the activation region
+  const int kst_max = std::max(s.H, s.nq * s.d) / 128;
+  if (P.tm_gu && mk::tc_proj_shape(s.H, s.nq, s.d, s.G, s.E, p->stage_bytes) &&
+      (long long)p->act_floats * 4 >= 4096LL * std::min(mk::TC_PROJ_UNITS, kst_max)) {
+    void* mq = nullptr;
+    void* mo = nullptr;
+    if (dalloc(p, (uint8_t**)&mq, L * sizeof(CUtensorMap)) != cudaSuccess ||
+        dalloc(p, (uint8_t**)&mo, L * sizeof(CUtensorMap)) != cudaSuccess ||
+        dalloc(p, &P.qkv_fx, L * bcap * s.qkv_rows * sizeof(unsigned long long)) != cudaSuccess ||
+        dalloc(p, &P.xmid_fx, L * bcap * s.H * sizeof(unsigned long long)) != cudaSuccess)
+      return fail(MK_ERR_CUDA);
+    if (encode_maps(s, (const void* const*)w->wqkv, s.qkv_rows, s.H, mq) &&
+        encode_maps(s, (const void* const*)w->wo, s.H, (long long)s.nq * s.d, mo)) {
+      P.tm_qkv = mq;
+      P.tm_o = mo;
+    }
   }
   bool ok = true;
   ok &= dalloc(p, &p->d_ctr, (size_t)p->cm.total * mk::CTR_STRIDE * sizeof(uint32_t)) == cudaSuccess;
@@ -1135,9 +1197,9 @@ static int read_debug_one(mk_plan* p, int what, void* dst, size_t bytes, mk_stre
 
 static int info_one(const mk_plan* p, int* out, int n) {
   if (!p || !out) return MK_ERR_INVALID;
-  const int v[11] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
-                     p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans, p->P.tm_gu ? 1 : 0};
-  for (int i = 0; i < n && i < 11; ++i) out[i] = v[i];
+  const int v[12] = {p->C, (int)p->tasks.size(), p->nstages, p->stage_bytes, p->smem, p->B,
+                     p->cnt.attn, p->cnt.gu, p->cnt.lm, p->replans, p->P.tm_gu ? 1 : 0, p->P.tm_qkv ? 1 : 0};
+  for (int i = 0; i < n && i < 12; ++i) out[i] = v[i];
   return MK_OK;
 }
 
@@ -1383,17 +1445,17 @@ int mk_plan_read_debug(mk_plan* p, int what, void* dst, size_t bytes, mk_stream 
 int mk_plan_info(const mk_plan* p, int* out, int n) {
   if (!p || p->subs.empty()) return info_one(p, out, n);
   if (!out) return MK_ERR_INVALID;
-  int v[11] = {0};
+  int v[12] = {0};
   for (size_t i = 0; i < p->subs.size(); ++i) {
-    int w[11];
-    info_one(p->subs[i], w, 11);
+    int w[12];
+    info_one(p->subs[i], w, 12);
     if (i == 0)
-      for (int j = 0; j < 11; ++j) v[j] = w[j];
+      for (int j = 0; j < 12; ++j) v[j] = w[j];
     else
       for (int j : {1, 6, 7, 8, 9}) v[j] += w[j];   // tasks, attention / expert / LM tiles, replans
   }
   v[5] = p->group_B;
-  for (int i = 0; i < n && i < 11; ++i) out[i] = v[i];
+  for (int i = 0; i < n && i < 12; ++i) out[i] = v[i];
   return MK_OK;
 }
 

@@ -311,10 +311,10 @@ class Plan:
         return out
 
     def info(self) -> dict:
-        buf = (ctypes.c_int * 11)()
-        lib().mk_plan_info(self.h, buf, 11)
+        buf = (ctypes.c_int * 12)()
+        lib().mk_plan_info(self.h, buf, 12)
         keys = ["num_ctas", "num_tasks", "nstages", "stage_bytes", "smem_bytes", "batch", "attn_tasks",
-                "gu_tasks", "lm_tiles", "replans", "tc_gate_up"]
+                "gu_tasks", "lm_tiles", "replans", "tc_gate_up", "tc_proj"]
         return dict(zip(keys, list(buf)))
 
     def close(self):

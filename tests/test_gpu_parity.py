@@ -485,24 +485,27 @@ def test_prefill_chunk_rows_match_per_token_decode(capacity):
 
 @pytest.mark.parametrize("name", ["tiny", "mid"])
 def test_expert_gate_up_on_tensor_cores(name):
-    # Batches of 5 to 8 run the experts' gate/up on the tensor cores (tcgen05
-    # MMAs from TMA tiles into TMEM): a ragged batch of 8 against the oracle,
-    # and against the same steps with the gate/up on the CUDA cores.  The
-    # tensor cores see each activation as bf16 hi + lo (16 significant bits,
-    # relative error about 2^-17 per element against fp32 on the CUDA cores),
-    # so the two agree to 1e-3 in relative L2, the tokens and experts exactly.
+    # Batches of 5 to 8 run the experts' gate/up and the QKV and O projections
+    # on the tensor cores (tcgen05 MMAs from TMA tiles into TMEM; the
+    # projections' 128-row tiles split over K and summed in fixed point): a
+    # ragged batch of 8 against the oracle, and against the same steps on the
+    # CUDA cores.  The tensor cores see each activation as bf16 hi + lo (16
+    # significant bits, relative error about 2^-17 per element against fp32 on
+    # the CUDA cores), so the two agree to 1e-3 in relative L2, the tokens and
+    # experts exactly.
     from persistent_moe_decode_02_gb300 import mk
     base = synth.workload(name)
     ctx = [128, 37, 95, 16, 1, 60, 77, 5] if name == "tiny" else [4096, 300, 1000, 17, 2500, 64, 999, 3000]
     wl = dataclasses.replace(base, ctx=ctx, steps=3)
     run = GpuRun(wl, steps=3)
-    assert run.plan.info()["tc_gate_up"] == 1
+    assert run.plan.info()["tc_gate_up"] == 1 and run.plan.info()["tc_proj"] == 1
     run.plan.close()
     rep = run_and_check(wl, steps=3)
     print(rep)
     rep.assert_ok()
     a, b = GpuRun(wl, steps=2), GpuRun(wl, steps=2, tc_off=True)
     assert a.plan.info()["tc_gate_up"] == 1 and b.plan.info()["tc_gate_up"] == 0
+    assert a.plan.info()["tc_proj"] == 1 and b.plan.info()["tc_proj"] == 0
     for _ in range(2):
         ra, rb = a.step(), b.step()
         assert torch.equal(ra.next_tok, rb.next_tok) and torch.equal(ra.ids, rb.ids)
