@@ -228,11 +228,23 @@ __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
-// 32.32 fixed point for the router-logit sums (two's complement in 64 bits).
+// 32.32 fixed point for the sums that tiles add in any order (router
+// logits; on the tensor-core path the projections' outputs): two's
+// complement in 64 bits.  Both forms give the same values: v * 2^32 is exact
+// (a power-of-two scale), then one rounding to the nearest integer; back, one
+// rounding of the integer to fp32 after an exact scale (|q| < 2^53).  FAST
+// (the batch-8 instance, whose expert tiles convert 16K values each) keeps
+// to fp32 scaling and 64-bit integer conversions: this part runs fp64 at a
+// small fraction of its fp32 rate.  The other instances convert a few
+// hundred values on the routing's critical path and keep the fp64 form.
+template <bool FAST>
 __device__ __forceinline__ unsigned long long to_fixed(float v) {
+  if constexpr (FAST) return (unsigned long long)__float2ll_rn(v * 4294967296.0f);
   return (unsigned long long)__double2ll_rn((double)v * 4294967296.0);
 }
+template <bool FAST>
 __device__ __forceinline__ float from_fixed(unsigned long long q) {
+  if constexpr (FAST) return __ll2float_rn((long long)q) * 2.3283064365386963e-10f;
   return (float)((double)(long long)q * 2.3283064365386963e-10);
 }
 
@@ -1116,7 +1128,7 @@ struct Consumer {
   // fixed-point sums.
   __device__ __forceinline__ float qkv_at(size_t off) const {
     if constexpr (NB == 8) {
-      if (p.qkv_fx) return from_fixed(__ldcg(p.qkv_fx + off));
+      if (p.qkv_fx) return from_fixed<NB == 8>(__ldcg(p.qkv_fx + off));
     }
     return __ldcg(p.qkv + off);
   }
@@ -1129,7 +1141,7 @@ struct Consumer {
       if (p.xmid_fx) {
         const ulonglong2 a = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off));
         const ulonglong2 c = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off) + 1);
-        return make_float4(from_fixed(a.x), from_fixed(a.y), from_fixed(c.x), from_fixed(c.y));
+        return make_float4(from_fixed<true>(a.x), from_fixed<true>(a.y), from_fixed<true>(c.x), from_fixed<true>(c.y));
       }
     }
     return __ldcg(reinterpret_cast<const float4*>(p.x_mid + off));
@@ -1137,7 +1149,7 @@ struct Consumer {
   __device__ __forceinline__ float xmid1(int l, int b, int i) const {
     const size_t off = ((size_t)l * p.bcap + b) * p.H + i;
     if constexpr (NB == 8) {
-      if (p.xmid_fx) return from_fixed(__ldcg(p.xmid_fx + off));
+      if (p.xmid_fx) return from_fixed<NB == 8>(__ldcg(p.xmid_fx + off));
     }
     return __ldcg(p.x_mid + off);
   }
@@ -1682,7 +1694,7 @@ struct Consumer {
         if (ok)
           for (int i = i0; i < i1; ++i) acc = fmaf(bf2f(wr[i * E + e]) * bf2f(gw[i]), xr[i], acc);
         const float other = __shfl_xor_sync(FULL, acc, 1);
-        if (ok && half == 0) atomicAdd(out + (size_t)b * E + e, to_fixed(acc + other));
+        if (ok && half == 0) atomicAdd(out + (size_t)b * E + e, to_fixed<NB == 8>(acc + other));
       }
     }
     release_stage(ab);
@@ -1933,7 +1945,7 @@ struct Consumer {
       const float inv0 = 1.0f / sqrtf(tot / (float)H + p.eps);
       if (ct == 0) m->inv[0] = inv0;
       for (int i = ct; i < BE; i += NCT) {
-        const float v = from_fixed(i == ct ? q0 : load_sum(i)) * inv0;
+        const float v = from_fixed<NB == 8>(i == ct ? q0 : load_sum(i)) * inv0;
         m->rl[i] = v == v ? v : -INFINITY;
       }
     } else {
@@ -1945,7 +1957,7 @@ struct Consumer {
       }
       cbar();
       if (ct < BE) {
-        const float v = from_fixed(q0) * m->inv[ct / E];
+        const float v = from_fixed<NB == 8>(q0) * m->inv[ct / E];
         m->rl[ct] = v == v ? v : -INFINITY;
       }
       // the rest two sums at a time, both sets of loads in flight together
@@ -1963,10 +1975,10 @@ struct Consumer {
           qa += a[c];
           qb += c2[c];
         }
-        const float va = from_fixed(qa) * m->inv[i / E];
+        const float va = from_fixed<NB == 8>(qa) * m->inv[i / E];
         m->rl[i] = va == va ? va : -INFINITY;
         if (i2 < BE) {
-          const float vb = from_fixed(qb) * m->inv[i2 / E];
+          const float vb = from_fixed<NB == 8>(qb) * m->inv[i2 / E];
           m->rl[i2] = vb == vb ? vb : -INFINITY;
         }
       }
@@ -2116,14 +2128,14 @@ struct Consumer {
         unsigned long long* out = p.qkv_fx + (size_t)l * p.bcap * p.qkv_rows + row;
 #pragma unroll
         for (int b = 0; b < 8; ++b)
-          if (!ab && b < B) atomicAdd(out + (size_t)b * p.qkv_rows, to_fixed((v[b] + v[8 + b]) * m->inv[b]));
+          if (!ab && b < B) atomicAdd(out + (size_t)b * p.qkv_rows, to_fixed<NB == 8>((v[b] + v[8 + b]) * m->inv[b]));
       } else {
         const float gn = bf2f(p.ffn_norm[l][row]);
         unsigned long long* out = p.xmid_fx + (size_t)l * p.bcap * p.H + row;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
           const float x = v[b] + v[8 + b] + xr[b];
-          if (!ab && b < B) atomicAdd(out + (size_t)b * p.H, to_fixed(x));
+          if (!ab && b < B) atomicAdd(out + (size_t)b * p.H, to_fixed<NB == 8>(x));
           vb[r * 8 + b] = b < B ? x * gn : 0.f;
         }
       }
@@ -2153,7 +2165,7 @@ struct Consumer {
             const float a[4] = {a0, a1, a2, a3};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (4 * bh + q < B) atomicAdd(out + (size_t)(4 * bh + q) * E + e, to_fixed(a[q]));
+              if (4 * bh + q < B) atomicAdd(out + (size_t)(4 * bh + q) * E + e, to_fixed<NB == 8>(a[q]));
           }
         }
       }
