@@ -61,6 +61,10 @@ __device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t byte
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// n arrivals at once (one warp standing in for n).
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
 
 // Flag handoff between this CTA's consumers and its producer thread.
 __device__ __forceinline__ void st_release_cta(int* p, int v) {
@@ -1015,6 +1019,14 @@ struct Consumer {
   __device__ void release_stage(bool ab) {
     __syncwarp();
     if (!ab && lane == 0) mbar_arrive(&m->empty[r.stage]);
+    if (p.strace && ct == 0) stage_stamp(2);
+    r.advance();
+  }
+  // The same for a stage that only n-th of the warps read: each of them
+  // arrives n times, so the slot's count is met without the other warps.
+  __device__ void release_stage_n(bool ab, int n) {
+    __syncwarp();
+    if (!ab && lane == 0) mbar_arrive_n(&m->empty[r.stage], (uint32_t)n);
     if (p.strace && ct == 0) stage_stamp(2);
     r.advance();
   }
@@ -2573,9 +2585,13 @@ struct Consumer {
     int si = 0;                                    // stage index within the chunk
     for (int pg = pg0; pg < pg1; pg += ppg, ++si) {
       const int npg = min(ppg, pg1 - pg);
-      const uint8_t* st = wait_stage(ab);
       const bool own = has_new && pos / PS >= pg && pos / PS < pg + npg;
       const bool patch = own || (nprev > 0 && pq0 < pq1 && pq0 / PS < pg + npg && (pq1 - 1) / PS >= pg);
+      // the stage belongs to one warp group (its ppg pages, one per warp): only
+      // that group waits for and releases it, each warp arriving npar times;
+      // every warp waits for a stage it helps patch
+      const bool mine = si % npar == par;
+      const uint8_t* st = mine || patch ? wait_stage(ab) : nullptr;
       if (st && patch) {
         // put the new token's K and V into its stage slot before anyone reads the
         // page, and zero the page's later slots: they hold no token yet, and
@@ -2619,7 +2635,7 @@ struct Consumer {
         cbar();
         cbar();
       }
-      if (st && si % npar == par && grp < npg) {
+      if (st && mine && grp < npg) {
         const int P = pg + grp;                    // global page index of this warp's page
         const int nvalid = min(PS, tok1 - P * PS); // tokens of the page inside the chunk
         const uint32_t kpage = smem_u32(st) + grp * PB;
@@ -2698,7 +2714,10 @@ struct Consumer {
           }
         }
       }
-      release_stage(ab);
+      if (mine)
+        release_stage_n(ab, npar);
+      else
+        r.advance();
     }
     mark(TR_STAGES);
     // merge the warps' partial softmax states of this chunk (a warp that saw
