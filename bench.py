@@ -272,7 +272,7 @@ def our_arm(args, wl):
     max_pages = max((c + total_steps + ps) // ps for c in wl.ctx) + 1
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, total_steps) + 4, max_pages, wl.seed)
     reqs = [kv.admit(rid, c, total_steps) for rid, c in enumerate(wl.ctx)]
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
+    plan = mk.Plan(D, model.weights(), kv.kv, [r.length for r in reqs], kv.page_table(reqs), max_pages,
                    tc_off=args.tc_off)
     B = wl.batch
     tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
@@ -407,7 +407,7 @@ def churn_arm(args, wl):
     live = [kv.admit(rid, c, n_steps + 1) for rid, c in enumerate(wl.ctx)]
     joiners = [kv.admit(B + i, jctx, n_steps + 1) for i in range(n_join)]
     join_tok = torch.tensor(initial_tokens(wl, [r.rid for r in joiners]), dtype=torch.int32, device="cuda")
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in live], kv.page_table(live), max_pages,
+    plan = mk.Plan(D, model.weights(), kv.kv, [r.length for r in live], kv.page_table(live), max_pages,
                    max_batch=B, tc_off=args.tc_off)
     tok = torch.tensor(initial_tokens(wl, list(range(B))), dtype=torch.int32, device="cuda")
     nxt = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -552,7 +552,7 @@ def timeline_arm(args, wl):
     max_pages = max((c + steps + 2 + ps) // ps for c in wl.ctx) + 1
     kv = PagedKV(D, kv_pages_needed(D, wl.ctx, steps + 2) + 4, max_pages, wl.seed)
     reqs = [kv.admit(i, c, steps + 2) for i, c in enumerate(wl.ctx)]
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs), max_pages,
+    plan = mk.Plan(D, model.weights(), kv.kv, [r.length for r in reqs], kv.page_table(reqs), max_pages,
                    trace=2 if args.stage_trace else 1)
     tok = torch.tensor(initial_tokens(wl, list(range(wl.batch))), dtype=torch.int32, device="cuda")
     times = []
@@ -597,16 +597,15 @@ def serve_arm(args, wl):
     ps = D.page_size
     max_pages = (256 + 128 + ps - 1) // ps
     num_pages = cap * max_pages
-    shape = (num_pages, D.n_kv_heads, D.head_dim, ps)
+    shape = (num_pages, D.n_kv_heads, 2, D.head_dim, ps)
     model = DeviceModel(D, wl.seed)
-    k = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
-    v = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
+    kv = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
     toks = synth.uniform_ints(int(sum(plen)), D.vocab, wl.seed, "serve tokens").tolist()
     prompts, o = [], 0
     for n in plen:
         prompts.append(toks[o:o + n])
         o += n
-    srv = mk.Server(D, model.weights(), k, v, max_batch=cap, max_pages=max_pages)
+    srv = mk.Server(D, model.weights(), kv, max_batch=cap, max_pages=max_pages)
     half = n_req // 2
     for i in range(half):
         srv.submit(i, prompts[i], olen[i])

@@ -86,16 +86,17 @@ typedef struct mk_weights {
   const void* const* w_down;
 } mk_weights;
 
-/* Paged KV cache: per layer one K pool and one V pool (HOST arrays of
- * n_layers device pointers), each bf16 [num_pages, n_kv_heads, head_dim,
- * page_size]: a page holds, per KV head, its tokens' vectors transposed (one
- * row of page_size slots per dimension), which keeps the tensor-core operand
- * loads of the attention tiles nearly free of shared-memory bank conflicts.
- * Token t of request b lives in page page_table[b][t / page_size], slot
- * t % page_size.  16-byte aligned. */
+/* Paged KV cache: per layer one pool (a HOST array of n_layers device
+ * pointers), bf16 [num_pages, n_kv_heads, 2, head_dim, page_size]: for each
+ * page and KV head its K block, then its V block, each holding the page's
+ * tokens' vectors transposed (one row of page_size slots per dimension).  A
+ * (page, head) is one contiguous 2 * head_dim * page_size * 2-byte copy for
+ * the attention tiles, and the transposed blocks keep their tensor-core
+ * operand loads nearly free of shared-memory bank conflicts.  Token t of
+ * request b lives in page page_table[b][t / page_size], slot t % page_size.
+ * 16-byte aligned. */
 typedef struct mk_kv {
-  void* const* k_pool;
-  void* const* v_pool;
+  void* const* kv_pool;
   int num_pages;
 } mk_kv;
 

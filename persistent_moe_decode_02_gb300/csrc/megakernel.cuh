@@ -783,10 +783,10 @@ struct Producer {
         const int pg = q.pg0 + s * q.ppg;
         const int n = min(q.ppg, q.pg1 - pg);
         const int* pt = p.page_table + (size_t)q.b * p.max_pages;
-        for (int i = 0; i < n; ++i) {
-          const size_t off = ((size_t)pt[pg + i] * p.nkv + q.g) * p.ps * p.d;
-          f(p.k_pool[l] + off, q.PB, (uint32_t)i * q.PB);
-          f(p.v_pool[l] + off, q.PB, (uint32_t)(q.ppg + i) * q.PB);
+#pragma unroll 1   // kept rolled: the producer's code shares the SM's instruction cache
+        for (int i = 0; i < n; ++i) {   // one copy per page: its K block, then its V block
+          const size_t off = ((size_t)pt[pg + i] * p.nkv + q.g) * 2 * p.ps * p.d;
+          f(p.kv_pool[l] + off, 2 * q.PB, (uint32_t)i * 2 * q.PB);
         }
         break;
       }
@@ -912,8 +912,11 @@ struct Producer {
             bulk_g2s(dst, p.router[q.l] + (size_t)q.r0 * p.E, nb, bar, pol);
           }
         } else {
+          // an attention stage's bytes are announced once, not per page
+          const bool one_tx = q.type == T_ATTN;
+          if (one_tx) mbar_expect_tx_only(bar, (uint32_t)min(q.ppg, q.pg1 - q.pg0 - s * q.ppg) * 2u * q.PB);
           segs(q, s, [&](const void* src, uint32_t b, uint32_t off) {
-            mbar_expect_tx_only(bar, b);
+            if (!one_tx) mbar_expect_tx_only(bar, b);
             bulk_g2s(dst + off, src, b, bar, pol);
           });
         }
@@ -2518,9 +2521,9 @@ struct Consumer {
       if (has_new) {
         const size_t kr = qo + (size_t)G * d, vr = kr + d;
         const size_t base =
-            ((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * d * PS + pos % PS;
-        uint16_t* kd = p.k_pool[l] + base;
-        uint16_t* vd = p.v_pool[l] + base;
+            ((size_t)p.page_table[(size_t)b * p.max_pages + pos / PS] * p.nkv + g) * 2 * d * PS + pos % PS;
+        uint16_t* kd = p.kv_pool[l] + base;
+        uint16_t* vd = kd + (size_t)d * PS;
         for (int i = ct; i < half; i += NCT) {
           const float2 cs = rope[i];
           const float a = qkv_at(kr + i), c = qkv_at(kr + i + half);
@@ -2600,8 +2603,8 @@ struct Consumer {
         cbar();
         if (own) {
           const int pi = pos / PS - pg, slot = pos % PS;
-          uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
-          uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
+          uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * 2 * PB);
+          uint16_t* vp = kp + (size_t)d * PS;
           for (int i = ct; i < d * PS; i += NCT) {
             const int dim = i / PS, sl = i - dim * PS;
             if (sl == slot) {
@@ -2619,8 +2622,8 @@ struct Consumer {
           for (int i = ct; i < (qb - qa) * d; i += NCT) {
             const int q = qa + i / d, dim = i - (i / d) * d;
             const int pi = q / PS - pg, sl = q % PS;
-            uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * PB);
-            uint16_t* vp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)(ppg + pi) * PB);
+            uint16_t* kp = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(st) + (size_t)pi * 2 * PB);
+            uint16_t* vp = kp + (size_t)d * PS;
             const size_t kr = qro + (size_t)(b - (pos - q)) * p.qkv_rows;   // row b - (pos - q)
             const int i0 = dim < half ? dim : dim - half;
             const float2 cs = p.rope[(size_t)q * half + i0];
@@ -2638,8 +2641,8 @@ struct Consumer {
       if (st && mine && grp < npg) {
         const int P = pg + grp;                    // global page index of this warp's page
         const int nvalid = min(PS, tok1 - P * PS); // tokens of the page inside the chunk
-        const uint32_t kpage = smem_u32(st) + grp * PB;
-        const uint32_t vpage = kpage + ppg * PB;
+        const uint32_t kpage = smem_u32(st) + grp * 2 * PB;   // the page's K block, then its V block
+        const uint32_t vpage = kpage + PB;
         // S = K . Q^T : A tiles of K^T-stored rows via ldmatrix.trans
         float s[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
         const int li = lane >> 3, lr = lane & 7;

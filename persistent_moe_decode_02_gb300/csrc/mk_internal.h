@@ -109,8 +109,7 @@ struct Params {
   const uint16_t* const* router;
   const uint16_t* const* w_gate_up;
   const uint16_t* const* w_down;
-  uint16_t* const* k_pool;
-  uint16_t* const* v_pool;
+  uint16_t* const* kv_pool;   // [num_pages][nkv][K, V][d][page_size] per layer
   // plan
   const Task* tasks;
   const int* cta_start;

@@ -250,7 +250,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
     return fail(MK_ERR_INVALID, "null argument or empty batch");
   if (batch > mk::MAX_BATCH) return fail(MK_ERR_UNSUPPORTED, "batch above 8");
   if (!w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->router || !w->w_gate_up || !w->w_down ||
-      !kv->k_pool || !kv->v_pool || !w->embed || !w->final_norm || !w->lm_head)
+      !kv->kv_pool || !w->embed || !w->final_norm || !w->lm_head)
     return fail(MK_ERR_INVALID, "null weight or KV pointer");
   int max_len = 0;
   for (int b = 0; b < batch; ++b) {
@@ -292,7 +292,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   // host staging layout: weight tables | seq lens | page table | tasks | cta offsets
   const size_t L = s.L;
   Carve hc;
-  const size_t h_tab = hc.take(9 * L * sizeof(void*));
+  const size_t h_tab = hc.take(8 * L * sizeof(void*));
   const size_t h_seq = hc.take((size_t)B * sizeof(int));
   const size_t h_pt = hc.take((size_t)B * max_pages_per_seq * sizeof(int));
   const size_t h_tasks = hc.take((size_t)ntasks * sizeof(mk::Task));
@@ -351,8 +351,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
     tab[4 * L + l] = w->router[l];
     tab[5 * L + l] = w->w_gate_up[l];
     tab[6 * L + l] = w->w_down[l];
-    tab[7 * L + l] = kv->k_pool[l];
-    tab[8 * L + l] = kv->v_pool[l];
+    tab[7 * L + l] = kv->kv_pool[l];
   }
   memcpy(hb + h_seq, seq_lens, (size_t)B * sizeof(int));
   memcpy(hb + h_pt, page_table, (size_t)B * max_pages_per_seq * sizeof(int));
@@ -393,8 +392,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.router = (const uint16_t* const*)(dtab + 4 * L);
   P.w_gate_up = (const uint16_t* const*)(dtab + 5 * L);
   P.w_down = (const uint16_t* const*)(dtab + 6 * L);
-  P.k_pool = (uint16_t* const*)(dtab + 7 * L);
-  P.v_pool = (uint16_t* const*)(dtab + 8 * L);
+  P.kv_pool = (uint16_t* const*)(dtab + 7 * L);
   P.embed = (const uint16_t*)w->embed;
   P.final_norm = (const uint16_t*)w->final_norm;
   P.lm_head = (const uint16_t*)w->lm_head;

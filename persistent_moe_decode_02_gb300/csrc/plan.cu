@@ -785,11 +785,11 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head)) return MK_ERR_INVALID;
   if (!w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->router || !w->w_gate_up || !w->w_down)
     return MK_ERR_INVALID;
-  if (!kv->k_pool || !kv->v_pool || kv->num_pages < 1) return MK_ERR_INVALID;
+  if (!kv->kv_pool || kv->num_pages < 1) return MK_ERR_INVALID;
   for (int l = 0; l < s.L; ++l) {
     if (!aligned16(w->attn_norm[l]) || !aligned16(w->wqkv[l]) || !aligned16(w->wo[l]) ||
         !aligned16(w->ffn_norm[l]) || !aligned16(w->router[l]) || !aligned16(w->w_gate_up[l]) ||
-        !aligned16(w->w_down[l]) || !aligned16(kv->k_pool[l]) || !aligned16(kv->v_pool[l]))
+        !aligned16(w->w_down[l]) || !aligned16(kv->kv_pool[l]))
       return MK_ERR_INVALID;
   }
   rc = validate_batch(s, batch, seq_lens, page_table, max_pages_per_seq, kv->num_pages, o.chunk_first);
@@ -864,7 +864,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   const size_t L = s.L;
   // weight pointer tables
   {
-    std::vector<const void*> tab(9 * L);
+    std::vector<const void*> tab(8 * L);
     for (size_t l = 0; l < L; ++l) {
       tab[0 * L + l] = w->attn_norm[l];
       tab[1 * L + l] = w->wqkv[l];
@@ -873,8 +873,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
       tab[4 * L + l] = w->router[l];
       tab[5 * L + l] = w->w_gate_up[l];
       tab[6 * L + l] = w->w_down[l];
-      tab[7 * L + l] = kv->k_pool[l];
-      tab[8 * L + l] = kv->v_pool[l];
+      tab[7 * L + l] = kv->kv_pool[l];
     }
     const void** d_tab = nullptr;
     if (dalloc(p, &d_tab, tab.size() * sizeof(void*)) != cudaSuccess) return fail(MK_ERR_CUDA);
@@ -887,8 +886,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
     P.router = (const uint16_t* const*)(d_tab + 4 * L);
     P.w_gate_up = (const uint16_t* const*)(d_tab + 5 * L);
     P.w_down = (const uint16_t* const*)(d_tab + 6 * L);
-    P.k_pool = (uint16_t* const*)(d_tab + 7 * L);
-    P.v_pool = (uint16_t* const*)(d_tab + 8 * L);
+    P.kv_pool = (uint16_t* const*)(d_tab + 7 * L);
     P.embed = (const uint16_t*)w->embed;
     P.final_norm = (const uint16_t*)w->final_norm;
     P.lm_head = (const uint16_t*)w->lm_head;

@@ -47,7 +47,7 @@ class MkWeights(ctypes.Structure):
 
 
 class MkKv(ctypes.Structure):
-    _fields_ = [("k_pool", _PP), ("v_pool", _PP), ("num_pages", ctypes.c_int)]
+    _fields_ = [("kv_pool", _PP), ("num_pages", ctypes.c_int)]
 
 
 class MkPlanOpts(ctypes.Structure):
@@ -158,26 +158,26 @@ def inspect_tasks(D, seq_lens: Sequence[int], num_ctas: int, split_pages: int = 
     return torch.tensor(list(buf), dtype=torch.int64).view(n, 12), list(cs)
 
 
-def _weight_structs(D, weights: dict, k_pools, v_pools):
+def _weight_structs(D, weights: dict, kv_pools):
     """ctypes views of the weight and KV pointers (the arrays must outlive the call)."""
     arrays = {k: _ptr_array(weights[k]) for k in
               ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down")}
-    kp, vp = _ptr_array(k_pools), _ptr_array(v_pools)
+    kvp = _ptr_array(kv_pools)
     cast = lambda a: ctypes.cast(a, _PP)
     w = MkWeights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr(),
                   *[cast(arrays[k]) for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up",
                                               "w_down")])
-    kv = MkKv(cast(kp), cast(vp), int(k_pools[0].shape[0]))
-    return w, kv, (arrays, kp, vp)
+    kv = MkKv(cast(kvp), int(kv_pools[0].shape[0]))
+    return w, kv, (arrays, kvp)
 
 
-def decode_step_noalloc(D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table, max_pages: int,
+def decode_step_noalloc(D, weights: dict, kv_pools, seq_lens: Sequence[int], page_table, max_pages: int,
                         tokens: torch.Tensor, next_token: torch.Tensor, logits: Optional[torch.Tensor] = None,
                         status: Optional[torch.Tensor] = None, stream=None) -> int:
     """One step through mk_decode_step_noalloc (no plan, no allocation inside
     the library).  Returns the enqueue status; the device status goes to
     `status` (int32[4] on the device) when given."""
-    w, kv, keep = _weight_structs(D, weights, k_pools, v_pools)
+    w, kv, keep = _weight_structs(D, weights, kv_pools)
     dims = dims_struct(D)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else 0)
     pt = [int(x) for x in page_table]
@@ -194,24 +194,24 @@ class Plan:
     weights: dict with 'embed', 'final_norm', 'lm_head' tensors and per-layer
     lists 'attn_norm', 'wqkv', 'wo', 'ffn_norm', 'router', 'w_gate_up',
     'w_down' (bf16 CUDA tensors in the layout of include/mk.h).
-    k_pools / v_pools: per-layer bf16 [num_pages, nkv, head_dim, page_size] (pages
-    stored transposed, slot fastest)."""
+    kv_pools: per-layer bf16 [num_pages, nkv, 2, head_dim, page_size] (per page
+    and KV head the K block, then the V block, each stored transposed, slot
+    fastest)."""
 
-    def __init__(self, D, weights: dict, k_pools, v_pools, seq_lens: Sequence[int], page_table,
+    def __init__(self, D, weights: dict, kv_pools, seq_lens: Sequence[int], page_table,
                  max_pages: int, timeout_us: int = 0, num_ctas: int = 0, max_batch: int = 0,
                  split_pages: int = 0, debug_drop_task: int = 0, trace: int = 0, tc_off: bool = False):
         self.D = D
-        self._keep = (weights, k_pools, v_pools)
+        self._keep = (weights, kv_pools)
         self._arrays = {k: _ptr_array(weights[k]) for k in
                         ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down")}
-        self._kp = _ptr_array(k_pools)
-        self._vp = _ptr_array(v_pools)
+        self._kvp = _ptr_array(kv_pools)
         cast = lambda a: ctypes.cast(a, _PP)
         self._w = MkWeights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
                             weights["lm_head"].data_ptr(), *[cast(self._arrays[k]) for k in
                                                              ("attn_norm", "wqkv", "wo", "ffn_norm", "router",
                                                               "w_gate_up", "w_down")])
-        self._kv = MkKv(cast(self._kp), cast(self._vp), int(k_pools[0].shape[0]))
+        self._kv = MkKv(cast(self._kvp), int(kv_pools[0].shape[0]))
         self._dims = dims_struct(D)
         opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, debug_drop_task, int(trace))
         opts.tc_off = int(bool(tc_off))
@@ -428,19 +428,19 @@ class Scheduler:
 
 class Server:
     """The serving loop: a Scheduler plus the plan it drives (created by the
-    first mk_serve_step).  k_pools / v_pools: the KV pool the scheduler's
-    pages index (every page of it is the scheduler's)."""
+    first mk_serve_step).  kv_pools: the KV pool the scheduler's pages index
+    (every page of it is the scheduler's)."""
 
-    def __init__(self, D, weights: dict, k_pools, v_pools, max_batch: int, max_pages: int, timeout_us: int = 0,
+    def __init__(self, D, weights: dict, kv_pools, max_batch: int, max_pages: int, timeout_us: int = 0,
                  num_ctas: int = 0, split_pages: int = 0, temperature: float = 0.0, seed: int = 0,
                  prefill: int = 8):
         self.D = D
-        self._keep = (weights, k_pools, v_pools)
-        self._w, self._kv, self._arrays = _weight_structs(D, weights, k_pools, v_pools)
+        self._keep = (weights, kv_pools)
+        self._w, self._kv, self._arrays = _weight_structs(D, weights, kv_pools)
         self._dims = dims_struct(D)
         self._opts = MkPlanOpts(timeout_us, num_ctas, max_batch, split_pages, 0, 0, float(temperature),
                                 int(seed) & (2 ** 64 - 1))
-        self.sched = Scheduler(int(k_pools[0].shape[0]), D.page_size, max_batch, max_pages)
+        self.sched = Scheduler(int(kv_pools[0].shape[0]), D.page_size, max_batch, max_pages)
         if prefill > 1:   # prompts enter the cache in chunks of up to `prefill` tokens per step
             self.sched.set_prefill(min(prefill, 8))
         self.plan = ctypes.c_void_p()

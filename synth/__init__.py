@@ -68,7 +68,7 @@ def _L():
                                        ctypes.c_int, ctypes.c_double, ctypes.c_void_p)
         lib.synth_fill_normal_bf16.argtypes = [vp, i64, u64, u32, i64, dbl, dbl, i32, vp]
         lib.synth_fill_uniform_int.argtypes = [vp, i64, u64, u32, i64, u32, i32, vp]
-        lib.synth_fill_kv_paged.argtypes = [vp, vp, i64, i32, i32, i32, u64, u32, dbl, i32, vp]
+        lib.synth_fill_kv_paged.argtypes = [vp, vp, i64, i32, i32, i32, i64, u64, u32, dbl, i32, vp]
         for f in (lib.synth_fill_normal_bf16, lib.synth_fill_uniform_int, lib.synth_fill_kv_paged):
             f.restype = ctypes.c_int
         _lib = lib
@@ -118,16 +118,19 @@ def fill_kv_paged_(pool: torch.Tensor, page_table: torch.Tensor, n_tok: int, see
                    name: str) -> None:
     """Write the first n_tok logical K (or V) rows of one request/layer into a
     paged pool [num_pages, nkv, d, page_size] (each page stores its block
-    transposed, one row per dimension) through its page table."""
-    assert pool.dtype == torch.bfloat16 and pool.is_contiguous() and pool.dim() == 4
-    assert page_table.dtype == torch.int32 and page_table.device == pool.device
+    transposed, one row per dimension) through its page table.  The pool may
+    be a view whose (page, head) blocks lie pool.stride(1) elements apart (the
+    K or V half of an interleaved pool); each block is contiguous."""
+    assert pool.dtype == torch.bfloat16 and pool.dim() == 4
     _, nkv, d, ps = pool.shape
+    assert pool.stride(3) == 1 and pool.stride(2) == ps and pool.stride(0) == nkv * pool.stride(1)
+    assert page_table.dtype == torch.int32 and page_table.device == pool.device
     need = (n_tok + ps - 1) // ps
     assert page_table.numel() >= need
     rc = _L().synth_fill_kv_paged(ctypes.c_void_p(pool.data_ptr()),
                                   ctypes.c_void_p(page_table.data_ptr()), n_tok, nkv, ps, d,
-                                  seed, stream_id(name), KV_SIGMA / _SD_IH4, int(pool.is_cuda),
-                                  _cuda_stream(pool))
+                                  pool.stride(1), seed, stream_id(name), KV_SIGMA / _SD_IH4,
+                                  int(pool.is_cuda), _cuda_stream(pool))
     if rc != 0:
         raise RuntimeError("synth_fill_kv_paged failed")
 

@@ -85,17 +85,20 @@ class Request:
 
 
 class PagedKV:
-    """Per-layer K and V page pools plus the host-side page bookkeeping of a
-    batch: which physical pages each request holds (seeded shuffled free list)."""
+    """Per-layer KV page pools plus the host-side page bookkeeping of a batch:
+    which physical pages each request holds (seeded shuffled free list).  A
+    pool is bf16 [num_pages, nkv, 2, head_dim, page_size] (per page and KV head
+    the K block, then the V block); k[l] and v[l] are views of its two halves."""
 
     def __init__(self, D: Dims, num_pages: int, max_pages: int, seed: int = 0, device: str = "cuda",
                  perm_salt: int = 0, poison: bool = False):
         self.D, self.seed, self.max_pages, self.num_pages = D, seed, max_pages, num_pages
-        shape = (num_pages, D.n_kv_heads, D.head_dim, D.page_size)   # pages hold [d, slot] blocks
-        self.k = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(D.n_layers)]
-        self.v = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(D.n_layers)]
+        shape = (num_pages, D.n_kv_heads, 2, D.head_dim, D.page_size)   # pages hold [d, slot] blocks
+        self.kv = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(D.n_layers)]
+        self.k = [t[:, :, 0] for t in self.kv]
+        self.v = [t[:, :, 1] for t in self.kv]
         if poison:   # NaN everywhere no token was written: unused slots must never matter
-            for t in self.k + self.v:
+            for t in self.kv:
                 t.fill_(float("nan"))
         self.free = [int(x) for x in page_permutation(num_pages, seed, perm_salt)]
         self._rng = np.random.Generator(np.random.PCG64([seed, 7]))

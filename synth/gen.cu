@@ -21,10 +21,12 @@ __global__ void k_fill_uniform(int32_t* out, int64_t n, syn_keys k, int64_t star
 }
 
 // Element (pos, g, e) of a request's logical [n_tok, nkv, d] cache goes to
-// pool[page_table[pos / ps]][g][e][pos % ps] (each page holds its head's
-// [d, page_size] block transposed: one row per dimension).
+// row e, slot pos % ps of block (page_table[pos / ps], g): each page holds its
+// head's [d, page_size] block transposed (one row per dimension), the blocks
+// `hs` elements apart (d * ps when the pool holds one kind, 2 * d * ps for
+// the K or V half of an interleaved pool).
 __global__ void k_fill_kv_paged(uint16_t* pool, const int32_t* page_table, int64_t n_tok, int nkv,
-                                int ps, int d, syn_keys k, double scale) {
+                                int ps, int d, int64_t hs, syn_keys k, double scale) {
   int64_t n = n_tok * nkv * d;
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -33,7 +35,7 @@ __global__ void k_fill_kv_paged(uint16_t* pool, const int32_t* page_table, int64
     int64_t g = (i / d) % nkv;
     int64_t pos = i / ((int64_t)d * nkv);
     int64_t page = page_table[pos / ps];
-    int64_t dst = ((page * nkv + g) * d + e) * ps + pos % ps;
+    int64_t dst = (page * nkv + g) * hs + e * ps + pos % ps;
     pool[dst] = syn_normal_bf16(k, (uint64_t)i, 0.0, scale);
   }
 }
@@ -78,17 +80,18 @@ int synth_fill_uniform_int(int32_t* out, int64_t n, uint64_t seed, uint32_t stre
 }
 
 // page_table: n_pages_used entries covering positions [0, n_tok); device pointer
-// when on_device, host pointer otherwise.  Pool layout [pages][nkv][d][page_size].
+// when on_device, host pointer otherwise.  Pool layout [pages][nkv][d][page_size]
+// with the (page, head) blocks head_stride elements apart.
 int synth_fill_kv_paged(void* pool, const int32_t* page_table, int64_t n_tok, int nkv, int page_size,
-                        int d, uint64_t seed, uint32_t stream, double scale, int on_device,
-                        void* cuda_stream) {
+                        int d, int64_t head_stride, uint64_t seed, uint32_t stream, double scale,
+                        int on_device, void* cuda_stream) {
   syn_keys k = syn_make_keys(seed, stream);
   uint16_t* p = (uint16_t*)pool;
   int64_t n = n_tok * nkv * d;
   if (n <= 0) return 0;
   if (on_device) {
     k_fill_kv_paged<<<grid_for(n), 256, 0, (cudaStream_t)cuda_stream>>>(p, page_table, n_tok, nkv,
-                                                                         page_size, d, k, scale);
+                                                                         page_size, d, head_stride, k, scale);
     return (int)cudaGetLastError();
   }
 #pragma omp parallel for schedule(static)
@@ -97,7 +100,7 @@ int synth_fill_kv_paged(void* pool, const int32_t* page_table, int64_t n_tok, in
     int64_t g = (i / d) % nkv;
     int64_t pos = i / ((int64_t)d * nkv);
     int64_t page = page_table[pos / page_size];
-    p[((page * nkv + g) * d + e) * page_size + pos % page_size] =
+    p[(page * nkv + g) * head_stride + e * page_size + pos % page_size] =
         syn_normal_bf16(k, (uint64_t)i, 0.0, scale);
   }
   return 0;

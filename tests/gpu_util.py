@@ -63,7 +63,7 @@ class GpuRun:
         self.reqs = [self.kv.admit(rid, c, self.steps + 1) for rid, c in zip(rids, wl.ctx)]
         self.next_rid = max(rids) + 1
         self.max_pages = max_pages
-        self.plan = mk.Plan(D, self.model.weights(), self.kv.k, self.kv.v, [r.length for r in self.reqs],
+        self.plan = mk.Plan(D, self.model.weights(), self.kv.kv, [r.length for r in self.reqs],
                             self.kv.page_table(self.reqs), max_pages, **plan_kw)
         self.tokens = torch.tensor(initial_tokens(wl, [r.rid for r in self.reqs]), dtype=torch.int32,
                                    device="cuda")

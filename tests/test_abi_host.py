@@ -226,7 +226,7 @@ def test_plan_create_rejects_unusable_temperatures(mk):
         shape = (64,)
 
     kp = [Pool(p.addr) for p in pools]
-    w, kv, keep = mk._weight_structs(D, weights, kp, kp)
+    w, kv, keep = mk._weight_structs(D, weights, kp)
     dims = mk.dims_struct(D)
     lens = mk._int_array([20])
     pt = mk._int_array(list(range(4)))

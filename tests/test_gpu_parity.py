@@ -206,13 +206,12 @@ def test_serving_loop_matches_oracle_greedy(max_batch, n_req, prefill):
     D = wl.dims
     model = DeviceModel(D, wl.seed)
     num_pages, max_pages = 3 * max_batch, 2
-    shape = (num_pages, D.n_kv_heads, D.head_dim, D.page_size)
-    k = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
-    v = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
+    shape = (num_pages, D.n_kv_heads, 2, D.head_dim, D.page_size)
+    kv = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
     rng = random.Random(11)
     reqs = [(100 + i, [rng.randrange(D.vocab) for _ in range(rng.randrange(1, 21))], rng.randrange(1, 7))
             for i in range(n_req)]
-    srv = mk.Server(D, model.weights(), k, v, max_batch=max_batch, max_pages=max_pages, prefill=prefill)
+    srv = mk.Server(D, model.weights(), kv, max_batch=max_batch, max_pages=max_pages, prefill=prefill)
     first = n_req // 2
     for rid, prompt, max_new in reqs[:first]:
         srv.submit(rid, prompt, max_new)
@@ -335,12 +334,11 @@ def test_serving_loop_sampling_is_reproducible():
     model = DeviceModel(D, wl.seed)
     rng = random.Random(3)
     reqs = [(i, [rng.randrange(D.vocab) for _ in range(rng.randrange(1, 12))], 8) for i in range(5)]
-    shape = (8, D.n_kv_heads, D.head_dim, D.page_size)
+    shape = (8, D.n_kv_heads, 2, D.head_dim, D.page_size)
 
     def serve(temperature, seed):
-        k = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
-        v = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
-        srv = mk.Server(D, model.weights(), k, v, max_batch=2, max_pages=2, temperature=temperature, seed=seed)
+        kv = [torch.zeros(shape, dtype=torch.bfloat16, device="cuda") for _ in range(D.n_layers)]
+        srv = mk.Server(D, model.weights(), kv, max_batch=2, max_pages=2, temperature=temperature, seed=seed)
         for rid, prompt, n in reqs:
             srv.submit(rid, prompt, n)
         srv.run(max_steps=200)
@@ -449,7 +447,7 @@ def test_prefill_chunk_rows_match_per_token_decode(capacity):
             owner.append(ri)
     B = len(seq)
     assert B <= capacity
-    plan = mk.Plan(D, model.weights(), kv.k, kv.v, [r.length for r in reqs], kv.page_table(reqs),
+    plan = mk.Plan(D, model.weights(), kv.kv, [r.length for r in reqs], kv.page_table(reqs),
                    kv.max_pages, split_pages=1, max_batch=capacity)
     plan.update_rows(seq, pt, kv.max_pages, cf)
     tok = torch.tensor(toks, dtype=torch.int32, device="cuda")

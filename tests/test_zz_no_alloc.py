@@ -40,7 +40,7 @@ def test_noalloc_matches_plan_step_on_two_calls(built, ctx):
     assert [r.pages for r in reqs_a] == [r.pages for r in reqs_b]
     pt = kv_a.page_table(reqs_a)
     lens = [r.length for r in reqs_a]
-    plan = mk.Plan(D, model.weights(), kv_a.k, kv_a.v, lens, pt, max_pages)
+    plan = mk.Plan(D, model.weights(), kv_a.kv, lens, pt, max_pages)
     tok_a = torch.tensor(initial_tokens(wl, list(range(wl.batch))), dtype=torch.int32, device="cuda")
     tok_b = tok_a.clone()
     B = wl.batch
@@ -52,7 +52,7 @@ def test_noalloc_matches_plan_step_on_two_calls(built, ctx):
         status = torch.full((4,), -99, dtype=torch.int32, device="cuda")
         assert plan.step(tok_a, nxt_a, lg_a) == mk.MK_OK
         assert plan.sync() == mk.MK_OK
-        rc = mk.decode_step_noalloc(D, model.weights(), kv_b.k, kv_b.v, lens, pt, max_pages, tok_b, nxt_b,
+        rc = mk.decode_step_noalloc(D, model.weights(), kv_b.kv, lens, pt, max_pages, tok_b, nxt_b,
                                     lg_b, status)
         assert rc == mk.MK_OK, mk.lib().mk_last_error()
         torch.cuda.synchronize()
@@ -74,12 +74,12 @@ def test_noalloc_rejects_oversized_step(built):
                   "lm_head": torch.zeros(8, device="cuda")}
     for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "router", "w_gate_up", "w_down"):
         model_like[k] = [torch.zeros(8, device="cuda")] * D.n_layers
-    pools = [torch.zeros(1 << 16, D.n_kv_heads, D.head_dim, D.page_size, dtype=torch.bfloat16, device="cuda")]
+    # only the pool's page count is read before the refusal: a 65,536-page stand-in
+    pools = [torch.zeros(1 << 16, 8, dtype=torch.bfloat16, device="cuda")]
     ctx = 600000
     pages = (ctx + D.page_size) // D.page_size
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = mk.decode_step_noalloc(D, model_like, pools * D.n_layers, pools * D.n_layers, [ctx],
-                                list(range(pages)), pages, tok, tok)
+    rc = mk.decode_step_noalloc(D, model_like, pools * D.n_layers, [ctx], list(range(pages)), pages, tok, tok)
     assert rc == mk.MK_ERR_CAPACITY
     msg = mk.lib().mk_last_error().decode()
     assert "bytes of scratch" in msg and str(64 << 20) in msg, msg
