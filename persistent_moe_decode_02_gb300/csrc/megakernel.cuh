@@ -1149,24 +1149,13 @@ struct Consumer {
   }
 
   // x_mid of layer l (after the O projection and residual), request b: four
-  // columns from i4 * 4, or column i; fp32 or fixed-point sums as qkv_at.
+  // columns from i4 * 4, or column i (fp32; on the tensor-core path the last
+  // O task of each 128-row tile converts the tile's fixed-point sums).
   __device__ __forceinline__ float4 xmid4(int l, int b, int i4) const {
-    const size_t off = ((size_t)l * p.bcap + b) * p.H + 4 * (size_t)i4;
-    if constexpr (NB == 8) {
-      if (p.xmid_fx) {
-        const ulonglong2 a = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off));
-        const ulonglong2 c = __ldcg(reinterpret_cast<const ulonglong2*>(p.xmid_fx + off) + 1);
-        return make_float4(from_fixed<true>(a.x), from_fixed<true>(a.y), from_fixed<true>(c.x), from_fixed<true>(c.y));
-      }
-    }
-    return __ldcg(reinterpret_cast<const float4*>(p.x_mid + off));
+    return __ldcg(reinterpret_cast<const float4*>(p.x_mid + ((size_t)l * p.bcap + b) * p.H) + i4);
   }
   __device__ __forceinline__ float xmid1(int l, int b, int i) const {
-    const size_t off = ((size_t)l * p.bcap + b) * p.H + i;
-    if constexpr (NB == 8) {
-      if (p.xmid_fx) return from_fixed<NB == 8>(__ldcg(p.xmid_fx + off));
-    }
-    return __ldcg(p.x_mid + off);
+    return __ldcg(p.x_mid + ((size_t)l * p.bcap + b) * p.H + i);
   }
 
   // dot of one 16-byte bf16 granule with 8 activations
@@ -2185,6 +2174,18 @@ struct Consumer {
         }
       }
       release_stage(ab);
+      // the tile's last task (a ticket over its t.a[6] tasks) turns its rows'
+      // sums into fp32 x_mid for the expert tiles and the reduce, and clears them
+      ab = cbar_or(ab);
+      if (!ab && ticket(p.cm.omt + l * p.cm.nomt + row0 / 128, (uint32_t)t.a[6], 1u)) {
+        unsigned long long* fx = p.xmid_fx + (size_t)l * p.bcap * p.H + row0;
+        float* xm = p.x_mid + (size_t)l * p.bcap * p.H + row0;
+        for (int i = ct; i < B * 128; i += NCT) {
+          const size_t off = (size_t)(i >> 7) * p.H + (i & 127);
+          xm[off] = from_fixed<NB == 8>(__ldcg(fx + off));
+          fx[off] = 0ull;
+        }
+      }
     }
     return ab;
   }
@@ -2460,9 +2461,6 @@ struct Consumer {
         float s = o == ct ? xres : xmid1(l, b, h);
         for (int c = 0; c < nch; ++c) s += rs[o * nch + c];
         xo[(size_t)b * H + h] = s;
-        if constexpr (NB == 8) {   // the last reader of the fixed-point x_mid: clear it for the next step
-          if (p.xmid_fx) p.xmid_fx[((size_t)l * p.bcap + b) * H + h] = 0ull;
-        }
       }
     }
     mark(TR_STAGES);

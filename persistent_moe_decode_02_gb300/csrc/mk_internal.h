@@ -63,10 +63,12 @@ static_assert(sizeof(Task) == 48, "task record is 48 bytes");
 // satisfied when counter >= epoch * cnt (epoch = 1, 2, ... since the last reset).
 struct CtrMap {
   int L, nkv, bcap;
-  int qkv, attn, combine, o, rdone, gu, down, lm, sdone, total;
+  int qkv, attn, combine, o, rdone, gu, down, lm, sdone, omt, nomt, total;
 
-  void init(int L_, int nkv_, int bcap_) {
-    L = L_; nkv = nkv_; bcap = bcap_;
+  // omt_: 128-row tiles of the O projection that count their tensor-core tasks
+  // (a ticket per tile: its last task converts the tile's x_mid rows)
+  void init(int L_, int nkv_, int bcap_, int omt_ = 0) {
+    L = L_; nkv = nkv_; bcap = bcap_; nomt = omt_;
     int c = 0;
     qkv = c; c += L * nkv;
     attn = c; c += L * bcap * nkv;
@@ -77,6 +79,7 @@ struct CtrMap {
     down = c; c += L;
     lm = c; c += 1;
     sdone = c; c += 1;   // a step's next tokens are written (one signal per step)
+    omt = c; c += L * omt_;
     total = c;
   }
 #if defined(__CUDACC__)
@@ -194,7 +197,8 @@ struct Params {
   const void* tm_qkv;
   const void* tm_o;
   unsigned long long* qkv_fx;    // [L][bcap][qkv_rows]; zeroed after use by the layer's O tiles
-  unsigned long long* xmid_fx;   // [L][bcap][H]; zeroed after use by the layer's reduce tasks
+  unsigned long long* xmid_fx;   // [L][bcap][H]; the last O task of each 128-row tile converts
+                                 // its rows to fp32 x_mid and zeroes them
 };
 
 // Expert gate/up on the tensor cores: a stage is a tile of 128 of an

@@ -160,7 +160,7 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
                 std::vector<int>& open_start, bool nucleus = false, bool tcp = false) {
   if (B < 1 || B > bcap || C < 1) return MK_ERR_INVALID;
   mk::CtrMap cm;
-  cm.init(s.L, s.nkv, bcap);
+  cm.init(s.L, s.nkv, bcap, s.H / 128);
   Assigner asg(C);
   const int Rg = (s.G + 2) * s.d;
   const int nqd = s.nq * s.d;
@@ -292,6 +292,7 @@ int build_tasks(const Shape& s, int B, int bcap, const int* seq_lens, int C, int
       t.a[3] = a;
       t.a[4] = b;
       t.a[5] = cnt.o;
+      t.a[6] = ko;   // tasks of this 128-row tile (its ticket's count)
       ph.push_back({(double)(b - a + 1) * 128 * 128 * 2, t});
     }
     for (int i = 0; !tcp && i < cnt.o; ++i) {
@@ -826,7 +827,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   p->seq.assign(seq_lens, seq_lens + batch);
   p->pt.assign(page_table, page_table + (size_t)batch * max_pages_per_seq);
   set_chunks(p, batch, o.chunk_first);
-  p->cm.init(s.L, s.nkv, bcap);
+  p->cm.init(s.L, s.nkv, bcap, s.H / 128);
   p->rm.init(std::min(s.E, bcap * s.k), bcap);
 
   auto fail = [&](int code) {
