@@ -657,7 +657,7 @@ def main():
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tc-off", action="store_true",
-                    help="expert gate/up and projections of batches 5-8 on the CUDA cores instead of the tensor cores")
+                    help="expert gate/up and projections of batches 3-8 on the CUDA cores instead of the tensor cores")
     ap.add_argument("--steps-per-launch", type=int, default=8,
                     help="also time this many decode steps per launch (tokens fed back on the device); 1: off")
     ap.add_argument("--timeline", default=None,

@@ -119,9 +119,11 @@ typedef struct mk_plan_opts {
   unsigned long long seed;
   float top_p;       /* nucleus sampling from the first step, as mk_plan_set_top_p; 0 -> 1 (off) */
   const int* chunk_first; /* prefill chunks of the first batch, as mk_plan_update_rows (host, nullable) */
-  int tc_off;        /* 1: the expert gate/up of batches 5-8 on the CUDA cores; 0 (default): on the
-                        tensor cores (tcgen05, TMEM accumulators, TMA tiles) when hidden is a multiple
-                        of 128 and expert_ffn of 64 */
+  int tc_off;        /* 1: plans of capacity 3-8 on the CUDA cores; 0 (default): a capacity of 3 to
+                        8 takes the batch-8 kernel instance, whose QKV and O projections and expert
+                        gate/up run on the tensor cores (tcgen05, TMEM accumulators, TMA tiles), when
+                        hidden, n_q_heads * head_dim and (G + 2) * head_dim are multiples of 128,
+                        expert_ffn of 64 and n_experts at most 128 */
 } mk_plan_opts;
 
 typedef struct mk_plan mk_plan;

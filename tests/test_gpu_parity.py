@@ -77,6 +77,22 @@ def test_paged_permutation_is_bit_identical():
         assert torch.equal(x.hidden, y.hidden)
 
 
+def test_capacity_bounds_updates_on_the_batch8_instance():
+    # a plan of capacity 3 runs on the batch-8 kernel instance (sized for 8
+    # requests), but its updates stay bounded by the capacity asked for
+    from persistent_moe_decode_02_gb300 import mk
+    wl = dataclasses.replace(synth.workload("tiny"), ctx=[40, 9, 70], steps=2)
+    run = GpuRun(wl, steps=2, max_batch=3)
+    assert run.plan.info()["tc_proj"] == 1
+    lens = [r.length for r in run.reqs]
+    pt = run.kv.page_table(run.reqs)
+    run.plan.update(lens, pt, run.max_pages)   # at the capacity
+    with pytest.raises(mk.MkError) as e:       # one row past it (refused before any other check)
+        run.plan.update(lens + lens[:1], pt + pt[:run.max_pages], run.max_pages)
+    assert e.value.code == mk.MK_ERR_CAPACITY
+    run.plan.close()
+
+
 def test_batch_equals_each_request_alone():
     wl = dataclasses.replace(synth.workload("tiny"), ctx=[128, 50, 77], steps=3)
     full = GpuRun(wl)
@@ -481,19 +497,21 @@ def test_prefill_chunk_rows_match_per_token_decode(capacity):
     plan.close()
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid"])
-def test_expert_gate_up_on_tensor_cores(name):
-    # Batches of 5 to 8 run the experts' gate/up and the QKV and O projections
+@pytest.mark.parametrize("name,n", [("tiny", 8), ("tiny", 5), ("tiny", 3), ("mid", 8)])
+def test_expert_gate_up_on_tensor_cores(name, n):
+    # Batches of 3 to 8 run the experts' gate/up and the QKV and O projections
     # on the tensor cores (tcgen05 MMAs from TMA tiles into TMEM; the
     # projections' 128-row tiles split over K and summed in fixed point): a
     # ragged batch of 8 against the oracle, and against the same steps on the
     # CUDA cores.  The tensor cores see each activation as bf16 hi + lo (16
     # significant bits, relative error about 2^-17 per element against fp32 on
     # the CUDA cores), so the two agree to 1e-3 in relative L2, the tokens and
-    # experts exactly.
+    # experts exactly.  Batches of 5 and 3 (plans of capacity 3 to 8 take the
+    # batch-8 instance) run with zero rows in every B operand.
     from persistent_moe_decode_02_gb300 import mk
     base = synth.workload(name)
     ctx = [128, 37, 95, 16, 1, 60, 77, 5] if name == "tiny" else [4096, 300, 1000, 17, 2500, 64, 999, 3000]
+    ctx = ctx[:n]
     wl = dataclasses.replace(base, ctx=ctx, steps=3)
     run = GpuRun(wl, steps=3)
     assert run.plan.info()["tc_gate_up"] == 1 and run.plan.info()["tc_proj"] == 1

@@ -22,8 +22,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("ctx", [[128, 45], [300, 17, 160]])
 def test_noalloc_matches_plan_step_on_two_calls(built, ctx):
-    # batch 2, and batch 3 (kernel capacity rounded up to 4) whose contexts
-    # split into several KV chunks per (request, group) with a combine each
+    # batch 2, and batch 3 whose contexts split into several KV chunks per
+    # (request, group) with a combine each (the plan runs batch 3 on the batch-8
+    # instance's tensor cores, the no-alloc step on the batch-4 instance's CUDA
+    # cores: the same tokens, logits within the parity tolerances)
     from persistent_moe_decode_02_gb300 import mk
     wl = dataclasses.replace(synth.workload("tiny"), ctx=ctx, steps=2)
     D = wl.dims
