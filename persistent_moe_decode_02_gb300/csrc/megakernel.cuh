@@ -128,9 +128,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, M = 128, N = 16.
+// Instruction descriptors, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = 16 or 32.
 constexpr uint32_t UMMA_IDESC_M128_N16 = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t)(16 >> 3) << 17 |
+                                         (uint32_t)(128 >> 4) << 24;
+constexpr uint32_t UMMA_IDESC_M128_N32 = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t)(32 >> 3) << 17 |
                                          (uint32_t)(128 >> 4) << 24;
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -397,8 +399,8 @@ struct Misc {
   int r_rank[MAX_UNION * MAX_BATCH];
   // the producer's copies of a layer's distinct experts, one per cursor
   RouteCache cp_route;
-  // tensor-core gate/up: accumulator-ready barrier (one commit per 64-unit
-  // tile), final-completion barrier, and the TMEM base address
+  // tensor-core gate/up: accumulator-ready barrier (one commit per 128-row
+  // tile or lone half), final-completion barrier, and the TMEM base address
   uint64_t acc_bar;
   uint64_t tc_fin;
   uint32_t tmem;
@@ -525,23 +527,31 @@ __device__ __forceinline__ long long gu_cut(int U, int F, const int* cnt, long l
 }
 
 // Whether expert tile t's gate/up runs on the tensor cores: the batch-8
-// instance with tensor maps, when the layer's 64-unit blocks, cut evenly
+// instance with tensor maps, when the layer's 32-unit halves, cut evenly
 // over the tiles, fit the coefficient scratch (the producer and the
 // consumers decide alike from the same routing).
 __device__ __forceinline__ bool tc_layer(const Params& p, const Task& t, int U) {
   if (!p.tm_gu) return false;
-  const long long T = (long long)U * p.F / TC_UNITS, n = t.a[1];
-  return (T + n - 1) / n * TC_UNITS <= p.cf_pairs;
+  const long long T = (long long)U * p.F / TC_HALF, n = t.a[1];
+  return (T + n - 1) / n * TC_HALF <= p.cf_pairs;
+}
+
+// Ring stages of a tensor-core gate/up range of nh halves: kst per pair of
+// halves (128-row tiles, 128 columns a stage), kst / 2 for a lone last half
+// (64 rows, 256 columns a stage).
+__device__ __forceinline__ int tc_gu_stages(const Params& p, int nh) {
+  const int kst = p.H / (64 * (p.stage_bytes / TC_BOX));
+  return (nh >> 1) * kst + (nh & 1) * (kst >> 1);
 }
 
 template <int NB>
 __device__ __forceinline__ void gu_range_w(const Params& p, const Task& t, int U, const int* cnt, long long& q0,
                                            long long& q1) {
   if constexpr (NB == 8) {
-    if (tc_layer(p, t, U)) {   // tensor-core gate/up: whole 64-unit blocks, evenly
-      const long long T = (long long)U * p.F / TC_UNITS, i = t.a[0], n = t.a[1];
-      q0 = T * i / n * TC_UNITS;
-      q1 = T * (i + 1) / n * TC_UNITS;
+    if (tc_layer(p, t, U)) {   // tensor-core gate/up: whole 32-unit halves, evenly
+      const long long T = (long long)U * p.F / TC_HALF, i = t.a[0], n = t.a[1];
+      q0 = T * i / n * TC_HALF;
+      q1 = T * (i + 1) / n * TC_HALF;
       return;
     }
   }
@@ -589,6 +599,7 @@ struct Geo {
   int cs, cu, cf;   // gate/up cursor: stage cs starts at unit cf of distinct expert cu
   int ws, wu, wf;   // down cursor, the same for down stage ws
   bool tc;          // gate/up stages are tensor-core tiles (128 rows x 64 columns per 16 KB)
+  int nh, tmt, tks, ty0, ty1;   // tensor-core cursor: halves, tile, its K stage, its halves' first rows
   // projection on the tensor cores: rows [r0, r0 + 128), nw stages of 128
   // columns from K stage ks0 (then, for O, the router stage)
   bool tcp;
@@ -667,12 +678,28 @@ struct Producer {
       nwd += (fb - fa + q.rpw - 1) / q.rpw;
     }
     q.tc = NB == 8 && tc_layer(p, t, U);
-    if (q.tc) ngu = (q.q1 - q.q0) / TC_UNITS * (p.H / (64 * (p.stage_bytes / TC_BOX)));   // 128-row tiles
+    if (q.tc) {
+      q.nh = (q.q1 - q.q0) / TC_HALF;
+      ngu = tc_gu_stages(p, q.nh);
+      if (q.nh > 0) tc_tile(q, 0);
+    }
     q.nst_gu = ngu;
     q.nst = ngu + nwd;
     q.cs = q.ws = 0;
     q.cu = q.wu = q.q0 / F;
     q.cf = q.wf = q.q0 - q.cu * F;
+  }
+
+  // The tensor-core cursor at tile mt of expert range q: K stage 0 and the
+  // first gate/up row of each of its halves (a lone last half: both its own).
+  __device__ void tc_tile(Geo& q, int mt) const {
+    q.tmt = mt;
+    q.tks = 0;
+    const int F = p.F;
+    const int a0 = q.q0 + 2 * mt * TC_HALF, u0 = a0 / F;
+    q.ty0 = q.rc->exp[u0] * 2 * F + 2 * (a0 - u0 * F);
+    const int a1 = a0 + (2 * mt + 1 < q.nh ? TC_HALF : 0), u1 = a1 / F;
+    q.ty1 = q.rc->exp[u1] * 2 * F + 2 * (a1 - u1 * F);
   }
 
   // Geometry of task t; false on a routing wait that timed out or gave up,
@@ -891,14 +918,20 @@ struct Producer {
         uint8_t* dst = r.base + (size_t)r.stage * r.sb;
         m->armed[r.stage] = r.round;
         if (NB == 8 && q.type == T_MOE && q.tc && s < q.nst_gu) {
-          // tensor-core gate/up tile: 128 interleaved gate/up rows (64 units of
-          // one expert) x 64 columns per 16 KB box of the stage
-          const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox), mt = s / kst, ks = s - mt * kst;
-          const int qa = q.q0 + mt * TC_UNITS, u = qa / p.F, f = qa - u * p.F;
-          const int y = q.rc->exp[u] * 2 * p.F + 2 * f;
+          // tensor-core gate/up: per 16 KB box of the stage, two 64-row copies
+          // (64 interleaved gate/up rows, 32 units of one expert, by 64
+          // columns).  A pair of halves: each half's rows at K box ks * nbox + h.
+          // A lone last half: its rows at K boxes 2 (ks * nbox + h) and the next.
+          const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox);
+          const bool lone = 2 * q.tmt + 1 == q.nh;
           const void* tm = reinterpret_cast<const uint8_t*>(p.tm_gu) + (size_t)q.l * 128;
           mbar_expect_tx_only(bar, (uint32_t)nbox * TC_BOX);
-          for (int h = 0; h < nbox; ++h) tma_g2s_2d(dst + h * TC_BOX, tm, (ks * nbox + h) * 64, y, bar, pol);
+          for (int h = 0; h < nbox; ++h) {
+            const int x = lone ? 2 * (q.tks * nbox + h) : q.tks * nbox + h;
+            tma_g2s_2d(dst + h * TC_BOX, tm, x * 64, q.ty0, bar, pol);
+            tma_g2s_2d(dst + h * TC_BOX + TC_BOX / 2, tm, (x + (lone ? 1 : 0)) * 64, q.ty1, bar, pol);
+          }
+          if (++q.tks == (lone ? kst >> 1 : kst) && 2 * (q.tmt + 1) < q.nh) tc_tile(q, q.tmt + 1);
         } else if (NB == 8 && q.tcp) {
           if (s < q.nw) {
             // projection tile: 128 rows x 128 columns (two 64-column boxes) of K stage ks0 + s
@@ -2191,36 +2224,44 @@ struct Consumer {
   }
 
   // The gate/up part of an expert tile on the tensor cores (batch instance 8):
-  // units [q0, q1) are whole 64-unit blocks.  Per block, 128 gate/up rows x
-  // H columns stream through the ring as 128 x 128 tiles; one thread issues
-  // M = 128, N = 16, K = 16 MMAs (A: the weight tile, B: the batch's
-  // activations as bf16 hi + lo rows) accumulating in TMEM, and commits each
-  // stage's release to the ring's empty barrier.  Warps 0-3 then read the
-  // accumulator (one TMEM lane per row), add the hi and lo columns of each
-  // request, pair gate and up rows and write the SwiGLU coefficients of the
-  // expert's token slots, as the CUDA-core epilogue does.
+  // units [q0, q1) are whole 32-unit halves.  Two halves make a 128-row tile
+  // (half hh in rows 64 hh ..) that streams through the ring as 128 x 128
+  // stages; one thread issues M = 128, N = 16, K = 16 MMAs (A: the weight
+  // tile, B: the batch's activations as bf16 hi + lo rows) accumulating in
+  // TMEM, and commits each stage's release to the ring's empty barrier.  A
+  // lone last half streams 64 x 256 stages, its rows of K box c above those of
+  // box c + 1; an N = 32 MMA from B box c reads box c + 1 as B rows 16-31, so
+  // TMEM holds the box-c partials in lanes 0-63, columns 0-15, and the box c + 1
+  // partials in lanes 64-127, columns 16-31, added in the epilogue.  Warps 0-3
+  // then read the accumulator (one TMEM lane per row), add the hi and lo
+  // columns of each request, pair gate and up rows and write the SwiGLU
+  // coefficients of the expert's token slots, as the CUDA-core epilogue does.
   uint32_t acc_ph = 0;
   __device__ bool gu_tc(int q0, int q1, bool ab, float* cf) {
     const int F = p.F, k = p.k, bc = p.rm.bcap;
-    const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox), nmt = (q1 - q0) / TC_UNITS;
+    const int nbox = p.stage_bytes / TC_BOX, kst = p.H / (64 * nbox), nh = (q1 - q0) / TC_HALF;
+    const int nfull = nh >> 1, nmt = nfull + (nh & 1);
     const uint32_t bsm = smem_u32(act), tmem = m->tmem;
+    float* xs = psum;   // the lone half's lanes 64-127, [column][row], between the warps
     for (int mt = 0; mt < nmt; ++mt) {
-      const int qa = q0 + mt * TC_UNITS, u = qa / F, f0 = qa - u * F;
-      for (int ks = 0; ks < kst; ++ks) {
+      const bool lone = mt == nfull;
+      const int ksn = lone ? kst >> 1 : kst;
+      for (int ks = 0; ks < ksn; ++ks) {
         const uint8_t* st = wait_stage(ab);
         if (cw == 0) {
           if (lane == 0) {
             if (st) {
               tc_fence_after();
               const uint32_t sa = smem_u32(st);
-              for (int h = 0; h < nbox; ++h)
+              for (int h = 0; h < nbox; ++h) {
+                const uint32_t bb = bsm + (lone ? 2 * (nbox * ks + h) : nbox * ks + h) * 2048;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  umma_f16(tmem, umma_desc_sw128(sa + h * TC_BOX + kk * 32),
-                           umma_desc_sw128(bsm + (nbox * ks + h) * 2048 + kk * 32), UMMA_IDESC_M128_N16,
-                           (ks | h | kk) != 0);
+                  umma_f16(tmem, umma_desc_sw128(sa + h * TC_BOX + kk * 32), umma_desc_sw128(bb + kk * 32),
+                           lone ? UMMA_IDESC_M128_N32 : UMMA_IDESC_M128_N16, (ks | h | kk) != 0);
+              }
               umma_commit(&m->empty[r.stage]);   // the stage is free once its MMAs are done
-              if (ks == kst - 1) umma_commit(&m->acc_bar);
+              if (ks == ksn - 1) umma_commit(&m->acc_bar);
             } else {
               mbar_arrive(&m->empty[r.stage]);
             }
@@ -2233,18 +2274,35 @@ struct Consumer {
         }
       }
       ab = cbar_or(ab);
-      if (!ab && cw < 4) {
+      if (lone) {
+        if (!ab && (cw == 2 || cw == 3)) {
+          if (!mbar_wait(p, m, &m->acc_bar, acc_ph, -6)) ab = true;
+          tc_fence_after();
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(cw * 32) << 16) + 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xs[i * 64 + (cw - 2) * 32 + lane] = v[i];
+        }
+        ab = cbar_or(ab);
+      }
+      if (!ab && cw < (lone ? 2 : 4)) {
         if (!mbar_wait(p, m, &m->acc_bar, acc_ph, -6)) ab = true;
         tc_fence_after();
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(cw * 32) << 16), v);
+        if (lone) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += xs[i * 64 + cw * 32 + lane];
+        }
         float gsum[8], usum[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) gsum[j] = v[j] + v[8 + j];   // hi + lo of request j
 #pragma unroll
         for (int j = 0; j < 8; ++j) usum[j] = __shfl_down_sync(FULL, gsum[j], 1);   // the up row below
+        // this lane's row: half 2 mt + cw / 2 of the range (the lone half: rows 0-63)
+        const int qa = q0 + (2 * mt + (cw >> 1)) * TC_HALF, u = qa / F;
         if (!ab && (lane & 1) == 0) {
-          const int f = f0 + ((cw * 32 + lane) >> 1);
+          const int f = qa - u * F + (((cw & 1) * 32 + lane) >> 1);
           const int nt = m->r_cnt[u];
           const int* toks = m->r_tok + u * bc;
           const int* ranks = m->r_rank + u * bc;
@@ -2264,7 +2322,7 @@ struct Consumer {
       }
       acc_ph ^= 1;
       tc_fence_before();
-      ab = cbar_or(ab);   // the accumulator is read before the next block's MMAs overwrite it
+      ab = cbar_or(ab);   // the accumulator is read before the next tile's MMAs overwrite it
     }
     return ab;
   }

@@ -201,13 +201,14 @@ struct Params {
                                  // its rows to fp32 x_mid and zeroes them
 };
 
-// Expert gate/up on the tensor cores: a stage is a tile of 128 of an
-// expert's interleaved gate/up rows (64 ffn units) by 64 columns per 16 KB of
-// stage (one or two 64-column boxes); an expert tile's range is a run of whole
-// 64-unit blocks.
-constexpr int TC_UNITS = 64;     // ffn units (gate + up row pairs) per tensor-core tile
+// Expert gate/up on the tensor cores: an expert tile's range is a run of whole
+// 32-unit halves (64 interleaved gate/up rows of one expert each).  Two halves
+// make one 128-row tile, streamed as 128 rows x 64 columns per 16 KB of stage
+// (one or two 64-column boxes, each two 64-row copies); a lone last half
+// streams its 64 rows x 128 columns per 16 KB instead (two K boxes stacked).
+constexpr int TC_HALF = 32;      // ffn units per half tile: the unit of the tiles' cut
 constexpr int TC_BOX = 16384;    // bytes of one 128-row x 64-column box
-inline bool tc_moe_shape(int H, int F) { return H % 128 == 0 && F % TC_UNITS == 0; }
+inline bool tc_moe_shape(int H, int F) { return H % 256 == 0 && F % TC_HALF == 0; }
 // The projections on the tensor cores: 128-row tiles that never straddle a KV
 // group's rows, 128-column K stages, and an O tile's router rows ([128][E]
 // bf16) in one stage.  TC_PROJ_UNITS bounds a task's K stages (their B operand

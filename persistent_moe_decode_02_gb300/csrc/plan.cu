@@ -747,7 +747,10 @@ static void set_chunks(mk_plan* p, int batch, const int* chunk_first) {
 // swizzle.  Uploaded to `dst` (device, L x 128 bytes).  False when the
 // driver's encoder is unavailable or refuses a map: the CUDA cores then take
 // the work.
-static bool encode_maps(const Shape& s, const void* const* mats, long long rows, long long cols, void* dst) {
+// One 2-D tensor map per layer over a [rows][cols] bf16 matrix: boxes of 64
+// columns (128 bytes, swizzled) by box_rows rows.
+static bool encode_maps(const Shape& s, const void* const* mats, long long rows, long long cols, int box_rows,
+                        void* dst) {
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -757,7 +760,7 @@ static bool encode_maps(const Shape& s, const void* const* mats, long long rows,
   std::vector<CUtensorMap> maps((size_t)s.L);
   const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t gstr[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   for (int l = 0; l < s.L; ++l) {
     if (enc(&maps[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(mats[l]), gdim, gstr, box, es,
@@ -909,10 +912,10 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   P.tm_gu = P.tm_qkv = P.tm_o = nullptr;
   P.qkv_fx = P.xmid_fx = nullptr;
   if (p->nb == 8 && mk::tc_moe_shape(s.H, s.F) && !o.tc_off && p->stage_bytes % mk::TC_BOX == 0 &&
-      s.H % (64 * (p->stage_bytes / mk::TC_BOX)) == 0 && (long long)p->act_floats * 4 >= 32LL * s.H) {
+      s.H % (128 * (p->stage_bytes / mk::TC_BOX)) == 0 && (long long)p->act_floats * 4 >= 32LL * s.H) {
     void* maps = nullptr;
     if (dalloc(p, (uint8_t**)&maps, L * sizeof(CUtensorMap)) != cudaSuccess) return fail(MK_ERR_CUDA);
-    if (encode_maps(s, (const void* const*)w->w_gate_up, (long long)s.E * 2 * s.F, s.H, maps)) P.tm_gu = maps;
+    if (encode_maps(s, (const void* const*)w->w_gate_up, (long long)s.E * 2 * s.F, s.H, 64, maps)) P.tm_gu = maps;
   }
   // and the QKV and O projections: B operand slots of a task's K stages (4 KB
   // each) in the activation region
@@ -926,8 +929,8 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
         dalloc(p, &P.qkv_fx, L * bcap * s.qkv_rows * sizeof(unsigned long long)) != cudaSuccess ||
         dalloc(p, &P.xmid_fx, L * bcap * s.H * sizeof(unsigned long long)) != cudaSuccess)
       return fail(MK_ERR_CUDA);
-    if (encode_maps(s, (const void* const*)w->wqkv, s.qkv_rows, s.H, mq) &&
-        encode_maps(s, (const void* const*)w->wo, s.H, (long long)s.nq * s.d, mo)) {
+    if (encode_maps(s, (const void* const*)w->wqkv, s.qkv_rows, s.H, 128, mq) &&
+        encode_maps(s, (const void* const*)w->wo, s.H, (long long)s.nq * s.d, 128, mo)) {
       P.tm_qkv = mq;
       P.tm_o = mo;
     }
