@@ -1738,11 +1738,51 @@ struct Consumer {
     return ab;
   }
 
+  // Order-preserving key of a router logit (never NaN here: moe_act stores
+  // NaN as -inf): a larger logit has a larger key, equal logits equal keys,
+  // and 0 is below them all.
+  __device__ __forceinline__ static uint32_t rkey(float v) {
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);   // -0 and +0 compare equal
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+
+  // The top-k of request b's logits (m->rl), by the calling warp: k rounds,
+  // each taking the largest logit left, the lowest index on ties, so pick i
+  // is the logit of rank i (how many logits are greater, or equal with a
+  // lower index).  Lane i < k returns pick i (expert and logit).
+  __device__ __forceinline__ void route_pick(int b, int& e_out, float& v_out) const {
+    const int E = p.E, k = p.k;
+    const float* row = m->rl + b * E;
+    constexpr int EPL = MAX_EXPERTS / 32;   // logits per lane: expert lane + 32 j
+    uint32_t key[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) key[j] = lane + 32 * j < E ? rkey(row[lane + 32 * j]) : 0u;
+    e_out = 0;
+    v_out = 0.f;
+    for (int r = 0; r < k; ++r) {
+      uint32_t bk = 0;
+      int bj = 0;
+#pragma unroll
+      for (int j = EPL - 1; j >= 0; --j)   // this lane's largest key, its lowest j on ties
+        if (key[j] >= bk) {
+          bk = key[j];
+          bj = j;
+        }
+      const uint32_t top = __reduce_max_sync(FULL, bk);
+      const int e = (int)__reduce_min_sync(FULL, bk == top ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (e == lane + 32 * j) key[j] = 0u;   // taken
+      if (lane == r) {
+        e_out = e;
+        v_out = row[e];
+      }
+    }
+  }
+
   // Routing of layer l from its router logits (m->rl), computed in every
   // gate/up task the same way, so every CTA gets the same bits:
-  //  - per request, each expert's rank: how many logits are greater, or equal
-  //    with a lower index (NaN counts as -inf), so ranks are a permutation;
-  //    the top-k are the ranks below k, in rank order;
+  //  - per request, the top-k by route_pick, in rank order;
   //  - gates: softmax over the selected logits;
   //  - the distinct experts in ascending order, with their (request, rank)
   //    pairs in request order (r_U, r_exp, r_cnt, r_tok, r_rank).
@@ -1754,55 +1794,27 @@ struct Consumer {
   __device__ void route_local(int l, bool publish) {
     const int E = p.E, k = p.k, B = p.B;
     const int umax = p.rm.umax, bc = p.rm.bcap;
-    // ranks: two threads per candidate when they fit, each counting half the row
-    const int split = 2 * B * E <= NCT ? 2 : 1;
-    const int per = NCT / split;
-    for (int c0 = 0; c0 < B * E; c0 += per) {
-      const int c = c0 + ct / split, half = ct & (split - 1);
-      const bool valid = c < B * E;
-      const int b = valid ? c / E : 0, e = valid ? c - b * E : 0;
-      const float* row = m->rl + b * E;
-      const float v = row[e];
-      const int e_lo = split == 2 ? half * (E >> 1) : 0, e_hi = split == 2 ? (half ? E : E >> 1) : E;
-      // four independent counts over float4 loads when every half-row starts
-      // 16-byte aligned (E a multiple of 8), else one at a time
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-      int e2 = e_lo;
-      const int vec_hi = (E & 7) == 0 ? e_hi : e_lo;
-#pragma unroll 8
-      for (; e2 + 4 <= vec_hi; e2 += 4) {   // branch-free: (w > v) | (w == v & index < e)
-        const float4 w = *reinterpret_cast<const float4*>(row + e2);
-        r0 += (w.x > v) | ((w.x == v) & (e2 < e));
-        r1 += (w.y > v) | ((w.y == v) & (e2 + 1 < e));
-        r2 += (w.z > v) | ((w.z == v) & (e2 + 2 < e));
-        r3 += (w.w > v) | ((w.w == v) & (e2 + 3 < e));
-      }
-      for (; e2 < e_hi; ++e2) r0 += (row[e2] > v) || (row[e2] == v && e2 < e);
-      int rank = (r0 + r1) + (r2 + r3);
-      if (split == 2) rank += __shfl_xor_sync(FULL, rank, 1);
-      if (valid && half == 0 && rank < k) {
-        m->sel[b * k + rank] = e;
-        m->selv[b * k + rank] = v;
-        atomicAdd(&m->cnt_of[e], 1);
-      }
-    }
-    cbar();
     if (B == 1) {
-      // one request: its k experts are distinct.  Warp 0 holds them in lanes
-      // 0 .. k-1: the gates (softmax over the selected; the butterfly over all
-      // 32 lanes adds only zeros past k), and each expert's place in ascending
-      // id order gives the distinct-expert table, one token slot each.
+      // one request: warp 0 alone.  Its k experts are distinct: the gates
+      // (softmax over the picks; the butterfly over all 32 lanes adds only
+      // zeros past k), and each pick's place in ascending id order gives the
+      // distinct-expert table, one token slot each, handed to the producer
+      // before the other warps hear of it.
       if (cw == 0) {
+        int e;
+        float v;
+        route_pick(0, e, v);
         const bool on = lane < k;
-        const int e = on ? m->sel[lane] : 0;
-        const float v = on ? m->selv[lane] : 0.f;
-        const float ex = on ? expf(v - m->selv[0]) : 0.f;
+        const float v0 = __shfl_sync(FULL, v, 0);   // every lane: the shuffle is warp-wide
+        const float ex = on ? expf(v - v0) : 0.f;
         float tot = ex;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
         int pos = 0;
-        for (int j = 0; j < k; ++j) pos += m->sel[j] < e;
+        for (int j = 0; j < k; ++j) pos += __shfl_sync(FULL, e, j) < e;
         if (on) {
+          m->sel[lane] = e;
+          m->selv[lane] = v;
           m->gate[lane] = ex / tot;
           m->r_exp[pos] = e;
           m->r_cnt[pos] = 1;
@@ -1810,25 +1822,30 @@ struct Consumer {
           m->r_rank[pos * bc] = lane;
         }
         if (lane == 0) m->r_U = k;
+        __syncwarp();
+        if (lane == 0) st_release_cta(&m->r_layer, step * p.L + l);
       }
       cbar();
-      if (ct == 0) st_release_cta(&m->r_layer, step * p.L + l);
     } else {
-      // gates: request b's k selected logits sit in lanes of warp 1 + b / (32 / k_pow2)
-      // groups of kp consecutive lanes (kp = k rounded up to a power of two)
-      {
-        int kp = 1;
-        while (kp < k) kp <<= 1;
-        const int per_warp = 32 / kp;
-        const int b = (cw - 1) * per_warp + lane / kp, j = lane % kp;
-        const bool mine = cw >= 1 && b < B;             // uniform per warp but for the tail
-        const bool act_j = mine && j < k;
-        const float first = mine ? m->selv[b * k] : 0.f;
-        const float ex = act_j ? expf(m->selv[b * k + j] - first) : 0.f;
+      // warp w picks request w's experts and gates (butterfly sum as above)
+      for (int b = cw; b < B; b += NCW) {
+        int e;
+        float v;
+        route_pick(b, e, v);
+        const bool on = lane < k;
+        const float v0 = __shfl_sync(FULL, v, 0);   // every lane: the shuffle is warp-wide
+        const float ex = on ? expf(v - v0) : 0.f;
         float tot = ex;
-        for (int o = 1; o < kp; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
-        if (act_j) m->gate[b * k + j] = ex / tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        if (on) {
+          m->sel[b * k + lane] = e;
+          m->selv[b * k + lane] = v;
+          m->gate[b * k + lane] = ex / tot;
+          atomicAdd(&m->cnt_of[e], 1);
+        }
       }
+      cbar();
       if (cw == 0) {
         int base = 0;
         for (int c = 0; c < (E + 31) / 32; ++c) {
@@ -2331,10 +2348,16 @@ struct Consumer {
     const int l = t.layer, H = p.H, F = p.F, k = p.k, bc = p.rm.bcap;
     int U = 0;
     if (!ab) {
+      // Whether this task routes: read before the barrier below, while no
+      // thread can have routed this layer yet, so every consumer thread
+      // decides alike (batch-1 routing publishes the layer from warp 0
+      // before any barrier, and a thread that skipped route_local would
+      // meet its barriers out of step).
+      const bool route = m->r_layer != step * p.L + l || t.a[0] == 0;
       moe_act(l);
       cbar();
       mark(TR_MID1);
-      if (m->r_layer != step * p.L + l || t.a[0] == 0) route_local(l, t.a[0] == 0);
+      if (route) route_local(l, t.a[0] == 0);
       mark(TR_MID2);
       U = m->r_U;
     }
