@@ -1018,6 +1018,8 @@ struct ProjGemv {
 
 template <int NB, bool NUC>
 struct Consumer {
+  // copies of the router-logit sums this instance adds to, reads and clears
+  static constexpr int RLC = NB == 8 ? RL_COPIES_B8 : RL_COPIES;
   const Params& p;
   Ring r;
   float* act;
@@ -1717,8 +1719,8 @@ struct Consumer {
     if (st) {
       const uint16_t* wr = reinterpret_cast<const uint16_t*>(st);
       const uint16_t* gw = reinterpret_cast<const uint16_t*>(st + router_stage_gain_off(nr, E)) + (r0 & 7);
-      // copy t % RL_COPIES of the sums: eight times fewer tiles contend for each address
-      unsigned long long* out = p.rlsum + ((size_t)t.layer * RL_COPIES + t.a[2] % RL_COPIES) * p.bcap * E;
+      // copy t % RLC of the sums: RLC times fewer tiles contend for each address
+      unsigned long long* out = p.rlsum + ((size_t)t.layer * RL_COPIES + t.a[2] % RLC) * p.bcap * E;
       // two neighbouring threads per (b, e), each half the rows, then one shuffle
       const int n2 = 2 * p.B * E, hr = (nr + 1) >> 1;
       for (int x0 = 0; x0 < n2; x0 += NCT) {
@@ -1905,17 +1907,17 @@ struct Consumer {
     const size_t cs = (size_t)p.bcap * E;   // one copy of the sums
     const unsigned long long* rs = p.rlsum + (size_t)l * RL_COPIES * cs;
     auto load_sum = [&](int i) {   // the copies' integer sum: exact in any order
-      unsigned long long v[RL_COPIES];
+      unsigned long long v[RLC];
 #pragma unroll
-      for (int c = 0; c < RL_COPIES; ++c) v[c] = __ldcg(rs + c * cs + i);
+      for (int c = 0; c < RLC; ++c) v[c] = __ldcg(rs + c * cs + i);
       unsigned long long q = 0;
 #pragma unroll
-      for (int c = 0; c < RL_COPIES; ++c) q += v[c];
+      for (int c = 0; c < RLC; ++c) q += v[c];
       return q;
     };
-    unsigned long long v0[RL_COPIES];   // this thread's first sum: its loads go out now, the adds come later
+    unsigned long long v0[RLC];   // this thread's first sum: its loads go out now, the adds come later
 #pragma unroll
-    for (int c = 0; c < RL_COPIES; ++c) v0[c] = ct < BE ? __ldcg(rs + c * cs + ct) : 0ull;
+    for (int c = 0; c < RLC; ++c) v0[c] = ct < BE ? __ldcg(rs + c * cs + ct) : 0ull;
     const uint2* gam = reinterpret_cast<const uint2*>(p.ffn_norm[l]);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 x0[2];
@@ -1989,7 +1991,7 @@ struct Consumer {
     cbar();
     unsigned long long q0 = 0;
 #pragma unroll
-    for (int c = 0; c < RL_COPIES; ++c) q0 += v0[c];
+    for (int c = 0; c < RLC; ++c) q0 += v0[c];
     if constexpr (NB == 1) {
       // one request: every thread forms the scale itself (the same sum in the
       // same order, so the same bits); the routing's barrier orders m->inv[0]
@@ -2017,15 +2019,15 @@ struct Consumer {
       // the rest two sums at a time, both sets of loads in flight together
       for (int i = ct + NCT; i < BE; i += 2 * NCT) {
         const int i2 = i + NCT;
-        unsigned long long a[RL_COPIES], c2[RL_COPIES];
+        unsigned long long a[RLC], c2[RLC];
 #pragma unroll
-        for (int c = 0; c < RL_COPIES; ++c) {
+        for (int c = 0; c < RLC; ++c) {
           a[c] = __ldcg(rs + c * cs + i);
           c2[c] = i2 < BE ? __ldcg(rs + c * cs + i2) : 0ull;
         }
         unsigned long long qa = 0, qb = 0;
 #pragma unroll
-        for (int c = 0; c < RL_COPIES; ++c) {
+        for (int c = 0; c < RLC; ++c) {
           qa += a[c];
           qb += c2[c];
         }
@@ -2202,7 +2204,7 @@ struct Consumer {
         // router share: thread (request half bh, expert e) over the tile's 128 rows
         const uint16_t* wr = reinterpret_cast<const uint16_t*>(rst);
         const int E = p.E;
-        unsigned long long* out = p.rlsum + ((size_t)l * RL_COPIES + t.a[2] % RL_COPIES) * p.bcap * E;
+        unsigned long long* out = p.rlsum + ((size_t)l * RL_COPIES + t.a[2] % RLC) * p.bcap * E;
         for (int x = ct; x < 2 * E; x += NCT) {
           const int bh = x / E, e = x - bh * E;
           if (4 * bh < B) {
@@ -2507,8 +2509,8 @@ struct Consumer {
     float* rs = act;                                   // [output][chunk] sums
     mark(TR_ACT);
     if (!ab) {   // every expert tile of the layer has read the router sums: zero this task's share
-      const long long n = (long long)RL_COPIES * p.bcap * p.E;
-      unsigned long long* rs = p.rlsum + (size_t)l * n;
+      const long long n = (long long)RLC * p.bcap * p.E;   // the copies in use, at the front
+      unsigned long long* rs = p.rlsum + (size_t)l * RL_COPIES * p.bcap * p.E;
       for (long long i = r0 * n / H + ct; i < (long long)t.a[1] * n / H; i += NCT) rs[i] = 0ull;
     }
     // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)

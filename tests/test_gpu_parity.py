@@ -529,3 +529,39 @@ def test_expert_gate_up_on_tensor_cores(name, n):
         assert rel_l2(ra.logits, rb.logits.double()) < 1e-3
     a.plan.close()
     b.plan.close()
+
+
+def _host_topk(row: torch.Tensor, k: int) -> list:
+    # the top-k by value, the lower expert index first on exact ties
+    return sorted(range(row.numel()), key=lambda e: (-float(row[e]), e))[:k]
+
+
+@pytest.mark.parametrize("n", [1, 8])
+def test_router_exact_ties_take_the_lower_index(n):
+    # Exact router ties through the kernel.  Layer 0's router is all zeros,
+    # so every logit is exactly 0 and the picks must be experts 0 .. k-1 in
+    # that order; layer 1's router column 2j + 1 is a copy of column 2j, so
+    # each pair's logits are bit-identical (the O tiles' fixed-point shares
+    # are computed alike) and the even expert must come first.  Every layer's
+    # picks must equal the top-k of the kernel's own logits (value, then the
+    # lower index).  Batch 1 and a ragged batch of 8 take the two routing
+    # paths (and, at 8, the tensor-core instance).
+    from synth.device import DeviceModel
+    base = synth.workload("tiny")
+    ctx = [128, 37, 95, 16, 1, 60, 77, 5][:n]
+    wl = dataclasses.replace(base, ctx=ctx, steps=3)
+    D = wl.dims
+    model = DeviceModel(D, wl.seed)
+    model.router[0].zero_()
+    model.router[1][:, 1::2].copy_(model.router[1][:, 0::2])
+    run = GpuRun(wl, steps=3, model=model)
+    k, E = D.top_k, D.n_experts
+    for _ in range(3):
+        rec = run.step()
+        for b in range(n):
+            assert torch.equal(rec.rlog[b, 0], torch.zeros(E)), rec.rlog[b, 0]
+            assert rec.ids[b, 0].tolist() == list(range(k))
+            assert torch.equal(rec.rlog[b, 1, 0::2], rec.rlog[b, 1, 1::2])
+            for l in range(D.n_layers):
+                assert rec.ids[b, l].tolist() == _host_topk(rec.rlog[b, l], k), (b, l)
+    run.plan.close()
