@@ -565,3 +565,34 @@ def test_router_exact_ties_take_the_lower_index(n):
             for l in range(D.n_layers):
                 assert rec.ids[b, l].tolist() == _host_topk(rec.rlog[b, l], k), (b, l)
     run.plan.close()
+
+
+@pytest.mark.parametrize("n_req", [1, 12])
+def test_host_buffer_steps_match_device_steps(n_req):
+    # mk_decode_step_host copies the tokens in and the next tokens out, from
+    # page-locked or pageable host memory; both must give the device-buffer
+    # path's next tokens, bit for bit.  Twelve requests make a group plan of
+    # two sub-plans (each sub-plan's rows at its own offset of the arrays).
+    from synth.device import DeviceModel
+    base = synth.workload("tiny")
+    ctx = ([128, 37, 95, 16, 1, 60, 77, 5] * 2)[:n_req]
+    wl = dataclasses.replace(base, ctx=ctx, steps=4)
+    model = DeviceModel(wl.dims, wl.seed)
+    runs = [GpuRun(wl, steps=4, model=model) for _ in range(3)]
+    toks = [runs[1].tokens.cpu(), runs[2].tokens.cpu()]
+    for _ in range(4):
+        ref = runs[0].step(capture=False, logits=False)
+        assert ref is None
+        want = runs[0].tokens.cpu()
+        for i, pinned in ((1, True), (2, False)):
+            h_tok = toks[i - 1].clone()
+            h_next = torch.empty_like(h_tok)
+            if pinned:
+                h_tok, h_next = h_tok.pin_memory(), h_next.pin_memory()
+            assert runs[i].plan.step_host(h_tok, h_next) == 0
+            assert torch.equal(h_next, want), (pinned, h_next, want)
+            toks[i - 1] = h_next.clone()
+            for r in runs[i].reqs:
+                r.length += 1
+    for r in runs:
+        r.plan.close()
