@@ -497,7 +497,7 @@ def test_prefill_chunk_rows_match_per_token_decode(capacity):
     plan.close()
 
 
-@pytest.mark.parametrize("name,n", [("tiny", 8), ("tiny", 5), ("tiny", 3), ("mid", 8)])
+@pytest.mark.parametrize("name,n", [("tiny", 8), ("tiny", 5), ("tiny", 3), ("mid", 8), ("mid", 5)])
 def test_expert_gate_up_on_tensor_cores(name, n):
     # Batches of 3 to 8 run the experts' gate/up and the QKV and O projections
     # on the tensor cores (tcgen05 MMAs from TMA tiles into TMEM; the
@@ -507,7 +507,10 @@ def test_expert_gate_up_on_tensor_cores(name, n):
     # significant bits, relative error about 2^-17 per element against fp32 on
     # the CUDA cores), so the two agree to 1e-3 in relative L2, the tokens and
     # experts exactly.  Batches of 5 and 3 (plans of capacity 3 to 8 take the
-    # batch-8 instance) run with zero rows in every B operand.
+    # batch-8 instance) run with zero rows in every B operand.  The expert
+    # tiles' ranges are whole 32-unit halves: tiny gives each tile at most
+    # one (a lone half, two K boxes per slot), mid several (pairs, some across
+    # two experts, and lone halves).
     from persistent_moe_decode_02_gb300 import mk
     base = synth.workload(name)
     ctx = [128, 37, 95, 16, 1, 60, 77, 5] if name == "tiny" else [4096, 300, 1000, 17, 2500, 64, 999, 3000]
