@@ -2495,6 +2495,15 @@ struct Consumer {
         }
       }
     }
+    if constexpr (NB > 1) {
+      // the requests whose rows this partial holds (the others stay zero)
+      if (!ab && ct == 0) {
+        uint32_t rows = 0;
+        for (int u = q0 / F; u * F < q1; ++u)
+          for (int j = 0; j < m->r_cnt[u]; ++j) rows |= 1u << m->r_tok[u * bc + j];
+        p.moe_mask[(size_t)l * t.a[1] + t.a[0]] = rows;
+      }
+    }
     ab = finish(ab);
     if (!ab) signal(p.cm.gu + l);
     return ab;
@@ -2515,7 +2524,55 @@ struct Consumer {
     }
     // the residual rows first: their load overlaps the partials' (thread o < no keeps row o)
     const float xres = !ab && ct < no ? xmid1(l, ct / nr, r0 + ct % nr) : 0.f;
-    if (!ab) {
+    if constexpr (NB > 1) {
+      // above batch 1 a request's row is nonzero only in the partials of the
+      // tiles serving its experts: warp b lists request b's tiles, in tile
+      // order, from the tiles' masks, and only those are summed (strided
+      // chunks of the list, then chunk order).  When the lists do not fit
+      // beside the chunk sums (very few CTAs), every tile is summed.
+      int* tl = reinterpret_cast<int*>(rs + no * nch);   // [B][ntiles] tile lists
+      int* tn = tl + B * ntiles;                         // [B] their lengths
+      uint32_t* msk = reinterpret_cast<uint32_t*>(tn + MAX_BATCH);
+      const bool lists = (long long)no * nch + (long long)(B + 1) * ntiles + MAX_BATCH <= p.act_floats;
+      if (lists) {
+        if (!ab)
+          for (int i = ct; i < ntiles; i += NCT) msk[i] = __ldcg(p.moe_mask + (size_t)l * ntiles + i);
+        cbar();
+        if (!ab && cw < B) {
+          int base = 0;
+          for (int i0 = 0; i0 < ntiles; i0 += 32) {
+            const int i = i0 + lane;
+            const bool on = i < ntiles && ((msk[i] >> cw) & 1u);
+            const unsigned bal = __ballot_sync(FULL, on);
+            if (on) tl[cw * ntiles + base + __popc(bal & ((1u << lane) - 1u))] = i;
+            base += __popc(bal);
+          }
+          if (lane == 0) tn[cw] = base;
+        }
+        cbar();
+      }
+      if (!ab) {
+        constexpr int BT = 10;
+        for (int x = ct; x < no * nch; x += NCT) {
+          const int c = x / no, o = x - c * no, b = o / nr, h = r0 + (o - b * nr);
+          const float* src = p.moe_part + (size_t)b * H + h;
+          const int* lb = lists ? tl + b * ntiles : nullptr;
+          const int nb = lists ? tn[b] : ntiles;
+          float s = 0.f;
+          for (int k0 = c; k0 < nb; k0 += BT * nch) {
+            float v[BT];
+#pragma unroll
+            for (int i = 0; i < BT; ++i) {
+              const int kk = k0 + i * nch;
+              v[i] = kk < nb ? __ldcg(src + (size_t)(lb ? lb[kk] : kk) * p.bcap * H) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < BT; ++i) s += v[i];
+          }
+          rs[o * nch + c] = s;
+        }
+      }
+    } else if (!ab) {
       // thread x takes output o = x % no and every nch-th tile from chunk c = x / no,
       // so a warp reads consecutive rows of a tile; up to BT loads in flight
       constexpr int BT = 10;

@@ -203,6 +203,10 @@ struct Params {
   unsigned long long* qkv_fx;    // [L][bcap][qkv_rows]; zeroed after use by the layer's O tiles
   unsigned long long* xmid_fx;   // [L][bcap][H]; the last O task of each 128-row tile converts
                                  // its rows to fp32 x_mid and zeroes them
+  // [L][expert tiles]: bit b set when the tile's partial holds request b's
+  // row (instances above batch 1; the other rows of a partial are zero, so the
+  // reduce tasks skip them)
+  uint32_t* moe_mask;
 };
 
 // Expert gate/up on the tensor cores: an expert tile's range is a run of whole

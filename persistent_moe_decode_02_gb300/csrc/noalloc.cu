@@ -325,6 +325,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   const size_t d_rp = dc.take(L * mk::RL_COPIES * B * s.E * sizeof(unsigned long long));
   const size_t d_lmv = dc.take((size_t)B * cnt.lm * sizeof(float));
   const size_t d_lmi = dc.take((size_t)B * cnt.lm * sizeof(int));
+  const size_t d_mm = dc.take(L * (size_t)cnt.gu * sizeof(uint32_t));
   if (dc.off > kScratchBytes) {
     char buf[160];
     snprintf(buf, sizeof(buf), "step needs %zu bytes of scratch, above the %zu-byte static limit", dc.off,
@@ -438,6 +439,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_dims* dims, const mk_weight
   P.gates = (float*)(base + d_gt);
   P.route = (int*)(base + d_route);
   P.moe_part = (float*)(base + d_mp);
+  P.moe_mask = (uint32_t*)(base + d_mm);
   P.rlsum = (unsigned long long*)(base + d_rp);
   P.lm_val = (float*)(base + d_lmv);
   P.lm_idx = (int*)(base + d_lmi);

@@ -953,6 +953,7 @@ static int create_one(const mk_model_dims* dims, const mk_weights* w, const mk_k
   // expert-tile partials, sized for the most tiles any batch up to the capacity needs
   const int moe_max = mk::moe_tiles(std::min(s.E, bcap * s.k), s.F, C, bcap, mk::cf_floats(s.E, s.k, s.F, C, bcap));
   ok &= dalloc(p, &P.moe_part, (size_t)moe_max * bcap * s.H * sizeof(float)) == cudaSuccess;
+  ok &= dalloc(p, &P.moe_mask, (size_t)L * moe_max * sizeof(uint32_t)) == cudaSuccess;
   ok &= dalloc(p, &P.rlsum, L * mk::RL_COPIES * bcap * s.E * sizeof(unsigned long long)) == cudaSuccess;
   const int lm_tiles = std::max(1, std::min(s.V, 4 * C));
   ok &= dalloc(p, &P.lm_val, (size_t)bcap * lm_tiles * sizeof(float)) == cudaSuccess;
