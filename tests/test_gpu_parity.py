@@ -599,3 +599,18 @@ def test_host_buffer_steps_match_device_steps(n_req):
                 r.length += 1
     for r in runs:
         r.plan.close()
+
+
+@pytest.mark.parametrize("ctas", [17, 24])
+def test_batch8_reduce_over_listed_tiles_on_few_ctas(ctas):
+    # Above batch 1 a reduce task sums only the expert tiles that hold each
+    # request's row, from per-request lists it builds beside its chunk sums.
+    # Few CTAs make few, long reduce tasks (17 CTAs, about the fewest the mid
+    # shape allows with batch 8: 121 rows x 8 requests per task, one chunk
+    # per output; the ring then takes 16 KB stages, so the CUDA cores do the
+    # batched contractions); both counts must match the oracle.
+    base = synth.workload("mid")
+    wl = dataclasses.replace(base, ctx=[40, 17, 33, 5, 64, 21, 48, 9], steps=2)
+    rep = run_and_check(wl, steps=2, num_ctas=ctas)
+    print(rep)
+    rep.assert_ok()
